@@ -1,0 +1,522 @@
+"""Benchmark of the MSA forward path on GB300.
+
+One step = one MSA layer prefill (index branch: msa_index_select, then main
+branch: msa_sparse_attn) over one sequence of the 128K-token workload
+(N=131072, H_q=32, H_kv=8, d=d_idx=128, Bk=128, k=16, seeded synthetic
+Gaussian inputs with 4 planted far blocks), inputs resident in HBM.
+
+Prints ONE JSON line. `value` is prefill tokens/s (all ranks). Further keys:
+  e2e          the same step through the C ABI from pinned host buffers,
+               host->device inputs and device->host output inside the timing
+  roofline     dominant kernel (the index branch): algorithmic flops per launch
+               / its CUDA-event time, against the measured dense bf16 peak
+  cpu_baseline the CPU oracle on a bounded sample of the same workload
+  extra        the other measured paths: 32K and (optionally) 1M prefill,
+               decode steps with bf16 and FP8-E4M3 KV, standalone top-16
+
+Multi-GPU: each rank runs its own independent sequence (no collective on the
+data path; weak scaling); time is the max over ranks.
+
+--impl reference times the CPU oracle (the only reference implementation of
+this method) on the same workload, metric and unit.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def index_flops(N, n_g, d_idx):
+    """Causal-visible index scores: 2 d_idx flops per (query, group, key <= query)."""
+    return 2.0 * d_idx * n_g * N * (N + 1) / 2.0
+
+
+def n_sel(t, Bk, k):
+    return t + 1 if t // Bk + 1 <= k else (k - 1) * Bk + t % Bk + 1
+
+
+def attn_flops(N, H_q, d, Bk, k):
+    """Main branch on the selected tokens: 4 d flops per (query, head, selected key)."""
+    t = np.arange(N, dtype=np.int64)
+    sel = np.where(t // Bk + 1 <= k, t + 1, (k - 1) * Bk + t % Bk + 1)
+    return 4.0 * d * H_q * float(sel.sum())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "ours":
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ GPU arm
+class Prefill:
+    """Device-resident prefill workload and its workspace."""
+
+    def __init__(self, msa, w, ws_rows=None):
+        import torch
+        import synth
+        self.msa, self.w = msa, w
+        self.q = synth.device_tensor(w, synth.T_Q)
+        self.k = synth.device_tensor(w, synth.T_K)
+        self.v = synth.device_tensor(w, synth.T_V)
+        self.qidx = synth.device_tensor(w, synth.T_QIDX)
+        self.kidx = synth.device_tensor(w, synth.T_KIDX)[:, 0].contiguous()
+        self.ids = torch.empty((w.N, w.n_g, w.k), dtype=torch.int32, device="cuda")
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((w.N, w.H_q), dtype=torch.float32, device="cuda")
+        rows = ws_rows or w.N
+        self.ws = torch.empty(msa.msa_sparse_attn_workspace_bytes(rows, w.N, w.H_q, w.H_kv, w.d,
+                                                                  w.Bk, w.k),
+                              dtype=torch.uint8, device="cuda")
+
+    def step(self, ev=None):
+        m, w = self.msa, self.w
+        if ev is not None:
+            ev[0].record()
+        m.msa_index_select(self.qidx, self.kidx, w.Bk, w.k, block_ids=self.ids)
+        if ev is not None:
+            ev[1].record()
+        m.msa_sparse_attn(self.q, self.k, self.v, self.ids, w.Bk, w.scale, workspace=self.ws,
+                          out=self.out, lse=self.lse)
+        if ev is not None:
+            ev[2].record()
+
+
+def time_prefill(msa, w, steps, warmup, world, ws_rows=None, clocks=None):
+    import torch
+    P = Prefill(msa, w, ws_rows)
+    for _ in range(warmup):
+        P.step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = msa.msa_launch_count()
+    ctx = ClockSampler(torch.cuda.current_device()) if clocks is not None else None
+    if ctx:
+        ctx.__enter__()
+    start.record()
+    for i in range(steps):
+        P.step(evs[i])
+    stop.record()
+    torch.cuda.synchronize()
+    if ctx:
+        ctx.__exit__()
+        clocks.update(ctx.summary())
+    barrier(world)
+    launches = msa.msa_launch_count() - n0
+    total_ms = start.elapsed_time(stop)
+    idx_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    att_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    return P, total_ms / steps, idx_ms, att_ms, launches
+
+
+def e2e_prefill(msa, P, steps, warmup):
+    """Same step through the public API with pinned host buffers: inputs H2D,
+    the layer, output (o, lse) D2H, all inside the timing."""
+    import torch
+    host = {n: getattr(P, n).cpu().pin_memory() for n in ("q", "k", "v", "qidx", "kidx")}
+    host_out = torch.empty(P.out.shape, dtype=P.out.dtype).pin_memory()
+    host_lse = torch.empty(P.lse.shape, dtype=P.lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+
+    def one():
+        for n, t in host.items():
+            getattr(P, n).copy_(t, non_blocking=True)
+        P.step()
+        host_out.copy_(P.out, non_blocking=True)
+        host_lse.copy_(P.lse, non_blocking=True)
+
+    for _ in range(max(1, warmup)):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3 / steps
+    return ms, h2d, d2h
+
+
+def time_decode(msa, w, fp8, steps, warmup):
+    """Decode step for B sequences: index branch (k_idx cache scan + top-k) and
+    main branch over the selected pages."""
+    import torch
+    import synth
+    dev = torch.device("cuda")
+    pt = torch.from_numpy(synth.page_table(w)).to(dev)
+    sl = torch.full((w.B,), w.L, dtype=torch.int32, device=dev)
+    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, :, 0].contiguous()
+    kp = synth.device_paged(w, synth.T_K, pt, fp8=fp8)
+    vp = synth.device_paged(w, synth.T_V, pt, fp8=fp8)
+    last = [(s, w.L - 1) for s in range(w.B)]
+    q = synth.device_rows(w, synth.T_Q, last)
+    qidx = synth.device_rows(w, synth.T_QIDX, last)
+    ks, vs = synth.fp8_scales(w.H_kv)
+    kw = dict(k_scale=torch.from_numpy(ks).to(dev), v_scale=torch.from_numpy(vs).to(dev)) if fp8 else {}
+    ids = torch.empty((w.B, w.n_g, w.k), dtype=torch.int32, device=dev)
+    ws_i = torch.empty(msa.msa_index_select_decode_workspace_bytes(w.B, w.nb, w.n_g),
+                       dtype=torch.uint8, device=dev)
+    ws_d = torch.empty(msa.msa_decode_workspace_bytes(w.B, w.H_q, w.d, w.k), dtype=torch.uint8,
+                       device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H_q), dtype=torch.float32, device=dev)
+    # L2 flush buffer (decode attention reads 0.25-0.5 GB: flush between steps)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        msa.msa_index_select_decode(qidx, kidx_p, pt, sl, w.Bk, w.k, block_ids=ids, workspace=ws_i)
+        if ev:
+            ev[1].record()
+        msa.msa_decode(q, kp, vp, pt, sl, ids, w.Bk, w.scale, workspace=ws_d, out=out, lse=lse,
+                       **kw)
+        if ev:
+            ev[2].record()
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    idx, att = [], []
+    for _ in range(steps):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        step(ev)
+        torch.cuda.synchronize()
+        idx.append(ev[0].elapsed_time(ev[1]))
+        att.append(ev[1].elapsed_time(ev[2]))
+    del kidx_p, kp, vp
+    return statistics.mean(idx), statistics.mean(att)
+
+
+def time_topk(msa, w, steps, warmup):
+    """Standalone exp-free top-16 over the [N, 8, 1024] block scores of the
+    128K workload (produced by the index branch)."""
+    import torch
+    import synth
+    qidx = synth.device_tensor(w, synth.T_QIDX)
+    kidx = synth.device_tensor(w, synth.T_KIDX)[:, 0].contiguous()
+    S = torch.empty((w.N, w.n_g, w.nb), dtype=torch.float32, device="cuda")
+    msa.msa_index_select(qidx, kidx, w.Bk, w.k, block_scores=S)
+    del qidx, kidx
+    ids = torch.empty((w.N, w.n_g, w.k), dtype=torch.int32, device="cuda")
+    for _ in range(warmup):
+        msa.msa_topk_blocks(S, w.Bk, w.k, block_ids=ids)
+    torch.cuda.synchronize()
+    ms = []
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        msa.msa_topk_blocks(S, w.Bk, w.k, block_ids=ids)
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    t = statistics.mean(ms)
+    # algorithmic bytes: the visible scores (b < loc(t)) read + the ids written
+    loc = np.arange(w.N) // w.Bk
+    read = 4.0 * w.n_g * float(loc.sum())
+    wr = 4.0 * w.N * w.n_g * w.k
+    return t, read + wr
+
+
+# ------------------------------------------------------------- CPU baseline
+def cpu_baseline(w, budget_s=20.0, seed=0):
+    """The oracle (as it stands) on a bounded sample of rows of workload w;
+    tokens/s extrapolated from the per-row costs, weighted by cost class."""
+    import oracle
+    import synth
+    rng = np.random.default_rng(seed)
+    kh = synth.host_tensor(w, synth.T_KIDX)[0, :, 0]
+    # strata: the index cost of row t grows with t, the attention cost is ~flat;
+    # sample rows uniformly over [0, N) in increasing batches until the budget
+    rows_done, secs = [], 0.0
+    n_batch = 4
+    Kh = np.zeros((w.nb * w.Bk, w.H_kv, w.d), dtype=np.uint16)
+    Vh = np.zeros_like(Kh)
+    filled = set()
+    per = w.H_kv * w.d
+    t_index = t_attn = 0.0
+    while secs < budget_s and len(rows_done) < w.N:
+        rows = np.sort(rng.integers(0, w.N, n_batch))
+        qi = synth.host_rows(w, synth.T_QIDX, 0, rows)
+        t0 = time.perf_counter()
+        ids = oracle.index_select(qi, rows, kh, w.Bk, w.k)
+        t1 = time.perf_counter()
+        for b in set(int(x) for x in ids.ravel() if x >= 0) - filled:
+            t0b, t1b = b * w.Bk, min(w.N, (b + 1) * w.Bk)
+            synth.host_fill(w, synth.T_K, Kh, t0b * per, (t1b - t0b) * per)
+            synth.host_fill(w, synth.T_V, Vh, t0b * per, (t1b - t0b) * per)
+            filled.add(b)
+        qh = synth.host_rows(w, synth.T_Q, 0, rows)
+        t2 = time.perf_counter()
+        oracle.sparse_attn(qh, rows, Kh, Vh, ids, w.Bk, w.scale)
+        t3 = time.perf_counter()
+        t_index += t1 - t0
+        t_attn += t3 - t2
+        secs += (t1 - t0) + (t3 - t2)
+        rows_done.extend(rows.tolist())
+        n_batch = min(n_batch * 2, 256)
+    rows_done = np.array(rows_done)
+    # index cost per row ~ (t + 1): scale by sum over all rows / sum over sampled rows
+    idx_full = t_index * (w.N * (w.N + 1) / 2.0) / float((rows_done + 1).sum())
+    att_full = t_attn * w.N / len(rows_done)
+    full_s = idx_full + att_full
+    return {"value": w.N / full_s, "unit": "tokens/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"{len(rows_done)} uniformly drawn query rows of the {w.name} workload "
+                      f"({secs:.1f} s of oracle time); full-sequence time extrapolated: index "
+                      f"cost weighted by (t+1), attention cost per row",
+            "sample_s": round(secs, 2), "extrapolated_full_s": round(full_s, 1)}
+
+
+def run_reference(args, world, rank):
+    import synth
+    if rank != 0:
+        return
+    w = synth.make(args.workload)
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(w, budget_s=2.0, seed=99)
+    for i in range(args.steps):
+        vals.append(cpu_baseline(w, budget_s=args.ref_budget, seed=i))
+    v = statistics.mean(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = v
+    print(json.dumps({
+        "impl": "reference", "metric": f"MSA layer prefill tokens/s ({w.name} context)",
+        "value": v, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * w.N / v, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d,
+                   "d_idx": w.d_idx, "Bk": w.Bk, "k": w.k, "seed": w.seed},
+        "cpu_baseline": cb,
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+# ---------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="128k")
+    ap.add_argument("--with-1m", action="store_true", help="also time the 1M-token prefill")
+    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_sparse_gqa_index_gb300 as msa
+    import synth
+
+    peaks, peak_src = load_peaks()
+    w = synth.make(args.workload)
+    clocks = {}
+    P, ms, idx_ms, att_ms, launches = time_prefill(msa, w, args.steps, args.warmup, world,
+                                                   clocks=clocks)
+    ms = max_over_ranks(world, ms)
+    value = world * w.N / (ms * 1e-3)
+    fl_idx, fl_att = index_flops(w.N, w.n_g, w.d_idx), attn_flops(w.N, w.H_q, w.d, w.Bk, w.k)
+    peak_t = peaks["bf16_tflops_sustained"]
+    dominant = "msa_index_select" if idx_ms >= att_ms else "msa_sparse_attn"
+    dom_ms, dom_fl = (idx_ms, fl_idx) if dominant == "msa_index_select" else (att_ms, fl_att)
+    achieved = dom_fl / (dom_ms * 1e-3) / 1e12
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        traffic = json.load(open(tr_path)).get(f"{dominant}@{w.name}")
+    roofline = {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
+                "peak": peak_t, "unit": "TFLOP/s", "frac": round(achieved / peak_t, 4),
+                "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": traffic,
+                "algorithmic_flops_per_launch": dom_fl, "ms_per_launch": round(dom_ms, 4)}
+    e2e_ms, h2d, d2h = e2e_prefill(msa, P, max(1, args.steps // 2), 1)
+    e2e_ms = max_over_ranks(world, e2e_ms)
+    del P
+    torch.cuda.empty_cache()
+
+    extra = {"prefill_128k_split_ms": {"index": round(idx_ms, 3), "attention": round(att_ms, 3)},
+             "attention_roofline": {
+                 "achieved": round(fl_att / (att_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                 "frac": round(fl_att / (att_ms * 1e-3) / 1e12 / peak_t, 4)}}
+    if not args.no_extra:
+        w32 = synth.make("32k")
+        P32, ms32, i32, a32, _ = time_prefill(msa, w32, args.steps, args.warmup, world)
+        del P32
+        torch.cuda.empty_cache()
+        extra["prefill_32k"] = {"tokens_per_s": w32.N / (ms32 * 1e-3), "ms": round(ms32, 3),
+                                "index_ms": round(i32, 3), "attention_ms": round(a32, 3),
+                                "tflops": round((index_flops(w32.N, 8, 128) +
+                                                 attn_flops(w32.N, 32, 128, 128, 16)) /
+                                                (ms32 * 1e-3) / 1e12, 2)}
+        tk_ms, tk_bytes = time_topk(msa, w, args.steps, 1)
+        torch.cuda.empty_cache()
+        gbs = tk_bytes / (tk_ms * 1e-3) / 1e9
+        extra["topk16_128k"] = {"ms": round(tk_ms, 4), "achieved_gbs": round(gbs, 1),
+                                "peak_gbs": peaks["hbm_gbs"], "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                "algorithmic_bytes": tk_bytes}
+        wd = synth.make("decode")
+        for fp8 in (False, True):
+            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, 1)
+            torch.cuda.empty_cache()
+            kv_bytes = 2.0 * wd.B * wd.n_g * (wd.k - 1) * wd.Bk * wd.d * (1 if fp8 else 2) + \
+                2.0 * wd.B * wd.n_g * 1 * wd.d * (1 if fp8 else 2)
+            scan_bytes = 2.0 * wd.B * wd.L * wd.d_idx
+            key = "decode_fp8" if fp8 else "decode_bf16"
+            extra[key] = {
+                "tokens_per_s": wd.B / ((i_ms + a_ms) * 1e-3),
+                "attention_only_tokens_per_s": wd.B / (a_ms * 1e-3),
+                "index_ms": round(i_ms, 4), "attention_ms": round(a_ms, 4),
+                "index_scan_gbs": round(scan_bytes / (i_ms * 1e-3) / 1e9, 1),
+                "attention_gbs": round(kv_bytes / (a_ms * 1e-3) / 1e9, 1),
+                "peak_gbs": peaks["hbm_gbs"]}
+        if args.with_1m:
+            w1 = synth.make("1m")
+            P1, ms1, i1, a1, _ = time_prefill(msa, w1, max(1, args.steps // 2), 1, world,
+                                              ws_rows=w1.N // 8)
+            del P1
+            torch.cuda.empty_cache()
+            extra["prefill_1m"] = {"tokens_per_s": w1.N / (ms1 * 1e-3), "ms": round(ms1, 2),
+                                   "index_ms": round(i1, 2), "attention_ms": round(a1, 2),
+                                   "tflops": round((index_flops(w1.N, 8, 128) +
+                                                    attn_flops(w1.N, 32, 128, 128, 16)) /
+                                                   (ms1 * 1e-3) / 1e12, 2)}
+    cb = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cb = cpu_baseline(w)
+    if rank == 0:
+        print(json.dumps({
+            "metric": f"MSA layer prefill tokens/s ({w.name} context)",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "N": w.N, "H_q": w.H_q, "H_kv": w.H_kv, "d": w.d,
+                       "d_idx": w.d_idx, "Bk": w.Bk, "k": w.k, "seed": w.seed,
+                       "l2": "inputs larger than L2 (q 1 GiB, q_idx/k/v 256 MiB each)",
+                       "parallelism": f"replicas{world}"},
+            "e2e": {"value": world * w.N / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "roofline": roofline, "cpu_baseline": cb, "clocks": clocks,
+            "gpu_launches": launches, "extra": extra}), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,279 @@
+"""MiniMax Sparse Attention (MSA) forward path on GB300 (sm_103a).
+
+Thin Python binding of libmsa.so (C ABI in include/msa.h). Every function here
+only checks and marshals its torch arguments (device pointers, sizes, the
+current CUDA stream) and calls the library entry point of the same name; all
+computation happens in the library's CUDA kernels. There is no other backend:
+importing this package fails if libmsa.so has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmsa.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+        "(or python block_sparse_gqa_index_gb300/build.py); there is no fallback path")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE, MSA_ERR_CUDA, \
+    MSA_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+MSA_KV_BF16, MSA_KV_E4M3 = 0, 1
+
+_P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+
+
+def _sig(name, argtypes, restype=ctypes.c_int):
+    fn = getattr(_lib, name)
+    fn.argtypes = argtypes
+    fn.restype = restype
+    return fn
+
+
+_status_string = _sig("msa_status_string", [_I], ctypes.c_char_p)
+_version = _sig("msa_version", [])
+_ws_index = _sig("msa_index_select_workspace_bytes", [_I64, _I, _I, _I, _I], _SZ)
+_index_select = _sig("msa_index_select", [_P, _P, _I64, _I, _I, _I, _I, _P, _P, _P, _SZ, _P])
+_topk = _sig("msa_topk_blocks", [_P, _I64, _I, _I64, _I, _I, _I64, _P, _P, _P])
+_ws_attn = _sig("msa_sparse_attn_workspace_bytes", [_I64, _I64, _I, _I, _I, _I, _I], _SZ)
+_sparse_attn = _sig("msa_sparse_attn", [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _F, _P, _P,
+                                        _P, _SZ, _P])
+_ws_index_dec = _sig("msa_index_select_decode_workspace_bytes", [_I, _I, _I], _SZ)
+_index_dec = _sig("msa_index_select_decode", [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
+                                              _P, _SZ, _P])
+_ws_dec = _sig("msa_decode_workspace_bytes", [_I, _I, _I, _I], _SZ)
+_decode = _sig("msa_decode", [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                              _P, _P, _P, _SZ, _P])
+_get_error = _sig("msa_get_error", [_P])
+_set_wait = _sig("msa_set_wait_limit", [_I64], _I64)
+_launch_count = _sig("msa_launch_count", [], _I64)
+
+EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes",
+           "msa_index_select", "msa_topk_blocks", "msa_sparse_attn_workspace_bytes",
+           "msa_sparse_attn", "msa_index_select_decode_workspace_bytes",
+           "msa_index_select_decode", "msa_decode_workspace_bytes", "msa_decode",
+           "msa_get_error", "msa_set_wait_limit", "msa_launch_count"]
+
+
+class MSAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_status_string(status).decode()} ({status})")
+
+
+def _check(rc: int, where: str):
+    if rc != MSA_OK:
+        raise MSAError(rc, where)
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _req(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def version() -> int:
+    return _version()
+
+
+def msa_status_string(status: int) -> str:
+    return _status_string(status).decode()
+
+
+# ------------------------------------------------------------------ prefill
+def msa_index_select(q_idx: torch.Tensor, k_idx: torch.Tensor, Bk: int = 128, k: int = 16,
+                     block_ids: Optional[torch.Tensor] = None,
+                     block_scores: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Index branch of prefill. q_idx [N, n_groups, d_idx] bf16, k_idx [N, d_idx]
+    bf16 -> block_ids [N, n_groups, k] int32 (and block_scores [N, n_groups,
+    ceil(N/Bk)] fp32 filled on the visible part when given)."""
+    N, n_g, d_idx = q_idx.shape
+    _req(q_idx, "q_idx", torch.bfloat16)
+    _req(k_idx, "k_idx", torch.bfloat16, (N, d_idx))
+    if block_ids is None:
+        block_ids = torch.empty((N, n_g, k), dtype=torch.int32, device=q_idx.device)
+    _req(block_ids, "block_ids", torch.int32, (N, n_g, k))
+    if block_scores is not None:
+        _req(block_scores, "block_scores", torch.float32, (N, n_g, (N + Bk - 1) // Bk))
+    _check(_index_select(q_idx.data_ptr(), k_idx.data_ptr(), N, n_g, d_idx, Bk, k,
+                         block_ids.data_ptr(), _ptr(block_scores), None, 0, _stream(q_idx)),
+           "msa_index_select")
+    return block_ids
+
+
+def msa_topk_blocks(block_scores: torch.Tensor, Bk: int = 128, k: int = 16, q_offset: int = 0,
+                    seq_lens: Optional[torch.Tensor] = None,
+                    block_ids: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Exp-free top-k over block scores [N, n_groups, nb] fp32 -> [N, n_groups, k]."""
+    N, n_g, nb = block_scores.shape
+    _req(block_scores, "block_scores", torch.float32)
+    if seq_lens is not None:
+        _req(seq_lens, "seq_lens", torch.int32, (N,))
+    if block_ids is None:
+        block_ids = torch.empty((N, n_g, k), dtype=torch.int32, device=block_scores.device)
+    _req(block_ids, "block_ids", torch.int32, (N, n_g, k))
+    _check(_topk(block_scores.data_ptr(), N, n_g, nb, Bk, k, q_offset, _ptr(seq_lens),
+                 block_ids.data_ptr(), _stream(block_scores)), "msa_topk_blocks")
+    return block_ids
+
+
+def msa_sparse_attn_workspace_bytes(chunk_rows: int, N: int, H_q: int, H_kv: int, d: int,
+                                    Bk: int = 128, k: int = 16) -> int:
+    return _ws_attn(chunk_rows, N, H_q, H_kv, d, Bk, k)
+
+
+def msa_sparse_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_ids: torch.Tensor,
+                    Bk: int = 128, scale: Optional[float] = None,
+                    workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                    lse: Optional[torch.Tensor] = None, want_lse: bool = True):
+    """Main branch of prefill. q [N, H_q, d], k/v [N, H_kv, d] bf16, block_ids
+    [N, H_kv, topk] int32 -> (out [N, H_q, d] bf16, lse [N, H_q] fp32)."""
+    N, H_q, d = q.shape
+    H_kv = k.shape[1]
+    topk = block_ids.shape[-1]
+    _req(q, "q", torch.bfloat16)
+    _req(k, "k", torch.bfloat16, (N, H_kv, d))
+    _req(v, "v", torch.bfloat16, (N, H_kv, d))
+    _req(block_ids, "block_ids", torch.int32, (N, H_kv, topk))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = torch.empty(msa_sparse_attn_workspace_bytes(N, N, H_q, H_kv, d, Bk, topk),
+                                dtype=torch.uint8, device=q.device)
+    _req(workspace, "workspace", torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, "out", torch.bfloat16, (N, H_q, d))
+    if lse is None and want_lse:
+        lse = torch.empty((N, H_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _req(lse, "lse", torch.float32, (N, H_q))
+    _check(_sparse_attn(q.data_ptr(), k.data_ptr(), v.data_ptr(), block_ids.data_ptr(), N, H_q,
+                        H_kv, d, Bk, topk, scale, out.data_ptr(), _ptr(lse),
+                        workspace.data_ptr(), workspace.numel(), _stream(q)), "msa_sparse_attn")
+    return out, lse
+
+
+# ------------------------------------------------------------------- decode
+def msa_index_select_decode(q_idx: torch.Tensor, k_idx_pages: torch.Tensor,
+                            page_table: torch.Tensor, seq_lens: torch.Tensor, Bk: int = 128,
+                            k: int = 16, block_ids: Optional[torch.Tensor] = None,
+                            block_scores: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Index branch of decode. q_idx [B, n_groups, d_idx], k_idx_pages [P, Bk,
+    d_idx] bf16, page_table [B, max_pages] int32, seq_lens [B] int32 ->
+    block_ids [B, n_groups, k] int32."""
+    B, n_g, d_idx = q_idx.shape
+    max_pages = page_table.shape[1]
+    _req(q_idx, "q_idx", torch.bfloat16)
+    _req(k_idx_pages, "k_idx_pages", torch.bfloat16)
+    if k_idx_pages.shape[1:] != (Bk, d_idx):
+        raise ValueError("k_idx_pages must be [P, Bk, d_idx]")
+    _req(page_table, "page_table", torch.int32, (B, max_pages))
+    _req(seq_lens, "seq_lens", torch.int32, (B,))
+    if block_ids is None:
+        block_ids = torch.empty((B, n_g, k), dtype=torch.int32, device=q_idx.device)
+    _req(block_ids, "block_ids", torch.int32, (B, n_g, k))
+    if block_scores is not None:
+        _req(block_scores, "block_scores", torch.float32, (B, n_g, max_pages))
+    elif workspace is None:
+        workspace = torch.empty(_ws_index_dec(B, max_pages, n_g), dtype=torch.uint8,
+                                device=q_idx.device)
+    ws_ptr, ws_n = (None, 0) if workspace is None else (_req(workspace, "workspace", torch.uint8),
+                                                         workspace.numel())
+    _check(_index_dec(q_idx.data_ptr(), k_idx_pages.data_ptr(), page_table.data_ptr(),
+                      seq_lens.data_ptr(), B, max_pages, n_g, d_idx, Bk, k, block_ids.data_ptr(),
+                      _ptr(block_scores), ws_ptr, ws_n, _stream(q_idx)),
+           "msa_index_select_decode")
+    return block_ids
+
+
+def msa_index_select_decode_workspace_bytes(B: int, max_pages: int, n_groups: int) -> int:
+    return _ws_index_dec(B, max_pages, n_groups)
+
+
+def msa_decode_workspace_bytes(B: int, H_q: int, d: int, k: int = 16) -> int:
+    return _ws_dec(B, H_q, d, k)
+
+
+def msa_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+               page_table: torch.Tensor, seq_lens: torch.Tensor, block_ids: torch.Tensor,
+               Bk: int = 128, scale: Optional[float] = None,
+               k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+               lse: Optional[torch.Tensor] = None, want_lse: bool = True):
+    """Main branch of decode. q [B, H_q, d] bf16; k_pages/v_pages [P, Bk, H_kv, d]
+    bf16, or uint8 E4M3 codes with k_scale/v_scale [H_kv] fp32."""
+    B, H_q, d = q.shape
+    P, _, H_kv, _ = k_pages.shape
+    max_pages = page_table.shape[1]
+    topk = block_ids.shape[-1]
+    fp8 = k_pages.dtype == torch.uint8
+    kv_dtype = MSA_KV_E4M3 if fp8 else MSA_KV_BF16
+    _req(q, "q", torch.bfloat16)
+    _req(k_pages, "k_pages", torch.uint8 if fp8 else torch.bfloat16, (P, Bk, H_kv, d))
+    _req(v_pages, "v_pages", torch.uint8 if fp8 else torch.bfloat16, (P, Bk, H_kv, d))
+    _req(page_table, "page_table", torch.int32, (B, max_pages))
+    _req(seq_lens, "seq_lens", torch.int32, (B,))
+    _req(block_ids, "block_ids", torch.int32, (B, H_kv, topk))
+    if fp8:
+        _req(k_scale, "k_scale", torch.float32, (H_kv,))
+        _req(v_scale, "v_scale", torch.float32, (H_kv,))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = torch.empty(_ws_dec(B, H_q, d, topk), dtype=torch.uint8, device=q.device)
+    _req(workspace, "workspace", torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, "out", torch.bfloat16, (B, H_q, d))
+    if lse is None and want_lse:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _req(lse, "lse", torch.float32, (B, H_q))
+    _check(_decode(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), kv_dtype,
+                   _ptr(k_scale), _ptr(v_scale), page_table.data_ptr(), seq_lens.data_ptr(),
+                   block_ids.data_ptr(), B, max_pages, H_q, H_kv, d, Bk, topk, scale,
+                   out.data_ptr(), _ptr(lse), workspace.data_ptr(), workspace.numel(),
+                   _stream(q)), "msa_decode")
+    return out, lse
+
+
+# -------------------------------------------------------------- diagnostics
+def msa_get_error(stream=None) -> int:
+    """Synchronise and return (and clear) the device error word."""
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    return _get_error(stream)
+
+
+def msa_set_wait_limit(polls: int) -> int:
+    return _set_wait(polls)
+
+
+def msa_launch_count() -> int:
+    """Kernel launches (and device memsets) enqueued by libmsa so far."""
+    return _launch_count()

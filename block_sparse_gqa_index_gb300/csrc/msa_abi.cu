@@ -1,0 +1,231 @@
+// C ABI of libmsa (declared in include/msa.h): argument checks, workspace
+// carving and kernel launches. No allocation, no synchronisation (except in
+// msa_get_error), no exceptions.
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "../../include/msa.h"
+#include "msa_kernels.h"
+
+namespace msa {
+static std::atomic<long long> g_launches{0};
+void note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace msa
+
+namespace {
+
+__device__ int g_msa_error = 0;
+
+long long g_wait_limit = 1ll << 26;
+std::mutex g_mu;
+int* g_err_ptr[64] = {nullptr};
+
+// Device address of the error word on the current device (looked up once per
+// device; the lookup is not a stream operation).
+int* err_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_msa_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = (int*)p;
+  }
+  return g_err_ptr[dev];
+}
+
+msa::Diag diag() { return msa::Diag{err_ptr(), g_wait_limit}; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+
+bool supported_k(int k) { return k >= 1 && k <= msa::kMaxK; }
+bool supported_d(int d) { return d == 64 || d == 128; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" {
+
+const char* msa_status_string(int s) {
+  switch (s) {
+    case MSA_OK: return "MSA_OK";
+    case MSA_ERR_INVALID_ARG: return "MSA_ERR_INVALID_ARG";
+    case MSA_ERR_UNSUPPORTED: return "MSA_ERR_UNSUPPORTED";
+    case MSA_ERR_WORKSPACE: return "MSA_ERR_WORKSPACE";
+    case MSA_ERR_CUDA: return "MSA_ERR_CUDA";
+    case MSA_ERR_TIMEOUT: return "MSA_ERR_TIMEOUT";
+    default: return "MSA_ERR_UNKNOWN";
+  }
+}
+
+int msa_version(void) { return 0x000100; }
+
+size_t msa_index_select_workspace_bytes(int64_t, int, int, int, int) { return 0; }
+
+int msa_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_groups, int d_idx,
+                     int Bk, int k, int32_t* block_ids, float* block_scores, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (N < 0 || n_groups < 1 || d_idx < 1 || Bk < 1 || k < 1) return MSA_ERR_INVALID_ARG;
+  if (N == 0) return MSA_OK;
+  if (!q_idx || !k_idx || !block_ids) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(block_ids) ||
+      (block_scores && !aligned16(block_scores)))
+    return MSA_ERR_INVALID_ARG;
+  if (Bk != 128 || !supported_k(k) || !supported_d(d_idx)) return MSA_ERR_UNSUPPORTED;
+  if (N * n_groups >= (1ll << 31)) return MSA_ERR_UNSUPPORTED;
+  int64_t nb = ceil_div(N, Bk);
+  return status_of(msa::launch_index_select(q_idx, k_idx, N, n_groups, d_idx, k, block_ids,
+                                            block_scores, nb, diag(), (cudaStream_t)stream));
+}
+
+int msa_topk_blocks(const float* block_scores, int64_t N, int n_groups, int64_t nb, int Bk,
+                    int k, int64_t q_offset, const int32_t* seq_lens, int32_t* block_ids,
+                    void* stream) {
+  if (N < 0 || n_groups < 1 || nb < 1 || Bk < 1 || k < 1 || q_offset < 0)
+    return MSA_ERR_INVALID_ARG;
+  if (N == 0) return MSA_OK;
+  if (!block_scores || !block_ids) return MSA_ERR_INVALID_ARG;
+  if (!seq_lens && (N - 1 + q_offset) / Bk >= nb) return MSA_ERR_INVALID_ARG;
+  if (!supported_k(k)) return MSA_ERR_UNSUPPORTED;
+  return status_of(msa::launch_topk(block_scores, N, n_groups, nb, Bk, k, q_offset, seq_lens,
+                                    block_ids, diag(), (cudaStream_t)stream));
+}
+
+size_t msa_sparse_attn_workspace_bytes(int64_t chunk_rows, int64_t N, int H_q, int H_kv, int d,
+                                       int Bk, int k) {
+  if (chunk_rows < 1 || N < 1 || H_kv < 1 || Bk < 1 || k < 1) return 0;
+  chunk_rows = std::min(chunk_rows, N);
+  return msa::attn_ws_bytes(chunk_rows, ceil_div(N, Bk), H_q, H_kv, d, k);
+}
+
+int msa_sparse_attn(const void* q, const void* k, const void* v, const int32_t* block_ids,
+                    int64_t N, int H_q, int H_kv, int d, int Bk, int topk, float scale, void* out,
+                    float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  if (N < 0 || H_q < 1 || H_kv < 1 || d < 1 || Bk < 1 || topk < 1) return MSA_ERR_INVALID_ARG;
+  if (N == 0) return MSA_OK;
+  if (!q || !k || !v || !block_ids || !out || !workspace) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(workspace) || !aligned16(block_ids) || (lse && !aligned16(lse)))
+    return MSA_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return MSA_ERR_INVALID_ARG;
+  const int G = H_q / H_kv;
+  if (Bk != 128 || !supported_k(topk) || !supported_d(d) || 128 % G != 0)
+    return MSA_ERR_UNSUPPORTED;
+  if (N >= (1ll << 27) || N * H_q * topk >= (1ll << 31)) return MSA_ERR_UNSUPPORTED;
+  const int64_t nb = ceil_div(N, Bk);
+  // largest chunk of query rows whose workspace fits
+  int64_t lo = 0, hi = N;
+  while (lo < hi) {
+    int64_t mid = (lo + hi + 1) / 2;
+    if (msa::attn_ws_bytes(mid, nb, H_q, H_kv, d, topk) <= workspace_bytes) lo = mid;
+    else hi = mid - 1;
+  }
+  if (lo < 1) return MSA_ERR_WORKSPACE;
+  const int64_t chunk = lo;
+  msa::AttnWs ws = msa::attn_ws_carve(workspace, chunk, nb, H_q, H_kv, d, topk);
+  msa::Diag dg = diag();
+  for (int64_t q0 = 0; q0 < N; q0 += chunk) {
+    int64_t q1 = std::min(N, q0 + chunk);
+    cudaError_t e = msa::launch_sparse_attn_chunk(q, k, v, block_ids, N, q0, q1, H_q, H_kv, d,
+                                                  topk, scale, out, lse, ws, nb, dg,
+                                                  (cudaStream_t)stream);
+    if (e != cudaSuccess) return MSA_ERR_CUDA;
+  }
+  return MSA_OK;
+}
+
+size_t msa_index_select_decode_workspace_bytes(int B, int max_pages, int n_groups) {
+  if (B < 0 || max_pages < 0 || n_groups < 0) return 0;
+  return (size_t)B * max_pages * n_groups * sizeof(float);
+}
+
+int msa_index_select_decode(const void* q_idx, const void* k_idx_pages,
+                            const int32_t* page_table, const int32_t* seq_lens, int B,
+                            int max_pages, int n_groups, int d_idx, int Bk, int k,
+                            int32_t* block_ids, float* block_scores, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (B < 0 || max_pages < 1 || n_groups < 1 || d_idx < 1 || Bk < 1 || k < 1)
+    return MSA_ERR_INVALID_ARG;
+  if (B == 0) return MSA_OK;
+  if (!q_idx || !k_idx_pages || !page_table || !seq_lens || !block_ids)
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx_pages) || (block_scores && !aligned16(block_scores)))
+    return MSA_ERR_INVALID_ARG;
+  if (Bk != 128 || !supported_k(k) || !supported_d(d_idx) || n_groups > 8)
+    return MSA_ERR_UNSUPPORTED;
+  float* scores = block_scores;
+  if (!scores) {
+    if (!workspace || workspace_bytes < msa_index_select_decode_workspace_bytes(B, max_pages,
+                                                                                n_groups))
+      return MSA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MSA_ERR_INVALID_ARG;
+    scores = (float*)workspace;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  msa::Diag dg = diag();
+  cudaError_t e = msa::launch_decode_index(q_idx, k_idx_pages, page_table, seq_lens, B,
+                                           max_pages, n_groups, d_idx, scores, dg, st);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  e = msa::launch_topk(scores, B, n_groups, max_pages, Bk, k, 0, seq_lens, block_ids, dg, st);
+  return status_of(e);
+}
+
+size_t msa_decode_workspace_bytes(int B, int H_q, int d, int k) {
+  if (B < 0 || H_q < 0 || d < 0 || k < 0) return 0;
+  return msa::decode_ws_bytes(B, H_q, d, k);
+}
+
+int msa_decode(const void* q, const void* k_pages, const void* v_pages, int kv_dtype,
+               const float* k_scale, const float* v_scale, const int32_t* page_table,
+               const int32_t* seq_lens, const int32_t* block_ids, int B, int max_pages, int H_q,
+               int H_kv, int d, int Bk, int k, float scale, void* out, float* lse,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || max_pages < 1 || H_q < 1 || H_kv < 1 || d < 1 || Bk < 1 || k < 1)
+    return MSA_ERR_INVALID_ARG;
+  if (B == 0) return MSA_OK;
+  if (kv_dtype != MSA_KV_BF16 && kv_dtype != MSA_KV_E4M3) return MSA_ERR_INVALID_ARG;
+  if (!q || !k_pages || !v_pages || !page_table || !seq_lens || !block_ids || !out)
+    return MSA_ERR_INVALID_ARG;
+  if (kv_dtype == MSA_KV_E4M3 && (!k_scale || !v_scale)) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+    return MSA_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return MSA_ERR_INVALID_ARG;
+  if (Bk != 128 || !supported_k(k) || !supported_d(d) || H_q / H_kv > 8)
+    return MSA_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < msa_decode_workspace_bytes(B, H_q, d, k))
+    return MSA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MSA_ERR_INVALID_ARG;
+  return status_of(msa::launch_decode_attn(q, k_pages, v_pages, kv_dtype == MSA_KV_E4M3,
+                                           k_scale, v_scale, page_table, seq_lens, block_ids,
+                                           B, max_pages, H_q, H_kv, d, k, scale, out, lse,
+                                           workspace, diag(), (cudaStream_t)stream));
+}
+
+int msa_get_error(void* stream) {
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MSA_ERR_CUDA;
+  int* p = err_ptr();
+  if (!p) return MSA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MSA_ERR_CUDA;
+  int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  return v;
+}
+
+int64_t msa_launch_count(void) { return msa::g_launches.load(std::memory_order_relaxed); }
+
+int64_t msa_set_wait_limit(int64_t polls) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int64_t old = g_wait_limit;
+  if (polls >= 0) g_wait_limit = polls;
+  return old;
+}
+
+}  // extern "C"

@@ -1,0 +1,127 @@
+// Device helpers shared by the MSA kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace msa {
+
+constexpr int kStatusTimeout = -5;
+constexpr int kStatusBadIds = -1;  // invalid block ids / sequence lengths found on the device
+constexpr int kMaxK = 16;        // largest k the kernels are built for
+constexpr int kMaxFar = kMaxK - 1;
+
+// Diagnostics every kernel receives: the device error word and the poll limit
+// of bounded waits.
+struct Diag {
+  int* err;
+  long long wait_limit;
+};
+
+__device__ __forceinline__ void report(const Diag& dg, int code) {
+  if (dg.err) atomicCAS(dg.err, 0, code);
+}
+
+// ---------------------------------------------------------------- ranking keys
+// A block is ranked by the 64-bit key (order-preserving bits of its fp32 score,
+// ~block id): a larger key is a better block, and among equal scores the lower
+// id has the larger key ("lower id wins"). NaN maps below -inf. Key 0 means
+// "empty slot" and is below every real key.
+__device__ __forceinline__ uint32_t ord_f32(float f) {
+  uint32_t b = __float_as_uint(f);
+  if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 0u;  // NaN
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ uint64_t rank_key(float score, uint32_t id) {
+  return ((uint64_t)ord_f32(score) << 32) | (uint64_t)(0xFFFFFFFFu - id);
+}
+__device__ __forceinline__ int key_id(uint64_t key) { return (int)(0xFFFFFFFFu - (uint32_t)key); }
+
+// ------------------------------------------------------- per-row streaming top-k
+// Keeps the `kfar` (<= 15) best blocks offered so far, in registers. Blocks must
+// be offered in increasing id order, so a later block with a score equal to the
+// current worst kept one never replaces it (the lower id wins).
+struct RowTopK {
+  uint64_t key[kMaxFar];
+  uint64_t worst;
+  int worst_slot;
+  int count;
+  int kfar;
+
+  __device__ __forceinline__ void init(int kf) {
+    kfar = kf;
+    count = 0;
+    worst = 0;
+    worst_slot = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxFar; ++i) key[i] = 0;
+  }
+  __device__ __forceinline__ void recompute() {
+    uint64_t w = ~0ull;
+    int ws = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxFar; ++i)
+      if (i < kfar && key[i] < w) { w = key[i]; ws = i; }
+    worst = w;
+    worst_slot = ws;
+  }
+  __device__ __forceinline__ void put(int slot, uint64_t k) {
+#pragma unroll
+    for (int i = 0; i < kMaxFar; ++i)
+      if (i == slot) key[i] = k;
+  }
+  // Cheap pre-test for the hot loop: can this score enter at all?
+  __device__ __forceinline__ bool wants(uint64_t k) const { return count < kfar || k > worst; }
+  __device__ __forceinline__ void offer(uint64_t k) {
+    if (count < kfar) {
+      put(count, k);
+      ++count;
+      if (count == kfar) recompute();
+      return;
+    }
+    if (kfar == 0 || k <= worst) return;
+    put(worst_slot, k);
+    recompute();
+  }
+  // Writes the kept blocks plus `local`, ascending, padded with -1, to out[0..k).
+  __device__ __forceinline__ void emit(int local, int k, int32_t* out) const {
+    int v[kMaxK];
+#pragma unroll
+    for (int i = 0; i < kMaxK; ++i) v[i] = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < kMaxFar; ++i)
+      if (i < count) v[i] = key_id(key[i]);
+    v[kMaxK - 1] = local;
+    // odd-even transposition sort, fully unrolled (16 elements, 16 rounds)
+#pragma unroll
+    for (int r = 0; r < kMaxK; ++r) {
+#pragma unroll
+      for (int i = (r & 1); i + 1 < kMaxK; i += 2) {
+        int a = v[i], b = v[i + 1];
+        v[i] = min(a, b);
+        v[i + 1] = max(a, b);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxK; ++i)
+      if (i < k) out[i] = v[i] == 0x7FFFFFFF ? -1 : v[i];
+  }
+};
+
+// ------------------------------------------------------------------- misc math
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+}  // namespace msa

@@ -1,0 +1,56 @@
+// Host-side launchers of the MSA kernels (internal to libmsa).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "msa_common.cuh"
+
+namespace msa {
+
+// Counts every kernel launch / device memset enqueued by the library.
+void note_launches(int n);
+
+// Index branch, prefill (msa_index.cu).
+cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_g,
+                                int d_idx, int k, int32_t* block_ids, float* block_scores,
+                                int64_t nb, const Diag& dg, cudaStream_t st);
+
+// Exp-free top-k over block scores (msa_topk.cu).
+cudaError_t launch_topk(const float* S, int64_t N, int n_g, int64_t nb, int Bk, int k,
+                        int64_t q_offset, const int32_t* seq_lens, int32_t* ids, const Diag& dg,
+                        cudaStream_t st);
+
+// Main branch, prefill (msa_attn.cu).
+struct AttnWs {
+  int32_t* counts;    // [n_g * nb]
+  int32_t* offsets;   // [n_g * nb + 1]
+  int32_t* cursor;    // [n_g * nb]
+  int32_t* tile_off;  // [n_g * nb + 1]
+  int32_t* entries;   // [chunk * n_g * k]
+  uint16_t* part_o;   // [chunk, H_q, k, d] bf16
+  float* part_lse;    // [chunk, H_q, k]
+};
+size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k);
+AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k);
+cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* v,
+                                     const int32_t* ids, int64_t N, int64_t q0, int64_t q1,
+                                     int H_q, int H_kv, int d, int k, float scale, void* out,
+                                     float* lse, const AttnWs& ws, int64_t nb, const Diag& dg,
+                                     cudaStream_t st);
+
+// Decode (msa_decode.cu).
+cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,
+                                const int32_t* page_table, const int32_t* seq_lens, int B,
+                                int max_pages, int n_g, int d_idx, float* scores,
+                                const Diag& dg, cudaStream_t st);
+size_t decode_ws_bytes(int B, int H_q, int d, int k);
+cudaError_t launch_decode_attn(const void* q, const void* k_pages, const void* v_pages,
+                               int kv_fp8, const float* k_scale, const float* v_scale,
+                               const int32_t* page_table, const int32_t* seq_lens,
+                               const int32_t* ids, int B, int max_pages, int H_q, int H_kv,
+                               int d, int k, float scale, void* out, float* lse, void* ws,
+                               const Diag& dg, cudaStream_t st);
+
+}  // namespace msa

@@ -1,0 +1,181 @@
+/* msa.h - C ABI of the MiniMax Sparse Attention (MSA) forward path on GB300.
+ *
+ * The method, as defined by "MiniMax Sparse Attention (MSA): a Two-Branch
+ * Block-Sparse Attention Trained on a 109B-Parameter MoE With a 3T-Token Budget"
+ * (Chinese edition; sections "什么是 MSA" / what MSA is, "两个分支如何工作" /
+ * how the two branches work, "内核协同设计" / kernel co-design, "运行 Kernel" /
+ * running the kernel):
+ *
+ *  index branch  one index-query head per GQA group scores every causally
+ *                visible key of one shared index-key head; the scores are
+ *                max-pooled to blocks of Bk tokens; per (query, group) the k
+ *                best blocks are kept, the query's own block always among them.
+ *  main branch   every query head of the group runs exact scaled-dot-product
+ *                softmax attention over the causally visible tokens of exactly
+ *                those blocks.
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller, contiguous,
+ *    row-major, 16-byte aligned. The library never allocates, frees or
+ *    synchronises: it enqueues kernels on `stream` (a cudaStream_t passed as
+ *    void*, NULL = legacy default stream) and returns.
+ *  - bf16 tensors are passed as void* (IEEE bfloat16 bit patterns).
+ *  - Head h of the main branch belongs to GQA group g = h / (H_q / H_kv); the
+ *    index branch has one index-query head per group (n_groups = H_kv).
+ *  - Block ids are int32, sorted ascending, padded with -1 at the end; the
+ *    query's local block (position / Bk) is always present. Among candidate
+ *    blocks of equal score the lower block id wins.
+ *  - Scores are raw dot products of the index heads (no scale, no activation);
+ *    they are accumulated in fp32. The main branch accumulates in fp32, feeds
+ *    the tensor cores bf16 (or E4M3-dequantised) operands, and returns bf16
+ *    outputs and fp32 natural-log LSE = log(sum_j exp(scale * q . k_j)).
+ *  - Supported by the kernels: Bk = 128, 1 <= k <= 16, d and d_idx in {64, 128},
+ *    H_q a multiple of H_kv with 128 % (H_q / H_kv) == 0. Other values return
+ *    MSA_ERR_UNSUPPORTED. Inputs must be finite.
+ *  - Errors are returned, never thrown; nothing is enqueued when an argument
+ *    check fails. A kernel whose bounded wait expires records MSA_ERR_TIMEOUT
+ *    in a device error word that msa_get_error() reads.
+ */
+#ifndef MSA_H
+#define MSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = -1, /* null pointer, bad size, misalignment            */
+  MSA_ERR_UNSUPPORTED = -2, /* valid for the method, not for these kernels      */
+  MSA_ERR_WORKSPACE = -3,   /* workspace smaller than *_workspace_bytes()       */
+  MSA_ERR_CUDA = -4,        /* a launch or runtime call failed                  */
+  MSA_ERR_TIMEOUT = -5      /* a bounded device wait gave up (see msa_get_error) */
+};
+
+enum { MSA_KV_BF16 = 0, MSA_KV_E4M3 = 1 };
+
+/* Human-readable name of a status code (static string). */
+const char* msa_status_string(int status);
+
+/* Library version, for load checks: 0xMMmmpp. */
+int msa_version(void);
+
+/* ---------------------------------------------------------------- prefill -- */
+
+/* Workspace bytes msa_index_select needs (0 today; kept for ABI stability). */
+size_t msa_index_select_workspace_bytes(int64_t N, int n_groups, int d_idx, int Bk, int k);
+
+/* Index branch of prefill: block selection for every (query, group).
+ *   q_idx        [N, n_groups, d_idx] bf16  index queries (one head per group)
+ *   k_idx        [N, d_idx] bf16            shared index keys
+ *   block_ids    [N, n_groups, k] int32     out: selected blocks (see above)
+ *   block_scores [N, n_groups, nb] fp32     out, optional (NULL to skip),
+ *                nb = ceil(N / Bk): S[t, g, b] = max over the visible keys of
+ *                block b of q_idx[t, g] . k_idx[j] for b <= t / Bk; entries
+ *                b > t / Bk are left untouched.
+ * The N x N score matrix is never materialised: scores are pooled and ranked
+ * as they come out of the tensor cores. */
+int msa_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_groups,
+                     int d_idx, int Bk, int k, int32_t* block_ids, float* block_scores,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Exp-free top-k over given block scores ("内核协同设计": ranking raw scores
+ * selects the same blocks as ranking their softmax).
+ *   block_scores [n_rows / n_groups... ] laid out [N, n_groups, nb] fp32; row
+ *                (t, g) is a query at position t + q_offset, or, when seq_lens
+ *                is not NULL, at position seq_lens[t] - 1 (decode: one row
+ *                per sequence t); only b <= position / Bk is read.
+ *   block_ids    [N, n_groups, k] int32 out.
+ * Requires position / Bk < nb for every row. */
+int msa_topk_blocks(const float* block_scores, int64_t N, int n_groups, int64_t nb, int Bk,
+                    int k, int64_t q_offset, const int32_t* seq_lens, int32_t* block_ids,
+                    void* stream);
+
+/* Workspace bytes msa_sparse_attn needs to process up to `chunk_rows` query
+ * positions per pass (chunk_rows = N: one pass). Larger workspaces let the
+ * call take fewer, longer passes. */
+size_t msa_sparse_attn_workspace_bytes(int64_t chunk_rows, int64_t N, int H_q, int H_kv, int d,
+                                       int Bk, int k);
+
+/* Main branch of prefill: exact softmax attention of every query head over
+ * the causally visible tokens of its group's selected blocks.
+ *   q          [N, H_q, d] bf16
+ *   k, v       [N, H_kv, d] bf16
+ *   block_ids  [N, H_kv, k] int32 (as produced by msa_index_select)
+ *   scale      softmax scale (the method uses 1 / sqrt(d))
+ *   out        [N, H_q, d] bf16 out
+ *   lse        [N, H_q] fp32 out (may be NULL)
+ *   workspace  at least msa_sparse_attn_workspace_bytes(c, ...) for some c >= 1;
+ *              the call picks the largest chunk that fits.
+ * Block ids must be valid for their row: -1 or 0 <= id <= t / Bk. */
+int msa_sparse_attn(const void* q, const void* k, const void* v, const int32_t* block_ids,
+                    int64_t N, int H_q, int H_kv, int d, int Bk, int topk, float scale,
+                    void* out, float* lse, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/* ----------------------------------------------------------------- decode -- */
+
+/* Paged caches ("运行 Kernel": page size = block size). Sequence s holds
+ * seq_lens[s] tokens; its logical block b lives in physical page
+ * page_table[s * max_pages + b]. The new token is the last one (position
+ * seq_lens[s] - 1) and must already be written to the caches. */
+
+/* Workspace bytes of the decode index branch: B * n_groups * max_pages fp32. */
+size_t msa_index_select_decode_workspace_bytes(int B, int max_pages, int n_groups);
+
+/* Index branch of decode, one query per sequence.
+ *   q_idx        [B, n_groups, d_idx] bf16
+ *   k_idx_pages  [P, Bk, d_idx] bf16 paged shared index keys
+ *   page_table   [B, max_pages] int32; seq_lens [B] int32 (>= 1)
+ *   block_ids    [B, n_groups, k] int32 out
+ *   block_scores [B, n_groups, max_pages] fp32 out, optional (NULL: kept in
+ *                the workspace); visible entries b <= (seq_lens[s]-1) / Bk. */
+int msa_index_select_decode(const void* q_idx, const void* k_idx_pages,
+                            const int32_t* page_table, const int32_t* seq_lens, int B,
+                            int max_pages, int n_groups, int d_idx, int Bk, int k,
+                            int32_t* block_ids, float* block_scores, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of msa_decode (split-KV partials). */
+size_t msa_decode_workspace_bytes(int B, int H_q, int d, int k);
+
+/* Main branch of decode over a paged bf16 or FP8-E4M3 KV cache.
+ *   q              [B, H_q, d] bf16
+ *   k_pages        [P, Bk, H_kv, d] bf16 or E4M3 bytes (kv_dtype)
+ *   v_pages        same layout and dtype
+ *   k_scale        [H_kv] fp32 per-kv-head dequantisation scale (E4M3 only;
+ *   v_scale        K or V value = code * scale); ignored for bf16
+ *   block_ids      [B, H_kv, k] int32 (msa_index_select_decode)
+ *   out            [B, H_q, d] bf16 out; lse [B, H_q] fp32 out (may be NULL) */
+int msa_decode(const void* q, const void* k_pages, const void* v_pages, int kv_dtype,
+               const float* k_scale, const float* v_scale, const int32_t* page_table,
+               const int32_t* seq_lens, const int32_t* block_ids, int B, int max_pages,
+               int H_q, int H_kv, int d, int Bk, int k, float scale, void* out, float* lse,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------ diagnostics -- */
+
+/* Synchronises `stream`, then returns and clears the device error word:
+ * MSA_OK; MSA_ERR_TIMEOUT if a bounded wait expired; MSA_ERR_INVALID_ARG if a
+ * kernel met device-side data it cannot use (a block id outside 0..t/Bk, a
+ * sequence length outside 1..max_pages*Bk) and skipped it. The first error
+ * since the last call is kept. */
+int msa_get_error(void* stream);
+
+/* Number of kernel launches (and device memsets) this library has enqueued
+ * since it was loaded, on all streams; for accounting in benchmarks. */
+int64_t msa_launch_count(void);
+
+/* Iteration limit of every bounded device wait (default 1 << 26 polls).
+ * Lower values make waits give up sooner; for fault tests. Returns the
+ * previous value. */
+int64_t msa_set_wait_limit(int64_t polls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H */

@@ -245,14 +245,16 @@ def _dims(w: Workload, tensor: int):
 
 
 def host_fill(w: Workload, tensor: int, out: np.ndarray, idx0: int, count: int,
-              fp8: bool = False) -> None:
-    """Write elements [idx0, idx0 + count) into out.flat[idx0 : idx0 + count]."""
+              fp8: bool = False, dst0: Optional[int] = None) -> None:
+    """Write elements [idx0, idx0 + count) into out.flat[dst0 : dst0 + count]
+    (dst0 defaults to idx0)."""
     lib = _host_lib()
     sp = w.spec(w.planted.ctypes.data)
     itemsize = 1 if fp8 else 2
+    dst0 = idx0 if dst0 is None else dst0
     assert out.dtype.itemsize == itemsize and out.flags["C_CONTIGUOUS"]
-    assert idx0 + count <= out.size
-    ptr = out.ctypes.data + idx0 * itemsize
+    assert dst0 + count <= out.size
+    ptr = out.ctypes.data + dst0 * itemsize
     if fp8:
         lib.synth_host_fill_e4m3(ctypes.byref(sp), tensor, idx0, count, ptr)
     else:
@@ -298,6 +300,23 @@ def host_sparse_blocks(w: Workload, tensor: int, blocks_per_seq, fp8: bool = Fal
     return out
 
 
+def host_paged(w: Workload, tensor: int, blocks_per_seq=None, fp8: bool = False) -> np.ndarray:
+    """Identity-paged cache [B * nb, Bk, H, D] (page = s * nb + b). Holds every
+    block when blocks_per_seq is None, else only the listed blocks of each
+    sequence (zeros elsewhere; untouched zero pages cost no host memory)."""
+    H, D = _dims(w, tensor)
+    out = np.zeros((w.B * w.nb, w.Bk, H, D), dtype=np.uint8 if fp8 else np.uint16)
+    per = H * D
+    for s in range(w.B):
+        blocks = range(w.nb) if blocks_per_seq is None else \
+            sorted(set(int(x) for x in blocks_per_seq[s] if x >= 0))
+        for b in blocks:
+            t0, t1 = b * w.Bk, min(w.L, (b + 1) * w.Bk)
+            host_fill(w, tensor, out, (s * w.L + t0) * per, (t1 - t0) * per, fp8,
+                      dst0=(s * w.nb + b) * w.Bk * per)
+    return out
+
+
 # -------------------------------------------------------------- device fill
 _dev = None
 
@@ -333,6 +352,24 @@ def device_tensor(w: Workload, tensor: int, device="cuda"):
                                         out.data_ptr(), stream)
     if rc != 0:
         raise RuntimeError("synth device fill failed")
+    torch.cuda.current_stream(out.device).synchronize()
+    return out
+
+
+def device_rows(w: Workload, tensor: int, seq_rows, device="cuda"):
+    """Rows (s, t) of a tensor: [len(seq_rows), H, D] torch bf16 on the device."""
+    import torch
+    H, D = _dims(w, tensor)
+    out = torch.empty((len(seq_rows), H, D), dtype=torch.bfloat16, device=device)
+    planted = torch.from_numpy(w.planted).to(device)
+    sp = w.spec(planted.data_ptr())
+    stream = torch.cuda.current_stream(out.device).cuda_stream
+    per = H * D
+    for i, (s, t) in enumerate(seq_rows):
+        rc = _dev_lib().synth_dev_fill_bf16(ctypes.byref(sp), tensor, (s * w.L + t) * per, per,
+                                            out[i].data_ptr(), stream)
+        if rc != 0:
+            raise RuntimeError("synth device fill failed")
     torch.cuda.current_stream(out.device).synchronize()
     return out
 

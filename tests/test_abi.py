@@ -1,0 +1,104 @@
+"""CPU tests of the C ABI: the library loads, exports every declared entry
+point, and rejects bad arguments with status codes before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msa.h")
+
+
+@pytest.fixture(scope="module")
+def msa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_sparse_gqa_index_gb300 as m
+    return m
+
+
+def declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(msa_\w+)\s*\(", src)))
+
+
+def test_header_symbols_exported(msa):
+    names = declared()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(msa.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in msa.EXPORTS, n
+
+
+def test_status_strings(msa):
+    for code, name in [(0, "MSA_OK"), (-1, "MSA_ERR_INVALID_ARG"), (-2, "MSA_ERR_UNSUPPORTED"),
+                       (-3, "MSA_ERR_WORKSPACE"), (-4, "MSA_ERR_CUDA"), (-5, "MSA_ERR_TIMEOUT")]:
+        assert msa.msa_status_string(code) == name
+    assert msa.version() == 0x000100
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every call below fails its checks first
+
+
+def test_index_select_rejects(msa):
+    f = msa._index_select
+    assert f(None, FAKE, 10, 1, 64, 128, 16, FAKE, None, None, 0, None) == -1  # null q_idx
+    assert f(FAKE, FAKE, -1, 1, 64, 128, 16, FAKE, None, None, 0, None) == -1  # N < 0
+    assert f(FAKE + 4, FAKE, 10, 1, 64, 128, 16, FAKE, None, None, 0, None) == -1  # misaligned
+    assert f(FAKE, FAKE, 10, 1, 64, 64, 16, FAKE, None, None, 0, None) == -2  # Bk != 128
+    assert f(FAKE, FAKE, 10, 1, 64, 128, 17, FAKE, None, None, 0, None) == -2  # k > 16
+    assert f(FAKE, FAKE, 10, 1, 96, 128, 16, FAKE, None, None, 0, None) == -2  # d_idx
+    assert f(FAKE, FAKE, 0, 1, 64, 128, 16, FAKE, None, None, 0, None) == 0   # empty: no-op
+
+
+def test_topk_rejects(msa):
+    f = msa._topk
+    assert f(FAKE, 300, 2, 2, 128, 16, 0, None, FAKE, None) == -1   # row 299 needs block 2
+    assert f(FAKE, 10, 2, 4, 128, 0, 0, None, FAKE, None) == -1     # k < 1
+    assert f(FAKE, 10, 2, 4, 128, 20, 0, None, FAKE, None) == -2    # k > 16
+    assert f(None, 10, 2, 4, 128, 16, 0, None, FAKE, None) == -1
+
+
+def test_sparse_attn_rejects_and_workspace(msa):
+    f = msa._sparse_attn
+    args = lambda **kw: [kw.get(n, d) for n, d in [  # noqa: E731
+        ("q", FAKE), ("k", FAKE), ("v", FAKE), ("ids", FAKE), ("N", 1000), ("H_q", 8),
+        ("H_kv", 2), ("d", 128), ("Bk", 128), ("topk", 16), ("scale", 0.1), ("out", FAKE),
+        ("lse", None), ("ws", FAKE), ("wsb", 0), ("st", None)]]
+    assert f(*args(H_q=6, H_kv=4)) == -1          # H_q % H_kv
+    assert f(*args(d=96)) == -2
+    assert f(*args(H_q=12, H_kv=4)) == -2         # G = 3 does not divide 128
+    assert f(*args(out=None)) == -1
+    assert f(*args(wsb=100)) == -3                # too small for a single row
+    w1 = msa.msa_sparse_attn_workspace_bytes(1, 1000, 8, 2, 128)
+    wN = msa.msa_sparse_attn_workspace_bytes(1000, 1000, 8, 2, 128)
+    assert 0 < w1 < wN
+    assert msa.msa_sparse_attn_workspace_bytes(5000, 1000, 8, 2, 128) == wN
+    # partials dominate: chunk * H_q * k * (d * 2 + 4) bytes
+    assert wN >= 1000 * 8 * 16 * (128 * 2 + 4)
+
+
+def test_decode_rejects(msa):
+    f = msa._decode
+    base = [FAKE, FAKE, FAKE, 0, None, None, FAKE, FAKE, FAKE, 4, 10, 32, 8, 128, 128, 16, 0.1,
+            FAKE, None, FAKE, 1 << 30, None]
+    a = list(base); a[3] = 7
+    assert f(*a) == -1                             # bad kv dtype
+    a = list(base); a[3] = 1
+    assert f(*a) == -1                             # E4M3 without scales
+    a = list(base); a[19] = None
+    assert f(*a) == -3                             # no workspace
+    a = list(base); a[11], a[12] = 32, 2
+    assert f(*a) == -2                             # G = 16 > 8
+    g = msa._index_dec
+    assert g(FAKE, FAKE, FAKE, FAKE, 4, 10, 9, 128, 128, 16, FAKE, None, FAKE, 1 << 20, None) == -2
+    assert g(FAKE, FAKE, FAKE, FAKE, 4, 10, 8, 128, 128, 16, FAKE, None, None, 0, None) == -3
+    assert msa.msa_index_select_decode_workspace_bytes(64, 1025, 8) == 64 * 1025 * 8 * 4
+
+
+def test_wait_limit_roundtrip(msa):
+    old = msa.msa_set_wait_limit(123)
+    assert msa.msa_set_wait_limit(old) == 123

@@ -1,0 +1,386 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bars: block ids bit-exact on integer index inputs; on Gaussian inputs set-equal
+up to near-tie swaps (tests/msa_check.py). Attention is compared on the same
+block ids on both sides (taken from the oracle, or equal to it): bf16 output
+max |err| <= 1e-2, fp32 LSE max |err| <= 1e-3, FP8-KV output max |err| <= 5e-2.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.msa_check import bf16_to_np, check_close, check_structure, compare_selection
+
+pytestmark = pytest.mark.gpu
+
+TOL_O, TOL_LSE, TOL_O_FP8 = 1e-2, 1e-3, 5e-2
+
+
+@pytest.fixture(scope="module")
+def msa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_sparse_gqa_index_gb300 as m
+    torch.cuda.set_device(0)
+    return m
+
+
+def kidx2d(t):
+    return t[:, 0].contiguous()
+
+
+# ---------------------------------------------------------------- generator
+
+def test_device_generator_matches_host(msa):
+    for w in [synth.make("tiny"), synth.make("32k", L=3000),
+              synth.make("decode", B=2, L=259, H_q=4, H_kv=2, d=64, d_idx=64)]:
+        for tensor in (synth.T_Q, synth.T_K, synth.T_V, synth.T_QIDX, synth.T_KIDX):
+            dev = synth.device_tensor(w, tensor).view(torch.int16).cpu().numpy().view(np.uint16)
+            host = synth.host_tensor(w, tensor).reshape(dev.shape)
+            assert np.array_equal(dev, host), (w.name, tensor)
+    w = synth.make("decode", B=2, L=259, H_q=4, H_kv=2, d=64, d_idx=64)
+    pt = torch.from_numpy(synth.page_table(w)).cuda()
+    ptn = synth.page_table(w)
+    for fp8 in (False, True):
+        dev = synth.device_paged(w, synth.T_V, pt, fp8=fp8)
+        dev = dev.view(torch.int16 if not fp8 else torch.uint8).cpu().numpy()
+        host = synth.host_paged(w, synth.T_V, fp8=fp8)
+        for s in range(w.B):
+            for b in range(w.nb):
+                n = min(w.Bk, w.L - b * w.Bk)
+                a = dev[ptn[s, b], :n].view(np.uint8 if fp8 else np.uint16)
+                assert np.array_equal(a, host[s * w.nb + b, :n]), (fp8, s, b)
+
+
+# ------------------------------------------------------------- index branch
+
+IDX_CASES = [  # N, n_g, d_idx, k
+    (1, 1, 64, 16), (5, 2, 64, 3), (127, 1, 128, 16), (128, 4, 64, 16), (129, 8, 128, 16),
+    (777, 3, 64, 5), (1000, 8, 128, 16), (2048 + 17, 8, 128, 1), (4096, 1, 64, 16),
+    (3000, 2, 128, 2), (5000, 8, 64, 16)]
+
+
+@pytest.mark.parametrize("N,n_g,d_idx,k", IDX_CASES)
+def test_index_select_exact_on_integer_inputs(msa, N, n_g, d_idx, k):
+    w = synth.make("tiny", L=N, H_q=n_g, H_kv=n_g, d=64, d_idx=d_idx, k=k)
+    qidx = synth.device_tensor(w, synth.T_QIDX)
+    kidx = kidx2d(synth.device_tensor(w, synth.T_KIDX))
+    nb = w.nb
+    scores = torch.full((N, n_g, nb), float("nan"), device="cuda")
+    ids = msa.msa_index_select(qidx, kidx, w.Bk, k, block_scores=scores)
+    ids2 = msa.msa_index_select(qidx, kidx, w.Bk, k)
+    torch.cuda.synchronize()
+    rows = np.arange(N)
+    want, want_s = oracle.index_select(synth.host_tensor(w, synth.T_QIDX)[0], rows,
+                                       synth.host_tensor(w, synth.T_KIDX)[0, :, 0], w.Bk, k,
+                                       nb_out=nb, want_scores=True)
+    got = ids.cpu().numpy()
+    assert np.array_equal(got, want)
+    assert np.array_equal(ids2.cpu().numpy(), want)
+    sc = scores.cpu().numpy().astype(np.float64)
+    vis = np.arange(nb)[None, None, :] <= (rows // w.Bk)[:, None, None]
+    vis = np.broadcast_to(vis, sc.shape)
+    assert np.array_equal(sc[vis], want_s[vis])
+    assert msa.msa_get_error() == 0
+
+
+def _sample_rows(N, Bk, n_random, seed, n_tail=256):
+    rng = np.random.default_rng(seed)
+    rows = set(range(min(N, 2 * Bk)))
+    for _ in range(2):
+        b = int(rng.integers(0, max(1, N // Bk)))
+        rows.update(range(b * Bk, min(N, (b + 1) * Bk)))
+    rows.update(range(max(0, N - n_tail), N))
+    rows.update(int(x) for x in rng.integers(0, N, n_random))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def _index_sampled(msa, w, rows, with_scores=False):
+    qidx = synth.device_tensor(w, synth.T_QIDX)
+    kidx = kidx2d(synth.device_tensor(w, synth.T_KIDX))
+    scores = None
+    if with_scores:
+        scores = torch.full((w.N, w.n_g, w.nb), float("nan"), device="cuda")
+    ids = msa.msa_index_select(qidx, kidx, w.Bk, w.k, block_scores=scores)
+    torch.cuda.synchronize()
+    del qidx
+    kh = synth.host_tensor(w, synth.T_KIDX)[0, :, 0]
+    qh = synth.host_rows(w, synth.T_QIDX, 0, rows)
+    want, want_s = oracle.index_select(qh, rows, kh, w.Bk, w.k, nb_out=w.nb, want_scores=True)
+    got = ids.cpu().numpy()[rows]
+    swaps = compare_selection(got, want, want_s, rows, w.Bk)
+    return ids, got, want, want_s, swaps, scores
+
+
+def test_index_select_gauss_32k(msa):
+    w = synth.make("32k")
+    rows = _sample_rows(w.N, w.Bk, 256, 7)
+    ids, got, want, want_s, swaps, scores = _index_sampled(msa, w, rows, with_scores=True)
+    assert swaps <= 0.01 * got.shape[0] * got.shape[1]
+    sc = scores.cpu().numpy()[rows].astype(np.float64)
+    vis = np.broadcast_to(np.arange(w.nb)[None, None, :] <= (rows // w.Bk)[:, None, None], sc.shape)
+    rel = np.abs(sc[vis] - want_s[vis]) / np.maximum(1.0, np.abs(want_s[vis]))
+    assert rel.max() < 1e-4
+
+
+# ------------------------------------------------------------ exp-free top-k
+
+@pytest.mark.parametrize("N,n_g,nb,k,q_offset,kind", [
+    (2048, 8, 16, 16, 0, "gauss"), (4096, 4, 1024, 16, 127 * 1024, "gauss"),
+    (1000, 2, 1023, 16, 129000, "int"), (700, 3, 3000, 7, 383000, "gauss"),
+    (512, 2, 1024, 16, 130000, "const"), (300, 8, 40, 1, 4800, "int"),
+    (256, 1, 4096, 2, 500000, "int")])
+def test_topk_standalone_exact(msa, N, n_g, nb, k, q_offset, kind):
+    rng = np.random.default_rng(N + nb + k)
+    if kind == "gauss":
+        S = rng.standard_normal((N, n_g, nb)).astype(np.float32)
+    elif kind == "int":
+        S = rng.integers(-3, 4, (N, n_g, nb)).astype(np.float32)  # many exact ties
+    else:
+        S = np.full((N, n_g, nb), 2.5, dtype=np.float32)  # every candidate tied
+    rows = np.arange(N) + q_offset
+    assert (rows[-1]) // 128 < nb
+    want = oracle.topk_blocks(S, rows, 128, k)
+    got = msa.msa_topk_blocks(torch.from_numpy(S).cuda(), 128, k, q_offset).cpu().numpy()
+    assert np.array_equal(got, want)
+
+
+def test_topk_seq_lens_mode(msa):
+    rng = np.random.default_rng(3)
+    B, n_g, nb = 37, 8, 1025
+    S = rng.standard_normal((B, n_g, nb)).astype(np.float32)
+    lens = rng.integers(1, nb * 128 + 1, B).astype(np.int32)
+    want = oracle.topk_blocks(S.reshape(B, n_g, nb), lens.astype(np.int64) - 1, 128, 16)
+    got = msa.msa_topk_blocks(torch.from_numpy(S).cuda(), 128, 16,
+                              seq_lens=torch.from_numpy(lens).cuda()).cpu().numpy()
+    assert np.array_equal(got, want)
+
+
+# -------------------------------------------------------------- main branch
+
+ATTN_CASES = [  # N, H_q, H_kv, d, k, ws_rows (None = one pass)
+    (1, 4, 1, 64, 16, None), (5, 8, 2, 128, 3, None), (129, 4, 1, 64, 16, None),
+    (300, 8, 8, 128, 2, 64), (1000, 16, 2, 64, 16, 333), (777, 32, 8, 128, 5, None),
+    (2048 + 3, 4, 4, 128, 1, None), (4096, 4, 1, 64, 16, 1000)]
+
+
+@pytest.mark.parametrize("N,H_q,H_kv,d,k,ws_rows", ATTN_CASES)
+def test_sparse_attn_on_oracle_ids(msa, N, H_q, H_kv, d, k, ws_rows):
+    w = synth.make("tiny", L=N, H_q=H_q, H_kv=H_kv, d=d, d_idx=64, k=k)
+    rows = np.arange(N)
+    ids = oracle.index_select(synth.host_tensor(w, synth.T_QIDX)[0], rows,
+                              synth.host_tensor(w, synth.T_KIDX)[0, :, 0], w.Bk, k)
+    q = synth.device_tensor(w, synth.T_Q)
+    kk = synth.device_tensor(w, synth.T_K)
+    v = synth.device_tensor(w, synth.T_V)
+    ws = None
+    if ws_rows is not None:
+        ws = torch.empty(msa.msa_sparse_attn_workspace_bytes(ws_rows, N, H_q, H_kv, d, w.Bk, k),
+                         dtype=torch.uint8, device="cuda")
+    out, lse = msa.msa_sparse_attn(q, kk, v, torch.from_numpy(ids).cuda(), w.Bk, w.scale,
+                                   workspace=ws)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.sparse_attn(synth.host_tensor(w, synth.T_Q)[0], rows,
+                                      synth.host_tensor(w, synth.T_K)[0],
+                                      synth.host_tensor(w, synth.T_V)[0], ids, w.Bk, w.scale)
+    check_close("o", bf16_to_np(out), o_ref, TOL_O)
+    check_close("lse", lse.cpu().numpy(), l_ref, TOL_LSE)
+
+
+# ------------------------------------------------------- end-to-end prefill
+
+def _pipeline(msa, w, rows, ws_rows=None):
+    """GPU index branch, then GPU main branch on the GPU's own ids; checks the
+    selection on the sampled rows and the attention on those whose ids equal
+    the oracle's."""
+    ids, got, want, want_s, swaps, _ = _index_sampled(msa, w, rows)
+    q = synth.device_tensor(w, synth.T_Q)
+    kk = synth.device_tensor(w, synth.T_K)
+    v = synth.device_tensor(w, synth.T_V)
+    ws_rows = ws_rows or w.N
+    ws = torch.empty(msa.msa_sparse_attn_workspace_bytes(ws_rows, w.N, w.H_q, w.H_kv, w.d, w.Bk,
+                                                         w.k), dtype=torch.uint8, device="cuda")
+    out, lse = msa.msa_sparse_attn(q, kk, v, ids, w.Bk, w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    del ws, kk, v
+    same = np.array([np.array_equal(got[i], want[i]) for i in range(len(rows))])
+    r2 = rows[same]
+    blocks = sorted(set(int(x) for x in want[same].ravel() if x >= 0))
+    Kh = np.zeros((1, w.nb * w.Bk, w.H_kv, w.d), dtype=np.uint16)
+    Vh = np.zeros_like(Kh)
+    per = w.H_kv * w.d
+    for b in blocks:
+        t0, t1 = b * w.Bk, min(w.N, (b + 1) * w.Bk)
+        synth.host_fill(w, synth.T_K, Kh, t0 * per, (t1 - t0) * per)
+        synth.host_fill(w, synth.T_V, Vh, t0 * per, (t1 - t0) * per)
+    qh = synth.host_rows(w, synth.T_Q, 0, r2)
+    o_ref, l_ref = oracle.sparse_attn(qh, r2, Kh[0], Vh[0], want[same], w.Bk, w.scale)
+    o_gpu = bf16_to_np(out[torch.from_numpy(r2).cuda()])
+    check_close("o", o_gpu, o_ref, TOL_O)
+    check_close("lse", lse[torch.from_numpy(r2).cuda()].cpu().numpy(), l_ref, TOL_LSE)
+    return swaps, len(r2)
+
+
+def test_pipeline_tiny_all_rows(msa):
+    w = synth.make("tiny")
+    rows = np.arange(w.N)
+    swaps, n_checked = _pipeline(msa, w, rows)
+    assert swaps == 0 and n_checked == w.N
+
+
+def test_pipeline_32k(msa):
+    w = synth.make("32k")
+    swaps, n = _pipeline(msa, w, _sample_rows(w.N, w.Bk, 512, 11))
+    assert n > 0
+
+
+def test_pipeline_128k(msa):
+    w = synth.make("128k")
+    swaps, n = _pipeline(msa, w, _sample_rows(w.N, w.Bk, 128, 13, n_tail=128))
+    assert n > 0
+
+
+def test_pipeline_1m(msa):
+    w = synth.make("1m")
+    swaps, n = _pipeline(msa, w, _sample_rows(w.N, w.Bk, 16, 17, n_tail=32)[::4],
+                         ws_rows=w.N // 8)
+    assert n > 0
+
+
+# ------------------------------------------------------------------ decode
+
+def _decode_case(msa, w, fp8):
+    dev = torch.device("cuda")
+    ptn = synth.page_table(w)
+    pt = torch.from_numpy(ptn).to(dev)
+    sl = torch.full((w.B,), w.L, dtype=torch.int32, device=dev)
+    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, :, 0].contiguous()
+    last = [(s, w.L - 1) for s in range(w.B)]
+    q = synth.device_rows(w, synth.T_Q, last)
+    qidx = synth.device_rows(w, synth.T_QIDX, last)
+    ids = msa.msa_index_select_decode(qidx, kidx_p, pt, sl, w.Bk, w.k)
+    torch.cuda.synchronize()
+    del kidx_p
+    ident = synth.page_table(w, permute=False)
+    sl_np = np.full(w.B, w.L, dtype=np.int32)
+    kh = synth.host_paged(w, synth.T_KIDX)[:, :, 0]
+    qidx_h = np.stack([synth.host_rows(w, synth.T_QIDX, s, [w.L - 1])[0] for s in range(w.B)])
+    want, want_s = oracle.decode_index_select(qidx_h, kh, ident, sl_np, w.Bk, w.k, nb_out=w.nb,
+                                              want_scores=True)
+    del kh
+    got = ids.cpu().numpy()
+    compare_selection(got, want, want_s, np.full(w.B, w.L - 1), w.Bk)
+    # attention on the oracle's ids
+    kp = synth.device_paged(w, synth.T_K, pt, fp8=fp8)
+    vp = synth.device_paged(w, synth.T_V, pt, fp8=fp8)
+    ks, vs = synth.fp8_scales(w.H_kv)
+    kw = {}
+    if fp8:
+        kw = dict(k_scale=torch.from_numpy(ks).to(dev), v_scale=torch.from_numpy(vs).to(dev))
+    out, lse = msa.msa_decode(q, kp, vp, pt, sl, torch.from_numpy(want).to(dev), w.Bk, w.scale,
+                              **kw)
+    torch.cuda.synchronize()
+    del kp, vp
+    blocks = [sorted(set(int(x) for x in want[s].ravel() if x >= 0)) for s in range(w.B)]
+    Kh = synth.host_paged(w, synth.T_K, blocks, fp8=fp8)
+    Vh = synth.host_paged(w, synth.T_V, blocks, fp8=fp8)
+    qh = np.stack([synth.host_rows(w, synth.T_Q, s, [w.L - 1])[0] for s in range(w.B)])
+    o_ref, l_ref = oracle.decode_attn(qh, Kh, Vh, ident, sl_np, want, w.Bk, w.scale, fp8=fp8,
+                                      k_scale=ks if fp8 else None, v_scale=vs if fp8 else None)
+    check_close("o", bf16_to_np(out), o_ref, TOL_O_FP8 if fp8 else TOL_O)
+    check_close("lse", lse.cpu().numpy(), l_ref, TOL_LSE * (10 if fp8 else 1))
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_small(msa, fp8):
+    w = synth.make("decode", B=5, L=128 * 20 + 1, H_q=16, H_kv=4, d=64, d_idx=64)
+    _decode_case(msa, w, fp8)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_full_config(msa, fp8):
+    _decode_case(msa, synth.make("decode"), fp8)
+
+
+def test_decode_ragged_lengths(msa):
+    """Sequences of different lengths (1 token up to several blocks, partial
+    last pages) in one batch; integer index inputs so the ids are exact."""
+    w = synth.make("decode", B=6, L=1000, H_q=8, H_kv=2, d=128, d_idx=128, kind=synth.KIND_INT,
+                   k=4)
+    lens = np.array([1, 2, 128, 129, 640, 1000], dtype=np.int32)
+    dev = torch.device("cuda")
+    ptn = synth.page_table(w)
+    pt = torch.from_numpy(ptn).to(dev)
+    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, :, 0].contiguous()
+    qidx = synth.device_rows(w, synth.T_QIDX, [(s, int(lens[s]) - 1) for s in range(w.B)])
+    ids = msa.msa_index_select_decode(qidx, kidx_p, pt, torch.from_numpy(lens).to(dev), w.Bk,
+                                      w.k)
+    ident = synth.page_table(w, permute=False)
+    kh = synth.host_paged(w, synth.T_KIDX)[:, :, 0]
+    qh = np.stack([synth.host_rows(w, synth.T_QIDX, s, [int(lens[s]) - 1])[0]
+                   for s in range(w.B)])
+    want = oracle.decode_index_select(qh, kh, ident, lens, w.Bk, w.k)
+    assert np.array_equal(ids.cpu().numpy(), want)
+    q = synth.device_rows(w, synth.T_Q, [(s, int(lens[s]) - 1) for s in range(w.B)])
+    kp = synth.device_paged(w, synth.T_K, pt)
+    vp = synth.device_paged(w, synth.T_V, pt)
+    out, lse = msa.msa_decode(q, kp, vp, pt, torch.from_numpy(lens).to(dev), ids, w.Bk, w.scale)
+    torch.cuda.synchronize()
+    Kh = synth.host_paged(w, synth.T_K)
+    Vh = synth.host_paged(w, synth.T_V)
+    qhq = np.stack([synth.host_rows(w, synth.T_Q, s, [int(lens[s]) - 1])[0] for s in range(w.B)])
+    o_ref, l_ref = oracle.decode_attn(qhq, Kh, Vh, ident, lens, want, w.Bk, w.scale)
+    check_close("o", bf16_to_np(out), o_ref, TOL_O)
+    check_close("lse", lse.cpu().numpy(), l_ref, TOL_LSE)
+
+
+def test_decode_matches_prefill_row_on_gpu(msa):
+    """Decoding the last token against the cache equals the last prefill row."""
+    w = synth.make("decode", B=1, L=128 * 9 + 5, H_q=8, H_kv=2, d=128, d_idx=128,
+                   kind=synth.KIND_INT, k=4)
+    dev = torch.device("cuda")
+    qidx = synth.device_tensor(w, synth.T_QIDX)
+    kidx = kidx2d(synth.device_tensor(w, synth.T_KIDX))
+    q = synth.device_tensor(w, synth.T_Q)
+    kk = synth.device_tensor(w, synth.T_K)
+    v = synth.device_tensor(w, synth.T_V)
+    ids_p = msa.msa_index_select(qidx, kidx, w.Bk, w.k)
+    out_p, lse_p = msa.msa_sparse_attn(q, kk, v, ids_p, w.Bk, w.scale)
+    pt = torch.from_numpy(synth.page_table(w)).to(dev)
+    sl = torch.tensor([w.L], dtype=torch.int32, device=dev)
+    ids_d = msa.msa_index_select_decode(qidx[-1:], synth.device_paged(w, synth.T_KIDX, pt)[:, :, 0]
+                                        .contiguous(), pt, sl, w.Bk, w.k)
+    out_d, lse_d = msa.msa_decode(q[-1:], synth.device_paged(w, synth.T_K, pt),
+                                  synth.device_paged(w, synth.T_V, pt), pt, sl, ids_d, w.Bk,
+                                  w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(ids_p[-1:], ids_d)
+    check_close("o", bf16_to_np(out_d), bf16_to_np(out_p[-1:]), 8e-3)
+    check_close("lse", lse_d.cpu().numpy(), lse_p[-1:].cpu().numpy(), 1e-4)
+
+
+# ------------------------------------------------------------ determinism
+
+def test_repeat_runs_bitwise_identical(msa):
+    w = synth.make("32k", L=8192 + 77)
+    qidx = synth.device_tensor(w, synth.T_QIDX)
+    kidx = kidx2d(synth.device_tensor(w, synth.T_KIDX))
+    q = synth.device_tensor(w, synth.T_Q)
+    kk = synth.device_tensor(w, synth.T_K)
+    v = synth.device_tensor(w, synth.T_V)
+    outs = []
+    for _ in range(3):
+        ids = msa.msa_index_select(qidx, kidx, w.Bk, w.k)
+        o, l = msa.msa_sparse_attn(q, kk, v, ids, w.Bk, w.scale)
+        outs.append((ids.clone(), o.clone(), l.clone()))
+    torch.cuda.synchronize()
+    for ids, o, l in outs[1:]:
+        assert torch.equal(ids, outs[0][0]) and torch.equal(o, outs[0][1]) and \
+            torch.equal(l, outs[0][2])
+    check_structure(outs[0][0].cpu().numpy(), np.arange(w.N), w.Bk)
+    assert msa.msa_get_error() == 0
