@@ -10,117 +10,335 @@
 //
 // Rows of the score matrix are the flattened (t, g) pairs of q_idx
 // [N, n_g, d_idx]; columns are keys. Because the index key head is shared, one
-// k_idx block serves all groups of a row tile.
+// k_idx block serves every group of a row tile.
 //
-// This version computes on CUDA cores: a CTA owns 64 rows and streams key
-// blocks 0 .. loc_max; each key block becomes one fp32 max per row, which the
-// row's owner thread feeds to its streaming top-k (RowTopK).
+// GB300 design (one persistent CTA per SM, 10 warps):
+//   warp 0      TMA producer: the CTA's 256 q_idx rows once per tile, then
+//               k_idx blocks (128 keys x d_idx) through a 4-stage ring;
+//   warp 1      TMEM owner and MMA issuer: per key block two 128x128xd_idx
+//               tcgen05 MMAs (the two 128-row halves share the k_idx tile, so
+//               every k_idx byte fetched from L2 feeds 256 rows) into one of
+//               two TMEM accumulator stages (4 x 128 of the 512 columns);
+//   warps 2-9   epilogue: each thread owns one row, reads its 128 scores of the
+//               block from TMEM, applies the causal mask on the diagonal block,
+//               max-pools them to the block score and feeds it to the row's
+//               streaming top-k (RowTopK), overlapping the next block's MMAs.
+// Tiles are visited heaviest-first in a boustrophedon order over the CTAs so
+// the causal triangle balances; all CTAs sweep k_idx in the same order, which
+// keeps the re-read k_idx stream in L2.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "msa_kernels.h"
+#include "msa_sm100.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kRows = 64;    // rows (t, g) per CTA
-constexpr int kBk = 128;     // keys per block
-constexpr int kDc = 32;      // d_idx chunk staged per pass
-constexpr int kThreads = 256;
+using namespace sm100;
 
-__global__ void __launch_bounds__(kThreads)
-index_select_cc_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx,
-                       int64_t N, int n_g, int d_idx, int k, int32_t* __restrict__ block_ids,
-                       float* __restrict__ block_scores, int64_t nb) {
-  __shared__ float As[kRows][kDc + 1];
-  __shared__ float Bs[kBk][kDc + 1];
+constexpr int kRows = 256;     // rows (t, g) per tile: two M = 128 halves
+constexpr int kKeys = 128;     // keys per block (= Bk)
+constexpr int kStages = 4;     // k_idx ring depth
+constexpr int kThreads = 320;  // 10 warps
+constexpr int kEpiWarps = 8;
 
+template <int DI>
+struct Smem {
+  static constexpr int kChunks = DI / 64;             // 128-byte K chunks
+  static constexpr int kAChunk = kRows * 128;         // bytes of one A K-chunk
+  static constexpr int kBChunk = kKeys * 128;         // bytes of one B K-chunk
+  static constexpr int kABytes = kAChunk * kChunks;
+  static constexpr int kBBytes = kBChunk * kChunks;
+  static constexpr int kBarOff = kABytes + kStages * kBBytes;
+  // barriers: a_full, a_empty, b_full[S], b_empty[S], t_full[2], t_empty[2], done
+  static constexpr int kNumBars = 2 + 2 * kStages + 4 + 1;
+  static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
+};
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// max of 32 TMEM columns; columns >= lim are masked (lim >= 32: no mask)
+__device__ __forceinline__ float max32(const uint32_t (&r)[32], int lim) {
+  float m0 = -INFINITY, m1 = -INFINITY;
+  if (lim >= 32) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      m0 = fmax3(m0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+      m1 = fmax3(m1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < lim) m0 = fmaxf(m0, __uint_as_float(r[i]));
+  }
+  return fmaxf(m0, m1);
+}
+
+template <int DI>
+__global__ void __launch_bounds__(kThreads, 1)
+index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k, int64_t N, int n_g, int k,
+                       int32_t* __restrict__ block_ids, float* __restrict__ block_scores,
+                       int64_t nb, int n_tiles, Diag dg) {
+  using S = Smem<DI>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sA = smem;
+  unsigned char* sB = smem + S::kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  uint64_t* a_full = bars + 0;
+  uint64_t* a_empty = bars + 1;
+  uint64_t* b_full = bars + 2;
+  uint64_t* b_empty = bars + 2 + kStages;
+  uint64_t* t_full = bars + 2 + 2 * kStages;
+  uint64_t* t_empty = t_full + 2;
+  uint64_t* done_bar = t_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t n_rows = N * n_g;
-  const int64_t n_tiles = (n_rows + kRows - 1) / kRows;
-  const int64_t tile = n_tiles - 1 - blockIdx.x;  // heavy tiles first
-  const int64_t row0 = tile * kRows;
-  const int tid = threadIdx.x;
-  const int rg = tid >> 4;   // rows rg*4 .. rg*4+3
-  const int kg = tid & 15;   // keys kg + 16 i
+  const bool want_scores = block_scores != nullptr;
 
-  const int64_t last_row = min(row0 + kRows, n_rows) - 1;
-  const int64_t loc_max = (last_row / n_g) / kBk;
-  const int64_t b_end = block_scores ? loc_max + 1 : loc_max;  // local block only pooled on request
+  if (threadIdx.x == 0) {
+    mbar_init(a_full, 1);
+    mbar_init(a_empty, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&t_full[s], 1);
+      mbar_init(&t_empty[s], kEpiWarps);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
 
-  // owner thread of row rg*4 + kg (kg < 4)
-  const bool owner = kg < 4;
-  const int64_t my_row = row0 + rg * 4 + kg;
-  const bool my_valid = owner && my_row < n_rows;
-  const int64_t my_t = my_valid ? my_row / n_g : 0;
-  const int64_t my_loc = my_t / kBk;
-  RowTopK top;
-  top.init(k - 1);
+  // tile schedule: heaviest first, boustrophedon over the CTAs
+  const int G = gridDim.x;
+  auto tile_of = [&](int round, int& tile) -> bool {
+    int i = round * G + ((round & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+    if (i >= n_tiles) return false;
+    tile = n_tiles - 1 - i;
+    return true;
+  };
+  auto key_blocks = [&](int tile) -> int64_t {
+    int64_t last = min((int64_t)tile * kRows + kRows, n_rows) - 1;
+    int64_t loc_max = (last / n_g) / kKeys;
+    return want_scores ? loc_max + 1 : loc_max;
+  };
+  const int rounds = (n_tiles + G - 1) / G;
 
-  for (int64_t b = 0; b < b_end; ++b) {
-    float acc[4][8];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[r][i] = 0.f;
-
-    for (int c0 = 0; c0 < d_idx; c0 += kDc) {
-      __syncthreads();
-      for (int e = tid; e < kRows * kDc; e += kThreads) {
-        int r = e / kDc, c = e % kDc;
-        int64_t row = row0 + r;
-        float x = 0.f;
-        if (row < n_rows) x = __uint_as_float((uint32_t)q_idx[row * d_idx + c0 + c] << 16);
-        As[r][c] = x;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t a_par = 0;
+      bool a_armed = false;
+      uint32_t armed_par[kStages];
+      bool armed[kStages];
+      for (int s = 0; s < kStages; ++s) armed[s] = false;
+      long long it = 0;
+      bool ok = true;
+      for (int rd = 0; rd < rounds && ok; ++rd) {
+        int tile;
+        if (!tile_of(rd, tile)) continue;
+        int64_t nkb = key_blocks(tile);
+        if (nkb <= 0) continue;
+        if (!mbar_wait(a_empty, a_par ^ 1, abort_flag, dg)) { ok = false; break; }
+        mbar_arrive_expect_tx(a_full, S::kABytes);
+        for (int c = 0; c < S::kChunks; ++c)
+          tma_load_2d(sA + c * S::kAChunk, &tm_q, a_full, c * 64, tile * kRows);
+        a_armed = true;
+        a_par ^= 1;
+        for (int64_t b = 0; b < nkb; ++b, ++it) {
+          const int s = (int)(it % kStages);
+          const uint32_t par = (uint32_t)((it / kStages) & 1);
+          if (!mbar_wait(&b_empty[s], par ^ 1, abort_flag, dg)) { ok = false; break; }
+          mbar_arrive_expect_tx(&b_full[s], S::kBBytes);
+          for (int c = 0; c < S::kChunks; ++c)
+            tma_load_2d(sB + s * S::kBBytes + c * S::kBChunk, &tm_k, &b_full[s], c * 64,
+                        (int32_t)(b * kKeys));
+          armed[s] = true;
+          armed_par[s] = par;
+        }
       }
-      for (int e = tid; e < kBk * kDc; e += kThreads) {
-        int j = e / kDc, c = e % kDc;
-        int64_t key = b * kBk + j;
-        float x = 0.f;
-        if (key < N) x = __uint_as_float((uint32_t)k_idx[key * d_idx + c0 + c] << 16);
-        Bs[j][c] = x;
-      }
-      __syncthreads();
-#pragma unroll 8
-      for (int c = 0; c < kDc; ++c) {
-        float a[4], bb[8];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) a[r] = As[rg * 4 + r][c];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) bb[i] = Bs[kg + 16 * i][c];
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[r][i] = fmaf(a[r], bb[i], acc[r][i]);
+      if (!ok) {  // let every issued copy land before shared memory is released
+        for (int s = 0; s < kStages; ++s)
+          if (armed[s]) mbar_drain(&b_full[s], armed_par[s]);
+        if (a_armed) mbar_drain(a_full, a_par ^ 1);
       }
     }
-    // causal mask and per-thread max over its 8 keys, then over the 16 lanes
-    float mx[4];
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kKeys);
+      const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+      uint32_t a_par = 0;
+      long long it = 0;
+      bool ok = true;
+      for (int rd = 0; rd < rounds && ok; ++rd) {
+        int tile;
+        if (!tile_of(rd, tile)) continue;
+        int64_t nkb = key_blocks(tile);
+        if (nkb <= 0) continue;
+        if (!mbar_wait(a_full, a_par, abort_flag, dg)) { ok = false; break; }
+        a_par ^= 1;
+        for (int64_t b = 0; b < nkb; ++b, ++it) {
+          const int s = (int)(it % kStages);
+          const uint32_t bpar = (uint32_t)((it / kStages) & 1);
+          const int acc = (int)(it & 1);
+          const uint32_t tpar = (uint32_t)((it >> 1) & 1);
+          if (!mbar_wait(&t_empty[acc], tpar ^ 1, abort_flag, dg)) { ok = false; break; }
+          if (!mbar_wait(&b_full[s], bpar, abort_flag, dg)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      int64_t row = row0 + rg * 4 + r;
-      int64_t t = row / n_g;
-      float m = -INFINITY;
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256 + h * 128);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        int64_t key = b * kBk + kg + 16 * i;
-        if (key <= t) m = fmaxf(m, acc[r][i]);
+            for (int kk = 0; kk < DI / 16; ++kk) {
+              const int c = kk / 4, off = (kk % 4) * 32;
+              uint64_t ad = desc_kmajor_sw128(a_base + c * S::kAChunk + h * 128 * 128 + off);
+              uint64_t bd = desc_kmajor_sw128(b_base + s * S::kBBytes + c * S::kBChunk + off);
+              mma_bf16_ss(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(&b_empty[s]);
+          mma_commit(&t_full[acc]);
+        }
+        if (ok) mma_commit(a_empty);
       }
-      mx[r] = m;
+      // every MMA issued by this thread has completed once done_bar flips
+      mma_commit(done_bar);
+      mbar_drain(done_bar, 0);
     }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;             // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;      // accumulator half (rows h*128 ..)
+    const int row_in_tile = h * 128 + q * 32 + lane;
+    long long it = 0;
+    bool ok = true;
+    for (int rd = 0; rd < rounds && ok; ++rd) {
+      int tile;
+      if (!tile_of(rd, tile)) continue;
+      const int64_t nkb = key_blocks(tile);
+      const int64_t r = (int64_t)tile * kRows + row_in_tile;
+      const bool valid = r < n_rows;
+      const int64_t t = valid ? r / n_g : 0;
+      const int64_t loc = t / kKeys;
+      RowTopK top;
+      top.init(k - 1);
+      for (int64_t b = 0; b < nkb; ++b, ++it) {
+        const int acc = (int)(it & 1);
+        const uint32_t tpar = (uint32_t)((it >> 1) & 1);
+        // one lane waits, the warp follows (tcgen05.ld needs a converged warp)
+        int got = 0;
+        if (lane == 0) got = mbar_wait(&t_full[acc], tpar, abort_flag, dg) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256 + h * 128);
+        // visible columns of this row in block b: all, or up to t on the diagonal
+        const int lim = (b < loc) ? 128 : (b == loc ? (int)(t - b * kKeys) + 1 : 0);
+        float m = -INFINITY;
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], off));
-    if (my_valid && b <= my_loc) {
-      float v = mx[0];
-#pragma unroll
-      for (int r = 1; r < 4; ++r)
-        if (kg == r) v = mx[r];
-      if (block_scores) block_scores[my_row * nb + b] = v;
-      if (b < my_loc) {
-        uint64_t key = rank_key(v, (uint32_t)b);
-        if (top.wants(key)) top.offer(key);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32(taddr + half * 64, r0);
+          tmem_ld32(taddr + half * 64 + 32, r1);
+          tmem_ld_wait();
+          m = fmaxf(m, max32(r0, lim - half * 64));
+          m = fmaxf(m, max32(r1, lim - half * 64 - 32));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&t_empty[acc]);
+        if (valid && b <= loc) {
+          if (want_scores) block_scores[r * nb + b] = m;
+          if (b < loc) {
+            const uint64_t key = rank_key(m, (uint32_t)b);
+            if (top.wants(key)) top.offer(key);
+          }
+        }
       }
+      if (ok && valid) top.emit((int)loc, k, block_ids + r * k);
     }
   }
-  if (my_valid) top.emit((int)my_loc, k, block_ids + my_row * k);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+// 2D bf16 tensor [rows, cols] (cols contiguous), box {64 cols, box_rows}, 128B swizzle
+bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <int DI>
+cudaError_t launch_tc(const void* q_idx, const void* k_idx, int64_t N, int n_g, int k,
+                      int32_t* block_ids, float* block_scores, int64_t nb, const Diag& dg,
+                      cudaStream_t st) {
+  const int64_t n_rows = N * n_g;
+  const int n_tiles = (int)((n_rows + kRows - 1) / kRows);
+  CUtensorMap tq, tk;
+  if (!make_map_2d(&tq, q_idx, n_rows, DI, kRows) || !make_map_2d(&tk, k_idx, N, DI, kKeys))
+    return cudaErrorInvalidValue;
+  const int smem = Smem<DI>::kBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(index_select_tc_kernel<DI>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = std::min(n_tiles, num_sms());
+  note_launches(1);
+  index_select_tc_kernel<DI><<<grid, kThreads, smem, st>>>(tq, tk, N, n_g, k, block_ids,
+                                                          block_scores, nb, n_tiles, dg);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -128,14 +346,10 @@ index_select_cc_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __res
 cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_g,
                                 int d_idx, int k, int32_t* block_ids, float* block_scores,
                                 int64_t nb, const Diag& dg, cudaStream_t st) {
-  (void)dg;
-  int64_t n_tiles = (N * n_g + kRows - 1) / kRows;
-  if (n_tiles == 0) return cudaSuccess;
-  note_launches(1);
-  index_select_cc_kernel<<<(unsigned)n_tiles, kThreads, 0, st>>>(
-      (const uint16_t*)q_idx, (const uint16_t*)k_idx, N, n_g, d_idx, k, block_ids,
-      block_scores, nb);
-  return cudaGetLastError();
+  if (N * n_g == 0) return cudaSuccess;
+  if (d_idx == 128)
+    return launch_tc<128>(q_idx, k_idx, N, n_g, k, block_ids, block_scores, nb, dg, st);
+  return launch_tc<64>(q_idx, k_idx, N, n_g, k, block_ids, block_scores, nb, dg, st);
 }
 
 }  // namespace msa
