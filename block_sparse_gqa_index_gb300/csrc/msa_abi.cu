@@ -1,6 +1,8 @@
 // C ABI of libmsa (declared in include/msa.h): argument checks, workspace
 // carving and kernel launches. No allocation, no synchronisation (except in
 // msa_get_error), no exceptions.
+#include <stdlib.h>
+
 #include <algorithm>
 #include <atomic>
 #include <mutex>
@@ -17,7 +19,15 @@ namespace {
 
 __device__ int g_msa_error = 0;
 
-long long g_wait_limit = 1ll << 26;
+long long initial_wait_limit() {
+  const char* e = getenv("MSA_WAIT_LIMIT");
+  if (e && *e) {
+    long long v = atoll(e);
+    if (v >= 0) return v;
+  }
+  return 1ll << 26;
+}
+long long g_wait_limit = initial_wait_limit();
 std::mutex g_mu;
 int* g_err_ptr[64] = {nullptr};
 

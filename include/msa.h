@@ -169,7 +169,8 @@ int msa_get_error(void* stream);
  * since it was loaded, on all streams; for accounting in benchmarks. */
 int64_t msa_launch_count(void);
 
-/* Iteration limit of every bounded device wait (default 1 << 26 polls).
+/* Iteration limit of every bounded device wait (default 1 << 26 polls, or
+ * the MSA_WAIT_LIMIT environment variable read when the library loads).
  * Lower values make waits give up sooner; for fault tests. Returns the
  * previous value. */
 int64_t msa_set_wait_limit(int64_t polls);
