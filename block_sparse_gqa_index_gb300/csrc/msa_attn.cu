@@ -15,14 +15,18 @@
 // (query, head) exactly:  lse = log sum_s exp(lse_s),
 //                         o   = sum_s exp(lse_s - lse) * o_s.
 // Queries are processed in chunks so that the partials fit the workspace.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "msa_kernels.h"
+#include "msa_sm100.cuh"
 
 namespace msa {
 namespace {
 
 constexpr int kBk = 128;
 constexpr int kTileRows = 128;
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;  // bucketing kernels
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -107,191 +111,338 @@ __global__ void bucket_fill_kernel(const int32_t* __restrict__ ids, int64_t q0, 
   }
 }
 
-// ------------------------------------------------------ tile kernel (CUDA cores)
+// ------------------------------------------------------- tile kernel (tcgen05)
+// One persistent CTA per SM walks a contiguous range of tiles (consecutive
+// tiles mostly share a bucket, so K / V of the bucket's block are loaded once):
+//   warp 0     TMA: K and V of the bucket's block (128 keys, head g) when the
+//              bucket changes (single buffer, released after the bucket's
+//              last P.V MMA);
+//   warp 1     TMEM owner and MMA issuer: S = Q K^T (128 x 128, A = Q tile,
+//              B = K block, both K-major 128B-swizzled in shared memory), then,
+//              once softmax wrote P, O = P V (A = P read from TMEM, B = V as an
+//              MN-major operand). Two TMEM stages of 256 columns (S/P | O); the
+//              S MMA of tile i+1 is issued before the P.V MMA of tile i;
+//   warps 2-5  Q producers, one per Q stage (4 stages): gather the G head rows
+//              of each of the tile's queries with 16-byte cp.async into the
+//              128B-swizzled layout, record each row's query position and
+//              partial slot, then publish the stage;
+//   warps 6-9  softmax + epilogue, one score row per thread: masked row max,
+//              exp2, row sum, P (bf16) back into TMEM over S; then O / l in
+//              bf16 and the row's LSE to the partial buffers.
 template <int D>
-__global__ void __launch_bounds__(kThreads)
-attn_tile_cc_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ kk,
-                    const uint16_t* __restrict__ v, int64_t N, int64_t q0, int H_q, int H_kv,
-                    int k, float scale_log2, int64_t nb, const int32_t* __restrict__ entries,
-                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_off,
-                    int64_t n_b, uint16_t* __restrict__ part_o, float* __restrict__ part_lse) {
-  constexpr int DP = D + 2;  // padded smem row (bf16 elements)
-  extern __shared__ __align__(16) unsigned char smem[];
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);
-  uint16_t* Ks = Qs + kTileRows * DP;
-  uint16_t* Vs = Ks + kBk * DP;
-  float* Ss = reinterpret_cast<float*>(Vs + kBk * DP);  // [128][129]
-  float* row_m = Ss + kTileRows * 129;
-  float* row_l = row_m + kTileRows;
-  int* row_t = reinterpret_cast<int*>(row_l + kTileRows);
-  int* row_dst = row_t + kTileRows;
+struct AttnSmem {
+  static constexpr int kKVBytes = kBk * D * 2;            // one of K or V
+  static constexpr int kQBytes = kTileRows * D * 2;       // one Q stage
+  static constexpr int kQStages = 4;
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKVBytes;
+  static constexpr int kQOff = 2 * kKVBytes;
+  static constexpr int kMetaOff = kQOff + kQStages * kQBytes;  // row_t, row_dst per stage
+  static constexpr int kBarOff = kMetaOff + kQStages * kTileRows * 8;
+  // kv_full, kv_empty, q_full[4], q_empty[4], s_full[2], p_full[2], o_full[2], t_empty[2], done
+  static constexpr int kNumBars = 2 + 2 * kQStages + 8 + 1;
+  static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
+};
 
+constexpr int kAttnThreads = 320;
+
+__device__ __forceinline__ int64_t find_bucket(const int32_t* __restrict__ tile_off, int64_t n_b,
+                                               int64_t tile) {
+  int64_t lo = 0, hi = n_b - 1;
+  while (lo < hi) {
+    int64_t mid = (lo + hi + 1) >> 1;
+    if (tile_off[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const uint16_t* __restrict__ q, int64_t q0, int H_q, int H_kv, int k,
+                    float scale_log2, int64_t nb, const int32_t* __restrict__ entries,
+                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_off,
+                    int64_t n_b, uint16_t* __restrict__ part_o, float* __restrict__ part_lse,
+                    Diag dg) {
+  using namespace sm100;
+  using S = AttnSmem<D>;
+  constexpr int QS = S::kQStages;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  int32_t* row_t_all = reinterpret_cast<int32_t*>(smem + S::kMetaOff);
+  int32_t* row_dst_all = row_t_all + QS * kTileRows;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* q_full = bars + 2;
+  uint64_t* q_empty = q_full + QS;
+  uint64_t* s_full = q_empty + QS;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_full = p_full + 2;
+  uint64_t* t_empty = o_full + 2;
+  uint64_t* done_bar = t_empty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = H_q / H_kv;
   const int qt = kTileRows / G;
-  const int tid = threadIdx.x;
-  const int total = tile_off[n_b];
-  int64_t cur_bk = -1;
 
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    // bucket of this tile: last bk with tile_off[bk] <= tile
-    int64_t lo = 0, hi = n_b - 1;
-    while (lo < hi) {
-      int64_t mid = (lo + hi + 1) >> 1;
-      if (tile_off[mid] <= tile) lo = mid; else hi = mid - 1;
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
+    for (int s = 0; s < QS; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1 + 4);  // S-MMA commit + the 4 softmax warps (row metadata read)
     }
-    const int64_t bk = lo;
-    const int g = (int)(bk / nb);
-    const int64_t b = bk % nb;
-    const int e0 = offsets[bk] + (tile - tile_off[bk]) * qt;
-    const int e1 = min(e0 + qt, offsets[bk + 1]);
-    const int nrows = (e1 - e0) * G;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 4);
+      mbar_init(&o_full[s], 1);
+      mbar_init(&t_empty[s], 4);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
 
-    __syncthreads();
-    if (bk != cur_bk) {  // K, V of block b, head g
-      for (int e = tid; e < kBk * (D / 2); e += kThreads) {
-        int j = e / (D / 2), c2 = e % (D / 2);
-        int64_t key = b * kBk + j;
-        uint32_t kw = 0, vw = 0;
-        if (key < N) {
-          size_t off = ((size_t)key * H_kv + g) * D + 2 * c2;
-          kw = *reinterpret_cast<const uint32_t*>(kk + off);
-          vw = *reinterpret_cast<const uint32_t*>(v + off);
-        }
-        *reinterpret_cast<uint32_t*>(Ks + j * DP + 2 * c2) = kw;
-        *reinterpret_cast<uint32_t*>(Vs + j * DP + 2 * c2) = vw;
-      }
-      cur_bk = bk;
-    }
-    if (tid < kTileRows) {
-      int r = tid;
-      if (r < nrows) {
-        int ent = entries[e0 + r / G];
-        int64_t tl = ent >> 4;
-        int slot = ent & 15;
-        int h = g * G + r % G;
-        row_t[r] = (int)(q0 + tl);
-        row_dst[r] = (int)((tl * H_q + h) * k + slot);
-      } else {
-        row_t[r] = 0x7FFFFFFF;
-        row_dst[r] = -1;
-      }
-    }
-    __syncthreads();
-    for (int e = tid; e < kTileRows * (D / 2); e += kThreads) {
-      int r = e / (D / 2), c2 = e % (D / 2);
-      uint32_t w = 0;
-      if (r < nrows) {
-        int64_t t = row_t[r];
-        int h = g * G + r % G;
-        w = *reinterpret_cast<const uint32_t*>(q + ((size_t)t * H_q + h) * D + 2 * c2);
-      }
-      *reinterpret_cast<uint32_t*>(Qs + r * DP + 2 * c2) = w;
-    }
-    __syncthreads();
+  // this CTA's contiguous range of tiles
+  const int64_t total = tile_off[n_b];
+  const int64_t t_begin = total * blockIdx.x / gridDim.x;
+  const int64_t t_end = total * (blockIdx.x + 1) / gridDim.x;
 
-    // S = Q K^T (rows rg*8.., keys kg + 16 i)
-    const int rg = tid >> 4, kg = tid & 15;
-    {
-      float acc[8][8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[r][i] = 0.f;
-#pragma unroll 4
-      for (int c = 0; c < D; c += 2) {
-        float qa[8], qb[8], ka[8], kb[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          uint32_t w = *reinterpret_cast<const uint32_t*>(Qs + (rg * 8 + r) * DP + c);
-          qa[r] = bf16_lo(w);
-          qb[r] = bf16_hi(w);
+  if (warp == 0) {
+    // ---------------------------------------------------------- K / V loads
+    if (lane == 0 && t_begin < t_end) {
+      int64_t bk = find_bucket(tile_off, n_b, t_begin), prev = -1;
+      uint32_t epoch = 0;
+      bool ok = true;
+      for (int64_t tile = t_begin; tile < t_end && ok; ++tile) {
+        while (tile_off[bk + 1] <= tile) ++bk;
+        if (bk == prev) continue;
+        if (!mbar_wait(kv_empty, (epoch & 1) ^ 1, abort_flag, dg)) { ok = false; break; }
+        const int g = (int)(bk / nb);
+        const int32_t key0 = (int32_t)((bk % nb) * kBk);
+        mbar_arrive_expect_tx(kv_full, 2 * S::kKVBytes);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(smem + S::kKOff + c * kBk * 128, &tm_k, kv_full, c * 64, g, key0);
+          tma_load_3d(smem + S::kVOff + c * kBk * 128, &tm_v, kv_full, c * 64, g, key0);
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint32_t w = *reinterpret_cast<const uint32_t*>(Ks + (kg + 16 * i) * DP + c);
-          ka[i] = bf16_lo(w);
-          kb[i] = bf16_hi(w);
-        }
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[r][i] = fmaf(qa[r], ka[i], fmaf(qb[r], kb[i], acc[r][i]));
+        prev = bk;
+        ++epoch;
       }
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        int row = rg * 8 + r;
-        int64_t t = row_t[row];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          int64_t key = b * kBk + kg + 16 * i;
-          Ss[row * 129 + kg + 16 * i] = key <= t ? acc[r][i] * scale_log2 : -INFINITY;
-        }
-      }
+      if (!ok && epoch > 0) mbar_drain(kv_full, (epoch - 1) & 1);
     }
-    __syncthreads();
-    // softmax: two threads per row (64 keys each), base-2 domain
-    {
-      int row = tid >> 1, half = tid & 1;
-      float* s = Ss + row * 129 + half * 64;
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && t_begin < t_end) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBk);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      const uint32_t k_base = smem_u32(smem + S::kKOff), v_base = smem_u32(smem + S::kVOff);
+      const uint32_t q_base = smem_u32(smem + S::kQOff);
+      int64_t bk = find_bucket(tile_off, n_b, t_begin), prev = -1;
+      uint32_t epoch = 0;
+      long long i = 0;
+      bool ok = true, pending = false;
+      auto issue_o = [&](long long j, bool last) -> bool {
+        const int st = (int)(j & 1);
+        if (!mbar_wait(&p_full[st], (uint32_t)((j >> 1) & 1), abort_flag, dg)) return false;
+        tc_fence_after();
+        const uint32_t d_o = tmem_base + (uint32_t)(st * 256 + 128);
+#pragma unroll
+        for (int kk = 0; kk < kBk / 16; ++kk) {
+          const uint32_t a_p = tmem_base + (uint32_t)(st * 256 + kk * 8);
+          const uint64_t bd = desc_mnmajor_sw128(v_base + kk * 16 * 128, kBk * 128);
+          mma_bf16_ts(d_o, a_p, bd, idesc_o, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&o_full[st]);
+        if (last) mma_commit(kv_empty);
+        return true;
+      };
+      for (int64_t tile = t_begin; tile < t_end; ++tile, ++i) {
+        while (tile_off[bk + 1] <= tile) ++bk;
+        const bool fresh = bk != prev;
+        if (fresh && pending) {
+          if (!issue_o(i - 1, true)) { ok = false; break; }
+          pending = false;
+        }
+        if (fresh) {
+          if (!mbar_wait(kv_full, epoch & 1, abort_flag, dg)) { ok = false; break; }
+          ++epoch;
+          prev = bk;
+        }
+        const int st = (int)(i & 1);
+        const int qs = (int)(i % QS);
+        if (!mbar_wait(&t_empty[st], (uint32_t)(((i >> 1) & 1) ^ 1), abort_flag, dg)) { ok = false; break; }
+        if (!mbar_wait(&q_full[qs], (uint32_t)((i / QS) & 1), abort_flag, dg)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_s = tmem_base + (uint32_t)(st * 256);
+        const uint32_t qa = q_base + qs * S::kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int c = kk / 4, off = (kk % 4) * 32;
+          mma_bf16_ss(d_s, desc_kmajor_sw128(qa + c * kTileRows * 128 + off),
+                      desc_kmajor_sw128(k_base + c * kBk * 128 + off), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[st]);
+        mma_commit(&q_empty[qs]);
+        if (pending && !issue_o(i - 1, false)) { ok = false; break; }
+        pending = true;
+      }
+      if (ok && pending) issue_o(i - 1, true);
+      mma_commit(done_bar);
+      mbar_drain(done_bar, 0);
+    }
+  } else if (warp < 6) {
+    // ---------------------------------------------------------- Q producers
+    const int my = warp - 2;  // Q stage owned by this warp
+    unsigned char* qbuf = smem + S::kQOff + my * S::kQBytes;
+    int32_t* row_t = row_t_all + my * kTileRows;
+    int32_t* row_dst = row_dst_all + my * kTileRows;
+    int64_t bk = t_begin < t_end ? find_bucket(tile_off, n_b, t_begin) : 0;
+    long long i = 0;
+    for (int64_t tile = t_begin; tile < t_end; ++tile, ++i) {
+      while (tile_off[bk + 1] <= tile) ++bk;
+      if ((int)(i % QS) != my) continue;
+      int got = 0;
+      if (lane == 0) got = mbar_wait(&q_empty[my], (uint32_t)(((i / QS) & 1) ^ 1), abort_flag, dg);
+      if (!__shfl_sync(0xffffffffu, got, 0)) break;
+      const int g = (int)(bk / nb);
+      const int e0 = offsets[bk] + (int)(tile - tile_off[bk]) * qt;
+      const int e1 = min(e0 + qt, offsets[bk + 1]);
+      const int nrows = (e1 - e0) * G;
+      for (int r = lane; r < kTileRows; r += 32) {
+        if (r < nrows) {
+          const int ent = entries[e0 + r / G];
+          const int tl = ent >> 4, slot = ent & 15;
+          row_t[r] = (int)(q0 + tl);
+          row_dst[r] = (tl * k + slot) * H_q + g * G + r % G;
+        } else {
+          row_t[r] = 0x7FFFFFFF;
+          row_dst[r] = -1;
+        }
+      }
+      __syncwarp();
+      constexpr int P16 = D / 8;  // 16-byte pieces per row
+      for (int p = lane; p < kTileRows * P16; p += 32) {
+        const int r = p / P16, j16 = p % P16;
+        if (r >= nrows) break;  // rows are filled in order
+        const int c = j16 >> 3, j = j16 & 7;
+        const int64_t t = row_t[r];
+        const int h = g * G + r % G;
+        const uint16_t* src = q + ((size_t)t * H_q + h) * D + c * 64 + j * 8;
+        cp_async16(qbuf + c * kTileRows * 128 + r * 128 + ((j ^ (r & 7)) << 4), src);
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[my]);
+    }
+    cp_async_wait_all();
+  } else {
+    // ---------------------------------------------------------- softmax + epilogue
+    const int qq = warp & 3;
+    const int row = qq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    int64_t bk = t_begin < t_end ? find_bucket(tile_off, n_b, t_begin) : 0;
+    long long i = 0;
+    for (int64_t tile = t_begin; tile < t_end; ++tile, ++i) {
+      while (tile_off[bk + 1] <= tile) ++bk;
+      const int64_t b = bk % nb;
+      const int st = (int)(i & 1);
+      const uint32_t par = (uint32_t)((i >> 1) & 1);
+      const int qs = (int)(i % QS);
+      // q_full: acquire the producer's row metadata; s_full: scores are in TMEM
+      int got = 0;
+      if (lane == 0)
+        got = mbar_wait(&q_full[qs], (uint32_t)((i / QS) & 1), abort_flag, dg) &&
+              mbar_wait(&s_full[st], par, abort_flag, dg);
+      if (!__shfl_sync(0xffffffffu, got, 0)) break;
+      const int64_t t = row_t_all[qs * kTileRows + row];
+      const int dst = row_dst_all[qs * kTileRows + row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_empty[qs]);
+      tc_fence_after();
+      const uint32_t ts = tmem_base + lane_off + (uint32_t)(st * 256);
+      const int lim = (dst >= 0 && t / kBk == b) ? (int)(t - b * kBk) + 1 : kBk;
+      // pass 1: row max
       float m = -INFINITY;
-      for (int i = 0; i < 64; ++i) m = fmaxf(m, s[i]);
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(ts + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c * 32 + j < lim) m = fmaxf(m, __uint_as_float(r[j]));
+      }
+      const float mc = m * scale_log2;
+      // pass 2: P = exp2(s * c - m * c) in bf16 over the first 64 columns, row sum
       float l = 0.f;
-      for (int i = 0; i < 64; ++i) {
-        float p = ex2_approx(s[i] - m);
-        s[i] = p;
-        l += p;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32], pk[16];
+        tmem_ld32(ts + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          float p0 = c * 32 + j < lim ? ex2_approx(fmaf(__uint_as_float(r[j]), scale_log2, -mc)) : 0.f;
+          float p1 = c * 32 + j + 1 < lim ? ex2_approx(fmaf(__uint_as_float(r[j + 1]), scale_log2, -mc)) : 0.f;
+          l += p0 + p1;
+          pk[j >> 1] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(ts + c * 16, pk);
       }
-      l += __shfl_xor_sync(0xffffffffu, l, 1);
-      if (half == 0) {
-        row_m[row] = m;
-        row_l[row] = l;
-      }
-    }
-    __syncthreads();
-    // O = P V (rows rg*8.., column pairs cg*2 + 32 i)
-    {
-      constexpr int NP = D / 32;  // column pairs per thread
-      const int cg = tid & 15;
-      float acc[8][2 * NP];
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[st]);
+      // O epilogue
+      got = 0;
+      if (lane == 0) got = mbar_wait(&o_full[st], par, abort_flag, dg);
+      if (!__shfl_sync(0xffffffffu, got, 0)) break;
+      tc_fence_after();
+      const float inv = 1.f / l;
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(ts + 128 + c * 32, r);
+        tmem_ld_wait();
+        if (dst >= 0) {
+          uint4* o = reinterpret_cast<uint4*>(part_o + (size_t)dst * D + c * 32);
 #pragma unroll
-        for (int i = 0; i < 2 * NP; ++i) acc[r][i] = 0.f;
-#pragma unroll 4
-      for (int j = 0; j < kBk; ++j) {
-        float p[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) p[r] = Ss[(rg * 8 + r) * 129 + j];
-#pragma unroll
-        for (int i = 0; i < NP; ++i) {
-          uint32_t w = *reinterpret_cast<const uint32_t*>(Vs + j * DP + cg * 2 + 32 * i);
-          float va = bf16_lo(w), vb = bf16_hi(w);
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            acc[r][2 * i] = fmaf(p[r], va, acc[r][2 * i]);
-            acc[r][2 * i + 1] = fmaf(p[r], vb, acc[r][2 * i + 1]);
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+            o[v] = w;
           }
         }
       }
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        int row = rg * 8 + r;
-        int dst = row_dst[row];
-        if (dst < 0) continue;
-        float inv = 1.f / row_l[row];
-#pragma unroll
-        for (int i = 0; i < NP; ++i) {
-          uint32_t w = pack_bf16x2(acc[r][2 * i] * inv, acc[r][2 * i + 1] * inv);
-          *reinterpret_cast<uint32_t*>(part_o + (size_t)dst * D + cg * 2 + 32 * i) = w;
-        }
-        if (cg == 0) part_lse[dst] = (row_m[row] + __log2f(row_l[row])) * 0.69314718055994531f;
-      }
+      if (dst >= 0) part_lse[dst] = (mc + __log2f(l)) * 0.69314718055994531f;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&t_empty[st]);
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
 // ---------------------------------------------------------------------- merge
+// partials: part_o [rows, k, H_q, D] bf16, part_lse [rows, k, H_q]; one warp per
+// (query, head)
 template <int D>
 __global__ void attn_merge_kernel(const uint16_t* __restrict__ part_o,
                                   const float* __restrict__ part_lse,
@@ -304,24 +455,24 @@ __global__ void attn_merge_kernel(const uint16_t* __restrict__ part_o,
   int64_t n = (q1 - q0) * H_q;
   for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < n;
        w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-    int64_t tl = w / H_q;
-    int h = (int)(w % H_q);
-    int64_t t = q0 + tl;
+    const int64_t tl = w / H_q;
+    const int h = (int)(w % H_q);
+    const int64_t t = q0 + tl;
     const int32_t* id = ids + ((size_t)t * H_kv + h / G) * k;
-    const float* pl = part_lse + (size_t)w * k;
     const Diag none{nullptr, 0};
     float M = -INFINITY;
     for (int s = 0; s < k; ++s)
-      if (id_ok(id[s], t, none)) M = fmaxf(M, pl[s]);
+      if (id_ok(id[s], t, none)) M = fmaxf(M, part_lse[((size_t)tl * k + s) * H_q + h]);
     float acc[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
     float L = 0.f;
     for (int s = 0; s < k; ++s) {
       if (!id_ok(id[s], t, none)) continue;
-      float wgt = __expf(pl[s] - M);
+      const size_t pr = ((size_t)tl * k + s) * H_q + h;
+      const float wgt = __expf(part_lse[pr] - M);
       L += wgt;
-      const uint16_t* po = part_o + ((size_t)w * k + s) * D + lane * PER;
+      const uint16_t* po = part_o + pr * D + lane * PER;
       if (PER == 4) {
         uint2 u = *reinterpret_cast<const uint2*>(po);
         acc[0] = fmaf(wgt, bf16_lo(u.x), acc[0]);
@@ -334,7 +485,7 @@ __global__ void attn_merge_kernel(const uint16_t* __restrict__ part_o,
         acc[1] = fmaf(wgt, bf16_hi(u), acc[1]);
       }
     }
-    float inv = 1.f / L;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
     uint16_t* o = out + ((size_t)t * H_q + h) * D + lane * PER;
     if (PER == 4) {
       uint2 u;
@@ -348,9 +499,52 @@ __global__ void attn_merge_kernel(const uint16_t* __restrict__ part_o,
   }
 }
 
+// 3D bf16 tensor [N, H, D] viewed as (D, H, N); box {64, 1, 128}, 128B swizzle
+bool make_map_kv(CUtensorMap* m, const void* base, int64_t N, int H, int D) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess || qr != cudaDriverEntryPointSuccess)
+      return false;
+    fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)N};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kBk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
 template <int D>
-size_t tile_smem_bytes() {
-  return (size_t)(kTileRows + 2 * kBk) * (D + 2) * 2 + kTileRows * 129 * 4 + kTileRows * 16;
+cudaError_t launch_tiles(const void* q, const void* kk, const void* v, int64_t N, int64_t q0,
+                         int H_q, int H_kv, int k, float scale_log2, int64_t nb, const AttnWs& ws,
+                         int64_t n_b, const Diag& dg, cudaStream_t st) {
+  CUtensorMap tk, tv;
+  if (!make_map_kv(&tk, kk, N, H_kv, D) || !make_map_kv(&tv, v, N, H_kv, D))
+    return cudaErrorInvalidValue;
+  const int smem = AttnSmem<D>::kBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(attn_tile_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  attn_tile_tc_kernel<D><<<sm_count(), kAttnThreads, smem, st>>>(
+      tk, tv, (const uint16_t*)q, q0, H_q, H_kv, k, scale_log2, nb, ws.entries, ws.offsets,
+      ws.tile_off, n_b, ws.part_o, ws.part_lse, dg);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -400,21 +594,9 @@ cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* 
   bucket_fill_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, ws.offsets, ws.cursor,
                                            ws.entries);
   const float scale_log2 = scale * 1.4426950408889634f;
-  if (d == 128) {
-    size_t sm = tile_smem_bytes<128>();
-    cudaFuncSetAttribute(attn_tile_cc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)sm);
-    attn_tile_cc_kernel<128><<<152, kThreads, sm, st>>>(
-        (const uint16_t*)q, (const uint16_t*)kk, (const uint16_t*)v, N, q0, H_q, H_kv, k,
-        scale_log2, nb, ws.entries, ws.offsets, ws.tile_off, n_b, ws.part_o, ws.part_lse);
-  } else {
-    size_t sm = tile_smem_bytes<64>();
-    cudaFuncSetAttribute(attn_tile_cc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)sm);
-    attn_tile_cc_kernel<64><<<152, kThreads, sm, st>>>(
-        (const uint16_t*)q, (const uint16_t*)kk, (const uint16_t*)v, N, q0, H_q, H_kv, k,
-        scale_log2, nb, ws.entries, ws.offsets, ws.tile_off, n_b, ws.part_o, ws.part_lse);
-  }
+  e = d == 128 ? launch_tiles<128>(q, kk, v, N, q0, H_q, H_kv, k, scale_log2, nb, ws, n_b, dg, st)
+               : launch_tiles<64>(q, kk, v, N, q0, H_q, H_kv, k, scale_log2, nb, ws, n_b, dg, st);
+  if (e != cudaSuccess) return e;
   int64_t nw = (q1 - q0) * H_q;
   unsigned mg = (unsigned)std::min<int64_t>((nw * 32 + 255) / 256, 152 * 64);
   if (d == 128)
