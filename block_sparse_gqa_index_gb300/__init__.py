@@ -56,12 +56,16 @@ _decode = _sig("msa_decode", [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I
 _get_error = _sig("msa_get_error", [_P])
 _set_wait = _sig("msa_set_wait_limit", [_I64], _I64)
 _launch_count = _sig("msa_launch_count", [], _I64)
+_index_dec_noalloc = _sig("msa_index_select_decode_noalloc", [_P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                                              _I, _P, _P])
+_noalloc_max = _sig("msa_index_select_decode_noalloc_max_scores", [], _I64)
 
 EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes",
            "msa_index_select", "msa_topk_blocks", "msa_sparse_attn_workspace_bytes",
            "msa_sparse_attn", "msa_index_select_decode_workspace_bytes",
            "msa_index_select_decode", "msa_decode_workspace_bytes", "msa_decode",
-           "msa_get_error", "msa_set_wait_limit", "msa_launch_count"]
+           "msa_get_error", "msa_set_wait_limit", "msa_launch_count",
+           "msa_index_select_decode_noalloc", "msa_index_select_decode_noalloc_max_scores"]
 
 
 class MSAError(RuntimeError):
@@ -209,6 +213,35 @@ def msa_index_select_decode(q_idx: torch.Tensor, k_idx_pages: torch.Tensor,
                       _ptr(block_scores), ws_ptr, ws_n, _stream(q_idx)),
            "msa_index_select_decode")
     return block_ids
+
+
+def msa_index_select_decode_noalloc(q_idx: torch.Tensor, k_idx_pages: torch.Tensor,
+                                    page_table: torch.Tensor, seq_lens: torch.Tensor,
+                                    Bk: int = 128, k: int = 16,
+                                    block_ids: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Decode index branch that allocates nothing on the device: the block
+    scores go to the library's fixed scratch array (see include/msa.h). Pass
+    `block_ids` to avoid the one torch allocation made here otherwise."""
+    B, n_g, d_idx = q_idx.shape
+    max_pages = page_table.shape[1]
+    _req(q_idx, "q_idx", torch.bfloat16)
+    _req(k_idx_pages, "k_idx_pages", torch.bfloat16)
+    if k_idx_pages.shape[1:] != (Bk, d_idx):
+        raise ValueError("k_idx_pages must be [P, Bk, d_idx]")
+    _req(page_table, "page_table", torch.int32, (B, max_pages))
+    _req(seq_lens, "seq_lens", torch.int32, (B,))
+    if block_ids is None:
+        block_ids = torch.empty((B, n_g, k), dtype=torch.int32, device=q_idx.device)
+    _req(block_ids, "block_ids", torch.int32, (B, n_g, k))
+    _check(_index_dec_noalloc(q_idx.data_ptr(), k_idx_pages.data_ptr(), page_table.data_ptr(),
+                              seq_lens.data_ptr(), B, max_pages, n_g, d_idx, Bk, k,
+                              block_ids.data_ptr(), _stream(q_idx)),
+           "msa_index_select_decode_noalloc")
+    return block_ids
+
+
+def msa_index_select_decode_noalloc_max_scores() -> int:
+    return _noalloc_max()
 
 
 def msa_index_select_decode_workspace_bytes(B: int, max_pages: int, n_groups: int) -> int:

@@ -47,6 +47,12 @@ int* err_ptr() {
 
 msa::Diag diag() { return msa::Diag{err_ptr(), g_wait_limit}; }
 
+}  // namespace
+
+msa::Diag msa::current_diag() { return diag(); }
+
+namespace {
+
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }

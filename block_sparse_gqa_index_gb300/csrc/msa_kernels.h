@@ -12,6 +12,10 @@ namespace msa {
 // Counts every kernel launch / device memset enqueued by the library.
 void note_launches(int n);
 
+// Error word and wait limit of the current device, for entry points defined
+// outside msa_abi.cu.
+Diag current_diag();
+
 // Index branch, prefill (msa_index.cu).
 cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_g,
                                 int d_idx, int k, int32_t* block_ids, float* block_scores,

@@ -156,6 +156,29 @@ int msa_decode(const void* q, const void* k_pages, const void* v_pages, int kv_d
                int H_q, int H_kv, int d, int Bk, int k, float scale, void* out, float* lse,
                void* workspace, size_t workspace_bytes, void* stream);
 
+/* Decode index branch without any allocation (no counterpart in the pages):
+ * same inputs, output and rules as msa_index_select_decode, but the per-page
+ * block scores go to a fixed 4 MiB scratch array compiled into the library
+ * instead of a caller workspace. For callers that may not allocate device
+ * memory while running (engines that reserve all memory at start-up, code
+ * where an allocation could stall or synchronise other device work).
+ *   - B * n_groups * max_pages must not exceed
+ *     msa_index_select_decode_noalloc_max_scores() (1 << 20); larger requests
+ *     return MSA_ERR_WORKSPACE and enqueue nothing.
+ *   - The first call on a device looks up the array's device address (a
+ *     cudaGetSymbolAddress, no allocation); make that first call before any
+ *     stream capture.
+ *   - All calls share the array: calls whose executions overlap on the GPU
+ *     (several streams or host threads) race and must be serialised.
+ *   - Calls no cudaMalloc / cudaFree and no allocating library routine. */
+int msa_index_select_decode_noalloc(const void* q_idx, const void* k_idx_pages,
+                                    const int32_t* page_table, const int32_t* seq_lens, int B,
+                                    int max_pages, int n_groups, int d_idx, int Bk, int k,
+                                    int32_t* block_ids, void* stream);
+
+/* Capacity of that scratch array, in block scores. */
+int64_t msa_index_select_decode_noalloc_max_scores(void);
+
 /* ------------------------------------------------------------ diagnostics -- */
 
 /* Synchronises `stream`, then returns and clears the device error word:
