@@ -144,7 +144,13 @@ struct AttnSmem {
   static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
 };
 
-constexpr int kAttnThreads = 320;
+constexpr int kAttnThreads = 448;  // 14 warps
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 __device__ __forceinline__ int64_t find_bucket(const int32_t* __restrict__ tile_off, int64_t n_b,
                                                int64_t tile) {
@@ -193,7 +199,7 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     mbar_init(kv_empty, 1);
     for (int s = 0; s < QS; ++s) {
       mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1 + 4);  // S-MMA commit + the 4 softmax warps (row metadata read)
+      mbar_init(&q_empty[s], 1 + 4);  // S-MMA commit + the owning softmax group's 4 warps
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
@@ -217,10 +223,11 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int64_t total = tile_off[n_b];
   const int64_t t_begin = total * blockIdx.x / gridDim.x;
   const int64_t t_end = total * (blockIdx.x + 1) / gridDim.x;
+  const long long n_local = t_end - t_begin;
 
   if (warp == 0) {
     // ---------------------------------------------------------- K / V loads
-    if (lane == 0 && t_begin < t_end) {
+    if (lane == 0 && n_local > 0) {
       int64_t bk = find_bucket(tile_off, n_b, t_begin), prev = -1;
       uint32_t epoch = 0;
       bool ok = true;
@@ -242,61 +249,76 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && t_begin < t_end) {
+    // Event loop: issue S(next) when its TMEM stage, Q stage and K/V are ready,
+    // and P.V(pending) when its softmax has written P, whichever comes first.
+    if (lane == 0 && n_local > 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBk);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
       const uint32_t k_base = smem_u32(smem + S::kKOff), v_base = smem_u32(smem + S::kVOff);
       const uint32_t q_base = smem_u32(smem + S::kQOff);
-      int64_t bk = find_bucket(tile_off, n_b, t_begin), prev = -1;
+      int64_t bk_s = find_bucket(tile_off, n_b, t_begin), bk_o = bk_s, cur = -1;
       uint32_t epoch = 0;
-      long long i = 0;
-      bool ok = true, pending = false;
-      auto issue_o = [&](long long j, bool last) -> bool {
-        const int st = (int)(j & 1);
-        if (!mbar_wait(&p_full[st], (uint32_t)((j >> 1) & 1), abort_flag, dg)) return false;
-        tc_fence_after();
-        const uint32_t d_o = tmem_base + (uint32_t)(st * 256 + 128);
+      long long si = 0, oi = 0, idle = 0;
+      while (oi < n_local) {
+        bool prog = false;
+        if (si < n_local) {
+          const int64_t tile = t_begin + si;
+          while (tile_off[bk_s + 1] <= tile) ++bk_s;
+          bool ready = true;
+          if (bk_s != cur) {  // new K/V: every P.V of the old block must be issued first
+            ready = oi == si && mbar_try_wait(kv_full, epoch & 1);
+            if (ready) { cur = bk_s; ++epoch; }
+          }
+          const int st = (int)(si & 1);
+          const int qs = (int)(si % QS);
+          if (ready && mbar_try_wait(&t_empty[st], (uint32_t)(((si >> 1) & 1) ^ 1)) &&
+              mbar_try_wait(&q_full[qs], (uint32_t)((si / QS) & 1))) {
+            tc_fence_after();
+            const uint32_t d_s = tmem_base + (uint32_t)(st * 256);
+            const uint32_t qa = q_base + qs * S::kQBytes;
 #pragma unroll
-        for (int kk = 0; kk < kBk / 16; ++kk) {
-          const uint32_t a_p = tmem_base + (uint32_t)(st * 256 + kk * 8);
-          const uint64_t bd = desc_mnmajor_sw128(v_base + kk * 16 * 128, kBk * 128);
-          mma_bf16_ts(d_o, a_p, bd, idesc_o, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const int c = kk / 4, off = (kk % 4) * 32;
+              mma_bf16_ss(d_s, desc_kmajor_sw128(qa + c * kTileRows * 128 + off),
+                          desc_kmajor_sw128(k_base + c * kBk * 128 + off), idesc_s,
+                          kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[st]);
+            mma_commit(&q_empty[qs]);
+            ++si;
+            prog = true;
+          }
         }
-        mma_commit(&o_full[st]);
-        if (last) mma_commit(kv_empty);
-        return true;
-      };
-      for (int64_t tile = t_begin; tile < t_end; ++tile, ++i) {
-        while (tile_off[bk + 1] <= tile) ++bk;
-        const bool fresh = bk != prev;
-        if (fresh && pending) {
-          if (!issue_o(i - 1, true)) { ok = false; break; }
-          pending = false;
-        }
-        if (fresh) {
-          if (!mbar_wait(kv_full, epoch & 1, abort_flag, dg)) { ok = false; break; }
-          ++epoch;
-          prev = bk;
-        }
-        const int st = (int)(i & 1);
-        const int qs = (int)(i % QS);
-        if (!mbar_wait(&t_empty[st], (uint32_t)(((i >> 1) & 1) ^ 1), abort_flag, dg)) { ok = false; break; }
-        if (!mbar_wait(&q_full[qs], (uint32_t)((i / QS) & 1), abort_flag, dg)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t d_s = tmem_base + (uint32_t)(st * 256);
-        const uint32_t qa = q_base + qs * S::kQBytes;
+        if (oi < si) {
+          const int st = (int)(oi & 1);
+          if (mbar_try_wait(&p_full[st], (uint32_t)((oi >> 1) & 1))) {
+            tc_fence_after();
+            const uint32_t d_o = tmem_base + (uint32_t)(st * 256 + 128);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int c = kk / 4, off = (kk % 4) * 32;
-          mma_bf16_ss(d_s, desc_kmajor_sw128(qa + c * kTileRows * 128 + off),
-                      desc_kmajor_sw128(k_base + c * kBk * 128 + off), idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kBk / 16; ++kk) {
+              const uint32_t a_p = tmem_base + (uint32_t)(st * 256 + kk * 8);
+              const uint64_t bd = desc_mnmajor_sw128(v_base + kk * 16 * 128, kBk * 128);
+              mma_bf16_ts(d_o, a_p, bd, idesc_o, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&o_full[st]);
+            const int64_t tile = t_begin + oi;
+            while (tile_off[bk_o + 1] <= tile) ++bk_o;
+            if (oi + 1 == n_local || tile_off[bk_o + 1] <= tile + 1) mma_commit(kv_empty);
+            ++oi;
+            prog = true;
+          }
         }
-        mma_commit(&s_full[st]);
-        mma_commit(&q_empty[qs]);
-        if (pending && !issue_o(i - 1, false)) { ok = false; break; }
-        pending = true;
+        if (prog) {
+          idle = 0;
+        } else {
+          if (*abort_flag) break;
+          if (++idle > dg.wait_limit) {
+            *abort_flag = 1;
+            report(dg, kStatusTimeout);
+            break;
+          }
+        }
       }
-      if (ok && pending) issue_o(i - 1, true);
       mma_commit(done_bar);
       mbar_drain(done_bar, 0);
     }
@@ -306,7 +328,7 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     unsigned char* qbuf = smem + S::kQOff + my * S::kQBytes;
     int32_t* row_t = row_t_all + my * kTileRows;
     int32_t* row_dst = row_dst_all + my * kTileRows;
-    int64_t bk = t_begin < t_end ? find_bucket(tile_off, n_b, t_begin) : 0;
+    int64_t bk = n_local > 0 ? find_bucket(tile_off, n_b, t_begin) : 0;
     long long i = 0;
     for (int64_t tile = t_begin; tile < t_end; ++tile, ++i) {
       while (tile_off[bk + 1] <= tile) ++bk;
@@ -348,15 +370,19 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     cp_async_wait_all();
   } else {
     // ---------------------------------------------------------- softmax + epilogue
+    // two groups of 4 warps; group wg takes the tiles i with i % 2 == wg, which
+    // use TMEM stage wg, so one group's softmax overlaps the other's epilogue
+    const int wg = (warp - 6) >> 2;
     const int qq = warp & 3;
     const int row = qq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
-    int64_t bk = t_begin < t_end ? find_bucket(tile_off, n_b, t_begin) : 0;
-    long long i = 0;
-    for (int64_t tile = t_begin; tile < t_end; ++tile, ++i) {
+    const int st = wg;
+    const uint32_t ts = tmem_base + lane_off + (uint32_t)(st * 256);
+    int64_t bk = n_local > 0 ? find_bucket(tile_off, n_b, t_begin) : 0;
+    for (long long i = wg; i < n_local; i += 2) {
+      const int64_t tile = t_begin + i;
       while (tile_off[bk + 1] <= tile) ++bk;
       const int64_t b = bk % nb;
-      const int st = (int)(i & 1);
       const uint32_t par = (uint32_t)((i >> 1) & 1);
       const int qs = (int)(i % QS);
       // q_full: acquire the producer's row metadata; s_full: scores are in TMEM
@@ -370,22 +396,31 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_empty[qs]);
       tc_fence_after();
-      const uint32_t ts = tmem_base + lane_off + (uint32_t)(st * 256);
       const int lim = (dst >= 0 && t / kBk == b) ? (int)(t - b * kBk) + 1 : kBk;
       // pass 1: row max
       float m = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(ts + c * 32, r);
+      for (int c = 0; c < 4; c += 2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(ts + c * 32, r0);
+        tmem_ld32(ts + c * 32 + 32, r1);
         tmem_ld_wait();
+        if (lim >= kBk) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (c * 32 + j < lim) m = fmaxf(m, __uint_as_float(r[j]));
+          for (int j = 0; j < 32; j += 2)
+            m = fmax3(m, fmaxf(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1])),
+                      fmaxf(__uint_as_float(r1[j]), __uint_as_float(r1[j + 1])));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (c * 32 + j < lim) m = fmaxf(m, __uint_as_float(r0[j]));
+            if (c * 32 + 32 + j < lim) m = fmaxf(m, __uint_as_float(r1[j]));
+          }
+        }
       }
       const float mc = m * scale_log2;
       // pass 2: P = exp2(s * c - m * c) in bf16 over the first 64 columns, row sum
-      float l = 0.f;
+      float l0 = 0.f, l1 = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32], pk[16];
@@ -395,11 +430,13 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         for (int j = 0; j < 32; j += 2) {
           float p0 = c * 32 + j < lim ? ex2_approx(fmaf(__uint_as_float(r[j]), scale_log2, -mc)) : 0.f;
           float p1 = c * 32 + j + 1 < lim ? ex2_approx(fmaf(__uint_as_float(r[j + 1]), scale_log2, -mc)) : 0.f;
-          l += p0 + p1;
+          l0 += p0;
+          l1 += p1;
           pk[j >> 1] = pack_bf16x2(p0, p1);
         }
         tmem_st16(ts + c * 16, pk);
       }
+      const float l = l0 + l1;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -424,7 +461,7 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
             w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
             w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
-            o[v] = w;
+            __stcs(o + v, w);
           }
         }
       }
@@ -442,45 +479,57 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
 // ---------------------------------------------------------------------- merge
 // partials: part_o [rows, k, H_q, D] bf16, part_lse [rows, k, H_q]; one warp per
-// (query, head)
+// (query, head). Lane s holds slot s's LSE; the max and the weights come from
+// warp shuffles, and the k slot loads of the output sum are all issued before
+// any is used (the slot loop is unrolled), so each warp keeps up to k loads in
+// flight.
 template <int D>
-__global__ void attn_merge_kernel(const uint16_t* __restrict__ part_o,
-                                  const float* __restrict__ part_lse,
-                                  const int32_t* __restrict__ ids, int64_t q0, int64_t q1,
-                                  int H_q, int H_kv, int k, uint16_t* __restrict__ out,
-                                  float* __restrict__ lse) {
+__global__ void __launch_bounds__(256)
+attn_merge_kernel(const uint16_t* __restrict__ part_o, const float* __restrict__ part_lse,
+                  const int32_t* __restrict__ ids, int64_t q0, int64_t q1, int H_q, int H_kv,
+                  int k, uint16_t* __restrict__ out, float* __restrict__ lse) {
   constexpr int PER = D / 32;  // elements per lane
   const int lane = threadIdx.x & 31;
   const int G = H_q / H_kv;
-  int64_t n = (q1 - q0) * H_q;
+  const int64_t n = (q1 - q0) * H_q;
+  const Diag none{nullptr, 0};
   for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < n;
        w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
     const int64_t tl = w / H_q;
     const int h = (int)(w % H_q);
     const int64_t t = q0 + tl;
-    const int32_t* id = ids + ((size_t)t * H_kv + h / G) * k;
-    const Diag none{nullptr, 0};
-    float M = -INFINITY;
-    for (int s = 0; s < k; ++s)
-      if (id_ok(id[s], t, none)) M = fmaxf(M, part_lse[((size_t)tl * k + s) * H_q + h]);
+    bool valid = false;
+    float ls = -INFINITY;
+    if (lane < k) {
+      valid = id_ok(ids[((size_t)t * H_kv + h / G) * k + lane], t, none);
+      if (valid) ls = part_lse[((size_t)tl * k + lane) * H_q + h];
+    }
+    float M = ls;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float wl = valid ? __expf(ls - M) : 0.f;
+    float L = wl;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
     float acc[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    float L = 0.f;
-    for (int s = 0; s < k; ++s) {
-      if (!id_ok(id[s], t, none)) continue;
-      const size_t pr = ((size_t)tl * k + s) * H_q + h;
-      const float wgt = __expf(part_lse[pr] - M);
-      L += wgt;
-      const uint16_t* po = part_o + pr * D + lane * PER;
+    const uint16_t* base = part_o + ((size_t)tl * k * H_q + h) * D + lane * PER;
+    const size_t slot_stride = (size_t)H_q * D;
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+      if (s >= k) break;
+      const float wgt = __shfl_sync(0xffffffffu, wl, s);
+      if (wgt == 0.f) continue;  // invalid or padded slot
+      const uint16_t* po = base + s * slot_stride;
       if (PER == 4) {
-        uint2 u = *reinterpret_cast<const uint2*>(po);
+        uint2 u = __ldcs(reinterpret_cast<const uint2*>(po));
         acc[0] = fmaf(wgt, bf16_lo(u.x), acc[0]);
         acc[1] = fmaf(wgt, bf16_hi(u.x), acc[1]);
         acc[2] = fmaf(wgt, bf16_lo(u.y), acc[2]);
         acc[3] = fmaf(wgt, bf16_hi(u.y), acc[3]);
       } else {
-        uint32_t u = *reinterpret_cast<const uint32_t*>(po);
+        uint32_t u = __ldcs(reinterpret_cast<const unsigned int*>(po));
         acc[0] = fmaf(wgt, bf16_lo(u), acc[0]);
         acc[1] = fmaf(wgt, bf16_hi(u), acc[1]);
       }
