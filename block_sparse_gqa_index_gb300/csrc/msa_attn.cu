@@ -266,13 +266,13 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           while (tile_off[bk_s + 1] <= tile) ++bk_s;
           bool ready = true;
           if (bk_s != cur) {  // new K/V: every P.V of the old block must be issued first
-            ready = oi == si && mbar_try_wait(kv_full, epoch & 1);
+            ready = oi == si && mbar_test(kv_full, epoch & 1);
             if (ready) { cur = bk_s; ++epoch; }
           }
           const int st = (int)(si & 1);
           const int qs = (int)(si % QS);
-          if (ready && mbar_try_wait(&t_empty[st], (uint32_t)(((si >> 1) & 1) ^ 1)) &&
-              mbar_try_wait(&q_full[qs], (uint32_t)((si / QS) & 1))) {
+          if (ready && mbar_test(&t_empty[st], (uint32_t)(((si >> 1) & 1) ^ 1)) &&
+              mbar_test(&q_full[qs], (uint32_t)((si / QS) & 1))) {
             tc_fence_after();
             const uint32_t d_s = tmem_base + (uint32_t)(st * 256);
             const uint32_t qa = q_base + qs * S::kQBytes;
@@ -291,7 +291,7 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         if (oi < si) {
           const int st = (int)(oi & 1);
-          if (mbar_try_wait(&p_full[st], (uint32_t)((oi >> 1) & 1))) {
+          if (mbar_test(&p_full[st], (uint32_t)((oi >> 1) & 1))) {
             tc_fence_after();
             const uint32_t d_o = tmem_base + (uint32_t)(st * 256 + 128);
 #pragma unroll

@@ -38,6 +38,19 @@ __device__ __forceinline__ uint64_t shfl64(uint64_t v, int src) {
   return ((uint64_t)hi << 32) | lo;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// score of a ranking key (inverse of ord_f32 on the upper half)
+__device__ __forceinline__ float key_value(uint64_t key) {
+  uint32_t o = (uint32_t)(key >> 32);
+  uint32_t b = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+  return __uint_as_float(b);
+}
+
 // bitonic sort of one key per lane, descending (lane 0 = largest)
 __device__ __forceinline__ uint64_t sort32_desc(uint64_t a, int lane) {
 #pragma unroll
@@ -92,6 +105,25 @@ __device__ __forceinline__ int sort32_asc(int a, int lane) {
   return a;
 }
 
+// bitonic sort of one float per lane, descending
+__device__ __forceinline__ float sort32_desc_f(float a, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      float p = __shfl_xor_sync(0xffffffffu, a, stride);
+      bool up = (lane & size) == 0;
+      bool lower = (lane & stride) == 0;
+      a = (lower == up) ? fmaxf(a, p) : fminf(a, p);
+    }
+  return a;
+}
+
+// key of the j-th value held by a lane in chunk c0 (see the load pattern)
+__device__ __forceinline__ int64_t elem_block(int64_t c0, int lane, int j) {
+  return c0 + (j >> 2) * 128 + lane * 4 + (j & 3);
+}
+
 __global__ void __launch_bounds__(kWarps * 32)
 topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, int Bk, int k,
             int64_t q_offset, const int32_t* __restrict__ seq_lens, int32_t* __restrict__ ids,
@@ -118,16 +150,22 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
       continue;
     }
     const float* row = S + r * nb;
-    uint64_t best = 0;  // lane i < kfar: i-th best key so far (descending)
+    uint64_t best = 0;           // lane i < kfar: i-th best key so far (descending), else 0
+    float best_min = -INFINITY;  // value of the kfar-th best so far (-inf before any chunk)
     for (int64_t c0 = 0; c0 < ncand; c0 += kChunk) {
       float v[32];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        int64_t b = c0 + i * 128 + lane * 4;
+        const int64_t b = c0 + i * 128 + lane * 4;
         float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         if (b < ncand) {
           if (vec) {
-            x = __ldg(reinterpret_cast<const float4*>(row + b));
+            x = __ldcs(reinterpret_cast<const float4*>(row + b));
+            if (b + 3 >= ncand) {  // ragged end: mask the blocks past the candidates
+              if (b + 1 >= ncand) x.y = -INFINITY;
+              if (b + 2 >= ncand) x.z = -INFINITY;
+              x.w = -INFINITY;
+            }
           } else {
             x.x = row[b];
             if (b + 1 < ncand) x.y = row[b + 1];
@@ -140,30 +178,20 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
         v[4 * i + 2] = x.z;
         v[4 * i + 3] = x.w;
       }
-      // 1. lane max key (0 if the lane holds no candidate)
-      uint64_t lmax = 0;
+      // 1. lane max, 2. threshold: the kfar-th largest lane max (>= kfar values
+      //    reach it) or the worst value kept so far, whichever is larger
+      float lmax = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        int64_t b = c0 + (j >> 2) * 128 + lane * 4 + (j & 3);
-        if (b < ncand) {
-          uint64_t key = rank_key(v[j], (uint32_t)b);
-          lmax = key > lmax ? key : lmax;
-        }
-      }
-      // 2. threshold
-      uint64_t srt = sort32_desc(lmax, lane);
-      uint64_t tau = shfl64(srt, kfar - 1);
-      uint64_t list_min = shfl64(best, kfar - 1);
-      tau = tau > list_min ? tau : list_min;
-      // 3. survivors
-      int cnt = 0;
+      for (int j = 0; j < 32; j += 2) lmax = fmax3(lmax, v[j], v[j + 1]);
+      const float srt = sort32_desc_f(lmax, lane);
+      float tau = __shfl_sync(0xffffffffu, srt, kfar - 1);
+      tau = fmaxf(tau, best_min);
+      // 3. survivors (>= tau; ties at tau are kept and settled by the keys)
+      uint32_t mask = 0;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        int64_t b = c0 + (j >> 2) * 128 + lane * 4 + (j & 3);
-        if (b < ncand && rank_key(v[j], (uint32_t)b) >= tau) ++cnt;
-      }
-      const bool keep_old = lane < kfar && best != 0 && best >= tau;
-      cnt += keep_old ? 1 : 0;
+      for (int j = 0; j < 32; ++j) mask |= (v[j] >= tau && v[j] != -INFINITY) ? (1u << j) : 0u;
+      const bool keep_old = lane < kfar && best != 0 && key_value(best) >= tau;
+      const int cnt = __popc(mask) + (keep_old ? 1 : 0);
       int incl = cnt;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -174,33 +202,36 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
       if (total <= kCap) {
         int p = incl - cnt;
         if (keep_old) buf[wid][p++] = best;
+        while (mask) {
+          const int j = __ffs(mask) - 1;
+          mask &= mask - 1;
+          float vj = v[0];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          int64_t b = c0 + (j >> 2) * 128 + lane * 4 + (j & 3);
-          if (b < ncand) {
-            uint64_t key = rank_key(v[j], (uint32_t)b);
-            if (key >= tau) buf[wid][p++] = key;
-          }
+          for (int q = 1; q < 32; ++q)
+            if (q == j) vj = v[q];
+          buf[wid][p++] = rank_key(vj, (uint32_t)elem_block(c0, lane, j));
         }
         __syncwarp();
         uint64_t a0 = lane < total ? buf[wid][lane] : 0;
-        uint64_t a1 = lane + 32 < total ? buf[wid][lane + 32] : 0;
+        if (total <= 32) {
+          a0 = sort32_desc(a0, lane);
+        } else {
+          uint64_t a1 = lane + 32 < total ? buf[wid][lane + 32] : 0;
+          sort64_desc(a0, a1, lane);
+        }
         __syncwarp();
-        sort64_desc(a0, a1, lane);
         best = lane < kfar ? a0 : 0;
       } else {
-        // rare: too many survivors; extract the k-1 best one by one
+        // rare: too many survivors (heavy ties); extract the k-1 best one by one
         uint64_t nb_best = 0, prev = ~0ull;
         const uint64_t old = lane < kfar ? best : 0;
         for (int round = 0; round < kfar; ++round) {
           uint64_t m = old < prev ? old : 0;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            int64_t b = c0 + (j >> 2) * 128 + lane * 4 + (j & 3);
-            if (b < ncand) {
-              uint64_t key = rank_key(v[j], (uint32_t)b);
-              if (key < prev && key > m) m = key;
-            }
+            if (!((mask >> j) & 1u)) continue;
+            uint64_t key = rank_key(v[j], (uint32_t)elem_block(c0, lane, j));
+            if (key < prev && key > m) m = key;
           }
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) {
@@ -212,6 +243,7 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
         }
         best = nb_best;
       }
+      best_min = key_value(shfl64(best, kfar - 1));
     }
     int id = lane < kfar ? key_id(best) : (lane == kfar ? (int)loc : 0x7FFFFFFF);
     id = sort32_asc(id, lane);
