@@ -411,6 +411,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=15.0)
+    ap.add_argument("--only", choices=["decode", "topk"], default=None,
+                    help="time only this path and print its numbers (for profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -426,6 +428,17 @@ def main():
     import synth
 
     peaks, peak_src = load_peaks()
+    if args.only == "decode":
+        wd = synth.make("decode")
+        for fp8 in (False, True):
+            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, args.warmup)
+            torch.cuda.empty_cache()
+            print(json.dumps({"only": "decode", "fp8": fp8, "index_ms": i_ms, "attention_ms": a_ms}))
+        return
+    if args.only == "topk":
+        t_ms, t_bytes = time_topk(msa, synth.make("128k"), args.steps, args.warmup)
+        print(json.dumps({"only": "topk", "ms": t_ms, "gbs": t_bytes / (t_ms * 1e-3) / 1e9}))
+        return
     w = synth.make(args.workload)
     clocks = {}
     P, ms, idx_ms, att_ms, launches = time_prefill(msa, w, args.steps, args.warmup, world,

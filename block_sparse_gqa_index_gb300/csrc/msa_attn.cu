@@ -329,10 +329,27 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     int32_t* row_t = row_t_all + my * kTileRows;
     int32_t* row_dst = row_dst_all + my * kTileRows;
     int64_t bk = n_local > 0 ? find_bucket(tile_off, n_b, t_begin) : 0;
+    int64_t bk_pf = bk;  // bucket cursor of the tile being prefetched
+    // L2 prefetch of one tile's query rows (each query's G head rows are one
+    // contiguous G * D * 2-byte run): the gather of that tile, QS tiles later,
+    // then reads from L2 instead of waiting on DRAM with only QS stages in flight
+    auto prefetch_tile = [&](int64_t tile) {
+      if (tile >= t_end) return;
+      while (tile_off[bk_pf + 1] <= tile) ++bk_pf;
+      const int gp = (int)(bk_pf / nb);
+      const int p0 = offsets[bk_pf] + (int)(tile - tile_off[bk_pf]) * qt;
+      const int p1 = min(p0 + qt, offsets[bk_pf + 1]);
+      for (int e = p0 + lane; e < p1; e += 32) {
+        const int64_t t = q0 + (entries[e] >> 4);
+        prefetch_l2_bulk(q + ((size_t)t * H_q + gp * G) * D, (uint32_t)(G * D * 2));
+      }
+    };
+    if (my < n_local) prefetch_tile(t_begin + my);
     long long i = 0;
     for (int64_t tile = t_begin; tile < t_end; ++tile, ++i) {
       while (tile_off[bk + 1] <= tile) ++bk;
       if ((int)(i % QS) != my) continue;
+      prefetch_tile(tile + QS);  // this warp's next tile
       int got = 0;
       if (lane == 0) got = mbar_wait(&q_empty[my], (uint32_t)(((i / QS) & 1) ^ 1), abort_flag, dg);
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
@@ -478,73 +495,87 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 }
 
 // ---------------------------------------------------------------------- merge
-// partials: part_o [rows, k, H_q, D] bf16, part_lse [rows, k, H_q]; one warp per
-// (query, head). Lane s holds slot s's LSE; the max and the weights come from
-// warp shuffles, and the k slot loads of the output sum are all issued before
-// any is used (the slot loop is unrolled), so each warp keeps up to k loads in
-// flight.
+// partials: part_o [rows, k, H_q, D] bf16, part_lse [rows, k, H_q]. Each half
+// warp merges one (query, head): lane s < k holds slot s's LSE, max and sum come
+// from shuffles within the half, and the k slot loads (16 bytes per lane for
+// D = 128) are all issued before they are summed. The two halves take adjacent
+// heads, so each slot read is one contiguous 2 * D * 2-byte run.
 template <int D>
 __global__ void __launch_bounds__(256)
 attn_merge_kernel(const uint16_t* __restrict__ part_o, const float* __restrict__ part_lse,
                   const int32_t* __restrict__ ids, int64_t q0, int64_t q1, int H_q, int H_kv,
                   int k, uint16_t* __restrict__ out, float* __restrict__ lse) {
-  constexpr int PER = D / 32;  // elements per lane
+  constexpr int PER = D / 16;  // elements per lane (8 or 4)
   const int lane = threadIdx.x & 31;
+  const int hl = lane & 15;          // lane within the half warp
   const int G = H_q / H_kv;
   const int64_t n = (q1 - q0) * H_q;
   const Diag none{nullptr, 0};
-  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < n;
-       w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-    const int64_t tl = w / H_q;
-    const int h = (int)(w % H_q);
+  const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; 2 * w < n; w += warps) {
+    const int64_t task = 2 * w + (lane >> 4);
+    const bool active = task < n;
+    const int64_t tk = active ? task : n - 1;
+    const int64_t tl = tk / H_q;
+    const int h = (int)(tk % H_q);
     const int64_t t = q0 + tl;
     bool valid = false;
     float ls = -INFINITY;
-    if (lane < k) {
-      valid = id_ok(ids[((size_t)t * H_kv + h / G) * k + lane], t, none);
-      if (valid) ls = part_lse[((size_t)tl * k + lane) * H_q + h];
+    if (hl < k) {
+      valid = id_ok(ids[((size_t)t * H_kv + h / G) * k + hl], t, none);
+      if (valid) ls = part_lse[((size_t)tl * k + hl) * H_q + h];
     }
     float M = ls;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    for (int off = 8; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off, 16));
     const float wl = valid ? __expf(ls - M) : 0.f;
     float L = wl;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    for (int off = 8; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off, 16);
+    const uint16_t* base = part_o + ((size_t)tl * k * H_q + h) * D + hl * PER;
+    const size_t slot_stride = (size_t)H_q * D;
     float acc[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-    const uint16_t* base = part_o + ((size_t)tl * k * H_q + h) * D + lane * PER;
-    const size_t slot_stride = (size_t)H_q * D;
 #pragma unroll
     for (int s = 0; s < kMaxK; ++s) {
       if (s >= k) break;
-      const float wgt = __shfl_sync(0xffffffffu, wl, s);
+      const float wgt = __shfl_sync(0xffffffffu, wl, s, 16);
       if (wgt == 0.f) continue;  // invalid or padded slot
       const uint16_t* po = base + s * slot_stride;
-      if (PER == 4) {
+      if (PER == 8) {
+        uint4 u = __ldcs(reinterpret_cast<const uint4*>(po));
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(wgt, bf16_lo(wd[i]), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wgt, bf16_hi(wd[i]), acc[2 * i + 1]);
+        }
+      } else {
         uint2 u = __ldcs(reinterpret_cast<const uint2*>(po));
         acc[0] = fmaf(wgt, bf16_lo(u.x), acc[0]);
         acc[1] = fmaf(wgt, bf16_hi(u.x), acc[1]);
         acc[2] = fmaf(wgt, bf16_lo(u.y), acc[2]);
         acc[3] = fmaf(wgt, bf16_hi(u.y), acc[3]);
-      } else {
-        uint32_t u = __ldcs(reinterpret_cast<const unsigned int*>(po));
-        acc[0] = fmaf(wgt, bf16_lo(u), acc[0]);
-        acc[1] = fmaf(wgt, bf16_hi(u), acc[1]);
       }
     }
+    if (!active) continue;
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    uint16_t* o = out + ((size_t)t * H_q + h) * D + lane * PER;
-    if (PER == 4) {
+    uint16_t* o = out + ((size_t)t * H_q + h) * D + hl * PER;
+    if (PER == 8) {
+      uint4 u;
+      u.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      u.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      u.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+      u.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+      *reinterpret_cast<uint4*>(o) = u;
+    } else {
       uint2 u;
       u.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
       u.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
       *reinterpret_cast<uint2*>(o) = u;
-    } else {
-      *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
     }
-    if (lse && lane == 0) lse[(size_t)t * H_q + h] = M + logf(L);
+    if (lse && hl == 0) lse[(size_t)t * H_q + h] = M + logf(L);
   }
 }
 
@@ -647,7 +678,7 @@ cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* 
                : launch_tiles<64>(q, kk, v, N, q0, H_q, H_kv, k, scale_log2, nb, ws, n_b, dg, st);
   if (e != cudaSuccess) return e;
   int64_t nw = (q1 - q0) * H_q;
-  unsigned mg = (unsigned)std::min<int64_t>((nw * 32 + 255) / 256, 152 * 64);
+  unsigned mg = (unsigned)std::min<int64_t>((nw * 16 + 255) / 256, 152 * 64);
   if (d == 128)
     attn_merge_kernel<128><<<mg, 256, 0, st>>>(ws.part_o, ws.part_lse, ids, q0, q1, H_q, H_kv, k,
                                                (uint16_t*)out, lse);

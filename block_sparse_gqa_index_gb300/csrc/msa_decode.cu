@@ -17,6 +17,8 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
+#include <type_traits>
+
 #include "msa_kernels.h"
 
 namespace msa {
@@ -95,41 +97,30 @@ decode_index_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restri
   }
 }
 
-template <bool FP8>
-__device__ __forceinline__ void load_row8(const void* base, size_t elem, float* out) {
-  // 8 consecutive elements starting at `elem`
-  if (FP8) {
-    uint2 u = *reinterpret_cast<const uint2*>((const uint8_t*)base + elem);
-    uint32_t w[2] = {u.x, u.y};
+// 8 elements from a 16-byte (bf16) or 8-byte (FP8) vector
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* out) {
+  out[0] = bf16_lo(u.x); out[1] = bf16_hi(u.x);
+  out[2] = bf16_lo(u.y); out[3] = bf16_hi(u.y);
+  out[4] = bf16_lo(u.z); out[5] = bf16_hi(u.z);
+  out[6] = bf16_lo(u.w); out[7] = bf16_hi(u.w);
+}
+__device__ __forceinline__ void unpack_e4m3x8(const uint2& u, float* out) {
+  const uint32_t w[2] = {u.x, u.y};
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFF), __NV_E4M3);
-      __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
-      float2 a = __half22float2(*reinterpret_cast<__half2*>(&lo));
-      float2 b = __half22float2(*reinterpret_cast<__half2*>(&hi));
-      out[4 * i + 0] = a.x;
-      out[4 * i + 1] = a.y;
-      out[4 * i + 2] = b.x;
-      out[4 * i + 3] = b.y;
-    }
-  } else {
-    uint4 u = *reinterpret_cast<const uint4*>((const uint16_t*)base + elem);
-    out[0] = bf16_lo(u.x); out[1] = bf16_hi(u.x);
-    out[2] = bf16_lo(u.y); out[3] = bf16_hi(u.y);
-    out[4] = bf16_lo(u.z); out[5] = bf16_hi(u.z);
-    out[6] = bf16_lo(u.w); out[7] = bf16_hi(u.w);
+  for (int i = 0; i < 2; ++i) {
+    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFF), __NV_E4M3);
+    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+    float2 a = __half22float2(*reinterpret_cast<__half2*>(&lo));
+    float2 b = __half22float2(*reinterpret_cast<__half2*>(&hi));
+    out[4 * i + 0] = a.x; out[4 * i + 1] = a.y; out[4 * i + 2] = b.x; out[4 * i + 3] = b.y;
   }
 }
 
-template <bool FP8>
-__device__ __forceinline__ float load1(const void* base, size_t elem) {
-  if (FP8) {
-    __half_raw h = __nv_cvt_fp8_to_halfraw(((const uint8_t*)base)[elem], __NV_E4M3);
-    return __half2float(*reinterpret_cast<__half*>(&h));
-  }
-  return __uint_as_float((uint32_t)((const uint16_t*)base)[elem] << 16);
-}
-
+// One CTA (128 threads) per (sequence, group, selected page). Scores: thread j
+// owns token j and issues all of its K-row loads before using them. P.V: the
+// threads form 16 column groups (8 columns each) x 8 token groups (16 tokens
+// each, strided so a warp reads whole token rows); partial sums over the token
+// groups are added up in shared memory.
 template <int D, bool FP8>
 __global__ void __launch_bounds__(128)
 decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
@@ -139,9 +130,13 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
                    int max_pages, int H_q, int H_kv, int k, float scale_log2,
                    float* __restrict__ part_o, float* __restrict__ part_lse, Diag dg) {
   constexpr int GMAX = 8;
+  constexpr int CG = D / 8;      // column groups
+  constexpr int TG = 128 / CG;   // token groups
+  constexpr int EB = FP8 ? 1 : 2;
   __shared__ float qs[GMAX][D];
   __shared__ float sc[GMAX][kBk];
   __shared__ float s_m[GMAX], s_l[GMAX];
+  __shared__ float red[TG][GMAX][D];
   const int G = H_q / H_kv;
   const int tid = threadIdx.x;
   const int64_t task = blockIdx.x;  // (s * H_kv + g) * k + slot
@@ -160,28 +155,39 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
   const int nvalid = min(kBk, L - id * kBk);
   const float ks = FP8 ? k_scale[g] : 1.f;
   const float vs = FP8 ? v_scale[g] : 1.f;
+  const size_t row_stride = (size_t)H_kv * D;  // elements between tokens
+  const size_t base = ((size_t)page * kBk * H_kv + g) * D;
 
-  for (int e = tid; e < G * D; e += blockDim.x) {
+  for (int e = tid; e < G * D; e += 128) {
     int h = e / D, c = e % D;
     qs[h][c] = __uint_as_float((uint32_t)q[((size_t)s * H_q + g * G + h) * D + c] << 16);
   }
-  __syncthreads();
-  {
-    const int j = tid;  // token of the block
-    float acc[GMAX];
+  // K row of token tid, all loads in flight before use
+  float acc[GMAX];
 #pragma unroll
-    for (int h = 0; h < GMAX; ++h) acc[h] = 0.f;
+  for (int h = 0; h < GMAX; ++h) acc[h] = 0.f;
+  {
+    const int j = tid;
+    // raw K row (16-byte bf16 or 8-byte E4M3 vectors), unpacked in the FMA loop
+    using Vec = typename std::conditional<FP8, uint2, uint4>::type;
+    Vec u[D / 8];
     if (j < nvalid) {
-      const size_t row = (((size_t)page * kBk + j) * H_kv + g) * D;
-#pragma unroll 4
-      for (int c = 0; c < D; c += 8) {
+      const Vec* kr = reinterpret_cast<const Vec*>((const unsigned char*)kp +
+                                                   (base + j * row_stride) * EB);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) u[c] = __ldcs(kr + c);
+    }
+    __syncthreads();  // qs ready
+    if (j < nvalid) {
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
         float x[8];
-        load_row8<FP8>(kp, row + c, x);
+        if constexpr (FP8) unpack_e4m3x8(u[c], x); else unpack_bf16x8(u[c], x);
 #pragma unroll
         for (int h = 0; h < GMAX; ++h)
           if (h < G)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[h] = fmaf(qs[h][c + i], x[i], acc[h]);
+            for (int i = 0; i < 8; ++i) acc[h] = fmaf(qs[h][8 * c + i], x[i], acc[h]);
       }
     }
 #pragma unroll
@@ -210,22 +216,52 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
     }
   }
   __syncthreads();
-  for (int c = tid; c < D; c += blockDim.x) {
-    float acc[GMAX];
+  {
+    const int cg = tid % CG, tg = tid / CG;
+    float o[GMAX][8];
 #pragma unroll
-    for (int h = 0; h < GMAX; ++h) acc[h] = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < nvalid; ++j) {
-      float x = load1<FP8>(vp, (((size_t)page * kBk + j) * H_kv + g) * D + c);
+    for (int h = 0; h < GMAX; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
+    constexpr int NT = kBk / TG;  // tokens per thread
+    using Vec = typename std::conditional<FP8, uint2, uint4>::type;
+    Vec vr[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int j = tg + n * TG;
+      if (j < nvalid)
+        vr[n] = __ldcs(reinterpret_cast<const Vec*>((const unsigned char*)vp +
+                                                    (base + j * row_stride + cg * 8) * EB));
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int j = tg + n * TG;
+      if (j >= nvalid) continue;
+      float x[8];
+      if constexpr (FP8) unpack_e4m3x8(vr[n], x); else unpack_bf16x8(vr[n], x);
 #pragma unroll
       for (int h = 0; h < GMAX; ++h)
-        if (h < G) acc[h] = fmaf(sc[h][j], x, acc[h]);
+        if (h < G) {
+          const float p = sc[h][j];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[h][i] = fmaf(p, x[i], o[h][i]);
+        }
     }
-    for (int h = 0; h < G; ++h) {
-      size_t dst = ((size_t)s * H_q + g * G + h) * k + slot;
-      part_o[dst * D + c] = acc[h] * vs / s_l[h];
-      if (c == 0) part_lse[dst] = (s_m[h] + __log2f(s_l[h])) * 0.69314718055994531f;
-    }
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h)
+      if (h < G)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) red[tg][h][cg * 8 + i] = o[h][i];
+  }
+  __syncthreads();
+  for (int e = tid; e < G * D; e += 128) {
+    const int h = e / D, c = e % D;
+    float sum = 0.f;
+#pragma unroll
+    for (int t = 0; t < TG; ++t) sum += red[t][h][c];
+    const size_t dst = ((size_t)s * H_q + g * G + h) * k + slot;
+    part_o[dst * D + c] = sum * vs / s_l[h];
+    if (c == 0) part_lse[dst] = (s_m[h] + __log2f(s_l[h])) * 0.69314718055994531f;
   }
 }
 
