@@ -248,7 +248,7 @@ def time_decode(msa, w, fp8, steps, warmup):
     dev = torch.device("cuda")
     pt = torch.from_numpy(synth.page_table(w)).to(dev)
     sl = torch.full((w.B,), w.L, dtype=torch.int32, device=dev)
-    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, :, 0].contiguous()
+    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, 0].contiguous()
     kp = synth.device_paged(w, synth.T_K, pt, fp8=fp8)
     vp = synth.device_paged(w, synth.T_V, pt, fp8=fp8)
     last = [(s, w.L - 1) for s in range(w.B)]

@@ -258,17 +258,17 @@ def msa_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
                k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
                workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                lse: Optional[torch.Tensor] = None, want_lse: bool = True):
-    """Main branch of decode. q [B, H_q, d] bf16; k_pages/v_pages [P, Bk, H_kv, d]
-    bf16, or uint8 E4M3 codes with k_scale/v_scale [H_kv] fp32."""
+    """Main branch of decode. q [B, H_q, d] bf16; k_pages/v_pages [P, H_kv, Bk, d]
+    (head-major pages) bf16, or uint8 E4M3 codes with k_scale/v_scale [H_kv] fp32."""
     B, H_q, d = q.shape
-    P, _, H_kv, _ = k_pages.shape
+    P, H_kv, _, _ = k_pages.shape
     max_pages = page_table.shape[1]
     topk = block_ids.shape[-1]
     fp8 = k_pages.dtype == torch.uint8
     kv_dtype = MSA_KV_E4M3 if fp8 else MSA_KV_BF16
     _req(q, "q", torch.bfloat16)
-    _req(k_pages, "k_pages", torch.uint8 if fp8 else torch.bfloat16, (P, Bk, H_kv, d))
-    _req(v_pages, "v_pages", torch.uint8 if fp8 else torch.bfloat16, (P, Bk, H_kv, d))
+    _req(k_pages, "k_pages", torch.uint8 if fp8 else torch.bfloat16, (P, H_kv, Bk, d))
+    _req(v_pages, "v_pages", torch.uint8 if fp8 else torch.bfloat16, (P, H_kv, Bk, d))
     _req(page_table, "page_table", torch.int32, (B, max_pages))
     _req(seq_lens, "seq_lens", torch.int32, (B,))
     _req(block_ids, "block_ids", torch.int32, (B, H_kv, topk))

@@ -10,6 +10,9 @@
 //   the M dimension of mma.m16n8k16 and the (up to 8) groups its N dimension;
 //   the d_idx reduction order is permuted identically in A and B so that each
 //   thread reads 16 contiguous bytes per key row. HBM-bound.
+// Caches: K / V pages are head-major [P, H_kv, 128, d] (the page tensor's second
+// dimension is the kv-head count in the usage listing), so the block a group
+// reads is one contiguous run; k_idx pages are [P, 128, d_idx].
 // decode_attn_kernel: one CTA per (sequence, group, selected block): the G
 //   query heads of the group against the block's visible tokens; writes the
 //   block's normalised output and LSE (split-KV partials).
@@ -155,8 +158,9 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
   const int nvalid = min(kBk, L - id * kBk);
   const float ks = FP8 ? k_scale[g] : 1.f;
   const float vs = FP8 ? v_scale[g] : 1.f;
-  const size_t row_stride = (size_t)H_kv * D;  // elements between tokens
-  const size_t base = ((size_t)page * kBk * H_kv + g) * D;
+  // pages are head-major [P, H_kv, Bk, D]: the (page, head g) block is contiguous
+  const size_t row_stride = D;  // elements between tokens
+  const size_t base = ((size_t)page * H_kv + g) * kBk * D;
 
   for (int e = tid; e < G * D; e += 128) {
     int h = e / D, c = e % D;

@@ -118,7 +118,8 @@ int msa_sparse_attn(const void* q, const void* k, const void* v, const int32_t* 
 
 /* ----------------------------------------------------------------- decode -- */
 
-/* Paged caches ("运行 Kernel": page size = block size). Sequence s holds
+/* Paged caches ("运行 Kernel": page size = block size; the page tensor's second
+ * dimension is the number of kv heads, so pages are head-major). Sequence s holds
  * seq_lens[s] tokens; its logical block b lives in physical page
  * page_table[s * max_pages + b]. The new token is the last one (position
  * seq_lens[s] - 1) and must already be written to the caches. */
@@ -144,7 +145,7 @@ size_t msa_decode_workspace_bytes(int B, int H_q, int d, int k);
 
 /* Main branch of decode over a paged bf16 or FP8-E4M3 KV cache.
  *   q              [B, H_q, d] bf16
- *   k_pages        [P, Bk, H_kv, d] bf16 or E4M3 bytes (kv_dtype)
+ *   k_pages        [P, H_kv, Bk, d] bf16 or E4M3 bytes (kv_dtype)
  *   v_pages        same layout and dtype
  *   k_scale        [H_kv] fp32 per-kv-head dequantisation scale (E4M3 only;
  *   v_scale        K or V value = code * scale); ignored for bf16

@@ -148,7 +148,7 @@ def decode_index_select(q_idx, k_idx_pages, page_table, seq_lens, Bk, k, nb_out=
 
 def decode_attn(q, k_pages, v_pages, page_table, seq_lens, ids, Bk, scale, fp8=False,
                 k_scale=None, v_scale=None):
-    """q [B, H_q, d]; k_pages, v_pages [P, Bk, H_kv, d] (bf16 bits, or E4M3 bits
+    """q [B, H_q, d]; k_pages, v_pages [P, H_kv, Bk, d] (bf16 bits, or E4M3 bits
     with per-kv-head fp32 scales when fp8)."""
     qq, qp = _c(q, np.uint16)
     kdt = np.uint8 if fp8 else np.uint16
@@ -158,7 +158,7 @@ def decode_attn(q, k_pages, v_pages, page_table, seq_lens, ids, Bk, scale, fp8=F
     sl, slp = _c(seq_lens, np.int32)
     ii, ip = _c(ids, np.int32)
     B, H_q, d = qq.shape
-    H_kv = kp.shape[2]
+    H_kv = kp.shape[1]
     ks = np.ascontiguousarray(k_scale if k_scale is not None else np.ones(H_kv), np.float32)
     vs = np.ascontiguousarray(v_scale if v_scale is not None else np.ones(H_kv), np.float32)
     o = np.empty((B, H_q, d), dtype=np.float64)

@@ -85,16 +85,20 @@ double e4m3_to_double(uint8_t b) {
   return sign ? -v : v;
 }
 
-// Key rows of one sequence: token position j -> pointer to its first element.
+// Key rows of one sequence. Unpaged tensors are [tokens, H, D]. Paged caches
+// keep each page head-major, [pages, H, Bk, D] (the page tensor's second
+// dimension is the number of kv heads in the pages' usage listing), with
+// logical block b of the sequence in page pages[b].
 struct Rows {
   const uint8_t* base = nullptr;   // element bytes
-  int64_t row_elems = 0;           // elements per token row (H * D)
+  int64_t H = 1, D = 0;            // heads and head dim of the tensor
   int elem_bytes = 2;
-  const int32_t* pages = nullptr;  // page table of this sequence (nullptr: contiguous)
+  const int32_t* pages = nullptr;  // page table of this sequence (nullptr: unpaged)
   int Bk = 128;
-  const uint8_t* row(int64_t j) const {
-    int64_t r = pages ? (int64_t)pages[j / Bk] * Bk + j % Bk : j;
-    return base + (size_t)(r * row_elems) * elem_bytes;
+  // first element of (token j, head h)
+  const uint8_t* at(int64_t j, int64_t h) const {
+    int64_t e = pages ? (((int64_t)pages[j / Bk] * H + h) * Bk + j % Bk) * D : (j * H + h) * D;
+    return base + (size_t)e * elem_bytes;
   }
 };
 
@@ -113,7 +117,7 @@ void block_scores(const double* qi, const Rows& kidx, int d_idx, int64_t t, int 
   int64_t loc = t / Bk;
   S.assign((size_t)(loc + 1), NEG_INF);
   for (int64_t j = 0; j <= t; ++j) {
-    const uint8_t* kr = kidx.row(j);
+    const uint8_t* kr = kidx.at(j, 0);
     double s = 0.0;
     for (int c = 0; c < d_idx; ++c) s += qi[c] * load(kr, c, 2);
     int64_t b = j / Bk;
@@ -151,9 +155,9 @@ void attend(const double* q, const Rows& K, const Rows& V, int kvh, int d,
   std::vector<double> x(J.size());
   double m = NEG_INF;
   for (size_t n = 0; n < J.size(); ++n) {
-    const uint8_t* kr = K.row(J[n]);
+    const uint8_t* kr = K.at(J[n], kvh);
     double s = 0.0;
-    for (int c = 0; c < d; ++c) s += q[c] * (load(kr, (int64_t)kvh * d + c, K.elem_bytes) * *kscale);
+    for (int c = 0; c < d; ++c) s += q[c] * (load(kr, c, K.elem_bytes) * *kscale);
     x[n] = s * scale;
     m = std::max(m, x[n]);
   }
@@ -162,8 +166,8 @@ void attend(const double* q, const Rows& K, const Rows& V, int kvh, int d,
   for (size_t n = 0; n < J.size(); ++n) {
     double p = std::exp(x[n] - m);
     l += p;
-    const uint8_t* vr = V.row(J[n]);
-    for (int c = 0; c < d; ++c) acc[(size_t)c] += p * (load(vr, (int64_t)kvh * d + c, V.elem_bytes) * *vscale);
+    const uint8_t* vr = V.at(J[n], kvh);
+    for (int c = 0; c < d; ++c) acc[(size_t)c] += p * (load(vr, c, V.elem_bytes) * *vscale);
   }
   for (int c = 0; c < d; ++c) o[c] = J.empty() ? 0.0 : acc[(size_t)c] / l;
   *lse = J.empty() ? NEG_INF : m + std::log(l);
@@ -201,7 +205,7 @@ int oracle_index_select(const uint16_t* q_idx_rows, const int64_t* rows, int64_t
   if (k < 1 || Bk < 1 || d_idx < 1 || n_g < 1) return -1;
   Rows kr;
   kr.base = (const uint8_t*)k_idx;
-  kr.row_elems = d_idx;
+  kr.D = d_idx;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < n_rows * n_g; ++r) {
     int64_t t = rows[r / n_g];
@@ -245,7 +249,8 @@ int oracle_sparse_attn(const uint16_t* q_rows, const int64_t* rows, int64_t n_ro
   Rows kr, vr;
   kr.base = (const uint8_t*)K;
   vr.base = (const uint8_t*)V;
-  kr.row_elems = vr.row_elems = (int64_t)H_kv * d;
+  kr.H = vr.H = H_kv;
+  kr.D = vr.D = d;
   const double one = 1.0;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t r = 0; r < n_rows * H_q; ++r) {
@@ -355,7 +360,7 @@ int oracle_decode_index_select(const uint16_t* q_idx, const uint16_t* k_idx_page
     int64_t t = (int64_t)seq_lens[s] - 1;
     Rows kr;
     kr.base = (const uint8_t*)k_idx_pages;
-    kr.row_elems = d_idx;
+    kr.D = d_idx;
     kr.pages = page_table + (size_t)s * max_pages;
     kr.Bk = Bk;
     std::vector<double> qi((size_t)d_idx), S;
@@ -370,7 +375,7 @@ int oracle_decode_index_select(const uint16_t* q_idx, const uint16_t* k_idx_page
 }
 
 // Decode main branch with a paged bf16 (kv_fp8 = 0) or E4M3 (kv_fp8 = 1) cache.
-//   q [B, H_q, d] bf16; k_pages, v_pages [P, Bk, H_kv, d]; k_scale, v_scale
+//   q [B, H_q, d] bf16; k_pages, v_pages [P, H_kv, Bk, d]; k_scale, v_scale
 //   [H_kv] fp32 (used for E4M3 only); ids [B, n_g, k]
 //   o_out [B, H_q, d] fp64; lse_out [B, H_q] fp64
 int oracle_decode_attn(const uint16_t* q, const void* k_pages, const void* v_pages, int kv_fp8,
@@ -388,7 +393,8 @@ int oracle_decode_attn(const uint16_t* q, const void* k_pages, const void* v_pag
     Rows kr, vr;
     kr.base = (const uint8_t*)k_pages;
     vr.base = (const uint8_t*)v_pages;
-    kr.row_elems = vr.row_elems = (int64_t)H_kv * d;
+    kr.H = vr.H = H_kv;
+    kr.D = vr.D = d;
     kr.elem_bytes = vr.elem_bytes = kv_fp8 ? 1 : 2;
     kr.pages = vr.pages = page_table + (size_t)s * max_pages;
     kr.Bk = vr.Bk = Bk;

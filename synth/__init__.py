@@ -301,19 +301,23 @@ def host_sparse_blocks(w: Workload, tensor: int, blocks_per_seq, fp8: bool = Fal
 
 
 def host_paged(w: Workload, tensor: int, blocks_per_seq=None, fp8: bool = False) -> np.ndarray:
-    """Identity-paged cache [B * nb, Bk, H, D] (page = s * nb + b). Holds every
-    block when blocks_per_seq is None, else only the listed blocks of each
-    sequence (zeros elsewhere; untouched zero pages cost no host memory)."""
+    """Identity-paged cache [B * nb, H, Bk, D] (page = s * nb + b, head-major
+    pages). Holds every block when blocks_per_seq is None, else only the listed
+    blocks of each sequence (zeros elsewhere; untouched zero pages cost no host
+    memory)."""
     H, D = _dims(w, tensor)
-    out = np.zeros((w.B * w.nb, w.Bk, H, D), dtype=np.uint8 if fp8 else np.uint16)
+    dt = np.uint8 if fp8 else np.uint16
+    out = np.zeros((w.B * w.nb, H, w.Bk, D), dtype=dt)
     per = H * D
+    tmp = np.empty(w.Bk * per, dtype=dt)
     for s in range(w.B):
         blocks = range(w.nb) if blocks_per_seq is None else \
             sorted(set(int(x) for x in blocks_per_seq[s] if x >= 0))
         for b in blocks:
             t0, t1 = b * w.Bk, min(w.L, (b + 1) * w.Bk)
-            host_fill(w, tensor, out, (s * w.L + t0) * per, (t1 - t0) * per, fp8,
-                      dst0=(s * w.nb + b) * w.Bk * per)
+            n = (t1 - t0) * per
+            host_fill(w, tensor, tmp, (s * w.L + t0) * per, n, fp8, dst0=0)
+            out[s * w.nb + b, :, :t1 - t0] = tmp[:n].reshape(t1 - t0, H, D).transpose(1, 0, 2)
     return out
 
 
@@ -375,13 +379,14 @@ def device_rows(w: Workload, tensor: int, seq_rows, device="cuda"):
 
 
 def device_paged(w: Workload, tensor: int, table, fp8: bool = False, device="cuda"):
-    """Paged cache [B*nb pages, Bk, H, D] placed by `table` ([B, nb] int32 torch
-    tensor on the device); bf16, or E4M3 bits as torch.uint8 when fp8."""
+    """Paged cache [B*nb pages, H, Bk, D] (head-major pages) placed by `table`
+    ([B, nb] int32 torch tensor on the device); bf16, or E4M3 bits as
+    torch.uint8 when fp8."""
     import torch
     H, D = _dims(w, tensor)
     P = w.B * w.nb
     dtype = torch.uint8 if fp8 else torch.bfloat16
-    out = torch.zeros((P, w.Bk, H, D), dtype=dtype, device=device)
+    out = torch.zeros((P, H, w.Bk, D), dtype=dtype, device=device)
     planted = torch.from_numpy(w.planted).to(device)
     sp = w.spec(planted.data_ptr())
     stream = torch.cuda.current_stream(out.device).cuda_stream

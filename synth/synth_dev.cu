@@ -13,8 +13,8 @@ __global__ void fill_bf16_kernel(SynthSpec sp, int tensor, uint64_t idx0, uint64
     out[i] = synth_element(&sp, tensor, idx0 + i);
 }
 
-/* Paged cache [P, Bk, H, D]: logical element (s, t, h, c) lives in physical
- * page page_table[s * max_pages + t / Bk], row t % Bk. */
+/* Paged cache [P, H, Bk, D] (head-major pages): logical element (s, t, h, c)
+ * lives in physical page page_table[s * max_pages + t / Bk], head h, row t % Bk. */
 template <typename T, bool FP8>
 __global__ void fill_paged_kernel(SynthSpec sp, int tensor, int H, int D,
                                   const int32_t* __restrict__ page_table, int max_pages,
@@ -27,8 +27,9 @@ __global__ void fill_paged_kernel(SynthSpec sp, int tensor, int H, int D,
     uint64_t rem = i % per_seq;
     uint64_t t = rem / ((uint64_t)H * D);
     uint64_t hc = rem % ((uint64_t)H * D);
+    uint64_t h = hc / D, c = hc % D;
     int64_t page = page_table[s * max_pages + t / sp.Bk];
-    uint64_t dst = ((uint64_t)page * sp.Bk + t % sp.Bk) * H * D + hc;
+    uint64_t dst = (((uint64_t)page * H + h) * sp.Bk + t % sp.Bk) * D + c;
     if (FP8)
       out[dst] = (T)synth_element_e4m3(&sp, tensor, i);
     else

@@ -53,8 +53,8 @@ def test_device_generator_matches_host(msa):
         for s in range(w.B):
             for b in range(w.nb):
                 n = min(w.Bk, w.L - b * w.Bk)
-                a = dev[ptn[s, b], :n].view(np.uint8 if fp8 else np.uint16)
-                assert np.array_equal(a, host[s * w.nb + b, :n]), (fp8, s, b)
+                a = dev[ptn[s, b], :, :n].view(np.uint8 if fp8 else np.uint16)
+                assert np.array_equal(a, host[s * w.nb + b, :, :n]), (fp8, s, b)
 
 
 # ------------------------------------------------------------- index branch
@@ -259,7 +259,7 @@ def _decode_case(msa, w, fp8):
     ptn = synth.page_table(w)
     pt = torch.from_numpy(ptn).to(dev)
     sl = torch.full((w.B,), w.L, dtype=torch.int32, device=dev)
-    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, :, 0].contiguous()
+    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, 0].contiguous()
     last = [(s, w.L - 1) for s in range(w.B)]
     q = synth.device_rows(w, synth.T_Q, last)
     qidx = synth.device_rows(w, synth.T_QIDX, last)
@@ -268,7 +268,7 @@ def _decode_case(msa, w, fp8):
     del kidx_p
     ident = synth.page_table(w, permute=False)
     sl_np = np.full(w.B, w.L, dtype=np.int32)
-    kh = synth.host_paged(w, synth.T_KIDX)[:, :, 0]
+    kh = synth.host_paged(w, synth.T_KIDX)[:, 0]
     qidx_h = np.stack([synth.host_rows(w, synth.T_QIDX, s, [w.L - 1])[0] for s in range(w.B)])
     want, want_s = oracle.decode_index_select(qidx_h, kh, ident, sl_np, w.Bk, w.k, nb_out=w.nb,
                                               want_scores=True)
@@ -316,12 +316,12 @@ def test_decode_ragged_lengths(msa):
     dev = torch.device("cuda")
     ptn = synth.page_table(w)
     pt = torch.from_numpy(ptn).to(dev)
-    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, :, 0].contiguous()
+    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, 0].contiguous()
     qidx = synth.device_rows(w, synth.T_QIDX, [(s, int(lens[s]) - 1) for s in range(w.B)])
     ids = msa.msa_index_select_decode(qidx, kidx_p, pt, torch.from_numpy(lens).to(dev), w.Bk,
                                       w.k)
     ident = synth.page_table(w, permute=False)
-    kh = synth.host_paged(w, synth.T_KIDX)[:, :, 0]
+    kh = synth.host_paged(w, synth.T_KIDX)[:, 0]
     qh = np.stack([synth.host_rows(w, synth.T_QIDX, s, [int(lens[s]) - 1])[0]
                    for s in range(w.B)])
     want = oracle.decode_index_select(qh, kh, ident, lens, w.Bk, w.k)
@@ -353,7 +353,7 @@ def test_decode_matches_prefill_row_on_gpu(msa):
     out_p, lse_p = msa.msa_sparse_attn(q, kk, v, ids_p, w.Bk, w.scale)
     pt = torch.from_numpy(synth.page_table(w)).to(dev)
     sl = torch.tensor([w.L], dtype=torch.int32, device=dev)
-    ids_d = msa.msa_index_select_decode(qidx[-1:], synth.device_paged(w, synth.T_KIDX, pt)[:, :, 0]
+    ids_d = msa.msa_index_select_decode(qidx[-1:], synth.device_paged(w, synth.T_KIDX, pt)[:, 0]
                                         .contiguous(), pt, sl, w.Bk, w.k)
     out_d, lse_d = msa.msa_decode(q[-1:], synth.device_paged(w, synth.T_K, pt),
                                   synth.device_paged(w, synth.T_V, pt), pt, sl, ids_d, w.Bk,

@@ -348,18 +348,18 @@ def test_decode_equals_prefill_row():
     qidx_all = synth.host_tensor(w, synth.T_QIDX)
     q_all = synth.host_tensor(w, synth.T_Q)
 
-    def paged(x):  # [B, L, H, D] -> [P, Bk, H, D] through the page table
+    def paged(x):  # [B, L, H, D] -> head-major pages [P, H, Bk, D] through the page table
         B, L, H, D = x.shape
         P = pt.size
-        out = np.zeros((P, w.Bk, H, D), dtype=x.dtype)
+        out = np.zeros((P, H, w.Bk, D), dtype=x.dtype)
         for s in range(B):
             for b in range(w.nb):
                 t0, t1 = b * w.Bk, min(L, (b + 1) * w.Bk)
-                out[pt[s, b], :t1 - t0] = x[s, t0:t1]
+                out[pt[s, b], :, :t1 - t0] = x[s, t0:t1].transpose(1, 0, 2)
         return out
 
     t = w.L - 1
-    ids_d = oracle.decode_index_select(qidx_all[:, t], paged(kidx)[:, :, 0], pt, seq_lens,
+    ids_d = oracle.decode_index_select(qidx_all[:, t], paged(kidx)[:, 0], pt, seq_lens,
                                        w.Bk, w.k)
     o_d, l_d = oracle.decode_attn(q_all[:, t], paged(K), paged(V), pt, seq_lens, ids_d, w.Bk,
                                   w.scale)
@@ -376,10 +376,10 @@ def test_decode_fp8_path_equals_bf16_on_exact_values():
     """One page, scale 1, values exact in both E4M3 and bf16: both KV paths agree."""
     rng = np.random.default_rng(41)
     Bk, H_kv, H_q, d = 128, 2, 4, 16
-    vals = rng.integers(-16, 17, size=(1, Bk, H_kv, d)).astype(np.float32) / 4.0
+    vals = rng.integers(-16, 17, size=(1, H_kv, Bk, d)).astype(np.float32) / 4.0
     kb = bf16_bits(vals)
     k8 = torch.from_numpy(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-    vv = rng.integers(-16, 17, size=(1, Bk, H_kv, d)).astype(np.float32) / 8.0
+    vv = rng.integers(-16, 17, size=(1, H_kv, Bk, d)).astype(np.float32) / 8.0
     vb = bf16_bits(vv)
     v8 = torch.from_numpy(vv).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     q = rand_bf16(rng, (1, H_q, d))

@@ -30,7 +30,7 @@ def msa():
 def _decode_inputs(w, lens):
     dev = torch.device("cuda")
     pt = torch.from_numpy(synth.page_table(w)).to(dev)
-    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, :, 0].contiguous()
+    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, 0].contiguous()
     qidx = synth.device_rows(w, synth.T_QIDX, [(s, int(lens[s]) - 1) for s in range(w.B)])
     return qidx, kidx_p, pt, torch.from_numpy(np.asarray(lens, dtype=np.int32)).to(dev)
 
