@@ -411,7 +411,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=15.0)
-    ap.add_argument("--only", choices=["decode", "topk"], default=None,
+    ap.add_argument("--only", choices=["decode", "topk", "index"], default=None,
                     help="time only this path and print its numbers (for profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -434,6 +434,24 @@ def main():
             i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, args.warmup)
             torch.cuda.empty_cache()
             print(json.dumps({"only": "decode", "fp8": fp8, "index_ms": i_ms, "attention_ms": a_ms}))
+        return
+    if args.only == "index":
+        w = synth.make(args.workload)
+        qidx = synth.device_tensor(w, synth.T_QIDX)
+        kidx = synth.device_tensor(w, synth.T_KIDX)[:, 0].contiguous()
+        ids = torch.empty((w.N, w.n_g, w.k), dtype=torch.int32, device="cuda")
+        for _ in range(args.warmup):
+            msa.msa_index_select(qidx, kidx, w.Bk, w.k, block_ids=ids)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            msa.msa_index_select(qidx, kidx, w.Bk, w.k, block_ids=ids)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        print(json.dumps({"only": "index", "workload": w.name, "ms": ms,
+                          "tflops": index_flops(w.N, w.n_g, w.d_idx) / (ms * 1e-3) / 1e12}))
         return
     if args.only == "topk":
         t_ms, t_bytes = time_topk(msa, synth.make("128k"), args.steps, args.warmup)
