@@ -23,7 +23,6 @@
 #include <type_traits>
 
 #include "msa_kernels.h"
-#include "msa_sm100.cuh"
 
 namespace msa {
 namespace {
@@ -120,235 +119,154 @@ __device__ __forceinline__ void unpack_e4m3x8(const uint2& u, float* out) {
   }
 }
 
-// Pipelined split-KV decode attention. One persistent CTA (256 threads) per SM
-// walks the (sequence, group, selected page) tasks blockIdx.x, + gridDim.x, ...
-// All tasks' validity and page numbers are looked up once up front; then thread
-// 0 keeps two tasks ahead, bulk-copying each task's K block, V block (each one
-// contiguous run of the head-major page) and the group's G query rows into a
-// 3-stage shared-memory ring, so DRAM latency hides behind the current task.
-//   scores  two threads per token (half of d each), reading their K row in a
-//           rotated chunk order so the 8 lanes of a quarter warp hit distinct
-//           banks;
-//   softmax one warp per head;
-//   P.V     warp w owns columns [w * D/8, (w+1) * D/8), lanes split the tokens
-//           and combine by shuffles; writes the block's normalised output and
-//           LSE (the split-KV partials that decode_merge_kernel combines).
-constexpr int kDecThreads = 256;
-constexpr int kDecStages = 3;
-constexpr int kDecMaxTasks = 64;  // tasks per CTA (grid grows beyond the SM count if needed)
-
-struct DecMeta {
-  int32_t valid, nvalid, page, parity;
-};
-
+// One CTA (128 threads) per (sequence, group, selected page). Scores: thread j
+// owns token j and issues all of its K-row loads before using them. P.V: the
+// threads form 16 column groups (8 columns each) x 8 token groups (16 tokens
+// each, strided so a warp reads whole token rows); partial sums over the token
+// groups are added up in shared memory.
 template <int D, bool FP8>
-struct DecSmem {
-  static constexpr int EB = FP8 ? 1 : 2;
-  static constexpr int kKVBytes = kBk * D * EB;      // one K or V block
-  static constexpr int kQBytes = 8 * D * 2;          // up to 8 query heads (bf16)
-  static constexpr int kStageBytes = 2 * kKVBytes + kQBytes;
-  static constexpr int kQsOff = kDecStages * kStageBytes;      // fp32 q [8][D]
-  static constexpr int kScOff = kQsOff + 8 * D * 4;            // fp32 scores [8][128]
-  static constexpr int kStatOff = kScOff + 8 * kBk * 4;        // m, l per head
-  static constexpr int kMetaOff = kStatOff + 2 * 8 * 4;
-  static constexpr int kBarOff = kMetaOff + kDecMaxTasks * (int)sizeof(DecMeta);
-  static constexpr int kBytes = kBarOff + kDecStages * 8 + 16;
-};
-
-template <int D, bool FP8>
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __launch_bounds__(128)
 decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
                    const void* __restrict__ vp, const float* __restrict__ k_scale,
                    const float* __restrict__ v_scale, const int32_t* __restrict__ page_table,
                    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ ids,
-                   int max_pages, int H_q, int H_kv, int k, int64_t n_tasks, float scale_log2,
+                   int max_pages, int H_q, int H_kv, int k, float scale_log2,
                    float* __restrict__ part_o, float* __restrict__ part_lse, Diag dg) {
-  using namespace sm100;
-  using S = DecSmem<D, FP8>;
-  constexpr int EB = S::EB;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 127) & ~(uintptr_t)127);
-  float* qs = reinterpret_cast<float*>(smem + S::kQsOff);
-  float* sc = reinterpret_cast<float*>(smem + S::kScOff);
-  float* s_m = reinterpret_cast<float*>(smem + S::kStatOff);
-  float* s_l = s_m + 8;
-  DecMeta* meta = reinterpret_cast<DecMeta*>(smem + S::kMetaOff);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kDecStages);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int GMAX = 8;
+  constexpr int CG = D / 8;      // column groups
+  constexpr int TG = 128 / CG;   // token groups
+  constexpr int EB = FP8 ? 1 : 2;
+  __shared__ float qs[GMAX][D];
+  __shared__ float sc[GMAX][kBk];
+  __shared__ float s_m[GMAX], s_l[GMAX];
+  __shared__ float red[TG][GMAX][D];
   const int G = H_q / H_kv;
-  const int64_t cnt64 = n_tasks > blockIdx.x ? (n_tasks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const int cnt = (int)(cnt64 < kDecMaxTasks ? cnt64 : kDecMaxTasks);
-  auto task_of = [&](int n) -> int64_t { return blockIdx.x + (int64_t)n * gridDim.x; };
+  const int tid = threadIdx.x;
+  const int64_t task = blockIdx.x;  // (s * H_kv + g) * k + slot
+  const int slot = (int)(task % k);
+  const int64_t sg = task / k;
+  const int g = (int)(sg % H_kv);
+  const int s = (int)(sg / H_kv);
+  const int id = ids[task];
+  if (id < 0) return;
+  const int L = seq_lens[s];
+  if (L < 1 || L > max_pages * kBk || id > (L - 1) / kBk) {  // merge skips this slot
+    if (tid == 0) report(dg, kStatusBadIds);
+    return;
+  }
+  const int64_t page = page_table[(size_t)s * max_pages + id];
+  const int nvalid = min(kBk, L - id * kBk);
+  const float ks = FP8 ? k_scale[g] : 1.f;
+  const float vs = FP8 ? v_scale[g] : 1.f;
+  // pages are head-major [P, H_kv, Bk, D]: the (page, head g) block is contiguous
+  const size_t row_stride = D;  // elements between tokens
+  const size_t base = ((size_t)page * H_kv + g) * kBk * D;
 
-  if (tid == 0) {
-    for (int s = 0; s < kDecStages; ++s) mbar_init(&full[s], 1);
-    *abort_flag = 0;
-    fence_barrier_init();
+  for (int e = tid; e < G * D; e += 128) {
+    int h = e / D, c = e % D;
+    qs[h][c] = __uint_as_float((uint32_t)q[((size_t)s * H_q + g * G + h) * D + c] << 16);
   }
-  // look up every task's block, page and visible length in one parallel pass
-  for (int n = tid; n < cnt; n += kDecThreads) {
-    const int64_t task = task_of(n);
-    const int64_t sg = task / k;
-    const int s = (int)(sg / H_kv);
-    const int id = ids[task];
-    const int L = seq_lens[s];
-    DecMeta m{0, 0, 0, 0};
-    if (id >= 0) {
-      if (L < 1 || L > max_pages * kBk || id > (L - 1) / kBk) {
-        report(dg, kStatusBadIds);  // the merge skips this slot too
-      } else {
-        m.valid = 1;
-        m.nvalid = min(kBk, L - id * kBk);
-        m.page = page_table[(size_t)s * max_pages + id];
+  // K row of token tid, all loads in flight before use
+  float acc[GMAX];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) acc[h] = 0.f;
+  {
+    const int j = tid;
+    // raw K row (16-byte bf16 or 8-byte E4M3 vectors), unpacked in the FMA loop
+    using Vec = typename std::conditional<FP8, uint2, uint4>::type;
+    Vec u[D / 8];
+    if (j < nvalid) {
+      const Vec* kr = reinterpret_cast<const Vec*>((const unsigned char*)kp +
+                                                   (base + j * row_stride) * EB);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) u[c] = __ldcs(kr + c);
+    }
+    __syncthreads();  // qs ready
+    if (j < nvalid) {
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        float x[8];
+        if constexpr (FP8) unpack_e4m3x8(u[c], x); else unpack_bf16x8(u[c], x);
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h)
+          if (h < G)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[h] = fmaf(qs[h][8 * c + i], x[i], acc[h]);
       }
     }
-    meta[n] = m;
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h)
+      if (h < G) sc[h][j] = j < nvalid ? acc[h] * ks * scale_log2 : -INFINITY;
   }
   __syncthreads();
-  // thread 0: parity bookkeeping and the bulk copies of task n into its stage
-  int issued[kDecStages] = {0, 0, 0};
-  auto issue = [&](int n) {
-    DecMeta& m = meta[n];
-    if (!m.valid) return;
-    const int st = n % kDecStages;
-    m.parity = issued[st] & 1;
-    ++issued[st];
-    const int64_t task = task_of(n);
-    const int64_t sg = task / k;
-    const int g = (int)(sg % H_kv);
-    const int s = (int)(sg / H_kv);
-    unsigned char* stage = smem + st * S::kStageBytes;
-    const size_t blk = ((size_t)m.page * H_kv + g) * kBk * D * EB;  // byte offset of the block
-    mbar_arrive_expect_tx(&full[st], 2 * S::kKVBytes + G * D * 2);
-    bulk_load(stage, (const unsigned char*)kp + blk, S::kKVBytes, &full[st]);
-    bulk_load(stage + S::kKVBytes, (const unsigned char*)vp + blk, S::kKVBytes, &full[st]);
-    bulk_load(stage + 2 * S::kKVBytes, q + ((size_t)s * H_q + g * G) * D, G * D * 2, &full[st]);
-  };
-  if (tid == 0) {
-    if (cnt > 0) issue(0);
-    if (cnt > 1) issue(1);
-  }
-  __syncthreads();
-  bool ok = true;
-  for (int n = 0; n < cnt; ++n) {
-    const int st = n % kDecStages;
-    if (tid == 0 && n + 2 < cnt) issue(n + 2);  // its stage was released at the end of n-1
-    const DecMeta m = meta[n];
-    if (m.valid && ok) {
-      const int64_t task = task_of(n);
-      const int slot = (int)(task % k);
-      const int64_t sg = task / k;
-      const int g = (int)(sg % H_kv);
-      const int s = (int)(sg / H_kv);
-      const unsigned char* stage = smem + st * S::kStageBytes;
-      int got = 0;
-      if (lane == 0) got = mbar_wait(&full[st], (uint32_t)m.parity, abort_flag, dg) ? 1 : 0;
-      got = __shfl_sync(0xffffffffu, got, 0);
-      if (__syncthreads_and(got) == 0) {
-        ok = false;
-      } else {
-        const float ks = FP8 ? k_scale[g] : 1.f;
-        const float vs = FP8 ? v_scale[g] : 1.f;
-        const uint16_t* qb = reinterpret_cast<const uint16_t*>(stage + 2 * S::kKVBytes);
-        for (int e = tid; e < G * D; e += kDecThreads)
-          qs[e] = __uint_as_float((uint32_t)qb[e] << 16);
-        __syncthreads();
-        // scores: token j = warp * 16 + (lane & 15), half of d = lane >> 4
-        {
-          constexpr int HALF = D / 2, NCH = HALF / 8;  // 8-element chunks per half
-          const int j = warp * 16 + (lane & 15), hf = lane >> 4;
-          float acc[8];
+  {
+    const int w = tid >> 5, lane = tid & 31;
+    for (int h = w; h < G; h += 4) {
+      float m = -INFINITY;
 #pragma unroll
-          for (int h = 0; h < 8; ++h) acc[h] = 0.f;
-          const unsigned char* krow = stage + (size_t)j * D * EB + hf * HALF * EB;
+      for (int i = 0; i < kBk / 32; ++i) m = fmaxf(m, sc[h][lane + 32 * i]);
 #pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-            const int ch = (c + j) % NCH;  // rotated: distinct banks within a quarter warp
-            float x[8];
-            if constexpr (FP8) unpack_e4m3x8(*reinterpret_cast<const uint2*>(krow + ch * 8), x);
-            else unpack_bf16x8(*reinterpret_cast<const uint4*>(krow + ch * 16), x);
-            const int col = hf * HALF + ch * 8;
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      float l = 0.f;
 #pragma unroll
-            for (int h = 0; h < 8; ++h)
-              if (h < G) {
-                const float4 qa = *reinterpret_cast<const float4*>(qs + h * D + col);
-                const float4 qc = *reinterpret_cast<const float4*>(qs + h * D + col + 4);
-                acc[h] = fmaf(qa.x, x[0], fmaf(qa.y, x[1], fmaf(qa.z, x[2], fmaf(qa.w, x[3], acc[h]))));
-                acc[h] = fmaf(qc.x, x[4], fmaf(qc.y, x[5], fmaf(qc.z, x[6], fmaf(qc.w, x[7], acc[h]))));
-              }
-          }
-#pragma unroll
-          for (int h = 0; h < 8; ++h) {
-            if (h >= G) break;
-            float a = acc[h] + __shfl_xor_sync(0xffffffffu, acc[h], 16);
-            if (hf == 0) sc[h * kBk + j] = j < m.nvalid ? a * ks * scale_log2 : -INFINITY;
-          }
-        }
-        __syncthreads();
-        if (warp < G) {  // softmax of head `warp` over the 128 tokens
-          float* row = sc + warp * kBk;
-          float mx = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < kBk / 32; ++i) mx = fmaxf(mx, row[lane + 32 * i]);
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          float l = 0.f;
-#pragma unroll
-          for (int i = 0; i < kBk / 32; ++i) {
-            const float p = ex2_approx(row[lane + 32 * i] - mx);
-            row[lane + 32 * i] = p;
-            l += p;
-          }
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-          if (lane == 0) { s_m[warp] = mx; s_l[warp] = l; }
-        }
-        __syncthreads();
-        // P.V: warp owns CPW columns; TQ lane groups split the tokens
-        {
-          constexpr int CPW = D / 8, TQ = 32 / CPW, TPG = kBk / TQ;
-          const int col = warp * CPW + lane % CPW, tq = lane / CPW;
-          float o[8];
-#pragma unroll
-          for (int h = 0; h < 8; ++h) o[h] = 0.f;
-          const unsigned char* vblk = stage + S::kKVBytes;
-          const int j0 = tq * TPG, j1 = min(j0 + TPG, m.nvalid);
-          for (int j = j0; j < j1; ++j) {
-            float x;
-            if constexpr (FP8) {
-              __half_raw hr = __nv_cvt_fp8_to_halfraw(vblk[(size_t)j * D + col], __NV_E4M3);
-              x = __half2float(*reinterpret_cast<__half*>(&hr));
-            } else {
-              x = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(vblk)[(size_t)j * D + col] << 16);
-            }
-#pragma unroll
-            for (int h = 0; h < 8; ++h)
-              if (h < G) o[h] = fmaf(sc[h * kBk + j], x, o[h]);
-          }
-#pragma unroll
-          for (int h = 0; h < 8; ++h) {
-            if (h >= G) break;
-            float a = o[h];
-#pragma unroll
-            for (int off = CPW; off < 32; off <<= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-            if (tq == 0) {
-              const size_t dst = ((size_t)s * H_q + g * G + h) * k + slot;
-              part_o[dst * D + col] = a * vs / s_l[h];
-              if (col == 0) part_lse[dst] = (s_m[h] + __log2f(s_l[h])) * 0.69314718055994531f;
-            }
-          }
-        }
+      for (int i = 0; i < kBk / 32; ++i) {
+        float p = ex2_approx(sc[h][lane + 32 * i] - m);
+        sc[h][lane + 32 * i] = p;
+        l += p;
       }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+      if (lane == 0) { s_m[h] = m; s_l[h] = l; }
     }
-    __syncthreads();  // stage st, qs and sc are free again
-  }
-  if (tid == 0 && !ok) {  // let copies in flight land before shared memory goes away
-    for (int n = 0; n < cnt; ++n)
-      if (meta[n].valid && n < cnt) mbar_drain(&full[n % kDecStages], (uint32_t)meta[n].parity);
   }
   __syncthreads();
+  {
+    const int cg = tid % CG, tg = tid / CG;
+    float o[GMAX][8];
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
+    constexpr int NT = kBk / TG;  // tokens per thread
+    using Vec = typename std::conditional<FP8, uint2, uint4>::type;
+    Vec vr[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int j = tg + n * TG;
+      if (j < nvalid)
+        vr[n] = __ldcs(reinterpret_cast<const Vec*>((const unsigned char*)vp +
+                                                    (base + j * row_stride + cg * 8) * EB));
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const int j = tg + n * TG;
+      if (j >= nvalid) continue;
+      float x[8];
+      if constexpr (FP8) unpack_e4m3x8(vr[n], x); else unpack_bf16x8(vr[n], x);
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h)
+        if (h < G) {
+          const float p = sc[h][j];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[h][i] = fmaf(p, x[i], o[h][i]);
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h)
+      if (h < G)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) red[tg][h][cg * 8 + i] = o[h][i];
+  }
+  __syncthreads();
+  for (int e = tid; e < G * D; e += 128) {
+    const int h = e / D, c = e % D;
+    float sum = 0.f;
+#pragma unroll
+    for (int t = 0; t < TG; ++t) sum += red[t][h][c];
+    const size_t dst = ((size_t)s * H_q + g * G + h) * k + slot;
+    part_o[dst * D + c] = sum * vs / s_l[h];
+    if (c == 0) part_lse[dst] = (s_m[h] + __log2f(s_l[h])) * 0.69314718055994531f;
+  }
 }
 
 template <int D>
@@ -429,24 +347,13 @@ cudaError_t launch_decode_attn(const void* q, const void* k_pages, const void* v
   float* part_o = (float*)ws;
   float* part_lse = (float*)((unsigned char*)ws + align256((size_t)B * H_q * k * d * 4));
   const float sl2 = scale * 1.4426950408889634f;
-  const int64_t n_tasks = (int64_t)B * H_kv * k;
-  if (n_tasks == 0) return cudaSuccess;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const unsigned grid = (unsigned)std::max<int64_t>(
-      std::min<int64_t>(sms, n_tasks), (n_tasks + kDecMaxTasks - 1) / kDecMaxTasks);
+  unsigned tasks = (unsigned)((int64_t)B * H_kv * k);
+  if (tasks == 0) return cudaSuccess;
   note_launches(2);  // attention, merge
 #define MSA_DEC(DD, F8)                                                                    \
-  do {                                                                                     \
-    const int smem = DecSmem<DD, F8>::kBytes + 128;                                        \
-    cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<DD, F8>,                       \
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
-    if (e != cudaSuccess) return e;                                                        \
-    decode_attn_kernel<DD, F8><<<grid, kDecThreads, smem, st>>>(                           \
-        (const uint16_t*)q, k_pages, v_pages, k_scale, v_scale, page_table, seq_lens, ids, \
-        max_pages, H_q, H_kv, k, n_tasks, sl2, part_o, part_lse, dg);                     \
-  } while (0)
+  decode_attn_kernel<DD, F8><<<tasks, 128, 0, st>>>(                                       \
+      (const uint16_t*)q, k_pages, v_pages, k_scale, v_scale, page_table, seq_lens, ids,   \
+      max_pages, H_q, H_kv, k, sl2, part_o, part_lse, dg)
   if (d == 128) {
     if (kv_fp8) MSA_DEC(128, true); else MSA_DEC(128, false);
   } else {
