@@ -165,7 +165,8 @@ __device__ __forceinline__ int64_t find_bucket(const int32_t* __restrict__ tile_
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                    const uint16_t* __restrict__ q, int64_t q0, int H_q, int H_kv, int k,
+                    const __grid_constant__ CUtensorMap tm_q, int64_t tm_rows,
+                    int64_t q0, int H_q, int H_kv, int k,
                     float scale_log2, int64_t nb, const int32_t* __restrict__ entries,
                     const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_off,
                     int64_t n_b, uint16_t* __restrict__ part_o, float* __restrict__ part_lse,
@@ -212,6 +213,7 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     fence_barrier_init();
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_q);
   }
   if (warp == 1) tmem_alloc(tmem_holder, 512);
   tc_fence_before();
@@ -324,67 +326,62 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     }
   } else if (warp < 6) {
     // ---------------------------------------------------------- Q producers
+    // Tile rows are head-major: row r holds head i = r / qt of query r % qt, so
+    // four consecutive rows are one head of four queries, fetched by one TMA
+    // row gather (tile::gather4) per 64-column chunk. Rows past the tile's
+    // queries use an out-of-range row and are zero-filled.
     const int my = warp - 2;  // Q stage owned by this warp
     unsigned char* qbuf = smem + S::kQOff + my * S::kQBytes;
     int32_t* row_t = row_t_all + my * kTileRows;
     int32_t* row_dst = row_dst_all + my * kTileRows;
+    const int32_t oob_row = (int32_t)(tm_rows);  // first row past q: zero fill
     int64_t bk = n_local > 0 ? find_bucket(tile_off, n_b, t_begin) : 0;
-    int64_t bk_pf = bk;  // bucket cursor of the tile being prefetched
-    // L2 prefetch of one tile's query rows (each query's G head rows are one
-    // contiguous G * D * 2-byte run): the gather of that tile, QS tiles later,
-    // then reads from L2 instead of waiting on DRAM with only QS stages in flight
-    auto prefetch_tile = [&](int64_t tile) {
-      if (tile >= t_end) return;
-      while (tile_off[bk_pf + 1] <= tile) ++bk_pf;
-      const int gp = (int)(bk_pf / nb);
-      const int p0 = offsets[bk_pf] + (int)(tile - tile_off[bk_pf]) * qt;
-      const int p1 = min(p0 + qt, offsets[bk_pf + 1]);
-      for (int e = p0 + lane; e < p1; e += 32) {
-        const int64_t t = q0 + (entries[e] >> 4);
-        prefetch_l2_bulk(q + ((size_t)t * H_q + gp * G) * D, (uint32_t)(G * D * 2));
-      }
-    };
-    if (my < n_local) prefetch_tile(t_begin + my);
+    bool armed = false;
+    uint32_t armed_par = 0;
     long long i = 0;
     for (int64_t tile = t_begin; tile < t_end; ++tile, ++i) {
       while (tile_off[bk + 1] <= tile) ++bk;
       if ((int)(i % QS) != my) continue;
-      prefetch_tile(tile + QS);  // this warp's next tile
+      const uint32_t par = (uint32_t)((i / QS) & 1);
       int got = 0;
-      if (lane == 0) got = mbar_wait(&q_empty[my], (uint32_t)(((i / QS) & 1) ^ 1), abort_flag, dg);
+      if (lane == 0) got = mbar_wait(&q_empty[my], par ^ 1, abort_flag, dg);
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
       const int g = (int)(bk / nb);
       const int e0 = offsets[bk] + (int)(tile - tile_off[bk]) * qt;
-      const int e1 = min(e0 + qt, offsets[bk + 1]);
-      const int nrows = (e1 - e0) * G;
+      const int nq = min(qt, offsets[bk + 1] - e0);  // queries in this tile
+      // row metadata for the softmax warps (row r: head r / qt, query r % qt)
       for (int r = lane; r < kTileRows; r += 32) {
-        if (r < nrows) {
-          const int ent = entries[e0 + r / G];
+        const int hi = r / qt, qi = r % qt;
+        if (qi < nq) {
+          const int ent = entries[e0 + qi];
           const int tl = ent >> 4, slot = ent & 15;
           row_t[r] = (int)(q0 + tl);
-          row_dst[r] = (tl * k + slot) * H_q + g * G + r % G;
+          row_dst[r] = (tl * k + slot) * H_q + g * G + hi;
         } else {
           row_t[r] = 0x7FFFFFFF;
           row_dst[r] = -1;
         }
       }
       __syncwarp();
-      constexpr int P16 = D / 8;  // 16-byte pieces per row
-      for (int p = lane; p < kTileRows * P16; p += 32) {
-        const int r = p / P16, j16 = p % P16;
-        if (r >= nrows) break;  // rows are filled in order
-        const int c = j16 >> 3, j = j16 & 7;
-        const int64_t t = row_t[r];
-        const int h = g * G + r % G;
-        const uint16_t* src = q + ((size_t)t * H_q + h) * D + c * 64 + j * 8;
-        cp_async16(qbuf + c * kTileRows * 128 + r * 128 + ((j ^ (r & 7)) << 4), src);
-      }
-      cp_async_wait_all();
-      fence_proxy_async_smem();
+      if (lane == 0) mbar_arrive_expect_tx(&q_full[my], S::kQBytes);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&q_full[my]);
+      // one gather4 per (group of 4 rows, 64-column chunk), spread over the lanes
+      constexpr int NCH = D / 64;
+      for (int job = lane; job < (kTileRows / 4) * NCH; job += 32) {
+        const int r0 = (job / NCH) * 4, c = job % NCH;
+        int32_t y[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int r = r0 + u, hi = r / qt, qi = r % qt;
+          y[u] = qi < nq ? (int32_t)(((int64_t)row_t[r] * H_q + g * G + hi)) : oob_row;
+        }
+        tma_gather4(qbuf + c * kTileRows * 128 + r0 * 128, &tm_q, &q_full[my], c * 64, y[0],
+                    y[1], y[2], y[3]);
+      }
+      armed = true;
+      armed_par = par;
     }
-    cp_async_wait_all();
+    if (lane == 0 && armed && *abort_flag) mbar_drain(&q_full[my], armed_par);
   } else {
     // ---------------------------------------------------------- softmax + epilogue
     // two groups of 4 warps; group wg takes the tiles i with i % 2 == wg, which
@@ -599,6 +596,27 @@ bool make_map_kv(CUtensorMap* m, const void* base, int64_t N, int H, int D) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D bf16 tensor [rows, D] with a one-row box of 64 columns, 128B swizzle (the
+// layout tile::gather4 row gathers use)
+bool make_map_rows(CUtensorMap* m, const void* base, int64_t rows, int D) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess || qr != cudaDriverEntryPointSuccess)
+      return false;
+    fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int n = 0;
   if (!n) {
@@ -615,14 +633,16 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, int64_t N
                          int H_q, int H_kv, int k, float scale_log2, int64_t nb, const AttnWs& ws,
                          int64_t n_b, const Diag& dg, cudaStream_t st) {
   CUtensorMap tk, tv;
-  if (!make_map_kv(&tk, kk, N, H_kv, D) || !make_map_kv(&tv, v, N, H_kv, D))
+  CUtensorMap tq;
+  if (!make_map_kv(&tk, kk, N, H_kv, D) || !make_map_kv(&tv, v, N, H_kv, D) ||
+      !make_map_rows(&tq, q, N * H_q, D))
     return cudaErrorInvalidValue;
   const int smem = AttnSmem<D>::kBytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(attn_tile_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   attn_tile_tc_kernel<D><<<sm_count(), kAttnThreads, smem, st>>>(
-      tk, tv, (const uint16_t*)q, q0, H_q, H_kv, k, scale_log2, nb, ws.entries, ws.offsets,
+      tk, tv, tq, N * H_q, q0, H_q, H_kv, k, scale_log2, nb, ws.entries, ws.offsets,
       ws.tile_off, n_b, ws.part_o, ws.part_lse, dg);
   return cudaGetLastError();
 }
