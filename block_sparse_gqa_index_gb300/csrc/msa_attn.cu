@@ -26,9 +26,15 @@ namespace {
 
 constexpr int kBk = 128;
 constexpr int kTileRows = 128;
-constexpr int kThreads = 256;  // bucketing kernels
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// upper bound on the tiles of a chunk: sum over buckets of ceil(count / qt)
+// <= entries / qt + buckets
+inline int64_t max_tiles(int64_t chunk, int64_t n_b, int H_q, int H_kv, int k) {
+  const int64_t qt = kTileRows / (H_q / H_kv);
+  return (chunk * H_kv * k + qt - 1) / qt + n_b;
+}
 
 // ------------------------------------------------------------ bucketing passes
 // A block id is usable for row (t, g) iff 0 <= id <= t / 128; anything else
@@ -42,15 +48,18 @@ __device__ __forceinline__ bool id_ok(int id, int64_t t, const Diag& dg) {
   return true;
 }
 
+// Counts the queries of every bucket; a slot with no usable block gets no
+// partial record (rec_of = -1).
 __global__ void bucket_count_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1,
                                     int n_g, int k, int64_t nb, int32_t* __restrict__ counts,
-                                    Diag dg) {
+                                    int32_t* __restrict__ rec_of, Diag dg) {
   int64_t n = (q1 - q0) * n_g * k;
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
        e += (int64_t)gridDim.x * blockDim.x) {
     int64_t row = q0 * n_g + e / k;  // (t, g) row
     int id = ids[row * k + e % k];
     if (id_ok(id, row / n_g, dg)) atomicAdd(&counts[(row % n_g) * nb + id], 1);
+    else rec_of[e] = -1;
   }
 }
 
@@ -93,10 +102,15 @@ __global__ void bucket_scan_kernel(const int32_t* __restrict__ counts, int64_t n
   }
 }
 
+// Places every (query, slot) of a bucket: its entry (query << 4 | slot) at the
+// bucket's next position, and the index of its partial record, which is the
+// tile-major position tile * qt + (query's place in its tile).
 __global__ void bucket_fill_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1,
-                                   int n_g, int k, int64_t nb,
+                                   int n_g, int k, int64_t nb, int qt,
                                    const int32_t* __restrict__ offsets,
-                                   int32_t* __restrict__ cursor, int32_t* __restrict__ entries) {
+                                   const int32_t* __restrict__ tile_off,
+                                   int32_t* __restrict__ cursor, int32_t* __restrict__ entries,
+                                   int32_t* __restrict__ rec_of) {
   const Diag none{nullptr, 0};
   int64_t n = (q1 - q0) * n_g * k;
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
@@ -106,27 +120,36 @@ __global__ void bucket_fill_kernel(const int32_t* __restrict__ ids, int64_t q0, 
     int id = ids[row * k + slot];
     if (!id_ok(id, row / n_g, none)) continue;
     int64_t bk = (row % n_g) * nb + id;
-    int pos = offsets[bk] + atomicAdd(&cursor[bk], 1);
-    entries[pos] = (int32_t)(((row / n_g - q0) << 4) | slot);
+    const int c = atomicAdd(&cursor[bk], 1);
+    entries[offsets[bk] + c] = (int32_t)(((row / n_g - q0) << 4) | slot);
+    rec_of[e] = tile_off[bk] * qt + c;
   }
 }
 
 // ------------------------------------------------------- tile kernel (tcgen05)
 // One persistent CTA per SM walks a contiguous range of tiles (consecutive
-// tiles mostly share a bucket, so K / V of the bucket's block are loaded once):
-//   warp 0     TMA: K and V of the bucket's block (128 keys, head g) when the
-//              bucket changes (single buffer, released after the bucket's
-//              last P.V MMA);
-//   warp 1     TMEM owner and MMA issuer: S = Q K^T (128 x 128, A = Q tile,
-//              B = K block, both K-major 128B-swizzled in shared memory), then,
-//              once softmax wrote P, O = P V (A = P read from TMEM, B = V as an
-//              MN-major operand). Two TMEM stages of 256 columns (S/P | O); the
-//              S MMA of tile i+1 is issued before the P.V MMA of tile i;
-//   warps 2-5  Q producers, one per Q stage (4 stages): gather the G head rows
-//              of each of the tile's queries with 16-byte cp.async into the
-//              128B-swizzled layout, record each row's query position and
-//              partial slot, then publish the stage;
-//   warps 6-9  softmax + epilogue, one score row per thread: masked row max,
+// tiles mostly share a bucket, so K / V of the bucket's block are loaded once).
+// Every role finds its tile through the tile's record (one 16-byte load,
+// fetched ahead of use). Two TMEM stages of 256 columns (S/P | O) alternate
+// between consecutive tiles.
+//   warp 0     K / V by TMA when the bucket changes (128 keys of head g; single
+//              buffer, freed by the bucket's last P.V), then S = Q K^T
+//              (128 x 128, A = Q tile, B = K block, both K-major and
+//              128B-swizzled in shared memory) into the tile's S/P columns as
+//              soon as the P.V that last read them has completed;
+//   warp 1     TMEM owner; O = P V (A = P read from TMEM, B = V as an MN-major
+//              operand) once the softmax has written P and the epilogue two
+//              tiles back has read the O columns. Splitting the two MMA streams
+//              over two threads lets each block on its own barriers;
+//   warps 2-5  Q producers: warp p fills the Q stages of the tiles i with
+//              i % 4 == p (stage i % 5). It reads the tile's entries before
+//              waiting for the stage, then gathers the G head rows of each of
+//              the tile's queries with TMA row gathers (tile::gather4) into the
+//              128B-swizzled layout; a stage is free again as soon as the S MMA
+//              that read it has completed;
+//   warps 6-13 softmax + epilogue, two groups of four warps (one per TMEM
+//              stage), one score row per thread: the row's query and partial
+//              slot come straight from the tile's entries; masked row max,
 //              exp2, row sum, P (bf16) back into TMEM over S; then O / l in
 //              bf16 and the row's LSE to the partial buffers.
 template <int D>
@@ -137,14 +160,20 @@ struct AttnSmem {
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKVBytes;
   static constexpr int kQOff = 2 * kKVBytes;
-  static constexpr int kMetaOff = kQOff + kQStages * kQBytes;  // row_t, row_dst per stage
-  static constexpr int kBarOff = kMetaOff + kQStages * kTileRows * 8;
-  // kv_full, kv_empty, q_full[4], q_empty[4], s_full[2], p_full[2], o_full[2], t_empty[2], done
-  static constexpr int kNumBars = 2 + 2 * kQStages + 8 + 1;
-  static constexpr int kBytes = kBarOff + kNumBars * 8 + 16;
+  static constexpr int kStgOff = kQOff + kQStages * kQBytes;
+  static constexpr int kStgBytes = kTileRows * D * 2 + kTileRows * 16;  // a tile's records (G = 1)
+  static constexpr int kBarOff = kStgOff + kStgBytes;
+  // kv_full, kv_empty, q_full[4], q_empty[4], s_full[2], p_full[2], o_full[2], o_empty[2],
+  // done[2], stg_empty[2], stg_full
+  static constexpr int kNumBars = 2 + 2 * kQStages + 8 + 2 + 3;
+  static constexpr int kBytes = kBarOff + kNumBars * 8 + 32;
 };
+// the kernel needs its dynamic shared memory 1024-byte aligned (it checks)
+static_assert(AttnSmem<128>::kBytes <= 232448, "attention tile exceeds shared memory");
 
-constexpr int kAttnThreads = 448;  // 14 warps
+constexpr int kProducers = 4;      // Q producer warps
+constexpr int kStoreWarp = 14;     // bulk stores of the partial records
+constexpr int kAttnThreads = 480;  // 15 warps
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -162,22 +191,38 @@ __device__ __forceinline__ int64_t find_bucket(const int32_t* __restrict__ tile_
   return lo;
 }
 
+// One record per tile, so that every role of the tile kernel finds its tile
+// with one independent load: {block b, first entry, queries | group g << 8,
+// end tile of the bucket}.
+__global__ void tile_map_kernel(const int32_t* __restrict__ tile_off,
+                                const int32_t* __restrict__ offsets, int64_t n_b, int64_t nb,
+                                int qt, int4* __restrict__ tinfo) {
+  const int64_t total = tile_off[n_b];
+  for (int64_t tile = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; tile < total;
+       tile += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t bk = find_bucket(tile_off, n_b, tile);
+    const int e0 = offsets[bk] + (int)(tile - tile_off[bk]) * qt;
+    tinfo[tile] = make_int4((int)(bk % nb), e0, min(qt, offsets[bk + 1] - e0) | (int)(bk / nb) << 8,
+                            tile_off[bk + 1]);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_q, int64_t tm_rows,
                     int64_t q0, int H_q, int H_kv, int k,
                     float scale_log2, int64_t nb, const int32_t* __restrict__ entries,
-                    const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_off,
-                    int64_t n_b, uint16_t* __restrict__ part_o, float* __restrict__ part_lse,
-                    Diag dg) {
+                    const int4* __restrict__ tinfo, const int32_t* __restrict__ n_tiles,
+                    unsigned char* __restrict__ part, Diag dg) {
   using namespace sm100;
   using S = AttnSmem<D>;
   constexpr int QS = S::kQStages;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  int32_t* row_t_all = reinterpret_cast<int32_t*>(smem + S::kMetaOff);
-  int32_t* row_dst_all = row_t_all + QS * kTileRows;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  if (smem_u32(smem) & 1023) {  // the 128B-swizzled operands need 1024-byte alignment
+    if (threadIdx.x == 0) report(dg, kStatusUnsupported);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
@@ -186,29 +231,42 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   uint64_t* s_full = q_empty + QS;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_full = p_full + 2;
-  uint64_t* t_empty = o_full + 2;
-  uint64_t* done_bar = t_empty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kNumBars);
+  uint64_t* o_empty = o_full + 2;
+  uint64_t* done_bar = o_empty + 2;
+  // stg_empty[i & 1] completes when tile i's records have been read out of the
+  // staging buffer. Two barriers, because a group can reach tile i + 2 before
+  // tile i's copy is done: a single barrier's parity would then be ambiguous.
+  uint64_t* stg_empty = done_bar + 2;
+  uint64_t* stg_full = stg_empty + 2;
+  // last local tile of the bucket whose K / V are loaded in epoch e (slot e & 1)
+  int32_t* kv_last = reinterpret_cast<int32_t*>(bars + S::kNumBars);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(kv_last + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = H_q / H_kv;
   const int qt = kTileRows / G;
+  const int q0i = (int)q0;
+  const int rec = attn_rec_bytes(G, D);
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
     for (int s = 0; s < QS; ++s) {
       mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1 + 4);  // S-MMA commit + the owning softmax group's 4 warps
+      mbar_init(&q_empty[s], 1);  // the S-MMA commit
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 4);
       mbar_init(&o_full[s], 1);
-      mbar_init(&t_empty[s], 4);
+      mbar_init(&o_empty[s], 4);
     }
-    mbar_init(done_bar, 1);
+    mbar_init(&done_bar[0], 1);
+    mbar_init(&done_bar[1], 1);
+    mbar_init(&stg_empty[0], 1);
+    mbar_init(&stg_empty[1], 1);
+    mbar_init(stg_full, 4);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_k);
@@ -222,195 +280,221 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const uint32_t tmem_base = *tmem_holder;
 
   // this CTA's contiguous range of tiles
-  const int64_t total = tile_off[n_b];
-  const int64_t t_begin = total * blockIdx.x / gridDim.x;
-  const int64_t t_end = total * (blockIdx.x + 1) / gridDim.x;
-  const long long n_local = t_end - t_begin;
+  const int64_t total = *n_tiles;
+  const int t_begin = (int)(total * blockIdx.x / gridDim.x);
+  const int t_end = (int)(total * (blockIdx.x + 1) / gridDim.x);
+  const int n_local = t_end - t_begin;
+  const int4 kNone = make_int4(0, 0, 0, 0);
 
   if (warp == 0) {
-    // ---------------------------------------------------------- K / V loads
-    if (lane == 0 && n_local > 0) {
-      int64_t bk = find_bucket(tile_off, n_b, t_begin), prev = -1;
-      uint32_t epoch = 0;
-      bool ok = true;
-      for (int64_t tile = t_begin; tile < t_end && ok; ++tile) {
-        while (tile_off[bk + 1] <= tile) ++bk;
-        if (bk == prev) continue;
-        if (!mbar_wait(kv_empty, (epoch & 1) ^ 1, abort_flag, dg)) { ok = false; break; }
-        const int g = (int)(bk / nb);
-        const int32_t key0 = (int32_t)((bk % nb) * kBk);
-        mbar_arrive_expect_tx(kv_full, 2 * S::kKVBytes);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(smem + S::kKOff + c * kBk * 128, &tm_k, kv_full, c * 64, g, key0);
-          tma_load_3d(smem + S::kVOff + c * kBk * 128, &tm_v, kv_full, c * 64, g, key0);
-        }
-        prev = bk;
-        ++epoch;
-      }
-      if (!ok && epoch > 0) mbar_drain(kv_full, (epoch - 1) & 1);
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    // Event loop: issue S(next) when its TMEM stage, Q stage and K/V are ready,
-    // and P.V(pending) when its softmax has written P, whichever comes first.
+    // ---------------------------------------------------------- K / V + S = Q K^T
+    // Per K/V block (the next one starts at this block's end tile): wait until
+    // the last P.V of the previous block has completed, load K and V by TMA.
+    // Per tile j: S(j) overwrites the S/P columns of TMEM stage j & 1, so it
+    // waits for P.V(j - 2) to have completed, and for its Q stage.
     if (lane == 0 && n_local > 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBk);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
-      const uint32_t k_base = smem_u32(smem + S::kKOff), v_base = smem_u32(smem + S::kVOff);
+      const uint32_t k_base = smem_u32(smem + S::kKOff);
       const uint32_t q_base = smem_u32(smem + S::kQOff);
-      int64_t bk_s = find_bucket(tile_off, n_b, t_begin), bk_o = bk_s, cur = -1;
       uint32_t epoch = 0;
-      long long si = 0, oi = 0, idle = 0;
-      while (oi < n_local) {
-        bool prog = false;
-        if (si < n_local) {
-          const int64_t tile = t_begin + si;
-          while (tile_off[bk_s + 1] <= tile) ++bk_s;
-          bool ready = true;
-          if (bk_s != cur) {  // new K/V: every P.V of the old block must be issued first
-            ready = oi == si && mbar_test(kv_full, epoch & 1);
-            if (ready) { cur = bk_s; ++epoch; }
+      int s_last = -1;
+      int4 inf = tinfo[t_begin];
+      for (int j = 0; j < n_local; ++j) {
+        if (j > s_last) {
+          s_last = min(inf.w - t_begin, n_local) - 1;
+          const int4 nxt = s_last + 1 < n_local ? tinfo[t_begin + s_last + 1] : kNone;
+          if (!mbar_wait(kv_empty, (epoch & 1) ^ 1, abort_flag, dg)) break;
+          kv_last[epoch & 1] = s_last;
+          const int g = inf.z >> 8;
+          const int32_t key0 = inf.x * kBk;
+          mbar_arrive_expect_tx(kv_full, 2 * S::kKVBytes);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_3d(smem + S::kKOff + c * kBk * 128, &tm_k, kv_full, c * 64, g, key0);
+            tma_load_3d(smem + S::kVOff + c * kBk * 128, &tm_v, kv_full, c * 64, g, key0);
           }
-          const int st = (int)(si & 1);
-          const int qs = (int)(si % QS);
-          if (ready && mbar_test(&t_empty[st], (uint32_t)(((si >> 1) & 1) ^ 1)) &&
-              mbar_test(&q_full[qs], (uint32_t)((si / QS) & 1))) {
-            tc_fence_after();
-            const uint32_t d_s = tmem_base + (uint32_t)(st * 256);
-            const uint32_t qa = q_base + qs * S::kQBytes;
+          ++epoch;
+          inf = nxt;
+          if (!mbar_wait(kv_full, (epoch - 1) & 1, abort_flag, dg)) break;
+        }
+        const int st = j & 1, qs = j % QS;
+        if ((j >= 2 && !mbar_wait(&o_full[st], (uint32_t)(((j - 2) >> 1) & 1), abort_flag, dg)) ||
+            !mbar_wait(&q_full[qs], (uint32_t)((j / QS) & 1), abort_flag, dg))
+          break;
+        tc_fence_after();
+        const uint32_t d_s = tmem_base + (uint32_t)(st * 256);
+        const uint32_t qa = q_base + qs * S::kQBytes;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const int c = kk / 4, off = (kk % 4) * 32;
-              mma_bf16_ss(d_s, desc_kmajor_sw128(qa + c * kTileRows * 128 + off),
-                          desc_kmajor_sw128(k_base + c * kBk * 128 + off), idesc_s,
-                          kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&s_full[st]);
-            mma_commit(&q_empty[qs]);
-            ++si;
-            prog = true;
-          }
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int c = kk / 4, off = (kk % 4) * 32;
+          mma_bf16_ss(d_s, desc_kmajor_sw128(qa + c * kTileRows * 128 + off),
+                      desc_kmajor_sw128(k_base + c * kBk * 128 + off), idesc_s, kk > 0 ? 1u : 0u);
         }
-        if (oi < si) {
-          const int st = (int)(oi & 1);
-          if (mbar_test(&p_full[st], (uint32_t)((oi >> 1) & 1))) {
-            tc_fence_after();
-            const uint32_t d_o = tmem_base + (uint32_t)(st * 256 + 128);
-#pragma unroll
-            for (int kk = 0; kk < kBk / 16; ++kk) {
-              const uint32_t a_p = tmem_base + (uint32_t)(st * 256 + kk * 8);
-              const uint64_t bd = desc_mnmajor_sw128(v_base + kk * 16 * 128, kBk * 128);
-              mma_bf16_ts(d_o, a_p, bd, idesc_o, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&o_full[st]);
-            const int64_t tile = t_begin + oi;
-            while (tile_off[bk_o + 1] <= tile) ++bk_o;
-            if (oi + 1 == n_local || tile_off[bk_o + 1] <= tile + 1) mma_commit(kv_empty);
-            ++oi;
-            prog = true;
-          }
-        }
-        if (prog) {
-          idle = 0;
-        } else {
-          if (*abort_flag) break;
-          if (++idle > dg.wait_limit) {
-            *abort_flag = 1;
-            report(dg, kStatusTimeout);
-            break;
-          }
-        }
+        mma_commit(&s_full[st]);
+        mma_commit(&q_empty[qs]);
       }
-      mma_commit(done_bar);
-      mbar_drain(done_bar, 0);
+      if (*abort_flag && epoch > 0) mbar_drain(kv_full, (epoch - 1) & 1);
+      mma_commit(&done_bar[0]);
+      mbar_drain(&done_bar[0], 0);
     }
-  } else if (warp < 6) {
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- O = P V
+    // Per tile j, once its softmax has written P: P.V(j) overwrites the O
+    // columns of TMEM stage j & 1, so it waits for the epilogue of tile j - 2
+    // to have read them. The last P.V of a K/V block frees the K/V buffer.
+    if (lane == 0 && n_local > 0) {
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      const uint32_t v_base = smem_u32(smem + S::kVOff);
+      uint32_t epoch = 0;
+      int o_last = -1;
+      for (int j = 0; j < n_local; ++j) {
+        if (j > o_last) {
+          if (!mbar_wait(kv_full, epoch & 1, abort_flag, dg)) break;
+          o_last = kv_last[epoch & 1];
+          ++epoch;
+        }
+        const int st = j & 1;
+        if (!mbar_wait(&p_full[st], (uint32_t)((j >> 1) & 1), abort_flag, dg) ||
+            (j >= 2 && !mbar_wait(&o_empty[st], (uint32_t)(((j - 2) >> 1) & 1), abort_flag, dg)))
+          break;
+        tc_fence_after();
+        const uint32_t d_o = tmem_base + (uint32_t)(st * 256 + 128);
+#pragma unroll
+        for (int kk = 0; kk < kBk / 16; ++kk) {
+          const uint32_t a_p = tmem_base + (uint32_t)(st * 256 + kk * 8);
+          const uint64_t bd = desc_mnmajor_sw128(v_base + kk * 16 * 128, kBk * 128);
+          mma_bf16_ts(d_o, a_p, bd, idesc_o, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&o_full[st]);
+        if (j == o_last) mma_commit(kv_empty);
+      }
+      mma_commit(&done_bar[1]);
+      mbar_drain(&done_bar[1], 0);
+    }
+  } else if (warp < 2 + kProducers) {
     // ---------------------------------------------------------- Q producers
     // Tile rows are head-major: row r holds head i = r / qt of query r % qt, so
     // four consecutive rows are one head of four queries, fetched by one TMA
     // row gather (tile::gather4) per 64-column chunk. Rows past the tile's
-    // queries use an out-of-range row and are zero-filled.
-    const int my = warp - 2;  // Q stage owned by this warp
-    unsigned char* qbuf = smem + S::kQOff + my * S::kQBytes;
-    int32_t* row_t = row_t_all + my * kTileRows;
-    int32_t* row_dst = row_dst_all + my * kTileRows;
+    // queries use an out-of-range row and are zero-filled. Lane l holds the
+    // entries of queries l, l + 32, ... of the tile; the gathers pick up their
+    // rows by shuffles. A tile's entries are loaded one iteration ahead and its
+    // record two iterations ahead, so no global load is waited on here.
+    const int p = warp - 2;
     const int32_t oob_row = (int32_t)(tm_rows);  // first row past q: zero fill
-    int64_t bk = n_local > 0 ? find_bucket(tile_off, n_b, t_begin) : 0;
-    bool armed = false;
-    uint32_t armed_par = 0;
-    long long i = 0;
-    for (int64_t tile = t_begin; tile < t_end; ++tile, ++i) {
-      while (tile_off[bk + 1] <= tile) ++bk;
-      if ((int)(i % QS) != my) continue;
+    const int nj = (qt + 31) / 32;
+    constexpr int NCH = D / 64;
+    uint32_t armed = 0, armed_par = 0;  // per-stage bits: issued a copy, its parity
+    int i = p;
+    int4 inf_c = i < n_local ? tinfo[t_begin + i] : kNone;
+    int ent_c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      ent_c[j] = (i < n_local && j < nj && lane + 32 * j < (inf_c.z & 0xFF))
+                     ? entries[inf_c.y + lane + 32 * j] : -1;
+    int4 inf_n = i + kProducers < n_local ? tinfo[t_begin + i + kProducers] : kNone;
+    bool stop = false;
+    for (; i < n_local && !stop; i += kProducers) {
+      int ent_n[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ent_n[j] = (i + kProducers < n_local && j < nj && lane + 32 * j < (inf_n.z & 0xFF))
+                       ? entries[inf_n.y + lane + 32 * j] : -1;
+      const int4 inf_nn = i + 2 * kProducers < n_local ? tinfo[t_begin + i + 2 * kProducers] : kNone;
+      const int gg = (inf_c.z >> 8) * G;
+      int32_t qrow[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        qrow[j] = ent_c[j] >= 0 ? (int32_t)((q0 + (ent_c[j] >> 4)) * H_q + gg) : -1;
+      const int qs = (int)(i % QS);
       const uint32_t par = (uint32_t)((i / QS) & 1);
       int got = 0;
-      if (lane == 0) got = mbar_wait(&q_empty[my], par ^ 1, abort_flag, dg);
+      if (lane == 0) got = mbar_wait(&q_empty[qs], par ^ 1, abort_flag, dg);
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
-      const int g = (int)(bk / nb);
-      const int e0 = offsets[bk] + (int)(tile - tile_off[bk]) * qt;
-      const int nq = min(qt, offsets[bk + 1] - e0);  // queries in this tile
-      // row metadata for the softmax warps (row r: head r / qt, query r % qt)
-      for (int r = lane; r < kTileRows; r += 32) {
-        const int hi = r / qt, qi = r % qt;
-        if (qi < nq) {
-          const int ent = entries[e0 + qi];
-          const int tl = ent >> 4, slot = ent & 15;
-          row_t[r] = (int)(q0 + tl);
-          row_dst[r] = (tl * k + slot) * H_q + g * G + hi;
-        } else {
-          row_t[r] = 0x7FFFFFFF;
-          row_dst[r] = -1;
-        }
-      }
+      if (lane == 0) mbar_arrive_expect_tx(&q_full[qs], S::kQBytes);
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&q_full[my], S::kQBytes);
-      __syncwarp();
-      // one gather4 per (group of 4 rows, 64-column chunk), spread over the lanes
-      constexpr int NCH = D / 64;
+      unsigned char* qbuf = smem + S::kQOff + qs * S::kQBytes;
+      // one gather4 per (group of 4 rows, 64-column chunk); 32 * NCH jobs, so
+      // every lane runs the same number of iterations (the shuffles need it)
       for (int job = lane; job < (kTileRows / 4) * NCH; job += 32) {
         const int r0 = (job / NCH) * 4, c = job % NCH;
+        const int hi = r0 / qt, qb = r0 % qt, jj = qb >> 5;
         int32_t y[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int r = r0 + u, hi = r / qt, qi = r % qt;
-          y[u] = qi < nq ? (int32_t)(((int64_t)row_t[r] * H_q + g * G + hi)) : oob_row;
+          const int src = (qb + u) & 31;
+          int32_t v = -1;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j < nj) {
+              const int32_t x = __shfl_sync(0xffffffffu, qrow[j], src);
+              if (j == jj) v = x;
+            }
+          }
+          y[u] = v >= 0 ? v + hi : oob_row;
         }
-        tma_gather4(qbuf + c * kTileRows * 128 + r0 * 128, &tm_q, &q_full[my], c * 64, y[0],
+        tma_gather4(qbuf + c * kTileRows * 128 + r0 * 128, &tm_q, &q_full[qs], c * 64, y[0],
                     y[1], y[2], y[3]);
       }
-      armed = true;
-      armed_par = par;
+      armed |= 1u << qs;
+      armed_par = (armed_par & ~(1u << qs)) | (par << qs);
+      stop = *abort_flag != 0;
+      inf_c = inf_n;
+      inf_n = inf_nn;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ent_c[j] = ent_n[j];
     }
-    if (lane == 0 && armed && *abort_flag) mbar_drain(&q_full[my], armed_par);
+    // on abort, let every copy this warp issued land before shared memory goes
+    if (lane == 0 && *abort_flag) {
+#pragma unroll
+      for (int s = 0; s < QS; ++s)
+        if ((armed >> s) & 1) mbar_drain(&q_full[s], (armed_par >> s) & 1);
+    }
+  } else if (warp == kStoreWarp) {
+    // ---------------------------------------------------------- partial records out
+    // Tile i's records (its first nq queries, contiguous in the staging buffer)
+    // go out in one bulk copy to their tile-major place once the four warps of
+    // the tile's softmax group have written them; the buffer is free again once
+    // the copy has read it.
+    if (lane == 0 && n_local > 0) {
+      int4 inf = tinfo[t_begin];
+      for (int i = 0; i < n_local; ++i) {
+        const int4 nxt = i + 1 < n_local ? tinfo[t_begin + i + 1] : kNone;
+        if (!mbar_wait(stg_full, (uint32_t)(i & 1), abort_flag, dg)) break;
+        bulk_store(part + (size_t)(t_begin + i) * qt * rec, smem + S::kStgOff,
+                   (uint32_t)((inf.z & 0xFF) * rec));
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(&stg_empty[i & 1]);
+        inf = nxt;
+      }
+    }
   } else {
     // ---------------------------------------------------------- softmax + epilogue
     // two groups of 4 warps; group wg takes the tiles i with i % 2 == wg, which
-    // use TMEM stage wg, so one group's softmax overlaps the other's epilogue
-    const int wg = (warp - 6) >> 2;
+    // use TMEM stage wg, so one group's softmax overlaps the other's epilogue.
+    // A row's entry is loaded one tile ahead, the tile record two tiles ahead.
+    const int wg = (warp - 2 - kProducers) >> 2;
     const int qq = warp & 3;
     const int row = qq * 32 + lane;
+    const int hi = row / qt, qi = row % qt;
     const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
     const int st = wg;
     const uint32_t ts = tmem_base + lane_off + (uint32_t)(st * 256);
-    int64_t bk = n_local > 0 ? find_bucket(tile_off, n_b, t_begin) : 0;
-    for (long long i = wg; i < n_local; i += 2) {
-      const int64_t tile = t_begin + i;
-      while (tile_off[bk + 1] <= tile) ++bk;
-      const int64_t b = bk % nb;
+    const uint32_t stg_base = smem_u32(smem + S::kStgOff);
+    int4 inf_c = wg < n_local ? tinfo[t_begin + wg] : kNone;
+    int ent_c = (wg < n_local && qi < (inf_c.z & 0xFF)) ? entries[inf_c.y + qi] : -1;
+    int4 inf_n = wg + 2 < n_local ? tinfo[t_begin + wg + 2] : kNone;
+    for (int i = wg; i < n_local; i += 2) {
+      const int ent_n = (i + 2 < n_local && qi < (inf_n.z & 0xFF)) ? entries[inf_n.y + qi] : -1;
+      const int4 inf_nn = i + 4 < n_local ? tinfo[t_begin + i + 4] : kNone;
+      const int b = inf_c.x;
       const uint32_t par = (uint32_t)((i >> 1) & 1);
-      const int qs = (int)(i % QS);
-      // q_full: acquire the producer's row metadata; s_full: scores are in TMEM
+      const int t = ent_c >= 0 ? q0i + (ent_c >> 4) : 0;
       int got = 0;
-      if (lane == 0)
-        got = mbar_wait(&q_full[qs], (uint32_t)((i / QS) & 1), abort_flag, dg) &&
-              mbar_wait(&s_full[st], par, abort_flag, dg);
+      if (lane == 0) got = mbar_wait(&s_full[st], par, abort_flag, dg);
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
-      const int64_t t = row_t_all[qs * kTileRows + row];
-      const int dst = row_dst_all[qs * kTileRows + row];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_empty[qs]);
       tc_fence_after();
-      const int lim = (dst >= 0 && t / kBk == b) ? (int)(t - b * kBk) + 1 : kBk;
+      const int lim = (ent_c >= 0 && t / kBk == b) ? t - b * kBk + 1 : kBk;
       // pass 1: row max
       float m = -INFINITY;
 #pragma unroll
@@ -455,34 +539,42 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[st]);
-      // O epilogue
+      // O epilogue: O / l in bf16 and the LSE into this tile's records in the
+      // staging buffer (shared by both groups, taken in tile order), then one
+      // bulk copy per query of its record to the partial buffer
       got = 0;
-      if (lane == 0) got = mbar_wait(&o_full[st], par, abort_flag, dg);
+      if (lane == 0)
+        got = mbar_wait(&o_full[st], par, abort_flag, dg) &&
+              (i == 0 ||
+               mbar_wait(&stg_empty[(i - 1) & 1], (uint32_t)(((i - 1) >> 1) & 1), abort_flag, dg));
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
       tc_fence_after();
       const float inv = 1.f / l;
+      const uint32_t srow = stg_base + (uint32_t)(qi * rec + hi * D * 2);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(ts + 128 + c * 32, r);
         tmem_ld_wait();
-        if (dst >= 0) {
-          uint4* o = reinterpret_cast<uint4*>(part_o + (size_t)dst * D + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
-            __stcs(o + v, w);
-          }
-        }
+        for (int v = 0; v < 4; ++v)
+          st_shared_v4(srow + c * 64 + v * 16,
+                       pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
+                       pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
+                       pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
+                       pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
       }
-      if (dst >= 0) part_lse[dst] = (mc + __log2f(l)) * 0.69314718055994531f;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&t_empty[st]);
+      if (lane == 0) mbar_arrive(&o_empty[st]);  // the O columns are free again
+      *reinterpret_cast<float*>(smem + S::kStgOff + qi * rec + G * D * 2 + hi * 4) =
+          (mc + __log2f(l)) * 0.69314718055994531f;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(stg_full);
+      inf_c = inf_n;
+      inf_n = inf_nn;
+      ent_c = ent_n;
     }
   }
   tc_fence_before();
@@ -492,22 +584,24 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 }
 
 // ---------------------------------------------------------------------- merge
-// partials: part_o [rows, k, H_q, D] bf16, part_lse [rows, k, H_q]. Each half
-// warp merges one (query, head): lane s < k holds slot s's LSE, max and sum come
-// from shuffles within the half, and the k slot loads (16 bytes per lane for
-// D = 128) are all issued before they are summed. The two halves take adjacent
-// heads, so each slot read is one contiguous 2 * D * 2-byte run.
+// partials: one record per (query, group, slot) holding the G heads' O rows
+// (bf16) and then their LSEs, found through rec_of (-1: the slot has none).
+// Each half warp merges one (query, head): lane s < k holds slot s's LSE, max
+// and sum come from shuffles within the half, and the k slot loads (16 bytes
+// per lane for D = 128) are all issued before they are summed. The two halves
+// take adjacent heads, so with G > 1 each slot read is one contiguous
+// 2 * D * 2-byte run.
 template <int D>
 __global__ void __launch_bounds__(256)
-attn_merge_kernel(const uint16_t* __restrict__ part_o, const float* __restrict__ part_lse,
-                  const int32_t* __restrict__ ids, int64_t q0, int64_t q1, int H_q, int H_kv,
-                  int k, uint16_t* __restrict__ out, float* __restrict__ lse) {
+attn_merge_kernel(const unsigned char* __restrict__ part, const int32_t* __restrict__ rec_of,
+                  int64_t q0, int64_t q1, int H_q, int H_kv, int k, uint16_t* __restrict__ out,
+                  float* __restrict__ lse) {
   constexpr int PER = D / 16;  // elements per lane (8 or 4)
   const int lane = threadIdx.x & 31;
   const int hl = lane & 15;          // lane within the half warp
   const int G = H_q / H_kv;
+  const int rec = attn_rec_bytes(G, D);
   const int64_t n = (q1 - q0) * H_q;
-  const Diag none{nullptr, 0};
   const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; 2 * w < n; w += warps) {
     const int64_t task = 2 * w + (lane >> 4);
@@ -515,13 +609,13 @@ attn_merge_kernel(const uint16_t* __restrict__ part_o, const float* __restrict__
     const int64_t tk = active ? task : n - 1;
     const int64_t tl = tk / H_q;
     const int h = (int)(tk % H_q);
+    const int g = h / G, hi = h % G;
     const int64_t t = q0 + tl;
-    bool valid = false;
-    float ls = -INFINITY;
-    if (hl < k) {
-      valid = id_ok(ids[((size_t)t * H_kv + h / G) * k + hl], t, none);
-      if (valid) ls = part_lse[((size_t)tl * k + hl) * H_q + h];
-    }
+    const int ri = hl < k ? rec_of[((size_t)tl * H_kv + g) * k + hl] : -1;
+    const bool valid = ri >= 0;
+    const float ls =
+        valid ? *reinterpret_cast<const float*>(part + (size_t)ri * rec + G * D * 2 + hi * 4)
+              : -INFINITY;
     float M = ls;
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off, 16));
@@ -529,8 +623,7 @@ attn_merge_kernel(const uint16_t* __restrict__ part_o, const float* __restrict__
     float L = wl;
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off, 16);
-    const uint16_t* base = part_o + ((size_t)tl * k * H_q + h) * D + hl * PER;
-    const size_t slot_stride = (size_t)H_q * D;
+    const int col = (hi * D + hl * PER) * 2;  // this lane's bytes within a record
     float acc[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) acc[i] = 0.f;
@@ -538,8 +631,9 @@ attn_merge_kernel(const uint16_t* __restrict__ part_o, const float* __restrict__
     for (int s = 0; s < kMaxK; ++s) {
       if (s >= k) break;
       const float wgt = __shfl_sync(0xffffffffu, wl, s, 16);
+      const int rs = __shfl_sync(0xffffffffu, ri, s, 16);
       if (wgt == 0.f) continue;  // invalid or padded slot
-      const uint16_t* po = base + s * slot_stride;
+      const unsigned char* po = part + (size_t)rs * rec + col;
       if (PER == 8) {
         uint4 u = __ldcs(reinterpret_cast<const uint4*>(po));
         const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
@@ -637,13 +731,13 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, int64_t N
   if (!make_map_kv(&tk, kk, N, H_kv, D) || !make_map_kv(&tv, v, N, H_kv, D) ||
       !make_map_rows(&tq, q, N * H_q, D))
     return cudaErrorInvalidValue;
-  const int smem = AttnSmem<D>::kBytes + 1024;
+  const int smem = AttnSmem<D>::kBytes;
   cudaError_t e = cudaFuncSetAttribute(attn_tile_tc_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   attn_tile_tc_kernel<D><<<sm_count(), kAttnThreads, smem, st>>>(
-      tk, tv, tq, N * H_q, q0, H_q, H_kv, k, scale_log2, nb, ws.entries, ws.offsets,
-      ws.tile_off, n_b, ws.part_o, ws.part_lse, dg);
+      tk, tv, tq, N * H_q, q0, H_q, H_kv, k, scale_log2, nb, ws.entries, ws.tinfo,
+      ws.tile_off + n_b, ws.part, dg);
   return cudaGetLastError();
 }
 
@@ -657,8 +751,10 @@ size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k)
   s += align256((size_t)n_b * 4);        // cursor
   s += align256((size_t)(n_b + 1) * 4);  // tile_off
   s += align256((size_t)chunk * H_kv * k * 4);
-  s += align256((size_t)chunk * H_q * k * d * 2);
-  s += align256((size_t)chunk * H_q * k * 4);
+  s += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * 16);
+  s += align256((size_t)chunk * H_kv * k * 4);
+  s += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * (kTileRows / (H_q / H_kv)) *
+                attn_rec_bytes(H_q / H_kv, d));
   return s;
 }
 
@@ -671,8 +767,9 @@ AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int
   w.cursor = (int32_t*)p;   p += align256((size_t)n_b * 4);
   w.tile_off = (int32_t*)p; p += align256((size_t)(n_b + 1) * 4);
   w.entries = (int32_t*)p;  p += align256((size_t)chunk * H_kv * k * 4);
-  w.part_o = (uint16_t*)p;  p += align256((size_t)chunk * H_q * k * d * 2);
-  w.part_lse = (float*)p;
+  w.tinfo = (int4*)p;       p += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * 16);
+  w.rec_of = (int32_t*)p;   p += align256((size_t)chunk * H_kv * k * 4);
+  w.part = p;
   return w;
 }
 
@@ -684,15 +781,18 @@ cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* 
   const int64_t n_b = (int64_t)H_kv * nb;
   const int G = H_q / H_kv;
   const int qt = kTileRows / G;
-  note_launches(6);  // memset, count, scan, fill, tile, merge
+  note_launches(7);  // memset, count, scan, fill, tile map, tile, merge
   cudaError_t e = cudaMemsetAsync(ws.counts, 0, (size_t)n_b * 4, st);
   if (e != cudaSuccess) return e;
   int64_t n = (q1 - q0) * H_kv * k;
   unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 32);
-  bucket_count_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, ws.counts, dg);
+  bucket_count_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, ws.counts, ws.rec_of, dg);
   bucket_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, n_b, qt, ws.offsets, ws.tile_off, ws.cursor);
-  bucket_fill_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, ws.offsets, ws.cursor,
-                                           ws.entries);
+  bucket_fill_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, qt, ws.offsets,
+                                           ws.tile_off, ws.cursor, ws.entries, ws.rec_of);
+  const int64_t tiles_max = max_tiles(q1 - q0, n_b, H_q, H_kv, k);
+  tile_map_kernel<<<(unsigned)std::min<int64_t>((tiles_max + 255) / 256, 152 * 16), 256, 0, st>>>(
+      ws.tile_off, ws.offsets, n_b, nb, qt, ws.tinfo);
   const float scale_log2 = scale * 1.4426950408889634f;
   e = d == 128 ? launch_tiles<128>(q, kk, v, N, q0, H_q, H_kv, k, scale_log2, nb, ws, n_b, dg, st)
                : launch_tiles<64>(q, kk, v, N, q0, H_q, H_kv, k, scale_log2, nb, ws, n_b, dg, st);
@@ -700,10 +800,10 @@ cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* 
   int64_t nw = (q1 - q0) * H_q;
   unsigned mg = (unsigned)std::min<int64_t>((nw * 16 + 255) / 256, 152 * 64);
   if (d == 128)
-    attn_merge_kernel<128><<<mg, 256, 0, st>>>(ws.part_o, ws.part_lse, ids, q0, q1, H_q, H_kv, k,
+    attn_merge_kernel<128><<<mg, 256, 0, st>>>(ws.part, ws.rec_of, q0, q1, H_q, H_kv, k,
                                                (uint16_t*)out, lse);
   else
-    attn_merge_kernel<64><<<mg, 256, 0, st>>>(ws.part_o, ws.part_lse, ids, q0, q1, H_q, H_kv, k,
+    attn_merge_kernel<64><<<mg, 256, 0, st>>>(ws.part, ws.rec_of, q0, q1, H_q, H_kv, k,
                                               (uint16_t*)out, lse);
   return cudaGetLastError();
 }

@@ -8,6 +8,7 @@
 namespace msa {
 
 constexpr int kStatusTimeout = -5;
+constexpr int kStatusUnsupported = -2;  // a kernel could not run as launched (did nothing)
 constexpr int kStatusBadIds = -1;  // invalid block ids / sequence lengths found on the device
 constexpr int kMaxK = 16;        // largest k the kernels are built for
 constexpr int kMaxFar = kMaxK - 1;

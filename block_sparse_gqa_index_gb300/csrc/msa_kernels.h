@@ -33,9 +33,13 @@ struct AttnWs {
   int32_t* cursor;    // [n_g * nb]
   int32_t* tile_off;  // [n_g * nb + 1]
   int32_t* entries;   // [chunk * n_g * k]
-  uint16_t* part_o;   // [chunk, H_q, k, d] bf16
-  float* part_lse;    // [chunk, H_q, k]
+  int4* tinfo;        // per tile: block, first entry, queries | group << 8, end tile
+  int32_t* rec_of;    // [chunk, n_g, k]: partial record of each (query, group, slot), or -1
+  unsigned char* part;  // [tiles, qt] records of attn_rec_bytes(G, d) bytes, tile-major
 };
+// One partial record per (query, group, slot): the G heads' normalised O rows
+// (bf16, d each), then their G LSEs (fp32), padded to a multiple of 16 bytes.
+__host__ __device__ inline int attn_rec_bytes(int G, int d) { return G * d * 2 + (G + 3) / 4 * 16; }
 size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k);
 AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k);
 cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* v,
