@@ -517,23 +517,47 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
       }
       const float mc = m * scale_log2;
-      // pass 2: P = exp2(s * c - m * c) in bf16 over the first 64 columns, row sum
-      float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32], pk[16];
-        tmem_ld32(ts + c * 32, r);
-        tmem_ld_wait();
+      // pass 2: P = exp2(s * c - m * c) in bf16 over the first 64 columns, row
+      // sum; the load of chunk c + 1 is in flight while chunk c is computed.
+      // Rows of the local block mask the columns past their query.
+      const bool full = __all_sync(0xffffffffu, lim >= kBk);
+      const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-mc, -mc);
+      uint64_t l2 = f2_pack(0.f, 0.f);
+      auto p_chunk = [&](const uint32_t(&r)[32], int c) {
+        uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
-          float p0 = c * 32 + j < lim ? ex2_approx(fmaf(__uint_as_float(r[j]), scale_log2, -mc)) : 0.f;
-          float p1 = c * 32 + j + 1 < lim ? ex2_approx(fmaf(__uint_as_float(r[j + 1]), scale_log2, -mc)) : 0.f;
-          l0 += p0;
-          l1 += p1;
+          float p0, p1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), sc2, nm2),
+                    p0, p1);
+          p0 = ex2_approx(p0);
+          p1 = ex2_approx(p1);
+          if (!full) {
+            p0 = c * 32 + j < lim ? p0 : 0.f;
+            p1 = c * 32 + j + 1 < lim ? p1 : 0.f;
+          }
+          l2 = f2_add(l2, f2_pack(p0, p1));
           pk[j >> 1] = pack_bf16x2(p0, p1);
         }
         tmem_st16(ts + c * 16, pk);
+      };
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(ts, ra);
+        tmem_ld_wait();
+        tmem_ld32(ts + 32, rb);
+        p_chunk(ra, 0);
+        tmem_ld_wait();
+        tmem_ld32(ts + 64, ra);
+        p_chunk(rb, 1);
+        tmem_ld_wait();
+        tmem_ld32(ts + 96, rb);
+        p_chunk(ra, 2);
+        tmem_ld_wait();
+        p_chunk(rb, 3);
       }
+      float l0, l1;
+      f2_unpack(l2, l0, l1);
       const float l = l0 + l1;
       tmem_st_wait();
       tc_fence_before();
@@ -550,19 +574,35 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
       tc_fence_after();
       const float inv = 1.f / l;
+      const uint64_t inv2 = f2_pack(inv, inv);
       const uint32_t srow = stg_base + (uint32_t)(qi * rec + hi * D * 2);
+      auto o_chunk = [&](const uint32_t(&r)[32], int c) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(ts + 128 + c * 32, r);
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            float x0, x1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(r[8 * v + 2 * u]),
+                                     __uint_as_float(r[8 * v + 2 * u + 1])), inv2), x0, x1);
+            w[u] = pack_bf16x2(x0, x1);
+          }
+          st_shared_v4(srow + c * 64 + v * 16, w[0], w[1], w[2], w[3]);
+        }
+      };
+      {
+        uint32_t ra[32], rb[32];
+        tmem_ld32(ts + 128, ra);
         tmem_ld_wait();
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          st_shared_v4(srow + c * 64 + v * 16,
-                       pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
-                       pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
-                       pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
-                       pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
+        for (int c = 0; c < D / 32; c += 2) {
+          tmem_ld32(ts + 128 + (c + 1) * 32, rb);
+          o_chunk(ra, c);
+          tmem_ld_wait();
+          if (c + 2 < D / 32) tmem_ld32(ts + 128 + (c + 2) * 32, ra);
+          o_chunk(rb, c + 1);
+          if (c + 2 < D / 32) tmem_ld_wait();
+        }
       }
       tc_fence_before();
       __syncwarp();
