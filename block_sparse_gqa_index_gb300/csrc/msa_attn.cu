@@ -132,26 +132,31 @@ __global__ void bucket_fill_kernel(const int32_t* __restrict__ ids, int64_t q0, 
 // Every role finds its tile through the tile's record (one 16-byte load,
 // fetched ahead of use). Two TMEM stages of 256 columns (S/P | O) alternate
 // between consecutive tiles.
-//   warp 0     K / V by TMA when the bucket changes (128 keys of head g; single
-//              buffer, freed by the bucket's last P.V), then S = Q K^T
-//              (128 x 128, A = Q tile, B = K block, both K-major and
+//   warp 0     K by TMA when the bucket changes (128 keys of head g; single
+//              buffer, reloaded once the bucket's last S has completed), then
+//              S = Q K^T (128 x 128, A = Q tile, B = K block, both K-major and
 //              128B-swizzled in shared memory) into the tile's S/P columns as
 //              soon as the P.V that last read them has completed;
-//   warp 1     TMEM owner; O = P V (A = P read from TMEM, B = V as an MN-major
-//              operand) once the softmax has written P and the epilogue two
-//              tiles back has read the O columns. Splitting the two MMA streams
-//              over two threads lets each block on its own barriers;
-//   warps 2-5  Q producers: warp p fills the Q stages of the tiles i with
-//              i % 4 == p (stage i % 5). It reads the tile's entries before
-//              waiting for the stage, then gathers the G head rows of each of
-//              the tile's queries with TMA row gathers (tile::gather4) into the
-//              128B-swizzled layout; a stage is free again as soon as the S MMA
-//              that read it has completed;
+//   warp 1     TMEM owner; V by TMA when the bucket changes (reloaded once the
+//              bucket's last P.V has completed), then O = P V (A = P read from
+//              TMEM, B = V as an MN-major operand) once the softmax has written
+//              P and the epilogue two tiles back has read the O columns.
+//              Splitting the two MMA streams over two threads lets each block
+//              on its own barriers;
+//   warps 2-5  Q producers: warp p fills the Q stage i % 4 of the tiles i with
+//              i % 4 == p. It reads the tile's entries ahead of time, then
+//              gathers the G head rows of each of the tile's queries with TMA
+//              row gathers (tile::gather4) into the 128B-swizzled layout; a
+//              stage is free again as soon as the S MMA that read it completed;
 //   warps 6-13 softmax + epilogue, two groups of four warps (one per TMEM
 //              stage), one score row per thread: the row's query and partial
 //              slot come straight from the tile's entries; masked row max,
 //              exp2, row sum, P (bf16) back into TMEM over S; then O / l in
-//              bf16 and the row's LSE to the partial buffers.
+//              bf16 and the row's LSE into the tile's partial records in a
+//              shared-memory staging buffer;
+//   warp 14    one bulk copy per tile of its records (tile-major, so a tile's
+//              records are contiguous) from the staging buffer to the partial
+//              buffer.
 template <int D>
 struct AttnSmem {
   static constexpr int kKVBytes = kBk * D * 2;            // one of K or V
@@ -163,9 +168,9 @@ struct AttnSmem {
   static constexpr int kStgOff = kQOff + kQStages * kQBytes;
   static constexpr int kStgBytes = kTileRows * D * 2 + kTileRows * 16;  // a tile's records (G = 1)
   static constexpr int kBarOff = kStgOff + kStgBytes;
-  // kv_full, kv_empty, q_full[4], q_empty[4], s_full[2], p_full[2], o_full[2], o_empty[2],
-  // done[2], stg_empty[2], stg_full
-  static constexpr int kNumBars = 2 + 2 * kQStages + 8 + 2 + 3;
+  // k_full, k_empty, v_full, v_empty, q_full[4], q_empty[4], s_full[2], p_full[2],
+  // o_full[2], o_empty[2], done[2], stg_empty[2], stg_full
+  static constexpr int kNumBars = 4 + 2 * kQStages + 8 + 2 + 3;
   static constexpr int kBytes = kBarOff + kNumBars * 8 + 32;
 };
 // the kernel needs its dynamic shared memory 1024-byte aligned (it checks)
@@ -224,9 +229,11 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
-  uint64_t* kv_full = bars + 0;
-  uint64_t* kv_empty = bars + 1;
-  uint64_t* q_full = bars + 2;
+  uint64_t* k_full = bars + 0;
+  uint64_t* k_empty = bars + 1;
+  uint64_t* v_full = bars + 2;
+  uint64_t* v_empty = bars + 3;
+  uint64_t* q_full = bars + 4;
   uint64_t* q_empty = q_full + QS;
   uint64_t* s_full = q_empty + QS;
   uint64_t* p_full = s_full + 2;
@@ -238,9 +245,7 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   // tile i's copy is done: a single barrier's parity would then be ambiguous.
   uint64_t* stg_empty = done_bar + 2;
   uint64_t* stg_full = stg_empty + 2;
-  // last local tile of the bucket whose K / V are loaded in epoch e (slot e & 1)
-  int32_t* kv_last = reinterpret_cast<int32_t*>(bars + S::kNumBars);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(kv_last + 2);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -250,8 +255,10 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int rec = attn_rec_bytes(G, D);
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    mbar_init(kv_empty, 1);
+    mbar_init(k_full, 1);
+    mbar_init(k_empty, 1);
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
     for (int s = 0; s < QS; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);  // the S-MMA commit
@@ -287,11 +294,11 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int4 kNone = make_int4(0, 0, 0, 0);
 
   if (warp == 0) {
-    // ---------------------------------------------------------- K / V + S = Q K^T
-    // Per K/V block (the next one starts at this block's end tile): wait until
-    // the last P.V of the previous block has completed, load K and V by TMA.
-    // Per tile j: S(j) overwrites the S/P columns of TMEM stage j & 1, so it
-    // waits for P.V(j - 2) to have completed, and for its Q stage.
+    // ---------------------------------------------------------- K + S = Q K^T
+    // Per K/V block (the next one starts at this block's end tile): once the
+    // previous block's last S has completed, load K by TMA. Per tile j: S(j)
+    // overwrites the S/P columns of TMEM stage j & 1, so it waits for
+    // P.V(j - 2) to have completed, and for its Q stage.
     if (lane == 0 && n_local > 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBk);
       const uint32_t k_base = smem_u32(smem + S::kKOff);
@@ -303,18 +310,14 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         if (j > s_last) {
           s_last = min(inf.w - t_begin, n_local) - 1;
           const int4 nxt = s_last + 1 < n_local ? tinfo[t_begin + s_last + 1] : kNone;
-          if (!mbar_wait(kv_empty, (epoch & 1) ^ 1, abort_flag, dg)) break;
-          kv_last[epoch & 1] = s_last;
-          const int g = inf.z >> 8;
-          const int32_t key0 = inf.x * kBk;
-          mbar_arrive_expect_tx(kv_full, 2 * S::kKVBytes);
-          for (int c = 0; c < D / 64; ++c) {
-            tma_load_3d(smem + S::kKOff + c * kBk * 128, &tm_k, kv_full, c * 64, g, key0);
-            tma_load_3d(smem + S::kVOff + c * kBk * 128, &tm_v, kv_full, c * 64, g, key0);
-          }
+          if (!mbar_wait(k_empty, (epoch & 1) ^ 1, abort_flag, dg)) break;
+          mbar_arrive_expect_tx(k_full, S::kKVBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + S::kKOff + c * kBk * 128, &tm_k, k_full, c * 64, inf.z >> 8,
+                        inf.x * kBk);
           ++epoch;
           inf = nxt;
-          if (!mbar_wait(kv_full, (epoch - 1) & 1, abort_flag, dg)) break;
+          if (!mbar_wait(k_full, (epoch - 1) & 1, abort_flag, dg)) break;
         }
         const int st = j & 1, qs = j % QS;
         if ((j >= 2 && !mbar_wait(&o_full[st], (uint32_t)(((j - 2) >> 1) & 1), abort_flag, dg)) ||
@@ -331,26 +334,37 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         mma_commit(&s_full[st]);
         mma_commit(&q_empty[qs]);
+        if (j == s_last) mma_commit(k_empty);
       }
-      if (*abort_flag && epoch > 0) mbar_drain(kv_full, (epoch - 1) & 1);
+      if (*abort_flag && epoch > 0) mbar_drain(k_full, (epoch - 1) & 1);
       mma_commit(&done_bar[0]);
       mbar_drain(&done_bar[0], 0);
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------- O = P V
-    // Per tile j, once its softmax has written P: P.V(j) overwrites the O
-    // columns of TMEM stage j & 1, so it waits for the epilogue of tile j - 2
-    // to have read them. The last P.V of a K/V block frees the K/V buffer.
+    // ---------------------------------------------------------- V + O = P V
+    // Per K/V block: once this thread's last P.V of the previous block has
+    // completed, load V by TMA (meanwhile the block's first softmax runs). Per
+    // tile j, once its softmax has written P: P.V(j) overwrites the O columns
+    // of TMEM stage j & 1, so it waits for the epilogue of tile j - 2 to have
+    // read them.
     if (lane == 0 && n_local > 0) {
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
       const uint32_t v_base = smem_u32(smem + S::kVOff);
       uint32_t epoch = 0;
       int o_last = -1;
+      int4 inf = tinfo[t_begin];
       for (int j = 0; j < n_local; ++j) {
         if (j > o_last) {
-          if (!mbar_wait(kv_full, epoch & 1, abort_flag, dg)) break;
-          o_last = kv_last[epoch & 1];
+          o_last = min(inf.w - t_begin, n_local) - 1;
+          const int4 nxt = o_last + 1 < n_local ? tinfo[t_begin + o_last + 1] : kNone;
+          if (!mbar_wait(v_empty, (epoch & 1) ^ 1, abort_flag, dg)) break;
+          mbar_arrive_expect_tx(v_full, S::kKVBytes);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(smem + S::kVOff + c * kBk * 128, &tm_v, v_full, c * 64, inf.z >> 8,
+                        inf.x * kBk);
           ++epoch;
+          inf = nxt;
+          if (!mbar_wait(v_full, (epoch - 1) & 1, abort_flag, dg)) break;
         }
         const int st = j & 1;
         if (!mbar_wait(&p_full[st], (uint32_t)((j >> 1) & 1), abort_flag, dg) ||
@@ -365,8 +379,9 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           mma_bf16_ts(d_o, a_p, bd, idesc_o, kk > 0 ? 1u : 0u);
         }
         mma_commit(&o_full[st]);
-        if (j == o_last) mma_commit(kv_empty);
+        if (j == o_last) mma_commit(v_empty);
       }
+      if (*abort_flag && epoch > 0) mbar_drain(v_full, (epoch - 1) & 1);
       mma_commit(&done_bar[1]);
       mbar_drain(&done_bar[1], 0);
     }
