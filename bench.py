@@ -411,7 +411,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=15.0)
-    ap.add_argument("--only", choices=["decode", "topk", "index"], default=None,
+    ap.add_argument("--only", choices=["decode", "topk", "index", "attn"], default=None,
                     help="time only this path and print its numbers (for profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -452,6 +452,31 @@ def main():
         ms = a.elapsed_time(b) / args.steps
         print(json.dumps({"only": "index", "workload": w.name, "ms": ms,
                           "tflops": index_flops(w.N, w.n_g, w.d_idx) / (ms * 1e-3) / 1e12}))
+        return
+    if args.only == "attn":
+        # main branch alone on the workload, on block ids from the index branch
+        w = synth.make(args.workload)
+        qidx = synth.device_tensor(w, synth.T_QIDX)
+        kidx = synth.device_tensor(w, synth.T_KIDX)[:, 0].contiguous()
+        ids = msa.msa_index_select(qidx, kidx, w.Bk, w.k)
+        del qidx, kidx
+        q = synth.device_tensor(w, synth.T_Q)
+        k = synth.device_tensor(w, synth.T_K)
+        v = synth.device_tensor(w, synth.T_V)
+        ws = torch.empty(msa.msa_sparse_attn_workspace_bytes(w.N, w.N, w.H_q, w.H_kv, w.d, w.Bk,
+                                                             w.k), dtype=torch.uint8, device="cuda")
+        for _ in range(args.warmup):
+            msa.msa_sparse_attn(q, k, v, ids, w.Bk, w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            msa.msa_sparse_attn(q, k, v, ids, w.Bk, w.scale, workspace=ws)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        print(json.dumps({"only": "attn", "workload": w.name, "ms": ms,
+                          "tflops": attn_flops(w.N, w.H_q, w.d, w.Bk, w.k) / (ms * 1e-3) / 1e12}))
         return
     if args.only == "topk":
         t_ms, t_bytes = time_topk(msa, synth.make("128k"), args.steps, args.warmup)
