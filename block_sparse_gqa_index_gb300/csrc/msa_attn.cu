@@ -725,6 +725,109 @@ attn_merge_kernel(const unsigned char* __restrict__ part, const int32_t* __restr
   }
 }
 
+// Group merge: one warp per (query, group) reads each selected slot's whole
+// record (the G heads' o/l rows are contiguous, so a slot is one G*D*2-byte
+// run) and writes the group's G output rows, which are contiguous as well.
+// Lane l covers the E = G*D/32 elements starting at l*E (head l*E/D). Lane
+// s < k holds slot s's record index and LSEs; per head, max and sum come from
+// shuffles over the slots. Used when G*D <= 1024.
+template <int D, int E>
+__global__ void __launch_bounds__(256)
+attn_merge_group_kernel(const unsigned char* __restrict__ part,
+                        const int32_t* __restrict__ rec_of, int64_t q0, int64_t q1, int H_q,
+                        int H_kv, int k, uint16_t* __restrict__ out, float* __restrict__ lse) {
+  constexpr int G = 32 * E / D;
+  constexpr int kRec = G * D * 2 + (G + 3) / 4 * 16;
+  static_assert(G >= 1 && 32 * E == G * D, "group merge needs G*D a multiple of 32");
+  const int lane = threadIdx.x & 31;
+  const int hi = lane * E / D;  // this lane's head within the group
+  const int64_t n = (q1 - q0) * H_kv;
+  const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < n; w += warps) {
+    const int64_t tl = w / H_kv;
+    const int g = (int)(w % H_kv);
+    const int ri = lane < k ? rec_of[((size_t)tl * H_kv + g) * k + lane] : -1;
+    float wl[G], M[G], L[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float ls = ri >= 0 ? *reinterpret_cast<const float*>(part + (size_t)ri * kRec +
+                                                                 G * D * 2 + h * 4)
+                               : -INFINITY;
+      float m = ls;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      const float e = ri >= 0 ? __expf(ls - m) : 0.f;
+      float s = e;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      wl[h] = e;
+      M[h] = m;
+      L[h] = s;
+    }
+    float acc[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+      if (s >= k) break;
+      const int rs = __shfl_sync(0xffffffffu, ri, s);
+      float wgt = 0.f;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float x = __shfl_sync(0xffffffffu, wl[h], s);
+        if (h == hi) wgt = x;
+      }
+      if (rs < 0) continue;  // padded slot (the same for the whole warp)
+      const uint32_t* po = reinterpret_cast<const uint32_t*>(part + (size_t)rs * kRec) + lane * E / 2;
+#pragma unroll
+      for (int v = 0; v < E / 2; v += (E >= 8 ? 4 : E / 2)) {
+        uint32_t wd[4];
+        if (E >= 8) {
+          const uint4 u = __ldcs(reinterpret_cast<const uint4*>(po + v));
+          wd[0] = u.x; wd[1] = u.y; wd[2] = u.z; wd[3] = u.w;
+        } else if (E == 4) {
+          const uint2 u = __ldcs(reinterpret_cast<const uint2*>(po + v));
+          wd[0] = u.x; wd[1] = u.y;
+        } else {
+          wd[0] = __ldcs(po + v);
+        }
+#pragma unroll
+        for (int j = 0; j < (E >= 8 ? 4 : E / 2); ++j) {
+          acc[2 * (v + j)] = fmaf(wgt, bf16_lo(wd[j]), acc[2 * (v + j)]);
+          acc[2 * (v + j) + 1] = fmaf(wgt, bf16_hi(wd[j]), acc[2 * (v + j) + 1]);
+        }
+      }
+    }
+    float Lh = 0.f, Mh = 0.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      if (h == hi) { Lh = L[h]; Mh = M[h]; }
+    const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
+    const int64_t t = q0 + tl;
+    uint32_t* o = reinterpret_cast<uint32_t*>(out + ((size_t)t * H_q + (size_t)g * G) * D) +
+                  lane * E / 2;
+#pragma unroll
+    for (int v = 0; v < E / 2; v += (E >= 8 ? 4 : E / 2)) {
+      if (E >= 8) {
+        uint4 u;
+        u.x = pack_bf16x2(acc[2 * v + 0] * inv, acc[2 * v + 1] * inv);
+        u.y = pack_bf16x2(acc[2 * v + 2] * inv, acc[2 * v + 3] * inv);
+        u.z = pack_bf16x2(acc[2 * v + 4] * inv, acc[2 * v + 5] * inv);
+        u.w = pack_bf16x2(acc[2 * v + 6] * inv, acc[2 * v + 7] * inv);
+        *reinterpret_cast<uint4*>(o + v) = u;
+      } else if (E == 4) {
+        uint2 u;
+        u.x = pack_bf16x2(acc[2 * v + 0] * inv, acc[2 * v + 1] * inv);
+        u.y = pack_bf16x2(acc[2 * v + 2] * inv, acc[2 * v + 3] * inv);
+        *reinterpret_cast<uint2*>(o + v) = u;
+      } else {
+        o[v] = pack_bf16x2(acc[2 * v] * inv, acc[2 * v + 1] * inv);
+      }
+    }
+    if (lse && (lane * E) % D == 0) lse[(size_t)t * H_q + g * G + hi] = Mh + logf(Lh);
+  }
+}
+
 // 3D bf16 tensor [N, H, D] viewed as (D, H, N); box {64, 1, 128}, 128B swizzle
 bool make_map_kv(CUtensorMap* m, const void* base, int64_t N, int H, int D) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -852,14 +955,37 @@ cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* 
   e = d == 128 ? launch_tiles<128>(q, kk, v, N, q0, H_q, H_kv, k, scale_log2, nb, ws, n_b, dg, st)
                : launch_tiles<64>(q, kk, v, N, q0, H_q, H_kv, k, scale_log2, nb, ws, n_b, dg, st);
   if (e != cudaSuccess) return e;
-  int64_t nw = (q1 - q0) * H_q;
-  unsigned mg = (unsigned)std::min<int64_t>((nw * 16 + 255) / 256, 152 * 64);
-  if (d == 128)
-    attn_merge_kernel<128><<<mg, 256, 0, st>>>(ws.part, ws.rec_of, q0, q1, H_q, H_kv, k,
-                                               (uint16_t*)out, lse);
-  else
-    attn_merge_kernel<64><<<mg, 256, 0, st>>>(ws.part, ws.rec_of, q0, q1, H_q, H_kv, k,
-                                              (uint16_t*)out, lse);
+  if (G * d <= 1024) {
+    const int64_t nw = (q1 - q0) * H_kv;  // one warp per (query, group)
+    const unsigned mg = (unsigned)std::min<int64_t>((nw * 32 + 255) / 256, 152 * 64);
+    const int E = G * d / 32;
+    auto* o16 = (uint16_t*)out;
+#define MSA_MERGE_G(DD, EE)                                                                   \
+  attn_merge_group_kernel<DD, EE><<<mg, 256, 0, st>>>(ws.part, ws.rec_of, q0, q1, H_q, H_kv, k, \
+                                                      o16, lse)
+    if (d == 128) {
+      if (E == 4) MSA_MERGE_G(128, 4);
+      else if (E == 8) MSA_MERGE_G(128, 8);
+      else if (E == 16) MSA_MERGE_G(128, 16);
+      else MSA_MERGE_G(128, 32);
+    } else {
+      if (E == 2) MSA_MERGE_G(64, 2);
+      else if (E == 4) MSA_MERGE_G(64, 4);
+      else if (E == 8) MSA_MERGE_G(64, 8);
+      else if (E == 16) MSA_MERGE_G(64, 16);
+      else MSA_MERGE_G(64, 32);
+    }
+#undef MSA_MERGE_G
+  } else {
+    int64_t nw = (q1 - q0) * H_q;
+    unsigned mg = (unsigned)std::min<int64_t>((nw * 16 + 255) / 256, 152 * 64);
+    if (d == 128)
+      attn_merge_kernel<128><<<mg, 256, 0, st>>>(ws.part, ws.rec_of, q0, q1, H_q, H_kv, k,
+                                                 (uint16_t*)out, lse);
+    else
+      attn_merge_kernel<64><<<mg, 256, 0, st>>>(ws.part, ws.rec_of, q0, q1, H_q, H_kv, k,
+                                                (uint16_t*)out, lse);
+  }
   return cudaGetLastError();
 }
 
