@@ -49,17 +49,27 @@ __device__ __forceinline__ bool id_ok(int id, int64_t t, const Diag& dg) {
 }
 
 // Counts the queries of every bucket; a slot with no usable block gets no
-// partial record (rec_of = -1).
+// partial record (rec_of = -1). Lanes of a warp that hit the same bucket add
+// their count with one atomic (popular blocks are selected by most queries).
 __global__ void bucket_count_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1,
                                     int n_g, int k, int64_t nb, int32_t* __restrict__ counts,
                                     int32_t* __restrict__ rec_of, Diag dg) {
-  int64_t n = (q1 - q0) * n_g * k;
-  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    int64_t row = q0 * n_g + e / k;  // (t, g) row
-    int id = ids[row * k + e % k];
-    if (id_ok(id, row / n_g, dg)) atomicAdd(&counts[(row % n_g) * nb + id], 1);
-    else rec_of[e] = -1;
+  const int n = (int)((q1 - q0) * n_g * k);  // entries of the chunk (< 2^31)
+  const int row0 = (int)(q0 * n_g);
+  const int lane = threadIdx.x & 31;
+  const int* __restrict__ cids = ids + (size_t)row0 * k;
+  for (int base = blockIdx.x * blockDim.x; base < n; base += gridDim.x * blockDim.x) {
+    const int e = base + threadIdx.x;
+    int bk = -1;
+    if (e < n) {
+      const int row = row0 + e / k;
+      const int t = row / n_g;
+      const int id = cids[e];
+      if (id_ok(id, t, dg)) bk = (row - t * n_g) * (int)nb + id;
+      else rec_of[e] = -1;
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, bk);
+    if (bk >= 0 && lane == __ffs(same) - 1) atomicAdd(&counts[bk], __popc(same));
   }
 }
 
@@ -104,7 +114,8 @@ __global__ void bucket_scan_kernel(const int32_t* __restrict__ counts, int64_t n
 
 // Places every (query, slot) of a bucket: its entry (query << 4 | slot) at the
 // bucket's next position, and the index of its partial record, which is the
-// tile-major position tile * qt + (query's place in its tile).
+// tile-major position tile * qt + (query's place in its tile). Lanes of a warp
+// that hit the same bucket take consecutive positions from one atomic.
 __global__ void bucket_fill_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1,
                                    int n_g, int k, int64_t nb, int qt,
                                    const int32_t* __restrict__ offsets,
@@ -112,17 +123,33 @@ __global__ void bucket_fill_kernel(const int32_t* __restrict__ ids, int64_t q0, 
                                    int32_t* __restrict__ cursor, int32_t* __restrict__ entries,
                                    int32_t* __restrict__ rec_of) {
   const Diag none{nullptr, 0};
-  int64_t n = (q1 - q0) * n_g * k;
-  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    int64_t row = q0 * n_g + e / k;
-    int slot = (int)(e % k);
-    int id = ids[row * k + slot];
-    if (!id_ok(id, row / n_g, none)) continue;
-    int64_t bk = (row % n_g) * nb + id;
-    const int c = atomicAdd(&cursor[bk], 1);
-    entries[offsets[bk] + c] = (int32_t)(((row / n_g - q0) << 4) | slot);
-    rec_of[e] = tile_off[bk] * qt + c;
+  const int n = (int)((q1 - q0) * n_g * k);
+  const int row0 = (int)(q0 * n_g);
+  const int lane = threadIdx.x & 31;
+  const int* __restrict__ cids = ids + (size_t)row0 * k;
+  for (int base = blockIdx.x * blockDim.x; base < n; base += gridDim.x * blockDim.x) {
+    const int e = base + threadIdx.x;
+    int bk = -1, ent = 0;
+    if (e < n) {
+      const int rl = e / k;
+      const int row = row0 + rl;
+      const int t = row / n_g;
+      const int id = cids[e];
+      if (id_ok(id, t, none)) {
+        bk = (row - t * n_g) * (int)nb + id;
+        ent = ((row / n_g - (int)q0) << 4) | (e - rl * k);
+      }
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, bk);
+    const int leader = __ffs(same) - 1;
+    int c0 = 0;
+    if (bk >= 0 && lane == leader) c0 = atomicAdd(&cursor[bk], __popc(same));
+    c0 = __shfl_sync(0xffffffffu, c0, leader);
+    if (bk >= 0) {
+      const int c = c0 + __popc(same & ((1u << lane) - 1));
+      entries[offsets[bk] + c] = ent;
+      rec_of[e] = tile_off[bk] * qt + c;
+    }
   }
 }
 
