@@ -254,15 +254,27 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256 + h * 128);
         // visible columns of this row in block b: all, or up to t on the diagonal
         const int lim = (b < loc) ? 128 : (b == loc ? (int)(t - b * kKeys) + 1 : 0);
+        // with every column visible to every row of the warp the loads reduce
+        // (sm_103 load-with-max); the diagonal block reduces in registers
+        const bool full = __all_sync(0xffffffffu, lim >= kKeys);
         float m = -INFINITY;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t r0[32], r1[32];
-          tmem_ld32(taddr + half * 64, r0);
-          tmem_ld32(taddr + half * 64 + 32, r1);
+          float m0 = -INFINITY, m1 = -INFINITY;
+          if (full) {
+            tmem_ld32_max(taddr + half * 64, r0, m0);
+            tmem_ld32_max(taddr + half * 64 + 32, r1, m1);
+          } else {
+            tmem_ld32(taddr + half * 64, r0);
+            tmem_ld32(taddr + half * 64 + 32, r1);
+          }
           tmem_ld_wait();
-          m = fmaxf(m, max32(r0, lim - half * 64));
-          m = fmaxf(m, max32(r1, lim - half * 64 - 32));
+          if (!full) {
+            m0 = max32(r0, lim - half * 64);
+            m1 = max32(r1, lim - half * 64 - 32);
+          }
+          m = fmax3(m, m0, m1);
         }
         tc_fence_before();
         __syncwarp();
