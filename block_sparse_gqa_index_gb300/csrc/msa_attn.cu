@@ -537,32 +537,35 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
       tc_fence_after();
       const int lim = (ent_c >= 0 && t / kBk == b) ? t - b * kBk + 1 : kBk;
-      // pass 1: row max
+      // pass 1: row max. With no masked column in the warp the loads reduce
+      // (sm_103 TMEM load-with-max); the local block's rows reduce in registers.
+      const bool full = __all_sync(0xffffffffu, lim >= kBk);
       float m = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; c += 2) {
         uint32_t r0[32], r1[32];
-        tmem_ld32(ts + c * 32, r0);
-        tmem_ld32(ts + c * 32 + 32, r1);
-        tmem_ld_wait();
-        if (lim >= kBk) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 2)
-            m = fmax3(m, fmaxf(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1])),
-                      fmaxf(__uint_as_float(r1[j]), __uint_as_float(r1[j + 1])));
+        float m0 = -INFINITY, m1 = -INFINITY;
+        if (full) {
+          tmem_ld32_max(ts + c * 32, r0, m0);
+          tmem_ld32_max(ts + c * 32 + 32, r1, m1);
         } else {
+          tmem_ld32(ts + c * 32, r0);
+          tmem_ld32(ts + c * 32 + 32, r1);
+        }
+        tmem_ld_wait();
+        if (!full) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (c * 32 + j < lim) m = fmaxf(m, __uint_as_float(r0[j]));
-            if (c * 32 + 32 + j < lim) m = fmaxf(m, __uint_as_float(r1[j]));
+            if (c * 32 + j < lim) m0 = fmaxf(m0, __uint_as_float(r0[j]));
+            if (c * 32 + 32 + j < lim) m1 = fmaxf(m1, __uint_as_float(r1[j]));
           }
         }
+        m = fmax3(m, m0, m1);
       }
       const float mc = m * scale_log2;
       // pass 2: P = exp2(s * c - m * c) in bf16 over the first 64 columns, row
       // sum; the load of chunk c + 1 is in flight while chunk c is computed.
       // Rows of the local block mask the columns past their query.
-      const bool full = __all_sync(0xffffffffu, lim >= kBk);
       const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-mc, -mc);
       uint64_t l2 = f2_pack(0.f, 0.f);
       auto p_chunk = [&](const uint32_t(&r)[32], int c) {
