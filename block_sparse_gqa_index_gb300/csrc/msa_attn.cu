@@ -73,6 +73,91 @@ __global__ void bucket_count_kernel(const int32_t* __restrict__ ids, int64_t q0,
   }
 }
 
+// Shared-memory bucketing, used when a CTA's shared memory holds one counter
+// per bucket. CTA c takes a contiguous slice of the chunk's entries. Popular
+// blocks (picked by most queries) then cost shared-memory atomics instead of
+// serialised global atomics on one address. Pass 1 counts per CTA; a scan over
+// the CTAs turns the counts into each CTA's first position per bucket; pass 2
+// places the entries from those positions.
+constexpr int kBucketCtas = 296;
+constexpr int kSmemBucketsMax = 48 * 1024 / 4;
+
+__device__ __forceinline__ void slice_of(int n, int c, int& e0, int& e1) {
+  e0 = (int)((int64_t)n * c / gridDim.x);
+  e1 = (int)((int64_t)n * (c + 1) / gridDim.x);
+}
+
+__global__ void __launch_bounds__(1024)
+bucket_count_smem_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1, int n_g, int k,
+                         int64_t nb, int32_t* __restrict__ counts, int32_t* __restrict__ percta,
+                         int32_t* __restrict__ rec_of, Diag dg) {
+  extern __shared__ int32_t hist[];
+  const int n_b = (int)(n_g * nb);
+  for (int i = threadIdx.x; i < n_b; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int n = (int)((q1 - q0) * n_g * k);
+  const int row0 = (int)(q0 * n_g);
+  const int* __restrict__ cids = ids + (size_t)row0 * k;
+  int e0, e1;
+  slice_of(n, blockIdx.x, e0, e1);
+  for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+    const int row = row0 + e / k;
+    const int t = row / n_g;
+    const int id = cids[e];
+    if (id_ok(id, t, dg)) atomicAdd(&hist[(row - t * n_g) * (int)nb + id], 1);
+    else rec_of[e] = -1;
+  }
+  __syncthreads();
+  int32_t* mine = percta + (size_t)blockIdx.x * n_b;
+  for (int i = threadIdx.x; i < n_b; i += blockDim.x) {
+    const int c = hist[i];
+    mine[i] = c;
+    if (c) atomicAdd(&counts[i], c);
+  }
+}
+
+// per bucket: percta[c][b] <- offsets[b] + (entries of b in CTAs before c)
+__global__ void bucket_cta_base_kernel(const int32_t* __restrict__ offsets, int n_b, int ctas,
+                                       int32_t* __restrict__ percta) {
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < n_b; b += gridDim.x * blockDim.x) {
+    int run = offsets[b];
+    for (int c = 0; c < ctas; ++c) {
+      const int x = percta[(size_t)c * n_b + b];
+      percta[(size_t)c * n_b + b] = run;
+      run += x;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024)
+bucket_fill_smem_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1, int n_g, int k,
+                        int64_t nb, int qt, const int32_t* __restrict__ offsets,
+                        const int32_t* __restrict__ tile_off, const int32_t* __restrict__ percta,
+                        int32_t* __restrict__ entries, int32_t* __restrict__ rec_of) {
+  extern __shared__ int32_t cur[];
+  const Diag none{nullptr, 0};
+  const int n_b = (int)(n_g * nb);
+  const int32_t* mine = percta + (size_t)blockIdx.x * n_b;
+  for (int i = threadIdx.x; i < n_b; i += blockDim.x) cur[i] = mine[i];
+  __syncthreads();
+  const int n = (int)((q1 - q0) * n_g * k);
+  const int row0 = (int)(q0 * n_g);
+  const int* __restrict__ cids = ids + (size_t)row0 * k;
+  int e0, e1;
+  slice_of(n, blockIdx.x, e0, e1);
+  for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+    const int rl = e / k;
+    const int row = row0 + rl;
+    const int t = row / n_g;
+    const int id = cids[e];
+    if (!id_ok(id, t, none)) continue;
+    const int bk = (row - t * n_g) * (int)nb + id;
+    const int pos = atomicAdd(&cur[bk], 1);
+    entries[pos] = ((t - (int)q0) << 4) | (e - rl * k);
+    rec_of[e] = tile_off[bk] * qt + (pos - offsets[bk]);
+  }
+}
+
 // single CTA: exclusive scans of counts and of ceil(counts / qt) (tiles)
 __global__ void bucket_scan_kernel(const int32_t* __restrict__ counts, int64_t n_b, int qt,
                                    int32_t* __restrict__ offsets, int32_t* __restrict__ tile_off,
@@ -938,6 +1023,7 @@ size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k)
   s += align256((size_t)(n_b + 1) * 4);  // offsets
   s += align256((size_t)n_b * 4);        // cursor
   s += align256((size_t)(n_b + 1) * 4);  // tile_off
+  if (n_b <= kSmemBucketsMax) s += align256((size_t)kBucketCtas * n_b * 4);  // percta
   s += align256((size_t)chunk * H_kv * k * 4);
   s += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * 16);
   s += align256((size_t)chunk * H_kv * k * 4);
@@ -954,6 +1040,11 @@ AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int
   w.offsets = (int32_t*)p;  p += align256((size_t)(n_b + 1) * 4);
   w.cursor = (int32_t*)p;   p += align256((size_t)n_b * 4);
   w.tile_off = (int32_t*)p; p += align256((size_t)(n_b + 1) * 4);
+  w.percta = nullptr;
+  if (n_b <= kSmemBucketsMax) {
+    w.percta = (int32_t*)p;
+    p += align256((size_t)kBucketCtas * n_b * 4);
+  }
   w.entries = (int32_t*)p;  p += align256((size_t)chunk * H_kv * k * 4);
   w.tinfo = (int4*)p;       p += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * 16);
   w.rec_of = (int32_t*)p;   p += align256((size_t)chunk * H_kv * k * 4);
@@ -969,15 +1060,28 @@ cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* 
   const int64_t n_b = (int64_t)H_kv * nb;
   const int G = H_q / H_kv;
   const int qt = kTileRows / G;
-  note_launches(7);  // memset, count, scan, fill, tile map, tile, merge
+  note_launches(n_b <= kSmemBucketsMax ? 8 : 7);  // memset, count, scan, (base,) fill, map, tile, merge
   cudaError_t e = cudaMemsetAsync(ws.counts, 0, (size_t)n_b * 4, st);
   if (e != cudaSuccess) return e;
   int64_t n = (q1 - q0) * H_kv * k;
+  const bool smem_buckets = n_b <= kSmemBucketsMax;
   unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 32);
-  bucket_count_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, ws.counts, ws.rec_of, dg);
+  if (smem_buckets)
+    bucket_count_smem_kernel<<<kBucketCtas, 1024, n_b * 4, st>>>(ids, q0, q1, H_kv, k, nb,
+                                                                 ws.counts, ws.percta, ws.rec_of,
+                                                                 dg);
+  else
+    bucket_count_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, ws.counts, ws.rec_of, dg);
   bucket_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, n_b, qt, ws.offsets, ws.tile_off, ws.cursor);
-  bucket_fill_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, qt, ws.offsets,
-                                           ws.tile_off, ws.cursor, ws.entries, ws.rec_of);
+  if (smem_buckets) {
+    bucket_cta_base_kernel<<<(unsigned)((n_b + 255) / 256), 256, 0, st>>>(ws.offsets, (int)n_b,
+                                                                          kBucketCtas, ws.percta);
+    bucket_fill_smem_kernel<<<kBucketCtas, 1024, n_b * 4, st>>>(
+        ids, q0, q1, H_kv, k, nb, qt, ws.offsets, ws.tile_off, ws.percta, ws.entries, ws.rec_of);
+  } else {
+    bucket_fill_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, qt, ws.offsets,
+                                             ws.tile_off, ws.cursor, ws.entries, ws.rec_of);
+  }
   const int64_t tiles_max = max_tiles(q1 - q0, n_b, H_q, H_kv, k);
   tile_map_kernel<<<(unsigned)std::min<int64_t>((tiles_max + 255) / 256, 152 * 16), 256, 0, st>>>(
       ws.tile_off, ws.offsets, n_b, nb, qt, ws.tinfo);

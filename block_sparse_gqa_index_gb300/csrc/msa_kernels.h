@@ -32,6 +32,7 @@ struct AttnWs {
   int32_t* offsets;   // [n_g * nb + 1]
   int32_t* cursor;    // [n_g * nb]
   int32_t* tile_off;  // [n_g * nb + 1]
+  int32_t* percta;    // [bucketing CTAs, n_g * nb] per-CTA counts, then first positions
   int32_t* entries;   // [chunk * n_g * k]
   int4* tinfo;        // per tile: block, first entry, queries | group << 8, end tile
   int32_t* rec_of;    // [chunk, n_g, k]: partial record of each (query, group, slot), or -1
