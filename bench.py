@@ -442,6 +442,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=15.0)
     ap.add_argument("--only", choices=["decode", "topk", "index", "attn"], default=None,
                     help="time only this path and print its numbers (for profiling runs)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="with --only decode: number of sequences (default: the workload's 64)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -458,7 +460,7 @@ def main():
 
     peaks, peak_src = load_peaks()
     if args.only == "decode":
-        wd = synth.make("decode")
+        wd = synth.make("decode", **({"B": args.batch} if args.batch else {}))
         for fp8 in (False, True):
             i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, args.warmup)
             torch.cuda.empty_cache()
@@ -508,8 +510,9 @@ def main():
                           "tflops": attn_flops(w.N, w.H_q, w.d, w.Bk, w.k) / (ms * 1e-3) / 1e12}))
         return
     if args.only == "topk":
-        t_ms, t_bytes = time_topk(msa, synth.make("128k"), args.steps, args.warmup)
-        print(json.dumps({"only": "topk", "ms": t_ms, "gbs": t_bytes / (t_ms * 1e-3) / 1e9}))
+        t_ms, t_bytes = time_topk(msa, synth.make(args.workload), args.steps, args.warmup)
+        print(json.dumps({"only": "topk", "workload": args.workload, "ms": t_ms,
+                          "gbs": t_bytes / (t_ms * 1e-3) / 1e9}))
         return
     w = synth.make(args.workload)
     clocks = {}

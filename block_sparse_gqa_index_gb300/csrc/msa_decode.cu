@@ -14,8 +14,10 @@
 // dimension is the kv-head count in the usage listing), so the block a group
 // reads is one contiguous run; k_idx pages are [P, 128, d_idx].
 // decode_attn_kernel: one CTA per (sequence, group, selected block): the G
-//   query heads of the group against the block's visible tokens; writes the
-//   block's normalised output and LSE (split-KV partials).
+//   query heads of the group against the block's visible tokens, with the
+//   block's K and V bytes all in flight at once (cp.async into swizzled shared
+//   memory) and both products on mma.m16n8k16; writes the block's normalised
+//   output and LSE (split-KV partials).
 // decode_merge_kernel: combines the k partials of every (sequence, head).
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -100,48 +102,101 @@ decode_index_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restri
   }
 }
 
-// 8 elements from a 16-byte (bf16) or 8-byte (FP8) vector
-__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* out) {
-  out[0] = bf16_lo(u.x); out[1] = bf16_hi(u.x);
-  out[2] = bf16_lo(u.y); out[3] = bf16_hi(u.y);
-  out[4] = bf16_lo(u.z); out[5] = bf16_hi(u.z);
-  out[6] = bf16_lo(u.w); out[7] = bf16_hi(u.w);
+// ---- decode attention: one CTA (4 warps) per (sequence, group, selected block)
+//
+// The block's K and V rows (32 KB each in bf16, 16 KB in E4M3 at d = 128) are
+// all put in flight at once by cp.async into shared memory, K in one group and
+// V in a second, so a CTA keeps its whole block's bytes outstanding; rows past
+// the sequence end are zero-filled by the copy itself. Shared rows are stored
+// with their 16-byte chunks XOR-swizzled by (row mod 8), so the fragment loads
+// below are free of bank conflicts.
+//
+// Warp w owns tokens 32w .. 32w+31 of the block. S = q K^T and O = P V run on
+// mma.m16n8k16 (bf16 operands, fp32 accumulate): the G <= 8 query heads of the
+// group are rows 0..G-1 of the 16-row A operand (the other rows are zero), so
+// the S accumulators hand P to the P.V A operand without any data movement.
+// E4M3 codes are widened to bf16 exactly (every E4M3 value is a bf16 value);
+// the per-head scales multiply the scores and the output. Each warp keeps its
+// own row max and sum; the four are combined in shared memory into the block's
+// normalised output and LSE (split-KV partials, merged by decode_merge_kernel).
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void unpack_e4m3x8(const uint2& u, float* out) {
-  const uint32_t w[2] = {u.x, u.y};
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xFFFF), __NV_E4M3);
-    __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
-    float2 a = __half22float2(*reinterpret_cast<__half2*>(&lo));
-    float2 b = __half22float2(*reinterpret_cast<__half2*>(&hi));
-    out[4 * i + 0] = a.x; out[4 * i + 1] = a.y; out[4 * i + 2] = b.x; out[4 * i + 3] = b.y;
-  }
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(a));
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u8 %0, [%1];\n" : "=h"(v) : "r"(a));
+  return v;
+}
+// two E4M3 codes (first in the low byte) -> bf16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+  return pack_bf16x2(f.x, f.y);
+}
+// byte offset of 16-byte chunk c of token row r in a swizzled K or V tile
+template <int ROWB>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  constexpr int kCpr = ROWB / 16;
+  constexpr int kMask = kCpr >= 8 ? 7 : kCpr - 1;
+  return (uint32_t)(r * ROWB + ((c ^ (r & kMask)) << 4));
 }
 
-// One CTA (128 threads) per (sequence, group, selected page). Scores: thread j
-// owns token j and issues all of its K-row loads before using them. P.V: the
-// threads form 16 column groups (8 columns each) x 8 token groups (16 tokens
-// each, strided so a warp reads whole token rows); partial sums over the token
-// groups are added up in shared memory.
 template <int D, bool FP8>
-__global__ void __launch_bounds__(128)
+constexpr int dec_smem_bytes() {
+  return 2 * kBk * D * (FP8 ? 1 : 2);
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(128, FP8 ? 4 : 3)
 decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
                    const void* __restrict__ vp, const float* __restrict__ k_scale,
                    const float* __restrict__ v_scale, const int32_t* __restrict__ page_table,
                    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ ids,
                    int max_pages, int H_q, int H_kv, int k, float scale_log2,
                    float* __restrict__ part_o, float* __restrict__ part_lse, Diag dg) {
-  constexpr int GMAX = 8;
-  constexpr int CG = D / 8;      // column groups
-  constexpr int TG = 128 / CG;   // token groups
   constexpr int EB = FP8 ? 1 : 2;
-  __shared__ float qs[GMAX][D];
-  __shared__ float sc[GMAX][kBk];
-  __shared__ float s_m[GMAX], s_l[GMAX];
-  __shared__ float red[TG][GMAX][D];
+  constexpr int ROWB = D * EB;      // bytes of one token row
+  constexpr int CPR = ROWB / 16;    // 16-byte chunks per row
+  constexpr int TILE = kBk * ROWB;  // bytes of one K or V block
+  constexpr int KS = D / 16;        // k-steps of q K^T
+  constexpr int NC = D / 8;         // 8-column tiles of P V
+  constexpr int RS = D + 8;         // row stride (floats) of the combine buffer
+  static_assert(4 * 8 * RS * 4 <= 2 * TILE, "combine buffer fits the K/V tiles");
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ float s_m[4][8], s_l[4][8];
+
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int gq = lane >> 2, t4 = lane & 3;
   const int G = H_q / H_kv;
-  const int tid = threadIdx.x;
   const int64_t task = blockIdx.x;  // (s * H_kv + g) * k + slot
   const int slot = (int)(task % k);
   const int64_t sg = task / k;
@@ -156,116 +211,155 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
   }
   const int64_t page = page_table[(size_t)s * max_pages + id];
   const int nvalid = min(kBk, L - id * kBk);
-  const float ks = FP8 ? k_scale[g] : 1.f;
-  const float vs = FP8 ? v_scale[g] : 1.f;
   // pages are head-major [P, H_kv, Bk, D]: the (page, head g) block is contiguous
-  const size_t row_stride = D;  // elements between tokens
-  const size_t base = ((size_t)page * H_kv + g) * kBk * D;
+  const size_t blk = ((size_t)page * H_kv + g) * TILE;
+  const unsigned char* gk = (const unsigned char*)kp + blk;
+  const unsigned char* gv = (const unsigned char*)vp + blk;
+  const uint32_t sk = smem_addr(dsm), sv = sk + TILE;
+#pragma unroll 4
+  for (int e = tid; e < kBk * CPR; e += 128) {
+    const int r = e / CPR;
+    cp_async16(sk + swz<ROWB>(r, e % CPR), gk + (size_t)e * 16, r < nvalid ? 16u : 0u);
+  }
+  cp_async_commit();
+#pragma unroll 4
+  for (int e = tid; e < kBk * CPR; e += 128) {
+    const int r = e / CPR;
+    cp_async16(sv + swz<ROWB>(r, e % CPR), gv + (size_t)e * 16, r < nvalid ? 16u : 0u);
+  }
+  cp_async_commit();
 
-  for (int e = tid; e < G * D; e += 128) {
-    int h = e / D, c = e % D;
-    qs[h][c] = __uint_as_float((uint32_t)q[((size_t)s * H_q + g * G + h) * D + c] << 16);
-  }
-  // K row of token tid, all loads in flight before use
-  float acc[GMAX];
-#pragma unroll
-  for (int h = 0; h < GMAX; ++h) acc[h] = 0.f;
+  // A operand rows: head gq of the group (rows >= G and the upper 8 rows are zero)
+  uint32_t qa[KS][2];
   {
-    const int j = tid;
-    // raw K row (16-byte bf16 or 8-byte E4M3 vectors), unpacked in the FMA loop
-    using Vec = typename std::conditional<FP8, uint2, uint4>::type;
-    Vec u[D / 8];
-    if (j < nvalid) {
-      const Vec* kr = reinterpret_cast<const Vec*>((const unsigned char*)kp +
-                                                   (base + j * row_stride) * EB);
+    const uint16_t* qr = q + ((size_t)s * H_q + (size_t)g * G + (gq < G ? gq : 0)) * D;
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) u[c] = __ldcs(kr + c);
+    for (int i = 0; i < KS; ++i) {
+      qa[i][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * i + 2 * t4) : 0u;
+      qa[i][1] = gq < G ? *reinterpret_cast<const uint32_t*>(qr + 16 * i + 8 + 2 * t4) : 0u;
     }
-    __syncthreads();  // qs ready
-    if (j < nvalid) {
+  }
+  const float cs = scale_log2 * (FP8 ? k_scale[g] : 1.f);
+  const float vs = FP8 ? v_scale[g] : 1.f;
+  const int tok0 = 32 * w;
+
+  cp_async_wait<1>();  // this thread's K chunks have landed
+  __syncthreads();     // everyone's have
+  float sacc[4][4];
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        float x[8];
-        if constexpr (FP8) unpack_e4m3x8(u[c], x); else unpack_bf16x8(u[c], x);
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int h = 0; h < GMAX; ++h)
-          if (h < G)
+    for (int i = 0; i < 4; ++i) sacc[nt][i] = 0.f;
+  if constexpr (!FP8) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[h] = fmaf(qs[h][8 * c + i], x[i], acc[h]);
+    for (int p = 0; p < KS / 2; ++p)
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(sk + swz<ROWB>(tok0 + 8 * nt + (lane & 7), 4 * p + (lane >> 3)), b0, b1, b2, b3);
+        mma_bf16_16816(sacc[nt], qa[2 * p][0], 0u, qa[2 * p][1], 0u, b0, b1);
+        mma_bf16_16816(sacc[nt], qa[2 * p + 1][0], 0u, qa[2 * p + 1][1], 0u, b2, b3);
+      }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KS; ++i)
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const uint32_t a = sk + swz<ROWB>(tok0 + 8 * nt + gq, i);
+        const uint32_t b0 = e4m3x2_to_bf16x2(lds_u16(a + 2 * t4));
+        const uint32_t b1 = e4m3x2_to_bf16x2(lds_u16(a + 8 + 2 * t4));
+        mma_bf16_16816(sacc[nt], qa[i][0], 0u, qa[i][1], 0u, b0, b1);
+      }
+  }
+
+  // warp-local softmax of head gq over the warp's 32 tokens (masked past nvalid)
+  float pr[4][2];
+  float mw = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int j = tok0 + 8 * nt + 2 * t4 + i;
+      pr[nt][i] = j < nvalid ? sacc[nt][i] * cs : -INFINITY;
+      mw = fmaxf(mw, pr[nt][i]);
+    }
+  mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
+  mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 2));
+  const float mref = mw == -INFINITY ? 0.f : mw;  // a warp past nvalid keeps p = 0
+  float lw = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      pr[nt][i] = ex2_approx(pr[nt][i] - mref);
+      lw += pr[nt][i];
+    }
+  lw += __shfl_xor_sync(0xffffffffu, lw, 1);
+  lw += __shfl_xor_sync(0xffffffffu, lw, 2);
+
+  cp_async_wait<0>();  // V has landed
+  __syncthreads();
+  float o[NC][4];
+#pragma unroll
+  for (int n = 0; n < NC; ++n)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[n][i] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {  // 16 tokens per k-step
+    const uint32_t a0 = pack_bf16x2(pr[2 * j][0], pr[2 * j][1]);
+    const uint32_t a2 = pack_bf16x2(pr[2 * j + 1][0], pr[2 * j + 1][1]);
+    if constexpr (!FP8) {
+      const int r = tok0 + 16 * j + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int n = 0; n < NC; n += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(sv + swz<ROWB>(r, n + (lane >> 4)), b0, b1, b2, b3);
+        mma_bf16_16816(o[n], a0, 0u, a2, 0u, b0, b1);
+        mma_bf16_16816(o[n + 1], a0, 0u, a2, 0u, b2, b3);
+      }
+    } else {
+      const int r = tok0 + 16 * j + 2 * t4;
+#pragma unroll
+      for (int n = 0; n < NC; ++n) {
+        const int col = 8 * n + gq;
+        const int ch = col >> 4, by = col & 15;
+        const uint32_t v00 = lds_u8(sv + swz<ROWB>(r, ch) + by);
+        const uint32_t v01 = lds_u8(sv + swz<ROWB>(r + 1, ch) + by);
+        const uint32_t v10 = lds_u8(sv + swz<ROWB>(r + 8, ch) + by);
+        const uint32_t v11 = lds_u8(sv + swz<ROWB>(r + 9, ch) + by);
+        mma_bf16_16816(o[n], a0, 0u, a2, 0u, e4m3x2_to_bf16x2(v00 | (v01 << 8)),
+                       e4m3x2_to_bf16x2(v10 | (v11 << 8)));
       }
     }
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h)
-      if (h < G) sc[h][j] = j < nvalid ? acc[h] * ks * scale_log2 : -INFINITY;
   }
-  __syncthreads();
-  {
-    const int w = tid >> 5, lane = tid & 31;
-    for (int h = w; h < G; h += 4) {
-      float m = -INFINITY;
+  __syncthreads();  // every warp is done with the K and V tiles: reuse them
+  float* red = reinterpret_cast<float*>(dsm);  // [4 warps][8 heads][RS]
+  if (gq < G) {
 #pragma unroll
-      for (int i = 0; i < kBk / 32; ++i) m = fmaxf(m, sc[h][lane + 32 * i]);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      float l = 0.f;
-#pragma unroll
-      for (int i = 0; i < kBk / 32; ++i) {
-        float p = ex2_approx(sc[h][lane + 32 * i] - m);
-        sc[h][lane + 32 * i] = p;
-        l += p;
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-      if (lane == 0) { s_m[h] = m; s_l[h] = l; }
+    for (int n = 0; n < NC; ++n)
+      *reinterpret_cast<float2*>(red + (w * 8 + gq) * RS + 8 * n + 2 * t4) =
+          make_float2(o[n][0], o[n][1]);
+    if (t4 == 0) {
+      s_m[w][gq] = mw;
+      s_l[w][gq] = lw;
     }
-  }
-  __syncthreads();
-  {
-    const int cg = tid % CG, tg = tid / CG;
-    float o[GMAX][8];
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[h][i] = 0.f;
-    constexpr int NT = kBk / TG;  // tokens per thread
-    using Vec = typename std::conditional<FP8, uint2, uint4>::type;
-    Vec vr[NT];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const int j = tg + n * TG;
-      if (j < nvalid)
-        vr[n] = __ldcs(reinterpret_cast<const Vec*>((const unsigned char*)vp +
-                                                    (base + j * row_stride + cg * 8) * EB));
-    }
-#pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      const int j = tg + n * TG;
-      if (j >= nvalid) continue;
-      float x[8];
-      if constexpr (FP8) unpack_e4m3x8(vr[n], x); else unpack_bf16x8(vr[n], x);
-#pragma unroll
-      for (int h = 0; h < GMAX; ++h)
-        if (h < G) {
-          const float p = sc[h][j];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) o[h][i] = fmaf(p, x[i], o[h][i]);
-        }
-    }
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h)
-      if (h < G)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) red[tg][h][cg * 8 + i] = o[h][i];
   }
   __syncthreads();
   for (int e = tid; e < G * D; e += 128) {
     const int h = e / D, c = e % D;
-    float sum = 0.f;
+    float M = s_m[0][h];
 #pragma unroll
-    for (int t = 0; t < TG; ++t) sum += red[t][h][c];
-    const size_t dst = ((size_t)s * H_q + g * G + h) * k + slot;
-    part_o[dst * D + c] = sum * vs / s_l[h];
-    if (c == 0) part_lse[dst] = (s_m[h] + __log2f(s_l[h])) * 0.69314718055994531f;
+    for (int i = 1; i < 4; ++i) M = fmaxf(M, s_m[i][h]);  // finite: token 0 is in warp 0
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float f = ex2_approx(s_m[i][h] - M);
+      num = fmaf(f, red[(i * 8 + h) * RS + c], num);
+      den = fmaf(f, s_l[i][h], den);
+    }
+    const size_t dst = ((size_t)s * H_q + (size_t)g * G + h) * k + slot;
+    part_o[dst * D + c] = num * vs / den;
+    if (c == 0) part_lse[dst] = (M + __log2f(den)) * 0.69314718055994531f;
   }
 }
 
@@ -350,10 +444,17 @@ cudaError_t launch_decode_attn(const void* q, const void* k_pages, const void* v
   unsigned tasks = (unsigned)((int64_t)B * H_kv * k);
   if (tasks == 0) return cudaSuccess;
   note_launches(2);  // attention, merge
+  cudaError_t e = cudaSuccess;
 #define MSA_DEC(DD, F8)                                                                    \
-  decode_attn_kernel<DD, F8><<<tasks, 128, 0, st>>>(                                       \
-      (const uint16_t*)q, k_pages, v_pages, k_scale, v_scale, page_table, seq_lens, ids,   \
-      max_pages, H_q, H_kv, k, sl2, part_o, part_lse, dg)
+  do {                                                                                     \
+    constexpr int sm = dec_smem_bytes<DD, F8>();                                           \
+    e = cudaFuncSetAttribute(decode_attn_kernel<DD, F8>,                                   \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, sm);             \
+    if (e != cudaSuccess) return e;                                                        \
+    decode_attn_kernel<DD, F8><<<tasks, 128, sm, st>>>(                                    \
+        (const uint16_t*)q, k_pages, v_pages, k_scale, v_scale, page_table, seq_lens, ids, \
+        max_pages, H_q, H_kv, k, sl2, part_o, part_lse, dg);                               \
+  } while (0)
   if (d == 128) {
     if (kv_fp8) MSA_DEC(128, true); else MSA_DEC(128, false);
   } else {

@@ -302,12 +302,22 @@ def test_decode_small(msa, fp8):
     _decode_case(msa, w, fp8)
 
 
+@pytest.mark.parametrize("H_q,H_kv,d,fp8", [(8, 8, 128, False), (8, 8, 64, True),
+                                             (8, 4, 128, True), (16, 2, 64, False),
+                                             (16, 2, 128, True), (16, 2, 128, False)])
+def test_decode_group_sizes(msa, H_q, H_kv, d, fp8):
+    """Group sizes G = 1, 2, 8 (rows of the warp MMA's A operand) with a partial last page."""
+    w = synth.make("decode", B=3, L=128 * 18 + 77, H_q=H_q, H_kv=H_kv, d=d, d_idx=d)
+    _decode_case(msa, w, fp8)
+
+
 @pytest.mark.parametrize("fp8", [False, True])
 def test_decode_full_config(msa, fp8):
     _decode_case(msa, synth.make("decode"), fp8)
 
 
-def test_decode_ragged_lengths(msa):
+@pytest.mark.parametrize("fp8", [False, True])
+def test_decode_ragged_lengths(msa, fp8):
     """Sequences of different lengths (1 token up to several blocks, partial
     last pages) in one batch; integer index inputs so the ids are exact."""
     w = synth.make("decode", B=6, L=1000, H_q=8, H_kv=2, d=128, d_idx=128, kind=synth.KIND_INT,
@@ -327,16 +337,21 @@ def test_decode_ragged_lengths(msa):
     want = oracle.decode_index_select(qh, kh, ident, lens, w.Bk, w.k)
     assert np.array_equal(ids.cpu().numpy(), want)
     q = synth.device_rows(w, synth.T_Q, [(s, int(lens[s]) - 1) for s in range(w.B)])
-    kp = synth.device_paged(w, synth.T_K, pt)
-    vp = synth.device_paged(w, synth.T_V, pt)
-    out, lse = msa.msa_decode(q, kp, vp, pt, torch.from_numpy(lens).to(dev), ids, w.Bk, w.scale)
+    kp = synth.device_paged(w, synth.T_K, pt, fp8=fp8)
+    vp = synth.device_paged(w, synth.T_V, pt, fp8=fp8)
+    ks, vs = synth.fp8_scales(w.H_kv)
+    kw = dict(k_scale=torch.from_numpy(ks).to(dev), v_scale=torch.from_numpy(vs).to(dev)) \
+        if fp8 else {}
+    out, lse = msa.msa_decode(q, kp, vp, pt, torch.from_numpy(lens).to(dev), ids, w.Bk, w.scale,
+                              **kw)
     torch.cuda.synchronize()
-    Kh = synth.host_paged(w, synth.T_K)
-    Vh = synth.host_paged(w, synth.T_V)
+    Kh = synth.host_paged(w, synth.T_K, fp8=fp8)
+    Vh = synth.host_paged(w, synth.T_V, fp8=fp8)
     qhq = np.stack([synth.host_rows(w, synth.T_Q, s, [int(lens[s]) - 1])[0] for s in range(w.B)])
-    o_ref, l_ref = oracle.decode_attn(qhq, Kh, Vh, ident, lens, want, w.Bk, w.scale)
-    check_close("o", bf16_to_np(out), o_ref, TOL_O)
-    check_close("lse", lse.cpu().numpy(), l_ref, TOL_LSE)
+    o_ref, l_ref = oracle.decode_attn(qhq, Kh, Vh, ident, lens, want, w.Bk, w.scale, fp8=fp8,
+                                      k_scale=ks if fp8 else None, v_scale=vs if fp8 else None)
+    check_close("o", bf16_to_np(out), o_ref, TOL_O_FP8 if fp8 else TOL_O)
+    check_close("lse", lse.cpu().numpy(), l_ref, TOL_LSE * (10 if fp8 else 1))
 
 
 def test_decode_matches_prefill_row_on_gpu(msa):
