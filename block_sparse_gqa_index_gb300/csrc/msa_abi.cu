@@ -108,7 +108,7 @@ int msa_topk_blocks(const float* block_scores, int64_t N, int n_groups, int64_t 
   if (N == 0) return MSA_OK;
   if (!block_scores || !block_ids) return MSA_ERR_INVALID_ARG;
   if (!seq_lens && (N - 1 + q_offset) / Bk >= nb) return MSA_ERR_INVALID_ARG;
-  if (!supported_k(k)) return MSA_ERR_UNSUPPORTED;
+  if (!supported_k(k) || N * (int64_t)n_groups > INT32_MAX) return MSA_ERR_UNSUPPORTED;
   return status_of(msa::launch_topk(block_scores, N, n_groups, nb, Bk, k, q_offset, seq_lens,
                                     block_ids, diag(), (cudaStream_t)stream));
 }

@@ -7,34 +7,45 @@
 // "两个分支如何工作": the query's local block is always kept and the other k-1
 // slots take the best earlier blocks; lower block id wins ties.
 //
-// One warp per (query, group) row. The row's candidates (blocks 0 .. loc-1) are
-// streamed in chunks of 1024 scores, 32 per lane, read with 16-byte loads. Per
-// chunk:
-//   1. every lane takes the max ranking key of its 32 scores;
-//   2. tau = max(15th largest lane max, worst key kept so far): at least k-1
+// Each 16-lane half of a warp ranks one (query, group) row, so every shuffle,
+// compare and select of the sorting networks below serves two rows. A row's
+// candidates (blocks 0 .. loc-1) are streamed in chunks of 512 scores, 32 per
+// lane, read with 16-byte loads; the half's next chunk (of this row or of its
+// next row) is already loading while the current one is ranked. Per chunk:
+//   1. the values are staged in the half's shared buffer, and every lane takes
+//      the max of its even and of its odd blocks (32 group maxima per row);
+//   2. tau = max(15th largest group max, worst key kept so far): at least k-1
 //      keys are >= tau, so no key below tau can be in the answer;
-//   3. the keys >= tau (typically a few dozen) are compacted into shared memory
-//      and bitonic-sorted across the warp (64 keys, 2 per lane); the best k-1
-//      are kept, one per lane. More than 64 survivors fall back to k-1 rounds of
-//      warp arg-max.
+//   3. the keys >= tau (typically 15-30) are compacted into shared memory (each
+//      lane reads its survivors back from its staged values) and bitonic-sorted
+//      within the half (32 keys, 2 per lane); the best k-1 are kept, one per
+//      lane. More than 32 survivors in either half send both halves through
+//      k-1 rounds of arg-max instead.
 // Finally the kept ids plus the local block are sorted ascending and written.
+// Blocks past the candidates read as NaN, which no comparison keeps and which
+// max.f32 ignores (inputs themselves must be finite).
+#include <algorithm>
+#include <climits>
+
 #include "msa_kernels.h"
 
 namespace msa {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kChunk = 1024;
-constexpr int kCap = 64;
+constexpr int kWarps = 4;
+constexpr int kHalf = 512;  // candidates per half-warp chunk: 32 per lane
+constexpr int kCap = 32;    // survivors of a row sorted in the fast path
+constexpr unsigned kAll = 0xffffffffu;
 
 __device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m) {
-  uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
-  uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+  uint32_t lo = __shfl_xor_sync(kAll, (uint32_t)v, m);
+  uint32_t hi = __shfl_xor_sync(kAll, (uint32_t)(v >> 32), m);
   return ((uint64_t)hi << 32) | lo;
 }
-__device__ __forceinline__ uint64_t shfl64(uint64_t v, int src) {
-  uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)v, src);
-  uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(v >> 32), src);
+// value of lane src of this lane's half
+__device__ __forceinline__ uint64_t shfl64_h(uint64_t v, int src) {
+  uint32_t lo = __shfl_sync(kAll, (uint32_t)v, src, 16);
+  uint32_t hi = __shfl_sync(kAll, (uint32_t)(v >> 32), src, 16);
   return ((uint64_t)hi << 32) | lo;
 }
 
@@ -51,203 +62,266 @@ __device__ __forceinline__ float key_value(uint64_t key) {
   return __uint_as_float(b);
 }
 
-// bitonic sort of one key per lane, descending (lane 0 = largest)
-__device__ __forceinline__ uint64_t sort32_desc(uint64_t a, int lane) {
+// Bitonic sort, descending, of the 32 elements a half holds 2 per lane
+// (element e = hl + 16 r is a[r] of half-lane hl). Exchanges at distance 16 stay
+// in the lane; the others are shuffles within the half.
+__device__ __forceinline__ float shx(float v, int m) { return __shfl_xor_sync(kAll, v, m); }
+__device__ __forceinline__ uint64_t shx(uint64_t v, int m) { return shfl_xor64(v, m); }
+
+template <typename T>
+__device__ __forceinline__ void sort32h_desc(T& a0, T& a1, int hl) {
 #pragma unroll
   for (int size = 2; size <= 32; size <<= 1)
 #pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      uint64_t p = shfl_xor64(a, stride);
-      bool up = (lane & size) == 0;
-      bool lower = (lane & stride) == 0;
-      uint64_t hi = a > p ? a : p, lo = a > p ? p : a;
-      a = (lower == up) ? hi : lo;
-    }
-  return a;
-}
-
-// bitonic sort of 64 keys (element e = lane + 32 r held in a[r]), descending
-__device__ __forceinline__ void sort64_desc(uint64_t& a0, uint64_t& a1, int lane) {
-#pragma unroll
-  for (int size = 2; size <= 64; size <<= 1)
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride == 32) {
-        uint64_t hi = a0 > a1 ? a0 : a1, lo = a0 > a1 ? a1 : a0;
-        a0 = hi;
-        a1 = lo;
+      if (stride == 16) {  // size 32: the whole sequence descends
+        const bool sw = a1 > a0;
+        const T x = sw ? a1 : a0, y = sw ? a0 : a1;
+        a0 = x;
+        a1 = y;
       } else {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          uint64_t& a = r ? a1 : a0;
-          int e = lane + 32 * r;
-          uint64_t p = shfl_xor64(a, stride);
-          bool up = (e & size) == 0;
-          bool lower = (e & stride) == 0;
-          uint64_t hi = a > p ? a : p, lo = a > p ? p : a;
-          a = (lower == up) ? hi : lo;
+          T& a = r ? a1 : a0;
+          const int e = hl + 16 * r;
+          const T p = shx(a, stride);
+          const bool up = (e & size) == 0;
+          const bool lower = (e & stride) == 0;
+          const T mx = a > p ? a : p, mn = a > p ? p : a;
+          a = (lower == up) ? mx : mn;
         }
       }
     }
 }
 
-// bitonic sort of one int per lane, ascending
-__device__ __forceinline__ int sort32_asc(int a, int lane) {
+// bitonic sort of one int per lane within each 16-lane half, ascending
+__device__ __forceinline__ int sort16h_asc(int a, int hl) {
 #pragma unroll
-  for (int size = 2; size <= 32; size <<= 1)
+  for (int size = 2; size <= 16; size <<= 1)
 #pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      int p = __shfl_xor_sync(0xffffffffu, a, stride);
-      bool up = (lane & size) == 0;
-      bool lower = (lane & stride) == 0;
+      const int p = __shfl_xor_sync(kAll, a, stride);
+      const bool up = (hl & size) == 0;
+      const bool lower = (hl & stride) == 0;
       a = (lower == up) ? min(a, p) : max(a, p);
     }
   return a;
 }
 
-// bitonic sort of one float per lane, descending
-__device__ __forceinline__ float sort32_desc_f(float a, int lane) {
+// Loads a half's chunk (p = first candidate of the chunk, rem = candidates left
+// in the row from there): lane value 4 i + e is candidate 64 i + 4 hl + e;
+// candidates at or past rem read as NaN. VEC: p is 16-byte aligned.
+template <bool VEC>
+__device__ __forceinline__ void load_chunk(float (&v)[32], const float* __restrict__ p, int rem,
+                                           int hl) {
+  const float nan = __int_as_float(0x7fffffff);
 #pragma unroll
-  for (int size = 2; size <= 32; size <<= 1)
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      float p = __shfl_xor_sync(0xffffffffu, a, stride);
-      bool up = (lane & size) == 0;
-      bool lower = (lane & stride) == 0;
-      a = (lower == up) ? fmaxf(a, p) : fminf(a, p);
+  for (int i = 0; i < 8; ++i) {
+    const int o = i * 64 + hl * 4;
+    float4 x = make_float4(nan, nan, nan, nan);
+    if (o < rem) {
+      if constexpr (VEC) {
+        x = __ldcs(reinterpret_cast<const float4*>(p + o));
+        if (o + 4 > rem) {  // ragged end: mask the blocks past the candidates
+          if (o + 1 >= rem) x.y = nan;
+          if (o + 2 >= rem) x.z = nan;
+          x.w = nan;
+        }
+      } else {
+        x.x = p[o];
+        if (o + 1 < rem) x.y = p[o + 1];
+        if (o + 2 < rem) x.z = p[o + 2];
+        if (o + 3 < rem) x.w = p[o + 3];
+      }
     }
-  return a;
+    v[4 * i + 0] = x.x;
+    v[4 * i + 1] = x.y;
+    v[4 * i + 2] = x.z;
+    v[4 * i + 3] = x.w;
+  }
 }
 
-// key of the j-th value held by a lane in chunk c0 (see the load pattern)
-__device__ __forceinline__ int64_t elem_block(int64_t c0, int lane, int j) {
-  return c0 + (j >> 2) * 128 + lane * 4 + (j & 3);
+// Row cursor of one half: row r = q * n_g + g walks by a fixed stride, and its
+// query index q follows without a division per step.
+struct RowCursor {
+  int64_t r;
+  int q, rm;  // r / n_g, r % n_g
+  __device__ __forceinline__ void step(int64_t stride, int sq, int sr, int n_g) {
+    r += stride;
+    q += sq;
+    rm += sr;
+    if (rm >= n_g) {
+      rm -= n_g;
+      ++q;
+    }
+  }
+};
+
+// Local block of the cursor's row (its query's position / Bk), or -1 when that
+// position lies outside the score rows.
+__device__ __forceinline__ int64_t row_loc(const RowCursor& c, int Bk, int bk_shift, int64_t nb,
+                                           int64_t q_offset, const int32_t* __restrict__ seq_lens) {
+  const int64_t pos = seq_lens ? (int64_t)seq_lens[c.q] - 1 : c.q + q_offset;
+  if (pos < 0) return -1;
+  const int64_t loc = bk_shift >= 0 ? pos >> bk_shift : pos / Bk;
+  return loc < nb ? loc : -1;
 }
 
-__global__ void __launch_bounds__(kWarps * 32)
-topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, int Bk, int k,
-            int64_t q_offset, const int32_t* __restrict__ seq_lens, int32_t* __restrict__ ids,
-            Diag dg) {
-  __shared__ uint64_t buf[kWarps][kCap];
+// Ranks each half's staged chunk (sv) into the kfar best keys the half kept so
+// far (best: half-lane i < kfar holds the i-th best, descending). m0, m1: the
+// lane's two group maxima.
+__device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1, uint64_t* buf,
+                                           int64_t c0, int kfar, int hl, uint64_t& best,
+                                           float& best_min) {
+  // threshold: the kfar-th largest group max (>= kfar values reach it) or the
+  // worst value kept so far, whichever is larger
+  sort32h_desc(m0, m1, hl);
+  float tau = __shfl_sync(kAll, m0, kfar - 1, 16);
+  tau = fmaxf(tau, best_min);
+  // survivors (>= tau; ties at tau are kept and settled by the keys)
+  uint32_t mask = 0;
+#pragma unroll 2
+  for (int i = 0; i < 8; ++i) {
+    const float4 x = sv[i * 16 + hl];
+    const uint32_t m4 = (x.x >= tau ? 1u : 0u) | (x.y >= tau ? 2u : 0u) |
+                        (x.z >= tau ? 4u : 0u) | (x.w >= tau ? 8u : 0u);
+    mask |= m4 << (4 * i);
+  }
+  const bool keep_old = hl < kfar && best != 0 && key_value(best) >= tau;
+  const int cnt = __popc(mask) + (keep_old ? 1 : 0);
+  int incl = cnt;
+#pragma unroll
+  for (int off = 1; off < 16; off <<= 1) {
+    const int y = __shfl_up_sync(kAll, incl, off, 16);
+    if (hl >= off) incl += y;
+  }
+  const int total = __shfl_sync(kAll, incl, 15, 16);
+  const float* svf = reinterpret_cast<const float*>(sv);
+  if (!__any_sync(kAll, total > kCap)) {
+    int p = incl - cnt;
+    if (keep_old) buf[p++] = best;
+    while (mask) {  // this lane's survivors, read back from its own staged values
+      const int j = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const int e = (j >> 2) * 64 + hl * 4 + (j & 3);
+      buf[p++] = rank_key(svf[e], (uint32_t)(c0 + e));
+    }
+    __syncwarp();
+    uint64_t a0 = hl < total ? buf[hl] : 0;
+    uint64_t a1 = hl + 16 < total ? buf[hl + 16] : 0;
+    __syncwarp();
+    sort32h_desc(a0, a1, hl);
+    best = hl < kfar ? a0 : 0;
+  } else {
+    // rare (heavy ties): extract the kfar best of each half one by one
+    uint64_t nb_best = 0, prev = ~0ull;
+    const uint64_t old = hl < kfar ? best : 0;
+    for (int round = 0; round < kfar; ++round) {
+      uint64_t m = old < prev ? old : 0;
+      for (uint32_t mm = mask; mm; mm &= mm - 1) {
+        const int j = __ffs(mm) - 1;
+        const int e = (j >> 2) * 64 + hl * 4 + (j & 3);
+        const uint64_t key = rank_key(svf[e], (uint32_t)(c0 + e));
+        if (key < prev && key > m) m = key;
+      }
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) {
+        const uint64_t y = shfl_xor64(m, off);
+        m = y > m ? y : m;
+      }
+      if (hl == round) nb_best = m;
+      prev = m;
+    }
+    best = nb_best;
+  }
+  best_min = key_value(shfl64_h(best, kfar - 1));
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kWarps * 32, 5)
+topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, int Bk,
+            int bk_shift, int k, int64_t q_offset, const int32_t* __restrict__ seq_lens,
+            int32_t* __restrict__ ids, Diag dg) {
+  __shared__ uint64_t buf[kWarps][2][kCap];
+  __shared__ float4 sval[kWarps][2][8 * 16];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
+  const int half = lane >> 4, hl = lane & 15;
   const int kfar = k - 1;
-  const bool vec = (nb % 4) == 0 && ((uintptr_t)S % 16) == 0;
+  const int64_t stride = (int64_t)gridDim.x * kWarps * 2;  // rows per sweep (one per half)
+  const int sq = (int)(stride / n_g), sr = (int)(stride % n_g);
+  float4* sv = sval[wid][half];
+  uint64_t* bf = buf[wid][half];
 
-  for (int64_t r = (int64_t)blockIdx.x * kWarps + wid; r < n_rows;
-       r += (int64_t)gridDim.x * kWarps) {
-    const int64_t pos = seq_lens ? (int64_t)seq_lens[r / n_g] - 1 : r / n_g + q_offset;
-    const int64_t loc = pos / Bk;
-    const int64_t ncand = loc;  // candidate blocks 0 .. loc-1
-    int32_t* out = ids + r * k;
-    if (pos < 0 || loc >= nb) {  // position outside the score rows: flag, emit padding
-      if (lane == 0) report(dg, kStatusBadIds);
-      if (lane < k) out[lane] = -1;
-      continue;
-    }
-    if (ncand <= kfar) {  // every visible block is kept
-      if (lane < k) out[lane] = lane <= loc ? lane : -1;
-      continue;
-    }
-    const float* row = S + r * nb;
-    uint64_t best = 0;           // lane i < kfar: i-th best key so far (descending), else 0
-    float best_min = -INFINITY;  // value of the kfar-th best so far (-inf before any chunk)
-    for (int64_t c0 = 0; c0 < ncand; c0 += kChunk) {
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int64_t b = c0 + i * 128 + lane * 4;
-        float4 x = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        if (b < ncand) {
-          if (vec) {
-            x = __ldcs(reinterpret_cast<const float4*>(row + b));
-            if (b + 3 >= ncand) {  // ragged end: mask the blocks past the candidates
-              if (b + 1 >= ncand) x.y = -INFINITY;
-              if (b + 2 >= ncand) x.z = -INFINITY;
-              x.w = -INFINITY;
-            }
-          } else {
-            x.x = row[b];
-            if (b + 1 < ncand) x.y = row[b + 1];
-            if (b + 2 < ncand) x.z = row[b + 2];
-            if (b + 3 < ncand) x.w = row[b + 3];
-          }
-        }
-        v[4 * i + 0] = x.x;
-        v[4 * i + 1] = x.y;
-        v[4 * i + 2] = x.z;
-        v[4 * i + 3] = x.w;
+  // Moves the cursor to the first row at or after it that needs ranking; rows
+  // that need none (position outside the score rows, or no more candidates than
+  // far slots) are written on the way by this half. loc_out: that row's local
+  // block. The cursor ends at n_rows or beyond when there is none.
+  auto seek = [&](RowCursor& c, int64_t& loc_out) {
+    for (; c.r < n_rows; c.step(stride, sq, sr, n_g)) {
+      const int64_t loc = row_loc(c, Bk, bk_shift, nb, q_offset, seq_lens);
+      int32_t* out = ids + c.r * k;
+      if (loc < 0) {  // flag, emit padding
+        if (hl == 0) report(dg, kStatusBadIds);
+        if (hl < k) out[hl] = -1;
+        continue;
       }
-      // 1. lane max, 2. threshold: the kfar-th largest lane max (>= kfar values
-      //    reach it) or the worst value kept so far, whichever is larger
-      float lmax = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) lmax = fmax3(lmax, v[j], v[j + 1]);
-      const float srt = sort32_desc_f(lmax, lane);
-      float tau = __shfl_sync(0xffffffffu, srt, kfar - 1);
-      tau = fmaxf(tau, best_min);
-      // 3. survivors (>= tau; ties at tau are kept and settled by the keys)
-      uint32_t mask = 0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) mask |= (v[j] >= tau && v[j] != -INFINITY) ? (1u << j) : 0u;
-      const bool keep_old = lane < kfar && best != 0 && key_value(best) >= tau;
-      const int cnt = __popc(mask) + (keep_old ? 1 : 0);
-      int incl = cnt;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
+      if (loc <= kfar) {  // every visible block is kept
+        if (hl < k) out[hl] = hl <= loc ? hl : -1;
+        continue;
       }
-      const int total = __shfl_sync(0xffffffffu, incl, 31);
-      if (total <= kCap) {
-        int p = incl - cnt;
-        if (keep_old) buf[wid][p++] = best;
-        while (mask) {
-          const int j = __ffs(mask) - 1;
-          mask &= mask - 1;
-          float vj = v[0];
-#pragma unroll
-          for (int q = 1; q < 32; ++q)
-            if (q == j) vj = v[q];
-          buf[wid][p++] = rank_key(vj, (uint32_t)elem_block(c0, lane, j));
-        }
-        __syncwarp();
-        uint64_t a0 = lane < total ? buf[wid][lane] : 0;
-        if (total <= 32) {
-          a0 = sort32_desc(a0, lane);
-        } else {
-          uint64_t a1 = lane + 32 < total ? buf[wid][lane + 32] : 0;
-          sort64_desc(a0, a1, lane);
-        }
-        __syncwarp();
-        best = lane < kfar ? a0 : 0;
-      } else {
-        // rare: too many survivors (heavy ties); extract the k-1 best one by one
-        uint64_t nb_best = 0, prev = ~0ull;
-        const uint64_t old = lane < kfar ? best : 0;
-        for (int round = 0; round < kfar; ++round) {
-          uint64_t m = old < prev ? old : 0;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (!((mask >> j) & 1u)) continue;
-            uint64_t key = rank_key(v[j], (uint32_t)elem_block(c0, lane, j));
-            if (key < prev && key > m) m = key;
-          }
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) {
-            uint64_t y = shfl_xor64(m, off);
-            m = y > m ? y : m;
-          }
-          if (lane == round) nb_best = m;
-          prev = m;
-        }
-        best = nb_best;
-      }
-      best_min = key_value(shfl64(best, kfar - 1));
+      loc_out = loc;
+      return;
     }
-    int id = lane < kfar ? key_id(best) : (lane == kfar ? (int)loc : 0x7FFFFFFF);
-    id = sort32_asc(id, lane);
-    if (lane < k) out[lane] = id == 0x7FFFFFFF ? -1 : id;
+  };
+
+  RowCursor cur;
+  cur.r = ((int64_t)blockIdx.x * kWarps + wid) * 2 + half;
+  cur.q = (int)(cur.r / n_g);
+  cur.rm = (int)(cur.r % n_g);
+  int64_t loc = 0, c0 = 0;
+  seek(cur, loc);
+  float vn[32];
+  load_chunk<VEC>(vn, S + (cur.r < n_rows ? cur.r * nb : 0),
+                  cur.r < n_rows ? (int)min(loc, (int64_t)kHalf) : 0, hl);
+  uint64_t best = 0;           // half-lane i < kfar: i-th best key so far, else 0
+  float best_min = -INFINITY;  // value of the kfar-th best so far (-inf before any chunk)
+  while (__any_sync(kAll, cur.r < n_rows)) {
+    const bool act = cur.r < n_rows;
+    // stage the chunk; group maxima over the lane's even and odd blocks (so a
+    // short row's few candidates still give two maxima per lane)
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      sv[i * 16 + hl] = make_float4(vn[4 * i], vn[4 * i + 1], vn[4 * i + 2], vn[4 * i + 3]);
+      m0 = fmax3(m0, vn[4 * i], vn[4 * i + 2]);
+      m1 = fmax3(m1, vn[4 * i + 1], vn[4 * i + 3]);
+    }
+    // the half's next work item: this row's next chunk, else its next row's first
+    RowCursor nxt = cur;
+    int64_t c2 = c0 + kHalf, loc2 = loc;
+    if (act && c2 >= loc) {
+      nxt.step(stride, sq, sr, n_g);
+      seek(nxt, loc2);
+      c2 = 0;
+    }
+    const bool act2 = nxt.r < n_rows;
+    load_chunk<VEC>(vn, S + (act2 ? nxt.r * nb + c2 : 0),
+                    act2 ? (int)min(loc2 - c2, (int64_t)kHalf) : 0, hl);
+    rank_chunk(sv, m0, m1, bf, c0, kfar, hl, best, best_min);
+    const bool done = act && c0 + kHalf >= loc;
+    if (__any_sync(kAll, done)) {  // kept ids plus the local block, ascending
+      int id = hl < kfar ? (best ? key_id(best) : INT_MAX) : (hl == kfar ? (int)loc : INT_MAX);
+      id = sort16h_asc(id, hl);
+      if (done) {
+        if (hl < k) ids[cur.r * k + hl] = id == INT_MAX ? -1 : id;
+        best = 0;
+        best_min = -INFINITY;
+      }
+    }
+    cur = nxt;
+    c0 = c2;
+    loc = loc2;
   }
 }
 
@@ -275,10 +349,25 @@ cudaError_t launch_topk(const float* S, int64_t N, int n_g, int64_t nb, int Bk, 
         n_rows, n_g, Bk, k, q_offset, seq_lens, ids);
     return cudaGetLastError();
   }
-  int64_t blocks = (n_rows + kWarps - 1) / kWarps;
-  if (blocks > 152 * 64) blocks = 152 * 64;
-  topk_kernel<<<(unsigned)blocks, kWarps * 32, 0, st>>>(S, n_rows, n_g, nb, Bk, k, q_offset,
-                                                       seq_lens, ids, dg);
+  // persistent: as many CTAs as fit on the device at once
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<true>, kWarps * 32, 0);
+  if (e != cudaSuccess) return e;
+  if (n_rows > INT_MAX) return cudaErrorInvalidValue;  // query indexes are 32-bit
+  int64_t blocks = (n_rows + 2 * kWarps - 1) / (2 * kWarps);
+  blocks = std::min<int64_t>(blocks, (int64_t)sms * std::max(per_sm, 1));
+  const int bk_shift = (Bk & (Bk - 1)) == 0 ? __builtin_ctz((unsigned)Bk) : -1;
+  const bool vec = (nb % 4) == 0 && ((uintptr_t)S % 16) == 0;
+  if (vec)
+    topk_kernel<true><<<(unsigned)blocks, kWarps * 32, 0, st>>>(S, n_rows, n_g, nb, Bk, bk_shift,
+                                                               k, q_offset, seq_lens, ids, dg);
+  else
+    topk_kernel<false><<<(unsigned)blocks, kWarps * 32, 0, st>>>(S, n_rows, n_g, nb, Bk,
+                                                                bk_shift, k, q_offset, seq_lens,
+                                                                ids, dg);
   return cudaGetLastError();
 }
 

@@ -89,7 +89,8 @@ int msa_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_grou
  *                is not NULL, at position seq_lens[t] - 1 (decode: one row
  *                per sequence t); only b <= position / Bk is read.
  *   block_ids    [N, n_groups, k] int32 out.
- * Requires position / Bk < nb for every row. */
+ * Requires position / Bk < nb for every row; N * n_groups above 2^31 - 1 rows
+ * returns MSA_ERR_UNSUPPORTED. */
 int msa_topk_blocks(const float* block_scores, int64_t N, int n_groups, int64_t nb, int Bk,
                     int k, int64_t q_offset, const int32_t* seq_lens, int32_t* block_ids,
                     void* stream);
