@@ -13,8 +13,9 @@ Prints ONE JSON line. `value` is prefill tokens/s (all ranks). Further keys:
   roofline     dominant kernel (the index branch): algorithmic flops per launch
                / its CUDA-event time, against the measured dense bf16 peak
   cpu_baseline the CPU oracle on a bounded sample of the same workload
-  extra        the other measured paths: 32K and (optionally) 1M prefill,
-               decode steps with bf16 and FP8-E4M3 KV, standalone top-16
+  extra        the other measured paths: 32K and 1M prefill (1M: 2 timed steps),
+               decode steps with bf16 and FP8-E4M3 KV, standalone top-16 (with
+               torch.topk over the same scores as a comparator)
 
 Multi-GPU: each rank runs its own independent sequence (no collective on the
 data path; weak scaling); time is the max over ranks.
@@ -450,7 +451,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="128k")
-    ap.add_argument("--with-1m", action="store_true", help="also time the 1M-token prefill")
+    ap.add_argument("--no-1m", action="store_true", help="skip the 1M-token prefill extra")
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=15.0)
@@ -590,10 +591,9 @@ def main():
                 "index_scan_gbs": round(scan_bytes / (i_ms * 1e-3) / 1e9, 1),
                 "attention_gbs": round(kv_bytes / (a_ms * 1e-3) / 1e9, 1),
                 "peak_gbs": peaks["hbm_gbs"]}
-        if args.with_1m:
+        if not args.no_1m:
             w1 = synth.make("1m")
-            P1, ms1, i1, a1, _ = time_prefill(msa, w1, max(1, args.steps // 2), 1, world,
-                                              ws_rows=w1.N // 8)
+            P1, ms1, i1, a1, _ = time_prefill(msa, w1, 2, 3, world, ws_rows=w1.N // 8)
             del P1
             torch.cuda.empty_cache()
             extra["prefill_1m"] = {"tokens_per_s": w1.N / (ms1 * 1e-3), "ms": round(ms1, 2),
