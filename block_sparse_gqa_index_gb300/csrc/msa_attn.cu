@@ -255,20 +255,25 @@ __global__ void bucket_fill_kernel(const int32_t* __restrict__ ids, int64_t q0, 
 //              P and the epilogue two tiles back has read the O columns.
 //              Splitting the two MMA streams over two threads lets each block
 //              on its own barriers;
-//   warps 2-5  Q producers: warp p fills the Q stage i % 4 of the tiles i with
-//              i % 4 == p. It reads the tile's entries ahead of time, then
+//   warps 2, 3, 12, 13
+//              Q producers: producer p fills the Q stage i % 4 of the tiles i
+//              with i % 4 == p. It reads the tile's entries ahead of time, then
 //              gathers the G head rows of each of the tile's queries with TMA
 //              row gathers (tile::gather4) into the 128B-swizzled layout; a
 //              stage is free again as soon as the S MMA that read it completed;
-//   warps 6-13 softmax + epilogue, two groups of four warps (one per TMEM
-//              stage), one score row per thread: the row's query and partial
-//              slot come straight from the tile's entries; masked row max,
-//              exp2, row sum, P (bf16) back into TMEM over S; then O / l in
-//              bf16 and the row's LSE into the tile's partial records in a
-//              shared-memory staging buffer;
+//   warps 4-11 softmax + epilogue, two groups of four warps (warpgroups 1 and
+//              2, one per TMEM stage), one score row per thread: the row's
+//              query and partial slot come straight from the tile's entries;
+//              the whole row of S in registers (one TMEM load round trip),
+//              masked row max, exp2, row sum, P (bf16) back into TMEM over S;
+//              then the whole O row, O / l in bf16 and the row's LSE into the
+//              tile's partial records in a shared-memory staging buffer;
 //   warp 14    one bulk copy per tile of its records (tile-major, so a tile's
 //              records are contiguous) from the staging buffer to the partial
-//              buffer.
+//              buffer. Warp 15 only rounds out warpgroup 3.
+// The softmax warpgroups hold 192 registers per thread and the other two 64
+// (setmaxnreg at the top of each role's branch, so that the compiler allocates
+// each branch with its own budget).
 template <int D>
 struct AttnSmem {
   static constexpr int kKVBytes = kBk * D * 2;            // one of K or V
@@ -288,9 +293,9 @@ struct AttnSmem {
 // the kernel needs its dynamic shared memory 1024-byte aligned (it checks)
 static_assert(AttnSmem<128>::kBytes <= 232448, "attention tile exceeds shared memory");
 
-constexpr int kProducers = 4;      // Q producer warps
+constexpr int kProducers = 4;      // Q producer warps (2, 3, 12, 13)
 constexpr int kStoreWarp = 14;     // bulk stores of the partial records
-constexpr int kAttnThreads = 480;  // 15 warps
+constexpr int kAttnThreads = 512;  // 16 warps: four warpgroups
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -397,6 +402,10 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // warpgroups 1 and 2 (warps 4-11) are the softmax groups: they take 192
+  // registers per thread so that a thread holds a whole row; warpgroups 0 and
+  // 3 (issuers, producers, store) drop to 64. 2 x 128 x 192 + 2 x 128 x 64
+  // is the 65536 registers the 512 threads were launched with.
 
   // this CTA's contiguous range of tiles
   const int64_t total = *n_tiles;
@@ -405,6 +414,9 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   const int n_local = t_end - t_begin;
   const int4 kNone = make_int4(0, 0, 0, 0);
 
+  const int wgid = warp >> 2;
+  if (wgid == 0 || wgid == 3) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
   if (warp == 0) {
     // ---------------------------------------------------------- K + S = Q K^T
     // Per K/V block (the next one starts at this block's end tile): once the
@@ -497,7 +509,7 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       mma_commit(&done_bar[1]);
       mbar_drain(&done_bar[1], 0);
     }
-  } else if (warp < 2 + kProducers) {
+  } else if (warp == 2 || warp == 3 || warp == 12 || warp == 13) {
     // ---------------------------------------------------------- Q producers
     // Tile rows are head-major: row r holds head i = r / qt of query r % qt, so
     // four consecutive rows are one head of four queries, fetched by one TMA
@@ -506,7 +518,7 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     // entries of queries l, l + 32, ... of the tile; the gathers pick up their
     // rows by shuffles. A tile's entries are loaded one iteration ahead and its
     // record two iterations ahead, so no global load is waited on here.
-    const int p = warp - 2;
+    const int p = warp < 4 ? warp - 2 : warp - 10;
     const int32_t oob_row = (int32_t)(tm_rows);  // first row past q: zero fill
     const int nj = (qt + 31) / 32;
     constexpr int NCH = D / 64;
@@ -595,12 +607,14 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         inf = nxt;
       }
     }
+  }
   } else {
     // ---------------------------------------------------------- softmax + epilogue
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory");
     // two groups of 4 warps; group wg takes the tiles i with i % 2 == wg, which
     // use TMEM stage wg, so one group's softmax overlaps the other's epilogue.
     // A row's entry is loaded one tile ahead, the tile record two tiles ahead.
-    const int wg = (warp - 2 - kProducers) >> 2;
+    const int wg = (warp - 4) >> 2;
     const int qq = warp & 3;
     const int row = qq * 32 + lane;
     const int hi = row / qt, qi = row % qt;
@@ -622,70 +636,52 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
       tc_fence_after();
       const int lim = (ent_c >= 0 && t / kBk == b) ? t - b * kBk + 1 : kBk;
-      // pass 1: row max. With no masked column in the warp the loads reduce
-      // (sm_103 TMEM load-with-max); the local block's rows reduce in registers.
+      // the whole row in registers: one load round trip; with no masked column
+      // in the warp the loads also reduce the row max (sm_103 load-with-max)
       const bool full = __all_sync(0xffffffffu, lim >= kBk);
-      float m = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        uint32_t r0[32], r1[32];
-        float m0 = -INFINITY, m1 = -INFINITY;
-        if (full) {
-          tmem_ld32_max(ts + c * 32, r0, m0);
-          tmem_ld32_max(ts + c * 32 + 32, r1, m1);
-        } else {
-          tmem_ld32(ts + c * 32, r0);
-          tmem_ld32(ts + c * 32 + 32, r1);
-        }
+      uint32_t r[128];
+      float m;
+      if (full) {
+        float m0, m1, m2, m3;
+        tmem_ld32_max(ts, *reinterpret_cast<uint32_t(*)[32]>(&r[0]), m0);
+        tmem_ld32_max(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]), m1);
+        tmem_ld32_max(ts + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]), m2);
+        tmem_ld32_max(ts + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]), m3);
         tmem_ld_wait();
-        if (!full) {
+        m = fmaxf(fmax3(m0, m1, m2), m3);
+      } else {
+        tmem_ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_ld32(ts + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+        tmem_ld32(ts + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+        tmem_ld_wait();
+        m = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (c * 32 + j < lim) m0 = fmaxf(m0, __uint_as_float(r0[j]));
-            if (c * 32 + 32 + j < lim) m1 = fmaxf(m1, __uint_as_float(r1[j]));
-          }
-        }
-        m = fmax3(m, m0, m1);
+        for (int j = 0; j < 128; ++j)
+          if (j < lim) m = fmaxf(m, __uint_as_float(r[j]));
       }
       const float mc = m * scale_log2;
-      // pass 2: P = exp2(s * c - m * c) in bf16 over the first 64 columns, row
-      // sum; the load of chunk c + 1 is in flight while chunk c is computed.
-      // Rows of the local block mask the columns past their query.
+      // P = exp2(s * c - m * c), packed to bf16 pairs in place (r[j] holds
+      // columns 2j, 2j + 1), row sum; rows of the local block mask the columns
+      // past their query
       const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-mc, -mc);
       uint64_t l2 = f2_pack(0.f, 0.f);
-      auto p_chunk = [&](const uint32_t(&r)[32], int c) {
-        uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          float p0, p1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), sc2, nm2),
-                    p0, p1);
-          p0 = ex2_approx(p0);
-          p1 = ex2_approx(p1);
-          if (!full) {
-            p0 = c * 32 + j < lim ? p0 : 0.f;
-            p1 = c * 32 + j + 1 < lim ? p1 : 0.f;
-          }
-          l2 = f2_add(l2, f2_pack(p0, p1));
-          pk[j >> 1] = pack_bf16x2(p0, p1);
+      for (int j = 0; j < 64; ++j) {
+        float p0, p1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), sc2,
+                         nm2), p0, p1);
+        p0 = ex2_approx(p0);
+        p1 = ex2_approx(p1);
+        if (!full) {
+          p0 = 2 * j < lim ? p0 : 0.f;
+          p1 = 2 * j + 1 < lim ? p1 : 0.f;
         }
-        tmem_st16(ts + c * 16, pk);
-      };
-      {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(ts, ra);
-        tmem_ld_wait();
-        tmem_ld32(ts + 32, rb);
-        p_chunk(ra, 0);
-        tmem_ld_wait();
-        tmem_ld32(ts + 64, ra);
-        p_chunk(rb, 1);
-        tmem_ld_wait();
-        tmem_ld32(ts + 96, rb);
-        p_chunk(ra, 2);
-        tmem_ld_wait();
-        p_chunk(rb, 3);
+        l2 = f2_add(l2, f2_pack(p0, p1));
+        r[j] = pack_bf16x2(p0, p1);
       }
+      tmem_st32(ts, *reinterpret_cast<const uint32_t(*)[32]>(&r[0]));
+      tmem_st32(ts + 32, *reinterpret_cast<const uint32_t(*)[32]>(&r[32]));
       float l0, l1;
       f2_unpack(l2, l0, l1);
       const float l = l0 + l1;
@@ -721,18 +717,13 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
       };
       {
-        uint32_t ra[32], rb[32];
-        tmem_ld32(ts + 128, ra);
+        uint32_t ro[D];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+          tmem_ld32(ts + 128 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&ro[32 * c]));
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < D / 32; c += 2) {
-          tmem_ld32(ts + 128 + (c + 1) * 32, rb);
-          o_chunk(ra, c);
-          tmem_ld_wait();
-          if (c + 2 < D / 32) tmem_ld32(ts + 128 + (c + 2) * 32, ra);
-          o_chunk(rb, c + 1);
-          if (c + 2 < D / 32) tmem_ld_wait();
-        }
+        for (int c = 0; c < D / 32; ++c) o_chunk(*reinterpret_cast<const uint32_t(*)[32]>(&ro[32 * c]), c);
       }
       tc_fence_before();
       __syncwarp();
