@@ -14,6 +14,7 @@ Prints ONE JSON line. `value` is prefill tokens/s (all ranks). Further keys:
                / its CUDA-event time, against the measured dense bf16 peak
   cpu_baseline the CPU oracle on a bounded sample of the same workload
   extra        the other measured paths: 32K and 1M prefill (1M: 2 timed steps),
+               the 128K tokens as 8 packed 16K sequences (varlen entry points),
                decode steps with bf16 and FP8-E4M3 KV, standalone top-16 (with
                torch.topk over the same scores as a comparator)
 
@@ -368,6 +369,44 @@ def time_topk(msa, w, steps, warmup):
     return t, read + wr, statistics.mean(ms_t)
 
 
+def time_varlen(msa, w, n_seq, steps, warmup):
+    """The workload's N tokens as n_seq packed sequences of N / n_seq tokens
+    (varlen entry points, one step = index + main branch over the batch)."""
+    import torch
+    import synth
+    qidx = synth.device_tensor(w, synth.T_QIDX)
+    kidx = synth.device_tensor(w, synth.T_KIDX)[:, 0].contiguous()
+    q = synth.device_tensor(w, synth.T_Q)
+    k = synth.device_tensor(w, synth.T_K)
+    v = synth.device_tensor(w, synth.T_V)
+    n = w.N // n_seq
+    cu = [i * n for i in range(n_seq + 1)]
+    ids = torch.empty((w.N, w.n_g, w.k), dtype=torch.int32, device="cuda")
+    ws = torch.empty(msa.msa_sparse_attn_varlen_workspace_bytes(cu, w.H_q, w.H_kv, w.d, w.Bk,
+                                                                w.k),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty((w.N, w.H_q), dtype=torch.float32, device="cuda")
+
+    def step():
+        msa.msa_index_select_varlen(qidx, kidx, cu, w.Bk, w.k, block_ids=ids)
+        msa.msa_sparse_attn_varlen(q, k, v, ids, cu, w.Bk, w.scale, workspace=ws, out=out,
+                                   lse=lse)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    flops = n_seq * (index_flops(n, w.n_g, w.d_idx) + attn_flops(n, w.H_q, w.d, w.Bk, w.k))
+    return ms, flops
+
+
 # ------------------------------------------------------------- CPU baseline
 def cpu_baseline(w, budget_s=20.0, seed=0):
     """The oracle (as it stands) on a bounded sample of rows of workload w;
@@ -576,6 +615,10 @@ def main():
                                 "algorithmic_bytes": tk_bytes,
                                 "torch_topk_ms": round(torch_ms, 4),
                                 "vs_torch_topk": round(torch_ms / tk_ms, 2)}
+        v_ms, v_fl = time_varlen(msa, w, 8, args.steps, 3)
+        torch.cuda.empty_cache()
+        extra["prefill_varlen_8x16k"] = {"tokens_per_s": w.N / (v_ms * 1e-3), "ms": round(v_ms, 3),
+                                         "tflops": round(v_fl / (v_ms * 1e-3) / 1e12, 2)}
         wd = synth.make("decode")
         for fp8 in (False, True):
             i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, 1)

@@ -59,13 +59,20 @@ _launch_count = _sig("msa_launch_count", [], _I64)
 _index_dec_noalloc = _sig("msa_index_select_decode_noalloc", [_P, _P, _P, _P, _I, _I, _I, _I, _I,
                                                               _I, _P, _P])
 _noalloc_max = _sig("msa_index_select_decode_noalloc_max_scores", [], _I64)
+_index_varlen = _sig("msa_index_select_varlen", [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P])
+_ws_attn_varlen = _sig("msa_sparse_attn_varlen_workspace_bytes", [_P, _I, _I, _I, _I, _I, _I],
+                       _SZ)
+_attn_varlen = _sig("msa_sparse_attn_varlen", [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
+                                               _P, _P, _P, _SZ, _P])
 
 EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes",
            "msa_index_select", "msa_topk_blocks", "msa_sparse_attn_workspace_bytes",
            "msa_sparse_attn", "msa_index_select_decode_workspace_bytes",
            "msa_index_select_decode", "msa_decode_workspace_bytes", "msa_decode",
            "msa_get_error", "msa_set_wait_limit", "msa_launch_count",
-           "msa_index_select_decode_noalloc", "msa_index_select_decode_noalloc_max_scores"]
+           "msa_index_select_decode_noalloc", "msa_index_select_decode_noalloc_max_scores",
+           "msa_index_select_varlen", "msa_sparse_attn_varlen_workspace_bytes",
+           "msa_sparse_attn_varlen"]
 
 
 class MSAError(RuntimeError):
@@ -178,6 +185,83 @@ def msa_sparse_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_ids
     _check(_sparse_attn(q.data_ptr(), k.data_ptr(), v.data_ptr(), block_ids.data_ptr(), N, H_q,
                         H_kv, d, Bk, topk, scale, out.data_ptr(), _ptr(lse),
                         workspace.data_ptr(), workspace.numel(), _stream(q)), "msa_sparse_attn")
+    return out, lse
+
+
+# ------------------------------------------------------------ varlen prefill
+def _cu_array(cu_seqlens):
+    """Host int64 copy of the cumulative sequence offsets [B + 1]."""
+    cu = torch.as_tensor(cu_seqlens, dtype=torch.int64, device="cpu").contiguous()
+    if cu.dim() != 1 or cu.numel() < 1:
+        raise ValueError("cu_seqlens must be a 1-D sequence of B + 1 offsets")
+    return cu
+
+
+def msa_index_select_varlen(q_idx: torch.Tensor, k_idx: torch.Tensor, cu_seqlens,
+                            Bk: int = 128, k: int = 16,
+                            block_ids: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Index branch over B sequences packed back to back: sequence b holds rows
+    cu_seqlens[b] .. cu_seqlens[b + 1] - 1 of q_idx [T, n_groups, d_idx] and
+    k_idx [T, d_idx]; -> block_ids [T, n_groups, k], counted from each
+    sequence's first token."""
+    cu = _cu_array(cu_seqlens)
+    T, n_g, d_idx = q_idx.shape
+    _req(q_idx, "q_idx", torch.bfloat16)
+    _req(k_idx, "k_idx", torch.bfloat16, (T, d_idx))
+    if int(cu[-1]) != T:
+        raise ValueError("cu_seqlens[-1] must equal the number of rows")
+    if block_ids is None:
+        block_ids = torch.empty((T, n_g, k), dtype=torch.int32, device=q_idx.device)
+    _req(block_ids, "block_ids", torch.int32, (T, n_g, k))
+    _check(_index_varlen(q_idx.data_ptr(), k_idx.data_ptr(), cu.data_ptr(), cu.numel() - 1, n_g,
+                         d_idx, Bk, k, block_ids.data_ptr(), _stream(q_idx)),
+           "msa_index_select_varlen")
+    return block_ids
+
+
+def msa_sparse_attn_varlen_workspace_bytes(cu_seqlens, H_q: int, H_kv: int, d: int,
+                                           Bk: int = 128, k: int = 16) -> int:
+    cu = _cu_array(cu_seqlens)
+    return _ws_attn_varlen(cu.data_ptr(), cu.numel() - 1, H_q, H_kv, d, Bk, k)
+
+
+def msa_sparse_attn_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                           block_ids: torch.Tensor, cu_seqlens, Bk: int = 128,
+                           scale: Optional[float] = None,
+                           workspace: Optional[torch.Tensor] = None,
+                           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                           want_lse: bool = True):
+    """Main branch over B packed sequences (rows as in msa_index_select_varlen):
+    q [T, H_q, d], k / v [T, H_kv, d] bf16, block_ids [T, H_kv, topk] ->
+    out [T, H_q, d] bf16, lse [T, H_q] fp32."""
+    cu = _cu_array(cu_seqlens)
+    T, H_q, d = q.shape
+    H_kv = k.shape[1]
+    topk = block_ids.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _req(q, "q", torch.bfloat16)
+    _req(k, "k", torch.bfloat16, (T, H_kv, d))
+    _req(v, "v", torch.bfloat16, (T, H_kv, d))
+    _req(block_ids, "block_ids", torch.int32, (T, H_kv, topk))
+    if int(cu[-1]) != T:
+        raise ValueError("cu_seqlens[-1] must equal the number of rows")
+    if workspace is None:
+        workspace = torch.empty(max(1, _ws_attn_varlen(cu.data_ptr(), cu.numel() - 1, H_q, H_kv,
+                                                       d, Bk, topk)),
+                                dtype=torch.uint8, device=q.device)
+    _req(workspace, "workspace", torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, "out", torch.bfloat16, (T, H_q, d))
+    if lse is None and want_lse:
+        lse = torch.empty((T, H_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _req(lse, "lse", torch.float32, (T, H_q))
+    _check(_attn_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), block_ids.data_ptr(),
+                        cu.data_ptr(), cu.numel() - 1, H_q, H_kv, d, Bk, topk, scale,
+                        out.data_ptr(), _ptr(lse), workspace.data_ptr(), workspace.numel(),
+                        _stream(q)), "msa_sparse_attn_varlen")
     return out, lse
 
 

@@ -156,6 +156,70 @@ int msa_sparse_attn(const void* q, const void* k, const void* v, const int32_t* 
   return MSA_OK;
 }
 
+// --------------------------------------------------------------- varlen prefill
+// cu_seqlens: host int64 [B + 1], 0 = cu[0] <= cu[1] <= ... <= cu[B]
+static bool cu_ok(const int64_t* cu, int B) {
+  if (B < 0 || (B > 0 && !cu) || (B > 0 && cu[0] != 0)) return false;
+  for (int b = 0; b < B; ++b)
+    if (cu[b + 1] < cu[b]) return false;
+  return true;
+}
+
+size_t msa_sparse_attn_varlen_workspace_bytes(const int64_t* cu_seqlens, int B, int H_q,
+                                              int H_kv, int d, int Bk, int k) {
+  if (!cu_ok(cu_seqlens, B)) return 0;
+  size_t need = 0;
+  for (int b = 0; b < B; ++b) {
+    const int64_t n = cu_seqlens[b + 1] - cu_seqlens[b];
+    if (n > 0) need = std::max(need, msa_sparse_attn_workspace_bytes(n, n, H_q, H_kv, d, Bk, k));
+  }
+  return need;
+}
+
+int msa_index_select_varlen(const void* q_idx, const void* k_idx, const int64_t* cu_seqlens,
+                            int B, int n_groups, int d_idx, int Bk, int k, int32_t* block_ids,
+                            void* stream) {
+  if (!cu_ok(cu_seqlens, B) || n_groups < 1 || d_idx < 1 || Bk < 1 || k < 1)
+    return MSA_ERR_INVALID_ARG;
+  if (B == 0 || cu_seqlens[B] == 0) return MSA_OK;
+  if (!q_idx || !k_idx || !block_ids) return MSA_ERR_INVALID_ARG;
+  // every sequence's rows must start 16-byte aligned
+  if (((int64_t)n_groups * k * 4) % 16 != 0 || (d_idx * 2) % 16 != 0) return MSA_ERR_UNSUPPORTED;
+  for (int b = 0; b < B; ++b) {
+    const int64_t t0 = cu_seqlens[b], n = cu_seqlens[b + 1] - t0;
+    if (n == 0) continue;
+    const int rc = msa_index_select((const unsigned char*)q_idx + t0 * n_groups * d_idx * 2,
+                                    (const unsigned char*)k_idx + t0 * d_idx * 2, n, n_groups,
+                                    d_idx, Bk, k, block_ids + t0 * n_groups * k, nullptr,
+                                    nullptr, 0, stream);
+    if (rc != MSA_OK) return rc;
+  }
+  return MSA_OK;
+}
+
+int msa_sparse_attn_varlen(const void* q, const void* k, const void* v, const int32_t* block_ids,
+                           const int64_t* cu_seqlens, int B, int H_q, int H_kv, int d, int Bk,
+                           int topk, float scale, void* out, float* lse, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!cu_ok(cu_seqlens, B) || H_q < 1 || H_kv < 1 || d < 1 || Bk < 1 || topk < 1)
+    return MSA_ERR_INVALID_ARG;
+  if (B == 0 || cu_seqlens[B] == 0) return MSA_OK;
+  if (!q || !k || !v || !block_ids || !out || !workspace) return MSA_ERR_INVALID_ARG;
+  if (((int64_t)H_kv * topk * 4) % 16 != 0 || (lse && (H_q * 4) % 16 != 0))
+    return MSA_ERR_UNSUPPORTED;
+  for (int b = 0; b < B; ++b) {
+    const int64_t t0 = cu_seqlens[b], n = cu_seqlens[b + 1] - t0;
+    if (n == 0) continue;
+    const int rc = msa_sparse_attn(
+        (const unsigned char*)q + t0 * H_q * d * 2, (const unsigned char*)k + t0 * H_kv * d * 2,
+        (const unsigned char*)v + t0 * H_kv * d * 2, block_ids + t0 * H_kv * topk, n, H_q, H_kv,
+        d, Bk, topk, scale, (unsigned char*)out + t0 * H_q * d * 2, lse ? lse + t0 * H_q : nullptr,
+        workspace, workspace_bytes, stream);
+    if (rc != MSA_OK) return rc;
+  }
+  return MSA_OK;
+}
+
 size_t msa_index_select_decode_workspace_bytes(int B, int max_pages, int n_groups) {
   if (B < 0 || max_pages < 0 || n_groups < 0) return 0;
   return (size_t)B * max_pages * n_groups * sizeof(float);

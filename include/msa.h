@@ -117,6 +117,35 @@ int msa_sparse_attn(const void* q, const void* k, const void* v, const int32_t* 
                     void* out, float* lse, void* workspace, size_t workspace_bytes,
                     void* stream);
 
+/* Varlen batched prefill: B sequences packed back to back, the serving form of
+ * the two prefill entry points above (the usage listing of the MSA page,
+ * "运行 Kernel", plans each call from per-sequence query and key lengths).
+ * Sequence b holds rows cu_seqlens[b] .. cu_seqlens[b + 1] - 1 of every tensor;
+ * its queries see only its own keys, and its block ids count blocks from its
+ * own first token.
+ *   cu_seqlens  host int64 [B + 1] with 0 = cu_seqlens[0] <= ... <= cu_seqlens[B]
+ *               (MSA_ERR_INVALID_ARG otherwise)
+ * Other tensors as in msa_index_select / msa_sparse_attn with N = cu_seqlens[B].
+ * Each sequence runs as its own pass of the single-sequence kernels on the
+ * stream, which reuses the workspace from one sequence to the next. Every
+ * sequence's rows must start 16-byte aligned: n_groups * k (and, for the
+ * main branch, H_kv * topk, and H_q when lse is given) a multiple of 4, else
+ * MSA_ERR_UNSUPPORTED. */
+int msa_index_select_varlen(const void* q_idx, const void* k_idx, const int64_t* cu_seqlens,
+                            int B, int n_groups, int d_idx, int Bk, int k, int32_t* block_ids,
+                            void* stream);
+
+/* Workspace for msa_sparse_attn_varlen to take every sequence in one pass (any
+ * msa_sparse_attn_workspace_bytes(c, ...) with c >= 1 also works, in chunks);
+ * 0 when cu_seqlens is invalid. */
+size_t msa_sparse_attn_varlen_workspace_bytes(const int64_t* cu_seqlens, int B, int H_q,
+                                              int H_kv, int d, int Bk, int k);
+
+int msa_sparse_attn_varlen(const void* q, const void* k, const void* v, const int32_t* block_ids,
+                           const int64_t* cu_seqlens, int B, int H_q, int H_kv, int d, int Bk,
+                           int topk, float scale, void* out, float* lse, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
 /* ----------------------------------------------------------------- decode -- */
 
 /* Paged caches ("运行 Kernel": page size = block size; the page tensor's second

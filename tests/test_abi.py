@@ -102,3 +102,41 @@ def test_decode_rejects(msa):
 def test_wait_limit_roundtrip(msa):
     old = msa.msa_set_wait_limit(123)
     assert msa.msa_set_wait_limit(old) == 123
+
+
+def test_varlen_rejects(msa):
+    """Varlen prefill validates the cumulative offsets and the per-sequence
+    alignment on the host, before anything is launched."""
+    import ctypes as C
+
+    def cu(*xs):
+        a = (C.c_int64 * len(xs))(*xs)
+        return C.cast(a, C.c_void_p), a
+
+    fi, fa = msa._index_varlen, msa._attn_varlen
+    p, keep = cu(1, 5)  # first offset must be 0
+    assert fi(FAKE, FAKE, p, 1, 8, 128, 128, 16, FAKE, None) == -1
+    p, keep = cu(0, 7, 5)  # offsets must not decrease
+    assert fi(FAKE, FAKE, p, 2, 8, 128, 128, 16, FAKE, None) == -1
+    assert fi(FAKE, FAKE, None, 1, 8, 128, 128, 16, FAKE, None) == -1  # no offsets
+    p, keep = cu(0)
+    assert fi(FAKE, FAKE, p, 0, 8, 128, 128, 16, FAKE, None) == 0  # no sequences
+    p, keep = cu(0, 0, 0)
+    assert fi(FAKE, FAKE, p, 2, 8, 128, 128, 16, FAKE, None) == 0  # only empty sequences
+    p, keep = cu(0, 100)
+    assert fi(FAKE, FAKE, p, 1, 8, 128, 64, 16, FAKE, None) == -2   # Bk != 128
+    assert fi(FAKE, FAKE, p, 1, 1, 128, 128, 3, FAKE, None) == -2   # n_g * k not a multiple of 4
+    assert fi(None, FAKE, p, 1, 8, 128, 128, 16, FAKE, None) == -1  # null q_idx
+    # main branch: same offset rules; lse rows of 2 heads would misalign sequences
+    args = (FAKE, FAKE, FAKE, FAKE)
+    p, keep = cu(3, 10)
+    assert fa(*args, p, 1, 32, 8, 128, 128, 16, 0.1, FAKE, None, FAKE, 1 << 20, None) == -1
+    p, keep = cu(0, 10)
+    assert fa(*args, p, 1, 2, 1, 128, 128, 16, 0.1, FAKE, FAKE, FAKE, 1 << 20, None) == -2
+    assert fa(*args, p, 1, 32, 8, 128, 64, 16, 0.1, FAKE, None, FAKE, 1 << 20, None) == -2
+    # workspace query: 0 for bad offsets, the largest sequence's one-pass need otherwise
+    p, keep = cu(0, 7, 5)
+    assert msa._ws_attn_varlen(p, 2, 32, 8, 128, 128, 16) == 0
+    p, keep = cu(0, 300, 300, 1000)
+    assert msa._ws_attn_varlen(p, 3, 32, 8, 128, 128, 16) == \
+        msa.msa_sparse_attn_workspace_bytes(700, 700, 32, 8, 128)

@@ -252,6 +252,67 @@ def test_pipeline_1m(msa):
     assert n > 0
 
 
+# ------------------------------------------------------------ varlen prefill
+
+@pytest.mark.parametrize("H_q,H_kv,d", [(8, 2, 64), (16, 4, 128)])
+def test_varlen_prefill_matches_each_sequence(msa, H_q, H_kv, d):
+    """Sequences of ragged lengths packed back to back (one seeded integer-index
+    workload each): every sequence's block ids equal the oracle's for that
+    sequence alone, bit for bit, and its attention rows match the oracle on
+    those ids, so no sequence sees another one's keys."""
+    lens = [1, 5, 127, 128, 129, 700, 2100, 300]
+    wls = [synth.make("tiny", L=n, H_q=H_q, H_kv=H_kv, d=d, d_idx=d, seed=50 + i)
+           for i, n in enumerate(lens)]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    qi = torch.cat([synth.device_tensor(w, synth.T_QIDX) for w in wls])
+    ki = torch.cat([kidx2d(synth.device_tensor(w, synth.T_KIDX)) for w in wls])
+    q = torch.cat([synth.device_tensor(w, synth.T_Q) for w in wls])
+    kk = torch.cat([synth.device_tensor(w, synth.T_K) for w in wls])
+    v = torch.cat([synth.device_tensor(w, synth.T_V) for w in wls])
+    ids = msa.msa_index_select_varlen(qi, ki, cu, 128, 16)
+    out, lse = msa.msa_sparse_attn_varlen(q, kk, v, ids, cu, 128, wls[0].scale)
+    torch.cuda.synchronize()
+    ids_h, out_h, lse_h = ids.cpu().numpy(), bf16_to_np(out), lse.cpu().numpy()
+    for i, w in enumerate(wls):
+        a, b = cu[i], cu[i + 1]
+        rows = np.arange(w.N)
+        want = oracle.index_select(synth.host_tensor(w, synth.T_QIDX)[0], rows,
+                                   synth.host_tensor(w, synth.T_KIDX)[0, :, 0], w.Bk, w.k)
+        assert np.array_equal(ids_h[a:b], want), f"sequence {i} (length {w.N})"
+        o_ref, l_ref = oracle.sparse_attn(synth.host_tensor(w, synth.T_Q)[0], rows,
+                                          synth.host_tensor(w, synth.T_K)[0],
+                                          synth.host_tensor(w, synth.T_V)[0], want, w.Bk, w.scale)
+        check_close(f"o[{i}]", out_h[a:b], o_ref, TOL_O)
+        check_close(f"lse[{i}]", lse_h[a:b], l_ref, TOL_LSE)
+
+
+def test_varlen_equals_single_sequence_calls(msa):
+    """The packed call gives exactly the bits of one single-sequence call per
+    sequence, including with a workspace too small for one pass."""
+    lens = [300, 1, 1000, 129]
+    wls = [synth.make("tiny", L=n, H_q=8, H_kv=2, d=64, d_idx=64, seed=70 + i)
+           for i, n in enumerate(lens)]
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    cat = lambda t: torch.cat([synth.device_tensor(w, t) for w in wls])
+    qi, q, kk, v = cat(synth.T_QIDX), cat(synth.T_Q), cat(synth.T_K), cat(synth.T_V)
+    ki = torch.cat([kidx2d(synth.device_tensor(w, synth.T_KIDX)) for w in wls])
+    ids = msa.msa_index_select_varlen(qi, ki, cu, 128, 16)
+    small = torch.empty(msa.msa_sparse_attn_workspace_bytes(200, 1000, 8, 2, 64),
+                        dtype=torch.uint8, device="cuda")
+    out, lse = msa.msa_sparse_attn_varlen(q, kk, v, ids, cu, 128, 0.125, workspace=small)
+    for i in range(len(lens)):
+        a, b = cu[i], cu[i + 1]
+        ids1 = msa.msa_index_select(qi[a:b].contiguous(), ki[a:b].contiguous(), 128, 16)
+        o1, l1 = msa.msa_sparse_attn(q[a:b].contiguous(), kk[a:b].contiguous(),
+                                     v[a:b].contiguous(), ids1, 128, 0.125)
+        assert torch.equal(ids[a:b], ids1)
+        assert torch.equal(out[a:b], o1) and torch.equal(lse[a:b], l1)
+
+
 # ------------------------------------------------------------------ decode
 
 def _decode_case(msa, w, fp8):
