@@ -15,6 +15,7 @@ Prints ONE JSON line. `value` is prefill tokens/s (all ranks). Further keys:
   cpu_baseline the CPU oracle on a bounded sample of the same workload
   extra        the other measured paths: 32K and 1M prefill (1M: 2 timed steps),
                the 128K tokens as 8 packed 16K sequences (varlen entry points),
+               the 128K step with the index branch on FP8-E4M3 codes,
                decode steps with bf16 and FP8-E4M3 KV, standalone top-16 (with
                torch.topk over the same scores as a comparator)
 
@@ -407,6 +408,38 @@ def time_varlen(msa, w, n_seq, steps, warmup):
     return ms, flops
 
 
+def time_prefill_fp8_index(msa, w, steps, warmup):
+    """Prefill step with the index branch on FP8-E4M3 codes of q_idx / k_idx
+    (rounded to nearest by torch before the timing) and the bf16 main branch."""
+    import torch
+    import synth
+    P = Prefill(msa, w)
+    q8 = P.qidx.to(torch.float8_e4m3fn)
+    k8 = P.kidx.to(torch.float8_e4m3fn)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record()
+        msa.msa_index_select_fp8(q8, k8, w.Bk, w.k, block_ids=P.ids)
+        if ev:
+            ev[1].record()
+        msa.msa_sparse_attn(P.q, P.k, P.v, P.ids, w.Bk, w.scale, workspace=P.ws, out=P.out,
+                            lse=P.lse)
+        if ev:
+            ev[2].record()
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    idx = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    tot = statistics.mean(e[0].elapsed_time(e[2]) for e in evs)
+    return tot, idx
+
+
 # ------------------------------------------------------------- CPU baseline
 def cpu_baseline(w, budget_s=20.0, seed=0):
     """The oracle (as it stands) on a bounded sample of rows of workload w;
@@ -615,6 +648,14 @@ def main():
                                 "algorithmic_bytes": tk_bytes,
                                 "torch_topk_ms": round(torch_ms, 4),
                                 "vs_torch_topk": round(torch_ms / tk_ms, 2)}
+        f_ms, f_idx = time_prefill_fp8_index(msa, w, args.steps, 3)
+        torch.cuda.empty_cache()
+        peak_f8 = peak_t * 2.0  # measured bf16 sustained x the nominal fp8 / bf16 ratio
+        extra["prefill_128k_fp8_index"] = {
+            "tokens_per_s": w.N / (f_ms * 1e-3), "ms": round(f_ms, 3), "index_ms": round(f_idx, 3),
+            "index_tflops": round(fl_idx / (f_idx * 1e-3) / 1e12, 2),
+            "index_frac_of_fp8_peak": round(fl_idx / (f_idx * 1e-3) / 1e12 / peak_f8, 4),
+            "fp8_peak": peak_f8, "fp8_peak_source": "measured bf16 sustained x 2 (nominal ratio)"}
         v_ms, v_fl = time_varlen(msa, w, 8, args.steps, 3)
         torch.cuda.empty_cache()
         extra["prefill_varlen_8x16k"] = {"tokens_per_s": w.N / (v_ms * 1e-3), "ms": round(v_ms, 3),

@@ -59,6 +59,7 @@ _launch_count = _sig("msa_launch_count", [], _I64)
 _index_dec_noalloc = _sig("msa_index_select_decode_noalloc", [_P, _P, _P, _P, _I, _I, _I, _I, _I,
                                                               _I, _P, _P])
 _noalloc_max = _sig("msa_index_select_decode_noalloc_max_scores", [], _I64)
+_index_fp8 = _sig("msa_index_select_fp8", [_P, _P, _I64, _I, _I, _I, _I, _P, _P, _F, _P])
 _index_varlen = _sig("msa_index_select_varlen", [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P])
 _ws_attn_varlen = _sig("msa_sparse_attn_varlen_workspace_bytes", [_P, _I, _I, _I, _I, _I, _I],
                        _SZ)
@@ -71,7 +72,8 @@ EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes
            "msa_index_select_decode", "msa_decode_workspace_bytes", "msa_decode",
            "msa_get_error", "msa_set_wait_limit", "msa_launch_count",
            "msa_index_select_decode_noalloc", "msa_index_select_decode_noalloc_max_scores",
-           "msa_index_select_varlen", "msa_sparse_attn_varlen_workspace_bytes",
+           "msa_index_select_fp8", "msa_index_select_varlen",
+           "msa_sparse_attn_varlen_workspace_bytes",
            "msa_sparse_attn_varlen"]
 
 
@@ -132,6 +134,32 @@ def msa_index_select(q_idx: torch.Tensor, k_idx: torch.Tensor, Bk: int = 128, k:
     _check(_index_select(q_idx.data_ptr(), k_idx.data_ptr(), N, n_g, d_idx, Bk, k,
                          block_ids.data_ptr(), _ptr(block_scores), None, 0, _stream(q_idx)),
            "msa_index_select")
+    return block_ids
+
+
+def msa_index_select_fp8(q_idx: torch.Tensor, k_idx: torch.Tensor, Bk: int = 128, k: int = 16,
+                         block_ids: Optional[torch.Tensor] = None,
+                         block_scores: Optional[torch.Tensor] = None,
+                         score_scale: float = 1.0) -> torch.Tensor:
+    """Index branch on FP8-E4M3 codes: q_idx [N, n_groups, 128] and k_idx [N, 128]
+    torch.float8_e4m3fn (or uint8 holding the codes) -> block_ids [N, n_groups, k];
+    block_scores, when given, receive the pooled scores times score_scale."""
+    N, n_g, d_idx = q_idx.shape
+    for t, name in ((q_idx, "q_idx"), (k_idx, "k_idx")):
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise TypeError(f"{name} must hold E4M3 codes (float8_e4m3fn or uint8)")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if tuple(k_idx.shape) != (N, d_idx):
+        raise ValueError("k_idx must be [N, d_idx]")
+    if block_ids is None:
+        block_ids = torch.empty((N, n_g, k), dtype=torch.int32, device=q_idx.device)
+    _req(block_ids, "block_ids", torch.int32, (N, n_g, k))
+    if block_scores is not None:
+        _req(block_scores, "block_scores", torch.float32, (N, n_g, (N + Bk - 1) // Bk))
+    _check(_index_fp8(q_idx.data_ptr(), k_idx.data_ptr(), N, n_g, d_idx, Bk, k,
+                      block_ids.data_ptr(), _ptr(block_scores), score_scale, _stream(q_idx)),
+           "msa_index_select_fp8")
     return block_ids
 
 

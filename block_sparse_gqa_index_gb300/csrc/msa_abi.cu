@@ -100,6 +100,23 @@ int msa_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_grou
                                             block_scores, nb, diag(), (cudaStream_t)stream));
 }
 
+int msa_index_select_fp8(const void* q_idx, const void* k_idx, int64_t N, int n_groups,
+                         int d_idx, int Bk, int k, int32_t* block_ids, float* block_scores,
+                         float score_scale, void* stream) {
+  if (N < 0 || n_groups < 1 || d_idx < 1 || Bk < 1 || k < 1) return MSA_ERR_INVALID_ARG;
+  if (N == 0) return MSA_OK;
+  if (!q_idx || !k_idx || !block_ids) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(block_ids) ||
+      (block_scores && !aligned16(block_scores)))
+    return MSA_ERR_INVALID_ARG;
+  if (Bk != 128 || !supported_k(k) || d_idx != 128) return MSA_ERR_UNSUPPORTED;
+  if (N * n_groups >= (1ll << 31)) return MSA_ERR_UNSUPPORTED;
+  int64_t nb = ceil_div(N, Bk);
+  return status_of(msa::launch_index_select(q_idx, k_idx, N, n_groups, d_idx, k, block_ids,
+                                            block_scores, nb, diag(), (cudaStream_t)stream,
+                                            true, score_scale));
+}
+
 int msa_topk_blocks(const float* block_scores, int64_t N, int n_groups, int64_t nb, int Bk,
                     int k, int64_t q_offset, const int32_t* seq_lens, int32_t* block_ids,
                     void* stream) {

@@ -43,9 +43,10 @@ constexpr int kStages = 4;     // k_idx ring depth
 constexpr int kThreads = 320;  // 10 warps
 constexpr int kEpiWarps = 8;
 
-template <int DI>
+// DI index dimensions of EB bytes each (bf16: 2, E4M3: 1)
+template <int DI, int EB>
 struct Smem {
-  static constexpr int kChunks = DI / 64;             // 128-byte K chunks
+  static constexpr int kChunks = DI * EB / 128;       // 128-byte K chunks
   static constexpr int kAChunk = kRows * 128;         // bytes of one A K-chunk
   static constexpr int kBChunk = kKeys * 128;         // bytes of one B K-chunk
   static constexpr int kABytes = kAChunk * kChunks;
@@ -79,13 +80,17 @@ __device__ __forceinline__ float max32(const uint32_t (&r)[32], int lim) {
   return fmaxf(m0, m1);
 }
 
-template <int DI>
+// F8: q_idx / k_idx are E4M3 codes (kind::f8f6f4 MMAs, 32 codes per 32-byte
+// K step) and score_scale multiplies the reported block scores.
+template <int DI, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k, int64_t N, int n_g, int k,
                        int32_t* __restrict__ block_ids, float* __restrict__ block_scores,
-                       int64_t nb, int n_tiles, Diag dg) {
-  using S = Smem<DI>;
+                       int64_t nb, int n_tiles, float score_scale, Diag dg) {
+  constexpr int EB = F8 ? 1 : 2;
+  constexpr int kColsPerChunk = 128 / EB;  // elements in a 128-byte K chunk
+  using S = Smem<DI, EB>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = (unsigned char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   unsigned char* sA = smem;
@@ -161,7 +166,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (!mbar_wait(a_empty, a_par ^ 1, abort_flag, dg)) { ok = false; break; }
         mbar_arrive_expect_tx(a_full, S::kABytes);
         for (int c = 0; c < S::kChunks; ++c)
-          tma_load_2d(sA + c * S::kAChunk, &tm_q, a_full, c * 64, tile * kRows);
+          tma_load_2d(sA + c * S::kAChunk, &tm_q, a_full, c * kColsPerChunk, tile * kRows);
         a_armed = true;
         a_par ^= 1;
         for (int64_t b = 0; b < nkb; ++b, ++it) {
@@ -170,7 +175,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           if (!mbar_wait(&b_empty[s], par ^ 1, abort_flag, dg)) { ok = false; break; }
           mbar_arrive_expect_tx(&b_full[s], S::kBBytes);
           for (int c = 0; c < S::kChunks; ++c)
-            tma_load_2d(sB + s * S::kBBytes + c * S::kBChunk, &tm_k, &b_full[s], c * 64,
+            tma_load_2d(sB + s * S::kBBytes + c * S::kBChunk, &tm_k, &b_full[s], c * kColsPerChunk,
                         (int32_t)(b * kKeys));
           armed[s] = true;
           armed_par[s] = par;
@@ -185,7 +190,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, kKeys);
+      constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(128, kKeys) : idesc_bf16_f32(128, kKeys);
       const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
       uint32_t a_par = 0;
       long long it = 0;
@@ -209,11 +214,12 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           for (int h = 0; h < 2; ++h) {
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256 + h * 128);
 #pragma unroll
-            for (int kk = 0; kk < DI / 16; ++kk) {
+            for (int kk = 0; kk < DI * EB / 32; ++kk) {  // 32-byte K steps
               const int c = kk / 4, off = (kk % 4) * 32;
               uint64_t ad = desc_kmajor_sw128(a_base + c * S::kAChunk + h * 128 * 128 + off);
               uint64_t bd = desc_kmajor_sw128(b_base + s * S::kBBytes + c * S::kBChunk + off);
-              mma_bf16_ss(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+              if constexpr (F8) mma_e4m3_ss(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+              else mma_bf16_ss(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
             }
           }
           mma_commit(&b_empty[s]);
@@ -280,7 +286,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         __syncwarp();
         if (lane == 0) mbar_arrive(&t_empty[acc]);
         if (valid && b <= loc) {
-          if (want_scores) block_scores[r * nb + b] = m;
+          if (want_scores) block_scores[r * nb + b] = F8 ? m * score_scale : m;
           if (b < loc) {
             const uint64_t key = rank_key(m, (uint32_t)b);
             if (top.wants(key)) top.offer(key);
@@ -309,15 +315,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D bf16 tensor [rows, cols] (cols contiguous), box {64 cols, box_rows}, 128B swizzle
-bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, int box_rows) {
+// 2D tensor [rows, cols] of bf16 (eb = 2) or byte codes (eb = 1), cols
+// contiguous, box {128 bytes of columns, box_rows}, 128B swizzle
+bool make_map_2d(CUtensorMap* m, const void* base, int64_t rows, int cols, int box_rows,
+                 int eb) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * eb};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  return fn(m, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+            const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -333,23 +342,25 @@ int num_sms() {
   return n;
 }
 
-template <int DI>
+template <int DI, bool F8>
 cudaError_t launch_tc(const void* q_idx, const void* k_idx, int64_t N, int n_g, int k,
-                      int32_t* block_ids, float* block_scores, int64_t nb, const Diag& dg,
-                      cudaStream_t st) {
+                      int32_t* block_ids, float* block_scores, int64_t nb, float score_scale,
+                      const Diag& dg, cudaStream_t st) {
+  constexpr int EB = F8 ? 1 : 2;
   const int64_t n_rows = N * n_g;
   const int n_tiles = (int)((n_rows + kRows - 1) / kRows);
   CUtensorMap tq, tk;
-  if (!make_map_2d(&tq, q_idx, n_rows, DI, kRows) || !make_map_2d(&tk, k_idx, N, DI, kKeys))
+  if (!make_map_2d(&tq, q_idx, n_rows, DI, kRows, EB) ||
+      !make_map_2d(&tk, k_idx, N, DI, kKeys, EB))
     return cudaErrorInvalidValue;
-  const int smem = Smem<DI>::kBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(index_select_tc_kernel<DI>,
+  const int smem = Smem<DI, EB>::kBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(index_select_tc_kernel<DI, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = std::min(n_tiles, num_sms());
   note_launches(1);
-  index_select_tc_kernel<DI><<<grid, kThreads, smem, st>>>(tq, tk, N, n_g, k, block_ids,
-                                                          block_scores, nb, n_tiles, dg);
+  index_select_tc_kernel<DI, F8><<<grid, kThreads, smem, st>>>(
+      tq, tk, N, n_g, k, block_ids, block_scores, nb, n_tiles, score_scale, dg);
   return cudaGetLastError();
 }
 
@@ -357,11 +368,16 @@ cudaError_t launch_tc(const void* q_idx, const void* k_idx, int64_t N, int n_g, 
 
 cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_g,
                                 int d_idx, int k, int32_t* block_ids, float* block_scores,
-                                int64_t nb, const Diag& dg, cudaStream_t st) {
+                                int64_t nb, const Diag& dg, cudaStream_t st, bool e4m3,
+                                float score_scale) {
   if (N * n_g == 0) return cudaSuccess;
+  if (e4m3)  // E4M3 codes: 128 dimensions fill one 128-byte swizzle row
+    return launch_tc<128, true>(q_idx, k_idx, N, n_g, k, block_ids, block_scores, nb,
+                                score_scale, dg, st);
   if (d_idx == 128)
-    return launch_tc<128>(q_idx, k_idx, N, n_g, k, block_ids, block_scores, nb, dg, st);
-  return launch_tc<64>(q_idx, k_idx, N, n_g, k, block_ids, block_scores, nb, dg, st);
+    return launch_tc<128, false>(q_idx, k_idx, N, n_g, k, block_ids, block_scores, nb, 1.f, dg,
+                                 st);
+  return launch_tc<64, false>(q_idx, k_idx, N, n_g, k, block_ids, block_scores, nb, 1.f, dg, st);
 }
 
 }  // namespace msa

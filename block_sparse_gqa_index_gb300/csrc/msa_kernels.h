@@ -17,9 +17,12 @@ void note_launches(int n);
 Diag current_diag();
 
 // Index branch, prefill (msa_index.cu).
+// e4m3: q_idx / k_idx hold E4M3 codes (d_idx = 128), and score_scale multiplies
+// the reported block scores.
 cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_g,
                                 int d_idx, int k, int32_t* block_ids, float* block_scores,
-                                int64_t nb, const Diag& dg, cudaStream_t st);
+                                int64_t nb, const Diag& dg, cudaStream_t st, bool e4m3 = false,
+                                float score_scale = 1.f);
 
 // Exp-free top-k over block scores (msa_topk.cu).
 cudaError_t launch_topk(const float* S, int64_t N, int n_g, int64_t nb, int Bk, int k,

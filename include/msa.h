@@ -82,6 +82,20 @@ int msa_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_grou
                      int d_idx, int Bk, int k, int32_t* block_ids, float* block_scores,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* Index branch with FP8-E4M3 index operands (the pages' kernel release supports
+ * FP8 among its precisions, [MSA-PT] "Kernel open source e MiniMax-M3"):
+ *   q_idx   [N, n_groups, 128] E4M3 codes, k_idx [N, 128] E4M3 codes
+ *   (d_idx must be 128: MSA_ERR_UNSUPPORTED otherwise).
+ * The scores are the dot products of the decoded codes, exact per product and
+ * accumulated in fp32 on the tensor cores (kind::f8f6f4). A positive scale of
+ * a whole q_idx row or of the whole k_idx tensor changes no ranking, so the
+ * selection depends on the codes alone; score_scale (say, the product of the
+ * two dequantisation scales) only multiplies the optional block_scores.
+ * Selection rules, outputs and errors otherwise as msa_index_select. */
+int msa_index_select_fp8(const void* q_idx, const void* k_idx, int64_t N, int n_groups,
+                         int d_idx, int Bk, int k, int32_t* block_ids, float* block_scores,
+                         float score_scale, void* stream);
+
 /* Exp-free top-k over given block scores ("内核协同设计": ranking raw scores
  * selects the same blocks as ranking their softmax).
  *   block_scores [n_rows / n_groups... ] laid out [N, n_groups, nb] fp32; row

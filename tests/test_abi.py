@@ -140,3 +140,12 @@ def test_varlen_rejects(msa):
     p, keep = cu(0, 300, 300, 1000)
     assert msa._ws_attn_varlen(p, 3, 32, 8, 128, 128, 16) == \
         msa.msa_sparse_attn_workspace_bytes(700, 700, 32, 8, 128)
+
+
+def test_index_fp8_rejects(msa):
+    f = msa._index_fp8
+    assert f(None, FAKE, 10, 1, 128, 128, 16, FAKE, None, 1.0, None) == -1   # null q_idx
+    assert f(FAKE + 8, FAKE, 10, 1, 128, 128, 16, FAKE, None, 1.0, None) == -1  # misaligned
+    assert f(FAKE, FAKE, 10, 1, 64, 128, 16, FAKE, None, 1.0, None) == -2    # d_idx != 128
+    assert f(FAKE, FAKE, 10, 1, 128, 64, 16, FAKE, None, 1.0, None) == -2    # Bk != 128
+    assert f(FAKE, FAKE, 0, 1, 128, 128, 16, FAKE, None, 1.0, None) == 0     # empty: no-op

@@ -117,6 +117,70 @@ def _index_sampled(msa, w, rows, with_scores=False):
     return ids, got, want, want_s, swaps, scores
 
 
+# ---------------------------------------------------------- FP8-E4M3 index
+
+def _to_e4m3(bits_u16):
+    """bf16 bits -> (E4M3 codes, bf16 bits of the decoded codes), both on the host
+    (torch's CPU conversion, round to nearest even); every E4M3 value is a bf16
+    value, so the second array feeds the fp64 oracle exactly."""
+    f = torch.from_numpy((np.asarray(bits_u16, dtype=np.uint32) << 16).view(np.float32))
+    codes = f.to(torch.float8_e4m3fn)
+    back = codes.to(torch.float32).numpy().view(np.uint32) >> 16
+    return codes.view(torch.uint8), back.astype(np.uint16)
+
+
+@pytest.mark.parametrize("N,n_g", [(1, 1), (129, 2), (1000, 8), (4096, 4), (5000, 8)])
+def test_index_fp8_exact_on_integer_inputs(msa, N, n_g):
+    """Integer-valued index inputs are exact in E4M3: the FP8 selection and block
+    scores equal the oracle's and the bf16 path's bit for bit."""
+    w = synth.make("tiny", L=N, H_q=4 * n_g, H_kv=n_g, d=64, d_idx=128)
+    qh = synth.host_tensor(w, synth.T_QIDX)[0]
+    kh = synth.host_tensor(w, synth.T_KIDX)[0, :, 0]
+    q8, qb = _to_e4m3(qh)
+    k8, kb = _to_e4m3(kh)
+    assert np.array_equal(qb, qh) and np.array_equal(kb, kh)  # integers survive E4M3
+    sc8 = torch.full((w.N, n_g, w.nb), float("nan"), device="cuda")
+    ids8 = msa.msa_index_select_fp8(q8.cuda(), k8.cuda(), w.Bk, w.k, block_scores=sc8)
+    scb = torch.full_like(sc8, float("nan"))
+    idsb = msa.msa_index_select(synth.device_tensor(w, synth.T_QIDX),
+                                kidx2d(synth.device_tensor(w, synth.T_KIDX)), w.Bk, w.k,
+                                block_scores=scb)
+    torch.cuda.synchronize()
+    rows = np.arange(w.N)
+    want, want_s = oracle.index_select(qh, rows, kh, w.Bk, w.k, nb_out=w.nb, want_scores=True)
+    assert np.array_equal(ids8.cpu().numpy(), want)
+    assert torch.equal(ids8, idsb)
+    vis = np.arange(w.nb)[None, None, :] <= (rows // w.Bk)[:, None, None]
+    got_s = sc8.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got_s[np.broadcast_to(vis, got_s.shape)],
+                          want_s[np.broadcast_to(vis, want_s.shape)])
+
+
+def test_index_fp8_gauss_32k(msa):
+    """Gaussian 32K index inputs rounded to E4M3: the FP8 selection matches the
+    oracle on the decoded codes, up to near-tie swaps, and the block scores
+    (times score_scale) agree to fp32 accumulation."""
+    w = synth.make("32k")
+    qh = synth.host_tensor(w, synth.T_QIDX)[0]
+    kh = synth.host_tensor(w, synth.T_KIDX)[0, :, 0]
+    q8, qb = _to_e4m3(qh)
+    k8, kb = _to_e4m3(kh)
+    sc = torch.full((w.N, w.n_g, w.nb), float("nan"), device="cuda")
+    ids = msa.msa_index_select_fp8(q8.cuda(), k8.cuda(), w.Bk, w.k, block_scores=sc,
+                                   score_scale=0.5)
+    torch.cuda.synchronize()
+    rows = _sample_rows(w.N, w.Bk, 256, 11)
+    want, want_s = oracle.index_select(qb[rows], rows, kb, w.Bk, w.k, nb_out=w.nb,
+                                       want_scores=True)
+    got = ids.cpu().numpy()[rows]
+    swaps = compare_selection(got, want, want_s, rows, w.Bk)
+    assert swaps <= 0.01 * got.shape[0] * got.shape[1]
+    s = sc.cpu().numpy()[rows].astype(np.float64) * 2.0
+    vis = np.broadcast_to(np.arange(w.nb)[None, None, :] <= (rows // w.Bk)[:, None, None], s.shape)
+    rel = np.abs(s[vis] - want_s[vis]) / np.maximum(1.0, np.abs(want_s[vis]))
+    assert rel.max() < 1e-4
+
+
 def test_index_select_gauss_32k(msa):
     w = synth.make("32k")
     rows = _sample_rows(w.N, w.Bk, 256, 7)
