@@ -404,8 +404,14 @@ def time_varlen(msa, w, n_seq, steps, warmup):
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
+    a.record()
+    for _ in range(steps):
+        msa.msa_index_select_varlen(qidx, kidx, cu, w.Bk, w.k, block_ids=ids)
+    b.record()
+    torch.cuda.synchronize()
+    idx_ms = a.elapsed_time(b) / steps
     flops = n_seq * (index_flops(n, w.n_g, w.d_idx) + attn_flops(n, w.H_q, w.d, w.Bk, w.k))
-    return ms, flops
+    return ms, flops, idx_ms
 
 
 def time_prefill_fp8_index(msa, w, steps, warmup):
@@ -656,9 +662,10 @@ def main():
             "index_tflops": round(fl_idx / (f_idx * 1e-3) / 1e12, 2),
             "index_frac_of_fp8_peak": round(fl_idx / (f_idx * 1e-3) / 1e12 / peak_f8, 4),
             "fp8_peak": peak_f8, "fp8_peak_source": "measured bf16 sustained x 2 (nominal ratio)"}
-        v_ms, v_fl = time_varlen(msa, w, 8, args.steps, 3)
+        v_ms, v_fl, v_idx = time_varlen(msa, w, 8, args.steps, 3)
         torch.cuda.empty_cache()
         extra["prefill_varlen_8x16k"] = {"tokens_per_s": w.N / (v_ms * 1e-3), "ms": round(v_ms, 3),
+                                         "index_ms": round(v_idx, 3),
                                          "tflops": round(v_fl / (v_ms * 1e-3) / 1e12, 2)}
         wd = synth.make("decode")
         for fp8 in (False, True):

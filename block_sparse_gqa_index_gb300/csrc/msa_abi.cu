@@ -200,18 +200,12 @@ int msa_index_select_varlen(const void* q_idx, const void* k_idx, const int64_t*
     return MSA_ERR_INVALID_ARG;
   if (B == 0 || cu_seqlens[B] == 0) return MSA_OK;
   if (!q_idx || !k_idx || !block_ids) return MSA_ERR_INVALID_ARG;
-  // every sequence's rows must start 16-byte aligned
-  if (((int64_t)n_groups * k * 4) % 16 != 0 || (d_idx * 2) % 16 != 0) return MSA_ERR_UNSUPPORTED;
-  for (int b = 0; b < B; ++b) {
-    const int64_t t0 = cu_seqlens[b], n = cu_seqlens[b + 1] - t0;
-    if (n == 0) continue;
-    const int rc = msa_index_select((const unsigned char*)q_idx + t0 * n_groups * d_idx * 2,
-                                    (const unsigned char*)k_idx + t0 * d_idx * 2, n, n_groups,
-                                    d_idx, Bk, k, block_ids + t0 * n_groups * k, nullptr,
-                                    nullptr, 0, stream);
-    if (rc != MSA_OK) return rc;
-  }
-  return MSA_OK;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(block_ids)) return MSA_ERR_INVALID_ARG;
+  if (Bk != 128 || !supported_k(k) || !supported_d(d_idx)) return MSA_ERR_UNSUPPORTED;
+  if (cu_seqlens[B] * n_groups >= (1ll << 31)) return MSA_ERR_UNSUPPORTED;
+  // all sequences in one schedule (one launch per 128 non-empty sequences)
+  return status_of(msa::launch_index_select_varlen(q_idx, k_idx, cu_seqlens, B, n_groups, d_idx,
+                                                   k, block_ids, diag(), (cudaStream_t)stream));
 }
 
 int msa_sparse_attn_varlen(const void* q, const void* k, const void* v, const int32_t* block_ids,

@@ -26,6 +26,14 @@
 // Tiles are visited heaviest-first in a boustrophedon order over the CTAs so
 // the causal triangle balances; all CTAs sweep k_idx in the same order, which
 // keeps the re-read k_idx stream in L2.
+//
+// One launch serves a packed batch of independent sequences (SeqTable): each
+// sequence is cut into its own 256-row tiles, and the tiles of all sequences
+// form one heaviest-first schedule. A tile's weight is its local index j (the
+// number of key blocks its rows see), so the schedule walks j downwards and,
+// at each j, round-robins over the sequences that have a tile j. A single
+// sequence is the one-entry table.
+#include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -80,14 +88,54 @@ __device__ __forceinline__ float max32(const uint32_t (&r)[32], int lim) {
   return fmaxf(m0, m1);
 }
 
+// Sequences of one launch, sorted by tile count (non-increasing). The tile
+// levels j in [tiles[s+1], tiles[s]) are shared by the first s+1 sequences;
+// their (s+1) * (tiles[s] - tiles[s+1]) schedule ranks end at seg_end[s].
+constexpr int kMaxSeq = 128;
+struct SeqTable {
+  int B;                     // sequences (1 .. kMaxSeq), none empty
+  int n_tiles;               // sum of tiles[]
+  int64_t start[kMaxSeq];    // first token of the sequence in the packed batch
+  int64_t len[kMaxSeq];      // tokens
+  int32_t tiles[kMaxSeq];    // 256-row tiles of the sequence's (t, g) rows
+  int32_t seg_end[kMaxSeq];  // exclusive end rank of level segment s
+};
+
+// one tile of the schedule
+struct TileRef {
+  int64_t row0;   // first (t, g) row of the tile in the packed batch
+  int64_t lrow0;  // the same row counted from the sequence's first row
+  int64_t rows;   // (t, g) rows of the sequence
+  int64_t key0;   // first key of the sequence
+};
+
+__device__ __forceinline__ bool tile_at(const SeqTable& tb, int i, int n_g, TileRef& tr) {
+  if (i >= tb.n_tiles) return false;
+  int lo = 0, hi = tb.B - 1;  // first segment whose ranks end after i
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (i < tb.seg_end[mid]) hi = mid;
+    else lo = mid + 1;
+  }
+  const int o = i - (lo ? tb.seg_end[lo - 1] : 0);
+  const int p = o % (lo + 1);
+  const int j = tb.tiles[lo] - 1 - o / (lo + 1);
+  tr.lrow0 = (int64_t)j * kRows;
+  tr.row0 = tb.start[p] * n_g + tr.lrow0;
+  tr.rows = tb.len[p] * n_g;
+  tr.key0 = tb.start[p];
+  return true;
+}
+
 // F8: q_idx / k_idx are E4M3 codes (kind::f8f6f4 MMAs, 32 codes per 32-byte
 // K step) and score_scale multiplies the reported block scores.
 template <int DI, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_k, int64_t N, int n_g, int k,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ SeqTable tab, int n_g, int k,
                        int32_t* __restrict__ block_ids, float* __restrict__ block_scores,
-                       int64_t nb, int n_tiles, float score_scale, Diag dg) {
+                       int64_t nb, float score_scale, Diag dg) {
   constexpr int EB = F8 ? 1 : 2;
   constexpr int kColsPerChunk = 128 / EB;  // elements in a 128-byte K chunk
   using S = Smem<DI, EB>;
@@ -107,7 +155,6 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t n_rows = N * n_g;
   const bool want_scores = block_scores != nullptr;
 
   if (threadIdx.x == 0) {
@@ -135,18 +182,16 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   // tile schedule: heaviest first, boustrophedon over the CTAs
   const int G = gridDim.x;
-  auto tile_of = [&](int round, int& tile) -> bool {
+  auto tile_of = [&](int round, TileRef& tr) -> bool {
     int i = round * G + ((round & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
-    if (i >= n_tiles) return false;
-    tile = n_tiles - 1 - i;
-    return true;
+    return tile_at(tab, i, n_g, tr);
   };
-  auto key_blocks = [&](int tile) -> int64_t {
-    int64_t last = min((int64_t)tile * kRows + kRows, n_rows) - 1;
+  auto key_blocks = [&](const TileRef& tr) -> int64_t {
+    int64_t last = min(tr.lrow0 + kRows, tr.rows) - 1;
     int64_t loc_max = (last / n_g) / kKeys;
     return want_scores ? loc_max + 1 : loc_max;
   };
-  const int rounds = (n_tiles + G - 1) / G;
+  const int rounds = (tab.n_tiles + G - 1) / G;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -159,14 +204,14 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       long long it = 0;
       bool ok = true;
       for (int rd = 0; rd < rounds && ok; ++rd) {
-        int tile;
-        if (!tile_of(rd, tile)) continue;
-        int64_t nkb = key_blocks(tile);
+        TileRef tr;
+        if (!tile_of(rd, tr)) continue;
+        int64_t nkb = key_blocks(tr);
         if (nkb <= 0) continue;
         if (!mbar_wait(a_empty, a_par ^ 1, abort_flag, dg)) { ok = false; break; }
         mbar_arrive_expect_tx(a_full, S::kABytes);
         for (int c = 0; c < S::kChunks; ++c)
-          tma_load_2d(sA + c * S::kAChunk, &tm_q, a_full, c * kColsPerChunk, tile * kRows);
+          tma_load_2d(sA + c * S::kAChunk, &tm_q, a_full, c * kColsPerChunk, (int32_t)tr.row0);
         a_armed = true;
         a_par ^= 1;
         for (int64_t b = 0; b < nkb; ++b, ++it) {
@@ -176,7 +221,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           mbar_arrive_expect_tx(&b_full[s], S::kBBytes);
           for (int c = 0; c < S::kChunks; ++c)
             tma_load_2d(sB + s * S::kBBytes + c * S::kBChunk, &tm_k, &b_full[s], c * kColsPerChunk,
-                        (int32_t)(b * kKeys));
+                        (int32_t)(tr.key0 + b * kKeys));
           armed[s] = true;
           armed_par[s] = par;
         }
@@ -196,9 +241,9 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       long long it = 0;
       bool ok = true;
       for (int rd = 0; rd < rounds && ok; ++rd) {
-        int tile;
-        if (!tile_of(rd, tile)) continue;
-        int64_t nkb = key_blocks(tile);
+        TileRef tr;
+        if (!tile_of(rd, tr)) continue;
+        int64_t nkb = key_blocks(tr);
         if (nkb <= 0) continue;
         if (!mbar_wait(a_full, a_par, abort_flag, dg)) { ok = false; break; }
         a_par ^= 1;
@@ -239,12 +284,13 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     long long it = 0;
     bool ok = true;
     for (int rd = 0; rd < rounds && ok; ++rd) {
-      int tile;
-      if (!tile_of(rd, tile)) continue;
-      const int64_t nkb = key_blocks(tile);
-      const int64_t r = (int64_t)tile * kRows + row_in_tile;
-      const bool valid = r < n_rows;
-      const int64_t t = valid ? r / n_g : 0;
+      TileRef tr;
+      if (!tile_of(rd, tr)) continue;
+      const int64_t nkb = key_blocks(tr);
+      const int64_t lr = tr.lrow0 + row_in_tile;  // row within the sequence
+      const int64_t r = tr.row0 + row_in_tile;    // row within the packed batch
+      const bool valid = lr < tr.rows;
+      const int64_t t = valid ? lr / n_g : 0;
       const int64_t loc = t / kKeys;
       RowTopK top;
       top.init(k - 1);
@@ -342,25 +388,45 @@ int num_sms() {
   return n;
 }
 
+// fills tb from the sequences' (start, len), none empty, at most kMaxSeq
+void make_table(SeqTable& tb, const int64_t* start, const int64_t* len, int B, int n_g) {
+  int idx[kMaxSeq];
+  for (int i = 0; i < B; ++i) idx[i] = i;
+  auto tiles_of = [&](int i) { return (int32_t)((len[i] * n_g + kRows - 1) / kRows); };
+  std::stable_sort(idx, idx + B, [&](int a, int b) { return tiles_of(a) > tiles_of(b); });
+  tb.B = B;
+  for (int s = 0; s < B; ++s) {
+    tb.start[s] = start[idx[s]];
+    tb.len[s] = len[idx[s]];
+    tb.tiles[s] = tiles_of(idx[s]);
+  }
+  int64_t end = 0;
+  for (int s = 0; s < B; ++s) {
+    const int32_t below = s + 1 < B ? tb.tiles[s + 1] : 0;
+    end += (int64_t)(s + 1) * (tb.tiles[s] - below);
+    tb.seg_end[s] = (int32_t)end;
+  }
+  tb.n_tiles = (int)end;
+}
+
+// q_idx [n_tok, n_g, DI] and k_idx [n_tok, DI] hold every sequence of tb
 template <int DI, bool F8>
-cudaError_t launch_tc(const void* q_idx, const void* k_idx, int64_t N, int n_g, int k,
-                      int32_t* block_ids, float* block_scores, int64_t nb, float score_scale,
-                      const Diag& dg, cudaStream_t st) {
+cudaError_t launch_tc(const void* q_idx, const void* k_idx, int64_t n_tok, const SeqTable& tb,
+                      int n_g, int k, int32_t* block_ids, float* block_scores, int64_t nb,
+                      float score_scale, const Diag& dg, cudaStream_t st) {
   constexpr int EB = F8 ? 1 : 2;
-  const int64_t n_rows = N * n_g;
-  const int n_tiles = (int)((n_rows + kRows - 1) / kRows);
   CUtensorMap tq, tk;
-  if (!make_map_2d(&tq, q_idx, n_rows, DI, kRows, EB) ||
-      !make_map_2d(&tk, k_idx, N, DI, kKeys, EB))
+  if (!make_map_2d(&tq, q_idx, n_tok * n_g, DI, kRows, EB) ||
+      !make_map_2d(&tk, k_idx, n_tok, DI, kKeys, EB))
     return cudaErrorInvalidValue;
   const int smem = Smem<DI, EB>::kBytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(index_select_tc_kernel<DI, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int grid = std::min(n_tiles, num_sms());
+  const int grid = std::min(tb.n_tiles, num_sms());
   note_launches(1);
   index_select_tc_kernel<DI, F8><<<grid, kThreads, smem, st>>>(
-      tq, tk, N, n_g, k, block_ids, block_scores, nb, n_tiles, score_scale, dg);
+      tq, tk, tb, n_g, k, block_ids, block_scores, nb, score_scale, dg);
   return cudaGetLastError();
 }
 
@@ -371,13 +437,47 @@ cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int64_t N,
                                 int64_t nb, const Diag& dg, cudaStream_t st, bool e4m3,
                                 float score_scale) {
   if (N * n_g == 0) return cudaSuccess;
+  SeqTable tb;
+  const int64_t start = 0;
+  make_table(tb, &start, &N, 1, n_g);
   if (e4m3)  // E4M3 codes: 128 dimensions fill one 128-byte swizzle row
-    return launch_tc<128, true>(q_idx, k_idx, N, n_g, k, block_ids, block_scores, nb,
+    return launch_tc<128, true>(q_idx, k_idx, N, tb, n_g, k, block_ids, block_scores, nb,
                                 score_scale, dg, st);
   if (d_idx == 128)
-    return launch_tc<128, false>(q_idx, k_idx, N, n_g, k, block_ids, block_scores, nb, 1.f, dg,
-                                 st);
-  return launch_tc<64, false>(q_idx, k_idx, N, n_g, k, block_ids, block_scores, nb, 1.f, dg, st);
+    return launch_tc<128, false>(q_idx, k_idx, N, tb, n_g, k, block_ids, block_scores, nb, 1.f,
+                                 dg, st);
+  return launch_tc<64, false>(q_idx, k_idx, N, tb, n_g, k, block_ids, block_scores, nb, 1.f, dg,
+                              st);
+}
+
+cudaError_t launch_index_select_varlen(const void* q_idx, const void* k_idx,
+                                       const int64_t* cu_seqlens, int B, int n_g, int d_idx,
+                                       int k, int32_t* block_ids, const Diag& dg,
+                                       cudaStream_t st) {
+  const int64_t n_tok = cu_seqlens[B];
+  int64_t start[kMaxSeq], len[kMaxSeq];
+  int m = 0;
+  // non-empty sequences, kMaxSeq per launch
+  for (int b = 0; b <= B; ++b) {
+    if (m == kMaxSeq || (b == B && m > 0)) {
+      SeqTable tb;
+      make_table(tb, start, len, m, n_g);
+      const cudaError_t e =
+          d_idx == 128 ? launch_tc<128, false>(q_idx, k_idx, n_tok, tb, n_g, k, block_ids,
+                                               nullptr, 0, 1.f, dg, st)
+                       : launch_tc<64, false>(q_idx, k_idx, n_tok, tb, n_g, k, block_ids,
+                                              nullptr, 0, 1.f, dg, st);
+      if (e != cudaSuccess) return e;
+      m = 0;
+    }
+    if (b == B) break;
+    if (cu_seqlens[b + 1] > cu_seqlens[b]) {
+      start[m] = cu_seqlens[b];
+      len[m] = cu_seqlens[b + 1] - cu_seqlens[b];
+      ++m;
+    }
+  }
+  return cudaSuccess;
 }
 
 }  // namespace msa

@@ -24,6 +24,13 @@ cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int64_t N,
                                 int64_t nb, const Diag& dg, cudaStream_t st, bool e4m3 = false,
                                 float score_scale = 1.f);
 
+// One launch per 128 non-empty sequences of a packed batch; cu_seqlens is a
+// host array [B + 1] of token offsets (msa_index.cu).
+cudaError_t launch_index_select_varlen(const void* q_idx, const void* k_idx,
+                                       const int64_t* cu_seqlens, int B, int n_g, int d_idx,
+                                       int k, int32_t* block_ids, const Diag& dg,
+                                       cudaStream_t st);
+
 // Exp-free top-k over block scores (msa_topk.cu).
 cudaError_t launch_topk(const float* S, int64_t N, int n_g, int64_t nb, int Bk, int k,
                         int64_t q_offset, const int32_t* seq_lens, int32_t* ids, const Diag& dg,

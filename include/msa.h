@@ -140,11 +140,15 @@ int msa_sparse_attn(const void* q, const void* k, const void* v, const int32_t* 
  *   cu_seqlens  host int64 [B + 1] with 0 = cu_seqlens[0] <= ... <= cu_seqlens[B]
  *               (MSA_ERR_INVALID_ARG otherwise)
  * Other tensors as in msa_index_select / msa_sparse_attn with N = cu_seqlens[B].
- * Each sequence runs as its own pass of the single-sequence kernels on the
- * stream, which reuses the workspace from one sequence to the next. Every
- * sequence's rows must start 16-byte aligned: n_groups * k (and, for the
- * main branch, H_kv * topk, and H_q when lse is given) a multiple of 4, else
- * MSA_ERR_UNSUPPORTED. */
+ * Index branch: one launch per 128 non-empty sequences; the row tiles of all of
+ * them form one heaviest-first schedule over the SMs, so short sequences fill
+ * the gaps that long ones leave. q_idx, k_idx and block_ids must be 16-byte
+ * aligned (MSA_ERR_INVALID_ARG); N * n_groups must stay below 2^31
+ * (MSA_ERR_UNSUPPORTED).
+ * Main branch: each sequence runs as its own pass of the single-sequence
+ * kernels on the stream, which reuses the workspace from one sequence to the
+ * next. Every sequence's rows must start 16-byte aligned: H_kv * topk (and H_q
+ * when lse is given) a multiple of 4, else MSA_ERR_UNSUPPORTED. */
 int msa_index_select_varlen(const void* q_idx, const void* k_idx, const int64_t* cu_seqlens,
                             int B, int n_groups, int d_idx, int Bk, int k, int32_t* block_ids,
                             void* stream);

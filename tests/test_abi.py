@@ -105,8 +105,9 @@ def test_wait_limit_roundtrip(msa):
 
 
 def test_varlen_rejects(msa):
-    """Varlen prefill validates the cumulative offsets and the per-sequence
-    alignment on the host, before anything is launched."""
+    """Varlen prefill validates the cumulative offsets, the sizes and (for the
+    main branch) the per-sequence alignment on the host, before anything is
+    launched."""
     import ctypes as C
 
     def cu(*xs):
@@ -125,7 +126,11 @@ def test_varlen_rejects(msa):
     assert fi(FAKE, FAKE, p, 2, 8, 128, 128, 16, FAKE, None) == 0  # only empty sequences
     p, keep = cu(0, 100)
     assert fi(FAKE, FAKE, p, 1, 8, 128, 64, 16, FAKE, None) == -2   # Bk != 128
-    assert fi(FAKE, FAKE, p, 1, 1, 128, 128, 3, FAKE, None) == -2   # n_g * k not a multiple of 4
+    assert fi(FAKE, FAKE, p, 1, 8, 96, 128, 16, FAKE, None) == -2   # d_idx not 64 or 128
+    assert fi(FAKE, FAKE, p, 1, 8, 128, 128, 17, FAKE, None) == -2  # k above the largest top-k
+    p, keep = cu(0, 1 << 28)
+    assert fi(FAKE, FAKE, p, 1, 8, 128, 128, 16, FAKE, None) == -2  # 2^31 (t, g) rows
+    p, keep = cu(0, 100)
     assert fi(None, FAKE, p, 1, 8, 128, 128, 16, FAKE, None) == -1  # null q_idx
     # main branch: same offset rules; lse rows of 2 heads would misalign sequences
     args = (FAKE, FAKE, FAKE, FAKE)

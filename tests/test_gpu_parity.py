@@ -352,6 +352,32 @@ def test_varlen_prefill_matches_each_sequence(msa, H_q, H_kv, d):
         check_close(f"lse[{i}]", lse_h[a:b], l_ref, TOL_LSE)
 
 
+def test_varlen_index_many_sequences(msa):
+    """150 packed sequences, more than one launch's schedule holds (so two
+    launches), empty ones among them, one long enough to own most tiles, and
+    k = 8: every sequence's block ids equal the oracle's for that sequence alone."""
+    rng = np.random.default_rng(11)
+    lens = [int(x) for x in rng.integers(1, 500, size=150)]
+    for i in (0, 3, 64, 127, 128, 149):
+        lens[i] = 0
+    lens[70] = 3000
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    wls = {i: synth.make("tiny", L=n, H_q=8, H_kv=2, d=64, d_idx=64, seed=300 + i)
+           for i, n in enumerate(lens) if n > 0}
+    qi = torch.cat([synth.device_tensor(wls[i], synth.T_QIDX) for i in sorted(wls)])
+    ki = torch.cat([kidx2d(synth.device_tensor(wls[i], synth.T_KIDX)) for i in sorted(wls)])
+    ids = msa.msa_index_select_varlen(qi, ki, cu, 128, 8)
+    torch.cuda.synchronize()
+    ids_h = ids.cpu().numpy()
+    assert ids_h.shape == (cu[-1], 2, 8)
+    for i, w in wls.items():
+        want = oracle.index_select(synth.host_tensor(w, synth.T_QIDX)[0], np.arange(w.N),
+                                   synth.host_tensor(w, synth.T_KIDX)[0, :, 0], w.Bk, 8)
+        assert np.array_equal(ids_h[cu[i]:cu[i + 1]], want), f"sequence {i} (length {w.N})"
+
+
 def test_varlen_equals_single_sequence_calls(msa):
     """The packed call gives exactly the bits of one single-sequence call per
     sequence, including with a workspace too small for one pass."""
