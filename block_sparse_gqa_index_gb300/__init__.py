@@ -65,6 +65,12 @@ _ws_attn_varlen = _sig("msa_sparse_attn_varlen_workspace_bytes", [_P, _I, _I, _I
                        _SZ)
 _attn_varlen = _sig("msa_sparse_attn_varlen", [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                                _P, _P, _P, _SZ, _P])
+_index_paged = _sig("msa_index_select_paged", [_P, _P, _I64, _P, _I, _P, _P, _I, _I, _I, _I, _I,
+                                               _P, _P])
+_ws_attn_paged = _sig("msa_sparse_attn_paged_workspace_bytes", [_P, _P, _I, _I, _I, _I, _I, _I,
+                                                                _I], _SZ)
+_attn_paged = _sig("msa_sparse_attn_paged", [_P, _P, _P, _I64, _P, _I, _P, _P, _P, _I, _I, _I, _I,
+                                             _I, _I, _F, _P, _P, _P, _SZ, _P])
 
 EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes",
            "msa_index_select", "msa_topk_blocks", "msa_sparse_attn_workspace_bytes",
@@ -74,7 +80,8 @@ EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes
            "msa_index_select_decode_noalloc", "msa_index_select_decode_noalloc_max_scores",
            "msa_index_select_fp8", "msa_index_select_varlen",
            "msa_sparse_attn_varlen_workspace_bytes",
-           "msa_sparse_attn_varlen"]
+           "msa_sparse_attn_varlen", "msa_index_select_paged",
+           "msa_sparse_attn_paged_workspace_bytes", "msa_sparse_attn_paged"]
 
 
 class MSAError(RuntimeError):
@@ -290,6 +297,93 @@ def msa_sparse_attn_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                         cu.data_ptr(), cu.numel() - 1, H_q, H_kv, d, Bk, topk, scale,
                         out.data_ptr(), _ptr(lse), workspace.data_ptr(), workspace.numel(),
                         _stream(q)), "msa_sparse_attn_varlen")
+    return out, lse
+
+
+# ------------------------------------------------------------ paged prefill
+def _paged_args(page_table: torch.Tensor, cu_q, kv_lens):
+    cu = _cu_array(cu_q)
+    kv = torch.as_tensor(kv_lens, dtype=torch.int64, device="cpu").contiguous().reshape(-1)
+    B = cu.numel() - 1
+    if kv.numel() != B:
+        raise ValueError("kv_lens must hold one length per sequence")
+    _req(page_table, "page_table", torch.int32)
+    if page_table.dim() != 2 or page_table.shape[0] != B:
+        raise ValueError("page_table must be [B, max_pages]")
+    return cu, kv, B, page_table.shape[1]
+
+
+def msa_index_select_paged(q_idx: torch.Tensor, k_idx_pages: torch.Tensor,
+                           page_table: torch.Tensor, cu_q, kv_lens, Bk: int = 128, k: int = 16,
+                           block_ids: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Index branch of a chunked prefill over a paged k_idx cache: sequence b
+    holds kv_lens[b] tokens, its last cu_q[b + 1] - cu_q[b] are its queries
+    (rows of q_idx [T, n_groups, d_idx]); k_idx_pages [P, Bk, d_idx], page_table
+    [B, max_pages] int32 -> block_ids [T, n_groups, k]."""
+    cu, kv, B, max_pages = _paged_args(page_table, cu_q, kv_lens)
+    T, n_g, d_idx = q_idx.shape
+    _req(q_idx, "q_idx", torch.bfloat16)
+    _req(k_idx_pages, "k_idx_pages", torch.bfloat16)
+    if k_idx_pages.dim() != 3 or k_idx_pages.shape[1] != Bk or k_idx_pages.shape[2] != d_idx:
+        raise ValueError("k_idx_pages must be [P, Bk, d_idx]")
+    if int(cu[-1]) != T:
+        raise ValueError("cu_q[-1] must equal the number of query rows")
+    if block_ids is None:
+        block_ids = torch.empty((T, n_g, k), dtype=torch.int32, device=q_idx.device)
+    _req(block_ids, "block_ids", torch.int32, (T, n_g, k))
+    _check(_index_paged(q_idx.data_ptr(), k_idx_pages.data_ptr(), k_idx_pages.shape[0],
+                        page_table.data_ptr(), max_pages, cu.data_ptr(), kv.data_ptr(), B, n_g,
+                        d_idx, Bk, k, block_ids.data_ptr(), _stream(q_idx)),
+           "msa_index_select_paged")
+    return block_ids
+
+
+def msa_sparse_attn_paged_workspace_bytes(cu_q, kv_lens, max_pages: int, H_q: int, H_kv: int,
+                                          d: int, Bk: int = 128, k: int = 16) -> int:
+    cu = _cu_array(cu_q)
+    kv = torch.as_tensor(kv_lens, dtype=torch.int64, device="cpu").contiguous().reshape(-1)
+    return _ws_attn_paged(cu.data_ptr(), kv.data_ptr(), cu.numel() - 1, max_pages, H_q, H_kv, d,
+                          Bk, k)
+
+
+def msa_sparse_attn_paged(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
+                          page_table: torch.Tensor, block_ids: torch.Tensor, cu_q, kv_lens,
+                          Bk: int = 128, scale: Optional[float] = None,
+                          workspace: Optional[torch.Tensor] = None,
+                          out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                          want_lse: bool = True):
+    """Main branch of a chunked prefill over paged K / V ([P, H_kv, Bk, d]
+    bf16, the decode layout): q [T, H_q, d], block_ids [T, H_kv, topk] ->
+    out [T, H_q, d] bf16, lse [T, H_q] fp32."""
+    cu, kv, B, max_pages = _paged_args(page_table, cu_q, kv_lens)
+    T, H_q, d = q.shape
+    P, H_kv = k_pages.shape[0], k_pages.shape[1]
+    topk = block_ids.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _req(q, "q", torch.bfloat16)
+    _req(k_pages, "k_pages", torch.bfloat16, (P, H_kv, Bk, d))
+    _req(v_pages, "v_pages", torch.bfloat16, (P, H_kv, Bk, d))
+    _req(block_ids, "block_ids", torch.int32, (T, H_kv, topk))
+    if int(cu[-1]) != T:
+        raise ValueError("cu_q[-1] must equal the number of query rows")
+    if workspace is None:
+        workspace = torch.empty(max(1, _ws_attn_paged(cu.data_ptr(), kv.data_ptr(), B, max_pages,
+                                                      H_q, H_kv, d, Bk, topk)),
+                                dtype=torch.uint8, device=q.device)
+    _req(workspace, "workspace", torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, "out", torch.bfloat16, (T, H_q, d))
+    if lse is None and want_lse:
+        lse = torch.empty((T, H_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _req(lse, "lse", torch.float32, (T, H_q))
+    _check(_attn_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), P,
+                       page_table.data_ptr(), max_pages, block_ids.data_ptr(), cu.data_ptr(),
+                       kv.data_ptr(), B, H_q, H_kv, d, Bk, topk, scale, out.data_ptr(), _ptr(lse),
+                       workspace.data_ptr(), workspace.numel(), _stream(q)),
+           "msa_sparse_attn_paged")
     return out, lse
 
 

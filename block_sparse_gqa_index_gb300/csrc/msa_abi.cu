@@ -182,15 +182,127 @@ static bool cu_ok(const int64_t* cu, int B) {
   return true;
 }
 
+}  // extern "C"
+
+namespace {
+
+// A batch for the main branch: queries packed by cu_q (host [B + 1]); keys
+// packed the same way (kv_lens null) or paged, sequence b holding kv_lens[b]
+// keys of which its queries are the last cu_q[b + 1] - cu_q[b].
+struct BatchPlan {
+  int64_t n_q = 0;   // query rows
+  int64_t nbv = 0;   // virtual blocks: the blocks of every sequence with queries
+  size_t fixed = 0;  // workspace bytes of qinfo and vinfo
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// false: bad lengths (a sequence with more queries than keys, or keys past
+// its page-table row)
+bool plan_batch(const int64_t* cu_q, const int64_t* kv_lens, int B, int max_pages,
+                BatchPlan& p) {
+  p = BatchPlan();
+  for (int b = 0; b < B; ++b) {
+    const int64_t nq = cu_q[b + 1] - cu_q[b];
+    const int64_t nk = kv_lens ? kv_lens[b] : nq;
+    if (nk < nq || (kv_lens && nk > (int64_t)max_pages * 128)) return false;
+    if (nq > 0) p.nbv += ceil_div(nk, 128);
+  }
+  p.n_q = B > 0 ? cu_q[B] : 0;
+  p.fixed = align256((size_t)p.n_q * 8) + align256((size_t)p.nbv * 8);
+  return true;
+}
+
+size_t batch_ws_bytes(const BatchPlan& p, int64_t chunk, int H_q, int H_kv, int d, int k,
+                      bool paged) {
+  return p.fixed + msa::attn_ws_bytes(std::min(chunk, p.n_q), p.nbv, H_q, H_kv, d, k, paged);
+}
+
+int attn_batch(const void* q, const void* k, const void* v, const int32_t* block_ids,
+               const int64_t* cu_q, const int64_t* kv_lens, const int32_t* page_table,
+               int64_t n_pages, int max_pages, int B, int H_q, int H_kv, int d, int Bk,
+               int topk, float scale, void* out, float* lse, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  if (H_q < 1 || H_kv < 1 || d < 1 || Bk < 1 || topk < 1) return MSA_ERR_INVALID_ARG;
+  BatchPlan p;
+  if (!plan_batch(cu_q, kv_lens, B, max_pages, p)) return MSA_ERR_INVALID_ARG;
+  if (p.n_q == 0) return MSA_OK;
+  if (!q || !k || !v || !block_ids || !out || !workspace) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(workspace) || !aligned16(block_ids) || (lse && !aligned16(lse)))
+    return MSA_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return MSA_ERR_INVALID_ARG;
+  const int G = H_q / H_kv;
+  if (Bk != 128 || !supported_k(topk) || !supported_d(d) || 128 % G != 0)
+    return MSA_ERR_UNSUPPORTED;
+  const bool paged = page_table != nullptr;
+  const int64_t kv_rows = paged ? n_pages * H_kv * 128 : p.n_q;
+  if (p.n_q >= (1ll << 27) || p.n_q * H_q * topk >= (1ll << 31) || kv_rows >= (1ll << 31) ||
+      p.nbv * H_kv >= (1ll << 31))
+    return MSA_ERR_UNSUPPORTED;
+  int64_t lo = 0, hi = p.n_q;  // largest chunk of query rows whose workspace fits
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) / 2;
+    if (batch_ws_bytes(p, mid, H_q, H_kv, d, topk, paged) <= workspace_bytes) lo = mid;
+    else hi = mid - 1;
+  }
+  if (lo < 1) return MSA_ERR_WORKSPACE;
+  const int64_t chunk = lo;
+  unsigned char* w = (unsigned char*)workspace;
+  int2* qinfo = (int2*)w;
+  int2* vinfo = (int2*)(w + align256((size_t)p.n_q * 8));
+  msa::AttnWs ws = msa::attn_ws_carve(w + p.fixed, chunk, p.nbv, H_q, H_kv, d, topk, paged);
+  const cudaStream_t st = (cudaStream_t)stream;
+  // the batch's geometry, kBatchSeqs sequences per launch
+  msa::BatchSeqs tb;
+  tb.B = 0;
+  int64_t vb = 0;
+  for (int b = 0; b <= B; ++b) {
+    if (tb.B == msa::kBatchSeqs || (b == B && tb.B > 0)) {
+      if (msa::launch_batch_info(tb, page_table, paged ? H_kv * 128 : 0, qinfo, vinfo, st) !=
+          cudaSuccess)
+        return MSA_ERR_CUDA;
+      tb.B = 0;
+    }
+    if (b == B) break;
+    const int64_t nq = cu_q[b + 1] - cu_q[b];
+    if (nq == 0) continue;
+    const int64_t nk = kv_lens ? kv_lens[b] : nq;
+    const int i = tb.B++;
+    tb.q_start[i] = (int32_t)cu_q[b];
+    tb.q_len[i] = (int32_t)nq;
+    tb.q_off[i] = (int32_t)(nk - nq);
+    tb.vb[i] = (int32_t)vb;
+    tb.n_blk[i] = (int32_t)ceil_div(nk, 128);
+    tb.kv_start[i] = (int32_t)(paged ? (int64_t)b * max_pages : cu_q[b]);
+    vb += tb.n_blk[i];
+  }
+  msa::AttnBatch bt;
+  bt.qinfo = qinfo;
+  bt.vinfo = vinfo;
+  bt.kv_rows = kv_rows;
+  bt.paged = paged;
+  const msa::Diag dg = diag();
+  for (int64_t q0 = 0; q0 < p.n_q; q0 += chunk) {
+    const int64_t q1 = std::min(p.n_q, q0 + chunk);
+    if (msa::launch_sparse_attn_chunk(q, k, v, block_ids, p.n_q, q0, q1, H_q, H_kv, d, topk,
+                                      scale, out, lse, ws, p.nbv, dg, st, bt) != cudaSuccess)
+      return MSA_ERR_CUDA;
+  }
+  return MSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 size_t msa_sparse_attn_varlen_workspace_bytes(const int64_t* cu_seqlens, int B, int H_q,
                                               int H_kv, int d, int Bk, int k) {
-  if (!cu_ok(cu_seqlens, B)) return 0;
-  size_t need = 0;
-  for (int b = 0; b < B; ++b) {
-    const int64_t n = cu_seqlens[b + 1] - cu_seqlens[b];
-    if (n > 0) need = std::max(need, msa_sparse_attn_workspace_bytes(n, n, H_q, H_kv, d, Bk, k));
-  }
-  return need;
+  BatchPlan p;
+  if (!cu_ok(cu_seqlens, B) || H_q < 1 || H_kv < 1 || Bk < 1 || k < 1 ||
+      !plan_batch(cu_seqlens, nullptr, B, 0, p) || p.n_q == 0)
+    return 0;
+  return batch_ws_bytes(p, p.n_q, H_q, H_kv, d, k, false);
 }
 
 int msa_index_select_varlen(const void* q_idx, const void* k_idx, const int64_t* cu_seqlens,
@@ -212,23 +324,62 @@ int msa_sparse_attn_varlen(const void* q, const void* k, const void* v, const in
                            const int64_t* cu_seqlens, int B, int H_q, int H_kv, int d, int Bk,
                            int topk, float scale, void* out, float* lse, void* workspace,
                            size_t workspace_bytes, void* stream) {
-  if (!cu_ok(cu_seqlens, B) || H_q < 1 || H_kv < 1 || d < 1 || Bk < 1 || topk < 1)
+  if (!cu_ok(cu_seqlens, B)) return MSA_ERR_INVALID_ARG;
+  return attn_batch(q, k, v, block_ids, cu_seqlens, nullptr, nullptr, 0, 0, B, H_q, H_kv, d, Bk,
+                    topk, scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------------------- paged prefill
+// cu_q host [B + 1] query offsets; kv_lens host [B], kv_lens[b] >= queries of b
+static bool paged_ok(const int64_t* cu_q, const int64_t* kv_lens, int B, int max_pages) {
+  if (!cu_ok(cu_q, B) || max_pages < 1 || (B > 0 && !kv_lens)) return false;
+  for (int b = 0; b < B; ++b)
+    if (kv_lens[b] < cu_q[b + 1] - cu_q[b] || kv_lens[b] > (int64_t)max_pages * 128) return false;
+  return true;
+}
+
+int msa_index_select_paged(const void* q_idx, const void* k_idx_pages, int64_t n_pages,
+                           const int32_t* page_table, int max_pages, const int64_t* cu_q,
+                           const int64_t* kv_lens, int B, int n_groups, int d_idx, int Bk, int k,
+                           int32_t* block_ids, void* stream) {
+  if (!paged_ok(cu_q, kv_lens, B, max_pages) || n_pages < 1 || n_groups < 1 || d_idx < 1 ||
+      Bk < 1 || k < 1)
     return MSA_ERR_INVALID_ARG;
-  if (B == 0 || cu_seqlens[B] == 0) return MSA_OK;
-  if (!q || !k || !v || !block_ids || !out || !workspace) return MSA_ERR_INVALID_ARG;
-  if (((int64_t)H_kv * topk * 4) % 16 != 0 || (lse && (H_q * 4) % 16 != 0))
+  if (B == 0 || cu_q[B] == 0) return MSA_OK;
+  if (!q_idx || !k_idx_pages || !page_table || !block_ids) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx_pages) || !aligned16(block_ids))
+    return MSA_ERR_INVALID_ARG;
+  if (Bk != 128 || !supported_k(k) || !supported_d(d_idx)) return MSA_ERR_UNSUPPORTED;
+  if (cu_q[B] * n_groups >= (1ll << 31) || n_pages * 128 >= (1ll << 31) ||
+      (int64_t)B * max_pages >= (1ll << 31))
     return MSA_ERR_UNSUPPORTED;
-  for (int b = 0; b < B; ++b) {
-    const int64_t t0 = cu_seqlens[b], n = cu_seqlens[b + 1] - t0;
-    if (n == 0) continue;
-    const int rc = msa_sparse_attn(
-        (const unsigned char*)q + t0 * H_q * d * 2, (const unsigned char*)k + t0 * H_kv * d * 2,
-        (const unsigned char*)v + t0 * H_kv * d * 2, block_ids + t0 * H_kv * topk, n, H_q, H_kv,
-        d, Bk, topk, scale, (unsigned char*)out + t0 * H_q * d * 2, lse ? lse + t0 * H_q : nullptr,
-        workspace, workspace_bytes, stream);
-    if (rc != MSA_OK) return rc;
-  }
-  return MSA_OK;
+  return status_of(msa::launch_index_select_paged(q_idx, k_idx_pages, n_pages, page_table,
+                                                  max_pages, cu_q, kv_lens, B, n_groups, d_idx,
+                                                  k, block_ids, diag(), (cudaStream_t)stream));
+}
+
+size_t msa_sparse_attn_paged_workspace_bytes(const int64_t* cu_q, const int64_t* kv_lens, int B,
+                                             int max_pages, int H_q, int H_kv, int d, int Bk,
+                                             int k) {
+  BatchPlan p;
+  if (!paged_ok(cu_q, kv_lens, B, max_pages) || H_q < 1 || H_kv < 1 || Bk < 1 || k < 1 ||
+      !plan_batch(cu_q, kv_lens, B, max_pages, p) || p.n_q == 0)
+    return 0;
+  return batch_ws_bytes(p, p.n_q, H_q, H_kv, d, k, true);
+}
+
+int msa_sparse_attn_paged(const void* q, const void* k_pages, const void* v_pages,
+                          int64_t n_pages, const int32_t* page_table, int max_pages,
+                          const int32_t* block_ids, const int64_t* cu_q, const int64_t* kv_lens,
+                          int B, int H_q, int H_kv, int d, int Bk, int topk, float scale,
+                          void* out, float* lse, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  if (!paged_ok(cu_q, kv_lens, B, max_pages) || n_pages < 1) return MSA_ERR_INVALID_ARG;
+  if (B > 0 && cu_q[B] > 0 && !page_table) return MSA_ERR_INVALID_ARG;
+  if ((int64_t)B * max_pages >= (1ll << 31)) return MSA_ERR_UNSUPPORTED;
+  return attn_batch(q, k_pages, v_pages, block_ids, cu_q, kv_lens, page_table, n_pages,
+                    max_pages, B, H_q, H_kv, d, Bk, topk, scale, out, lse, workspace,
+                    workspace_bytes, stream);
 }
 
 size_t msa_index_select_decode_workspace_bytes(int B, int max_pages, int n_groups) {

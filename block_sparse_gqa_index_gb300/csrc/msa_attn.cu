@@ -48,12 +48,29 @@ __device__ __forceinline__ bool id_ok(int id, int64_t t, const Diag& dg) {
   return true;
 }
 
+// Bucket of entry (row, id), or -1 when the id is not usable. Without qinfo
+// the query row t is its position and the bucket is (group, block id); with
+// qinfo (packed or paged sequences) qinfo[t] = {the first virtual block of
+// t's sequence, t's position in it}, and the bucket is (group, virtual block).
+__device__ __forceinline__ int bucket_of(const int2* __restrict__ qinfo, int id, int row, int t,
+                                         int n_g, int nb, const Diag& dg) {
+  int pos = t, vb = 0;
+  if (qinfo) {
+    const int2 qi = qinfo[t];
+    vb = qi.x;
+    pos = qi.y;
+  }
+  if (!id_ok(id, pos, dg)) return -1;
+  return (row - t * n_g) * nb + vb + id;
+}
+
 // Counts the queries of every bucket; a slot with no usable block gets no
 // partial record (rec_of = -1). Lanes of a warp that hit the same bucket add
 // their count with one atomic (popular blocks are selected by most queries).
 __global__ void bucket_count_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1,
-                                    int n_g, int k, int64_t nb, int32_t* __restrict__ counts,
-                                    int32_t* __restrict__ rec_of, Diag dg) {
+                                    int n_g, int k, int64_t nb, const int2* __restrict__ qinfo,
+                                    int32_t* __restrict__ counts, int32_t* __restrict__ rec_of,
+                                    Diag dg) {
   const int n = (int)((q1 - q0) * n_g * k);  // entries of the chunk (< 2^31)
   const int row0 = (int)(q0 * n_g);
   const int lane = threadIdx.x & 31;
@@ -63,10 +80,8 @@ __global__ void bucket_count_kernel(const int32_t* __restrict__ ids, int64_t q0,
     int bk = -1;
     if (e < n) {
       const int row = row0 + e / k;
-      const int t = row / n_g;
-      const int id = cids[e];
-      if (id_ok(id, t, dg)) bk = (row - t * n_g) * (int)nb + id;
-      else rec_of[e] = -1;
+      bk = bucket_of(qinfo, cids[e], row, row / n_g, n_g, (int)nb, dg);
+      if (bk < 0) rec_of[e] = -1;
     }
     const unsigned same = __match_any_sync(0xffffffffu, bk);
     if (bk >= 0 && lane == __ffs(same) - 1) atomicAdd(&counts[bk], __popc(same));
@@ -89,8 +104,8 @@ __device__ __forceinline__ void slice_of(int n, int c, int& e0, int& e1) {
 
 __global__ void __launch_bounds__(1024)
 bucket_count_smem_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1, int n_g, int k,
-                         int64_t nb, int32_t* __restrict__ counts, int32_t* __restrict__ percta,
-                         int32_t* __restrict__ rec_of, Diag dg) {
+                         int64_t nb, const int2* __restrict__ qinfo, int32_t* __restrict__ counts,
+                         int32_t* __restrict__ percta, int32_t* __restrict__ rec_of, Diag dg) {
   extern __shared__ int32_t hist[];
   const int n_b = (int)(n_g * nb);
   for (int i = threadIdx.x; i < n_b; i += blockDim.x) hist[i] = 0;
@@ -102,9 +117,8 @@ bucket_count_smem_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1
   slice_of(n, blockIdx.x, e0, e1);
   for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
     const int row = row0 + e / k;
-    const int t = row / n_g;
-    const int id = cids[e];
-    if (id_ok(id, t, dg)) atomicAdd(&hist[(row - t * n_g) * (int)nb + id], 1);
+    const int bk = bucket_of(qinfo, cids[e], row, row / n_g, n_g, (int)nb, dg);
+    if (bk >= 0) atomicAdd(&hist[bk], 1);
     else rec_of[e] = -1;
   }
   __syncthreads();
@@ -131,7 +145,8 @@ __global__ void bucket_cta_base_kernel(const int32_t* __restrict__ offsets, int 
 
 __global__ void __launch_bounds__(1024)
 bucket_fill_smem_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1, int n_g, int k,
-                        int64_t nb, int qt, const int32_t* __restrict__ offsets,
+                        int64_t nb, const int2* __restrict__ qinfo, int qt,
+                        const int32_t* __restrict__ offsets,
                         const int32_t* __restrict__ tile_off, const int32_t* __restrict__ percta,
                         int32_t* __restrict__ entries, int32_t* __restrict__ rec_of) {
   extern __shared__ int32_t cur[];
@@ -149,9 +164,8 @@ bucket_fill_smem_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1,
     const int rl = e / k;
     const int row = row0 + rl;
     const int t = row / n_g;
-    const int id = cids[e];
-    if (!id_ok(id, t, none)) continue;
-    const int bk = (row - t * n_g) * (int)nb + id;
+    const int bk = bucket_of(qinfo, cids[e], row, t, n_g, (int)nb, none);
+    if (bk < 0) continue;
     const int pos = atomicAdd(&cur[bk], 1);
     entries[pos] = ((t - (int)q0) << 4) | (e - rl * k);
     rec_of[e] = tile_off[bk] * qt + (pos - offsets[bk]);
@@ -202,7 +216,8 @@ __global__ void bucket_scan_kernel(const int32_t* __restrict__ counts, int64_t n
 // tile-major position tile * qt + (query's place in its tile). Lanes of a warp
 // that hit the same bucket take consecutive positions from one atomic.
 __global__ void bucket_fill_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1,
-                                   int n_g, int k, int64_t nb, int qt,
+                                   int n_g, int k, int64_t nb, const int2* __restrict__ qinfo,
+                                   int qt,
                                    const int32_t* __restrict__ offsets,
                                    const int32_t* __restrict__ tile_off,
                                    int32_t* __restrict__ cursor, int32_t* __restrict__ entries,
@@ -219,11 +234,8 @@ __global__ void bucket_fill_kernel(const int32_t* __restrict__ ids, int64_t q0, 
       const int rl = e / k;
       const int row = row0 + rl;
       const int t = row / n_g;
-      const int id = cids[e];
-      if (id_ok(id, t, none)) {
-        bk = (row - t * n_g) * (int)nb + id;
-        ent = ((row / n_g - (int)q0) << 4) | (e - rl * k);
-      }
+      bk = bucket_of(qinfo, cids[e], row, t, n_g, (int)nb, none);
+      if (bk >= 0) ent = ((t - (int)q0) << 4) | (e - rl * k);
     }
     const unsigned same = __match_any_sync(0xffffffffu, bk);
     const int leader = __ffs(same) - 1;
@@ -314,17 +326,29 @@ __device__ __forceinline__ int64_t find_bucket(const int32_t* __restrict__ tile_
 }
 
 // One record per tile, so that every role of the tile kernel finds its tile
-// with one independent load: {block b, first entry, queries | group g << 8,
-// end tile of the bucket}.
+// with one independent load: {row of the block's first key in K / V, first
+// entry, queries | group g << 8, end tile of the bucket}. A single sequence's
+// block b starts at row 128 b; with vinfo (packed or paged sequences) virtual
+// block v starts at row vinfo[v].x, and tbase[tile] = vinfo[v].y is the query
+// row that would sit at the block's first key position (the causal mask of
+// the block is then key column c visible to query row t iff c <= t - base).
 __global__ void tile_map_kernel(const int32_t* __restrict__ tile_off,
                                 const int32_t* __restrict__ offsets, int64_t n_b, int64_t nb,
-                                int qt, int4* __restrict__ tinfo) {
+                                int qt, const int2* __restrict__ vinfo,
+                                int32_t* __restrict__ tbase, int4* __restrict__ tinfo) {
   const int64_t total = tile_off[n_b];
   for (int64_t tile = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; tile < total;
        tile += (int64_t)gridDim.x * blockDim.x) {
     const int64_t bk = find_bucket(tile_off, n_b, tile);
     const int e0 = offsets[bk] + (int)(tile - tile_off[bk]) * qt;
-    tinfo[tile] = make_int4((int)(bk % nb), e0, min(qt, offsets[bk + 1] - e0) | (int)(bk / nb) << 8,
+    const int v = (int)(bk % nb);
+    int row = v * kBk;
+    if (vinfo) {
+      const int2 vi = vinfo[v];
+      row = vi.x;
+      if (tbase) tbase[tile] = vi.y;
+    }
+    tinfo[tile] = make_int4(row, e0, min(qt, offsets[bk + 1] - e0) | (int)(bk / nb) << 8,
                             tile_off[bk + 1]);
   }
 }
@@ -335,7 +359,8 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                     const __grid_constant__ CUtensorMap tm_q, int64_t tm_rows,
                     int64_t q0, int H_q, int H_kv, int k,
                     float scale_log2, int64_t nb, const int32_t* __restrict__ entries,
-                    const int4* __restrict__ tinfo, const int32_t* __restrict__ n_tiles,
+                    const int4* __restrict__ tinfo, const int32_t* __restrict__ tbase,
+                    const int32_t* __restrict__ n_tiles,
                     unsigned char* __restrict__ part, Diag dg) {
   using namespace sm100;
   using S = AttnSmem<D>;
@@ -437,8 +462,7 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           if (!mbar_wait(k_empty, (epoch & 1) ^ 1, abort_flag, dg)) break;
           mbar_arrive_expect_tx(k_full, S::kKVBytes);
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(smem + S::kKOff + c * kBk * 128, &tm_k, k_full, c * 64, inf.z >> 8,
-                        inf.x * kBk);
+            tma_load_3d(smem + S::kKOff + c * kBk * 128, &tm_k, k_full, c * 64, inf.z >> 8, inf.x);
           ++epoch;
           inf = nxt;
           if (!mbar_wait(k_full, (epoch - 1) & 1, abort_flag, dg)) break;
@@ -484,8 +508,7 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
           if (!mbar_wait(v_empty, (epoch & 1) ^ 1, abort_flag, dg)) break;
           mbar_arrive_expect_tx(v_full, S::kKVBytes);
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(smem + S::kVOff + c * kBk * 128, &tm_v, v_full, c * 64, inf.z >> 8,
-                        inf.x * kBk);
+            tma_load_3d(smem + S::kVOff + c * kBk * 128, &tm_v, v_full, c * 64, inf.z >> 8, inf.x);
           ++epoch;
           inf = nxt;
           if (!mbar_wait(v_full, (epoch - 1) & 1, abort_flag, dg)) break;
@@ -628,14 +651,14 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     for (int i = wg; i < n_local; i += 2) {
       const int ent_n = (i + 2 < n_local && qi < (inf_n.z & 0xFF)) ? entries[inf_n.y + qi] : -1;
       const int4 inf_nn = i + 4 < n_local ? tinfo[t_begin + i + 4] : kNone;
-      const int b = inf_c.x;
+      const int base = tbase ? tbase[t_begin + i] : inf_c.x;  // query row at the block's key 0
       const uint32_t par = (uint32_t)((i >> 1) & 1);
       const int t = ent_c >= 0 ? q0i + (ent_c >> 4) : 0;
       int got = 0;
       if (lane == 0) got = mbar_wait(&s_full[st], par, abort_flag, dg);
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
       tc_fence_after();
-      const int lim = (ent_c >= 0 && t / kBk == b) ? t - b * kBk + 1 : kBk;
+      const int lim = (ent_c >= 0 && t - base < kBk) ? t - base + 1 : kBk;
       // the whole row in registers: one load round trip; with no masked column
       // in the warp the loads also reduce the row max (sm_103 load-with-max)
       const bool full = __all_sync(0xffffffffu, lim >= kBk);
@@ -954,6 +977,29 @@ bool make_map_kv(CUtensorMap* m, const void* base, int64_t N, int H, int D) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Pages [P, H, 128, D] bf16 seen through the same (D, H, rows) box as
+// make_map_kv: coordinate (x, g, z) with z = page * H * 128 + r addresses row r
+// of head g in the page (head stride 128 * D, row stride D elements), so a
+// 128-row box at z = page * H * 128 is head g's whole page.
+bool make_map_kv_pages(CUtensorMap* m, const void* base, int64_t pages, int H, int D) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess || qr != cudaDriverEntryPointSuccess)
+      return false;
+    fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(pages * H * kBk)};
+  cuuint64_t strides[2] = {(cuuint64_t)kBk * D * 2, (cuuint64_t)D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kBk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2D bf16 tensor [rows, D] with a one-row box of 64 columns, 128B swizzle (the
 // layout tile::gather4 row gathers use)
 bool make_map_rows(CUtensorMap* m, const void* base, int64_t rows, int D) {
@@ -987,12 +1033,16 @@ int sm_count() {
 }
 
 template <int D>
-cudaError_t launch_tiles(const void* q, const void* kk, const void* v, int64_t N, int64_t q0,
-                         int H_q, int H_kv, int k, float scale_log2, int64_t nb, const AttnWs& ws,
-                         int64_t n_b, const Diag& dg, cudaStream_t st) {
+cudaError_t launch_tiles(const void* q, const void* kk, const void* v, int64_t N, int64_t kv_rows,
+                         int64_t q0, int H_q, int H_kv, int k, float scale_log2, int64_t nb,
+                         const AttnWs& ws, const int32_t* tbase, int64_t n_b, const Diag& dg,
+                         cudaStream_t st) {
   CUtensorMap tk, tv;
   CUtensorMap tq;
-  if (!make_map_kv(&tk, kk, N, H_kv, D) || !make_map_kv(&tv, v, N, H_kv, D) ||
+  const bool paged = tbase != nullptr;  // kv_rows = pages * H_kv * 128
+  const int64_t pages = kv_rows / ((int64_t)H_kv * kBk);
+  if (!(paged ? make_map_kv_pages(&tk, kk, pages, H_kv, D) : make_map_kv(&tk, kk, kv_rows, H_kv, D)) ||
+      !(paged ? make_map_kv_pages(&tv, v, pages, H_kv, D) : make_map_kv(&tv, v, kv_rows, H_kv, D)) ||
       !make_map_rows(&tq, q, N * H_q, D))
     return cudaErrorInvalidValue;
   const int smem = AttnSmem<D>::kBytes;
@@ -1000,14 +1050,15 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, int64_t N
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   attn_tile_tc_kernel<D><<<sm_count(), kAttnThreads, smem, st>>>(
-      tk, tv, tq, N * H_q, q0, H_q, H_kv, k, scale_log2, nb, ws.entries, ws.tinfo,
+      tk, tv, tq, N * H_q, q0, H_q, H_kv, k, scale_log2, nb, ws.entries, ws.tinfo, tbase,
       ws.tile_off + n_b, ws.part, dg);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k) {
+size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k,
+                     bool with_tbase) {
   int64_t n_b = (int64_t)H_kv * nb;
   size_t s = 0;
   s += align256((size_t)n_b * 4);        // counts
@@ -1017,13 +1068,15 @@ size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k)
   if (n_b <= kSmemBucketsMax) s += align256((size_t)kBucketCtas * n_b * 4);  // percta
   s += align256((size_t)chunk * H_kv * k * 4);
   s += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * 16);
+  if (with_tbase) s += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * 4);
   s += align256((size_t)chunk * H_kv * k * 4);
   s += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * (kTileRows / (H_q / H_kv)) *
                 attn_rec_bytes(H_q / H_kv, d));
   return s;
 }
 
-AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k) {
+AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k,
+                     bool with_tbase) {
   int64_t n_b = (int64_t)H_kv * nb;
   unsigned char* p = (unsigned char*)ws;
   AttnWs w;
@@ -1038,6 +1091,11 @@ AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int
   }
   w.entries = (int32_t*)p;  p += align256((size_t)chunk * H_kv * k * 4);
   w.tinfo = (int4*)p;       p += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * 16);
+  w.tbase = nullptr;
+  if (with_tbase) {
+    w.tbase = (int32_t*)p;
+    p += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * 4);
+  }
   w.rec_of = (int32_t*)p;   p += align256((size_t)chunk * H_kv * k * 4);
   w.part = p;
   return w;
@@ -1047,8 +1105,10 @@ cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* 
                                      const int32_t* ids, int64_t N, int64_t q0, int64_t q1,
                                      int H_q, int H_kv, int d, int k, float scale, void* out,
                                      float* lse, const AttnWs& ws, int64_t nb, const Diag& dg,
-                                     cudaStream_t st) {
+                                     cudaStream_t st, const AttnBatch& bt) {
   const int64_t n_b = (int64_t)H_kv * nb;
+  const int32_t* tbase = bt.paged ? ws.tbase : nullptr;
+  if (bt.paged && !tbase) return cudaErrorInvalidValue;
   const int G = H_q / H_kv;
   const int qt = kTileRows / G;
   note_launches(n_b <= kSmemBucketsMax ? 8 : 7);  // memset, count, scan, (base,) fill, map, tile, merge
@@ -1058,27 +1118,31 @@ cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* 
   const bool smem_buckets = n_b <= kSmemBucketsMax;
   unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 32);
   if (smem_buckets)
-    bucket_count_smem_kernel<<<kBucketCtas, 1024, n_b * 4, st>>>(ids, q0, q1, H_kv, k, nb,
-                                                                 ws.counts, ws.percta, ws.rec_of,
-                                                                 dg);
+    bucket_count_smem_kernel<<<kBucketCtas, 1024, n_b * 4, st>>>(
+        ids, q0, q1, H_kv, k, nb, bt.qinfo, ws.counts, ws.percta, ws.rec_of, dg);
   else
-    bucket_count_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, ws.counts, ws.rec_of, dg);
+    bucket_count_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, bt.qinfo, ws.counts,
+                                              ws.rec_of, dg);
   bucket_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, n_b, qt, ws.offsets, ws.tile_off, ws.cursor);
   if (smem_buckets) {
     bucket_cta_base_kernel<<<(unsigned)((n_b + 255) / 256), 256, 0, st>>>(ws.offsets, (int)n_b,
                                                                           kBucketCtas, ws.percta);
     bucket_fill_smem_kernel<<<kBucketCtas, 1024, n_b * 4, st>>>(
-        ids, q0, q1, H_kv, k, nb, qt, ws.offsets, ws.tile_off, ws.percta, ws.entries, ws.rec_of);
+        ids, q0, q1, H_kv, k, nb, bt.qinfo, qt, ws.offsets, ws.tile_off, ws.percta, ws.entries,
+        ws.rec_of);
   } else {
-    bucket_fill_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, qt, ws.offsets,
+    bucket_fill_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, bt.qinfo, qt, ws.offsets,
                                              ws.tile_off, ws.cursor, ws.entries, ws.rec_of);
   }
   const int64_t tiles_max = max_tiles(q1 - q0, n_b, H_q, H_kv, k);
   tile_map_kernel<<<(unsigned)std::min<int64_t>((tiles_max + 255) / 256, 152 * 16), 256, 0, st>>>(
-      ws.tile_off, ws.offsets, n_b, nb, qt, ws.tinfo);
+      ws.tile_off, ws.offsets, n_b, nb, qt, bt.vinfo, const_cast<int32_t*>(tbase), ws.tinfo);
   const float scale_log2 = scale * 1.4426950408889634f;
-  e = d == 128 ? launch_tiles<128>(q, kk, v, N, q0, H_q, H_kv, k, scale_log2, nb, ws, n_b, dg, st)
-               : launch_tiles<64>(q, kk, v, N, q0, H_q, H_kv, k, scale_log2, nb, ws, n_b, dg, st);
+  const int64_t kv_rows = bt.kv_rows > 0 ? bt.kv_rows : N;
+  e = d == 128 ? launch_tiles<128>(q, kk, v, N, kv_rows, q0, H_q, H_kv, k, scale_log2, nb, ws,
+                                   tbase, n_b, dg, st)
+               : launch_tiles<64>(q, kk, v, N, kv_rows, q0, H_q, H_kv, k, scale_log2, nb, ws,
+                                  tbase, n_b, dg, st);
   if (e != cudaSuccess) return e;
   if (G * d <= 1024) {
     const int64_t nw = (q1 - q0) * H_kv;  // one warp per (query, group)
@@ -1111,6 +1175,33 @@ cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* 
       attn_merge_kernel<64><<<mg, 256, 0, st>>>(ws.part, ws.rec_of, q0, q1, H_q, H_kv, k,
                                                 (uint16_t*)out, lse);
   }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ batch geometry
+// grid (sequences, slices): slice y of sequence s writes every gridDim.y-th
+// query and block of s
+__global__ void batch_info_kernel(const __grid_constant__ BatchSeqs tb,
+                                  const int32_t* __restrict__ page_table, int page_rows,
+                                  int2* __restrict__ qinfo, int2* __restrict__ vinfo) {
+  const int s = blockIdx.x;
+  const int step = gridDim.y * blockDim.x;
+  const int first = blockIdx.y * blockDim.x + threadIdx.x;
+  const int vb = tb.vb[s], q_start = tb.q_start[s], q_off = tb.q_off[s];
+  for (int i = first; i < tb.q_len[s]; i += step) qinfo[q_start + i] = make_int2(vb, q_off + i);
+  for (int b = first; b < tb.n_blk[s]; b += step) {
+    const int row = page_table ? page_table[tb.kv_start[s] + b] * page_rows
+                               : tb.kv_start[s] + b * kBk;
+    vinfo[vb + b] = make_int2(row, q_start - q_off + b * kBk);
+  }
+}
+
+cudaError_t launch_batch_info(const BatchSeqs& tb, const int32_t* page_table, int page_rows,
+                              int2* qinfo, int2* vinfo, cudaStream_t st) {
+  if (tb.B <= 0) return cudaSuccess;
+  note_launches(1);
+  batch_info_kernel<<<dim3((unsigned)tb.B, 16), 256, 0, st>>>(tb, page_table, page_rows, qinfo,
+                                                              vinfo);
   return cudaGetLastError();
 }
 

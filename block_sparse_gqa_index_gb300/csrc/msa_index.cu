@@ -91,12 +91,18 @@ __device__ __forceinline__ float max32(const uint32_t (&r)[32], int lim) {
 // Sequences of one launch, sorted by tile count (non-increasing). The tile
 // levels j in [tiles[s+1], tiles[s]) are shared by the first s+1 sequences;
 // their (s+1) * (tiles[s] - tiles[s+1]) schedule ranks end at seg_end[s].
+// A sequence's queries are its last len tokens: query i sits at position
+// q_off + i and sees the keys at positions 0 .. q_off + i. Keys are packed
+// (key position p at k_idx row key0 + p) or paged (at row 128 *
+// page_table[pt_row + p / 128] + p % 128).
 constexpr int kMaxSeq = 128;
 struct SeqTable {
   int B;                     // sequences (1 .. kMaxSeq), none empty
   int n_tiles;               // sum of tiles[]
-  int64_t start[kMaxSeq];    // first token of the sequence in the packed batch
-  int64_t len[kMaxSeq];      // tokens
+  int32_t start[kMaxSeq];    // first query row of the sequence (q_idx rows / n_g)
+  int32_t len[kMaxSeq];      // queries
+  int32_t q_off[kMaxSeq];    // position of the first query
+  int32_t key0[kMaxSeq];     // packed: k_idx row of key position 0; paged: pt_row
   int32_t tiles[kMaxSeq];    // 256-row tiles of the sequence's (t, g) rows
   int32_t seg_end[kMaxSeq];  // exclusive end rank of level segment s
 };
@@ -106,7 +112,8 @@ struct TileRef {
   int64_t row0;   // first (t, g) row of the tile in the packed batch
   int64_t lrow0;  // the same row counted from the sequence's first row
   int64_t rows;   // (t, g) rows of the sequence
-  int64_t key0;   // first key of the sequence
+  int64_t key0;   // packed: k_idx row of key position 0; paged: first page-table entry
+  int64_t q_off;  // position of the sequence's first query
 };
 
 __device__ __forceinline__ bool tile_at(const SeqTable& tb, int i, int n_g, TileRef& tr) {
@@ -121,9 +128,10 @@ __device__ __forceinline__ bool tile_at(const SeqTable& tb, int i, int n_g, Tile
   const int p = o % (lo + 1);
   const int j = tb.tiles[lo] - 1 - o / (lo + 1);
   tr.lrow0 = (int64_t)j * kRows;
-  tr.row0 = tb.start[p] * n_g + tr.lrow0;
-  tr.rows = tb.len[p] * n_g;
-  tr.key0 = tb.start[p];
+  tr.row0 = (int64_t)tb.start[p] * n_g + tr.lrow0;
+  tr.rows = (int64_t)tb.len[p] * n_g;
+  tr.key0 = tb.key0[p];
+  tr.q_off = tb.q_off[p];
   return true;
 }
 
@@ -133,7 +141,8 @@ template <int DI, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ SeqTable tab, int n_g, int k,
+                       const __grid_constant__ SeqTable tab,
+                       const int32_t* __restrict__ page_table, int n_g, int k,
                        int32_t* __restrict__ block_ids, float* __restrict__ block_scores,
                        int64_t nb, float score_scale, Diag dg) {
   constexpr int EB = F8 ? 1 : 2;
@@ -188,8 +197,12 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   };
   auto key_blocks = [&](const TileRef& tr) -> int64_t {
     int64_t last = min(tr.lrow0 + kRows, tr.rows) - 1;
-    int64_t loc_max = (last / n_g) / kKeys;
+    int64_t loc_max = (tr.q_off + last / n_g) / kKeys;
     return want_scores ? loc_max + 1 : loc_max;
+  };
+  // k_idx row of key block b's first key
+  auto key_row = [&](const TileRef& tr, int64_t b) -> int32_t {
+    return page_table ? page_table[tr.key0 + b] * kKeys : (int32_t)(tr.key0 + b * kKeys);
   };
   const int rounds = (tab.n_tiles + G - 1) / G;
 
@@ -214,14 +227,17 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           tma_load_2d(sA + c * S::kAChunk, &tm_q, a_full, c * kColsPerChunk, (int32_t)tr.row0);
         a_armed = true;
         a_par ^= 1;
+        int32_t row_next = key_row(tr, 0);  // paged: the page id is read a block ahead
         for (int64_t b = 0; b < nkb; ++b, ++it) {
           const int s = (int)(it % kStages);
           const uint32_t par = (uint32_t)((it / kStages) & 1);
+          const int32_t krow = row_next;
+          if (b + 1 < nkb) row_next = key_row(tr, b + 1);
           if (!mbar_wait(&b_empty[s], par ^ 1, abort_flag, dg)) { ok = false; break; }
           mbar_arrive_expect_tx(&b_full[s], S::kBBytes);
           for (int c = 0; c < S::kChunks; ++c)
             tma_load_2d(sB + s * S::kBBytes + c * S::kBChunk, &tm_k, &b_full[s], c * kColsPerChunk,
-                        (int32_t)(tr.key0 + b * kKeys));
+                        krow);
           armed[s] = true;
           armed_par[s] = par;
         }
@@ -290,7 +306,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int64_t lr = tr.lrow0 + row_in_tile;  // row within the sequence
       const int64_t r = tr.row0 + row_in_tile;    // row within the packed batch
       const bool valid = lr < tr.rows;
-      const int64_t t = valid ? lr / n_g : 0;
+      const int64_t t = valid ? tr.q_off + lr / n_g : 0;  // the query's position
       const int64_t loc = t / kKeys;
       RowTopK top;
       top.init(k - 1);
@@ -388,16 +404,25 @@ int num_sms() {
   return n;
 }
 
-// fills tb from the sequences' (start, len), none empty, at most kMaxSeq
-void make_table(SeqTable& tb, const int64_t* start, const int64_t* len, int B, int n_g) {
+// one sequence of a launch: queries start .. start + len - 1 at positions
+// q_off .. q_off + len - 1, keys from key0 (packed row or page-table entry)
+struct SeqIn {
+  int64_t start, len, q_off, key0;
+};
+
+// fills tb from at most kMaxSeq non-empty sequences
+void make_table(SeqTable& tb, const SeqIn* in, int B, int n_g) {
   int idx[kMaxSeq];
   for (int i = 0; i < B; ++i) idx[i] = i;
-  auto tiles_of = [&](int i) { return (int32_t)((len[i] * n_g + kRows - 1) / kRows); };
+  auto tiles_of = [&](int i) { return (int32_t)((in[i].len * n_g + kRows - 1) / kRows); };
   std::stable_sort(idx, idx + B, [&](int a, int b) { return tiles_of(a) > tiles_of(b); });
   tb.B = B;
   for (int s = 0; s < B; ++s) {
-    tb.start[s] = start[idx[s]];
-    tb.len[s] = len[idx[s]];
+    const SeqIn& x = in[idx[s]];
+    tb.start[s] = (int32_t)x.start;
+    tb.len[s] = (int32_t)x.len;
+    tb.q_off[s] = (int32_t)x.q_off;
+    tb.key0[s] = (int32_t)x.key0;
     tb.tiles[s] = tiles_of(idx[s]);
   }
   int64_t end = 0;
@@ -409,15 +434,17 @@ void make_table(SeqTable& tb, const int64_t* start, const int64_t* len, int B, i
   tb.n_tiles = (int)end;
 }
 
-// q_idx [n_tok, n_g, DI] and k_idx [n_tok, DI] hold every sequence of tb
+// q_idx [n_q, n_g, DI] holds every query of tb; k_idx [n_keys, DI] its keys
+// (packed, or pages of 128 rows when page_table is given)
 template <int DI, bool F8>
-cudaError_t launch_tc(const void* q_idx, const void* k_idx, int64_t n_tok, const SeqTable& tb,
-                      int n_g, int k, int32_t* block_ids, float* block_scores, int64_t nb,
-                      float score_scale, const Diag& dg, cudaStream_t st) {
+cudaError_t launch_tc(const void* q_idx, const void* k_idx, int64_t n_q, int64_t n_keys,
+                      const SeqTable& tb, const int32_t* page_table, int n_g, int k,
+                      int32_t* block_ids, float* block_scores, int64_t nb, float score_scale,
+                      const Diag& dg, cudaStream_t st) {
   constexpr int EB = F8 ? 1 : 2;
   CUtensorMap tq, tk;
-  if (!make_map_2d(&tq, q_idx, n_tok * n_g, DI, kRows, EB) ||
-      !make_map_2d(&tk, k_idx, n_tok, DI, kKeys, EB))
+  if (!make_map_2d(&tq, q_idx, n_q * n_g, DI, kRows, EB) ||
+      !make_map_2d(&tk, k_idx, n_keys, DI, kKeys, EB))
     return cudaErrorInvalidValue;
   const int smem = Smem<DI, EB>::kBytes + 1024;
   cudaError_t e = cudaFuncSetAttribute(index_select_tc_kernel<DI, F8>,
@@ -426,8 +453,32 @@ cudaError_t launch_tc(const void* q_idx, const void* k_idx, int64_t n_tok, const
   const int grid = std::min(tb.n_tiles, num_sms());
   note_launches(1);
   index_select_tc_kernel<DI, F8><<<grid, kThreads, smem, st>>>(
-      tq, tk, tb, n_g, k, block_ids, block_scores, nb, score_scale, dg);
+      tq, tk, tb, page_table, n_g, k, block_ids, block_scores, nb, score_scale, dg);
   return cudaGetLastError();
+}
+
+// bf16 launches over a batch, kMaxSeq non-empty sequences at a time
+cudaError_t launch_batch(const void* q_idx, const void* k_idx, int64_t n_q, int64_t n_keys,
+                         const SeqIn* seqs, int B, const int32_t* page_table, int n_g, int d_idx,
+                         int k, int32_t* block_ids, const Diag& dg, cudaStream_t st) {
+  SeqIn part[kMaxSeq];
+  int m = 0;
+  for (int b = 0; b <= B; ++b) {
+    if (m == kMaxSeq || (b == B && m > 0)) {
+      SeqTable tb;
+      make_table(tb, part, m, n_g);
+      const cudaError_t e =
+          d_idx == 128 ? launch_tc<128, false>(q_idx, k_idx, n_q, n_keys, tb, page_table, n_g, k,
+                                               block_ids, nullptr, 0, 1.f, dg, st)
+                       : launch_tc<64, false>(q_idx, k_idx, n_q, n_keys, tb, page_table, n_g, k,
+                                              block_ids, nullptr, 0, 1.f, dg, st);
+      if (e != cudaSuccess) return e;
+      m = 0;
+    }
+    if (b == B) break;
+    if (seqs[b].len > 0) part[m++] = seqs[b];
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -438,16 +489,16 @@ cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int64_t N,
                                 float score_scale) {
   if (N * n_g == 0) return cudaSuccess;
   SeqTable tb;
-  const int64_t start = 0;
-  make_table(tb, &start, &N, 1, n_g);
+  const SeqIn one{0, N, 0, 0};
+  make_table(tb, &one, 1, n_g);
   if (e4m3)  // E4M3 codes: 128 dimensions fill one 128-byte swizzle row
-    return launch_tc<128, true>(q_idx, k_idx, N, tb, n_g, k, block_ids, block_scores, nb,
-                                score_scale, dg, st);
+    return launch_tc<128, true>(q_idx, k_idx, N, N, tb, nullptr, n_g, k, block_ids, block_scores,
+                                nb, score_scale, dg, st);
   if (d_idx == 128)
-    return launch_tc<128, false>(q_idx, k_idx, N, tb, n_g, k, block_ids, block_scores, nb, 1.f,
-                                 dg, st);
-  return launch_tc<64, false>(q_idx, k_idx, N, tb, n_g, k, block_ids, block_scores, nb, 1.f, dg,
-                              st);
+    return launch_tc<128, false>(q_idx, k_idx, N, N, tb, nullptr, n_g, k, block_ids,
+                                 block_scores, nb, 1.f, dg, st);
+  return launch_tc<64, false>(q_idx, k_idx, N, N, tb, nullptr, n_g, k, block_ids, block_scores,
+                              nb, 1.f, dg, st);
 }
 
 cudaError_t launch_index_select_varlen(const void* q_idx, const void* k_idx,
@@ -455,27 +506,37 @@ cudaError_t launch_index_select_varlen(const void* q_idx, const void* k_idx,
                                        int k, int32_t* block_ids, const Diag& dg,
                                        cudaStream_t st) {
   const int64_t n_tok = cu_seqlens[B];
-  int64_t start[kMaxSeq], len[kMaxSeq];
-  int m = 0;
-  // non-empty sequences, kMaxSeq per launch
-  for (int b = 0; b <= B; ++b) {
-    if (m == kMaxSeq || (b == B && m > 0)) {
-      SeqTable tb;
-      make_table(tb, start, len, m, n_g);
-      const cudaError_t e =
-          d_idx == 128 ? launch_tc<128, false>(q_idx, k_idx, n_tok, tb, n_g, k, block_ids,
-                                               nullptr, 0, 1.f, dg, st)
-                       : launch_tc<64, false>(q_idx, k_idx, n_tok, tb, n_g, k, block_ids,
-                                              nullptr, 0, 1.f, dg, st);
-      if (e != cudaSuccess) return e;
-      m = 0;
+  for (int b0 = 0; b0 < B; b0 += kMaxSeq) {  // the table is filled in slices of kMaxSeq
+    SeqIn seqs[kMaxSeq];
+    const int m = std::min(kMaxSeq, B - b0);
+    for (int i = 0; i < m; ++i) {
+      const int64_t t0 = cu_seqlens[b0 + i];
+      seqs[i] = SeqIn{t0, cu_seqlens[b0 + i + 1] - t0, 0, t0};
     }
-    if (b == B) break;
-    if (cu_seqlens[b + 1] > cu_seqlens[b]) {
-      start[m] = cu_seqlens[b];
-      len[m] = cu_seqlens[b + 1] - cu_seqlens[b];
-      ++m;
+    const cudaError_t e = launch_batch(q_idx, k_idx, n_tok, n_tok, seqs, m, nullptr, n_g, d_idx,
+                                       k, block_ids, dg, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_index_select_paged(const void* q_idx, const void* k_idx_pages,
+                                      int64_t n_pages, const int32_t* page_table, int max_pages,
+                                      const int64_t* cu_q, const int64_t* kv_lens, int B, int n_g,
+                                      int d_idx, int k, int32_t* block_ids, const Diag& dg,
+                                      cudaStream_t st) {
+  const int64_t n_q = cu_q[B];
+  for (int b0 = 0; b0 < B; b0 += kMaxSeq) {
+    SeqIn seqs[kMaxSeq];
+    const int m = std::min(kMaxSeq, B - b0);
+    for (int i = 0; i < m; ++i) {
+      const int b = b0 + i;
+      const int64_t len = cu_q[b + 1] - cu_q[b];
+      seqs[i] = SeqIn{cu_q[b], len, kv_lens[b] - len, (int64_t)b * max_pages};
     }
+    const cudaError_t e = launch_batch(q_idx, k_idx_pages, n_q, n_pages * kKeys, seqs, m,
+                                       page_table, n_g, d_idx, k, block_ids, dg, st);
+    if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }

@@ -24,12 +24,20 @@ cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int64_t N,
                                 int64_t nb, const Diag& dg, cudaStream_t st, bool e4m3 = false,
                                 float score_scale = 1.f);
 
-// One launch per 128 non-empty sequences of a packed batch; cu_seqlens is a
-// host array [B + 1] of token offsets (msa_index.cu).
+// One launch per 128 sequences of a packed batch; cu_seqlens is a host
+// array [B + 1] of token offsets (msa_index.cu).
 cudaError_t launch_index_select_varlen(const void* q_idx, const void* k_idx,
                                        const int64_t* cu_seqlens, int B, int n_g, int d_idx,
                                        int k, int32_t* block_ids, const Diag& dg,
                                        cudaStream_t st);
+// Paged k_idx: pages [n_pages, 128, d_idx]; sequence b's queries are rows
+// cu_q[b] .. cu_q[b + 1] - 1 of q_idx, its last tokens of kv_lens[b]; its key
+// block j is page page_table[b * max_pages + j] (host arrays cu_q, kv_lens).
+cudaError_t launch_index_select_paged(const void* q_idx, const void* k_idx_pages,
+                                      int64_t n_pages, const int32_t* page_table, int max_pages,
+                                      const int64_t* cu_q, const int64_t* kv_lens, int B, int n_g,
+                                      int d_idx, int k, int32_t* block_ids, const Diag& dg,
+                                      cudaStream_t st);
 
 // Exp-free top-k over block scores (msa_topk.cu).
 cudaError_t launch_topk(const float* S, int64_t N, int n_g, int64_t nb, int Bk, int k,
@@ -44,20 +52,58 @@ struct AttnWs {
   int32_t* tile_off;  // [n_g * nb + 1]
   int32_t* percta;    // [bucketing CTAs, n_g * nb] per-CTA counts, then first positions
   int32_t* entries;   // [chunk * n_g * k]
-  int4* tinfo;        // per tile: block, first entry, queries | group << 8, end tile
+  int4* tinfo;        // per tile: K / V row, first entry, queries | group << 8, end tile
+  int32_t* tbase;     // per tile: query row at the block's first key (paged batches only)
   int32_t* rec_of;    // [chunk, n_g, k]: partial record of each (query, group, slot), or -1
   unsigned char* part;  // [tiles, qt] records of attn_rec_bytes(G, d) bytes, tile-major
 };
 // One partial record per (query, group, slot): the G heads' normalised O rows
 // (bf16, d each), then their G LSEs (fp32), padded to a multiple of 16 bytes.
 __host__ __device__ inline int attn_rec_bytes(int G, int d) { return G * d * 2 + (G + 3) / 4 * 16; }
-size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k);
-AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k);
+// with_tbase: room for the per-tile query bases that paged K / V needs
+size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k,
+                     bool with_tbase = false);
+AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k,
+                     bool with_tbase = false);
+
+// Geometry of a batch of sequences for the main branch. All null: one
+// sequence whose query row t sits at position t and whose block b starts at
+// K / V row 128 b. Otherwise blocks are numbered per batch ("virtual blocks",
+// each sequence's blocks consecutive from its first virtual block) and
+//   qinfo[t] = {first virtual block of query row t's sequence, t's position},
+//   vinfo[v] = {K / V row of block v's first key,
+//               query row that would sit at that key's position}.
+// Packed sequences keep queries and keys in the same rows, so the two fields
+// of vinfo agree; paged K / V (kv_rows rows of pages) is where they differ.
+struct AttnBatch {
+  const int2* qinfo = nullptr;
+  const int2* vinfo = nullptr;
+  int64_t kv_rows = 0;  // rows of the K / V tensors (0: as many as query rows)
+  bool paged = false;
+};
 cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* v,
                                      const int32_t* ids, int64_t N, int64_t q0, int64_t q1,
                                      int H_q, int H_kv, int d, int k, float scale, void* out,
                                      float* lse, const AttnWs& ws, int64_t nb, const Diag& dg,
-                                     cudaStream_t st);
+                                     cudaStream_t st, const AttnBatch& bt = AttnBatch());
+
+// Sequences of a batch for the main branch's geometry, at most kBatchSeqs
+// per launch of launch_batch_info.
+constexpr int kBatchSeqs = 128;
+struct BatchSeqs {
+  int B;
+  int32_t q_start[kBatchSeqs];   // first query row
+  int32_t q_len[kBatchSeqs];     // query rows
+  int32_t q_off[kBatchSeqs];     // position of the first query (keys before it are cached)
+  int32_t vb[kBatchSeqs];        // first virtual block
+  int32_t n_blk[kBatchSeqs];     // blocks of the sequence's keys
+  int32_t kv_start[kBatchSeqs];  // packed: first K / V row; paged: first page-table entry
+};
+// fills qinfo / vinfo (AttnBatch) for the sequences of tb; page_table null:
+// packed K / V; else block j of a sequence starts at K / V row
+// page_table[kv_start + j] * page_rows
+cudaError_t launch_batch_info(const BatchSeqs& tb, const int32_t* page_table, int page_rows,
+                              int2* qinfo, int2* vinfo, cudaStream_t st);
 
 // Decode (msa_decode.cu).
 cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,

@@ -140,22 +140,21 @@ int msa_sparse_attn(const void* q, const void* k, const void* v, const int32_t* 
  *   cu_seqlens  host int64 [B + 1] with 0 = cu_seqlens[0] <= ... <= cu_seqlens[B]
  *               (MSA_ERR_INVALID_ARG otherwise)
  * Other tensors as in msa_index_select / msa_sparse_attn with N = cu_seqlens[B].
- * Index branch: one launch per 128 non-empty sequences; the row tiles of all of
- * them form one heaviest-first schedule over the SMs, so short sequences fill
- * the gaps that long ones leave. q_idx, k_idx and block_ids must be 16-byte
- * aligned (MSA_ERR_INVALID_ARG); N * n_groups must stay below 2^31
- * (MSA_ERR_UNSUPPORTED).
- * Main branch: each sequence runs as its own pass of the single-sequence
- * kernels on the stream, which reuses the workspace from one sequence to the
- * next. Every sequence's rows must start 16-byte aligned: H_kv * topk (and H_q
- * when lse is given) a multiple of 4, else MSA_ERR_UNSUPPORTED. */
+ * Index branch: one launch per 128 sequences; the row tiles of all of them
+ * form one heaviest-first schedule over the SMs, so short sequences fill the
+ * gaps that long ones leave. Main branch: one pass over the whole batch (its
+ * buckets are the blocks of every sequence), in chunks of query rows when the
+ * workspace is smaller than msa_sparse_attn_varlen_workspace_bytes.
+ * Tensors must be 16-byte aligned (MSA_ERR_INVALID_ARG); N * n_groups must
+ * stay below 2^31 (MSA_ERR_UNSUPPORTED). */
 int msa_index_select_varlen(const void* q_idx, const void* k_idx, const int64_t* cu_seqlens,
                             int B, int n_groups, int d_idx, int Bk, int k, int32_t* block_ids,
                             void* stream);
 
-/* Workspace for msa_sparse_attn_varlen to take every sequence in one pass (any
- * msa_sparse_attn_workspace_bytes(c, ...) with c >= 1 also works, in chunks);
- * 0 when cu_seqlens is invalid. */
+/* Workspace for msa_sparse_attn_varlen to take the whole batch in one pass;
+ * 0 when cu_seqlens is invalid or holds no token. A smaller workspace works in
+ * chunks of query rows as long as it holds 16 bytes per token plus one
+ * chunk's bucketing and partials (MSA_ERR_WORKSPACE otherwise). */
 size_t msa_sparse_attn_varlen_workspace_bytes(const int64_t* cu_seqlens, int B, int H_q,
                                               int H_kv, int d, int Bk, int k);
 
@@ -163,6 +162,60 @@ int msa_sparse_attn_varlen(const void* q, const void* k, const void* v, const in
                            const int64_t* cu_seqlens, int B, int H_q, int H_kv, int d, int Bk,
                            int topk, float scale, void* out, float* lse, void* workspace,
                            size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------- paged prefill -- */
+
+/* Prefill over paged caches (chunked prefill): sequence b holds kv_lens[b]
+ * tokens, already written to the caches, of which the last
+ * cu_q[b + 1] - cu_q[b] are its queries, packed back to back as rows cu_q[b] ..
+ * cu_q[b + 1] - 1 of q_idx / q / out / lse / block_ids. Query i of sequence b
+ * sits at position kv_lens[b] - (cu_q[b + 1] - cu_q[b]) + i and sees the keys
+ * at positions 0 .. its own. Logical block j of sequence b is physical page
+ * page_table[b * max_pages + j] (device int32 [B, max_pages]), the layout the
+ * decode entry points below use ("运行 Kernel" of the MSA page plans its calls
+ * from per-sequence query and key lengths over paged KV with page size = block
+ * size). Block ids count from the sequence's first token, as in decode; with
+ * kv_lens[b] equal to the query count every sequence is a plain varlen
+ * sequence, and the results are those of msa_*_varlen.
+ *   cu_q       host int64 [B + 1], 0 = cu_q[0] <= ... <= cu_q[B]
+ *   kv_lens    host int64 [B], queries of b <= kv_lens[b] <= max_pages * Bk
+ *              (MSA_ERR_INVALID_ARG otherwise)
+ *   n_pages    pages P of the cache tensors; page ids outside 0 .. P - 1 read
+ *              zeros (the caller keeps the table valid)
+ * Sizes: cu_q[B] * n_groups and P * Bk (index), P * H_kv * Bk (main branch)
+ * and B * max_pages below 2^31, else MSA_ERR_UNSUPPORTED. */
+
+/* Index branch.
+ *   q_idx        [cu_q[B], n_groups, d_idx] bf16
+ *   k_idx_pages  [P, Bk, d_idx] bf16
+ *   block_ids    [cu_q[B], n_groups, k] int32 out
+ * One launch per 128 sequences; tiles are ordered by their row-tile index
+ * within the sequence (the cached prefix adds the same key blocks to every
+ * tile of a sequence). */
+int msa_index_select_paged(const void* q_idx, const void* k_idx_pages, int64_t n_pages,
+                           const int32_t* page_table, int max_pages, const int64_t* cu_q,
+                           const int64_t* kv_lens, int B, int n_groups, int d_idx, int Bk, int k,
+                           int32_t* block_ids, void* stream);
+
+/* Workspace for msa_sparse_attn_paged in one pass; 0 on invalid lengths or
+ * no query. Smaller workspaces work in chunks, as for varlen. */
+size_t msa_sparse_attn_paged_workspace_bytes(const int64_t* cu_q, const int64_t* kv_lens, int B,
+                                             int max_pages, int H_q, int H_kv, int d, int Bk,
+                                             int k);
+
+/* Main branch.
+ *   q            [cu_q[B], H_q, d] bf16
+ *   k_pages      [P, H_kv, Bk, d] bf16 (the decode layout)
+ *   v_pages      same
+ *   block_ids    [cu_q[B], H_kv, k] int32 (msa_index_select_paged)
+ *   out, lse     [cu_q[B], H_q, d] bf16, [cu_q[B], H_q] fp32 (lse may be NULL)
+ * Other arguments as in msa_sparse_attn. */
+int msa_sparse_attn_paged(const void* q, const void* k_pages, const void* v_pages,
+                          int64_t n_pages, const int32_t* page_table, int max_pages,
+                          const int32_t* block_ids, const int64_t* cu_q, const int64_t* kv_lens,
+                          int B, int H_q, int H_kv, int d, int Bk, int topk, float scale,
+                          void* out, float* lse, void* workspace, size_t workspace_bytes,
+                          void* stream);
 
 /* ----------------------------------------------------------------- decode -- */
 

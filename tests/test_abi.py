@@ -132,19 +132,64 @@ def test_varlen_rejects(msa):
     assert fi(FAKE, FAKE, p, 1, 8, 128, 128, 16, FAKE, None) == -2  # 2^31 (t, g) rows
     p, keep = cu(0, 100)
     assert fi(None, FAKE, p, 1, 8, 128, 128, 16, FAKE, None) == -1  # null q_idx
-    # main branch: same offset rules; lse rows of 2 heads would misalign sequences
+    # main branch: same offset rules, then the single-sequence shape rules
     args = (FAKE, FAKE, FAKE, FAKE)
     p, keep = cu(3, 10)
     assert fa(*args, p, 1, 32, 8, 128, 128, 16, 0.1, FAKE, None, FAKE, 1 << 20, None) == -1
     p, keep = cu(0, 10)
-    assert fa(*args, p, 1, 2, 1, 128, 128, 16, 0.1, FAKE, FAKE, FAKE, 1 << 20, None) == -2
+    assert fa(*args, p, 1, 12, 4, 128, 128, 16, 0.1, FAKE, None, FAKE, 1 << 20, None) == -2  # G=3
+    assert fa(*args, p, 1, 32, 8, 96, 128, 16, 0.1, FAKE, None, FAKE, 1 << 20, None) == -2
     assert fa(*args, p, 1, 32, 8, 128, 64, 16, 0.1, FAKE, None, FAKE, 1 << 20, None) == -2
-    # workspace query: 0 for bad offsets, the largest sequence's one-pass need otherwise
+    assert fa(*args, p, 1, 32, 8, 128, 128, 16, 0.1, FAKE, None, FAKE, 1000, None) == -3
+    # workspace query: 0 for bad offsets; one pass = 8 bytes per query and per
+    # block of the sequences with queries, plus the bucketing of all rows over
+    # those blocks (here 3 + 6 blocks, like one sequence of 9 blocks)
     p, keep = cu(0, 7, 5)
     assert msa._ws_attn_varlen(p, 2, 32, 8, 128, 128, 16) == 0
     p, keep = cu(0, 300, 300, 1000)
     assert msa._ws_attn_varlen(p, 3, 32, 8, 128, 128, 16) == \
-        msa.msa_sparse_attn_workspace_bytes(700, 700, 32, 8, 128)
+        8192 + 256 + msa.msa_sparse_attn_workspace_bytes(1000, 9 * 128, 32, 8, 128)
+
+
+def test_paged_rejects(msa):
+    """Paged prefill checks the query offsets, the cached lengths against the
+    page table's width and the shapes on the host."""
+    import ctypes as C
+
+    def arr(*xs):
+        a = (C.c_int64 * len(xs))(*xs)
+        return C.cast(a, C.c_void_p), a
+
+    fi, fa, fw = msa._index_paged, msa._attn_paged, msa._ws_attn_paged
+    cu, k1 = arr(0, 100, 150)
+    kv, k2 = arr(1000, 50)
+    # index: q_idx, k_idx_pages, P, page_table, max_pages, cu_q, kv_lens, B, n_g, d_idx, Bk, k
+    bad, k3 = arr(1000, 40)   # 50 queries but 40 keys
+    assert fi(FAKE, FAKE, 64, FAKE, 8, cu, bad, 2, 8, 128, 128, 16, FAKE, None) == -1
+    big, k4 = arr(1025, 50)   # 1025 keys do not fit 8 pages of 128
+    assert fi(FAKE, FAKE, 64, FAKE, 8, cu, big, 2, 8, 128, 128, 16, FAKE, None) == -1
+    assert fi(FAKE, FAKE, 64, None, 8, cu, kv, 2, 8, 128, 128, 16, FAKE, None) == -1
+    assert fi(FAKE, FAKE, 64, FAKE, 8, cu, kv, 2, 8, 128, 64, 16, FAKE, None) == -2
+    assert fi(FAKE, FAKE, 0, FAKE, 8, cu, kv, 2, 8, 128, 128, 16, FAKE, None) == -1
+    empty, k5 = arr(0, 0, 0)
+    assert fi(FAKE, FAKE, 64, FAKE, 8, empty, kv, 2, 8, 128, 128, 16, FAKE, None) == 0
+    # main branch: q, k_pages, v_pages, P, page_table, max_pages, ids, cu_q, kv_lens, B, H_q,
+    # H_kv, d, Bk, topk, scale, out, lse, ws, ws_bytes, stream
+    base = [FAKE, FAKE, FAKE, 64, FAKE, 8, FAKE, cu, kv, 2, 32, 8, 128, 128, 16, 0.1, FAKE, None,
+            FAKE, 1 << 20, None]
+    a = list(base); a[8] = bad
+    assert fa(*a) == -1
+    a = list(base); a[4] = None
+    assert fa(*a) == -1
+    a = list(base); a[10] = 24
+    assert fa(*a) == -2                            # G = 3
+    a = list(base); a[19] = 64
+    assert fa(*a) == -3
+    assert fw(cu, bad, 2, 8, 32, 8, 128, 128, 16) == 0
+    # one pass: 150 queries and 8 + 1 blocks of the two sequences, with the
+    # per-tile query bases of paged K / V
+    assert fw(cu, kv, 2, 8, 32, 8, 128, 128, 16) > \
+        msa.msa_sparse_attn_workspace_bytes(150, 9 * 128, 32, 8, 128)
 
 
 def test_index_fp8_rejects(msa):

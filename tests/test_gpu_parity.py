@@ -550,3 +550,114 @@ def test_repeat_runs_bitwise_identical(msa):
             torch.equal(l, outs[0][2])
     check_structure(outs[0][0].cpu().numpy(), np.arange(w.N), w.Bk)
     assert msa.msa_get_error() == 0
+
+
+# ------------------------------------------------------------- paged prefill
+def _paged_batch(kv_lens, q_lens, H_q, H_kv, d, seed, fill=3.0):
+    """Sequences of kv_lens tokens (one seeded integer-index workload each)
+    whose last q_lens tokens are the queries. K / V / k_idx go to a shared pool
+    of 128-token pages in shuffled order, with spare pages and the unused rows
+    of each sequence's last page set to `fill`, so a read outside the page
+    table or past a sequence's end changes the result."""
+    rng = np.random.default_rng(seed)
+    wls = [synth.make("tiny", L=L, H_q=H_q, H_kv=H_kv, d=d, d_idx=d, seed=seed + i)
+           for i, L in enumerate(kv_lens)]
+    n_blk = [(L + 127) // 128 for L in kv_lens]
+    max_pages = max(n_blk) + 1
+    P = sum(n_blk) + 3
+    perm = rng.permutation(P)
+    pt = np.zeros((len(kv_lens), max_pages), dtype=np.int32)
+    kp = torch.full((P, H_kv, 128, d), fill, dtype=torch.bfloat16, device="cuda")
+    vp = torch.full((P, H_kv, 128, d), fill, dtype=torch.bfloat16, device="cuda")
+    kip = torch.full((P, 128, d), fill, dtype=torch.bfloat16, device="cuda")
+    used = 0
+    for b, (w, nb) in enumerate(zip(wls, n_blk)):
+        pages = perm[used:used + nb]
+        used += nb
+        pt[b, :nb] = pages
+        L = w.N
+        pad = nb * 128 - L
+        idx = torch.as_tensor(pages, dtype=torch.long, device="cuda")
+        for src, dst in ((synth.T_K, kp), (synth.T_V, vp)):
+            t = synth.device_tensor(w, src)                                   # [L, H_kv, d]
+            t = torch.cat([t, torch.full((pad, H_kv, d), fill, dtype=t.dtype, device="cuda")])
+            dst[idx] = t.view(nb, 128, H_kv, d).permute(0, 2, 1, 3)
+        ki = kidx2d(synth.device_tensor(w, synth.T_KIDX))                     # [L, d]
+        ki = torch.cat([ki, torch.full((pad, d), fill, dtype=ki.dtype, device="cuda")])
+        kip[idx] = ki.view(nb, 128, d)
+    cu = [0]
+    for n in q_lens:
+        cu.append(cu[-1] + n)
+    qi = torch.cat([synth.device_tensor(w, synth.T_QIDX)[w.N - n:] for w, n in zip(wls, q_lens)])
+    q = torch.cat([synth.device_tensor(w, synth.T_Q)[w.N - n:] for w, n in zip(wls, q_lens)])
+    return wls, cu, torch.as_tensor(pt, device="cuda"), kip, kp, vp, qi, q
+
+
+@pytest.mark.parametrize("H_q,H_kv,d", [(8, 2, 64), (16, 4, 128)])
+def test_paged_prefill_matches_oracle(msa, H_q, H_kv, d):
+    """Chunked prefill over shuffled pages: per sequence the queries are the
+    last q_len of kv_len tokens (a whole sequence, one token, a chunk that
+    starts mid-block, an empty chunk). Block ids equal the oracle's for those
+    positions bit for bit; attention matches the oracle on them."""
+    kv_lens = [700, 129, 2100, 1000, 300]
+    q_lens = [700, 1, 900, 0, 77]
+    wls, cu, pt, kip, kp, vp, qi, q = _paged_batch(kv_lens, q_lens, H_q, H_kv, d, seed=400)
+    ids = msa.msa_index_select_paged(qi, kip, pt, cu, kv_lens, 128, 16)
+    out, lse = msa.msa_sparse_attn_paged(q, kp, vp, pt, ids, cu, kv_lens, 128, wls[0].scale)
+    torch.cuda.synchronize()
+    ids_h, out_h, lse_h = ids.cpu().numpy(), bf16_to_np(out), lse.cpu().numpy()
+    for i, (w, n) in enumerate(zip(wls, q_lens)):
+        if n == 0:
+            continue
+        a, b = cu[i], cu[i + 1]
+        rows = np.arange(w.N - n, w.N)
+        want = oracle.index_select(synth.host_tensor(w, synth.T_QIDX)[0][w.N - n:], rows,
+                                   synth.host_tensor(w, synth.T_KIDX)[0, :, 0], w.Bk, w.k)
+        assert np.array_equal(ids_h[a:b], want), f"sequence {i}"
+        o_ref, l_ref = oracle.sparse_attn(synth.host_tensor(w, synth.T_Q)[0][w.N - n:], rows,
+                                          synth.host_tensor(w, synth.T_K)[0],
+                                          synth.host_tensor(w, synth.T_V)[0], want, w.Bk, w.scale)
+        check_close(f"o[{i}]", out_h[a:b], o_ref, TOL_O)
+        check_close(f"lse[{i}]", lse_h[a:b], l_ref, TOL_LSE)
+
+
+def test_paged_chunk_equals_full_prefill_rows(msa):
+    """A chunk of the last 1000 of 2500 tokens over paged caches gives exactly
+    the bits of rows 1500 .. 2499 of the single-sequence prefill of all 2500
+    tokens (ids, output and LSE), including with a workspace that forces
+    several chunks of query rows."""
+    L, n = 2500, 1000
+    wls, cu, pt, kip, kp, vp, qi, q = _paged_batch([L], [n], 8, 2, 64, seed=500)
+    w = wls[0]
+    ids = msa.msa_index_select_paged(qi, kip, pt, cu, [L], 128, 16)
+    ws = torch.empty(msa.msa_sparse_attn_paged_workspace_bytes(cu, [L], pt.shape[1], 8, 2, 64)
+                     // 3, dtype=torch.uint8, device="cuda")
+    out, lse = msa.msa_sparse_attn_paged(q, kp, vp, pt, ids, cu, [L], 128, 0.125, workspace=ws)
+    qf = synth.device_tensor(w, synth.T_QIDX)
+    kf = kidx2d(synth.device_tensor(w, synth.T_KIDX))
+    ids_f = msa.msa_index_select(qf, kf, 128, 16)
+    out_f, lse_f = msa.msa_sparse_attn(synth.device_tensor(w, synth.T_Q),
+                                       synth.device_tensor(w, synth.T_K),
+                                       synth.device_tensor(w, synth.T_V), ids_f, 128, 0.125)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids_f[L - n:])
+    assert torch.equal(out, out_f[L - n:])
+    assert torch.equal(lse, lse_f[L - n:])
+
+
+def test_paged_whole_sequences_equal_varlen(msa):
+    """With every token a query (kv_len = q_len) the paged calls give exactly
+    the bits of the packed varlen calls."""
+    lens = [300, 1, 1000, 129]
+    wls, cu, pt, kip, kp, vp, qi, q = _paged_batch(lens, lens, 8, 2, 64, seed=600)
+    ids = msa.msa_index_select_paged(qi, kip, pt, cu, lens, 128, 16)
+    out, lse = msa.msa_sparse_attn_paged(q, kp, vp, pt, ids, cu, lens, 128, 0.125)
+    cat = lambda t: torch.cat([synth.device_tensor(w, t) for w in wls])  # noqa: E731
+    ki = torch.cat([kidx2d(synth.device_tensor(w, synth.T_KIDX)) for w in wls])
+    ids_v = msa.msa_index_select_varlen(qi, ki, cu, 128, 16)
+    out_v, lse_v = msa.msa_sparse_attn_varlen(q, cat(synth.T_K), cat(synth.T_V), ids_v, cu, 128,
+                                              0.125)
+    torch.cuda.synchronize()
+    assert torch.equal(ids, ids_v)
+    assert torch.equal(out, out_v)
+    assert torch.equal(lse, lse_v)
