@@ -15,6 +15,8 @@ Prints ONE JSON line. `value` is prefill tokens/s (all ranks). Further keys:
   cpu_baseline the CPU oracle on a bounded sample of the same workload
   extra        the other measured paths: 32K and 1M prefill (1M: 2 timed steps),
                the 128K tokens as 8 packed 16K sequences (varlen entry points),
+               a chunked prefill of the last 16K of the 128K tokens over paged
+               caches with a shuffled page table,
                the 128K step with the index branch on FP8-E4M3 codes,
                decode steps with bf16 and FP8-E4M3 KV, standalone top-16 (with
                torch.topk over the same scores as a comparator)
@@ -414,6 +416,61 @@ def time_varlen(msa, w, n_seq, steps, warmup):
     return ms, flops, idx_ms
 
 
+def time_paged_chunk(msa, w, nq, steps, warmup):
+    """Chunked prefill over paged caches: the workload's last nq tokens are the
+    queries, all N tokens' K / V / k_idx sit in 128-token pages in a seeded
+    shuffled order (the decode layout). One step = msa_index_select_paged then
+    msa_sparse_attn_paged."""
+    import torch
+    import synth
+    L = w.N
+    nb = L // w.Bk
+    P = nb + 8
+    gen = torch.Generator().manual_seed(5)
+    perm = torch.randperm(P, generator=gen)[:nb].to(torch.int32)
+    pt = perm.view(1, -1).cuda().contiguous()
+    idx = perm.long().cuda()
+    kp = torch.zeros((P, w.H_kv, w.Bk, w.d), dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    kip = torch.zeros((P, w.Bk, w.d_idx), dtype=torch.bfloat16, device="cuda")
+    kp[idx] = synth.device_tensor(w, synth.T_K).view(nb, w.Bk, w.H_kv, w.d).permute(0, 2, 1, 3)
+    vp[idx] = synth.device_tensor(w, synth.T_V).view(nb, w.Bk, w.H_kv, w.d).permute(0, 2, 1, 3)
+    kip[idx] = synth.device_tensor(w, synth.T_KIDX)[:, 0].reshape(nb, w.Bk, w.d_idx)
+    q = synth.device_tensor(w, synth.T_Q)[L - nq:].contiguous()
+    qi = synth.device_tensor(w, synth.T_QIDX)[L - nq:].contiguous()
+    cu, kv = [0, nq], [L]
+    ids = torch.empty((nq, w.n_g, w.k), dtype=torch.int32, device="cuda")
+    ws = torch.empty(msa.msa_sparse_attn_paged_workspace_bytes(cu, kv, nb, w.H_q, w.H_kv, w.d,
+                                                               w.Bk, w.k),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty((nq, w.H_q), dtype=torch.float32, device="cuda")
+
+    def index():
+        msa.msa_index_select_paged(qi, kip, pt, cu, kv, w.Bk, w.k, block_ids=ids)
+
+    def step():
+        index()
+        msa.msa_sparse_attn_paged(q, kp, vp, pt, ids, cu, kv, w.Bk, w.scale, workspace=ws,
+                                  out=out, lse=lse)
+
+    res = []
+    for f in (step, index):
+        for _ in range(warmup):
+            f()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            f()
+        b.record()
+        torch.cuda.synchronize()
+        res.append(a.elapsed_time(b) / steps)
+    fl_i = index_flops(L, w.n_g, w.d_idx) - index_flops(L - nq, w.n_g, w.d_idx)
+    fl_a = attn_flops(L, w.H_q, w.d, w.Bk, w.k) - attn_flops(L - nq, w.H_q, w.d, w.Bk, w.k)
+    return res[0], res[1], fl_i, fl_a
+
+
 def time_prefill_fp8_index(msa, w, steps, warmup):
     """Prefill step with the index branch on FP8-E4M3 codes of q_idx / k_idx
     (rounded to nearest by torch before the timing) and the bf16 main branch."""
@@ -667,6 +724,13 @@ def main():
         extra["prefill_varlen_8x16k"] = {"tokens_per_s": w.N / (v_ms * 1e-3), "ms": round(v_ms, 3),
                                          "index_ms": round(v_idx, 3),
                                          "tflops": round(v_fl / (v_ms * 1e-3) / 1e12, 2)}
+        p_ms, p_idx, p_fli, p_fla = time_paged_chunk(msa, w, 16384, args.steps, 3)
+        torch.cuda.empty_cache()
+        extra["prefill_paged_chunk_16k_of_128k"] = {
+            "query_tokens_per_s": 16384 / (p_ms * 1e-3), "ms": round(p_ms, 3),
+            "index_ms": round(p_idx, 3),
+            "index_tflops": round(p_fli / (p_idx * 1e-3) / 1e12, 2),
+            "tflops": round((p_fli + p_fla) / (p_ms * 1e-3) / 1e12, 2)}
         wd = synth.make("decode")
         for fp8 in (False, True):
             i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, 1)
