@@ -18,7 +18,8 @@ Prints ONE JSON line. `value` is prefill tokens/s (all ranks). Further keys:
                a chunked prefill of the last 16K of the 128K tokens over paged
                caches with a shuffled page table,
                the 128K step with the index branch on FP8-E4M3 codes,
-               decode steps with bf16 and FP8-E4M3 KV, standalone top-16 (with
+               decode steps with bf16 KV, FP8-E4M3 KV, and FP8-E4M3 KV plus an
+               FP8-E4M3 k_idx cache, standalone top-16 (with
                torch.topk over the same scores as a comparator)
 
 Multi-GPU: each rank runs its own independent sequence (no collective on the
@@ -274,9 +275,10 @@ def e2e_prefill(msa, P, steps, warmup):
     return ms, h2d, d2h
 
 
-def time_decode(msa, w, fp8, steps, warmup):
+def time_decode(msa, w, fp8, steps, warmup, fp8_index=False):
     """Decode step for B sequences: index branch (k_idx cache scan + top-k) and
-    main branch over the selected pages."""
+    main branch over the selected pages. fp8: E4M3 K / V pages; fp8_index: the
+    k_idx cache and q_idx as E4M3 codes too (rounded by torch before timing)."""
     import torch
     import synth
     dev = torch.device("cuda")
@@ -290,6 +292,11 @@ def time_decode(msa, w, fp8, steps, warmup):
     qidx = synth.device_rows(w, synth.T_QIDX, last)
     ks, vs = synth.fp8_scales(w.H_kv)
     kw = dict(k_scale=torch.from_numpy(ks).to(dev), v_scale=torch.from_numpy(vs).to(dev)) if fp8 else {}
+    if fp8_index:
+        kidx_p = kidx_p.to(torch.float8_e4m3fn)
+        qidx = qidx.to(torch.float8_e4m3fn)
+        torch.cuda.empty_cache()
+    index = msa.msa_index_select_decode_fp8 if fp8_index else msa.msa_index_select_decode
     ids = torch.empty((w.B, w.n_g, w.k), dtype=torch.int32, device=dev)
     ws_i = torch.empty(msa.msa_index_select_decode_workspace_bytes(w.B, w.nb, w.n_g),
                        dtype=torch.uint8, device=dev)
@@ -303,7 +310,7 @@ def time_decode(msa, w, fp8, steps, warmup):
     def step(ev=None):
         if ev:
             ev[0].record()
-        msa.msa_index_select_decode(qidx, kidx_p, pt, sl, w.Bk, w.k, block_ids=ids, workspace=ws_i)
+        index(qidx, kidx_p, pt, sl, w.Bk, w.k, block_ids=ids, workspace=ws_i)
         if ev:
             ev[1].record()
         msa.msa_decode(q, kp, vp, pt, sl, ids, w.Bk, w.scale, workspace=ws_d, out=out, lse=lse,
@@ -611,10 +618,11 @@ def main():
     peaks, peak_src = load_peaks()
     if args.only == "decode":
         wd = synth.make("decode", **({"B": args.batch} if args.batch else {}))
-        for fp8 in (False, True):
-            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, args.warmup)
+        for fp8, fp8_index in ((False, False), (True, False), (True, True)):
+            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, args.warmup, fp8_index)
             torch.cuda.empty_cache()
-            print(json.dumps({"only": "decode", "fp8": fp8, "index_ms": i_ms, "attention_ms": a_ms}))
+            print(json.dumps({"only": "decode", "fp8": fp8, "fp8_index": fp8_index,
+                              "index_ms": i_ms, "attention_ms": a_ms}))
         return
     if args.only == "index":
         w = synth.make(args.workload)
@@ -732,13 +740,13 @@ def main():
             "index_tflops": round(p_fli / (p_idx * 1e-3) / 1e12, 2),
             "tflops": round((p_fli + p_fla) / (p_ms * 1e-3) / 1e12, 2)}
         wd = synth.make("decode")
-        for fp8 in (False, True):
-            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, 1)
+        for fp8, fp8_index in ((False, False), (True, False), (True, True)):
+            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, 1, fp8_index)
             torch.cuda.empty_cache()
             kv_bytes = 2.0 * wd.B * wd.n_g * (wd.k - 1) * wd.Bk * wd.d * (1 if fp8 else 2) + \
                 2.0 * wd.B * wd.n_g * 1 * wd.d * (1 if fp8 else 2)
-            scan_bytes = 2.0 * wd.B * wd.L * wd.d_idx
-            key = "decode_fp8" if fp8 else "decode_bf16"
+            scan_bytes = (1.0 if fp8_index else 2.0) * wd.B * wd.L * wd.d_idx
+            key = "decode_fp8_index_and_kv" if fp8_index else ("decode_fp8" if fp8 else "decode_bf16")
             extra[key] = {
                 "tokens_per_s": wd.B / ((i_ms + a_ms) * 1e-3),
                 "attention_only_tokens_per_s": wd.B / (a_ms * 1e-3),

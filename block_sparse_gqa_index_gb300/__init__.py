@@ -65,6 +65,8 @@ _ws_attn_varlen = _sig("msa_sparse_attn_varlen_workspace_bytes", [_P, _I, _I, _I
                        _SZ)
 _attn_varlen = _sig("msa_sparse_attn_varlen", [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                                _P, _P, _P, _SZ, _P])
+_index_dec_fp8 = _sig("msa_index_select_decode_fp8", [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                                      _P, _P, _F, _P, _SZ, _P])
 _index_paged = _sig("msa_index_select_paged", [_P, _P, _I64, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                                                _P, _P])
 _ws_attn_paged = _sig("msa_sparse_attn_paged_workspace_bytes", [_P, _P, _I, _I, _I, _I, _I, _I,
@@ -81,7 +83,8 @@ EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes
            "msa_index_select_fp8", "msa_index_select_varlen",
            "msa_sparse_attn_varlen_workspace_bytes",
            "msa_sparse_attn_varlen", "msa_index_select_paged",
-           "msa_sparse_attn_paged_workspace_bytes", "msa_sparse_attn_paged"]
+           "msa_sparse_attn_paged_workspace_bytes", "msa_sparse_attn_paged",
+           "msa_index_select_decode_fp8"]
 
 
 class MSAError(RuntimeError):
@@ -418,6 +421,46 @@ def msa_index_select_decode(q_idx: torch.Tensor, k_idx_pages: torch.Tensor,
                       seq_lens.data_ptr(), B, max_pages, n_g, d_idx, Bk, k, block_ids.data_ptr(),
                       _ptr(block_scores), ws_ptr, ws_n, _stream(q_idx)),
            "msa_index_select_decode")
+    return block_ids
+
+
+def msa_index_select_decode_fp8(q_idx: torch.Tensor, k_idx_pages: torch.Tensor,
+                                page_table: torch.Tensor, seq_lens: torch.Tensor, Bk: int = 128,
+                                k: int = 16, block_ids: Optional[torch.Tensor] = None,
+                                block_scores: Optional[torch.Tensor] = None,
+                                score_scale: float = 1.0,
+                                workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Index branch of decode over an E4M3 k_idx cache: q_idx [B, n_groups, d_idx]
+    and k_idx_pages [P, Bk, d_idx] torch.float8_e4m3fn (or uint8 holding the
+    codes), page_table [B, max_pages] int32, seq_lens [B] int32 -> block_ids
+    [B, n_groups, k]; block_scores, when given, receive the pooled scores times
+    score_scale."""
+    B, n_g, d_idx = q_idx.shape
+    max_pages = page_table.shape[1]
+    for t, name in ((q_idx, "q_idx"), (k_idx_pages, "k_idx_pages")):
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise TypeError(f"{name} must hold E4M3 codes (float8_e4m3fn or uint8)")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k_idx_pages.dim() != 3 or tuple(k_idx_pages.shape[1:]) != (Bk, d_idx):
+        raise ValueError("k_idx_pages must be [P, Bk, d_idx]")
+    _req(page_table, "page_table", torch.int32, (B, max_pages))
+    _req(seq_lens, "seq_lens", torch.int32, (B,))
+    if block_ids is None:
+        block_ids = torch.empty((B, n_g, k), dtype=torch.int32, device=q_idx.device)
+    _req(block_ids, "block_ids", torch.int32, (B, n_g, k))
+    if block_scores is not None:
+        _req(block_scores, "block_scores", torch.float32, (B, n_g, max_pages))
+    elif workspace is None:
+        workspace = torch.empty(_ws_index_dec(B, max_pages, n_g), dtype=torch.uint8,
+                                device=q_idx.device)
+    ws_ptr, ws_n = (None, 0) if workspace is None else (_req(workspace, "workspace", torch.uint8),
+                                                         workspace.numel())
+    _check(_index_dec_fp8(q_idx.data_ptr(), k_idx_pages.data_ptr(), page_table.data_ptr(),
+                          seq_lens.data_ptr(), B, max_pages, n_g, d_idx, Bk, k,
+                          block_ids.data_ptr(), _ptr(block_scores), score_scale, ws_ptr, ws_n,
+                          _stream(q_idx)),
+           "msa_index_select_decode_fp8")
     return block_ids
 
 

@@ -387,11 +387,10 @@ size_t msa_index_select_decode_workspace_bytes(int B, int max_pages, int n_group
   return (size_t)B * max_pages * n_groups * sizeof(float);
 }
 
-int msa_index_select_decode(const void* q_idx, const void* k_idx_pages,
-                            const int32_t* page_table, const int32_t* seq_lens, int B,
-                            int max_pages, int n_groups, int d_idx, int Bk, int k,
-                            int32_t* block_ids, float* block_scores, void* workspace,
-                            size_t workspace_bytes, void* stream) {
+static int index_decode(const void* q_idx, const void* k_idx_pages, const int32_t* page_table,
+                        const int32_t* seq_lens, int B, int max_pages, int n_groups, int d_idx,
+                        int Bk, int k, int32_t* block_ids, float* block_scores, void* workspace,
+                        size_t workspace_bytes, void* stream, bool e4m3, float score_scale) {
   if (B < 0 || max_pages < 1 || n_groups < 1 || d_idx < 1 || Bk < 1 || k < 1)
     return MSA_ERR_INVALID_ARG;
   if (B == 0) return MSA_OK;
@@ -412,10 +411,31 @@ int msa_index_select_decode(const void* q_idx, const void* k_idx_pages,
   cudaStream_t st = (cudaStream_t)stream;
   msa::Diag dg = diag();
   cudaError_t e = msa::launch_decode_index(q_idx, k_idx_pages, page_table, seq_lens, B,
-                                           max_pages, n_groups, d_idx, scores, dg, st);
+                                           max_pages, n_groups, d_idx, scores, dg, st, e4m3,
+                                           score_scale);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
   e = msa::launch_topk(scores, B, n_groups, max_pages, Bk, k, 0, seq_lens, block_ids, dg, st);
   return status_of(e);
+}
+
+int msa_index_select_decode(const void* q_idx, const void* k_idx_pages,
+                            const int32_t* page_table, const int32_t* seq_lens, int B,
+                            int max_pages, int n_groups, int d_idx, int Bk, int k,
+                            int32_t* block_ids, float* block_scores, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  return index_decode(q_idx, k_idx_pages, page_table, seq_lens, B, max_pages, n_groups, d_idx,
+                      Bk, k, block_ids, block_scores, workspace, workspace_bytes, stream, false,
+                      1.f);
+}
+
+int msa_index_select_decode_fp8(const void* q_idx, const void* k_idx_pages,
+                                const int32_t* page_table, const int32_t* seq_lens, int B,
+                                int max_pages, int n_groups, int d_idx, int Bk, int k,
+                                int32_t* block_ids, float* block_scores, float score_scale,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  return index_decode(q_idx, k_idx_pages, page_table, seq_lens, B, max_pages, n_groups, d_idx,
+                      Bk, k, block_ids, block_scores, workspace, workspace_bytes, stream, true,
+                      score_scale);
 }
 
 size_t msa_decode_workspace_bytes(int B, int H_q, int d, int k) {

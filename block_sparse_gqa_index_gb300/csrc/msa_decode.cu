@@ -7,9 +7,10 @@
 //
 // decode_index_kernel: streams each sequence's shared index-key cache once and
 //   max-pools q_idx . k_idx per 128-key page for all groups at once. Keys are
-//   the M dimension of mma.m16n8k16 and the (up to 8) groups its N dimension;
-//   the d_idx reduction order is permuted identically in A and B so that each
-//   thread reads 16 contiguous bytes per key row. HBM-bound.
+//   the M dimension of mma.m16n8k16 (bf16) or mma.m16n8k32 (E4M3 codes, half
+//   the bytes) and the (up to 8) groups its N dimension; the d_idx reduction
+//   order is permuted identically in A and B so that each thread reads 16
+//   contiguous bytes per key row. HBM-bound.
 // Caches: K / V pages are head-major [P, H_kv, 128, d] (the page tensor's second
 // dimension is the kv-head count in the usage listing), so the block a group
 // reads is one contiguous run; k_idx pages are [P, 128, d_idx].
@@ -40,12 +41,27 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int DI>
+__device__ __forceinline__ void mma_e4m3_16832(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// F8: q_idx and the k_idx pages hold E4M3 codes; out_scale multiplies the
+// block scores written (a positive scale of all keys or of a query's row
+// ranks the blocks the same)
+template <int DI, bool F8>
 __global__ void __launch_bounds__(256)
-decode_index_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ kpages,
+decode_index_kernel(const unsigned char* __restrict__ q_idx,
+                    const unsigned char* __restrict__ kpages,
                     const int32_t* __restrict__ page_table, const int32_t* __restrict__ seq_lens,
-                    int B, int max_pages, int n_g, float* __restrict__ scores, Diag dg) {
-  constexpr int NC = DI / 32;  // 16-byte chunks per thread per key row
+                    int B, int max_pages, int n_g, float out_scale, float* __restrict__ scores,
+                    Diag dg) {
+  constexpr int RB = DI * (F8 ? 1 : 2);  // bytes of one key row
+  constexpr int NC = RB / 64;            // 16-byte chunks per thread per key row
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, t4 = lane & 3;
   const int64_t n_tasks = (int64_t)B * max_pages;
@@ -65,11 +81,11 @@ decode_index_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restri
     for (int i = 0; i < NC; ++i) {
       bq[i] = make_uint4(0, 0, 0, 0);
       if (gq < n_g)
-        bq[i] = *reinterpret_cast<const uint4*>(q_idx + ((size_t)s * n_g + gq) * DI +
-                                                8 * (t4 + 4 * i));
+        bq[i] = *reinterpret_cast<const uint4*>(q_idx + ((size_t)s * n_g + gq) * RB +
+                                                16 * (t4 + 4 * i));
     }
     const int64_t page = page_table[(size_t)s * max_pages + b];
-    const uint16_t* base = kpages + (size_t)page * kBk * DI;
+    const unsigned char* base = kpages + (size_t)page * kBk * RB;
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll 2
     for (int m = 0; m < kBk / 16; ++m) {
@@ -77,14 +93,19 @@ decode_index_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restri
       uint4 a0[NC], a1[NC];
 #pragma unroll
       for (int i = 0; i < NC; ++i) {
-        a0[i] = __ldg(reinterpret_cast<const uint4*>(base + (size_t)key0 * DI + 8 * (t4 + 4 * i)));
-        a1[i] = __ldg(reinterpret_cast<const uint4*>(base + (size_t)key1 * DI + 8 * (t4 + 4 * i)));
+        a0[i] = __ldg(reinterpret_cast<const uint4*>(base + (size_t)key0 * RB + 16 * (t4 + 4 * i)));
+        a1[i] = __ldg(reinterpret_cast<const uint4*>(base + (size_t)key1 * RB + 16 * (t4 + 4 * i)));
       }
       float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < NC; ++i) {
-        mma_bf16_16816(c, a0[i].x, a1[i].x, a0[i].y, a1[i].y, bq[i].x, bq[i].y);
-        mma_bf16_16816(c, a0[i].z, a1[i].z, a0[i].w, a1[i].w, bq[i].z, bq[i].w);
+        if constexpr (F8) {
+          mma_e4m3_16832(c, a0[i].x, a1[i].x, a0[i].y, a1[i].y, bq[i].x, bq[i].y);
+          mma_e4m3_16832(c, a0[i].z, a1[i].z, a0[i].w, a1[i].w, bq[i].z, bq[i].w);
+        } else {
+          mma_bf16_16816(c, a0[i].x, a1[i].x, a0[i].y, a1[i].y, bq[i].x, bq[i].y);
+          mma_bf16_16816(c, a0[i].z, a1[i].z, a0[i].w, a1[i].w, bq[i].z, bq[i].w);
+        }
       }
       if (key0 < nvalid) { mx0 = fmaxf(mx0, c[0]); mx1 = fmaxf(mx1, c[1]); }
       if (key1 < nvalid) { mx0 = fmaxf(mx0, c[2]); mx1 = fmaxf(mx1, c[3]); }
@@ -96,8 +117,8 @@ decode_index_kernel(const uint16_t* __restrict__ q_idx, const uint16_t* __restri
     }
     if (gq == 0) {
       int g0 = 2 * t4, g1 = 2 * t4 + 1;
-      if (g0 < n_g) scores[((size_t)s * n_g + g0) * max_pages + b] = mx0;
-      if (g1 < n_g) scores[((size_t)s * n_g + g1) * max_pages + b] = mx1;
+      if (g0 < n_g) scores[((size_t)s * n_g + g0) * max_pages + b] = F8 ? mx0 * out_scale : mx0;
+      if (g1 < n_g) scores[((size_t)s * n_g + g1) * max_pages + b] = F8 ? mx1 * out_scale : mx1;
     }
   }
 }
@@ -412,19 +433,24 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,
                                 const int32_t* page_table, const int32_t* seq_lens, int B,
                                 int max_pages, int n_g, int d_idx, float* scores,
-                                const Diag& dg, cudaStream_t st) {
+                                const Diag& dg, cudaStream_t st, bool e4m3, float score_scale) {
   int64_t warps = (int64_t)B * max_pages;
   if (warps == 0) return cudaSuccess;
   note_launches(1);
   unsigned grid = (unsigned)std::min<int64_t>((warps + 7) / 8, 152 * 16);
-  if (d_idx == 128)
-    decode_index_kernel<128><<<grid, 256, 0, st>>>((const uint16_t*)q_idx,
-                                                   (const uint16_t*)k_idx_pages, page_table,
-                                                   seq_lens, B, max_pages, n_g, scores, dg);
-  else
-    decode_index_kernel<64><<<grid, 256, 0, st>>>((const uint16_t*)q_idx,
-                                                  (const uint16_t*)k_idx_pages, page_table,
-                                                  seq_lens, B, max_pages, n_g, scores, dg);
+  auto q = (const unsigned char*)q_idx;
+  auto kp = (const unsigned char*)k_idx_pages;
+#define MSA_DEC_INDEX(DI, F8)                                                                 \
+  decode_index_kernel<DI, F8><<<grid, 256, 0, st>>>(q, kp, page_table, seq_lens, B, max_pages, \
+                                                    n_g, score_scale, scores, dg)
+  if (e4m3) {
+    if (d_idx == 128) MSA_DEC_INDEX(128, true);
+    else MSA_DEC_INDEX(64, true);
+  } else {
+    if (d_idx == 128) MSA_DEC_INDEX(128, false);
+    else MSA_DEC_INDEX(64, false);
+  }
+#undef MSA_DEC_INDEX
   return cudaGetLastError();
 }
 

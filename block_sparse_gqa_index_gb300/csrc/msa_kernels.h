@@ -106,10 +106,13 @@ cudaError_t launch_batch_info(const BatchSeqs& tb, const int32_t* page_table, in
                               int2* qinfo, int2* vinfo, cudaStream_t st);
 
 // Decode (msa_decode.cu).
+// e4m3: q_idx and the k_idx pages hold E4M3 codes, and the block scores are
+// written times score_scale
 cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,
                                 const int32_t* page_table, const int32_t* seq_lens, int B,
                                 int max_pages, int n_g, int d_idx, float* scores,
-                                const Diag& dg, cudaStream_t st);
+                                const Diag& dg, cudaStream_t st, bool e4m3 = false,
+                                float score_scale = 1.f);
 size_t decode_ws_bytes(int B, int H_q, int d, int k);
 cudaError_t launch_decode_attn(const void* q, const void* k_pages, const void* v_pages,
                                int kv_fp8, const float* k_scale, const float* v_scale,

@@ -82,8 +82,9 @@ int msa_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_grou
                      int d_idx, int Bk, int k, int32_t* block_ids, float* block_scores,
                      void* workspace, size_t workspace_bytes, void* stream);
 
-/* Index branch with FP8-E4M3 index operands (the pages' kernel release supports
- * FP8 among its precisions, [MSA-PT] "Kernel open source e MiniMax-M3"):
+/* Index branch with FP8-E4M3 index operands (the kernel release lists FP8 among
+ * its precisions: "MiniMax lança MSA ...", section "Kernel open source e
+ * MiniMax-M3"):
  *   q_idx   [N, n_groups, 128] E4M3 codes, k_idx [N, 128] E4M3 codes
  *   (d_idx must be 128: MSA_ERR_UNSUPPORTED otherwise).
  * The scores are the dot products of the decoded codes, exact per product and
@@ -240,6 +241,20 @@ int msa_index_select_decode(const void* q_idx, const void* k_idx_pages,
                             int max_pages, int n_groups, int d_idx, int Bk, int k,
                             int32_t* block_ids, float* block_scores, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/* Index branch of decode over an FP8-E4M3 k_idx cache: q_idx [B, n_groups,
+ * d_idx] and k_idx_pages [P, Bk, d_idx] hold E4M3 codes (half the bytes of the
+ * scan, which dominates a decode step). Scores are the dot products of the
+ * decoded codes, exact per product and accumulated in fp32 (mma.m16n8k32 on
+ * E4M3). A positive scale of all keys or of a query's row ranks the blocks
+ * the same, so the selection depends on the codes alone; score_scale only
+ * multiplies the optional block_scores. Everything else as
+ * msa_index_select_decode. */
+int msa_index_select_decode_fp8(const void* q_idx, const void* k_idx_pages,
+                                const int32_t* page_table, const int32_t* seq_lens, int B,
+                                int max_pages, int n_groups, int d_idx, int Bk, int k,
+                                int32_t* block_ids, float* block_scores, float score_scale,
+                                void* workspace, size_t workspace_bytes, void* stream);
 
 /* Workspace bytes of msa_decode (split-KV partials). */
 size_t msa_decode_workspace_bytes(int B, int H_q, int d, int k);

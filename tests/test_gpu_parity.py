@@ -505,6 +505,73 @@ def test_decode_ragged_lengths(msa, fp8):
     check_close("lse", lse.cpu().numpy(), l_ref, TOL_LSE * (10 if fp8 else 1))
 
 
+def _decode_index_fp8_inputs(w, lens):
+    """E4M3 codes of the last query rows and of the k_idx cache (host rounding),
+    the device cache placed by the seeded page table, and the decoded bf16 bits
+    for the oracle (identity pages)."""
+    dev = torch.device("cuda")
+    pt = torch.from_numpy(synth.page_table(w)).to(dev)
+    kh = synth.host_paged(w, synth.T_KIDX)[:, 0]                      # [B * nb, Bk, d_idx]
+    qh = np.stack([synth.host_rows(w, synth.T_QIDX, s, [int(lens[s]) - 1])[0]
+                   for s in range(w.B)])
+    k8, kb = _to_e4m3(kh)
+    q8, qb = _to_e4m3(qh)
+    k8_dev = torch.empty_like(k8, device=dev)
+    k8_dev[pt.flatten().long()] = k8.to(dev)                          # logical (s, b) -> page
+    return pt, q8.to(dev), k8_dev, qb, kb
+
+
+def test_decode_index_fp8_exact_on_integer_inputs(msa):
+    """An E4M3 k_idx cache on integer inputs (exact in E4M3): ids equal the
+    oracle's and the bf16 decode's bit for bit over ragged lengths; block scores
+    equal the bf16 ones times score_scale."""
+    w = synth.make("decode", B=6, L=1000, H_q=16, H_kv=8, d=128, d_idx=128, kind=synth.KIND_INT,
+                   k=4)
+    lens = np.array([1, 2, 128, 129, 640, 1000], dtype=np.int32)
+    dev = torch.device("cuda")
+    sl = torch.from_numpy(lens).to(dev)
+    pt, q8, k8, qb, kb = _decode_index_fp8_inputs(w, lens)
+    s8 = torch.full((w.B, w.n_g, w.nb), float("nan"), device=dev)
+    ids8 = msa.msa_index_select_decode_fp8(q8, k8, pt, sl, w.Bk, w.k, block_scores=s8,
+                                           score_scale=0.25)
+    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, 0].contiguous()
+    qidx = synth.device_rows(w, synth.T_QIDX, [(s, int(lens[s]) - 1) for s in range(w.B)])
+    s16 = torch.full((w.B, w.n_g, w.nb), float("nan"), device=dev)
+    ids16 = msa.msa_index_select_decode(qidx, kidx_p, pt, sl, w.Bk, w.k, block_scores=s16)
+    torch.cuda.synchronize()
+    ident = synth.page_table(w, permute=False)
+    want = oracle.decode_index_select(qb, kb, ident, lens, w.Bk, w.k)
+    assert np.array_equal(ids8.cpu().numpy(), want)
+    assert torch.equal(ids8, ids16)
+    for s in range(w.B):
+        nv = (int(lens[s]) - 1) // w.Bk + 1
+        assert torch.equal(s8[s, :, :nv], s16[s, :, :nv] * 0.25)
+
+
+@pytest.mark.parametrize("d_idx,H_kv", [(128, 8), (64, 2)])
+def test_decode_index_fp8_gauss(msa, d_idx, H_kv):
+    """Gaussian index inputs rounded to E4M3: the selection matches the oracle
+    on the decoded codes up to near-tie swaps, and the block scores match its
+    scores to fp32 accumulation."""
+    w = synth.make("decode", B=8, L=128 * 40 + 3, H_q=4 * H_kv, H_kv=H_kv, d=d_idx, d_idx=d_idx)
+    lens = np.full(w.B, w.L, dtype=np.int32)
+    dev = torch.device("cuda")
+    pt, q8, k8, qb, kb = _decode_index_fp8_inputs(w, lens)
+    sc = torch.full((w.B, w.n_g, w.nb), float("nan"), device=dev)
+    ids = msa.msa_index_select_decode_fp8(q8, k8, pt, torch.from_numpy(lens).to(dev), w.Bk, w.k,
+                                          block_scores=sc)
+    torch.cuda.synchronize()
+    ident = synth.page_table(w, permute=False)
+    want, want_s = oracle.decode_index_select(qb, kb, ident, lens, w.Bk, w.k, nb_out=w.nb,
+                                              want_scores=True)
+    got = ids.cpu().numpy()
+    swaps = compare_selection(got, want, want_s, np.full(w.B, w.L - 1), w.Bk)
+    assert swaps <= 0.01 * got.shape[0] * got.shape[1]
+    s = sc.cpu().numpy().astype(np.float64)
+    rel = np.abs(s - want_s) / np.maximum(1.0, np.abs(want_s))
+    assert rel.max() < 1e-4
+
+
 def test_decode_matches_prefill_row_on_gpu(msa):
     """Decoding the last token against the cache equals the last prefill row."""
     w = synth.make("decode", B=1, L=128 * 9 + 5, H_q=8, H_kv=2, d=128, d_idx=128,
