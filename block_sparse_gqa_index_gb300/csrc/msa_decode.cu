@@ -87,7 +87,7 @@ decode_index_kernel(const unsigned char* __restrict__ q_idx,
     const int64_t page = page_table[(size_t)s * max_pages + b];
     const unsigned char* base = kpages + (size_t)page * kBk * RB;
     float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll 2
+#pragma unroll (F8 ? 4 : 2)
     for (int m = 0; m < kBk / 16; ++m) {
       const int key0 = m * 16 + gq, key1 = key0 + 8;
       uint4 a0[NC], a1[NC];
@@ -437,7 +437,7 @@ cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,
   int64_t warps = (int64_t)B * max_pages;
   if (warps == 0) return cudaSuccess;
   note_launches(1);
-  unsigned grid = (unsigned)std::min<int64_t>((warps + 7) / 8, 152 * 16);
+  unsigned grid = (unsigned)std::min<int64_t>((warps + 7) / 8, 152 * 32);
   auto q = (const unsigned char*)q_idx;
   auto kp = (const unsigned char*)k_idx_pages;
 #define MSA_DEC_INDEX(DI, F8)                                                                 \
