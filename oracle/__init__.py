@@ -34,6 +34,8 @@ def lib():
         L.oracle_topk_blocks.argtypes = [P, P, I64, I32, I64, I32, I32, P]
         L.oracle_sparse_attn.argtypes = [P, P, I64, P, P, P, I32, I32, I32, I32, I32, D, P, P]
         L.oracle_dense_gqa.argtypes = [P, P, I64, P, P, I32, I32, I32, D, P, P]
+        L.oracle_kl_teacher.argtypes = [P, P, P, I64, P, P, P, I32, I32, I32, I32, I32, I32, D,
+                                        P, P]
         L.oracle_index_brute.argtypes = [P, P, I64, P, I32, I32, I32, I32, P]
         L.oracle_decode_index_select.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, I32, I64,
                                                  P, P]
@@ -86,6 +88,28 @@ def topk_blocks(S_rows, rows, Bk, k):
     ids = np.full((n, n_g, k), -2, dtype=np.int32)
     _ok(lib().oracle_topk_blocks(sp, rp, n, n_g, nb, Bk, k, ids.ctypes.data))
     return ids
+
+
+def kl_teacher(q_rows, qi_rows, rows, K, k_idx, ids, Bk, scale):
+    """KL(teacher || index distribution) per (row, group) over the selected
+    tokens: q_rows [n, H_q, d], qi_rows [n, n_g, d_idx], K [N, H_kv, d], k_idx
+    [N, d_idx] bf16 bits, ids [n, n_g, k]. Returns (kl, mag) fp64 [n, n_g], mag
+    the summed size of the terms (sum p_main (|log p_main| + |log p_idx|))."""
+    q, qp = _c(q_rows, np.uint16)
+    qi, qip = _c(qi_rows, np.uint16)
+    r, rp = _c(rows, np.int64)
+    K = np.ascontiguousarray(K, dtype=np.uint16)
+    kk = np.ascontiguousarray(k_idx, dtype=np.uint16)
+    ii, ip = _c(ids, np.int32)
+    n, H_q, d = q.shape
+    H_kv = K.shape[-2]
+    d_idx = qi.shape[-1]
+    k = ii.shape[-1]
+    kl = np.empty((n, H_kv), dtype=np.float64)
+    mag = np.empty((n, H_kv), dtype=np.float64)
+    _ok(lib().oracle_kl_teacher(qp, qip, rp, n, K.ctypes.data, kk.ctypes.data, ip, H_q, H_kv, d,
+                                d_idx, Bk, k, float(scale), kl.ctypes.data, mag.ctypes.data))
+    return kl, mag
 
 
 def sparse_attn(q_rows, rows, K, V, ids, Bk, scale):

@@ -265,6 +265,84 @@ int oracle_sparse_attn(const uint16_t* q_rows, const int64_t* rows, int64_t n_ro
   return 0;
 }
 
+// KL alignment signal of the index branch ([MSA-2B] "MSA 如何训练", how MSA is
+// trained; [MSA-PT] "Treinamento com KL Divergence"): the teacher is the main
+// branch's distribution over the selected tokens J of (t, g), averaged over
+// the group's G query heads,
+//   p_main(j) = (1/G) sum_h exp(scale q_h . k_j - lse_h),  lse_h = log sum_J exp(scale q_h . k_j);
+// the student is the index branch's distribution over the same tokens,
+//   p_idx(j) = exp(s_j - LSE),  s_j = q_idx[t,g] . k_idx[j] (raw, as in a1),
+//   LSE = log sum_J exp(s_j);
+// and the signal is KL(p_main || p_idx) = sum_J p_main (log p_main - log p_idx),
+// a term with p_main = 0 counting 0.
+//   q_rows [n_rows, H_q, d], qi_rows [n_rows, n_g, d_idx], K [N, H_kv, d],
+//   k_idx [N, d_idx] (bf16 bits), ids [n_rows, n_g, k]
+//   kl_out [n_rows, n_g]; mag_out [n_rows, n_g] or null:
+//   sum_J p_main (|log p_main| + |log p_idx|), the size of the terms that cancel
+int oracle_kl_teacher(const uint16_t* q_rows, const uint16_t* qi_rows, const int64_t* rows,
+                      int64_t n_rows, const uint16_t* K, const uint16_t* k_idx,
+                      const int32_t* ids, int H_q, int H_kv, int d, int d_idx, int Bk, int k,
+                      double scale, double* kl_out, double* mag_out) {
+  if (H_kv < 1 || H_q % H_kv != 0 || Bk < 1 || k < 1) return -1;
+  const int G = H_q / H_kv;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n_rows * H_kv; ++r) {
+    const int64_t i = r / H_kv, t = rows[i];
+    const int g = (int)(r % H_kv);
+    const int32_t* sel = ids + (size_t)r * k;
+    std::vector<int64_t> J;
+    for (int u = 0; u < k; ++u) {
+      if (sel[u] < 0) continue;
+      for (int64_t j = (int64_t)sel[u] * Bk; j < ((int64_t)sel[u] + 1) * Bk && j <= t; ++j)
+        J.push_back(j);
+    }
+    std::sort(J.begin(), J.end());
+    J.erase(std::unique(J.begin(), J.end()), J.end());
+    const size_t n = J.size();
+    // teacher: the group's heads, each normalised over J, then averaged
+    std::vector<double> pm(n, 0.0), x(n), q((size_t)d);
+    for (int h = g * G; h < (g + 1) * G; ++h) {
+      decode_row(q_rows + ((size_t)i * H_q + h) * d, d, q.data());
+      double m = NEG_INF;
+      for (size_t u = 0; u < n; ++u) {
+        const uint16_t* kj = K + ((size_t)J[u] * H_kv + g) * d;
+        double s = 0.0;
+        for (int c = 0; c < d; ++c) s += q[(size_t)c] * bf16_to_double(kj[c]);
+        x[u] = s * scale;
+        m = std::max(m, x[u]);
+      }
+      double l = 0.0;
+      for (size_t u = 0; u < n; ++u) l += std::exp(x[u] - m);
+      const double lse = m + std::log(l);
+      for (size_t u = 0; u < n; ++u) pm[u] += std::exp(x[u] - lse) / G;
+    }
+    // student: softmax of the raw index scores over J
+    std::vector<double> qi((size_t)d_idx), sidx(n);
+    decode_row(qi_rows + (size_t)r * d_idx, d_idx, qi.data());
+    double ms = NEG_INF;
+    for (size_t u = 0; u < n; ++u) {
+      const uint16_t* kj = k_idx + (size_t)J[u] * d_idx;
+      double s = 0.0;
+      for (int c = 0; c < d_idx; ++c) s += qi[(size_t)c] * bf16_to_double(kj[c]);
+      sidx[u] = s;
+      ms = std::max(ms, s);
+    }
+    double ls = 0.0;
+    for (size_t u = 0; u < n; ++u) ls += std::exp(sidx[u] - ms);
+    const double LSE = ms + std::log(ls);
+    double kl = 0.0, mag = 0.0;
+    for (size_t u = 0; u < n; ++u) {
+      if (pm[u] <= 0.0) continue;
+      const double lp = std::log(pm[u]), lq = sidx[u] - LSE;
+      kl += pm[u] * (lp - lq);
+      mag += pm[u] * (std::fabs(lp) + std::fabs(lq));
+    }
+    kl_out[r] = kl;
+    if (mag_out) mag_out[r] = mag;
+  }
+  return 0;
+}
+
 // Textbook dense causal GQA attention (every j <= t), used to pin a4.
 int oracle_dense_gqa(const uint16_t* q_rows, const int64_t* rows, int64_t n_rows,
                      const uint16_t* K, const uint16_t* V, int H_q, int H_kv, int d,

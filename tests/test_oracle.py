@@ -394,3 +394,95 @@ def test_decode_fp8_path_equals_bf16_on_exact_values():
     o3, l3 = oracle.decode_attn(q, k8, v8, pt, sl, ids, Bk, 0.25, fp8=True,
                                 k_scale=np.ones(H_kv), v_scale=np.full(H_kv, 2.0))
     assert np.array_equal(o3, 2 * o1) and np.array_equal(l3, l1)
+
+
+# ----------------------------------------------------- KL alignment signal
+def _sig(x):
+    return 1.0 / (1.0 + math.exp(-x))
+
+
+def test_kl_two_tokens_bernoulli_closed_form():
+    """t = 1 sees tokens {0, 1}: the teacher and the student are Bernoulli
+    distributions, so the KL is the textbook two-point form. Two heads with
+    different attention check the group average; the two directions of KL
+    differ here, so a swapped KL fails."""
+    q = bf16_bits([[[2, 0], [0, 1]]])             # [1 row, H_q = 2, d = 2]
+    K = bf16_bits([[[1, 0]], [[0, 1]]])           # [2 tokens, H_kv = 1, d = 2]
+    qi = bf16_bits([[[1, 3]]])                    # [1 row, n_g = 1, d_idx = 2]
+    ki = bf16_bits([[1, 1], [0, 2]])              # [2 tokens, d_idx = 2]
+    ids = np.array([[[0, -1]]], dtype=np.int32)
+    kl, mag = oracle.kl_teacher(q, qi, np.array([1]), K, ki, ids, 128, 1.0)
+    a = (_sig(2.0) + _sig(-1.0)) / 2.0            # teacher mass on token 0
+    b = _sig(4.0 - 6.0)                           # student mass on token 0
+    want = a * math.log(a / b) + (1 - a) * math.log((1 - a) / (1 - b))
+    assert abs(kl[0, 0] - want) < 1e-12
+    assert abs(want - (b * math.log(b / a) + (1 - b) * math.log((1 - b) / (1 - a)))) > 1e-3
+    assert mag[0, 0] >= kl[0, 0]
+
+
+def test_kl_zero_when_index_scores_equal_scaled_attention_logits():
+    """G = 1 with q_idx = scale * q and k_idx = k: the student equals the
+    teacher on every row and every selection, so the KL is 0. Fails if the
+    teacher drops the scale or the student scales its raw scores."""
+    rng = np.random.default_rng(3)
+    N, d, Bk, k = 300, 64, 16, 4
+    qf = rng.integers(-4, 5, size=(N, 1, d)).astype(np.float32)
+    kf = rng.integers(-4, 5, size=(N, 1, d)).astype(np.float32)
+    q, K = bf16_bits(qf), bf16_bits(kf)
+    qi, ki = bf16_bits(qf / 8.0), bf16_bits(kf[:, 0])
+    rows = np.arange(N)
+    ids = oracle.index_select(qi, rows, ki, Bk, k)
+    kl, _ = oracle.kl_teacher(q, qi, rows, K, ki, ids, Bk, 1.0 / 8.0)
+    assert np.abs(kl).max() < 1e-9
+
+
+def test_kl_nonnegative_and_group_of_equal_heads():
+    """Gibbs' inequality on Gaussian inputs, and a group of G equal heads
+    gives the KL of one head (the group average of equal distributions)."""
+    rng = np.random.default_rng(4)
+    N, d, Bk, k = 200, 32, 8, 5
+    q1 = rand_bf16(rng, (N, 2, d))
+    K = rand_bf16(rng, (N, 2, d))
+    qi = rand_bf16(rng, (N, 2, d))
+    ki = rand_bf16(rng, (N, d))
+    rows = np.arange(N)
+    ids = oracle.index_select(qi, rows, ki, Bk, k)
+    kl1, _ = oracle.kl_teacher(q1, qi, rows, K, ki, ids, Bk, 0.2)
+    assert kl1.min() > -1e-12
+    assert kl1.max() > 1e-3
+    q3 = np.repeat(q1, 3, axis=1)                 # heads 0,0,0 | 1,1,1: G = 3
+    kl3, _ = oracle.kl_teacher(q3, qi, rows, K, ki, ids, Bk, 0.2)
+    assert np.allclose(kl3, kl1, rtol=1e-12, atol=1e-12)
+
+
+def test_kl_matches_brute_force_on_tiny_inputs():
+    """An independently written per-token loop on tiny shapes with a real
+    selection (k below the visible blocks): every selected block's tokens up
+    to t, each head's softmax, the group mean, the index softmax."""
+    rng = np.random.default_rng(5)
+    N, H_q, H_kv, d, Bk, k = 40, 4, 2, 8, 4, 3
+    q = rand_bf16(rng, (N, H_q, d))
+    K = rand_bf16(rng, (N, H_kv, d))
+    qi = rand_bf16(rng, (N, H_kv, d))
+    ki = rand_bf16(rng, (N, d))
+    rows = np.arange(N)
+    ids = oracle.index_select(qi, rows, ki, Bk, k)
+    kl, _ = oracle.kl_teacher(q, qi, rows, K, ki, ids, Bk, 0.3)
+    qf, Kf, qif, kif = bits_to_f64(q), bits_to_f64(K), bits_to_f64(qi), bits_to_f64(ki)
+    G = H_q // H_kv
+    for t in range(N):
+        for g in range(H_kv):
+            toks = [j for j in range(t + 1) if j // Bk in set(int(b) for b in ids[t, g] if b >= 0)]
+            teacher = [0.0] * len(toks)
+            for h in range(g * G, (g + 1) * G):
+                logits = [0.3 * sum(qf[t, h, c] * Kf[j, g, c] for c in range(d)) for j in toks]
+                top = max(logits)
+                z = sum(math.exp(x - top) for x in logits)
+                for u, x in enumerate(logits):
+                    teacher[u] += math.exp(x - top) / z / G
+            sc = [sum(qif[t, g, c] * kif[j, c] for c in range(d)) for j in toks]
+            top = max(sc)
+            z = sum(math.exp(x - top) for x in sc)
+            student = [math.exp(x - top) / z for x in sc]
+            want = sum(p * math.log(p / s) for p, s in zip(teacher, student) if p > 0)
+            assert abs(kl[t, g] - want) < 1e-10 * max(1.0, abs(want)), (t, g)
