@@ -65,6 +65,9 @@ _ws_attn_varlen = _sig("msa_sparse_attn_varlen_workspace_bytes", [_P, _I, _I, _I
                        _SZ)
 _attn_varlen = _sig("msa_sparse_attn_varlen", [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                                _P, _P, _P, _SZ, _P])
+_ws_kl = _sig("msa_kl_teacher_workspace_bytes", [_I64, _I64, _I, _I, _I, _I, _I], _SZ)
+_kl = _sig("msa_kl_teacher", [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                              _SZ, _P])
 _index_dec_fp8 = _sig("msa_index_select_decode_fp8", [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                       _P, _P, _F, _P, _SZ, _P])
 _index_paged = _sig("msa_index_select_paged", [_P, _P, _I64, _P, _I, _P, _P, _I, _I, _I, _I, _I,
@@ -84,7 +87,8 @@ EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes
            "msa_sparse_attn_varlen_workspace_bytes",
            "msa_sparse_attn_varlen", "msa_index_select_paged",
            "msa_sparse_attn_paged_workspace_bytes", "msa_sparse_attn_paged",
-           "msa_index_select_decode_fp8"]
+           "msa_index_select_decode_fp8", "msa_kl_teacher_workspace_bytes",
+           "msa_kl_teacher"]
 
 
 class MSAError(RuntimeError):
@@ -301,6 +305,41 @@ def msa_sparse_attn_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                         out.data_ptr(), _ptr(lse), workspace.data_ptr(), workspace.numel(),
                         _stream(q)), "msa_sparse_attn_varlen")
     return out, lse
+
+
+def msa_kl_teacher(q: torch.Tensor, k: torch.Tensor, q_idx: torch.Tensor, k_idx: torch.Tensor,
+                   block_ids: torch.Tensor, lse: torch.Tensor, Bk: int = 128,
+                   scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
+                   out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """KL alignment signal of the index branch: q [N, H_q, d], k [N, H_kv, d],
+    q_idx [N, H_kv, d_idx], k_idx [N, d_idx] bf16, block_ids [N, H_kv, topk],
+    lse [N, H_q] fp32 (the main branch's, on the same ids) -> kl [N, H_kv] fp32,
+    KL(group-averaged main-branch distribution || index softmax) over each
+    row's selected tokens."""
+    N, H_q, d = q.shape
+    H_kv = k.shape[1]
+    d_idx = q_idx.shape[2]
+    topk = block_ids.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _req(q, "q", torch.bfloat16)
+    _req(k, "k", torch.bfloat16, (N, H_kv, d))
+    _req(q_idx, "q_idx", torch.bfloat16, (N, H_kv, d_idx))
+    _req(k_idx, "k_idx", torch.bfloat16, (N, d_idx))
+    _req(block_ids, "block_ids", torch.int32, (N, H_kv, topk))
+    _req(lse, "lse", torch.float32, (N, H_q))
+    if workspace is None:
+        workspace = torch.empty(max(1, _ws_kl(N, N, H_q, H_kv, d, Bk, topk)), dtype=torch.uint8,
+                                device=q.device)
+    _req(workspace, "workspace", torch.uint8)
+    if out is None:
+        out = torch.empty((N, H_kv), dtype=torch.float32, device=q.device)
+    _req(out, "out", torch.float32, (N, H_kv))
+    _check(_kl(q.data_ptr(), k.data_ptr(), q_idx.data_ptr(), k_idx.data_ptr(),
+               block_ids.data_ptr(), lse.data_ptr(), N, H_q, H_kv, d, d_idx, Bk, topk, scale,
+               out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(q)),
+           "msa_kl_teacher")
+    return out
 
 
 # ------------------------------------------------------------ paged prefill

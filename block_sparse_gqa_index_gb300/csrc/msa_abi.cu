@@ -173,6 +173,50 @@ int msa_sparse_attn(const void* q, const void* k, const void* v, const int32_t* 
   return MSA_OK;
 }
 
+// ------------------------------------------------------- KL alignment signal
+size_t msa_kl_teacher_workspace_bytes(int64_t chunk_rows, int64_t N, int H_q, int H_kv, int d,
+                                      int Bk, int k) {
+  return msa_sparse_attn_workspace_bytes(chunk_rows, N, H_q, H_kv, d, Bk, k);
+}
+
+int msa_kl_teacher(const void* q, const void* k, const void* q_idx, const void* k_idx,
+                   const int32_t* block_ids, const float* lse, int64_t N, int H_q, int H_kv,
+                   int d, int d_idx, int Bk, int topk, float scale, float* kl, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  if (N < 0 || H_q < 1 || H_kv < 1 || d < 1 || d_idx < 1 || Bk < 1 || topk < 1)
+    return MSA_ERR_INVALID_ARG;
+  if (N == 0) return MSA_OK;
+  if (!q || !k || !q_idx || !k_idx || !block_ids || !lse || !kl || !workspace)
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(q_idx) || !aligned16(k_idx) ||
+      !aligned16(block_ids) || !aligned16(lse) || !aligned16(kl) || !aligned16(workspace))
+    return MSA_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return MSA_ERR_INVALID_ARG;
+  const int G = H_q / H_kv;
+  if (Bk != 128 || !supported_k(topk) || !supported_d(d) || !supported_d(d_idx) ||
+      (G != 1 && G != 2 && G != 4 && G != 8))
+    return MSA_ERR_UNSUPPORTED;
+  if (N >= (1ll << 27) || N * H_q * topk >= (1ll << 31)) return MSA_ERR_UNSUPPORTED;
+  const int64_t nb = ceil_div(N, Bk);
+  int64_t lo = 0, hi = N;  // largest chunk of query rows whose workspace fits
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) / 2;
+    if (msa::attn_ws_bytes(mid, nb, H_q, H_kv, d, topk) <= workspace_bytes) lo = mid;
+    else hi = mid - 1;
+  }
+  if (lo < 1) return MSA_ERR_WORKSPACE;
+  const int64_t chunk = lo;
+  msa::AttnWs ws = msa::attn_ws_carve(workspace, chunk, nb, H_q, H_kv, d, topk);
+  const msa::Diag dg = diag();
+  for (int64_t q0 = 0; q0 < N; q0 += chunk) {
+    const int64_t q1 = std::min(N, q0 + chunk);
+    if (msa::launch_kl_chunk(q, k, q_idx, k_idx, block_ids, lse, N, q0, q1, H_q, H_kv, d, d_idx,
+                             topk, scale, kl, ws, nb, dg, (cudaStream_t)stream) != cudaSuccess)
+      return MSA_ERR_CUDA;
+  }
+  return MSA_OK;
+}
+
 // --------------------------------------------------------------- varlen prefill
 // cu_seqlens: host int64 [B + 1], 0 = cu[0] <= cu[1] <= ... <= cu[B]
 static bool cu_ok(const int64_t* cu, int B) {

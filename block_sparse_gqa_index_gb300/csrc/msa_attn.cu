@@ -1101,17 +1101,15 @@ AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int
   return w;
 }
 
-cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* v,
-                                     const int32_t* ids, int64_t N, int64_t q0, int64_t q1,
-                                     int H_q, int H_kv, int d, int k, float scale, void* out,
-                                     float* lse, const AttnWs& ws, int64_t nb, const Diag& dg,
-                                     cudaStream_t st, const AttnBatch& bt) {
+cudaError_t launch_bucketing(const int32_t* ids, int64_t q0, int64_t q1, int H_q, int H_kv,
+                             int k, const AttnWs& ws, int64_t nb, const Diag& dg, cudaStream_t st,
+                             const AttnBatch& bt) {
   const int64_t n_b = (int64_t)H_kv * nb;
   const int32_t* tbase = bt.paged ? ws.tbase : nullptr;
   if (bt.paged && !tbase) return cudaErrorInvalidValue;
   const int G = H_q / H_kv;
   const int qt = kTileRows / G;
-  note_launches(n_b <= kSmemBucketsMax ? 8 : 7);  // memset, count, scan, (base,) fill, map, tile, merge
+  note_launches(n_b <= kSmemBucketsMax ? 6 : 5);  // memset, count, scan, (base,) fill, map
   cudaError_t e = cudaMemsetAsync(ws.counts, 0, (size_t)n_b * 4, st);
   if (e != cudaSuccess) return e;
   int64_t n = (q1 - q0) * H_kv * k;
@@ -1137,6 +1135,20 @@ cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* 
   const int64_t tiles_max = max_tiles(q1 - q0, n_b, H_q, H_kv, k);
   tile_map_kernel<<<(unsigned)std::min<int64_t>((tiles_max + 255) / 256, 152 * 16), 256, 0, st>>>(
       ws.tile_off, ws.offsets, n_b, nb, qt, bt.vinfo, const_cast<int32_t*>(tbase), ws.tinfo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* v,
+                                     const int32_t* ids, int64_t N, int64_t q0, int64_t q1,
+                                     int H_q, int H_kv, int d, int k, float scale, void* out,
+                                     float* lse, const AttnWs& ws, int64_t nb, const Diag& dg,
+                                     cudaStream_t st, const AttnBatch& bt) {
+  const int64_t n_b = (int64_t)H_kv * nb;
+  const int32_t* tbase = bt.paged ? ws.tbase : nullptr;
+  const int G = H_q / H_kv;
+  cudaError_t e = launch_bucketing(ids, q0, q1, H_q, H_kv, k, ws, nb, dg, st, bt);
+  if (e != cudaSuccess) return e;
+  note_launches(2);  // tile, merge
   const float scale_log2 = scale * 1.4426950408889634f;
   const int64_t kv_rows = bt.kv_rows > 0 ? bt.kv_rows : N;
   e = d == 128 ? launch_tiles<128>(q, kk, v, N, kv_rows, q0, H_q, H_kv, k, scale_log2, nb, ws,

@@ -81,11 +81,28 @@ struct AttnBatch {
   int64_t kv_rows = 0;  // rows of the K / V tensors (0: as many as query rows)
   bool paged = false;
 };
+// Bucketing of query rows q0 .. q1 - 1 by (group, block): fills ws.counts ..
+// ws.tinfo (and ws.tbase when paged) and ws.rec_of, the tile layout the tile
+// kernels below read. A tile is one bucket's block against up to 128 / G of
+// its queries; query i of tile T owns partial record T * (128 / G) + i.
+cudaError_t launch_bucketing(const int32_t* ids, int64_t q0, int64_t q1, int H_q, int H_kv,
+                             int k, const AttnWs& ws, int64_t nb, const Diag& dg, cudaStream_t st,
+                             const AttnBatch& bt = AttnBatch());
 cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* v,
                                      const int32_t* ids, int64_t N, int64_t q0, int64_t q1,
                                      int H_q, int H_kv, int d, int k, float scale, void* out,
                                      float* lse, const AttnWs& ws, int64_t nb, const Diag& dg,
                                      cudaStream_t st, const AttnBatch& bt = AttnBatch());
+
+// KL alignment signal (msa_kl.cu) for query rows q0 .. q1 - 1 of one
+// sequence: bucketing as for the main branch, the KL tiles into ws.part (32
+// bytes per record), the merge into kl[t * H_kv + g]. G = H_q / H_kv in
+// {1, 2, 4, 8}.
+cudaError_t launch_kl_chunk(const void* q, const void* kk, const void* q_idx, const void* k_idx,
+                            const int32_t* ids, const float* lse, int64_t N, int64_t q0,
+                            int64_t q1, int H_q, int H_kv, int d, int d_idx, int k, float scale,
+                            float* kl, const AttnWs& ws, int64_t nb, const Diag& dg,
+                            cudaStream_t st);
 
 // Sequences of a batch for the main branch's geometry, at most kBatchSeqs
 // per launch of launch_batch_info.

@@ -132,6 +132,30 @@ int msa_sparse_attn(const void* q, const void* k, const void* v, const int32_t* 
                     void* out, float* lse, void* workspace, size_t workspace_bytes,
                     void* stream);
 
+/* KL alignment signal of the index branch, forward only ("MiniMax Sparse
+ * Attention (MSA) ...", section "MSA 如何训练"; "MiniMax lança MSA ...", section
+ * "Treinamento com KL Divergence"): per (t, g), over the causally visible
+ * tokens J of the group's selected blocks, the teacher is the main branch's
+ * distribution averaged over the group's query heads,
+ *   p_main(j) = (1/G) sum_h exp(scale q_h . k_j - lse_h),
+ * and the student is the softmax of the raw index scores over the same tokens,
+ *   p_idx(j) = exp(s_j) / sum_J exp(s_j),  s_j = q_idx[t, g] . k_idx[j].
+ *   kl[t, g] = sum_J p_main(j) (log p_main(j) - log p_idx(j))   fp32 out [N, H_kv]
+ *   lse          [N, H_q] fp32: the main branch's LSE on the same block ids
+ *                (msa_sparse_attn)
+ *   q, k, q_idx, k_idx, block_ids as in msa_sparse_attn / msa_index_select;
+ *   d and d_idx in {64, 128}, G = H_q / H_kv in {1, 2, 4, 8}, else
+ *   MSA_ERR_UNSUPPORTED.
+ *   workspace    at least msa_kl_teacher_workspace_bytes(c, ...) for some c >= 1
+ *                (the main branch's bucketing; the call takes the largest chunk
+ *                of query rows that fits). */
+size_t msa_kl_teacher_workspace_bytes(int64_t chunk_rows, int64_t N, int H_q, int H_kv, int d,
+                                      int Bk, int k);
+int msa_kl_teacher(const void* q, const void* k, const void* q_idx, const void* k_idx,
+                   const int32_t* block_ids, const float* lse, int64_t N, int H_q, int H_kv,
+                   int d, int d_idx, int Bk, int topk, float scale, float* kl, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
 /* Varlen batched prefill: B sequences packed back to back, the serving form of
  * the two prefill entry points above (the usage listing of the MSA page,
  * "运行 Kernel", plans each call from per-sequence query and key lengths).

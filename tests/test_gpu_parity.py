@@ -728,3 +728,49 @@ def test_paged_whole_sequences_equal_varlen(msa):
     assert torch.equal(ids, ids_v)
     assert torch.equal(out, out_v)
     assert torch.equal(lse, lse_v)
+
+
+# ------------------------------------------------------- KL alignment signal
+@pytest.mark.parametrize("N,H_q,H_kv,d", [(2000, 8, 2, 64), (1500, 16, 2, 128), (700, 2, 2, 64),
+                                          (900, 4, 2, 128)])
+def test_kl_teacher_matches_oracle(msa, N, H_q, H_kv, d):
+    """The KL signal on the GPU's own ids and LSE against the oracle's fp64 KL
+    on the same ids, for G = 4, 8, 1, 2 over several tiles and a ragged last
+    block. The bound scales with the size of the terms that cancel."""
+    w = synth.make("tiny", L=N, H_q=H_q, H_kv=H_kv, d=d, d_idx=d, seed=800 + H_q)
+    qi = synth.device_tensor(w, synth.T_QIDX)
+    ki = kidx2d(synth.device_tensor(w, synth.T_KIDX))
+    q = synth.device_tensor(w, synth.T_Q)
+    kk = synth.device_tensor(w, synth.T_K)
+    v = synth.device_tensor(w, synth.T_V)
+    ids = msa.msa_index_select(qi, ki, w.Bk, w.k)
+    _, lse = msa.msa_sparse_attn(q, kk, v, ids, w.Bk, w.scale)
+    kl = msa.msa_kl_teacher(q, kk, qi, ki, ids, lse, w.Bk, w.scale)
+    torch.cuda.synchronize()
+    rows = np.arange(N)
+    want, mag = oracle.kl_teacher(synth.host_tensor(w, synth.T_Q)[0],
+                                  synth.host_tensor(w, synth.T_QIDX)[0], rows,
+                                  synth.host_tensor(w, synth.T_K)[0],
+                                  synth.host_tensor(w, synth.T_KIDX)[0, :, 0], ids.cpu().numpy(),
+                                  w.Bk, w.scale)
+    got = kl.cpu().numpy().astype(np.float64)
+    err = np.abs(got - want) / (1.0 + mag)
+    assert err.max() < 1e-4, (err.max(), np.unravel_index(err.argmax(), err.shape))
+
+
+def test_kl_teacher_zero_when_student_equals_teacher(msa):
+    """One group of one head with q_idx = q / 8 and k_idx = k (scale 1/8): the
+    index softmax equals the main branch's distribution, so the KL vanishes up
+    to fp32 rounding."""
+    N, d = 1200, 64
+    w = synth.make("tiny", L=N, H_q=1, H_kv=1, d=d, d_idx=d, seed=900)
+    q = synth.device_tensor(w, synth.T_Q)
+    kk = synth.device_tensor(w, synth.T_K)
+    v = synth.device_tensor(w, synth.T_V)
+    qi = (q.float() / 8.0).to(torch.bfloat16)
+    ki = kk[:, 0].contiguous()
+    ids = msa.msa_index_select(qi, ki, 128, 4)
+    _, lse = msa.msa_sparse_attn(q, kk, v, ids, 128, 0.125)
+    kl = msa.msa_kl_teacher(q, kk, qi, ki, ids, lse, 128, 0.125)
+    torch.cuda.synchronize()
+    assert kl.abs().max().item() < 1e-4
