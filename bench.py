@@ -17,7 +17,8 @@ Prints ONE JSON line. `value` is prefill tokens/s (all ranks). Further keys:
                the 128K tokens as 8 packed 16K sequences (varlen entry points),
                a chunked prefill of the last 16K of the 128K tokens over paged
                caches with a shuffled page table,
-               the 128K step with the index branch on FP8-E4M3 codes,
+               the 128K step with the index branch on FP8-E4M3 codes, the KL
+               alignment signal of the index branch at 128K,
                decode steps with bf16 KV, FP8-E4M3 KV, and FP8-E4M3 KV plus an
                FP8-E4M3 k_idx cache, standalone top-16 (with
                torch.topk over the same scores as a comparator)
@@ -478,6 +479,43 @@ def time_paged_chunk(msa, w, nq, steps, warmup):
     return res[0], res[1], fl_i, fl_a
 
 
+def time_kl_teacher(msa, w, steps, warmup):
+    """KL alignment signal of the index branch over the whole workload, on the
+    index branch's ids and the main branch's LSE (computed once, untimed)."""
+    import torch
+    import synth
+    qidx = synth.device_tensor(w, synth.T_QIDX)
+    kidx = synth.device_tensor(w, synth.T_KIDX)[:, 0].contiguous()
+    q = synth.device_tensor(w, synth.T_Q)
+    k = synth.device_tensor(w, synth.T_K)
+    v = synth.device_tensor(w, synth.T_V)
+    ids = msa.msa_index_select(qidx, kidx, w.Bk, w.k)
+    _, lse = msa.msa_sparse_attn(q, k, v, ids, w.Bk, w.scale)
+    del v
+    ws = torch.empty(msa._ws_kl(w.N, w.N, w.H_q, w.H_kv, w.d, w.Bk, w.k), dtype=torch.uint8,
+                     device="cuda")
+    kl = torch.empty((w.N, w.H_kv), dtype=torch.float32, device="cuda")
+
+    def step():
+        msa.msa_kl_teacher(q, k, qidx, kidx, ids, lse, w.Bk, w.scale, workspace=ws, out=kl)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    # teacher logits (2 d per head and selected key) plus index scores (2 d_idx per group and key)
+    t = np.arange(w.N, dtype=np.int64)
+    sel = float(np.where(t // w.Bk + 1 <= w.k, t + 1, (w.k - 1) * w.Bk + t % w.Bk + 1).sum())
+    flops = 2.0 * sel * (w.d * w.H_q + w.d_idx * w.H_kv)
+    return ms, flops
+
+
 def time_prefill_fp8_index(msa, w, steps, warmup):
     """Prefill step with the index branch on FP8-E4M3 codes of q_idx / k_idx
     (rounded to nearest by torch before the timing) and the bf16 main branch."""
@@ -727,6 +765,10 @@ def main():
             "index_tflops": round(fl_idx / (f_idx * 1e-3) / 1e12, 2),
             "index_frac_of_fp8_peak": round(fl_idx / (f_idx * 1e-3) / 1e12 / peak_f8, 4),
             "fp8_peak": peak_f8, "fp8_peak_source": "measured bf16 sustained x 2 (nominal ratio)"}
+        kl_ms, kl_fl = time_kl_teacher(msa, w, args.steps, 3)
+        torch.cuda.empty_cache()
+        extra["kl_teacher_128k"] = {"ms": round(kl_ms, 3),
+                                    "tflops": round(kl_fl / (kl_ms * 1e-3) / 1e12, 2)}
         v_ms, v_fl, v_idx = time_varlen(msa, w, 8, args.steps, 3)
         torch.cuda.empty_cache()
         extra["prefill_varlen_8x16k"] = {"tokens_per_s": w.N / (v_ms * 1e-3), "ms": round(v_ms, 3),
