@@ -20,7 +20,7 @@ Prints ONE JSON line. `value` is prefill tokens/s (all ranks). Further keys:
                the 128K step with the index branch on FP8-E4M3 codes, the KL
                alignment signal of the index branch at 128K,
                decode steps with bf16 KV, FP8-E4M3 KV, and FP8-E4M3 KV plus an
-               FP8-E4M3 k_idx cache, standalone top-16 (with
+               FP8-E4M3 or NVFP4 k_idx cache, standalone top-16 (with
                torch.topk over the same scores as a comparator)
 
 Multi-GPU: each rank runs its own independent sequence (no collective on the
@@ -276,10 +276,26 @@ def e2e_prefill(msa, P, steps, warmup):
     return ms, h2d, d2h
 
 
-def time_decode(msa, w, fp8, steps, warmup, fp8_index=False):
+def nvfp4_quantise(x):
+    """[..., d] tensor -> (E2M1 codes two per byte, even dimension low; E4M3
+    scale per 16 dimensions = amax / 6; codes = nearest E2M1 value of x /
+    scale). Input preparation with torch ops, outside any timing."""
+    import torch
+    xb = x.float().reshape(*x.shape[:-1], x.shape[-1] // 16, 16)
+    sc = (xb.abs().amax(dim=-1).clamp(min=0.012) / 6.0).to(torch.float8_e4m3fn)
+    y = xb / sc.float().unsqueeze(-1)
+    mids = torch.tensor([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], device=x.device)
+    codes = torch.bucketize(y.abs(), mids).to(torch.uint8) | ((y < 0).to(torch.uint8) << 3)
+    codes = codes.reshape(x.shape)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).contiguous()
+    return packed, sc.view(torch.uint8).contiguous()
+
+
+def time_decode(msa, w, fp8, steps, warmup, fp8_index=False, fp4_index=False):
     """Decode step for B sequences: index branch (k_idx cache scan + top-k) and
     main branch over the selected pages. fp8: E4M3 K / V pages; fp8_index: the
-    k_idx cache and q_idx as E4M3 codes too (rounded by torch before timing)."""
+    k_idx cache and q_idx as E4M3 codes too (rounded by torch before timing);
+    fp4_index: an NVFP4 k_idx cache (quantised by torch before timing)."""
     import torch
     import synth
     dev = torch.device("cuda")
@@ -298,6 +314,14 @@ def time_decode(msa, w, fp8, steps, warmup, fp8_index=False):
         qidx = qidx.to(torch.float8_e4m3fn)
         torch.cuda.empty_cache()
     index = msa.msa_index_select_decode_fp8 if fp8_index else msa.msa_index_select_decode
+    if fp4_index:
+        codes, scales = nvfp4_quantise(kidx_p)
+        del kidx_p
+        torch.cuda.empty_cache()
+
+        def index(qi, _k, pt_, sl_, Bk, k, **kw):
+            return msa.msa_index_select_decode_nvfp4(qi, codes, scales, pt_, sl_, Bk, k, **kw)
+        kidx_p = None
     ids = torch.empty((w.B, w.n_g, w.k), dtype=torch.int32, device=dev)
     ws_i = torch.empty(msa.msa_index_select_decode_workspace_bytes(w.B, w.nb, w.n_g),
                        dtype=torch.uint8, device=dev)
@@ -656,11 +680,12 @@ def main():
     peaks, peak_src = load_peaks()
     if args.only == "decode":
         wd = synth.make("decode", **({"B": args.batch} if args.batch else {}))
-        for fp8, fp8_index in ((False, False), (True, False), (True, True)):
-            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, args.warmup, fp8_index)
+        for fp8, fp8_index, fp4_index in ((False, False, False), (True, False, False),
+                                          (True, True, False), (True, False, True)):
+            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, args.warmup, fp8_index, fp4_index)
             torch.cuda.empty_cache()
             print(json.dumps({"only": "decode", "fp8": fp8, "fp8_index": fp8_index,
-                              "index_ms": i_ms, "attention_ms": a_ms}))
+                              "fp4_index": fp4_index, "index_ms": i_ms, "attention_ms": a_ms}))
         return
     if args.only == "index":
         w = synth.make(args.workload)
@@ -782,13 +807,17 @@ def main():
             "index_tflops": round(p_fli / (p_idx * 1e-3) / 1e12, 2),
             "tflops": round((p_fli + p_fla) / (p_ms * 1e-3) / 1e12, 2)}
         wd = synth.make("decode")
-        for fp8, fp8_index in ((False, False), (True, False), (True, True)):
-            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, 1, fp8_index)
+        for fp8, fp8_index, fp4_index in ((False, False, False), (True, False, False),
+                                          (True, True, False), (True, False, True)):
+            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, 1, fp8_index, fp4_index)
             torch.cuda.empty_cache()
             kv_bytes = 2.0 * wd.B * wd.n_g * (wd.k - 1) * wd.Bk * wd.d * (1 if fp8 else 2) + \
                 2.0 * wd.B * wd.n_g * 1 * wd.d * (1 if fp8 else 2)
-            scan_bytes = (1.0 if fp8_index else 2.0) * wd.B * wd.L * wd.d_idx
-            key = "decode_fp8_index_and_kv" if fp8_index else ("decode_fp8" if fp8 else "decode_bf16")
+            per_elem = 0.5 + 1.0 / 16 if fp4_index else (1.0 if fp8_index else 2.0)
+            scan_bytes = per_elem * wd.B * wd.L * wd.d_idx
+            key = ("decode_nvfp4_index_fp8_kv" if fp4_index else
+                   "decode_fp8_index_and_kv" if fp8_index else
+                   ("decode_fp8" if fp8 else "decode_bf16"))
             extra[key] = {
                 "tokens_per_s": wd.B / ((i_ms + a_ms) * 1e-3),
                 "attention_only_tokens_per_s": wd.B / (a_ms * 1e-3),

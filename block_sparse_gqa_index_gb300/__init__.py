@@ -65,6 +65,8 @@ _ws_attn_varlen = _sig("msa_sparse_attn_varlen_workspace_bytes", [_P, _I, _I, _I
                        _SZ)
 _attn_varlen = _sig("msa_sparse_attn_varlen", [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                                _P, _P, _P, _SZ, _P])
+_index_dec_fp4 = _sig("msa_index_select_decode_nvfp4", [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                                         _I, _P, _P, _F, _P, _SZ, _P])
 _ws_kl = _sig("msa_kl_teacher_workspace_bytes", [_I64, _I64, _I, _I, _I, _I, _I], _SZ)
 _kl = _sig("msa_kl_teacher", [_P, _P, _P, _P, _P, _P, _I64, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                               _SZ, _P])
@@ -88,7 +90,7 @@ EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes
            "msa_sparse_attn_varlen", "msa_index_select_paged",
            "msa_sparse_attn_paged_workspace_bytes", "msa_sparse_attn_paged",
            "msa_index_select_decode_fp8", "msa_kl_teacher_workspace_bytes",
-           "msa_kl_teacher"]
+           "msa_kl_teacher", "msa_index_select_decode_nvfp4"]
 
 
 class MSAError(RuntimeError):
@@ -500,6 +502,44 @@ def msa_index_select_decode_fp8(q_idx: torch.Tensor, k_idx_pages: torch.Tensor,
                           block_ids.data_ptr(), _ptr(block_scores), score_scale, ws_ptr, ws_n,
                           _stream(q_idx)),
            "msa_index_select_decode_fp8")
+    return block_ids
+
+
+def msa_index_select_decode_nvfp4(q_idx: torch.Tensor, k_idx_codes: torch.Tensor,
+                                  k_idx_scales: torch.Tensor, page_table: torch.Tensor,
+                                  seq_lens: torch.Tensor, Bk: int = 128, k: int = 16,
+                                  block_ids: Optional[torch.Tensor] = None,
+                                  block_scores: Optional[torch.Tensor] = None,
+                                  score_scale: float = 1.0,
+                                  workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Index branch of decode over an NVFP4 k_idx cache: q_idx [B, n_groups, d_idx]
+    bf16, k_idx_codes [P, Bk, d_idx / 2] uint8 (two E2M1 codes per byte, even
+    dimension in the low nibble), k_idx_scales [P, Bk, d_idx / 16] uint8 (E4M3,
+    one per 16 dimensions), page_table [B, max_pages] int32, seq_lens [B] int32
+    -> block_ids [B, n_groups, k]."""
+    B, n_g, d_idx = q_idx.shape
+    max_pages = page_table.shape[1]
+    _req(q_idx, "q_idx", torch.bfloat16)
+    P = k_idx_codes.shape[0]
+    _req(k_idx_codes, "k_idx_codes", torch.uint8, (P, Bk, d_idx // 2))
+    _req(k_idx_scales, "k_idx_scales", torch.uint8, (P, Bk, d_idx // 16))
+    _req(page_table, "page_table", torch.int32, (B, max_pages))
+    _req(seq_lens, "seq_lens", torch.int32, (B,))
+    if block_ids is None:
+        block_ids = torch.empty((B, n_g, k), dtype=torch.int32, device=q_idx.device)
+    _req(block_ids, "block_ids", torch.int32, (B, n_g, k))
+    if block_scores is not None:
+        _req(block_scores, "block_scores", torch.float32, (B, n_g, max_pages))
+    elif workspace is None:
+        workspace = torch.empty(_ws_index_dec(B, max_pages, n_g), dtype=torch.uint8,
+                                device=q_idx.device)
+    ws_ptr, ws_n = (None, 0) if workspace is None else (_req(workspace, "workspace", torch.uint8),
+                                                         workspace.numel())
+    _check(_index_dec_fp4(q_idx.data_ptr(), k_idx_codes.data_ptr(), k_idx_scales.data_ptr(),
+                          page_table.data_ptr(), seq_lens.data_ptr(), B, max_pages, n_g, d_idx,
+                          Bk, k, block_ids.data_ptr(), _ptr(block_scores), score_scale, ws_ptr,
+                          ws_n, _stream(q_idx)),
+           "msa_index_select_decode_nvfp4")
     return block_ids
 
 

@@ -482,6 +482,40 @@ int msa_index_select_decode_fp8(const void* q_idx, const void* k_idx_pages,
                       score_scale);
 }
 
+int msa_index_select_decode_nvfp4(const void* q_idx, const void* k_idx_codes,
+                                  const void* k_idx_scales, const int32_t* page_table,
+                                  const int32_t* seq_lens, int B, int max_pages, int n_groups,
+                                  int d_idx, int Bk, int k, int32_t* block_ids,
+                                  float* block_scores, float score_scale, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (B < 0 || max_pages < 1 || n_groups < 1 || d_idx < 1 || Bk < 1 || k < 1)
+    return MSA_ERR_INVALID_ARG;
+  if (B == 0) return MSA_OK;
+  if (!q_idx || !k_idx_codes || !k_idx_scales || !page_table || !seq_lens || !block_ids)
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx_codes) || !aligned16(k_idx_scales) ||
+      (block_scores && !aligned16(block_scores)))
+    return MSA_ERR_INVALID_ARG;
+  if (Bk != 128 || !supported_k(k) || !supported_d(d_idx) || n_groups > 8)
+    return MSA_ERR_UNSUPPORTED;
+  float* scores = block_scores;
+  if (!scores) {
+    if (!workspace || workspace_bytes < msa_index_select_decode_workspace_bytes(B, max_pages,
+                                                                                n_groups))
+      return MSA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MSA_ERR_INVALID_ARG;
+    scores = (float*)workspace;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  msa::Diag dg = diag();
+  cudaError_t e = msa::launch_decode_index_fp4(q_idx, k_idx_codes, k_idx_scales, page_table,
+                                               seq_lens, B, max_pages, n_groups, d_idx,
+                                               score_scale, scores, dg, st);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  e = msa::launch_topk(scores, B, n_groups, max_pages, Bk, k, 0, seq_lens, block_ids, dg, st);
+  return status_of(e);
+}
+
 size_t msa_decode_workspace_bytes(int B, int H_q, int d, int k) {
   if (B < 0 || H_q < 0 || d < 0 || k < 0) return 0;
   return msa::decode_ws_bytes(B, H_q, d, k);

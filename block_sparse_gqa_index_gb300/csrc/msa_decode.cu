@@ -191,6 +191,138 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * ROWB + ((c ^ (r & kMask)) << 4));
 }
 
+// ---- decode index scan over an NVFP4 k_idx cache
+//
+// Keys are E2M1 codes, two per byte (the even dimension in the low nibble),
+// with one E4M3 scale per 16 consecutive dimensions of a key ("micro-block");
+// a key's value in dimension c is e2m1 * scale[c / 16]. One warp per
+// (sequence, page): it copies the page's codes and scales into its own shared
+// buffer (cp.async: a whole page's bytes in flight per warp), then for every
+// 16 keys runs one mma.m16n8k16 per micro-block (keys x the groups' q_idx, f16
+// operands: every E2M1 value is an f16 value, and q_idx is rounded to f16) and
+// adds the product times the keys' scales of that micro-block into fp32, so
+// the scales never touch the operands. Within a micro-block the four lanes of
+// a row take 4 contiguous dimensions each (one 16-bit read), and q_idx is
+// permuted the same way.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}\n"
+      : "=r"(r)
+      : "r"(byte));
+  return r;
+}
+__device__ __forceinline__ void mma_f16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
+  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)byte, __NV_E4M3);
+  return __half2float(__ushort_as_half(h.x));
+}
+
+constexpr int kFp4Warps = 4;
+
+template <int DI>
+__global__ void __launch_bounds__(kFp4Warps * 32)
+decode_index_fp4_kernel(const uint16_t* __restrict__ q_idx, const unsigned char* __restrict__ codes,
+                        const unsigned char* __restrict__ kscales,
+                        const int32_t* __restrict__ page_table,
+                        const int32_t* __restrict__ seq_lens, int B, int max_pages, int n_g,
+                        float out_scale, float* __restrict__ scores, Diag dg) {
+  constexpr int CB = DI / 2;    // code bytes per key
+  constexpr int SB = DI / 16;   // scale bytes per key
+  constexpr int KS = DI / 16;   // micro-blocks = k-steps
+  static_assert(SB == 4 || SB == 8, "d_idx is 64 or 128");
+  constexpr int WBYTES = kBk * (CB + SB);
+  extern __shared__ __align__(128) unsigned char f4s[];
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+  const int gq = lane >> 2, t4 = lane & 3;
+  unsigned char* sc = f4s + wi * WBYTES;  // codes [128][CB], then scales [128][SB]
+  unsigned char* ss = sc + kBk * CB;
+  const uint32_t sc_a = smem_addr(sc), ss_a = smem_addr(ss);
+  const int64_t n_tasks = (int64_t)B * max_pages;
+  for (int64_t task = (int64_t)blockIdx.x * kFp4Warps + wi; task < n_tasks;
+       task += (int64_t)gridDim.x * kFp4Warps) {
+    const int s = (int)(task / max_pages);
+    const int b = (int)(task % max_pages);
+    const int L = seq_lens[s];
+    if (L < 1 || L > max_pages * kBk) {
+      if (b == 0 && lane == 0) report(dg, kStatusBadIds);
+      continue;
+    }
+    if ((int64_t)b * kBk >= L) continue;
+    const int nvalid = min(kBk, L - b * kBk);
+    const int64_t page = page_table[(size_t)s * max_pages + b];
+    const unsigned char* gc = codes + (size_t)page * kBk * CB;
+    const unsigned char* gs = kscales + (size_t)page * kBk * SB;
+    __syncwarp();  // the previous task's reads of the buffer are done
+    for (int e = lane; e < kBk * CB / 16; e += 32) cp_async16(sc_a + e * 16, gc + e * 16, 16u);
+    for (int e = lane; e < kBk * SB / 16; e += 32) cp_async16(ss_a + e * 16, gs + e * 16, 16u);
+    cp_async_commit();
+    // B operand: group gq's q_idx in f16, dimensions 16 ks + 4 t4 + {0,1} | {2,3}
+    uint32_t bq[KS][2];
+    const uint16_t* qr = q_idx + ((size_t)s * n_g + (gq < n_g ? gq : 0)) * DI;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const uint2 w = gq < n_g ? *reinterpret_cast<const uint2*>(qr + 16 * ks + 4 * t4)
+                               : make_uint2(0u, 0u);
+      bq[ks][0] = f16x2_of(bf16_lo(w.x), bf16_hi(w.x));
+      bq[ks][1] = f16x2_of(bf16_lo(w.y), bf16_hi(w.y));
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll 2
+    for (int m = 0; m < kBk / 16; ++m) {
+      const int key0 = m * 16 + gq, key1 = key0 + 8;
+      uint2 s0, s1;  // the keys' micro-block scales (E4M3 bytes)
+      if constexpr (SB == 8) {
+        s0 = *reinterpret_cast<const uint2*>(ss + key0 * SB);
+        s1 = *reinterpret_cast<const uint2*>(ss + key1 * SB);
+      } else {
+        s0 = make_uint2(*reinterpret_cast<const uint32_t*>(ss + key0 * SB), 0u);
+        s1 = make_uint2(*reinterpret_cast<const uint32_t*>(ss + key1 * SB), 0u);
+      }
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint32_t c0 = lds_u16(sc_a + key0 * CB + 8 * ks + 2 * t4);
+        const uint32_t c1 = lds_u16(sc_a + key1 * CB + 8 * ks + 2 * t4);
+        float p[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16_16816(p, e2m1x2_to_f16x2(c0 & 0xFF), e2m1x2_to_f16x2(c1 & 0xFF),
+                      e2m1x2_to_f16x2(c0 >> 8), e2m1x2_to_f16x2(c1 >> 8), bq[ks][0], bq[ks][1]);
+        const uint32_t w0 = ks < 4 ? s0.x : s0.y, w1 = ks < 4 ? s1.x : s1.y;
+        const float f0 = e4m3_to_float((w0 >> (8 * (ks & 3))) & 0xFF);
+        const float f1 = e4m3_to_float((w1 >> (8 * (ks & 3))) & 0xFF);
+        acc[0] = fmaf(p[0], f0, acc[0]);
+        acc[1] = fmaf(p[1], f0, acc[1]);
+        acc[2] = fmaf(p[2], f1, acc[2]);
+        acc[3] = fmaf(p[3], f1, acc[3]);
+      }
+      if (key0 < nvalid) { mx0 = fmaxf(mx0, acc[0]); mx1 = fmaxf(mx1, acc[1]); }
+      if (key1 < nvalid) { mx0 = fmaxf(mx0, acc[2]); mx1 = fmaxf(mx1, acc[3]); }
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    if (gq == 0) {
+      const int g0 = 2 * t4, g1 = 2 * t4 + 1;
+      if (g0 < n_g) scores[((size_t)s * n_g + g0) * max_pages + b] = mx0 * out_scale;
+      if (g1 < n_g) scores[((size_t)s * n_g + g1) * max_pages + b] = mx1 * out_scale;
+    }
+  }
+}
+
 template <int D, bool FP8>
 constexpr int dec_smem_bytes() {
   return 2 * kBk * D * (FP8 ? 1 : 2);
@@ -451,6 +583,36 @@ cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,
     else MSA_DEC_INDEX(64, false);
   }
 #undef MSA_DEC_INDEX
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_index_fp4(const void* q_idx, const void* codes, const void* kscales,
+                                    const int32_t* page_table, const int32_t* seq_lens, int B,
+                                    int max_pages, int n_g, int d_idx, float score_scale,
+                                    float* scores, const Diag& dg, cudaStream_t st) {
+  const int64_t tasks = (int64_t)B * max_pages;
+  if (tasks == 0) return cudaSuccess;
+  note_launches(1);
+  const unsigned grid =
+      (unsigned)std::min<int64_t>((tasks + kFp4Warps - 1) / kFp4Warps, 152 * 32);
+  const int smem = kFp4Warps * kBk * (d_idx / 2 + d_idx / 16);
+  auto q = (const uint16_t*)q_idx;
+  auto c = (const unsigned char*)codes;
+  auto sc = (const unsigned char*)kscales;
+  cudaError_t e;
+  if (d_idx == 128) {
+    e = cudaFuncSetAttribute(decode_index_fp4_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    decode_index_fp4_kernel<128><<<grid, kFp4Warps * 32, smem, st>>>(
+        q, c, sc, page_table, seq_lens, B, max_pages, n_g, score_scale, scores, dg);
+  } else {
+    e = cudaFuncSetAttribute(decode_index_fp4_kernel<64>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    decode_index_fp4_kernel<64><<<grid, kFp4Warps * 32, smem, st>>>(
+        q, c, sc, page_table, seq_lens, B, max_pages, n_g, score_scale, scores, dg);
+  }
   return cudaGetLastError();
 }
 

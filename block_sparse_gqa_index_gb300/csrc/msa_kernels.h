@@ -130,6 +130,13 @@ cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,
                                 int max_pages, int n_g, int d_idx, float* scores,
                                 const Diag& dg, cudaStream_t st, bool e4m3 = false,
                                 float score_scale = 1.f);
+// NVFP4 k_idx cache: codes [P, 128, d_idx / 2] (two E2M1 per byte, even
+// dimension low), kscales [P, 128, d_idx / 16] E4M3 micro-block scales;
+// q_idx bf16. Scores written times score_scale.
+cudaError_t launch_decode_index_fp4(const void* q_idx, const void* codes, const void* kscales,
+                                    const int32_t* page_table, const int32_t* seq_lens, int B,
+                                    int max_pages, int n_g, int d_idx, float score_scale,
+                                    float* scores, const Diag& dg, cudaStream_t st);
 size_t decode_ws_bytes(int B, int H_q, int d, int k);
 cudaError_t launch_decode_attn(const void* q, const void* k_pages, const void* v_pages,
                                int kv_fp8, const float* k_scale, const float* v_scale,

@@ -280,6 +280,26 @@ int msa_index_select_decode_fp8(const void* q_idx, const void* k_idx_pages,
                                 int32_t* block_ids, float* block_scores, float score_scale,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Index branch of decode over an NVFP4 k_idx cache (the kernel release lists
+ * NVFP4 and FP4 among its precisions: "MiniMax lança MSA ...", section "Kernel
+ * open source e MiniMax-M3"; a quarter of the bf16 scan's bytes plus one scale
+ * byte per 16 dimensions):
+ *   k_idx_codes   [P, Bk, d_idx / 2] uint8: two OCP E2M1 codes per byte, the
+ *                 even dimension in the low nibble
+ *   k_idx_scales  [P, Bk, d_idx / 16] uint8: one E4M3 scale per 16 consecutive
+ *                 dimensions of a key; key value = e2m1 * scale
+ *   q_idx         [B, n_groups, d_idx] bf16, rounded to f16 for the products
+ *                 (exact for |x| >= 2^-14 and below 65504 with 8 significant
+ *                 bits, which every bf16 value in that range has)
+ * A tensor-wide scale changes no ranking; score_scale only multiplies the
+ * optional block_scores. Everything else as msa_index_select_decode. */
+int msa_index_select_decode_nvfp4(const void* q_idx, const void* k_idx_codes,
+                                  const void* k_idx_scales, const int32_t* page_table,
+                                  const int32_t* seq_lens, int B, int max_pages, int n_groups,
+                                  int d_idx, int Bk, int k, int32_t* block_ids,
+                                  float* block_scores, float score_scale, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
 /* Workspace bytes of msa_decode (split-KV partials). */
 size_t msa_decode_workspace_bytes(int B, int H_q, int d, int k);
 

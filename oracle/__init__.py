@@ -30,6 +30,8 @@ def lib():
         L.oracle_bf16_to_f64.restype = D
         L.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         L.oracle_e4m3_to_f64.restype = D
+        L.oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        L.oracle_e2m1_to_f64.restype = D
         L.oracle_index_select.argtypes = [P, P, I64, P, I32, I32, I32, I32, I64, P, P]
         L.oracle_topk_blocks.argtypes = [P, P, I64, I32, I64, I32, I32, P]
         L.oracle_sparse_attn.argtypes = [P, P, I64, P, P, P, I32, I32, I32, I32, I32, D, P, P]
@@ -64,6 +66,11 @@ def bf16_to_f64(bits: int) -> float:
 
 def e4m3_to_f64(bits: int) -> float:
     return lib().oracle_e4m3_to_f64(bits)
+
+
+def e2m1_to_f64(code: int) -> float:
+    """OCP FP4 E2M1 code (low 4 bits) -> value."""
+    return lib().oracle_e2m1_to_f64(code & 0xF)
 
 
 def index_select(q_idx_rows, rows, k_idx, Bk, k, nb_out=0, want_scores=False):

@@ -85,6 +85,14 @@ double e4m3_to_double(uint8_t b) {
   return sign ? -v : v;
 }
 
+// OCP FP4 E2M1: 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit, no
+// infinities or NaN; exponent 0 is subnormal (m * 0.5).
+double e2m1_to_double(uint8_t c) {
+  int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+  double v = e == 0 ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, e - 1);
+  return sign ? -v : v;
+}
+
 // Key rows of one sequence. Unpaged tensors are [tokens, H, D]. Paged caches
 // keep each page head-major, [pages, H, Bk, D] (the page tensor's second
 // dimension is the number of kv heads in the pages' usage listing), with
@@ -193,6 +201,7 @@ unsigned oracle_hardware_concurrency(void) { return std::thread::hardware_concur
 
 double oracle_bf16_to_f64(uint16_t h) { return bf16_to_double(h); }
 double oracle_e4m3_to_f64(uint8_t b) { return e4m3_to_double(b); }
+double oracle_e2m1_to_f64(uint8_t c) { return e2m1_to_double(c); }
 
 // Prefill index branch (a1-a3) for n_rows query positions rows[i].
 //   q_idx_rows [n_rows, n_g, d_idx] bf16 bits: the index queries of those rows

@@ -115,6 +115,22 @@ def test_decode_index_fp8_rejects(msa):
              None) == 0                                              # empty batch
 
 
+def test_decode_index_nvfp4_rejects(msa):
+    g = msa._index_dec_fp4
+    # q_idx, codes, scales, page_table, seq_lens, B, max_pages, n_g, d_idx, Bk, k, ids, scores,
+    # score_scale, ws, ws_bytes, stream
+    assert g(FAKE, FAKE, None, FAKE, FAKE, 4, 10, 8, 128, 128, 16, FAKE, None, 1.0, FAKE, 1 << 20,
+             None) == -1                                             # no scales
+    assert g(FAKE, FAKE, FAKE + 8, FAKE, FAKE, 4, 10, 8, 128, 128, 16, FAKE, None, 1.0, FAKE,
+             1 << 20, None) == -1                                    # misaligned scales
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, 9, 128, 128, 16, FAKE, None, 1.0, FAKE, 1 << 20,
+             None) == -2                                             # 9 groups
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, 8, 96, 128, 16, FAKE, None, 1.0, FAKE, 1 << 20,
+             None) == -2                                             # d_idx
+    assert g(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, 8, 128, 128, 16, FAKE, None, 1.0, None, 0,
+             None) == -3                                             # no workspace
+
+
 def test_wait_limit_roundtrip(msa):
     old = msa.msa_set_wait_limit(123)
     assert msa.msa_set_wait_limit(old) == 123

@@ -572,6 +572,91 @@ def test_decode_index_fp8_gauss(msa, d_idx, H_kv):
     assert rel.max() < 1e-4
 
 
+def _nvfp4_cache(w, rng, gaussian):
+    """An NVFP4 k_idx cache for the decode workload w: E2M1 codes (two per
+    byte, even dimension low) and one E4M3 scale per 16 dimensions of a key,
+    identity-paged on the host ([B * nb, Bk, ...]), with the decoded values as
+    bf16 bits (exact: an E2M1 value times an E4M3 scale has at most 6
+    significant bits). Integer mode draws codes and power-of-two-and-1.5
+    scales; Gaussian mode quantises the workload's k_idx (scale = the E4M3 of
+    amax / 6, amax at least 0.012 so that the scale is at least the smallest
+    E4M3 subnormal, codes rounded to the nearest E2M1 value)."""
+    e2m1 = np.array([oracle.e2m1_to_f64(c) for c in range(16)])
+    P, d = w.B * w.nb, w.d_idx
+    if gaussian:
+        x = bits_f64(synth.host_paged(w, synth.T_KIDX)[:, 0])          # [P, Bk, d]
+        xb = x.reshape(P, w.Bk, d // 16, 16)
+        amax = np.abs(xb).max(axis=-1)
+        sc_codes = torch.from_numpy((np.maximum(amax, 0.012) / 6.0).astype(np.float32)) \
+            .to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        sc = np.array([oracle.e4m3_to_f64(int(c)) for c in range(256)])[sc_codes]
+        y = xb / sc[..., None]
+        mags = e2m1[:8]
+        idx = np.abs(np.abs(y)[..., None] - mags).argmin(axis=-1)
+        codes = (idx | np.where(y < 0, 8, 0)).astype(np.uint8).reshape(P, w.Bk, d)
+    else:
+        codes = rng.integers(0, 16, size=(P, w.Bk, d)).astype(np.uint8)
+        sc_codes = rng.choice(np.array([0x30, 0x38, 0x3C, 0x40, 0x48], dtype=np.uint8),
+                              size=(P, w.Bk, d // 16))
+    vals = e2m1[codes] * np.repeat(np.array([oracle.e4m3_to_f64(int(c)) for c in range(256)])
+                                   [sc_codes], 16, axis=-1)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    bits = (vals.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(bits_f64(bits), vals)                          # exact in bf16
+    return packed, sc_codes.astype(np.uint8), bits
+
+
+def bits_f64(b):
+    return (np.ascontiguousarray(b).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("gaussian,d_idx,H_kv", [(False, 128, 8), (False, 64, 2), (True, 128, 8)])
+def test_decode_index_nvfp4(msa, gaussian, d_idx, H_kv):
+    """NVFP4 k_idx cache: ids against the oracle on the decoded values (bit for
+    bit on integer-valued inputs, up to near-tie swaps on quantised Gaussian
+    ones) over ragged lengths and a shuffled page table; block scores against
+    the bf16 path on the decoded cache times score_scale."""
+    kind = synth.KIND_GAUSS if gaussian else synth.KIND_INT
+    w = synth.make("decode", B=6, L=128 * 12 + 5, H_q=2 * H_kv, H_kv=H_kv, d=d_idx, d_idx=d_idx,
+                   kind=kind, k=6)
+    lens = np.array([1, 2, 128, 129, 900, w.L], dtype=np.int32)
+    rng = np.random.default_rng(17)
+    packed, scales, bits = _nvfp4_cache(w, rng, gaussian)
+    dev = torch.device("cuda")
+    pt = torch.from_numpy(synth.page_table(w)).to(dev)
+    order = pt.flatten().long()
+    codes_d = torch.empty(packed.shape, dtype=torch.uint8, device=dev)
+    codes_d[order] = torch.from_numpy(packed).to(dev)
+    scales_d = torch.empty(scales.shape, dtype=torch.uint8, device=dev)
+    scales_d[order] = torch.from_numpy(scales).to(dev)
+    bf_d = torch.empty(bits.shape, dtype=torch.int16, device=dev)
+    bf_d[order] = torch.from_numpy(bits.view(np.int16)).to(dev)
+    sl = torch.from_numpy(lens).to(dev)
+    qidx = synth.device_rows(w, synth.T_QIDX, [(s, int(lens[s]) - 1) for s in range(w.B)])
+    s4 = torch.full((w.B, w.n_g, w.nb), float("nan"), device=dev)
+    ids4 = msa.msa_index_select_decode_nvfp4(qidx, codes_d, scales_d, pt, sl, w.Bk, w.k,
+                                             block_scores=s4, score_scale=0.5)
+    s16 = torch.full((w.B, w.n_g, w.nb), float("nan"), device=dev)
+    ids16 = msa.msa_index_select_decode(qidx, bf_d.view(torch.bfloat16), pt, sl, w.Bk, w.k,
+                                        block_scores=s16)
+    torch.cuda.synchronize()
+    qh = np.stack([synth.host_rows(w, synth.T_QIDX, s, [int(lens[s]) - 1])[0]
+                   for s in range(w.B)])
+    want, want_s = oracle.decode_index_select(qh, bits, synth.page_table(w, permute=False), lens,
+                                              w.Bk, w.k, nb_out=w.nb, want_scores=True)
+    got = ids4.cpu().numpy()
+    if gaussian:
+        swaps = compare_selection(got, want, want_s, lens - 1, w.Bk)
+        assert swaps <= 0.01 * got.shape[0] * got.shape[1]
+    else:
+        assert np.array_equal(got, want)
+        assert torch.equal(ids4, ids16)
+    for s in range(w.B):
+        nv = (int(lens[s]) - 1) // w.Bk + 1
+        a, b = s4[s, :, :nv].double() * 2.0, s16[s, :, :nv].double()
+        assert ((a - b).abs() <= 1e-5 * b.abs().clamp(min=1.0)).all()
+
+
 def test_decode_matches_prefill_row_on_gpu(msa):
     """Decoding the last token against the cache equals the last prefill row."""
     w = synth.make("decode", B=1, L=128 * 9 + 5, H_q=8, H_kv=2, d=128, d_idx=128,

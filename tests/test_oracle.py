@@ -486,3 +486,13 @@ def test_kl_matches_brute_force_on_tiny_inputs():
             student = [math.exp(x - top) / z for x in sc]
             want = sum(p * math.log(p / s) for p, s in zip(teacher, student) if p > 0)
             assert abs(kl[t, g] - want) < 1e-10 * max(1.0, abs(want)), (t, g)
+
+
+def test_e2m1_decoder_exhaustive_vs_ocp():
+    """All 16 FP4 E2M1 codes against the OCP table: sign bit 3, exponent bits
+    2..1 with bias 1, one mantissa bit, exponent 0 subnormal (m * 0.5)."""
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(16):
+        want = table[c & 7] * (-1.0 if c & 8 else 1.0)
+        got = oracle.e2m1_to_f64(c)
+        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), c
