@@ -17,10 +17,10 @@
 //   2. tau = max(15th largest group max, worst key kept so far): at least k-1
 //      keys are >= tau, so no key below tau can be in the answer;
 //   3. the keys >= tau (typically 15-30) are compacted into shared memory (each
-//      lane reads its survivors back from its staged values) and bitonic-sorted
-//      within the half (32 keys, 2 per lane); the best k-1 are kept, one per
-//      lane. More than 32 survivors in either half send both halves through
-//      k-1 rounds of arg-max instead.
+//      lane reads its survivors back from its staged values); every survivor
+//      counts the survivors that beat it, and the k-1 with the lowest counts
+//      are kept, one per lane, in descending order. More than 32 survivors in
+//      either half send both halves through k-1 rounds of arg-max instead.
 // Finally the kept ids plus the local block are sorted ascending and written.
 // Blocks past the candidates read as NaN, which no comparison keeps and which
 // max.f32 ignores (inputs themselves must be finite).
@@ -62,34 +62,27 @@ __device__ __forceinline__ float key_value(uint64_t key) {
   return __uint_as_float(b);
 }
 
-// Bitonic sort, descending, of the 32 elements a half holds 2 per lane
-// (element e = hl + 16 r is a[r] of half-lane hl). Exchanges at distance 16 stay
-// in the lane; the others are shuffles within the half.
-__device__ __forceinline__ float shx(float v, int m) { return __shfl_xor_sync(kAll, v, m); }
-__device__ __forceinline__ uint64_t shx(uint64_t v, int m) { return shfl_xor64(v, m); }
-
-template <typename T>
-__device__ __forceinline__ void sort32h_desc(T& a0, T& a1, int hl) {
+// Bitonic sort, descending, of the 32 floats a half holds 2 per lane: element
+// e = 2 hl + r is a[r] of half-lane hl, so the exchanges at distance 1 stay in
+// the lane and the others are shuffles at lane distance stride / 2. Both
+// elements of a lane share each stage's direction.
+__device__ __forceinline__ void sort32h_desc(float& a0, float& a1, int hl) {
 #pragma unroll
   for (int size = 2; size <= 32; size <<= 1)
 #pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride == 16) {  // size 32: the whole sequence descends
-        const bool sw = a1 > a0;
-        const T x = sw ? a1 : a0, y = sw ? a0 : a1;
-        a0 = x;
-        a1 = y;
+      const bool up = ((2 * hl) & size) == 0;  // this pair descends
+      if (stride == 1) {
+        const float mx = fmaxf(a0, a1), mn = fminf(a0, a1);
+        a0 = up ? mx : mn;
+        a1 = up ? mn : mx;
       } else {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          T& a = r ? a1 : a0;
-          const int e = hl + 16 * r;
-          const T p = shx(a, stride);
-          const bool up = (e & size) == 0;
-          const bool lower = (e & stride) == 0;
-          const T mx = a > p ? a : p, mn = a > p ? p : a;
-          a = (lower == up) ? mx : mn;
-        }
+        const bool lower = (hl & (stride >> 1)) == 0;
+        const bool take_max = lower == up;
+        const float p0 = __shfl_xor_sync(kAll, a0, stride >> 1);
+        const float p1 = __shfl_xor_sync(kAll, a1, stride >> 1);
+        a0 = take_max ? fmaxf(a0, p0) : fminf(a0, p0);
+        a1 = take_max ? fmaxf(a1, p1) : fminf(a1, p1);
       }
     }
 }
@@ -176,7 +169,7 @@ __device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1,
   // threshold: the kfar-th largest group max (>= kfar values reach it) or the
   // worst value kept so far, whichever is larger
   sort32h_desc(m0, m1, hl);
-  float tau = __shfl_sync(kAll, m0, kfar - 1, 16);
+  float tau = __shfl_sync(kAll, (kfar - 1) & 1 ? m1 : m0, (kfar - 1) >> 1, 16);
   tau = fmaxf(tau, best_min);
   // survivors (>= tau; ties at tau are kept and settled by the keys)
   uint32_t mask = 0;
@@ -207,11 +200,23 @@ __device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1,
       buf[p++] = rank_key(svf[e], (uint32_t)(c0 + e));
     }
     __syncwarp();
-    uint64_t a0 = hl < total ? buf[hl] : 0;
-    uint64_t a1 = hl + 16 < total ? buf[hl + 16] : 0;
+    const uint64_t a0 = hl < total ? buf[hl] : 0;
+    const uint64_t a1 = hl + 16 < total ? buf[hl + 16] : 0;
+    // rank of a survivor = how many survivors beat it (keys are distinct, so the
+    // ranks are a permutation); the kfar best land in slots 0..kfar-1, descending
+    int r0 = 0, r1 = 0;
+#pragma unroll 4
+    for (int j = 0; j < total; ++j) {
+      const uint64_t y = buf[j];
+      r0 += y > a0 ? 1 : 0;
+      r1 += y > a1 ? 1 : 0;
+    }
     __syncwarp();
-    sort32h_desc(a0, a1, hl);
-    best = hl < kfar ? a0 : 0;
+    if (hl < total && r0 < kfar) buf[r0] = a0;
+    if (hl + 16 < total && r1 < kfar) buf[r1] = a1;
+    __syncwarp();
+    best = hl < kfar ? buf[hl] : 0;
+    __syncwarp();
   } else {
     // rare (heavy ties): extract the kfar best of each half one by one
     uint64_t nb_best = 0, prev = ~0ull;
@@ -242,7 +247,7 @@ __global__ void __launch_bounds__(kWarps * 32, 5)
 topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, int Bk,
             int bk_shift, int k, int64_t q_offset, const int32_t* __restrict__ seq_lens,
             int32_t* __restrict__ ids, Diag dg) {
-  __shared__ uint64_t buf[kWarps][2][kCap];
+  __shared__ uint64_t buf[kWarps][2][kCap + 1];  // +1: the halves on different banks
   __shared__ float4 sval[kWarps][2][8 * 16];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
