@@ -19,7 +19,8 @@
 //   block's K and V bytes all in flight at once (cp.async into swizzled shared
 //   memory) and both products on mma.m16n8k16; writes the block's normalised
 //   output and LSE (split-KV partials).
-// decode_merge_kernel: combines the k partials of every (sequence, head).
+// decode_merge_kernel: combines the k partials of every (sequence, head), one
+//   warp each, with all of its partial rows in flight at once.
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
@@ -516,43 +517,82 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
   }
 }
 
+// One warp per (sequence, head). Lane i < k holds slot i: its block id, its
+// LSE and (through the warp reductions) the slot's weight. Every lane owns D/32
+// contiguous output columns, and the k partial rows of those columns are all
+// requested before the first is used, so a warp waits on memory about twice
+// (the ids and LSEs, then the rows) instead of once per slot. Slots whose block
+// id is invalid get weight 0 and their rows, which the attention kernel may not
+// have written, are never added.
 template <int D>
-__global__ void decode_merge_kernel(const float* __restrict__ part_o,
-                                    const float* __restrict__ part_lse,
-                                    const int32_t* __restrict__ ids,
-                                    const int32_t* __restrict__ seq_lens, int max_pages, int B,
-                                    int H_q, int H_kv, int k, uint16_t* __restrict__ out,
-                                    float* __restrict__ lse) {
+__global__ void __launch_bounds__(256)
+decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse,
+                    const int32_t* __restrict__ ids, const int32_t* __restrict__ seq_lens,
+                    int max_pages, int B, int H_q, int H_kv, int k, uint16_t* __restrict__ out,
+                    float* __restrict__ lse) {
+  constexpr int PER = D / 32;
+  constexpr unsigned kAll = 0xffffffffu;
   const int lane = threadIdx.x & 31;
   const int G = H_q / H_kv;
   const int64_t n = (int64_t)B * H_q;
   for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < n;
        w += ((int64_t)gridDim.x * blockDim.x) >> 5) {
     const int s = (int)(w / H_q), h = (int)(w % H_q);
-    const int32_t* id = ids + ((size_t)s * H_kv + h / G) * k;
-    const float* pl = part_lse + (size_t)w * k;
+    const float* po = part_o + (size_t)w * k * D + lane * PER;
+    float x[kMaxK][PER];
+#pragma unroll
+    for (int sl = 0; sl < kMaxK; ++sl) {
+      if (sl < k) {
+        if constexpr (PER == 4) {
+          const float4 t = __ldcs(reinterpret_cast<const float4*>(po + (size_t)sl * D));
+          x[sl][0] = t.x; x[sl][1] = t.y; x[sl][2] = t.z; x[sl][3] = t.w;
+        } else {
+          const float2 t = __ldcs(reinterpret_cast<const float2*>(po + (size_t)sl * D));
+          x[sl][0] = t.x; x[sl][1] = t.y;
+        }
+      }
+    }
     const int L = seq_lens[s];
     const int lim = (L < 1 || L > max_pages * kBk) ? -1 : (L - 1) / kBk;  // valid ids: 0..lim
-    float M = -INFINITY;
-    for (int i = 0; i < k; ++i)
-      if (id[i] >= 0 && id[i] <= lim) M = fmaxf(M, pl[i]);
-    float acc[D / 32];
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
-    float Lsum = 0.f;
-    for (int sl = 0; sl < k; ++sl) {
-      if (id[sl] < 0 || id[sl] > lim) continue;
-      float wgt = __expf(pl[sl] - M);
-      Lsum += wgt;
-      const float* po = part_o + ((size_t)w * k + sl) * D;
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(wgt, po[lane + 32 * i], acc[i]);
+    bool valid = false;
+    float li = -INFINITY;
+    if (lane < k) {
+      const int b = ids[((size_t)s * H_kv + h / G) * k + lane];
+      const float l_raw = part_lse[(size_t)w * k + lane];
+      valid = b >= 0 && b <= lim;
+      li = valid ? l_raw : -INFINITY;
     }
-    float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    float M = li;
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) {
-      __nv_bfloat16 bv = __float2bfloat16_rn(acc[i] * inv);
-      out[(size_t)w * D + lane + 32 * i] = *reinterpret_cast<uint16_t*>(&bv);
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(kAll, M, off));
+    const float wgt = valid ? __expf(li - M) : 0.f;
+    float Lsum = wgt;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(kAll, Lsum, off);
+    float acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int sl = 0; sl < kMaxK; ++sl) {
+      const float ws = __shfl_sync(kAll, wgt, sl);
+      if (sl < k && ws != 0.f) {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[i] = fmaf(ws, x[sl][i], acc[i]);
+      }
+    }
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    uint16_t o16[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const __nv_bfloat16 bv = __float2bfloat16_rn(acc[i] * inv);
+      o16[i] = *reinterpret_cast<const uint16_t*>(&bv);
+    }
+    uint16_t* op = out + (size_t)w * D + lane * PER;
+    if constexpr (PER == 4) {
+      *reinterpret_cast<uint2*>(op) = make_uint2(o16[0] | ((uint32_t)o16[1] << 16),
+                                                 o16[2] | ((uint32_t)o16[3] << 16));
+    } else {
+      *reinterpret_cast<uint32_t*>(op) = o16[0] | ((uint32_t)o16[1] << 16);
     }
     if (lse && lane == 0) lse[w] = M + logf(Lsum);
   }
