@@ -40,50 +40,29 @@ __device__ __forceinline__ uint64_t rank_key(float score, uint32_t id) {
 __device__ __forceinline__ int key_id(uint64_t key) { return (int)(0xFFFFFFFFu - (uint32_t)key); }
 
 // ------------------------------------------------------- per-row streaming top-k
-// Keeps the `kfar` (<= 15) best blocks offered so far, in registers. Blocks must
-// be offered in increasing id order, so a later block with a score equal to the
-// current worst kept one never replaces it (the lower id wins).
+// Keeps the `kfar` (<= 15) best blocks offered so far, in registers, sorted
+// descending in the last kfar slots, so the worst kept key is always the last
+// slot. The slots before them hold all-ones keys that nothing displaces, and a
+// kept slot not yet filled holds 0, below every real key. An offered key is
+// compared with every slot at once and the slots from its place on shift down
+// by one, which keeps the dependent chain of an insertion a few instructions
+// long. Keys carry the tie-break (the lower id has the larger key).
 struct RowTopK {
   uint64_t key[kMaxFar];
-  uint64_t worst;
-  int worst_slot;
-  int count;
-  int kfar;
 
   __device__ __forceinline__ void init(int kf) {
-    kfar = kf;
-    count = 0;
-    worst = 0;
-    worst_slot = 0;
 #pragma unroll
-    for (int i = 0; i < kMaxFar; ++i) key[i] = 0;
+    for (int i = 0; i < kMaxFar; ++i) key[i] = i < kMaxFar - kf ? ~0ull : 0ull;
   }
-  __device__ __forceinline__ void recompute() {
-    uint64_t w = ~0ull;
-    int ws = 0;
-#pragma unroll
-    for (int i = 0; i < kMaxFar; ++i)
-      if (i < kfar && key[i] < w) { w = key[i]; ws = i; }
-    worst = w;
-    worst_slot = ws;
-  }
-  __device__ __forceinline__ void put(int slot, uint64_t k) {
-#pragma unroll
-    for (int i = 0; i < kMaxFar; ++i)
-      if (i == slot) key[i] = k;
-  }
-  // Cheap pre-test for the hot loop: can this score enter at all?
-  __device__ __forceinline__ bool wants(uint64_t k) const { return count < kfar || k > worst; }
+  // Cheap pre-test for the hot loop: can this key enter at all?
+  __device__ __forceinline__ bool wants(uint64_t k) const { return k > key[kMaxFar - 1]; }
   __device__ __forceinline__ void offer(uint64_t k) {
-    if (count < kfar) {
-      put(count, k);
-      ++count;
-      if (count == kfar) recompute();
-      return;
-    }
-    if (kfar == 0 || k <= worst) return;
-    put(worst_slot, k);
-    recompute();
+    bool gt[kMaxFar];
+#pragma unroll
+    for (int i = 0; i < kMaxFar; ++i) gt[i] = k > key[i];
+#pragma unroll
+    for (int i = kMaxFar - 1; i >= 0; --i)  // key[i - 1] is still the old value here
+      key[i] = gt[i] ? ((i > 0 && gt[i - 1]) ? key[i - 1] : k) : key[i];
   }
   // Writes the kept blocks plus `local`, ascending, padded with -1, to out[0..k).
   __device__ __forceinline__ void emit(int local, int k, int32_t* out) const {
@@ -92,7 +71,7 @@ struct RowTopK {
     for (int i = 0; i < kMaxK; ++i) v[i] = 0x7FFFFFFF;
 #pragma unroll
     for (int i = 0; i < kMaxFar; ++i)
-      if (i < count) v[i] = key_id(key[i]);
+      if (key[i] != 0 && key[i] != ~0ull) v[i] = key_id(key[i]);
     v[kMaxK - 1] = local;
     // odd-even transposition sort, fully unrolled (16 elements, 16 rounds)
 #pragma unroll
