@@ -41,37 +41,43 @@ __device__ __forceinline__ int key_id(uint64_t key) { return (int)(0xFFFFFFFFu -
 
 // ------------------------------------------------------- per-row streaming top-k
 // Keeps the `kfar` (<= 15) best blocks offered so far, in registers, sorted
-// descending in the last kfar slots, so the worst kept key is always the last
-// slot. The slots before them hold all-ones keys that nothing displaces, and a
-// kept slot not yet filled holds 0, below every real key. An offered key is
-// compared with every slot at once and the slots from its place on shift down
-// by one, which keeps the dependent chain of an insertion a few instructions
-// long. Keys carry the tie-break (the lower id has the larger key).
+// descending by score in the last kfar slots, so the worst kept score is always
+// the last slot. The slots before them hold +inf, which nothing displaces, and
+// a kept slot not yet filled holds -inf (id -1). An offered block is compared
+// with every slot at once and the slots from its place on shift down by one,
+// which keeps the dependent chain of an insertion a few instructions long.
+// Blocks must be offered in increasing id order: the comparisons are strict,
+// so of two equal scores the earlier (lower) id stays ahead, and a later block
+// whose score equals the worst kept one does not enter.
 struct RowTopK {
-  uint64_t key[kMaxFar];
+  float val[kMaxFar];
+  int32_t id[kMaxFar];
 
   __device__ __forceinline__ void init(int kf) {
 #pragma unroll
-    for (int i = 0; i < kMaxFar; ++i) key[i] = i < kMaxFar - kf ? ~0ull : 0ull;
+    for (int i = 0; i < kMaxFar; ++i) {
+      val[i] = i < kMaxFar - kf ? INFINITY : -INFINITY;
+      id[i] = -1;
+    }
   }
-  // Cheap pre-test for the hot loop: can this key enter at all?
-  __device__ __forceinline__ bool wants(uint64_t k) const { return k > key[kMaxFar - 1]; }
-  __device__ __forceinline__ void offer(uint64_t k) {
+  // Cheap pre-test for the hot loop: can this score enter at all?
+  __device__ __forceinline__ bool wants(float v) const { return v > val[kMaxFar - 1]; }
+  __device__ __forceinline__ void offer(float v, int32_t b) {
     bool gt[kMaxFar];
 #pragma unroll
-    for (int i = 0; i < kMaxFar; ++i) gt[i] = k > key[i];
+    for (int i = 0; i < kMaxFar; ++i) gt[i] = v > val[i];
 #pragma unroll
-    for (int i = kMaxFar - 1; i >= 0; --i)  // key[i - 1] is still the old value here
-      key[i] = gt[i] ? ((i > 0 && gt[i - 1]) ? key[i - 1] : k) : key[i];
+    for (int i = kMaxFar - 1; i >= 0; --i) {  // slot i - 1 still holds its old entry here
+      const bool from_prev = i > 0 && gt[i - 1];
+      val[i] = gt[i] ? (from_prev ? val[i - 1] : v) : val[i];
+      id[i] = gt[i] ? (from_prev ? id[i - 1] : b) : id[i];
+    }
   }
   // Writes the kept blocks plus `local`, ascending, padded with -1, to out[0..k).
   __device__ __forceinline__ void emit(int local, int k, int32_t* out) const {
     int v[kMaxK];
 #pragma unroll
-    for (int i = 0; i < kMaxK; ++i) v[i] = 0x7FFFFFFF;
-#pragma unroll
-    for (int i = 0; i < kMaxFar; ++i)
-      if (key[i] != 0 && key[i] != ~0ull) v[i] = key_id(key[i]);
+    for (int i = 0; i < kMaxFar; ++i) v[i] = id[i] >= 0 ? id[i] : 0x7FFFFFFF;
     v[kMaxK - 1] = local;
     // odd-even transposition sort, fully unrolled (16 elements, 16 rounds)
 #pragma unroll

@@ -349,10 +349,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (lane == 0) mbar_arrive(&t_empty[acc]);
         if (valid && b <= loc) {
           if (want_scores) block_scores[r * nb + b] = F8 ? m * score_scale : m;
-          if (b < loc) {
-            const uint64_t key = rank_key(m, (uint32_t)b);
-            if (top.wants(key)) top.offer(key);
-          }
+          if (b < loc && top.wants(m)) top.offer(m, (int32_t)b);
         }
       }
       if (ok && valid) top.emit((int)loc, k, block_ids + r * k);
