@@ -27,11 +27,13 @@ __device__ __forceinline__ void report(const Diag& dg, int code) {
 // ---------------------------------------------------------------- ranking keys
 // A block is ranked by the 64-bit key (order-preserving bits of its fp32 score,
 // ~block id): a larger key is a better block, and among equal scores the lower
-// id has the larger key ("lower id wins"). NaN maps below -inf. Key 0 means
-// "empty slot" and is below every real key.
+// id has the larger key ("lower id wins"). -0 ranks as +0 (the two scores are
+// equal), NaN maps below -inf. Key 0 means "empty slot" and is below every real
+// key.
 __device__ __forceinline__ uint32_t ord_f32(float f) {
   uint32_t b = __float_as_uint(f);
   if ((b & 0x7FFFFFFFu) > 0x7F800000u) return 0u;  // NaN
+  if (b == 0x80000000u) b = 0u;                     // -0 -> +0
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 __device__ __forceinline__ uint64_t rank_key(float score, uint32_t id) {

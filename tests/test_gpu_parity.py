@@ -198,13 +198,15 @@ def test_index_select_gauss_32k(msa):
     (2048, 8, 16, 16, 0, "gauss"), (4096, 4, 1024, 16, 120 * 1024, "gauss"),
     (1000, 2, 1023, 16, 129000, "int"), (700, 3, 3000, 7, 383000, "gauss"),
     (512, 2, 1024, 16, 130000, "const"), (300, 8, 40, 1, 4800, "int"),
-    (256, 1, 4096, 2, 500000, "int")])
+    (256, 1, 4096, 2, 500000, "int"), (640, 2, 1024, 16, 120000, "zeros")])
 def test_topk_standalone_exact(msa, N, n_g, nb, k, q_offset, kind):
     rng = np.random.default_rng(N + nb + k)
     if kind == "gauss":
         S = rng.standard_normal((N, n_g, nb)).astype(np.float32)
     elif kind == "int":
         S = rng.integers(-3, 4, (N, n_g, nb)).astype(np.float32)  # many exact ties
+    elif kind == "zeros":  # -0 and +0 are equal scores: only the block id may separate them
+        S = rng.choice(np.array([-0.0, 0.0, -1.0], dtype=np.float32), (N, n_g, nb))
     else:
         S = np.full((N, n_g, nb), 2.5, dtype=np.float32)  # every candidate tied
     rows = np.arange(N) + q_offset
