@@ -297,20 +297,21 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int q = warp & 3;             // TMEM lane quarter this warp may access
     const int h = (warp - 2) >> 2;      // accumulator half (rows h*128 ..)
     const int row_in_tile = h * 128 + q * 32 + lane;
-    long long it = 0;
+    uint32_t it = 0;  // key blocks of this CTA so far (all tiles)
     bool ok = true;
     for (int rd = 0; rd < rounds && ok; ++rd) {
       TileRef tr;
       if (!tile_of(rd, tr)) continue;
-      const int64_t nkb = key_blocks(tr);
-      const int64_t lr = tr.lrow0 + row_in_tile;  // row within the sequence
-      const int64_t r = tr.row0 + row_in_tile;    // row within the packed batch
+      // row and position indexes fit 32 bits (the host caps rows x groups below 2^31)
+      const int nkb = (int)key_blocks(tr);
+      const int lr = (int)(tr.lrow0 + row_in_tile);  // row within the sequence
+      const int r = (int)(tr.row0 + row_in_tile);    // row within the packed batch
       const bool valid = lr < tr.rows;
-      const int64_t t = valid ? tr.q_off + lr / n_g : 0;  // the query's position
-      const int64_t loc = t / kKeys;
+      const int t = valid ? (int)tr.q_off + lr / n_g : 0;  // the query's position
+      const int loc = t / kKeys;
       RowTopK top;
       top.init(k - 1);
-      for (int64_t b = 0; b < nkb; ++b, ++it) {
+      for (int b = 0; b < nkb; ++b, ++it) {
         const int acc = (int)(it & 1);
         const uint32_t tpar = (uint32_t)((it >> 1) & 1);
         // one lane waits, the warp follows (tcgen05.ld needs a converged warp)
@@ -321,7 +322,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256 + h * 128);
         // visible columns of this row in block b: all, or up to t on the diagonal
-        const int lim = (b < loc) ? 128 : (b == loc ? (int)(t - b * kKeys) + 1 : 0);
+        const int lim = (b < loc) ? 128 : (b == loc ? t - b * kKeys + 1 : 0);
         // with every column visible to every row of the warp the loads reduce
         // (sm_103 load-with-max); the diagonal block reduces in registers
         const bool full = __all_sync(0xffffffffu, lim >= kKeys);
@@ -348,11 +349,11 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         __syncwarp();
         if (lane == 0) mbar_arrive(&t_empty[acc]);
         if (valid && b <= loc) {
-          if (want_scores) block_scores[r * nb + b] = F8 ? m * score_scale : m;
-          if (b < loc && top.wants(m)) top.offer(m, (int32_t)b);
+          if (want_scores) block_scores[(int64_t)r * nb + b] = F8 ? m * score_scale : m;
+          if (b < loc && top.wants(m)) top.offer(m, b);
         }
       }
-      if (ok && valid) top.emit((int)loc, k, block_ids + r * k);
+      if (ok && valid) top.emit(loc, k, block_ids + (int64_t)r * k);
     }
   }
   tc_fence_before();
