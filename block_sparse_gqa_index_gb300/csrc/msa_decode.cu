@@ -330,7 +330,7 @@ constexpr int dec_smem_bytes() {
 }
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(128, FP8 ? 4 : 3)
+__global__ void __launch_bounds__(128, FP8 ? 6 : 3)
 decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
                    const void* __restrict__ vp, const float* __restrict__ k_scale,
                    const float* __restrict__ v_scale, const int32_t* __restrict__ page_table,
