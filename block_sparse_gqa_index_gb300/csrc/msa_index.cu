@@ -242,7 +242,9 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           armed_par[s] = par;
         }
       }
-      if (!ok) {  // let every issued copy land before shared memory is released
+      // let every issued copy land before shared memory is released, also when
+      // another role gave up after this one had issued all of its copies
+      if (!ok || *abort_flag) {
         for (int s = 0; s < kStages; ++s)
           if (armed[s]) mbar_drain(&b_full[s], armed_par[s]);
         if (a_armed) mbar_drain(a_full, a_par ^ 1);
