@@ -108,6 +108,17 @@ template <bool VEC>
 __device__ __forceinline__ void load_chunk(float (&v)[32], const float* __restrict__ p, int rem,
                                            int hl) {
   const float nan = __int_as_float(0x7fffffff);
+  if (VEC && rem >= kHalf) {  // a whole chunk: no masking
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 x = __ldcs(reinterpret_cast<const float4*>(p + i * 64 + hl * 4));
+      v[4 * i + 0] = x.x;
+      v[4 * i + 1] = x.y;
+      v[4 * i + 2] = x.z;
+      v[4 * i + 3] = x.w;
+    }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int o = i * 64 + hl * 4;
