@@ -125,12 +125,13 @@ __device__ __forceinline__ void load_chunk(float (&v)[32], const float* __restri
     float4 x = make_float4(nan, nan, nan, nan);
     if (o < rem) {
       if constexpr (VEC) {
+        // the whole vector is in the row (rows hold a multiple of 4 scores);
+        // the blocks past the candidates are masked by selects, not branches
         x = __ldcs(reinterpret_cast<const float4*>(p + o));
-        if (o + 4 > rem) {  // ragged end: mask the blocks past the candidates
-          if (o + 1 >= rem) x.y = nan;
-          if (o + 2 >= rem) x.z = nan;
-          x.w = nan;
-        }
+        const int nv = rem - o;
+        x.y = nv > 1 ? x.y : nan;
+        x.z = nv > 2 ? x.z : nan;
+        x.w = nv > 3 ? x.w : nan;
       } else {
         x.x = p[o];
         if (o + 1 < rem) x.y = p[o + 1];
@@ -148,9 +149,9 @@ __device__ __forceinline__ void load_chunk(float (&v)[32], const float* __restri
 // Row cursor of one half: row r = q * n_g + g walks by a fixed stride, and its
 // query index q follows without a division per step.
 struct RowCursor {
-  int64_t r;
-  int q, rm;  // r / n_g, r % n_g
-  __device__ __forceinline__ void step(int64_t stride, int sq, int sr, int n_g) {
+  uint32_t r;  // rows number at most INT_MAX, so r + stride stays below 2^32
+  int q, rm;   // r / n_g, r % n_g
+  __device__ __forceinline__ void step(uint32_t stride, int sq, int sr, int n_g) {
     r += stride;
     q += sq;
     rm += sr;
@@ -163,19 +164,19 @@ struct RowCursor {
 
 // Local block of the cursor's row (its query's position / Bk), or -1 when that
 // position lies outside the score rows.
-__device__ __forceinline__ int64_t row_loc(const RowCursor& c, int Bk, int bk_shift, int64_t nb,
-                                           int64_t q_offset, const int32_t* __restrict__ seq_lens) {
+__device__ __forceinline__ int row_loc(const RowCursor& c, int Bk, int bk_shift, int64_t nb,
+                                       int64_t q_offset, const int32_t* __restrict__ seq_lens) {
   const int64_t pos = seq_lens ? (int64_t)seq_lens[c.q] - 1 : c.q + q_offset;
   if (pos < 0) return -1;
   const int64_t loc = bk_shift >= 0 ? pos >> bk_shift : pos / Bk;
-  return loc < nb ? loc : -1;
+  return loc < nb ? (int)loc : -1;
 }
 
 // Ranks each half's staged chunk (sv) into the kfar best keys the half kept so
 // far (best: half-lane i < kfar holds the i-th best, descending). m0, m1: the
 // lane's two group maxima.
 __device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1, uint64_t* buf,
-                                           int64_t c0, int kfar, int hl, uint64_t& best,
+                                           int c0, int kfar, int hl, uint64_t& best,
                                            float& best_min) {
   // threshold: the kfar-th largest group max (>= kfar values reach it) or the
   // worst value kept so far, whichever is larger
@@ -264,7 +265,8 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
   const int wid = threadIdx.x >> 5;
   const int half = lane >> 4, hl = lane & 15;
   const int kfar = k - 1;
-  const int64_t stride = (int64_t)gridDim.x * kWarps * 2;  // rows per sweep (one per half)
+  const uint32_t stride = gridDim.x * kWarps * 2;  // rows per sweep (one per half)
+  const uint32_t rows = (uint32_t)n_rows;           // at most INT_MAX (host check)
   const int sq = (int)(stride / n_g), sr = (int)(stride % n_g);
   float4* sv = sval[wid][half];
   uint64_t* bf = buf[wid][half];
@@ -273,10 +275,10 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
   // that need none (position outside the score rows, or no more candidates than
   // far slots) are written on the way by this half. loc_out: that row's local
   // block. The cursor ends at n_rows or beyond when there is none.
-  auto seek = [&](RowCursor& c, int64_t& loc_out) {
-    for (; c.r < n_rows; c.step(stride, sq, sr, n_g)) {
-      const int64_t loc = row_loc(c, Bk, bk_shift, nb, q_offset, seq_lens);
-      int32_t* out = ids + c.r * k;
+  auto seek = [&](RowCursor& c, int& loc_out) {
+    for (; c.r < rows; c.step(stride, sq, sr, n_g)) {
+      const int loc = row_loc(c, Bk, bk_shift, nb, q_offset, seq_lens);
+      int32_t* out = ids + (int64_t)c.r * k;
       if (loc < 0) {  // flag, emit padding
         if (hl == 0) report(dg, kStatusBadIds);
         if (hl < k) out[hl] = -1;
@@ -292,18 +294,18 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
   };
 
   RowCursor cur;
-  cur.r = ((int64_t)blockIdx.x * kWarps + wid) * 2 + half;
+  cur.r = (blockIdx.x * kWarps + wid) * 2 + half;
   cur.q = (int)(cur.r / n_g);
   cur.rm = (int)(cur.r % n_g);
-  int64_t loc = 0, c0 = 0;
+  int loc = 0, c0 = 0;
   seek(cur, loc);
   float vn[32];
-  load_chunk<VEC>(vn, S + (cur.r < n_rows ? cur.r * nb : 0),
-                  cur.r < n_rows ? (int)min(loc, (int64_t)kHalf) : 0, hl);
+  load_chunk<VEC>(vn, S + (cur.r < rows ? (int64_t)cur.r * nb : 0),
+                  cur.r < rows ? min(loc, kHalf) : 0, hl);
   uint64_t best = 0;           // half-lane i < kfar: i-th best key so far, else 0
   float best_min = -INFINITY;  // value of the kfar-th best so far (-inf before any chunk)
-  while (__any_sync(kAll, cur.r < n_rows)) {
-    const bool act = cur.r < n_rows;
+  while (__any_sync(kAll, cur.r < rows)) {
+    const bool act = cur.r < rows;
     // stage the chunk; group maxima over the lane's even and odd blocks (so a
     // short row's few candidates still give two maxima per lane)
     float m0 = -INFINITY, m1 = -INFINITY;
@@ -315,22 +317,22 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
     }
     // the half's next work item: this row's next chunk, else its next row's first
     RowCursor nxt = cur;
-    int64_t c2 = c0 + kHalf, loc2 = loc;
+    int c2 = c0 + kHalf, loc2 = loc;
     if (act && c2 >= loc) {
       nxt.step(stride, sq, sr, n_g);
       seek(nxt, loc2);
       c2 = 0;
     }
-    const bool act2 = nxt.r < n_rows;
-    load_chunk<VEC>(vn, S + (act2 ? nxt.r * nb + c2 : 0),
-                    act2 ? (int)min(loc2 - c2, (int64_t)kHalf) : 0, hl);
+    const bool act2 = nxt.r < rows;
+    load_chunk<VEC>(vn, S + (act2 ? (int64_t)nxt.r * nb + c2 : 0),
+                    act2 ? min(loc2 - c2, kHalf) : 0, hl);
     rank_chunk(sv, m0, m1, bf, c0, kfar, hl, best, best_min);
     const bool done = act && c0 + kHalf >= loc;
     if (__any_sync(kAll, done)) {  // kept ids plus the local block, ascending
-      int id = hl < kfar ? (best ? key_id(best) : INT_MAX) : (hl == kfar ? (int)loc : INT_MAX);
+      int id = hl < kfar ? (best ? key_id(best) : INT_MAX) : (hl == kfar ? loc : INT_MAX);
       id = sort16h_asc(id, hl);
       if (done) {
-        if (hl < k) ids[cur.r * k + hl] = id == INT_MAX ? -1 : id;
+        if (hl < k) ids[(int64_t)cur.r * k + hl] = id == INT_MAX ? -1 : id;
         best = 0;
         best_min = -INFINITY;
       }
