@@ -255,7 +255,7 @@ __device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1,
 }
 
 template <bool VEC>
-__global__ void __launch_bounds__(kWarps * 32, 5)
+__global__ void __launch_bounds__(kWarps * 32, 6)
 topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, int Bk,
             int bk_shift, int k, int64_t q_offset, const int32_t* __restrict__ seq_lens,
             int32_t* __restrict__ ids, Diag dg) {
