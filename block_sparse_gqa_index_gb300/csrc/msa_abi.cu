@@ -426,9 +426,13 @@ int msa_sparse_attn_paged(const void* q, const void* k_pages, const void* v_page
                     workspace_bytes, stream);
 }
 
+// Rows of the decode block scores kept in the workspace start on 16-byte
+// boundaries (a multiple of four floats), so the top-k reads them as vectors.
+static int64_t decode_score_stride(int max_pages) { return ((int64_t)max_pages + 3) & ~(int64_t)3; }
+
 size_t msa_index_select_decode_workspace_bytes(int B, int max_pages, int n_groups) {
   if (B < 0 || max_pages < 0 || n_groups < 0) return 0;
-  return (size_t)B * max_pages * n_groups * sizeof(float);
+  return (size_t)B * decode_score_stride(max_pages) * n_groups * sizeof(float);
 }
 
 static int index_decode(const void* q_idx, const void* k_idx_pages, const int32_t* page_table,
@@ -445,20 +449,23 @@ static int index_decode(const void* q_idx, const void* k_idx_pages, const int32_
   if (Bk != 128 || !supported_k(k) || !supported_d(d_idx) || n_groups > 8)
     return MSA_ERR_UNSUPPORTED;
   float* scores = block_scores;
+  int64_t ss = max_pages;  // caller's block_scores: [B, n_groups, max_pages]
   if (!scores) {
     if (!workspace || workspace_bytes < msa_index_select_decode_workspace_bytes(B, max_pages,
                                                                                 n_groups))
       return MSA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return MSA_ERR_INVALID_ARG;
     scores = (float*)workspace;
+    ss = decode_score_stride(max_pages);
   }
   cudaStream_t st = (cudaStream_t)stream;
   msa::Diag dg = diag();
   cudaError_t e = msa::launch_decode_index(q_idx, k_idx_pages, page_table, seq_lens, B,
                                            max_pages, n_groups, d_idx, scores, dg, st, e4m3,
-                                           score_scale);
+                                           score_scale, ss);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_topk(scores, B, n_groups, max_pages, Bk, k, 0, seq_lens, block_ids, dg, st);
+  e = msa::launch_topk(scores, B, n_groups, max_pages, Bk, k, 0, seq_lens, block_ids, dg, st,
+                       ss);
   return status_of(e);
 }
 
@@ -499,20 +506,23 @@ int msa_index_select_decode_nvfp4(const void* q_idx, const void* k_idx_codes,
   if (Bk != 128 || !supported_k(k) || !supported_d(d_idx) || n_groups > 8)
     return MSA_ERR_UNSUPPORTED;
   float* scores = block_scores;
+  int64_t ss = max_pages;  // caller's block_scores: [B, n_groups, max_pages]
   if (!scores) {
     if (!workspace || workspace_bytes < msa_index_select_decode_workspace_bytes(B, max_pages,
                                                                                 n_groups))
       return MSA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return MSA_ERR_INVALID_ARG;
     scores = (float*)workspace;
+    ss = decode_score_stride(max_pages);
   }
   cudaStream_t st = (cudaStream_t)stream;
   msa::Diag dg = diag();
   cudaError_t e = msa::launch_decode_index_fp4(q_idx, k_idx_codes, k_idx_scales, page_table,
                                                seq_lens, B, max_pages, n_groups, d_idx,
-                                               score_scale, scores, dg, st);
+                                               score_scale, scores, dg, st, ss);
   if (e != cudaSuccess) return MSA_ERR_CUDA;
-  e = msa::launch_topk(scores, B, n_groups, max_pages, Bk, k, 0, seq_lens, block_ids, dg, st);
+  e = msa::launch_topk(scores, B, n_groups, max_pages, Bk, k, 0, seq_lens, block_ids, dg, st,
+                       ss);
   return status_of(e);
 }
 

@@ -60,7 +60,7 @@ decode_index_kernel(const unsigned char* __restrict__ q_idx,
                     const unsigned char* __restrict__ kpages,
                     const int32_t* __restrict__ page_table, const int32_t* __restrict__ seq_lens,
                     int B, int max_pages, int n_g, float out_scale, float* __restrict__ scores,
-                    Diag dg) {
+                    int64_t ss, Diag dg) {
   constexpr int RB = DI * (F8 ? 1 : 2);  // bytes of one key row
   constexpr int NC = RB / 64;            // 16-byte chunks per thread per key row
   const int lane = threadIdx.x & 31;
@@ -118,8 +118,8 @@ decode_index_kernel(const unsigned char* __restrict__ q_idx,
     }
     if (gq == 0) {
       int g0 = 2 * t4, g1 = 2 * t4 + 1;
-      if (g0 < n_g) scores[((size_t)s * n_g + g0) * max_pages + b] = F8 ? mx0 * out_scale : mx0;
-      if (g1 < n_g) scores[((size_t)s * n_g + g1) * max_pages + b] = F8 ? mx1 * out_scale : mx1;
+      if (g0 < n_g) scores[((size_t)s * n_g + g0) * ss + b] = F8 ? mx0 * out_scale : mx0;
+      if (g1 < n_g) scores[((size_t)s * n_g + g1) * ss + b] = F8 ? mx1 * out_scale : mx1;
     }
   }
 }
@@ -237,7 +237,7 @@ decode_index_fp4_kernel(const uint16_t* __restrict__ q_idx, const unsigned char*
                         const unsigned char* __restrict__ kscales,
                         const int32_t* __restrict__ page_table,
                         const int32_t* __restrict__ seq_lens, int B, int max_pages, int n_g,
-                        float out_scale, float* __restrict__ scores, Diag dg) {
+                        float out_scale, float* __restrict__ scores, int64_t srow, Diag dg) {
   constexpr int CB = DI / 2;    // code bytes per key
   constexpr int SB = DI / 16;   // scale bytes per key
   constexpr int KS = DI / 16;   // micro-blocks = k-steps
@@ -318,8 +318,8 @@ decode_index_fp4_kernel(const uint16_t* __restrict__ q_idx, const unsigned char*
     }
     if (gq == 0) {
       const int g0 = 2 * t4, g1 = 2 * t4 + 1;
-      if (g0 < n_g) scores[((size_t)s * n_g + g0) * max_pages + b] = mx0 * out_scale;
-      if (g1 < n_g) scores[((size_t)s * n_g + g1) * max_pages + b] = mx1 * out_scale;
+      if (g0 < n_g) scores[((size_t)s * n_g + g0) * srow + b] = mx0 * out_scale;
+      if (g1 < n_g) scores[((size_t)s * n_g + g1) * srow + b] = mx1 * out_scale;
     }
   }
 }
@@ -605,7 +605,9 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,
                                 const int32_t* page_table, const int32_t* seq_lens, int B,
                                 int max_pages, int n_g, int d_idx, float* scores,
-                                const Diag& dg, cudaStream_t st, bool e4m3, float score_scale) {
+                                const Diag& dg, cudaStream_t st, bool e4m3, float score_scale,
+                                int64_t ss) {
+  if (ss <= 0) ss = max_pages;
   int64_t warps = (int64_t)B * max_pages;
   if (warps == 0) return cudaSuccess;
   note_launches(1);
@@ -614,7 +616,7 @@ cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,
   auto kp = (const unsigned char*)k_idx_pages;
 #define MSA_DEC_INDEX(DI, F8)                                                                 \
   decode_index_kernel<DI, F8><<<grid, 256, 0, st>>>(q, kp, page_table, seq_lens, B, max_pages, \
-                                                    n_g, score_scale, scores, dg)
+                                                    n_g, score_scale, scores, ss, dg)
   if (e4m3) {
     if (d_idx == 128) MSA_DEC_INDEX(128, true);
     else MSA_DEC_INDEX(64, true);
@@ -629,7 +631,8 @@ cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,
 cudaError_t launch_decode_index_fp4(const void* q_idx, const void* codes, const void* kscales,
                                     const int32_t* page_table, const int32_t* seq_lens, int B,
                                     int max_pages, int n_g, int d_idx, float score_scale,
-                                    float* scores, const Diag& dg, cudaStream_t st) {
+                                    float* scores, const Diag& dg, cudaStream_t st, int64_t ss) {
+  if (ss <= 0) ss = max_pages;
   const int64_t tasks = (int64_t)B * max_pages;
   if (tasks == 0) return cudaSuccess;
   note_launches(1);
@@ -645,13 +648,13 @@ cudaError_t launch_decode_index_fp4(const void* q_idx, const void* codes, const 
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     decode_index_fp4_kernel<128><<<grid, kFp4Warps * 32, smem, st>>>(
-        q, c, sc, page_table, seq_lens, B, max_pages, n_g, score_scale, scores, dg);
+        q, c, sc, page_table, seq_lens, B, max_pages, n_g, score_scale, scores, ss, dg);
   } else {
     e = cudaFuncSetAttribute(decode_index_fp4_kernel<64>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     decode_index_fp4_kernel<64><<<grid, kFp4Warps * 32, smem, st>>>(
-        q, c, sc, page_table, seq_lens, B, max_pages, n_g, score_scale, scores, dg);
+        q, c, sc, page_table, seq_lens, B, max_pages, n_g, score_scale, scores, ss, dg);
   }
   return cudaGetLastError();
 }

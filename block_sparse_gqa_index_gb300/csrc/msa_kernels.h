@@ -40,9 +40,10 @@ cudaError_t launch_index_select_paged(const void* q_idx, const void* k_idx_pages
                                       cudaStream_t st);
 
 // Exp-free top-k over block scores (msa_topk.cu).
+// ld: row stride of S in floats (0: nb); rows are read at S + r * ld.
 cudaError_t launch_topk(const float* S, int64_t N, int n_g, int64_t nb, int Bk, int k,
                         int64_t q_offset, const int32_t* seq_lens, int32_t* ids, const Diag& dg,
-                        cudaStream_t st);
+                        cudaStream_t st, int64_t ld = 0);
 
 // Main branch, prefill (msa_attn.cu).
 struct AttnWs {
@@ -124,19 +125,20 @@ cudaError_t launch_batch_info(const BatchSeqs& tb, const int32_t* page_table, in
 
 // Decode (msa_decode.cu).
 // e4m3: q_idx and the k_idx pages hold E4M3 codes, and the block scores are
-// written times score_scale
+// written times score_scale. ss: row stride of scores in floats (0: max_pages).
 cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,
                                 const int32_t* page_table, const int32_t* seq_lens, int B,
                                 int max_pages, int n_g, int d_idx, float* scores,
                                 const Diag& dg, cudaStream_t st, bool e4m3 = false,
-                                float score_scale = 1.f);
+                                float score_scale = 1.f, int64_t ss = 0);
 // NVFP4 k_idx cache: codes [P, 128, d_idx / 2] (two E2M1 per byte, even
 // dimension low), kscales [P, 128, d_idx / 16] E4M3 micro-block scales;
 // q_idx bf16. Scores written times score_scale.
 cudaError_t launch_decode_index_fp4(const void* q_idx, const void* codes, const void* kscales,
                                     const int32_t* page_table, const int32_t* seq_lens, int B,
                                     int max_pages, int n_g, int d_idx, float score_scale,
-                                    float* scores, const Diag& dg, cudaStream_t st);
+                                    float* scores, const Diag& dg, cudaStream_t st,
+                                    int64_t ss = 0);
 size_t decode_ws_bytes(int B, int H_q, int d, int k);
 cudaError_t launch_decode_attn(const void* q, const void* k_pages, const void* v_pages,
                                int kv_fp8, const float* k_scale, const float* v_scale,

@@ -256,7 +256,7 @@ __device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1,
 
 template <bool VEC>
 __global__ void __launch_bounds__(kWarps * 32, 6)
-topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, int Bk,
+topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, int64_t ld, int Bk,
             int bk_shift, int k, int64_t q_offset, const int32_t* __restrict__ seq_lens,
             int32_t* __restrict__ ids, Diag dg) {
   __shared__ uint64_t buf[kWarps][2][kCap + 1];  // +1: the halves on different banks
@@ -300,7 +300,7 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
   int loc = 0, c0 = 0;
   seek(cur, loc);
   float vn[32];
-  load_chunk<VEC>(vn, S + (cur.r < rows ? (int64_t)cur.r * nb : 0),
+  load_chunk<VEC>(vn, S + (cur.r < rows ? (int64_t)cur.r * ld : 0),
                   cur.r < rows ? min(loc, kHalf) : 0, hl);
   uint64_t best = 0;           // half-lane i < kfar: i-th best key so far, else 0
   float best_min = -INFINITY;  // value of the kfar-th best so far (-inf before any chunk)
@@ -324,7 +324,7 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
       c2 = 0;
     }
     const bool act2 = nxt.r < rows;
-    load_chunk<VEC>(vn, S + (act2 ? (int64_t)nxt.r * nb + c2 : 0),
+    load_chunk<VEC>(vn, S + (act2 ? (int64_t)nxt.r * ld + c2 : 0),
                     act2 ? min(loc2 - c2, kHalf) : 0, hl);
     rank_chunk(sv, m0, m1, bf, c0, kfar, hl, best, best_min);
     const bool done = act && c0 + kHalf >= loc;
@@ -357,7 +357,8 @@ __global__ void topk_local_only_kernel(int64_t n_rows, int n_g, int Bk, int k, i
 
 cudaError_t launch_topk(const float* S, int64_t N, int n_g, int64_t nb, int Bk, int k,
                         int64_t q_offset, const int32_t* seq_lens, int32_t* ids, const Diag& dg,
-                        cudaStream_t st) {
+                        cudaStream_t st, int64_t ld) {
+  if (ld <= 0) ld = nb;
   int64_t n_rows = N * n_g;
   if (n_rows == 0) return cudaSuccess;
   note_launches(1);
@@ -378,12 +379,13 @@ cudaError_t launch_topk(const float* S, int64_t N, int n_g, int64_t nb, int Bk, 
   int64_t blocks = (n_rows + 2 * kWarps - 1) / (2 * kWarps);
   blocks = std::min<int64_t>(blocks, (int64_t)sms * std::max(per_sm, 1));
   const int bk_shift = (Bk & (Bk - 1)) == 0 ? __builtin_ctz((unsigned)Bk) : -1;
-  const bool vec = (nb % 4) == 0 && ((uintptr_t)S % 16) == 0;
+  const bool vec = (ld % 4) == 0 && ((uintptr_t)S % 16) == 0;
   if (vec)
-    topk_kernel<true><<<(unsigned)blocks, kWarps * 32, 0, st>>>(S, n_rows, n_g, nb, Bk, bk_shift,
-                                                               k, q_offset, seq_lens, ids, dg);
+    topk_kernel<true><<<(unsigned)blocks, kWarps * 32, 0, st>>>(S, n_rows, n_g, nb, ld, Bk,
+                                                               bk_shift, k, q_offset, seq_lens,
+                                                               ids, dg);
   else
-    topk_kernel<false><<<(unsigned)blocks, kWarps * 32, 0, st>>>(S, n_rows, n_g, nb, Bk,
+    topk_kernel<false><<<(unsigned)blocks, kWarps * 32, 0, st>>>(S, n_rows, n_g, nb, ld, Bk,
                                                                 bk_shift, k, q_offset, seq_lens,
                                                                 ids, dg);
   return cudaGetLastError();

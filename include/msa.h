@@ -250,7 +250,9 @@ int msa_sparse_attn_paged(const void* q, const void* k_pages, const void* v_page
  * page_table[s * max_pages + b]. The new token is the last one (position
  * seq_lens[s] - 1) and must already be written to the caches. */
 
-/* Workspace bytes of the decode index branch: B * n_groups * max_pages fp32. */
+/* Workspace bytes of the decode index branch: the block scores, B * n_groups
+ * rows of max_pages fp32 each, every row padded to a multiple of 4 floats
+ * (16-byte aligned rows, which the top-k reads as vectors). */
 size_t msa_index_select_decode_workspace_bytes(int B, int max_pages, int n_groups);
 
 /* Index branch of decode, one query per sequence.

@@ -96,7 +96,8 @@ def test_decode_rejects(msa):
     g = msa._index_dec
     assert g(FAKE, FAKE, FAKE, FAKE, 4, 10, 9, 128, 128, 16, FAKE, None, FAKE, 1 << 20, None) == -2
     assert g(FAKE, FAKE, FAKE, FAKE, 4, 10, 8, 128, 128, 16, FAKE, None, None, 0, None) == -3
-    assert msa.msa_index_select_decode_workspace_bytes(64, 1025, 8) == 64 * 1025 * 8 * 4
+    # rows of 1025 scores padded to 1028 (16-byte aligned rows)
+    assert msa.msa_index_select_decode_workspace_bytes(64, 1025, 8) == 64 * 1028 * 8 * 4
 
 
 def test_decode_index_fp8_rejects(msa):
