@@ -761,7 +761,7 @@ def main():
                 "peak": peak_t, "unit": "TFLOP/s", "frac": round(achieved / peak_t, 4),
                 "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": traffic,
                 "algorithmic_flops_per_launch": dom_fl, "ms_per_launch": round(dom_ms, 4)}
-    e2e_ms, h2d, d2h = e2e_prefill(msa, P, max(3, args.steps), 1)
+    e2e_ms, h2d, d2h = e2e_prefill(msa, P, max(3, args.steps), args.warmup)
     e2e_ms, e2e_value = job_rate(world, w.N, e2e_ms)
     del P
     torch.cuda.empty_cache()
