@@ -248,7 +248,12 @@ int msa_sparse_attn_paged(const void* q, const void* k_pages, const void* v_page
  * dimension is the number of kv heads, so pages are head-major). Sequence s holds
  * seq_lens[s] tokens; its logical block b lives in physical page
  * page_table[s * max_pages + b]. The new token is the last one (position
- * seq_lens[s] - 1) and must already be written to the caches. */
+ * seq_lens[s] - 1) and must already be written to the caches.
+ * The decode entry points take no page count, so they cannot check page ids:
+ * every entry page_table[s * max_pages + b] with b <= (seq_lens[s] - 1) / Bk
+ * must name a page of the caches passed (0 <= id < P). A page id outside them
+ * is read as an address, with undefined results. Sequence lengths and block
+ * ids ARE checked on the device (see msa_get_error). */
 
 /* Workspace bytes of the decode index branch: the block scores, B * n_groups
  * rows of max_pages fp32 each, every row padded to a multiple of 4 floats
@@ -330,7 +335,12 @@ int msa_decode(const void* q, const void* k_pages, const void* v_pages, int kv_d
  *     return MSA_ERR_WORKSPACE and enqueue nothing.
  *   - The first call on a device looks up the array's device address (a
  *     cudaGetSymbolAddress, no allocation); make that first call before any
- *     stream capture.
+ *     stream capture. With CUDA's default lazy module loading that first
+ *     call is also when the driver loads this library's kernels and commits
+ *     the 4 MiB array in device memory, which can fail (MSA_ERR_CUDA) once
+ *     the caller has reserved all device memory. Make one warm-up call at
+ *     start-up, before reserving memory, or load modules eagerly
+ *     (CUDA_MODULE_LOADING=EAGER).
  *   - All calls share the array: calls whose executions overlap on the GPU
  *     (several streams or host threads) race and must be serialised.
  *   - Calls no cudaMalloc / cudaFree and no allocating library routine. */

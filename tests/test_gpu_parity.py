@@ -2,9 +2,11 @@
 same seeded inputs.
 
 Bars: block ids bit-exact on integer index inputs; on Gaussian inputs set-equal
-up to near-tie swaps (tests/msa_check.py). Attention is compared on the same
-block ids on both sides (taken from the oracle, or equal to it): bf16 output
-max |err| <= 1e-2, fp32 LSE max |err| <= 1e-3, FP8-KV output max |err| <= 5e-2.
+up to near-tie swaps (tests/msa_check.py), at most 1% of the sampled (row,
+group) pairs. Attention is compared on the same block ids on both sides: in the
+end-to-end pipelines and decode cases those are the GPU's own ids, which the
+oracle takes as given. bf16 output max |err| <= 1e-2, fp32 LSE max |err| <=
+1e-3 (bf16 and FP8-E4M3 KV), FP8-KV output max |err| <= 5e-2.
 """
 import math
 
@@ -262,8 +264,9 @@ def test_sparse_attn_on_oracle_ids(msa, N, H_q, H_kv, d, k, ws_rows):
 
 def _pipeline(msa, w, rows, ws_rows=None):
     """GPU index branch, then GPU main branch on the GPU's own ids; checks the
-    selection on the sampled rows and the attention on those whose ids equal
-    the oracle's."""
+    selection on the sampled rows (returns the number of near-tie swaps) and
+    the attention of every sampled row against the oracle run on those same
+    GPU ids."""
     ids, got, want, want_s, swaps, _ = _index_sampled(msa, w, rows)
     q = synth.device_tensor(w, synth.T_Q)
     kk = synth.device_tensor(w, synth.T_K)
@@ -274,9 +277,7 @@ def _pipeline(msa, w, rows, ws_rows=None):
     out, lse = msa.msa_sparse_attn(q, kk, v, ids, w.Bk, w.scale, workspace=ws)
     torch.cuda.synchronize()
     del ws, kk, v
-    same = np.array([np.array_equal(got[i], want[i]) for i in range(len(rows))])
-    r2 = rows[same]
-    blocks = sorted(set(int(x) for x in want[same].ravel() if x >= 0))
+    blocks = sorted(set(int(x) for x in got.ravel() if x >= 0))
     Kh = np.zeros((1, w.nb * w.Bk, w.H_kv, w.d), dtype=np.uint16)
     Vh = np.zeros_like(Kh)
     per = w.H_kv * w.d
@@ -284,12 +285,19 @@ def _pipeline(msa, w, rows, ws_rows=None):
         t0, t1 = b * w.Bk, min(w.N, (b + 1) * w.Bk)
         synth.host_fill(w, synth.T_K, Kh, t0 * per, (t1 - t0) * per)
         synth.host_fill(w, synth.T_V, Vh, t0 * per, (t1 - t0) * per)
-    qh = synth.host_rows(w, synth.T_Q, 0, r2)
-    o_ref, l_ref = oracle.sparse_attn(qh, r2, Kh[0], Vh[0], want[same], w.Bk, w.scale)
-    o_gpu = bf16_to_np(out[torch.from_numpy(r2).cuda()])
-    check_close("o", o_gpu, o_ref, TOL_O)
-    check_close("lse", lse[torch.from_numpy(r2).cuda()].cpu().numpy(), l_ref, TOL_LSE)
-    return swaps, len(r2)
+    qh = synth.host_rows(w, synth.T_Q, 0, rows)
+    o_ref, l_ref = oracle.sparse_attn(qh, rows, Kh[0], Vh[0], got, w.Bk, w.scale)
+    sel = torch.from_numpy(rows).cuda()
+    e_o = check_close("o", bf16_to_np(out[sel]), o_ref, TOL_O)
+    e_l = check_close("lse", lse[sel].cpu().numpy(), l_ref, TOL_LSE)
+    print(f"[{w.name}] rows {len(rows)} swaps {swaps} max|err| o {e_o:.3e} lse {e_l:.3e}")
+    return swaps, len(rows)
+
+
+def _swap_bound(swaps, n_rows, n_g):
+    """At most 1% of the sampled (row, group) pairs (and at least one pair) may
+    differ by near-tie swaps."""
+    assert swaps <= max(1.0, 0.01 * n_rows * n_g), (swaps, n_rows * n_g)
 
 
 def test_pipeline_tiny_all_rows(msa):
@@ -302,20 +310,20 @@ def test_pipeline_tiny_all_rows(msa):
 def test_pipeline_32k(msa):
     w = synth.make("32k")
     swaps, n = _pipeline(msa, w, _sample_rows(w.N, w.Bk, 512, 11))
-    assert n > 0
+    _swap_bound(swaps, n, w.n_g)
 
 
 def test_pipeline_128k(msa):
     w = synth.make("128k")
     swaps, n = _pipeline(msa, w, _sample_rows(w.N, w.Bk, 128, 13, n_tail=128))
-    assert n > 0
+    _swap_bound(swaps, n, w.n_g)
 
 
 def test_pipeline_1m(msa):
     w = synth.make("1m")
     swaps, n = _pipeline(msa, w, _sample_rows(w.N, w.Bk, 16, 17, n_tail=32)[::4],
                          ws_rows=w.N // 8)
-    assert n > 0
+    _swap_bound(swaps, n, w.n_g)
 
 
 # ------------------------------------------------------------ varlen prefill
@@ -427,26 +435,28 @@ def _decode_case(msa, w, fp8):
                                               want_scores=True)
     del kh
     got = ids.cpu().numpy()
-    compare_selection(got, want, want_s, np.full(w.B, w.L - 1), w.Bk)
-    # attention on the oracle's ids
+    swaps = compare_selection(got, want, want_s, np.full(w.B, w.L - 1), w.Bk)
+    _swap_bound(swaps, w.B, w.n_g)
+    # attention on the GPU's own ids, on both sides
     kp = synth.device_paged(w, synth.T_K, pt, fp8=fp8)
     vp = synth.device_paged(w, synth.T_V, pt, fp8=fp8)
     ks, vs = synth.fp8_scales(w.H_kv)
     kw = {}
     if fp8:
         kw = dict(k_scale=torch.from_numpy(ks).to(dev), v_scale=torch.from_numpy(vs).to(dev))
-    out, lse = msa.msa_decode(q, kp, vp, pt, sl, torch.from_numpy(want).to(dev), w.Bk, w.scale,
-                              **kw)
+    out, lse = msa.msa_decode(q, kp, vp, pt, sl, ids, w.Bk, w.scale, **kw)
     torch.cuda.synchronize()
     del kp, vp
-    blocks = [sorted(set(int(x) for x in want[s].ravel() if x >= 0)) for s in range(w.B)]
+    blocks = [sorted(set(int(x) for x in got[s].ravel() if x >= 0)) for s in range(w.B)]
     Kh = synth.host_paged(w, synth.T_K, blocks, fp8=fp8)
     Vh = synth.host_paged(w, synth.T_V, blocks, fp8=fp8)
     qh = np.stack([synth.host_rows(w, synth.T_Q, s, [w.L - 1])[0] for s in range(w.B)])
-    o_ref, l_ref = oracle.decode_attn(qh, Kh, Vh, ident, sl_np, want, w.Bk, w.scale, fp8=fp8,
+    o_ref, l_ref = oracle.decode_attn(qh, Kh, Vh, ident, sl_np, got, w.Bk, w.scale, fp8=fp8,
                                       k_scale=ks if fp8 else None, v_scale=vs if fp8 else None)
-    check_close("o", bf16_to_np(out), o_ref, TOL_O_FP8 if fp8 else TOL_O)
-    check_close("lse", lse.cpu().numpy(), l_ref, TOL_LSE * (10 if fp8 else 1))
+    e_o = check_close("o", bf16_to_np(out), o_ref, TOL_O_FP8 if fp8 else TOL_O)
+    e_l = check_close("lse", lse.cpu().numpy(), l_ref, TOL_LSE)
+    print(f"[decode B={w.B} L={w.L} fp8={fp8}] swaps {swaps} max|err| o {e_o:.3e} "
+          f"lse {e_l:.3e}")
 
 
 @pytest.mark.parametrize("fp8", [False, True])
@@ -503,8 +513,9 @@ def test_decode_ragged_lengths(msa, fp8):
     qhq = np.stack([synth.host_rows(w, synth.T_Q, s, [int(lens[s]) - 1])[0] for s in range(w.B)])
     o_ref, l_ref = oracle.decode_attn(qhq, Kh, Vh, ident, lens, want, w.Bk, w.scale, fp8=fp8,
                                       k_scale=ks if fp8 else None, v_scale=vs if fp8 else None)
-    check_close("o", bf16_to_np(out), o_ref, TOL_O_FP8 if fp8 else TOL_O)
-    check_close("lse", lse.cpu().numpy(), l_ref, TOL_LSE * (10 if fp8 else 1))
+    e_o = check_close("o", bf16_to_np(out), o_ref, TOL_O_FP8 if fp8 else TOL_O)
+    e_l = check_close("lse", lse.cpu().numpy(), l_ref, TOL_LSE)
+    print(f"[decode ragged fp8={fp8}] max|err| o {e_o:.3e} lse {e_l:.3e}")
 
 
 def _decode_index_fp8_inputs(w, lens):

@@ -80,6 +80,62 @@ def test_golden_hand_example():
     assert np.isneginf(sc[0, :, 1:]).all()  # invisible blocks
 
 
+def _golden_scores(rows):
+    """JSON numbers, with "-0" for a negative zero, as fp32."""
+    return np.array([[[(-0.0 if v == "-0" else float(v)) for v in g] for g in r] for r in rows],
+                    dtype=np.float32)
+
+
+def test_golden_topk_hand_example():
+    """The standalone top-k step on hand-worked block scores: q_offset > 0, two
+    groups, ties among candidates, -0 against +0, a local block with the
+    highest score (forced, never ranked), blocks after the query holding the
+    largest values (never read), and rows whose local block is the last one."""
+    g = json.load(open(os.path.join(GOLDEN, "topk_hand_example.json")))
+    sh = g["shape"]
+    S = _golden_scores(g["block_scores"])
+    assert S.shape == (sh["N"], sh["n_g"], sh["nb"])
+    assert np.signbit(S[0, 1, 1]) and not np.signbit(S[0, 1, 2])  # the -0 / +0 pair
+    rows = sh["q_offset"] + np.arange(sh["N"])
+    ids = oracle.topk_blocks(S, rows, sh["Bk"], sh["k"])
+    assert ids.tolist() == g["expected_ids"]
+
+
+@pytest.mark.parametrize("Bk,N,q_offset,n_g,k", [
+    (8, 40, 0, 2, 3), (8, 57, 96, 3, 4), (16, 64, 300, 2, 16), (4, 33, 21, 4, 5),
+    (128, 200, 2000, 2, 16), (2, 30, 7, 1, 2)])
+def test_topk_blocks_equals_index_select_on_integer_inputs(Bk, N, q_offset, n_g, k):
+    """The top-k step alone, given the block scores index_select pools, picks
+    what index_select picks (itself pinned to the brute force above). Integer
+    inputs make every score an integer below 2^24, so the fp32 block scores are
+    exact, and many scores tie. Rows sit at q_offset + i with n_g groups each."""
+    rng = np.random.default_rng(7 * N + Bk + q_offset)
+    d_idx = 8
+    L = q_offset + N
+    qidx = rand_int_bf16(rng, (N, n_g, d_idx), -2, 2)
+    kidx = rand_int_bf16(rng, (L, d_idx), -2, 2)
+    rows = q_offset + np.arange(N)
+    nb = (L + Bk - 1) // Bk
+    ids, sc = oracle.index_select(qidx, rows, kidx, Bk, k, nb_out=nb, want_scores=True)
+    vis = np.isfinite(sc)
+    assert np.array_equal(sc[vis], sc[vis].astype(np.float32).astype(np.float64))
+    got = oracle.topk_blocks(sc.astype(np.float32), rows, Bk, k)
+    assert np.array_equal(got, ids)
+    # scores past each row's local block do not matter
+    noisy = sc.astype(np.float32)
+    noisy[~vis] = 1e30
+    assert np.array_equal(oracle.topk_blocks(noisy, rows, Bk, k), ids)
+
+
+def test_topk_blocks_skips_rows_past_the_score_rows():
+    """A row whose local block lies beyond the given nb blocks is left untouched."""
+    S = np.zeros((3, 2, 4), dtype=np.float32)
+    ids = oracle.topk_blocks(S, np.array([0, 511, 512]), 128, 2)
+    assert ids[0].tolist() == [[0, -1], [0, -1]]
+    assert ids[1].tolist() == [[0, 3], [0, 3]]
+    assert (ids[2] == -2).all()  # the wrapper's fill value: not written
+
+
 @pytest.mark.parametrize("Bk,N,n_g,k", [
     (1, 23, 1, 1), (1, 40, 2, 3), (2, 33, 1, 2), (2, 64, 4, 3), (4, 61, 2, 16),
     (8, 64, 4, 3), (4, 64, 1, 2), (8, 57, 2, 1), (2, 50, 4, 16)])
