@@ -38,6 +38,7 @@ def lib():
         L.oracle_dense_gqa.argtypes = [P, P, I64, P, P, I32, I32, I32, D, P, P]
         L.oracle_kl_teacher.argtypes = [P, P, P, I64, P, P, P, I32, I32, I32, I32, I32, I32, D,
                                         P, P]
+        L.oracle_index_project.argtypes = [P, P, P, I64, I32, I32, I32, P, P]
         L.oracle_index_brute.argtypes = [P, P, I64, P, I32, I32, I32, I32, P]
         L.oracle_decode_index_select.argtypes = [P, P, P, P, I32, I32, I32, I32, I32, I32, I64,
                                                  P, P]
@@ -134,6 +135,23 @@ def sparse_attn(q_rows, rows, K, V, ids, Bk, scale):
     _ok(lib().oracle_sparse_attn(qp, rp, n, K.ctypes.data, V.ctypes.data, ip, H_q, H_kv, d,
                                  Bk, k, scale, o.ctypes.data, lse.ctypes.data))
     return o, lse
+
+
+def index_project(x, w_qidx, w_kidx):
+    """x [n, d_model], w_qidx [n_g * d_idx, d_model], w_kidx [d_idx, d_model] bf16
+    bits -> (q_idx [n, n_g, d_idx], k_idx [n, d_idx]) fp64."""
+    xx, xp = _c(x, np.uint16)
+    wq, wqp = _c(w_qidx, np.uint16)
+    wk, wkp = _c(w_kidx, np.uint16)
+    n, d_model = xx.shape
+    d_idx = wk.shape[0]
+    n_g = wq.shape[0] // d_idx
+    assert wq.shape == (n_g * d_idx, d_model) and wk.shape == (d_idx, d_model)
+    q = np.empty((n, n_g, d_idx), dtype=np.float64)
+    k = np.empty((n, d_idx), dtype=np.float64)
+    _ok(lib().oracle_index_project(xp, wqp, wkp, n, d_model, n_g, d_idx, q.ctypes.data,
+                                   k.ctypes.data))
+    return q, k
 
 
 def dense_gqa(q_rows, rows, K, V, scale):

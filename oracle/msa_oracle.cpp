@@ -28,6 +28,9 @@
 //                      causally visible tokens of the group's selected blocks
 //                      ([MSA-2B] "两个分支如何工作"; [MSA-PT] "Como funciona o
 //                      MSA").
+//   projections        q_idx = x W_qidx^T (n_g heads of d_idx), k_idx = x W_kidx^T
+//                      (one shared head): the index branch's two projection
+//                      matrices ([MSA-2B] "两个分支如何工作"), plain linear maps.
 //   decode             the same steps for one new token at position L-1 of a
 //                      paged KV cache whose page size is the block size
 //                      ([MSA-2B] "运行 Kernel", the usage listing), with bf16 or
@@ -348,6 +351,36 @@ int oracle_kl_teacher(const uint16_t* q_rows, const uint16_t* qi_rows, const int
     }
     kl_out[r] = kl;
     if (mag_out) mag_out[r] = mag;
+  }
+  return 0;
+}
+
+// Index-branch projections ([MSA-2B] "两个分支如何工作": the index branch adds
+// two projection matrices to the GQA layer, one giving the index-query head of
+// every group, one giving the shared index-key head). Read as plain linear
+// maps of the layer input, no bias and no activation:
+//   q_idx[t, g, c] = sum_m x[t, m] * w_qidx[g * d_idx + c, m]
+//   k_idx[t, c]    = sum_m x[t, m] * w_kidx[c, m]
+//   x [n_rows, d_model], w_qidx [n_g * d_idx, d_model], w_kidx [d_idx, d_model]
+//   (bf16 bits; weights in [out, in] layout); outputs fp64.
+int oracle_index_project(const uint16_t* x, const uint16_t* w_qidx, const uint16_t* w_kidx,
+                         int64_t n_rows, int d_model, int n_g, int d_idx, double* q_out,
+                         double* k_out) {
+  if (n_rows < 0 || d_model < 1 || n_g < 1 || d_idx < 1) return -1;
+  const int n_out = n_g * d_idx + d_idx;
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < n_rows; ++t) {
+    std::vector<double> xr((size_t)d_model);
+    decode_row(x + (size_t)t * d_model, d_model, xr.data());
+    for (int o = 0; o < n_out; ++o) {
+      const bool is_q = o < n_g * d_idx;
+      const uint16_t* w = is_q ? w_qidx + (size_t)o * d_model
+                               : w_kidx + (size_t)(o - n_g * d_idx) * d_model;
+      double acc = 0.0;
+      for (int m = 0; m < d_model; ++m) acc += xr[(size_t)m] * bf16_to_double(w[m]);
+      if (is_q) q_out[(size_t)t * n_g * d_idx + o] = acc;
+      else k_out[(size_t)t * d_idx + (o - n_g * d_idx)] = acc;
+    }
   }
   return 0;
 }

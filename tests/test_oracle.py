@@ -552,3 +552,50 @@ def test_e2m1_decoder_exhaustive_vs_ocp():
         want = table[c & 7] * (-1.0 if c & 8 else 1.0)
         got = oracle.e2m1_to_f64(c)
         assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), c
+
+
+# --------------------------------------------------- index-branch projections
+def test_projection_one_hot_rows_pick_weight_columns():
+    """x = e_m (one-hot) gives q_idx[g, c] = w_qidx[g * d_idx + c, m] and
+    k_idx[c] = w_kidx[c, m]: pins the [out, in] weight layout, the group-major
+    split of the query outputs and the two outputs' ranges."""
+    rng = np.random.default_rng(61)
+    d_model, n_g, d_idx = 24, 3, 8
+    wq = rand_bf16(rng, (n_g * d_idx, d_model))
+    wk = rand_bf16(rng, (d_idx, d_model))
+    x = bf16_bits(np.eye(d_model, dtype=np.float32))
+    q, k = oracle.index_project(x, wq, wk)
+    wqf, wkf = bits_to_f64(wq), bits_to_f64(wk)
+    for m in range(d_model):
+        for g in range(n_g):
+            assert np.array_equal(q[m, g], wqf[g * d_idx:(g + 1) * d_idx, m])
+        assert np.array_equal(k[m], wkf[:, m])
+
+
+def test_projection_integer_inputs_equal_integer_matmul():
+    """Integer-valued x and weights: the fp64 sums are exact integers, equal to
+    numpy's int64 matrix product (an independent routine)."""
+    rng = np.random.default_rng(62)
+    n, d_model, n_g, d_idx = 37, 96, 4, 16
+    xi = rng.integers(-8, 9, (n, d_model))
+    wqi = rng.integers(-8, 9, (n_g * d_idx, d_model))
+    wki = rng.integers(-8, 9, (d_idx, d_model))
+    q, k = oracle.index_project(bf16_bits(xi.astype(np.float32)), bf16_bits(wqi.astype(np.float32)),
+                                bf16_bits(wki.astype(np.float32)))
+    assert np.array_equal(q.reshape(n, -1), (xi @ wqi.T).astype(np.float64))
+    assert np.array_equal(k, (xi @ wki.T).astype(np.float64))
+
+
+def test_projection_is_linear():
+    """project(x1 + 2 x2) = project(x1) + 2 project(x2) for values exact in bf16."""
+    rng = np.random.default_rng(63)
+    n, d_model, n_g, d_idx = 9, 40, 2, 8
+    x1 = rng.integers(-4, 5, (n, d_model)).astype(np.float32) / 4
+    x2 = rng.integers(-4, 5, (n, d_model)).astype(np.float32) / 4
+    wq = rand_bf16(rng, (n_g * d_idx, d_model))
+    wk = rand_bf16(rng, (d_idx, d_model))
+    qa, ka = oracle.index_project(bf16_bits(x1 + 2 * x2), wq, wk)
+    q1, k1 = oracle.index_project(bf16_bits(x1), wq, wk)
+    q2, k2 = oracle.index_project(bf16_bits(x2), wq, wk)
+    assert np.allclose(qa, q1 + 2 * q2, rtol=1e-12, atol=1e-12)
+    assert np.allclose(ka, k1 + 2 * k2, rtol=1e-12, atol=1e-12)
