@@ -18,7 +18,8 @@ Prints ONE JSON line. `value` is prefill tokens/s (all ranks). Further keys:
                the 128K tokens as 8 packed 16K sequences (varlen entry points),
                a chunked prefill of the last 16K of the 128K tokens over paged
                caches with a shuffled page table,
-               the 128K step with the index branch on FP8-E4M3 codes, the KL
+               the 128K step with the index branch on FP8-E4M3 codes, the
+               index-branch projections of the 128K tokens (d_model 4096), the KL
                alignment signal of the index branch at 128K,
                decode steps with bf16 KV, FP8-E4M3 KV, and FP8-E4M3 KV plus an
                FP8-E4M3 or NVFP4 k_idx cache, standalone top-16 (with
@@ -548,6 +549,31 @@ def time_kl_teacher(msa, w, steps, warmup):
     return ms, flops
 
 
+def time_index_project(msa, w, steps, warmup, d_model=4096):
+    """Index-branch projections of the workload's N tokens: x [N, d_model] times
+    W_qidx [n_g * d_idx, d_model] and W_kidx [d_idx, d_model] (seeded Gaussian
+    values; d_model = H_q * d). Returns (ms, algorithmic flops)."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(w.seed)
+    x = torch.randn((w.N, d_model), device="cuda", generator=g).to(torch.bfloat16)
+    wq = (torch.randn((w.n_g * w.d_idx, d_model), device="cuda", generator=g)
+          / d_model ** 0.5).to(torch.bfloat16)
+    wk = (torch.randn((w.d_idx, d_model), device="cuda", generator=g)
+          / d_model ** 0.5).to(torch.bfloat16)
+    q = torch.empty((w.N, w.n_g, w.d_idx), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty((w.N, w.d_idx), dtype=torch.bfloat16, device="cuda")
+    for _ in range(warmup):
+        msa.msa_index_project(x, wq, wk, q, k)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        msa.msa_index_project(x, wq, wk, q, k)
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, 2.0 * w.N * d_model * (w.n_g + 1) * w.d_idx
+
+
 def time_prefill_fp8_index(msa, w, steps, warmup):
     """Prefill step with the index branch on FP8-E4M3 codes of q_idx / k_idx
     (rounded to nearest by torch before the timing) and the bf16 main branch."""
@@ -667,7 +693,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=15.0)
-    ap.add_argument("--only", choices=["decode", "topk", "index", "attn"], default=None,
+    ap.add_argument("--only", choices=["decode", "topk", "index", "attn", "proj"], default=None,
                     help="time only this path and print its numbers (for profiling runs)")
     ap.add_argument("--batch", type=int, default=None,
                     help="with --only decode: number of sequences (default: the workload's 64)")
@@ -738,6 +764,12 @@ def main():
         print(json.dumps({"only": "attn", "workload": w.name, "ms": ms,
                           "tflops": attn_flops(w.N, w.H_q, w.d, w.Bk, w.k) / (ms * 1e-3) / 1e12}))
         return
+    if args.only == "proj":
+        w = synth.make(args.workload)
+        ms, fl = time_index_project(msa, w, args.steps, args.warmup)
+        print(json.dumps({"only": "proj", "workload": w.name, "ms": ms,
+                          "tflops": fl / (ms * 1e-3) / 1e12}))
+        return
     if args.only == "topk":
         t_ms, t_bytes, torch_ms = time_topk(msa, synth.make(args.workload), args.steps,
                                             args.warmup)
@@ -801,6 +833,12 @@ def main():
             "index_tflops": round(fl_idx / (f_idx * 1e-3) / 1e12, 2),
             "index_frac_of_fp8_peak": round(fl_idx / (f_idx * 1e-3) / 1e12 / peak_f8, 4),
             "fp8_peak": peak_f8, "fp8_peak_source": "measured bf16 burst x 2 (nominal ratio)"}
+        pj_ms, pj_fl = time_index_project(msa, w, args.steps, 3)
+        torch.cuda.empty_cache()
+        extra["index_projection_128k"] = {
+            "ms": round(pj_ms, 4), "d_model": 4096,
+            "tflops": round(pj_fl / (pj_ms * 1e-3) / 1e12, 2),
+            "frac_of_burst": round(pj_fl / (pj_ms * 1e-3) / 1e12 / peak_t, 4)}
         kl_ms, kl_fl = time_kl_teacher(msa, w, args.steps, 3)
         torch.cuda.empty_cache()
         extra["kl_teacher_128k"] = {"ms": round(kl_ms, 3),

@@ -59,6 +59,7 @@ _launch_count = _sig("msa_launch_count", [], _I64)
 _index_dec_noalloc = _sig("msa_index_select_decode_noalloc", [_P, _P, _P, _P, _I, _I, _I, _I, _I,
                                                               _I, _P, _P])
 _noalloc_max = _sig("msa_index_select_decode_noalloc_max_scores", [], _I64)
+_index_project = _sig("msa_index_project", [_P, _P, _P, _I64, _I, _I, _I, _P, _P, _P])
 _index_fp8 = _sig("msa_index_select_fp8", [_P, _P, _I64, _I, _I, _I, _I, _P, _P, _F, _P])
 _index_varlen = _sig("msa_index_select_varlen", [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P])
 _ws_attn_varlen = _sig("msa_sparse_attn_varlen_workspace_bytes", [_P, _I, _I, _I, _I, _I, _I],
@@ -90,7 +91,7 @@ EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes
            "msa_sparse_attn_varlen", "msa_index_select_paged",
            "msa_sparse_attn_paged_workspace_bytes", "msa_sparse_attn_paged",
            "msa_index_select_decode_fp8", "msa_kl_teacher_workspace_bytes",
-           "msa_kl_teacher", "msa_index_select_decode_nvfp4"]
+           "msa_kl_teacher", "msa_index_select_decode_nvfp4", "msa_index_project"]
 
 
 class MSAError(RuntimeError):
@@ -151,6 +152,30 @@ def msa_index_select(q_idx: torch.Tensor, k_idx: torch.Tensor, Bk: int = 128, k:
                          block_ids.data_ptr(), _ptr(block_scores), None, 0, _stream(q_idx)),
            "msa_index_select")
     return block_ids
+
+
+def msa_index_project(x: torch.Tensor, w_qidx: torch.Tensor, w_kidx: torch.Tensor,
+                      q_idx: Optional[torch.Tensor] = None,
+                      k_idx: Optional[torch.Tensor] = None):
+    """Index-branch projections: x [N, d_model] bf16, w_qidx [n_groups * d_idx,
+    d_model] bf16, w_kidx [d_idx, d_model] bf16 -> (q_idx [N, n_groups, d_idx],
+    k_idx [N, d_idx]) bf16."""
+    N, d_model = x.shape
+    d_idx = w_kidx.shape[0]
+    n_g = w_qidx.shape[0] // d_idx
+    _req(x, "x", torch.bfloat16)
+    _req(w_qidx, "w_qidx", torch.bfloat16, (n_g * d_idx, d_model))
+    _req(w_kidx, "w_kidx", torch.bfloat16, (d_idx, d_model))
+    if q_idx is None:
+        q_idx = torch.empty((N, n_g, d_idx), dtype=torch.bfloat16, device=x.device)
+    if k_idx is None:
+        k_idx = torch.empty((N, d_idx), dtype=torch.bfloat16, device=x.device)
+    _req(q_idx, "q_idx", torch.bfloat16, (N, n_g, d_idx))
+    _req(k_idx, "k_idx", torch.bfloat16, (N, d_idx))
+    _check(_index_project(x.data_ptr(), w_qidx.data_ptr(), w_kidx.data_ptr(), N, d_model, n_g,
+                          d_idx, q_idx.data_ptr(), k_idx.data_ptr(), _stream(x)),
+           "msa_index_project")
+    return q_idx, k_idx
 
 
 def msa_index_select_fp8(q_idx: torch.Tensor, k_idx: torch.Tensor, Bk: int = 128, k: int = 16,

@@ -10,7 +10,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmsa.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 SOURCES = ["msa_abi.cu", "msa_index.cu", "msa_topk.cu", "msa_attn.cu", "msa_decode.cu",
-           "msa_noalloc.cu", "msa_kl.cu"]
+           "msa_noalloc.cu", "msa_kl.cu", "msa_proj.cu"]
 FLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
          "-Xcompiler", "-fPIC", "-Xptxas", "-warn-spills"]
 

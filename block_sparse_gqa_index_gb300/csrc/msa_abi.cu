@@ -100,6 +100,22 @@ int msa_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_grou
                                             block_scores, nb, diag(), (cudaStream_t)stream));
 }
 
+int msa_index_project(const void* x, const void* w_qidx, const void* w_kidx, int64_t N,
+                      int d_model, int n_groups, int d_idx, void* q_idx, void* k_idx,
+                      void* stream) {
+  if (N < 0 || d_model < 1 || n_groups < 1 || d_idx < 1) return MSA_ERR_INVALID_ARG;
+  if (N == 0) return MSA_OK;
+  if (!x || !w_qidx || !w_kidx || !q_idx || !k_idx) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_qidx) || !aligned16(w_kidx) || !aligned16(q_idx) ||
+      !aligned16(k_idx))
+    return MSA_ERR_INVALID_ARG;
+  if (d_model % 8 != 0 || !supported_d(d_idx) || N >= (1ll << 31) ||
+      (int64_t)n_groups * d_idx >= (1 << 20))
+    return MSA_ERR_UNSUPPORTED;
+  return status_of(msa::launch_index_project(x, w_qidx, w_kidx, N, d_model, n_groups, d_idx,
+                                             q_idx, k_idx, diag(), (cudaStream_t)stream));
+}
+
 int msa_index_select_fp8(const void* q_idx, const void* k_idx, int64_t N, int n_groups,
                          int d_idx, int Bk, int k, int32_t* block_ids, float* block_scores,
                          float score_scale, void* stream) {

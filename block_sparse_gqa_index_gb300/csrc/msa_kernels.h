@@ -39,6 +39,12 @@ cudaError_t launch_index_select_paged(const void* q_idx, const void* k_idx_pages
                                       int d_idx, int k, int32_t* block_ids, const Diag& dg,
                                       cudaStream_t st);
 
+// Index-branch projections (msa_proj.cu): q_idx [N, n_g * d_idx] = x W_qidx^T,
+// k_idx [N, d_idx] = x W_kidx^T; x [N, d_model], weights [out, d_model], bf16.
+cudaError_t launch_index_project(const void* x, const void* w_qidx, const void* w_kidx,
+                                 int64_t N, int d_model, int n_g, int d_idx, void* q_idx,
+                                 void* k_idx, const Diag& dg, cudaStream_t st);
+
 // Exp-free top-k over block scores (msa_topk.cu).
 // ld: row stride of S in floats (0: nb); rows are read at S + r * ld.
 cudaError_t launch_topk(const float* S, int64_t N, int n_g, int64_t nb, int Bk, int k,

@@ -82,6 +82,23 @@ int msa_index_select(const void* q_idx, const void* k_idx, int64_t N, int n_grou
                      int d_idx, int Bk, int k, int32_t* block_ids, float* block_scores,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* Index-branch projections: the two projection matrices the index branch adds
+ * to a GQA layer ("MiniMax Sparse Attention (MSA) ...", section "两个分支如何工作":
+ * one index-query head per group, one shared index-key head), read as plain
+ * linear maps of the layer input (no bias, no activation):
+ *   x       [N, d_model] bf16                  layer input
+ *   w_qidx  [n_groups * d_idx, d_model] bf16   [out, in]; rows g*d_idx .. give group g
+ *   w_kidx  [d_idx, d_model] bf16              [out, in]
+ *   q_idx   [N, n_groups, d_idx] bf16 out      q_idx[t,g,c] = sum_m x[t,m] w_qidx[g*d_idx+c, m]
+ *   k_idx   [N, d_idx] bf16 out                k_idx[t,c]   = sum_m x[t,m] w_kidx[c, m]
+ * One tensor-core GEMM over both weight matrices, fp32 accumulation, each
+ * output rounded once to bf16; the outputs feed msa_index_select directly.
+ * d_model must be a multiple of 8 and d_idx in {64, 128} (MSA_ERR_UNSUPPORTED
+ * otherwise); every tensor 16-byte aligned (MSA_ERR_INVALID_ARG otherwise). */
+int msa_index_project(const void* x, const void* w_qidx, const void* w_kidx, int64_t N,
+                      int d_model, int n_groups, int d_idx, void* q_idx, void* k_idx,
+                      void* stream);
+
 /* Index branch with FP8-E4M3 index operands (the kernel release lists FP8 among
  * its precisions: "MiniMax lança MSA ...", section "Kernel open source e
  * MiniMax-M3"):
