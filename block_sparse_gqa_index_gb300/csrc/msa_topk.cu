@@ -15,7 +15,9 @@
 //   1. the values are staged in the half's shared buffer, and every lane takes
 //      the max of its even and of its odd blocks (32 group maxima per row);
 //   2. tau = max(15th largest group max, worst key kept so far): at least k-1
-//      keys are >= tau, so no key below tau can be in the answer;
+//      keys are >= tau, so no key below tau can be in the answer. Once both
+//      rows of the warp keep k-1 keys, the worst kept key alone is tried first,
+//      and the 32-element network runs only when more than 32 values reach it;
 //   3. the keys >= tau (typically 15-30) are compacted into shared memory (each
 //      lane reads its survivors back from its staged values); every survivor
 //      counts the survivors that beat it, and the k-1 with the lowest counts
@@ -175,16 +177,12 @@ __device__ __forceinline__ int row_loc(const RowCursor& c, int Bk, int bk_shift,
 // Ranks each half's staged chunk (sv) into the kfar best keys the half kept so
 // far (best: half-lane i < kfar holds the i-th best, descending). m0, m1: the
 // lane's two group maxima.
-__device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1, uint64_t* buf,
-                                           int c0, int kfar, int hl, uint64_t& best,
-                                           float& best_min) {
-  // threshold: the kfar-th largest group max (>= kfar values reach it) or the
-  // worst value kept so far, whichever is larger
-  sort32h_desc(m0, m1, hl);
-  float tau = __shfl_sync(kAll, (kfar - 1) & 1 ? m1 : m0, (kfar - 1) >> 1, 16);
-  tau = fmaxf(tau, best_min);
-  // survivors (>= tau; ties at tau are kept and settled by the keys)
-  uint32_t mask = 0;
+// survivor mask of the lane's staged values (>= tau; ties at tau are kept and
+// settled by the keys), the kept entries >= tau, and the half's prefix count
+__device__ __forceinline__ void survivors(const float4* sv, float tau, int kfar, int hl,
+                                          uint64_t best, uint32_t& mask, bool& keep_old,
+                                          int& cnt, int& incl, int& total) {
+  mask = 0;
 #pragma unroll 2
   for (int i = 0; i < 8; ++i) {
     const float4 x = sv[i * 16 + hl];
@@ -192,15 +190,39 @@ __device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1,
                         (x.z >= tau ? 4u : 0u) | (x.w >= tau ? 8u : 0u);
     mask |= m4 << (4 * i);
   }
-  const bool keep_old = hl < kfar && best != 0 && key_value(best) >= tau;
-  const int cnt = __popc(mask) + (keep_old ? 1 : 0);
-  int incl = cnt;
+  keep_old = hl < kfar && best != 0 && key_value(best) >= tau;
+  cnt = __popc(mask) + (keep_old ? 1 : 0);
+  incl = cnt;
 #pragma unroll
   for (int off = 1; off < 16; off <<= 1) {
     const int y = __shfl_up_sync(kAll, incl, off, 16);
     if (hl >= off) incl += y;
   }
-  const int total = __shfl_sync(kAll, incl, 15, 16);
+  total = __shfl_sync(kAll, incl, 15, 16);
+}
+
+__device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1, uint64_t* buf,
+                                           int c0, int kfar, int hl, uint64_t& best,
+                                           float& best_min) {
+  uint32_t mask;
+  bool keep_old;
+  int cnt, incl, total;
+  // once both halves keep kfar entries, their worst kept score is a threshold
+  // of its own (kfar values reach it); the sorting network below is needed only
+  // when too many of the chunk's values reach it
+  bool settled = false;
+  if (__all_sync(kAll, best_min > -INFINITY)) {
+    survivors(sv, best_min, kfar, hl, best, mask, keep_old, cnt, incl, total);
+    settled = !__any_sync(kAll, total > kCap);
+  }
+  if (!settled) {
+    // threshold: the kfar-th largest group max (>= kfar values reach it) or the
+    // worst value kept so far, whichever is larger
+    sort32h_desc(m0, m1, hl);
+    float tau = __shfl_sync(kAll, (kfar - 1) & 1 ? m1 : m0, (kfar - 1) >> 1, 16);
+    tau = fmaxf(tau, best_min);
+    survivors(sv, tau, kfar, hl, best, mask, keep_old, cnt, incl, total);
+  }
   const float* svf = reinterpret_cast<const float*>(sv);
   if (!__any_sync(kAll, total > kCap)) {
     int p = incl - cnt;
