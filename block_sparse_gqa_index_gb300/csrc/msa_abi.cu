@@ -150,7 +150,7 @@ size_t msa_sparse_attn_workspace_bytes(int64_t chunk_rows, int64_t N, int H_q, i
                                        int Bk, int k) {
   if (chunk_rows < 1 || N < 1 || H_kv < 1 || Bk < 1 || k < 1) return 0;
   chunk_rows = std::min(chunk_rows, N);
-  return msa::attn_ws_bytes(chunk_rows, ceil_div(N, Bk), H_q, H_kv, d, k);
+  return msa::attn_ws_bytes(chunk_rows, ceil_div(N, Bk), H_q, H_kv, d, k, false, true);
 }
 
 int msa_sparse_attn(const void* q, const void* k, const void* v, const int32_t* block_ids,
@@ -172,12 +172,12 @@ int msa_sparse_attn(const void* q, const void* k, const void* v, const int32_t* 
   int64_t lo = 0, hi = N;
   while (lo < hi) {
     int64_t mid = (lo + hi + 1) / 2;
-    if (msa::attn_ws_bytes(mid, nb, H_q, H_kv, d, topk) <= workspace_bytes) lo = mid;
+    if (msa::attn_ws_bytes(mid, nb, H_q, H_kv, d, topk, false, true) <= workspace_bytes) lo = mid;
     else hi = mid - 1;
   }
   if (lo < 1) return MSA_ERR_WORKSPACE;
   const int64_t chunk = lo;
-  msa::AttnWs ws = msa::attn_ws_carve(workspace, chunk, nb, H_q, H_kv, d, topk);
+  msa::AttnWs ws = msa::attn_ws_carve(workspace, chunk, nb, H_q, H_kv, d, topk, false, true);
   msa::Diag dg = diag();
   for (int64_t q0 = 0; q0 < N; q0 += chunk) {
     int64_t q1 = std::min(N, q0 + chunk);

@@ -18,6 +18,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <climits>
+
 #include "msa_kernels.h"
 #include "msa_sm100.cuh"
 
@@ -34,6 +36,110 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 inline int64_t max_tiles(int64_t chunk, int64_t n_b, int H_q, int H_kv, int k) {
   const int64_t qt = kTileRows / (H_q / H_kv);
   return (chunk * H_kv * k + qt - 1) / qt + n_b;
+}
+
+// ------------------------------------------------------------ shared blocks
+// Query tiles of qt consecutive rows (at most 32 here, one per lane). A block
+// that at least half of a full tile's queries selected in group g is "shared":
+// its (query, slot) entries leave the block-outer tiles and go to the
+// query-outer pass (attn_shared_tc_kernel), which runs the tile's queries
+// against each of their shared blocks with the output accumulated across
+// blocks, and writes one record per (query, group) for all of them. Candidates
+// are the blocks of four probe queries of the tile (first, a third, two
+// thirds, last); a block selected by at least half the queries is missed only
+// if none of the four probes selected it, and then simply stays block-outer.
+constexpr int kShMax = 16;  // shared blocks kept per (query tile, group)
+
+__global__ void __launch_bounds__(256)
+shared_sets_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1, int n_g, int k,
+                   int qt, int64_t n_qt, int32_t* __restrict__ shlist,
+                   int32_t* __restrict__ rowmask, int32_t* __restrict__ rec_of, int64_t rec0) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; w < n_qt * n_g;
+       w += nw) {
+    const int64_t u = w / n_g;
+    const int g = (int)(w % n_g);
+    const int64_t t0 = q0 + u * qt;
+    const int64_t left = q1 - t0;
+    const int nq = (int)(left < qt ? left : qt);
+    const bool has_q = lane < nq;
+    const int64_t t = t0 + lane;
+    // this lane's query: its usable block ids (others -1)
+    int id[kMaxK];
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+      int v = -1;
+      if (has_q && s < k) {
+        v = ids[(t * n_g + g) * k + s];
+        if (v < 0 || (int64_t)v > t / kBk) v = -1;
+      }
+      id[s] = v;
+    }
+    int my_entry = -1;  // lane j holds shared block j
+    int n_sh = 0;
+    if (2 * nq >= qt) {  // tiles with too few queries keep every block block-outer
+      const int thr = (nq + 1) / 2;
+#pragma unroll 1
+      for (int pb = 0; pb < 4; ++pb) {
+        const int pi = pb == 0 ? 0 : (pb == 3 ? nq - 1 : pb * nq / 3);
+#pragma unroll
+        for (int s = 0; s < kMaxK; ++s) {
+          if (s >= k) break;
+          const int c = __shfl_sync(0xffffffffu, id[s], pi);
+          if (c < 0 || n_sh >= kShMax || __any_sync(0xffffffffu, my_entry == c)) continue;
+          bool mine = false;
+#pragma unroll
+          for (int s2 = 0; s2 < kMaxK; ++s2) mine |= id[s2] == c;
+          if (__popc(__ballot_sync(0xffffffffu, mine)) >= thr) {
+            if (lane == n_sh) my_entry = c;
+            ++n_sh;
+          }
+        }
+      }
+    }
+    // shared blocks in ascending order (a canonical order of accumulation,
+    // whichever probe found them): bitonic sort over the first 16 lanes
+    {
+      int v = lane < n_sh ? my_entry : INT_MAX;
+#pragma unroll
+      for (int size = 2; size <= 16; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          const int p = __shfl_xor_sync(0xffffffffu, v, stride);
+          const bool up = (lane & size) == 0, lower = (lane & stride) == 0;
+          v = (lower == up) ? min(v, p) : max(v, p);
+        }
+      my_entry = lane < n_sh ? v : -1;
+    }
+    // the slots of this lane's query that the shared blocks cover, and which of
+    // the shared blocks it selected
+    uint32_t slots = 0, sel = 0;
+#pragma unroll 1
+    for (int j = 0; j < n_sh; ++j) {
+      const int c = __shfl_sync(0xffffffffu, my_entry, j);
+#pragma unroll
+      for (int s = 0; s < kMaxK; ++s)
+        if (id[s] == c) {
+          slots |= 1u << s;
+          sel |= 1u << j;
+        }
+    }
+    if (lane < kShMax) shlist[w * kShMax + lane] = my_entry;
+    if (has_q) {
+      const int64_t row = (t - q0) * n_g + g;
+      rowmask[row] = (int32_t)(slots | (sel << 16));
+      // the first covered slot points at the (query, group)'s shared record
+      // (item-major: the records of item w are contiguous)
+      bool first = true;
+#pragma unroll
+      for (int s = 0; s < kMaxK; ++s)
+        if ((slots >> s) & 1u) {
+          rec_of[row * k + s] = first ? (int32_t)(rec0 + w * qt + lane) : -1;
+          first = false;
+        }
+    }
+  }
 }
 
 // ------------------------------------------------------------ bucketing passes
@@ -67,8 +173,14 @@ __device__ __forceinline__ int bucket_of(const int2* __restrict__ qinfo, int id,
 // Counts the queries of every bucket; a slot with no usable block gets no
 // partial record (rec_of = -1). Lanes of a warp that hit the same bucket add
 // their count with one atomic (popular blocks are selected by most queries).
+// entries of the chunk that the shared-block pass covers (rowmask bits 0-15)
+__device__ __forceinline__ bool is_shared(const int32_t* __restrict__ rowmask, int e, int k) {
+  return rowmask && ((rowmask[e / k] >> (e % k)) & 1);
+}
+
 __global__ void bucket_count_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1,
                                     int n_g, int k, int64_t nb, const int2* __restrict__ qinfo,
+                                    const int32_t* __restrict__ rowmask,
                                     int32_t* __restrict__ counts, int32_t* __restrict__ rec_of,
                                     Diag dg) {
   const int n = (int)((q1 - q0) * n_g * k);  // entries of the chunk (< 2^31)
@@ -78,7 +190,7 @@ __global__ void bucket_count_kernel(const int32_t* __restrict__ ids, int64_t q0,
   for (int base = blockIdx.x * blockDim.x; base < n; base += gridDim.x * blockDim.x) {
     const int e = base + threadIdx.x;
     int bk = -1;
-    if (e < n) {
+    if (e < n && !is_shared(rowmask, e, k)) {
       const int row = row0 + e / k;
       bk = bucket_of(qinfo, cids[e], row, row / n_g, n_g, (int)nb, dg);
       if (bk < 0) rec_of[e] = -1;
@@ -104,7 +216,8 @@ __device__ __forceinline__ void slice_of(int n, int c, int& e0, int& e1) {
 
 __global__ void __launch_bounds__(1024)
 bucket_count_smem_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1, int n_g, int k,
-                         int64_t nb, const int2* __restrict__ qinfo, int32_t* __restrict__ counts,
+                         int64_t nb, const int2* __restrict__ qinfo,
+                         const int32_t* __restrict__ rowmask, int32_t* __restrict__ counts,
                          int32_t* __restrict__ percta, int32_t* __restrict__ rec_of, Diag dg) {
   extern __shared__ int32_t hist[];
   const int n_b = (int)(n_g * nb);
@@ -116,6 +229,7 @@ bucket_count_smem_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1
   int e0, e1;
   slice_of(n, blockIdx.x, e0, e1);
   for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+    if (is_shared(rowmask, e, k)) continue;
     const int row = row0 + e / k;
     const int bk = bucket_of(qinfo, cids[e], row, row / n_g, n_g, (int)nb, dg);
     if (bk >= 0) atomicAdd(&hist[bk], 1);
@@ -145,7 +259,8 @@ __global__ void bucket_cta_base_kernel(const int32_t* __restrict__ offsets, int 
 
 __global__ void __launch_bounds__(1024)
 bucket_fill_smem_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1, int n_g, int k,
-                        int64_t nb, const int2* __restrict__ qinfo, int qt,
+                        int64_t nb, const int2* __restrict__ qinfo,
+                        const int32_t* __restrict__ rowmask, int qt,
                         const int32_t* __restrict__ offsets,
                         const int32_t* __restrict__ tile_off, const int32_t* __restrict__ percta,
                         int32_t* __restrict__ entries, int32_t* __restrict__ rec_of) {
@@ -161,6 +276,7 @@ bucket_fill_smem_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1,
   int e0, e1;
   slice_of(n, blockIdx.x, e0, e1);
   for (int e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+    if (is_shared(rowmask, e, k)) continue;
     const int rl = e / k;
     const int row = row0 + rl;
     const int t = row / n_g;
@@ -217,7 +333,7 @@ __global__ void bucket_scan_kernel(const int32_t* __restrict__ counts, int64_t n
 // that hit the same bucket take consecutive positions from one atomic.
 __global__ void bucket_fill_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1,
                                    int n_g, int k, int64_t nb, const int2* __restrict__ qinfo,
-                                   int qt,
+                                   const int32_t* __restrict__ rowmask, int qt,
                                    const int32_t* __restrict__ offsets,
                                    const int32_t* __restrict__ tile_off,
                                    int32_t* __restrict__ cursor, int32_t* __restrict__ entries,
@@ -230,7 +346,7 @@ __global__ void bucket_fill_kernel(const int32_t* __restrict__ ids, int64_t q0, 
   for (int base = blockIdx.x * blockDim.x; base < n; base += gridDim.x * blockDim.x) {
     const int e = base + threadIdx.x;
     int bk = -1, ent = 0;
-    if (e < n) {
+    if (e < n && !is_shared(rowmask, e, k)) {
       const int rl = e / k;
       const int row = row0 + rl;
       const int t = row / n_g;
@@ -767,6 +883,392 @@ attn_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
   if (warp == 1) tmem_dealloc(tmem_base, 512);
 }
 
+// ------------------------------------------------- shared blocks, query-outer
+// One item = one (query tile, group) with its shared blocks (shared_sets_kernel):
+// the tile's qt queries x G heads (128 rows, query-major: row r = query r / G,
+// head r % G, loaded by one TMA box per 64-column chunk) against each shared
+// block in turn, the output accumulated in TMEM across the blocks. A row whose
+// query did not select a block, or whose local block masks it, takes P = 0
+// there. Online softmax with a lazy rescale: a row keeps the running max it
+// used for P unless a block's max exceeds it by more than 8 (a factor 2^8 in
+// P, well within bf16 / fp32); only then does it rescale its O row in TMEM and
+// its sum, and move its max. S(j + 1) is issued once P.V(j) has completed, so
+// when the softmax sees S(j) its O holds every block before j. The item ends
+// with its qt records (one per query, in the format of the block-outer
+// partials, item-major so that they are contiguous), staged in the V buffer
+// (free once the item's last P.V has completed) and written by one bulk copy;
+// the merge combines them with the block-outer partials.
+//
+// Each CTA runs one item at a time, as a chain S -> softmax -> P.V -> S; two
+// CTAs per SM (256 TMEM columns and about 100 KB of shared memory each) keep
+// the tensor core busy with one while the other's softmax runs. 8 warps:
+//   warp 0     TMA: each item's Q and each block's K (one buffer each);
+//   warp 1     TMEM owner; MMA issuer;
+//   warp 2     TMA: each block's V (one buffer, also the record staging);
+//   warp 3     bulk copy of the staged records;
+//   warps 4-7  softmax and epilogue, one row per thread.
+template <int D>
+struct ShSmem {
+  static constexpr int kQBytes = kTileRows * D * 2;
+  static constexpr int kKVBytes = kBk * D * 2;
+  // an item's records: qt (G * D * 2 + G * 4) bytes = 128 (2 D + 4), any G
+  static constexpr int kStgBytes = kTileRows * (2 * D + 4);
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQBytes;
+  static constexpr int kVOff = kKOff + kKVBytes;
+  static constexpr int kVBytes = kStgBytes > kKVBytes ? kStgBytes : kKVBytes;
+  static constexpr int kBarOff = kVOff + kVBytes;
+  // q_full, q_empty, k_full, k_empty, v_full, v_empty, s_full, p_full,
+  // pv_done, o_full, o_free, stg_full, stg_free, done
+  static constexpr int kNumBars = 14;
+  static constexpr int kBytes = kBarOff + kNumBars * 8 + 32;
+};
+static_assert(2 * (ShSmem<128>::kBytes + 1024) <= 233472, "two shared-block CTAs per SM");
+constexpr int kShThreads = 256;
+
+// number of shared blocks of item w (its list is -1 past them)
+__device__ __forceinline__ int sh_count(const int32_t* __restrict__ shlist, int64_t w) {
+  const int4* p = reinterpret_cast<const int4*>(shlist + w * kShMax);
+  int c = 0;
+#pragma unroll
+  for (int i = 0; i < kShMax / 4; ++i) {
+    const int4 v = __ldg(p + i);
+    c += (v.x >= 0) + (v.y >= 0) + (v.z >= 0) + (v.w >= 0);
+  }
+  return c;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kShThreads, 2)
+attn_shared_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, int64_t q0, int64_t q1,
+                      int H_q, int H_kv, float scale_log2, int64_t n_items,
+                      const int32_t* __restrict__ shlist, const int32_t* __restrict__ rowmask,
+                      int64_t rec0, unsigned char* __restrict__ part, Diag dg) {
+  using namespace sm100;
+  using S = ShSmem<D>;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  if (smem_u32(smem) & 1023) {
+    if (threadIdx.x == 0) report(dg, kStatusUnsupported);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_empty = bars + 3;
+  uint64_t* v_full = bars + 4;
+  uint64_t* v_empty = bars + 5;
+  uint64_t* s_full = bars + 6;
+  uint64_t* p_full = bars + 7;
+  uint64_t* pv_done = bars + 8;
+  uint64_t* o_full = bars + 9;
+  uint64_t* o_free = bars + 10;
+  uint64_t* stg_full = bars + 11;
+  uint64_t* stg_free = bars + 12;
+  uint64_t* done_bar = bars + 13;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = H_q / H_kv;
+  const int qt = kTileRows / G;
+  const int n_g = H_kv;
+  const int rec = attn_rec_bytes(G, D);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S::kNumBars; ++i) mbar_init(&bars[i], 1);
+    mbar_init(p_full, 4);
+    mbar_init(o_free, 4);
+    mbar_init(stg_full, 4);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  // warpgroup 0 (TMA, MMA, store) runs on 48 registers per thread, the
+  // softmax warpgroup on 208: 128 x 48 + 128 x 208 = 256 x 128, the launch's share
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 48;\n" ::: "memory");
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ TMA: Q, K
+      uint32_t it = 0, e = 0;
+      bool q_armed = false, k_armed = false;
+      bool ok = true;
+      for (int64_t w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const int cnt = sh_count(shlist, w);
+        if (cnt == 0) continue;
+        const int g = (int)(w % n_g);
+        if (!mbar_wait(q_empty, (it & 1) ^ 1, abort_flag, dg)) break;
+        mbar_arrive_expect_tx(q_full, S::kQBytes);
+        const int64_t t0 = q0 + (w / n_g) * qt;
+        for (int ch = 0; ch < D / 64; ++ch)
+          tma_load_3d(smem + S::kQOff + ch * kTileRows * 128, &tm_q, q_full, ch * 64, g * G,
+                      (int32_t)t0);
+        q_armed = true;
+        for (int j = 0; j < cnt; ++j, ++e) {
+          const int b = shlist[w * kShMax + j];
+          if (!mbar_wait(k_empty, (e & 1) ^ 1, abort_flag, dg)) { ok = false; break; }
+          mbar_arrive_expect_tx(k_full, S::kKVBytes);
+          for (int ch = 0; ch < D / 64; ++ch)
+            tma_load_3d(smem + S::kKOff + ch * kBk * 128, &tm_k, k_full, ch * 64, g, b * kBk);
+          k_armed = true;
+        }
+        ++it;
+      }
+      if (*abort_flag) {  // let issued copies land before shared memory goes
+        if (q_armed) mbar_drain(q_full, (it - (ok ? 1 : 0)) & 1);
+        if (k_armed) mbar_drain(k_full, (e - 1) & 1);
+      }
+    } else if (warp == 2 && lane == 0) {
+      // ------------------------------------------------------------ TMA: V
+      // A new item's first V overwrites the staged records of the previous
+      // item, so it waits for their bulk copy to have read them.
+      uint32_t it = 0, e = 0;
+      bool armed = false;
+      bool ok = true;
+      for (int64_t w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const int cnt = sh_count(shlist, w);
+        if (cnt == 0) continue;
+        const int g = (int)(w % n_g);
+        for (int j = 0; j < cnt; ++j, ++e) {
+          const int b = shlist[w * kShMax + j];
+          if (!mbar_wait(v_empty, (e & 1) ^ 1, abort_flag, dg) ||
+              (j == 0 && it > 0 && !mbar_wait(stg_free, (it - 1) & 1, abort_flag, dg))) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(v_full, S::kKVBytes);
+          for (int ch = 0; ch < D / 64; ++ch)
+            tma_load_3d(smem + S::kVOff + ch * kBk * 128, &tm_v, v_full, ch * 64, g, b * kBk);
+          armed = true;
+        }
+        ++it;
+      }
+      if (*abort_flag && armed) mbar_drain(v_full, (e - (ok ? 1 : 0)) & 1);
+    } else if (warp == 3 && lane == 0) {
+      // ------------------------------------------------------------ records out
+      uint32_t it = 0;
+      for (int64_t w = blockIdx.x; w < n_items; w += gridDim.x) {
+        if (sh_count(shlist, w) == 0) continue;
+        if (!mbar_wait(stg_full, it & 1, abort_flag, dg)) break;
+        bulk_store(part + (size_t)(rec0 + w * qt) * rec, smem + S::kVOff, (uint32_t)(qt * rec));
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(stg_free);
+        ++it;
+      }
+      bulk_wait_all();
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBk);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, false, true);
+      const uint32_t q_base = smem_u32(smem + S::kQOff);
+      const uint32_t k_base = smem_u32(smem + S::kKOff), v_base = smem_u32(smem + S::kVOff);
+      uint32_t it = 0, e = 0;
+      bool ok = true;
+      for (int64_t w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+        const int cnt = sh_count(shlist, w);
+        if (cnt == 0) continue;
+        for (int j = 0; j < cnt; ++j, ++e) {
+          // S(j) = Q K(j)^T over the S / P columns, once K(j) has landed and
+          // P.V(j - 1), which read them, has completed
+          if ((j == 0 && !mbar_wait(q_full, it & 1, abort_flag, dg)) ||
+              !mbar_wait(k_full, e & 1, abort_flag, dg) ||
+              (e > 0 && !mbar_wait(pv_done, (e - 1) & 1, abort_flag, dg))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int c = kk / 4, off = (kk % 4) * 32;
+            mma_bf16_ss(tmem_base, desc_kmajor_sw128(q_base + c * kTileRows * 128 + off),
+                        desc_kmajor_sw128(k_base + c * kBk * 128 + off), idesc_s,
+                        kk > 0 ? 1u : 0u);
+          }
+          mma_commit(s_full);
+          mma_commit(k_empty);
+          if (j + 1 == cnt) mma_commit(q_empty);
+          // O += P(j) V(j), once the softmax has written P(j), V(j) has landed
+          // and (first block) the previous item's epilogue has read O
+          if (!mbar_wait(p_full, e & 1, abort_flag, dg) ||
+              (j == 0 && it > 0 && !mbar_wait(o_free, (it - 1) & 1, abort_flag, dg)) ||
+              !mbar_wait(v_full, e & 1, abort_flag, dg)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBk / 16; ++kk) {
+            const uint64_t bd = desc_mnmajor_sw128(v_base + kk * 16 * 128, kBk * 128);
+            mma_bf16_ts(tmem_base + 128, tmem_base + (uint32_t)(kk * 8), bd, idesc_o,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(v_empty);
+          mma_commit(pv_done);
+          if (j + 1 == cnt) mma_commit(o_full);
+        }
+        ++it;
+      }
+      // every MMA issued by this thread has completed once done_bar flips
+      mma_commit(done_bar);
+      mbar_drain(done_bar, 0);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory");
+    // ------------------------------------------------------------ softmax + epilogue
+    const int qq = warp & 3;
+    const int row = qq * 32 + lane;
+    const int qi = row / G, hi = row % G;
+    const uint32_t lane_off = (uint32_t)(qq * 32) << 16;
+    const uint32_t ts = tmem_base + lane_off;
+    const uint32_t srow = smem_u32(smem + S::kVOff) + (uint32_t)(qi * rec + hi * D * 2);
+    uint32_t e = 0, it = 0;
+    bool ok = true;
+    for (int64_t w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const int cnt = sh_count(shlist, w);
+      if (cnt == 0) continue;
+      const int g = (int)(w % n_g);
+      const int64_t t = q0 + (w / n_g) * qt + qi;
+      const bool valid = t < q1;
+      const uint32_t sel = valid ? (uint32_t)rowmask[(t - q0) * n_g + g] >> 16 : 0u;
+      const int64_t loc = t / kBk;
+      float m = -INFINITY, l = 0.f;  // running max (log2 units) used for P, and sum
+      for (int j = 0; j < cnt; ++j, ++e) {
+        const int b = shlist[w * kShMax + j];
+        const int lim = ((sel >> j) & 1) ? (b == loc ? (int)(t - (int64_t)b * kBk) + 1 : kBk) : 0;
+        int got = 0;
+        if (lane == 0) got = mbar_wait(s_full, e & 1, abort_flag, dg);
+        if (!__shfl_sync(0xffffffffu, got, 0)) { ok = false; break; }
+        tc_fence_after();
+        // every row takes all of the block or none of it, unless it is the
+        // rows' local block: then the row max comes with the loads
+        const bool whole = !__any_sync(0xffffffffu, lim > 0 && lim < kBk);
+        uint32_t r[128];
+        float mx;
+        if (whole) {
+          float m0, m1, m2, m3;
+          tmem_ld32_max(ts, *reinterpret_cast<uint32_t(*)[32]>(&r[0]), m0);
+          tmem_ld32_max(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]), m1);
+          tmem_ld32_max(ts + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]), m2);
+          tmem_ld32_max(ts + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]), m3);
+          tmem_ld_wait();
+          mx = lim > 0 ? fmaxf(fmax3(m0, m1, m2), m3) : -INFINITY;
+        } else {
+          tmem_ld32(ts, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld32(ts + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          tmem_ld32(ts + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[64]));
+          tmem_ld32(ts + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[96]));
+          tmem_ld_wait();
+          mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c < lim) mx = fmaxf(mx, __uint_as_float(r[c]));
+        }
+        const float mb = mx * scale_log2;  // -inf when the row takes nothing here
+        const bool grow = lim > 0 && m > -INFINITY && mb > m + 8.f;
+        if (__any_sync(0xffffffffu, grow)) {
+          // rescale the O rows whose max grows by more than 8
+          const float f = grow ? ex2_approx(m - mb) : 1.f;
+          const uint64_t f2 = f2_pack(f, f);
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(ts + 128 + c, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 32; x += 2) {
+              float x0, x1;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[x]), __uint_as_float(o[x + 1])), f2), x0,
+                        x1);
+              o[x] = __float_as_uint(x0);
+              o[x + 1] = __float_as_uint(x1);
+            }
+            tmem_st32(ts + 128 + c, o);
+          }
+          tmem_st_wait();
+          l *= f;
+          if (grow) m = mb;
+        }
+        if (lim > 0 && m == -INFINITY) m = mb;  // the row's first block
+        // P = exp2(s * c - m); a row that takes nothing here gets exp2(-inf) = 0
+        const float nm = lim > 0 ? -m : -INFINITY;
+        const uint64_t sc2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(nm, nm);
+        uint64_t l2 = f2_pack(0.f, 0.f);
+#pragma unroll
+        for (int c2 = 0; c2 < 64; ++c2) {
+          float p0, p1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * c2]), __uint_as_float(r[2 * c2 + 1])), sc2,
+                           nm2), p0, p1);
+          p0 = ex2_approx(p0);
+          p1 = ex2_approx(p1);
+          if (!whole) {
+            p0 = 2 * c2 < lim ? p0 : 0.f;
+            p1 = 2 * c2 + 1 < lim ? p1 : 0.f;
+          }
+          l2 = f2_add(l2, f2_pack(p0, p1));
+          r[c2] = pack_bf16x2(p0, p1);
+        }
+        float l0, l1;
+        f2_unpack(l2, l0, l1);
+        l += l0 + l1;
+        tmem_st32(ts, *reinterpret_cast<const uint32_t(*)[32]>(&r[0]));
+        tmem_st32(ts + 32, *reinterpret_cast<const uint32_t(*)[32]>(&r[32]));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      if (!ok) break;
+      // the item's records: O / l in bf16 and the LSE of this thread's (query,
+      // head), staged in the V buffer (its last P.V has completed)
+      int got = 0;
+      if (lane == 0) got = mbar_wait(o_full, it & 1, abort_flag, dg);
+      if (!__shfl_sync(0xffffffffu, got, 0)) break;
+      tc_fence_after();
+      uint32_t o[D];
+#pragma unroll
+      for (int c = 0; c < D; c += 32)
+        tmem_ld32(ts + 128 + c, *reinterpret_cast<uint32_t(*)[32]>(&o[c]));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const uint64_t inv2 = f2_pack(inv, inv);
+#pragma unroll
+      for (int v = 0; v < D / 8; ++v) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float x0, x1;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(o[8 * v + 2 * u]),
+                                   __uint_as_float(o[8 * v + 2 * u + 1])), inv2), x0, x1);
+          wv[u] = pack_bf16x2(x0, x1);
+        }
+        st_shared_v4(srow + v * 16, wv[0], wv[1], wv[2], wv[3]);
+      }
+      *reinterpret_cast<float*>(smem + S::kVOff + qi * rec + G * D * 2 + hi * 4) =
+          (m + __log2f(l)) * 0.69314718055994531f;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(stg_full);
+      ++it;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, 256);
+}
+
 // ---------------------------------------------------------------------- merge
 // partials: one record per (query, group, slot) holding the G heads' O rows
 // (bf16) and then their LSEs, found through rec_of (-1: the slot has none).
@@ -1055,11 +1557,58 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, int64_t N
   return cudaGetLastError();
 }
 
+// Q [N, H_q, D] seen as (D, H_q, N) with a box of all G heads of qt queries
+bool make_map_q_tile(CUtensorMap* m, const void* base, int64_t N, int H_q, int D, int G, int qt) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess || qr != cudaDriverEntryPointSuccess)
+      return false;
+    fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H_q, (cuuint64_t)N};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H_q * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)qt};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_shared(const void* q, const void* kk, const void* v, int64_t N, int64_t q0,
+                          int64_t q1, int H_q, int H_kv, float scale_log2, const AttnWs& ws,
+                          const Diag& dg, cudaStream_t st) {
+  const int G = H_q / H_kv, qt = kTileRows / G;
+  CUtensorMap tq, tk, tv;
+  if (!make_map_q_tile(&tq, q, N, H_q, D, G, qt) || !make_map_kv(&tk, kk, N, H_kv, D) ||
+      !make_map_kv(&tv, v, N, H_kv, D))
+    return cudaErrorInvalidValue;
+  const int smem = ShSmem<D>::kBytes;
+  cudaError_t e = cudaFuncSetAttribute(attn_shared_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t n_items = (q1 - q0 + qt - 1) / qt * H_kv;
+  attn_shared_tc_kernel<D><<<2 * sm_count(), kShThreads, smem, st>>>(tq, tk, tv, q0, q1, H_q, H_kv,
+                                                          scale_log2, n_items, ws.shlist,
+                                                          ws.rowmask, ws.shared_rec0, ws.part, dg);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
+// the shared-block pass needs query tiles of at most 32 queries (G >= 4)
+inline bool shared_pass(bool with_shared, int H_q, int H_kv) {
+  return with_shared && H_q / H_kv >= 4;
+}
+
 size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k,
-                     bool with_tbase) {
+                     bool with_tbase, bool with_shared) {
   int64_t n_b = (int64_t)H_kv * nb;
+  const int G = H_q / H_kv, qt = kTileRows / G;
+  const bool sh = shared_pass(with_shared, H_q, H_kv);
   size_t s = 0;
   s += align256((size_t)n_b * 4);        // counts
   s += align256((size_t)(n_b + 1) * 4);  // offsets
@@ -1070,14 +1619,22 @@ size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k,
   s += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * 16);
   if (with_tbase) s += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * 4);
   s += align256((size_t)chunk * H_kv * k * 4);
-  s += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * (kTileRows / (H_q / H_kv)) *
-                attn_rec_bytes(H_q / H_kv, d));
+  if (sh) {
+    s += align256((size_t)chunk * H_kv * 4);                                // rowmask
+    s += align256((size_t)((chunk + qt - 1) / qt) * H_kv * kShMax * 4);     // shlist
+  }
+  // block-outer partials, then the shared-block records (qt per item)
+  const size_t sh_recs = sh ? (size_t)((chunk + qt - 1) / qt) * H_kv * qt : 0;
+  s += align256(((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * qt + sh_recs) *
+                attn_rec_bytes(G, d));
   return s;
 }
 
 AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k,
-                     bool with_tbase) {
+                     bool with_tbase, bool with_shared) {
   int64_t n_b = (int64_t)H_kv * nb;
+  const int G = H_q / H_kv, qt = kTileRows / G;
+  const bool sh = shared_pass(with_shared, H_q, H_kv);
   unsigned char* p = (unsigned char*)ws;
   AttnWs w;
   w.counts = (int32_t*)p;   p += align256((size_t)n_b * 4);
@@ -1097,6 +1654,11 @@ AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int
     p += align256((size_t)max_tiles(chunk, n_b, H_q, H_kv, k) * 4);
   }
   w.rec_of = (int32_t*)p;   p += align256((size_t)chunk * H_kv * k * 4);
+  if (sh) {
+    w.rowmask = (int32_t*)p;  p += align256((size_t)chunk * H_kv * 4);
+    w.shlist = (int32_t*)p;   p += align256((size_t)((chunk + qt - 1) / qt) * H_kv * kShMax * 4);
+    w.shared_rec0 = max_tiles(chunk, n_b, H_q, H_kv, k) * qt;
+  }
   w.part = p;
   return w;
 }
@@ -1112,25 +1674,34 @@ cudaError_t launch_bucketing(const int32_t* ids, int64_t q0, int64_t q1, int H_q
   note_launches(n_b <= kSmemBucketsMax ? 6 : 5);  // memset, count, scan, (base,) fill, map
   cudaError_t e = cudaMemsetAsync(ws.counts, 0, (size_t)n_b * 4, st);
   if (e != cudaSuccess) return e;
+  if (ws.rowmask) {  // blocks shared by the query tiles leave the block-outer buckets
+    note_launches(1);
+    const int64_t n_qt = (q1 - q0 + qt - 1) / qt;
+    const int64_t warps = n_qt * H_kv;
+    shared_sets_kernel<<<(unsigned)std::min<int64_t>((warps * 32 + 255) / 256, 152 * 32), 256, 0,
+                         st>>>(ids, q0, q1, H_kv, k, qt, n_qt, ws.shlist, ws.rowmask, ws.rec_of,
+                               ws.shared_rec0);
+  }
   int64_t n = (q1 - q0) * H_kv * k;
   const bool smem_buckets = n_b <= kSmemBucketsMax;
   unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 32);
   if (smem_buckets)
     bucket_count_smem_kernel<<<kBucketCtas, 1024, n_b * 4, st>>>(
-        ids, q0, q1, H_kv, k, nb, bt.qinfo, ws.counts, ws.percta, ws.rec_of, dg);
+        ids, q0, q1, H_kv, k, nb, bt.qinfo, ws.rowmask, ws.counts, ws.percta, ws.rec_of, dg);
   else
-    bucket_count_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, bt.qinfo, ws.counts,
-                                              ws.rec_of, dg);
+    bucket_count_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, bt.qinfo, ws.rowmask,
+                                              ws.counts, ws.rec_of, dg);
   bucket_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, n_b, qt, ws.offsets, ws.tile_off, ws.cursor);
   if (smem_buckets) {
     bucket_cta_base_kernel<<<(unsigned)((n_b + 255) / 256), 256, 0, st>>>(ws.offsets, (int)n_b,
                                                                           kBucketCtas, ws.percta);
     bucket_fill_smem_kernel<<<kBucketCtas, 1024, n_b * 4, st>>>(
-        ids, q0, q1, H_kv, k, nb, bt.qinfo, qt, ws.offsets, ws.tile_off, ws.percta, ws.entries,
-        ws.rec_of);
+        ids, q0, q1, H_kv, k, nb, bt.qinfo, ws.rowmask, qt, ws.offsets, ws.tile_off, ws.percta,
+        ws.entries, ws.rec_of);
   } else {
-    bucket_fill_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, bt.qinfo, qt, ws.offsets,
-                                             ws.tile_off, ws.cursor, ws.entries, ws.rec_of);
+    bucket_fill_kernel<<<grid, 256, 0, st>>>(ids, q0, q1, H_kv, k, nb, bt.qinfo, ws.rowmask, qt,
+                                             ws.offsets, ws.tile_off, ws.cursor, ws.entries,
+                                             ws.rec_of);
   }
   const int64_t tiles_max = max_tiles(q1 - q0, n_b, H_q, H_kv, k);
   tile_map_kernel<<<(unsigned)std::min<int64_t>((tiles_max + 255) / 256, 152 * 16), 256, 0, st>>>(
@@ -1156,6 +1727,12 @@ cudaError_t launch_sparse_attn_chunk(const void* q, const void* kk, const void* 
                : launch_tiles<64>(q, kk, v, N, kv_rows, q0, H_q, H_kv, k, scale_log2, nb, ws,
                                   tbase, n_b, dg, st);
   if (e != cudaSuccess) return e;
+  if (ws.rowmask) {
+    note_launches(1);
+    e = d == 128 ? launch_shared<128>(q, kk, v, N, q0, q1, H_q, H_kv, scale_log2, ws, dg, st)
+                 : launch_shared<64>(q, kk, v, N, q0, q1, H_q, H_kv, scale_log2, ws, dg, st);
+    if (e != cudaSuccess) return e;
+  }
   if (G * d <= 1024) {
     const int64_t nw = (q1 - q0) * H_kv;  // one warp per (query, group)
     const unsigned mg = (unsigned)std::min<int64_t>((nw * 32 + 255) / 256, 152 * 64);

@@ -62,16 +62,24 @@ struct AttnWs {
   int4* tinfo;        // per tile: K / V row, first entry, queries | group << 8, end tile
   int32_t* tbase;     // per tile: query row at the block's first key (paged batches only)
   int32_t* rec_of;    // [chunk, n_g, k]: partial record of each (query, group, slot), or -1
-  unsigned char* part;  // [tiles, qt] records of attn_rec_bytes(G, d) bytes, tile-major
+  unsigned char* part;  // [tiles, qt] records of attn_rec_bytes(G, d) bytes, tile-major,
+                        // then (shared pass) one record per (query, group) of the chunk
+  // shared-block pass (null when not carved): per (query, group) row of the
+  // chunk, the slots it covers (bits 0-15) and the tile's shared blocks the
+  // row selected (bits 16-31); per (query tile, group) its shared blocks
+  int32_t* rowmask = nullptr;  // [chunk, n_g]
+  int32_t* shlist = nullptr;   // [query tiles, n_g, 16], -1 padded
+  int64_t shared_rec0 = 0;     // first shared record in part
 };
 // One partial record per (query, group, slot): the G heads' normalised O rows
 // (bf16, d each), then their G LSEs (fp32), padded to a multiple of 16 bytes.
 __host__ __device__ inline int attn_rec_bytes(int G, int d) { return G * d * 2 + (G + 3) / 4 * 16; }
 // with_tbase: room for the per-tile query bases that paged K / V needs
+// with_shared: room for the shared-block pass of single-sequence calls
 size_t attn_ws_bytes(int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k,
-                     bool with_tbase = false);
+                     bool with_tbase = false, bool with_shared = false);
 AttnWs attn_ws_carve(void* ws, int64_t chunk, int64_t nb, int H_q, int H_kv, int d, int k,
-                     bool with_tbase = false);
+                     bool with_tbase = false, bool with_shared = false);
 
 // Geometry of a batch of sequences for the main branch. All null: one
 // sequence whose query row t sits at position t and whose block b starts at

@@ -137,6 +137,18 @@ def test_wait_limit_roundtrip(msa):
     assert msa.msa_set_wait_limit(old) == 123
 
 
+def _shared_pass_bytes(chunk, nb, H_kv=8, k=16, G=4, d=128):
+    """Workspace the single-sequence main branch adds for its shared-block pass:
+    a row mask, 16 shared ids per (query tile, group) and qt records per (query
+    tile, group) after the block-outer partials, each area rounded up to 256 B."""
+    a256 = lambda x: (x + 255) // 256 * 256
+    qt, rec = 128 // G, G * d * 2 + G * 4
+    n_qt = -(-chunk // qt)
+    tiles = (chunk * H_kv * k + qt - 1) // qt + H_kv * nb
+    return a256(chunk * H_kv * 4) + a256(n_qt * H_kv * 16 * 4) + \
+        a256((tiles * qt + n_qt * H_kv * qt) * rec) - a256(tiles * qt * rec)
+
+
 def test_varlen_rejects(msa):
     """Varlen prefill validates the cumulative offsets, the sizes and (for the
     main branch) the per-sequence alignment on the host, before anything is
@@ -180,8 +192,10 @@ def test_varlen_rejects(msa):
     p, keep = cu(0, 7, 5)
     assert msa._ws_attn_varlen(p, 2, 32, 8, 128, 128, 16) == 0
     p, keep = cu(0, 300, 300, 1000)
+    # the single-sequence call also holds the shared-block pass; packed sequences do not
     assert msa._ws_attn_varlen(p, 3, 32, 8, 128, 128, 16) == \
-        8192 + 256 + msa.msa_sparse_attn_workspace_bytes(1000, 9 * 128, 32, 8, 128)
+        8192 + 256 + msa.msa_sparse_attn_workspace_bytes(1000, 9 * 128, 32, 8, 128) - \
+        _shared_pass_bytes(1000, 9)
 
 
 def test_paged_rejects(msa):
@@ -222,7 +236,7 @@ def test_paged_rejects(msa):
     # one pass: 150 queries and 8 + 1 blocks of the two sequences, with the
     # per-tile query bases of paged K / V
     assert fw(cu, kv, 2, 8, 32, 8, 128, 128, 16) > \
-        msa.msa_sparse_attn_workspace_bytes(150, 9 * 128, 32, 8, 128)
+        msa.msa_sparse_attn_workspace_bytes(150, 9 * 128, 32, 8, 128) - _shared_pass_bytes(150, 9)
 
 
 def test_index_fp8_rejects(msa):

@@ -7,9 +7,10 @@ Every invalid value used here addresses memory inside its own tensor (a block
 id between the row's local block and the last block of the sequence, a
 sequence length one page past its page-table row), so a kernel that failed to
 check would compute something wrong, never read out of bounds. Each test
-checks the error code, that every row without invalid data is bit-identical to
-a clean call, how the row with invalid data is treated, and that the next
-clean call gives the clean bits again.
+checks the error code, that the rows without invalid data keep the results of
+a clean call (bit for bit, or to rounding where they share a query tile with a
+planted row in the prefill main branch), how the row with invalid data is
+treated, and that the next clean call gives the clean bits again.
 """
 import numpy as np
 import pytest
@@ -36,7 +37,7 @@ def msa():
 def test_sparse_attn_skips_causally_invalid_ids(msa):
     """A block id after the row's local block (still below nb) is skipped: the
     row attends over its other blocks (the oracle on the ids with that slot
-    emptied), every other row keeps its bits, and the error word says so."""
+    emptied), the other rows keep their results, and the error word says so."""
     w = synth.make("tiny", L=1000, H_q=8, H_kv=2, d=64, d_idx=64)
     qidx = synth.device_tensor(w, synth.T_QIDX)
     kidx = synth.device_tensor(w, synth.T_KIDX)[:, 0].contiguous()
@@ -56,9 +57,19 @@ def test_sparse_attn_skips_causally_invalid_ids(msa):
     assert msa.msa_get_error() == MSA_ERR_INVALID_ARG
     assert msa.msa_get_error() == 0  # read and cleared
     rows_bad = sorted({t for t, _, _, _ in plant})
-    keep = np.setdiff1d(np.arange(w.N), rows_bad)
+    # rows in other query tiles (128 / G queries) keep their bits; rows that
+    # share a tile with a planted row agree to rounding: the tile's blocks
+    # selected by at least half of its queries are combined in one pass, and a
+    # planted id can move a block across that line
+    qt = 128 // (w.H_q // w.H_kv)
+    tiles_bad = {t // qt for t in rows_bad}
+    keep = np.array([t for t in range(w.N) if t // qt not in tiles_bad])
+    near = np.array([t for t in range(w.N) if t // qt in tiles_bad and t not in rows_bad])
     kt = torch.from_numpy(keep).cuda()
     assert torch.equal(out1[kt], out0[kt]) and torch.equal(lse1[kt], lse0[kt])
+    nt = torch.from_numpy(near).cuda()
+    check_close("o near", bf16_to_np(out1[nt]), bf16_to_np(out0[nt]), 1e-2)
+    check_close("lse near", lse1[nt].cpu().numpy(), lse0[nt].cpu().numpy(), 1e-4)
     # the planted rows: attention over their remaining valid blocks
     emptied = bad.cpu().numpy()
     for t, g, s, b in plant:

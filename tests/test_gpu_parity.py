@@ -389,8 +389,11 @@ def test_varlen_index_many_sequences(msa):
 
 
 def test_varlen_equals_single_sequence_calls(msa):
-    """The packed call gives exactly the bits of one single-sequence call per
-    sequence, including with a workspace too small for one pass."""
+    """The packed call gives one single-sequence call's block ids per sequence,
+    bit for bit, and its outputs to rounding (the single-sequence main branch
+    combines the blocks a query tile shares in one pass first, so it adds the
+    same terms in another order), including with a workspace too small for one
+    pass."""
     lens = [300, 1, 1000, 129]
     wls = [synth.make("tiny", L=n, H_q=8, H_kv=2, d=64, d_idx=64, seed=70 + i)
            for i, n in enumerate(lens)]
@@ -410,7 +413,8 @@ def test_varlen_equals_single_sequence_calls(msa):
         o1, l1 = msa.msa_sparse_attn(q[a:b].contiguous(), kk[a:b].contiguous(),
                                      v[a:b].contiguous(), ids1, 128, 0.125)
         assert torch.equal(ids[a:b], ids1)
-        assert torch.equal(out[a:b], o1) and torch.equal(lse[a:b], l1)
+        check_close("o", bf16_to_np(out[a:b]), bf16_to_np(o1), TOL_O)
+        check_close("lse", lse[a:b].cpu().numpy(), l1.cpu().numpy(), 1e-4)
 
 
 # ------------------------------------------------------------------ decode
@@ -788,9 +792,10 @@ def test_paged_prefill_matches_oracle(msa, H_q, H_kv, d):
 
 def test_paged_chunk_equals_full_prefill_rows(msa):
     """A chunk of the last 1000 of 2500 tokens over paged caches gives exactly
-    the bits of rows 1500 .. 2499 of the single-sequence prefill of all 2500
-    tokens (ids, output and LSE), including with a workspace that forces
-    several chunks of query rows."""
+    the block ids of rows 1500 .. 2499 of the single-sequence prefill of all
+    2500 tokens, and their outputs and LSE to rounding (the single-sequence
+    main branch adds the blocks a query tile shares in another order),
+    including with a workspace that forces several chunks of query rows."""
     L, n = 2500, 1000
     wls, cu, pt, kip, kp, vp, qi, q = _paged_batch([L], [n], 8, 2, 64, seed=500)
     w = wls[0]
@@ -806,8 +811,8 @@ def test_paged_chunk_equals_full_prefill_rows(msa):
                                        synth.device_tensor(w, synth.T_V), ids_f, 128, 0.125)
     torch.cuda.synchronize()
     assert torch.equal(ids, ids_f[L - n:])
-    assert torch.equal(out, out_f[L - n:])
-    assert torch.equal(lse, lse_f[L - n:])
+    check_close("o", bf16_to_np(out), bf16_to_np(out_f[L - n:]), TOL_O)
+    check_close("lse", lse.cpu().numpy(), lse_f[L - n:].cpu().numpy(), 1e-4)
 
 
 def test_paged_whole_sequences_equal_varlen(msa):
@@ -872,3 +877,65 @@ def test_kl_teacher_zero_when_student_equals_teacher(msa):
     kl = msa.msa_kl_teacher(q, kk, qi, ki, ids, lse, 128, 0.125)
     torch.cuda.synchronize()
     assert kl.abs().max().item() < 1e-4
+
+
+# ------------------------------------------------ main branch: shared blocks
+def _bits_of(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("H_q,H_kv,ws_rows", [(16, 4, None), (16, 4, 200), (16, 2, None),
+                                              (32, 4, 333)])
+def test_sparse_attn_shared_blocks(msa, H_q, H_kv, ws_rows):
+    """Block ids built so that the query tiles (128 / G consecutive queries)
+    share blocks: block 0 and the local block are selected by every query,
+    block 2 by exactly half of each tile (the threshold: shared), block 1 by
+    one query fewer than half (not shared), the rest at random. Block 2's keys
+    are scaled by 4, so rows rescale their running max when it follows block 0
+    (V is scaled by 1/4 so that those sharply peaked rows stay below 1 in
+    magnitude, where two bf16 roundings fit the output bound).
+    Chunked workspaces put tiles across chunk ends. Output and LSE against the
+    oracle on the same ids."""
+    rng = np.random.default_rng(H_q + (ws_rows or 0))
+    N, d, k = 1500, 128, 16
+    G = H_q // H_kv
+    qt = 128 // G
+    q = rng.standard_normal((N, H_q, d)).astype(np.float32)
+    K = rng.standard_normal((N, H_kv, d)).astype(np.float32)
+    V = rng.standard_normal((N, H_kv, d)).astype(np.float32)
+    K[2 * 128:3 * 128] *= 4.0
+    V *= 0.25  # the peaked rows then keep |o| < 1, where bf16 rounds within the bound
+    ids = np.full((N, H_kv, k), -1, dtype=np.int32)
+    for t in range(N):
+        loc = t // 128
+        for g in range(H_kv):
+            chosen = {loc, 0}
+            if (t % qt) < qt // 2 and loc > 2:
+                chosen.add(2)
+            if (t % qt) < qt // 2 - 1 and loc > 1:
+                chosen.add(1)
+            pool = [b for b in range(3, loc)]
+            rng.shuffle(pool)
+            for b in pool:
+                if len(chosen) >= k:
+                    break
+                chosen.add(b)
+            sel = sorted(chosen)[:k]
+            ids[t, g, :len(sel)] = sel
+    qb, Kb, Vb = _bits_of(q), _bits_of(K), _bits_of(V)
+    dev = torch.device("cuda")
+    as_t = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)  # noqa: E731
+    ws = None
+    if ws_rows is not None:
+        ws = torch.empty(msa.msa_sparse_attn_workspace_bytes(ws_rows, N, H_q, H_kv, d, 128, k),
+                         dtype=torch.uint8, device=dev)
+    scale = 1.0 / np.sqrt(d)
+    out, lse = msa.msa_sparse_attn(as_t(qb), as_t(Kb), as_t(Vb), torch.from_numpy(ids).to(dev),
+                                   128, scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert msa.msa_get_error() == 0
+    o_ref, l_ref = oracle.sparse_attn(qb, np.arange(N), Kb, Vb, ids, 128, scale)
+    e_o = check_close("o", bf16_to_np(out), o_ref, TOL_O)
+    e_l = check_close("lse", lse.cpu().numpy(), l_ref, TOL_LSE)
+    print(f"[shared blocks G={G} ws_rows={ws_rows}] max|err| o {e_o:.3e} lse {e_l:.3e}")
