@@ -12,13 +12,15 @@
 // [N, n_g, d_idx]; columns are keys. Because the index key head is shared, one
 // k_idx block serves every group of a row tile.
 //
-// GB300 design (one persistent CTA per SM, 10 warps):
+// GB300 design (one persistent CTA per SM, 11 warps):
 //   warp 0      TMA producer: the CTA's 256 q_idx rows once per tile, then
 //               k_idx blocks (128 keys x d_idx) through a 4-stage ring;
 //   warp 1      TMEM owner and MMA issuer: per key block two 128x128xd_idx
 //               tcgen05 MMAs (the two 128-row halves share the k_idx tile, so
 //               every k_idx byte fetched from L2 feeds 256 rows) into one of
 //               two TMEM accumulator stages (4 x 128 of the 512 columns);
+//   warp 10     the second MMA issuer: warps 1 and 10 take alternate key
+//               blocks, so the pipe is fed while the other waits;
 //   warps 2-9   epilogue: each thread owns one row, reads its 128 scores of the
 //               block from TMEM, applies the causal mask on the diagonal block,
 //               max-pools them to the block score and feeds it to the row's
@@ -48,7 +50,8 @@ using namespace sm100;
 constexpr int kRows = 256;     // rows (t, g) per tile: two M = 128 halves
 constexpr int kKeys = 128;     // keys per block (= Bk)
 constexpr int kStages = 4;     // k_idx ring depth
-constexpr int kThreads = 320;  // 10 warps
+constexpr int kThreads = 352;  // 11 warps
+constexpr int kIssuer2 = 10;   // the second MMA issuer
 constexpr int kEpiWarps = 8;
 
 // DI index dimensions of EB bytes each (bf16: 2, E4M3: 1)
@@ -168,7 +171,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (threadIdx.x == 0) {
     mbar_init(a_full, 1);
-    mbar_init(a_empty, 1);
+    mbar_init(a_empty, 2);  // one commit per MMA issuer
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
@@ -177,7 +180,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_init(&t_full[s], 1);
       mbar_init(&t_empty[s], kEpiWarps);
     }
-    mbar_init(done_bar, 1);
+    mbar_init(done_bar, 2);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_q);
@@ -250,9 +253,15 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (a_armed) mbar_drain(a_full, a_par ^ 1);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kIssuer2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads issue the MMAs, warp 1 those of the even key blocks (of the
+    // CTA's running count), warp 10 the odd ones: while one waits on its
+    // barriers the other keeps the tensor pipe fed. Even and odd blocks use
+    // disjoint accumulator and k_idx stages; both wait for every tile's q_idx
+    // (so that each sees every phase of a_full) and both release it.
     if (lane == 0) {
+      const int mine = warp == 1 ? 0 : 1;
       constexpr uint32_t idesc = F8 ? idesc_e4m3_f32(128, kKeys) : idesc_bf16_f32(128, kKeys);
       const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
       uint32_t a_par = 0;
@@ -266,6 +275,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (!mbar_wait(a_full, a_par, abort_flag, dg)) { ok = false; break; }
         a_par ^= 1;
         for (int64_t b = 0; b < nkb; ++b, ++it) {
+          if ((int)(it & 1) != mine) continue;
           const int s = (int)(it % kStages);
           const uint32_t bpar = (uint32_t)((it / kStages) & 1);
           const int acc = (int)(it & 1);
@@ -294,7 +304,7 @@ index_select_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       mma_commit(done_bar);
       mbar_drain(done_bar, 0);
     }
-  } else {
+  } else if (warp < kIssuer2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;             // TMEM lane quarter this warp may access
     const int h = (warp - 2) >> 2;      // accumulator half (rows h*128 ..)
