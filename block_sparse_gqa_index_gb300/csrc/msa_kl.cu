@@ -322,11 +322,13 @@ kl_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       tc_fence_after();
       float m = -INFINITY, l = 0.f, Dp = 0.f, C = 0.f, A = 0.f;
       const bool full = __all_sync(0xffffffffu, lim >= kKlKeys);
+      // chunk ch + 1's columns load while chunk ch's sums are formed; the
+      // stage is released as soon as the last chunk's columns have arrived
+      uint32_t sr[32], xr[32];
+      tmem_ld32(ts, sr);
+      tmem_ld32(ts + 128, xr);
 #pragma unroll 1
       for (int ch = 0; ch < kKlKeys / 32; ++ch) {
-        uint32_t sr[32], xr[32];
-        tmem_ld32(ts + ch * 32, sr);
-        tmem_ld32(ts + 128 + ch * 32, xr);
         tmem_ld_wait();
         float pv[32], xv[32];
         if (full) {  // no row of the warp masks a column of this block
@@ -342,6 +344,14 @@ kl_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
                 ch * 32 + e < lim ? ex2_approx(__uint_as_float(sr[e]) * scale_log2 - lse2) : 0.f;
             xv[e] = __uint_as_float(xr[e]);
           }
+        }
+        if (ch + 1 < kKlKeys / 32) {
+          tmem_ld32(ts + (ch + 1) * 32, sr);
+          tmem_ld32(ts + 128 + (ch + 1) * 32, xr);
+        } else {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&t_empty[wg]);  // the stage's columns are free again
         }
         // reduce-scatter over the G lanes of the query: after step s a lane
         // keeps the half of its keys that its lane bit s selects
@@ -376,9 +386,6 @@ kl_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&t_empty[wg]);  // the stage's columns are free again
       // combine the G lanes of the query
 #pragma unroll
       for (int off = 1; off < G; off <<= 1) {
