@@ -16,17 +16,21 @@
 // reads is one contiguous run; k_idx pages are [P, 128, d_idx].
 // decode_attn_kernel: one CTA per (sequence, group, selected block): the G
 //   query heads of the group against the block's visible tokens, with the
-//   block's K and V bytes all in flight at once (cp.async into swizzled shared
-//   memory) and both products on mma.m16n8k16; writes the block's normalised
-//   output and LSE (split-KV partials).
+//   block's K and V bytes all in flight at once (two TMA copies, or 16-byte
+//   cp.async for rows narrower than 128 bytes, into swizzled shared memory)
+//   and both products on mma.m16n8k16; writes the block's normalised output
+//   and LSE (split-KV partials).
 // decode_merge_kernel: combines the k partials of every (sequence, head), one
 //   warp each, with all of its partial rows in flight at once.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 
 #include <type_traits>
 
 #include "msa_kernels.h"
+#include "msa_sm100.cuh"
 
 namespace msa {
 namespace {
@@ -324,14 +328,30 @@ decode_index_fp4_kernel(const uint16_t* __restrict__ q_idx, const unsigned char*
   }
 }
 
+// K / V rows of 128 bytes or a multiple of it arrive by TMA (one thread, two
+// mbarriers, 128-byte swizzled boxes through a 3-D map over the pages);
+// narrower rows by 16-byte cp.async into the row-swizzled layout
+template <int D, bool FP8>
+__host__ __device__ constexpr bool dec_tma() {
+  return (D * (FP8 ? 1 : 2)) % 128 == 0;
+}
 template <int D, bool FP8>
 constexpr int dec_smem_bytes() {
-  return 2 * kBk * D * (FP8 ? 1 : 2);
+  // K and V tiles, then the combine's m / l and (TMA) two mbarriers
+  return 2 * kBk * D * (FP8 ? 1 : 2) + 2 * 32 * 4 + 16;
+}
+
+// byte offset of 16-byte unit c of row r in a tile that arrived as 128-byte
+// swizzled boxes: chunk c / 8 of 128 bytes per row at (c / 8) * 16 KB, the
+// units XOR-ed with r % 8
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return (uint32_t)((c >> 3) * (kBk * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 template <int D, bool FP8>
 __global__ void __launch_bounds__(128, FP8 ? 6 : 3)
-decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
+decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const uint16_t* __restrict__ q, const void* __restrict__ kp,
                    const void* __restrict__ vp, const float* __restrict__ k_scale,
                    const float* __restrict__ v_scale, const int32_t* __restrict__ page_table,
                    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ ids,
@@ -344,9 +364,17 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
   constexpr int KS = D / 16;        // k-steps of q K^T
   constexpr int NC = D / 8;         // 8-column tiles of P V
   constexpr int RS = D + 8;         // row stride (floats) of the combine buffer
+  constexpr bool TMA = dec_tma<D, FP8>();
   static_assert(4 * 8 * RS * 4 <= 2 * TILE, "combine buffer fits the K/V tiles");
-  extern __shared__ __align__(128) unsigned char dsm[];
-  __shared__ float s_m[4][8], s_l[4][8];
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  // tile addressing: TMA boxes or the cp.async layout
+  auto tile_off = [](int r, int c) -> uint32_t {
+    if constexpr (TMA) return sw128(r, c);
+    else return swz<ROWB>(r, c);
+  };
+  float(*s_m)[8] = reinterpret_cast<float(*)[8]>(dsm + 2 * TILE);
+  float(*s_l)[8] = reinterpret_cast<float(*)[8]>(dsm + 2 * TILE + 128);
+  uint64_t* kv_bar = reinterpret_cast<uint64_t*>(dsm + 2 * TILE + 256);  // K, V landed (TMA)
 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int gq = lane >> 2, t4 = lane & 3;
@@ -370,18 +398,43 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
   const unsigned char* gk = (const unsigned char*)kp + blk;
   const unsigned char* gv = (const unsigned char*)vp + blk;
   const uint32_t sk = smem_addr(dsm), sv = sk + TILE;
+  volatile int abort_flag = 0;  // this thread's waits only
+  if constexpr (TMA) {
+    if (sk & 1023) {
+      if (tid == 0) report(dg, kStatusUnsupported);
+      return;
+    }
+    if (tid == 0) {
+      sm100::mbar_init(&kv_bar[0], 1);
+      sm100::mbar_init(&kv_bar[1], 1);
+      sm100::fence_barrier_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const int32_t z = (int32_t)(page * H_kv + g);
+      sm100::mbar_arrive_expect_tx(&kv_bar[0], TILE);
+#pragma unroll
+      for (int c = 0; c < ROWB / 128; ++c)
+        sm100::tma_load_3d(dsm + c * kBk * 128, &tm_k, &kv_bar[0], c * (128 / EB), 0, z);
+      sm100::mbar_arrive_expect_tx(&kv_bar[1], TILE);
+#pragma unroll
+      for (int c = 0; c < ROWB / 128; ++c)
+        sm100::tma_load_3d(dsm + TILE + c * kBk * 128, &tm_v, &kv_bar[1], c * (128 / EB), 0, z);
+    }
+  } else {
 #pragma unroll 4
-  for (int e = tid; e < kBk * CPR; e += 128) {
-    const int r = e / CPR;
-    cp_async16(sk + swz<ROWB>(r, e % CPR), gk + (size_t)e * 16, r < nvalid ? 16u : 0u);
-  }
-  cp_async_commit();
+    for (int e = tid; e < kBk * CPR; e += 128) {
+      const int r = e / CPR;
+      cp_async16(sk + swz<ROWB>(r, e % CPR), gk + (size_t)e * 16, r < nvalid ? 16u : 0u);
+    }
+    cp_async_commit();
 #pragma unroll 4
-  for (int e = tid; e < kBk * CPR; e += 128) {
-    const int r = e / CPR;
-    cp_async16(sv + swz<ROWB>(r, e % CPR), gv + (size_t)e * 16, r < nvalid ? 16u : 0u);
+    for (int e = tid; e < kBk * CPR; e += 128) {
+      const int r = e / CPR;
+      cp_async16(sv + swz<ROWB>(r, e % CPR), gv + (size_t)e * 16, r < nvalid ? 16u : 0u);
+    }
+    cp_async_commit();
   }
-  cp_async_commit();
 
   // A operand rows: head gq of the group (rows >= G and the upper 8 rows are zero)
   uint32_t qa[KS][2];
@@ -397,8 +450,16 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
   const float vs = FP8 ? v_scale[g] : 1.f;
   const int tok0 = 32 * w;
 
-  cp_async_wait<1>();  // this thread's K chunks have landed
-  __syncthreads();     // everyone's have
+  if constexpr (TMA) {  // K has landed (a timed-out wait lets both copies land, then leaves)
+    if (!sm100::mbar_wait(&kv_bar[0], 0, &abort_flag, dg)) {
+      sm100::mbar_drain(&kv_bar[0], 0);
+      sm100::mbar_drain(&kv_bar[1], 0);
+      return;
+    }
+  } else {
+    cp_async_wait<1>();  // this thread's K chunks have landed
+    __syncthreads();     // everyone's have
+  }
   float sacc[4][4];
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)
@@ -410,7 +471,7 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(sk + swz<ROWB>(tok0 + 8 * nt + (lane & 7), 4 * p + (lane >> 3)), b0, b1, b2, b3);
+        ldsm_x4(sk + tile_off(tok0 + 8 * nt + (lane & 7), 4 * p + (lane >> 3)), b0, b1, b2, b3);
         mma_bf16_16816(sacc[nt], qa[2 * p][0], 0u, qa[2 * p][1], 0u, b0, b1);
         mma_bf16_16816(sacc[nt], qa[2 * p + 1][0], 0u, qa[2 * p + 1][1], 0u, b2, b3);
       }
@@ -419,7 +480,7 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
     for (int i = 0; i < KS; ++i)
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
-        const uint32_t a = sk + swz<ROWB>(tok0 + 8 * nt + gq, i);
+        const uint32_t a = sk + tile_off(tok0 + 8 * nt + gq, i);
         const uint32_t b0 = e4m3x2_to_bf16x2(lds_u16(a + 2 * t4));
         const uint32_t b1 = e4m3x2_to_bf16x2(lds_u16(a + 8 + 2 * t4));
         mma_bf16_16816(sacc[nt], qa[i][0], 0u, qa[i][1], 0u, b0, b1);
@@ -451,8 +512,24 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
   lw += __shfl_xor_sync(0xffffffffu, lw, 1);
   lw += __shfl_xor_sync(0xffffffffu, lw, 2);
 
-  cp_async_wait<0>();  // V has landed
-  __syncthreads();
+  if constexpr (TMA) {
+    if (!sm100::mbar_wait(&kv_bar[1], 0, &abort_flag, dg)) {  // V has landed
+      sm100::mbar_drain(&kv_bar[1], 0);
+      return;
+    }
+    // the block's rows past its last token hold other data: zero this warp's
+    // V rows there (their P is 0, and 0 times a NaN is not)
+    if (nvalid < tok0 + 32) {
+      for (int e = lane; e < 32 * CPR; e += 32) {
+        const int r = tok0 + e / CPR;
+        if (r >= nvalid) sm100::st_shared_v4(sv + tile_off(r, e % CPR), 0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
+  } else {
+    cp_async_wait<0>();  // V has landed
+    __syncthreads();
+  }
   float o[NC][4];
 #pragma unroll
   for (int n = 0; n < NC; ++n)
@@ -467,7 +544,7 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
 #pragma unroll
       for (int n = 0; n < NC; n += 2) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sv + swz<ROWB>(r, n + (lane >> 4)), b0, b1, b2, b3);
+        ldsm_x4_t(sv + tile_off(r, n + (lane >> 4)), b0, b1, b2, b3);
         mma_bf16_16816(o[n], a0, 0u, a2, 0u, b0, b1);
         mma_bf16_16816(o[n + 1], a0, 0u, a2, 0u, b2, b3);
       }
@@ -477,10 +554,10 @@ decode_attn_kernel(const uint16_t* __restrict__ q, const void* __restrict__ kp,
       for (int n = 0; n < NC; ++n) {
         const int col = 8 * n + gq;
         const int ch = col >> 4, by = col & 15;
-        const uint32_t v00 = lds_u8(sv + swz<ROWB>(r, ch) + by);
-        const uint32_t v01 = lds_u8(sv + swz<ROWB>(r + 1, ch) + by);
-        const uint32_t v10 = lds_u8(sv + swz<ROWB>(r + 8, ch) + by);
-        const uint32_t v11 = lds_u8(sv + swz<ROWB>(r + 9, ch) + by);
+        const uint32_t v00 = lds_u8(sv + tile_off(r, ch) + by);
+        const uint32_t v01 = lds_u8(sv + tile_off(r + 1, ch) + by);
+        const uint32_t v10 = lds_u8(sv + tile_off(r + 8, ch) + by);
+        const uint32_t v11 = lds_u8(sv + tile_off(r + 9, ch) + by);
         mma_bf16_16816(o[n], a0, 0u, a2, 0u, e4m3x2_to_bf16x2(v00 | (v01 << 8)),
                        e4m3x2_to_bf16x2(v10 | (v11 << 8)));
       }
@@ -600,6 +677,32 @@ decode_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ 
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// K or V pages [P, H_kv, 128, d] (bf16 or E4M3 bytes) seen as (columns, 128
+// rows, block z = page * H_kv + head) with a box of one block's 128 rows by
+// 128 bytes, 128-byte swizzle. The page count is not passed in; 2^25 blocks
+// bound any pool that fits in device memory (a block is at least 8 KB), and a
+// block past the bound would read as zeros instead of faulting.
+bool make_map_dec_pages(CUtensorMap* m, const void* base, int D, bool fp8) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess || qr != cudaDriverEntryPointSuccess)
+      return false;
+    fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  const int eb = fp8 ? 1 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)kBk, (cuuint64_t)1 << 25};
+  cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)kBk * D * eb};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / eb), (cuuint32_t)kBk, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_decode_index(const void* q_idx, const void* k_idx_pages,
@@ -679,12 +782,16 @@ cudaError_t launch_decode_attn(const void* q, const void* k_pages, const void* v
 #define MSA_DEC(DD, F8)                                                                    \
   do {                                                                                     \
     constexpr int sm = dec_smem_bytes<DD, F8>();                                           \
+    CUtensorMap tk{}, tv{};                                                                \
+    if (dec_tma<DD, F8>() &&                                                               \
+        (!make_map_dec_pages(&tk, k_pages, DD, F8) || !make_map_dec_pages(&tv, v_pages, DD, F8))) \
+      return cudaErrorInvalidValue;                                                        \
     e = cudaFuncSetAttribute(decode_attn_kernel<DD, F8>,                                   \
                              cudaFuncAttributeMaxDynamicSharedMemorySize, sm);             \
     if (e != cudaSuccess) return e;                                                        \
     decode_attn_kernel<DD, F8><<<tasks, 128, sm, st>>>(                                    \
-        (const uint16_t*)q, k_pages, v_pages, k_scale, v_scale, page_table, seq_lens, ids, \
-        max_pages, H_q, H_kv, k, sl2, part_o, part_lse, dg);                               \
+        tk, tv, (const uint16_t*)q, k_pages, v_pages, k_scale, v_scale, page_table, seq_lens, \
+        ids, max_pages, H_q, H_kv, k, sl2, part_o, part_lse, dg);                          \
   } while (0)
   if (d == 128) {
     if (kv_fp8) MSA_DEC(128, true); else MSA_DEC(128, false);
