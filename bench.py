@@ -9,7 +9,8 @@ Prints ONE JSON line. `value` is prefill tokens/s (all ranks). Further keys:
   e2e          the same step through the C ABI from pinned host buffers,
                host->device inputs and device->host output inside the timing,
                the copies on their own streams overlapping the compute of a
-               stream of independent prefills
+               stream of independent prefills (two device buffers per input
+               and output, used by alternate steps)
   roofline     dominant kernel (the index branch's single kernel): algorithmic
                flops per launch / its CUDA-event time, against the measured dense
                bf16 burst peak (the kernel is timed per launch); frac_of_sustained
@@ -234,48 +235,57 @@ def time_prefill(msa, w, steps, warmup, world, ws_rows=None, clocks=None):
 def e2e_prefill(msa, P, steps, warmup):
     """Same step through the public API from pinned host buffers: every step copies its
     inputs in and its result (o, lse) out inside the timing. The copies run on their own
-    streams so that they overlap the compute of a stream of independent prefills: the
-    index inputs first, q/k/v while the index branch runs, the result out while the next
-    step starts. Events keep every device buffer from being overwritten before the step
+    streams so that they overlap the compute of a stream of independent prefills, and the
+    inputs and results have two device buffers each, used by alternate steps: step i + 1's
+    inputs load while step i computes, and step i's result copies out while step i + 1
+    computes. Events keep every device buffer from being overwritten before the step
     that reads it is done with it."""
     import torch
     w = P.w
-    host = {n: getattr(P, n).cpu().pin_memory() for n in ("q", "k", "v", "qidx", "kidx")}
+    names_in = ("q", "k", "v", "qidx", "kidx")
+    host = {n: getattr(P, n).cpu().pin_memory() for n in names_in}
     host_out = torch.empty(P.out.shape, dtype=P.out.dtype).pin_memory()
     host_lse = torch.empty(P.lse.shape, dtype=P.lse.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    dev = [{n: getattr(P, n) for n in names_in + ("out", "lse")},
+           {n: torch.empty_like(getattr(P, n)) for n in names_in + ("out", "lse")}]
     comp = torch.cuda.current_stream()
     c_in, c_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = {n: torch.cuda.Event() for n in ("idx_in", "att_in", "idx_done", "att_done", "out_done")}
-    for e in ev.values():
-        e.record(comp)
+    ev = [{n: torch.cuda.Event() for n in ("idx_in", "att_in", "idx_done", "att_done", "out_done")}
+          for _ in range(2)]
+    for e in ev:
+        for x in e.values():
+            x.record(comp)
+    step = [0]
 
     def one():
+        b, e = dev[step[0] & 1], ev[step[0] & 1]
+        step[0] += 1
         with torch.cuda.stream(c_in):
-            c_in.wait_event(ev["idx_done"])      # the previous index branch has read q_idx, k_idx
+            c_in.wait_event(e["idx_done"])      # this buffer's last index branch has read it
             for n in ("qidx", "kidx"):
-                getattr(P, n).copy_(host[n], non_blocking=True)
-            ev["idx_in"].record(c_in)
-            c_in.wait_event(ev["att_done"])      # the previous main branch has read q, k, v
+                b[n].copy_(host[n], non_blocking=True)
+            e["idx_in"].record(c_in)
+            c_in.wait_event(e["att_done"])      # this buffer's last main branch has read it
             for n in ("q", "k", "v"):
-                getattr(P, n).copy_(host[n], non_blocking=True)
-            ev["att_in"].record(c_in)
-        comp.wait_event(ev["idx_in"])
-        msa.msa_index_select(P.qidx, P.kidx, w.Bk, w.k, block_ids=P.ids)
-        ev["idx_done"].record(comp)
-        comp.wait_event(ev["att_in"])
-        comp.wait_event(ev["out_done"])          # the previous result has been copied out
-        msa.msa_sparse_attn(P.q, P.k, P.v, P.ids, w.Bk, w.scale, workspace=P.ws, out=P.out,
-                            lse=P.lse)
-        ev["att_done"].record(comp)
+                b[n].copy_(host[n], non_blocking=True)
+            e["att_in"].record(c_in)
+        comp.wait_event(e["idx_in"])
+        msa.msa_index_select(b["qidx"], b["kidx"], w.Bk, w.k, block_ids=P.ids)
+        e["idx_done"].record(comp)
+        comp.wait_event(e["att_in"])
+        comp.wait_event(e["out_done"])          # this buffer's last result has been copied out
+        msa.msa_sparse_attn(b["q"], b["k"], b["v"], P.ids, w.Bk, w.scale, workspace=P.ws,
+                            out=b["out"], lse=b["lse"])
+        e["att_done"].record(comp)
         with torch.cuda.stream(c_out):
-            c_out.wait_event(ev["att_done"])
-            host_out.copy_(P.out, non_blocking=True)
-            host_lse.copy_(P.lse, non_blocking=True)
-            ev["out_done"].record(c_out)
+            c_out.wait_event(e["att_done"])
+            host_out.copy_(b["out"], non_blocking=True)
+            host_lse.copy_(b["lse"], non_blocking=True)
+            e["out_done"].record(c_out)
 
-    for _ in range(max(1, warmup)):
+    for _ in range(max(2, warmup)):
         one()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -283,6 +293,7 @@ def e2e_prefill(msa, P, steps, warmup):
         one()
     torch.cuda.synchronize()
     ms = (time.perf_counter() - t0) * 1e3 / steps
+    del dev
     return ms, h2d, d2h
 
 
