@@ -23,8 +23,9 @@ Prints ONE JSON line. `value` is prefill tokens/s (all ranks). Further keys:
                the 128K step with the index branch on FP8-E4M3 codes, the
                index-branch projections of the 128K tokens (d_model 4096), the KL
                alignment signal of the index branch at 128K,
-               decode steps with bf16 KV, FP8-E4M3 KV, and FP8-E4M3 KV plus an
-               FP8-E4M3 or NVFP4 k_idx cache, standalone top-16 (with
+               decode steps with bf16 KV, FP8-E4M3 KV, FP8-E4M3 KV plus an
+               FP8-E4M3 or NVFP4 k_idx cache, and NVFP4 KV with an NVFP4 k_idx
+               cache, standalone top-16 (with
                torch.topk over the same scores as a comparator)
 
 Multi-GPU: each rank runs its own independent sequence (no collective on the
@@ -312,11 +313,18 @@ def nvfp4_quantise(x):
     return packed, sc.view(torch.uint8).contiguous()
 
 
-def time_decode(msa, w, fp8, steps, warmup, fp8_index=False, fp4_index=False):
+# decode variants timed: (E4M3 K / V, E4M3 k_idx, NVFP4 k_idx, NVFP4 K / V)
+DECODE_VARIANTS = ((False, False, False, False), (True, False, False, False),
+                   (True, True, False, False), (True, False, True, False),
+                   (False, False, True, True))
+
+
+def time_decode(msa, w, fp8, steps, warmup, fp8_index=False, fp4_index=False, fp4_kv=False):
     """Decode step for B sequences: index branch (k_idx cache scan + top-k) and
     main branch over the selected pages. fp8: E4M3 K / V pages; fp8_index: the
     k_idx cache and q_idx as E4M3 codes too (rounded by torch before timing);
-    fp4_index: an NVFP4 k_idx cache (quantised by torch before timing)."""
+    fp4_index: an NVFP4 k_idx cache; fp4_kv: NVFP4 K / V pages (both quantised
+    by torch before timing)."""
     import torch
     import synth
     dev = torch.device("cuda")
@@ -343,6 +351,15 @@ def time_decode(msa, w, fp8, steps, warmup, fp8_index=False, fp4_index=False):
         def index(qi, _k, pt_, sl_, Bk, k, **kw):
             return msa.msa_index_select_decode_nvfp4(qi, codes, scales, pt_, sl_, Bk, k, **kw)
         kidx_p = None
+    attend = msa.msa_decode
+    if fp4_kv:
+        kc, ksc = nvfp4_quantise(kp)
+        vc, vsc = nvfp4_quantise(vp)
+        kp = vp = None
+        torch.cuda.empty_cache()
+
+        def attend(q_, _k, _v, pt_, sl_, ids_, Bk, scale, **kw_):
+            return msa.msa_decode_nvfp4(q_, kc, ksc, vc, vsc, pt_, sl_, ids_, Bk, scale, **kw_)
     ids = torch.empty((w.B, w.n_g, w.k), dtype=torch.int32, device=dev)
     ws_i = torch.empty(msa.msa_index_select_decode_workspace_bytes(w.B, w.nb, w.n_g),
                        dtype=torch.uint8, device=dev)
@@ -359,8 +376,7 @@ def time_decode(msa, w, fp8, steps, warmup, fp8_index=False, fp4_index=False):
         index(qidx, kidx_p, pt, sl, w.Bk, w.k, block_ids=ids, workspace=ws_i)
         if ev:
             ev[1].record()
-        msa.msa_decode(q, kp, vp, pt, sl, ids, w.Bk, w.scale, workspace=ws_d, out=out, lse=lse,
-                       **kw)
+        attend(q, kp, vp, pt, sl, ids, w.Bk, w.scale, workspace=ws_d, out=out, lse=lse, **kw)
         if ev:
             ev[2].record()
 
@@ -726,12 +742,13 @@ def main():
     peaks, peak_src = load_peaks()
     if args.only == "decode":
         wd = synth.make("decode", **({"B": args.batch} if args.batch else {}))
-        for fp8, fp8_index, fp4_index in ((False, False, False), (True, False, False),
-                                          (True, True, False), (True, False, True)):
-            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, args.warmup, fp8_index, fp4_index)
+        for fp8, fp8_index, fp4_index, fp4_kv in DECODE_VARIANTS:
+            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, args.warmup, fp8_index, fp4_index,
+                                     fp4_kv)
             torch.cuda.empty_cache()
             print(json.dumps({"only": "decode", "fp8": fp8, "fp8_index": fp8_index,
-                              "fp4_index": fp4_index, "index_ms": i_ms, "attention_ms": a_ms}))
+                              "fp4_index": fp4_index, "fp4_kv": fp4_kv, "index_ms": i_ms,
+                              "attention_ms": a_ms}))
         return
     if args.only == "index":
         w = synth.make(args.workload)
@@ -872,15 +889,16 @@ def main():
             "index_tflops": round(p_fli / (p_idx * 1e-3) / 1e12, 2),
             "tflops": round((p_fli + p_fla) / (p_ms * 1e-3) / 1e12, 2)}
         wd = synth.make("decode")
-        for fp8, fp8_index, fp4_index in ((False, False, False), (True, False, False),
-                                          (True, True, False), (True, False, True)):
-            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, 1, fp8_index, fp4_index)
+        for fp8, fp8_index, fp4_index, fp4_kv in DECODE_VARIANTS:
+            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, 1, fp8_index, fp4_index, fp4_kv)
             torch.cuda.empty_cache()
-            kv_bytes = 2.0 * wd.B * wd.n_g * (wd.k - 1) * wd.Bk * wd.d * (1 if fp8 else 2) + \
-                2.0 * wd.B * wd.n_g * 1 * wd.d * (1 if fp8 else 2)
+            kv_elem = 0.5 + 1.0 / 16 if fp4_kv else (1.0 if fp8 else 2.0)
+            kv_bytes = 2.0 * wd.B * wd.n_g * (wd.k - 1) * wd.Bk * wd.d * kv_elem + \
+                2.0 * wd.B * wd.n_g * 1 * wd.d * kv_elem
             per_elem = 0.5 + 1.0 / 16 if fp4_index else (1.0 if fp8_index else 2.0)
             scan_bytes = per_elem * wd.B * wd.L * wd.d_idx
-            key = ("decode_nvfp4_index_fp8_kv" if fp4_index else
+            key = ("decode_nvfp4_index_and_kv" if fp4_kv else
+                   "decode_nvfp4_index_fp8_kv" if fp4_index else
                    "decode_fp8_index_and_kv" if fp8_index else
                    ("decode_fp8" if fp8 else "decode_bf16"))
             extra[key] = {

@@ -53,6 +53,8 @@ _index_dec = _sig("msa_index_select_decode", [_P, _P, _P, _P, _I, _I, _I, _I, _I
 _ws_dec = _sig("msa_decode_workspace_bytes", [_I, _I, _I, _I], _SZ)
 _decode = _sig("msa_decode", [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                               _P, _P, _P, _SZ, _P])
+_decode_fp4 = _sig("msa_decode_nvfp4", [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                         _I, _F, _P, _P, _P, _SZ, _P])
 _get_error = _sig("msa_get_error", [_P])
 _set_wait = _sig("msa_set_wait_limit", [_I64], _I64)
 _launch_count = _sig("msa_launch_count", [], _I64)
@@ -91,7 +93,8 @@ EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes
            "msa_sparse_attn_varlen", "msa_index_select_paged",
            "msa_sparse_attn_paged_workspace_bytes", "msa_sparse_attn_paged",
            "msa_index_select_decode_fp8", "msa_kl_teacher_workspace_bytes",
-           "msa_kl_teacher", "msa_index_select_decode_nvfp4", "msa_index_project"]
+           "msa_kl_teacher", "msa_index_select_decode_nvfp4", "msa_index_project",
+           "msa_decode_nvfp4"]
 
 
 class MSAError(RuntimeError):
@@ -645,6 +648,47 @@ def msa_decode(q: torch.Tensor, k_pages: torch.Tensor, v_pages: torch.Tensor,
                    block_ids.data_ptr(), B, max_pages, H_q, H_kv, d, Bk, topk, scale,
                    out.data_ptr(), _ptr(lse), workspace.data_ptr(), workspace.numel(),
                    _stream(q)), "msa_decode")
+    return out, lse
+
+
+def msa_decode_nvfp4(q: torch.Tensor, k_codes: torch.Tensor, k_scales: torch.Tensor,
+                     v_codes: torch.Tensor, v_scales: torch.Tensor, page_table: torch.Tensor,
+                     seq_lens: torch.Tensor, block_ids: torch.Tensor, Bk: int = 128,
+                     scale: Optional[float] = None, workspace: Optional[torch.Tensor] = None,
+                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                     want_lse: bool = True):
+    """Main branch of decode over an NVFP4 KV cache. q [B, H_q, d] bf16;
+    k_codes/v_codes [P, H_kv, Bk, d / 2] uint8 (two E2M1 codes per byte, even
+    dimension low); k_scales/v_scales [P, H_kv, Bk, d / 16] uint8 (E4M3)."""
+    B, H_q, d = q.shape
+    P, H_kv = k_codes.shape[0], k_codes.shape[1]
+    max_pages = page_table.shape[1]
+    topk = block_ids.shape[-1]
+    _req(q, "q", torch.bfloat16)
+    for t, n in ((k_codes, "k_codes"), (v_codes, "v_codes")):
+        _req(t, n, torch.uint8, (P, H_kv, Bk, d // 2))
+    for t, n in ((k_scales, "k_scales"), (v_scales, "v_scales")):
+        _req(t, n, torch.uint8, (P, H_kv, Bk, d // 16))
+    _req(page_table, "page_table", torch.int32, (B, max_pages))
+    _req(seq_lens, "seq_lens", torch.int32, (B,))
+    _req(block_ids, "block_ids", torch.int32, (B, H_kv, topk))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = torch.empty(_ws_dec(B, H_q, d, topk), dtype=torch.uint8, device=q.device)
+    _req(workspace, "workspace", torch.uint8)
+    if out is None:
+        out = torch.empty_like(q)
+    _req(out, "out", torch.bfloat16, (B, H_q, d))
+    if lse is None and want_lse:
+        lse = torch.empty((B, H_q), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _req(lse, "lse", torch.float32, (B, H_q))
+    _check(_decode_fp4(q.data_ptr(), k_codes.data_ptr(), k_scales.data_ptr(), v_codes.data_ptr(),
+                       v_scales.data_ptr(), page_table.data_ptr(), seq_lens.data_ptr(),
+                       block_ids.data_ptr(), B, max_pages, H_q, H_kv, d, Bk, topk, scale,
+                       out.data_ptr(), _ptr(lse), workspace.data_ptr(), workspace.numel(),
+                       _stream(q)), "msa_decode_nvfp4")
     return out, lse
 
 

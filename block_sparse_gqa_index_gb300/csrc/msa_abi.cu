@@ -573,6 +573,32 @@ int msa_decode(const void* q, const void* k_pages, const void* v_pages, int kv_d
                                            workspace, diag(), (cudaStream_t)stream));
 }
 
+int msa_decode_nvfp4(const void* q, const void* k_codes, const void* k_scales,
+                     const void* v_codes, const void* v_scales, const int32_t* page_table,
+                     const int32_t* seq_lens, const int32_t* block_ids, int B, int max_pages,
+                     int H_q, int H_kv, int d, int Bk, int k, float scale, void* out, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || max_pages < 1 || H_q < 1 || H_kv < 1 || d < 1 || Bk < 1 || k < 1)
+    return MSA_ERR_INVALID_ARG;
+  if (B == 0) return MSA_OK;
+  if (!q || !k_codes || !k_scales || !v_codes || !v_scales || !page_table || !seq_lens ||
+      !block_ids || !out)
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_codes) || !aligned16(k_scales) || !aligned16(v_codes) ||
+      !aligned16(v_scales) || !aligned16(out))
+    return MSA_ERR_INVALID_ARG;
+  if (H_q % H_kv != 0) return MSA_ERR_INVALID_ARG;
+  if (Bk != 128 || !supported_k(k) || !supported_d(d) || H_q / H_kv > 8)
+    return MSA_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < msa_decode_workspace_bytes(B, H_q, d, k))
+    return MSA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MSA_ERR_INVALID_ARG;
+  return status_of(msa::launch_decode_attn_fp4(q, k_codes, k_scales, v_codes, v_scales,
+                                               page_table, seq_lens, block_ids, B, max_pages,
+                                               H_q, H_kv, d, k, scale, out, lse, workspace, diag(),
+                                               (cudaStream_t)stream));
+}
+
 int msa_get_error(void* stream) {
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MSA_ERR_CUDA;
   int* p = err_ptr();

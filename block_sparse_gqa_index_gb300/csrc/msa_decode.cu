@@ -594,6 +594,265 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   }
 }
 
+// ---- decode attention over an NVFP4 K/V cache
+//
+// K and V pages hold E2M1 codes [P, H_kv, 128, D / 2] (two per byte, the even
+// dimension in the low nibble) and one E4M3 scale per 16 dimensions of a row
+// [P, H_kv, 128, D / 16]; a value is its code times its scale. One CTA per
+// (sequence, group, selected block), as decode_attn_kernel: the block's codes
+// and scales arrive by cp.async (rows past the sequence end zero-filled, so
+// they decode to 0). q . K^T runs per 16-dimension micro-block on
+// mma.m16n8k16 with f16 operands (every E2M1 value is an f16 value; q is
+// rounded to f16), the key's scale multiplying each micro-block's product in
+// fp32 (a key's scales read in one load and converted two at a time); within
+// a micro-block the four lanes of a row take 4 contiguous dimensions each (one
+// 16-bit read), and q is permuted the same way. V is widened once into an f16
+// tile (a code times an E4M3 scale has at most 5 significant bits and lies in
+// f16's normal range, so the widening is exact), and P . V runs on f16
+// operands, reading V by ldmatrix.trans as the bf16 path does.
+template <int D>
+constexpr int dec_fp4_smem_bytes() {
+  return 2 * kBk * (D / 2) + 2 * kBk * (D / 16) + kBk * D * 2 + 2 * 32 * 4;
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(a));
+  return v;
+}
+// two E4M3 codes (first in the low byte) -> two floats, exact
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  return __half22float2(*reinterpret_cast<__half2*>(&h));
+}
+__device__ __forceinline__ uint2 lds_u64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+
+template <int D>
+__global__ void __launch_bounds__(128, 4)
+decode_attn_fp4_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict__ kc,
+                       const uint8_t* __restrict__ ksc, const uint8_t* __restrict__ vc,
+                       const uint8_t* __restrict__ vsc, const int32_t* __restrict__ page_table,
+                       const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ ids,
+                       int max_pages, int H_q, int H_kv, int k, float scale_log2,
+                       float* __restrict__ part_o, float* __restrict__ part_lse, Diag dg) {
+  constexpr int CB = D / 2;          // code bytes of a row
+  constexpr int SB = D / 16;         // scale bytes of a row
+  constexpr int CCH = CB / 16;       // 16-byte chunks of a code row
+  constexpr int CTILE = kBk * CB;
+  constexpr int STILE = kBk * SB;
+  constexpr int VROWB = D * 2;       // bf16 row of the widened V tile
+  constexpr int MB = D / 16;         // micro-blocks of a row
+  constexpr int NC = D / 8;          // 8-column tiles of P V
+  constexpr int RS = D + 8;          // row stride (floats) of the combine buffer
+  static_assert(4 * 8 * RS * 4 <= kBk * VROWB, "combine buffer fits the V tile");
+  extern __shared__ __align__(128) unsigned char dsm[];
+  const uint32_t s_kc = smem_addr(dsm), s_vc = s_kc + CTILE;
+  const uint32_t s_ks = s_vc + CTILE, s_vs = s_ks + STILE;
+  const uint32_t s_vb = s_vs + STILE;  // widened V (f16, row-swizzled)
+  float(*s_m)[8] = reinterpret_cast<float(*)[8]>(dsm + 2 * CTILE + 2 * STILE + kBk * VROWB);
+  float(*s_l)[8] = s_m + 4;
+
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int gq = lane >> 2, t4 = lane & 3;
+  const int G = H_q / H_kv;
+  const int64_t task = blockIdx.x;  // (s * H_kv + g) * k + slot
+  const int slot = (int)(task % k);
+  const int64_t sg = task / k;
+  const int g = (int)(sg % H_kv);
+  const int s = (int)(sg / H_kv);
+  const int id = ids[task];
+  if (id < 0) return;
+  const int L = seq_lens[s];
+  if (L < 1 || L > max_pages * kBk || id > (L - 1) / kBk) {  // merge skips this slot
+    if (tid == 0) report(dg, kStatusBadIds);
+    return;
+  }
+  const int64_t page = page_table[(size_t)s * max_pages + id];
+  const int nvalid = min(kBk, L - id * kBk);
+  const size_t blk = (size_t)page * H_kv + g;  // the (page, head g) block of codes / scales
+  const unsigned char* gkc = kc + blk * CTILE;
+  const unsigned char* gvc = vc + blk * CTILE;
+  const unsigned char* gks = ksc + blk * STILE;
+  const unsigned char* gvs = vsc + blk * STILE;
+  // K codes and scales, then V codes and scales (rows past nvalid read as 0)
+#pragma unroll
+  for (int e = tid; e < kBk * CCH; e += 128) {
+    const int r = e / CCH;
+    cp_async16(s_kc + swz<CB>(r, e % CCH), gkc + (size_t)e * 16, r < nvalid ? 16u : 0u);
+  }
+#pragma unroll
+  for (int e = tid; e < STILE / 16; e += 128) {
+    const int r0 = e * 16 / SB;  // first row of the chunk
+    const int nb = max(0, min(16, (nvalid - r0) * SB));
+    cp_async16(s_ks + e * 16, gks + (size_t)e * 16, (uint32_t)nb);
+  }
+  cp_async_commit();
+#pragma unroll
+  for (int e = tid; e < kBk * CCH; e += 128) {
+    const int r = e / CCH;
+    cp_async16(s_vc + swz<CB>(r, e % CCH), gvc + (size_t)e * 16, r < nvalid ? 16u : 0u);
+  }
+#pragma unroll
+  for (int e = tid; e < STILE / 16; e += 128) {
+    const int r0 = e * 16 / SB;
+    const int nb = max(0, min(16, (nvalid - r0) * SB));
+    cp_async16(s_vs + e * 16, gvs + (size_t)e * 16, (uint32_t)nb);
+  }
+  cp_async_commit();
+
+  // A operand: head gq of the group in f16, each micro-block's dimensions in
+  // the lanes' order (lane t4 holds dims 4 t4 .. 4 t4 + 3)
+  uint32_t qa[MB][2];
+  {
+    const uint16_t* qr = q + ((size_t)s * H_q + (size_t)g * G + (gq < G ? gq : 0)) * D;
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb) {
+      const uint2 v = *reinterpret_cast<const uint2*>(qr + mb * 16 + 4 * t4);
+      const float x0 = __uint_as_float(v.x << 16), x1 = __uint_as_float(v.x & 0xFFFF0000u);
+      const float x2 = __uint_as_float(v.y << 16), x3 = __uint_as_float(v.y & 0xFFFF0000u);
+      qa[mb][0] = gq < G ? f16x2_of(x0, x1) : 0u;
+      qa[mb][1] = gq < G ? f16x2_of(x2, x3) : 0u;
+    }
+  }
+  const int tok0 = 32 * w;
+
+  cp_async_wait<1>();  // this thread's K chunks have landed
+  __syncthreads();     // everyone's have
+  float sacc[4][2];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) sacc[nt][0] = sacc[nt][1] = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    const int kr = tok0 + 8 * nt + gq;           // the key of this lane's B fragment
+    const int key0 = tok0 + 8 * nt + 2 * t4;     // the keys of this lane's accumulators
+    // the two keys' scales (SB bytes each), as floats
+    float sc0[MB], sc1[MB];
+#pragma unroll
+    for (int u = 0; u < SB / 4; ++u) {
+      const uint32_t w0 = lds_u32(s_ks + key0 * SB + 4 * u);
+      const uint32_t w1 = lds_u32(s_ks + (key0 + 1) * SB + 4 * u);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float2 f0 = e4m3x2_to_float2((w0 >> (16 * hh)) & 0xFFFF);
+        const float2 f1 = e4m3x2_to_float2((w1 >> (16 * hh)) & 0xFFFF);
+        sc0[4 * u + 2 * hh] = f0.x;
+        sc0[4 * u + 2 * hh + 1] = f0.y;
+        sc1[4 * u + 2 * hh] = f1.x;
+        sc1[4 * u + 2 * hh + 1] = f1.y;
+      }
+    }
+#pragma unroll
+    for (int mb = 0; mb < MB; ++mb) {
+      const uint32_t c = lds_u16(s_kc + swz<CB>(kr, mb >> 1) + (mb & 1) * 8 + 2 * t4);
+      float p[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f16_16816(p, qa[mb][0], 0u, qa[mb][1], 0u, e2m1x2_to_f16x2(c & 0xFF),
+                    e2m1x2_to_f16x2(c >> 8));
+      sacc[nt][0] = fmaf(p[0], sc0[mb], sacc[nt][0]);
+      sacc[nt][1] = fmaf(p[1], sc1[mb], sacc[nt][1]);
+    }
+  }
+
+  // warp-local softmax of head gq over the warp's 32 tokens (masked past nvalid)
+  float pr[4][2];
+  float mw = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int j = tok0 + 8 * nt + 2 * t4 + i;
+      pr[nt][i] = j < nvalid ? sacc[nt][i] * scale_log2 : -INFINITY;
+      mw = fmaxf(mw, pr[nt][i]);
+    }
+  mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
+  mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 2));
+  const float mref = mw == -INFINITY ? 0.f : mw;  // a warp past nvalid keeps p = 0
+  float lw = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      pr[nt][i] = ex2_approx(pr[nt][i] - mref);
+      lw += pr[nt][i];
+    }
+  lw += __shfl_xor_sync(0xffffffffu, lw, 1);
+  lw += __shfl_xor_sync(0xffffffffu, lw, 2);
+
+  // V: widen codes times scales to f16 (exact), 16 dimensions (8 code bytes)
+  // per job
+  cp_async_wait<0>();
+  __syncthreads();
+#pragma unroll 2
+  for (int e = tid; e < kBk * MB; e += 128) {
+    const int r = e / MB, gi = e % MB;
+    const uint2 c8 = lds_u64(s_vc + swz<CB>(r, gi >> 1) + (gi & 1) * 8);
+    const __half_raw hs = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)lds_u8(s_vs + r * SB + gi),
+                                                  __NV_E4M3);
+    const __half2 sc2 = __halves2half2(__half(hs), __half(hs));
+    uint32_t wv[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const uint32_t byte = ((b < 4 ? c8.x : c8.y) >> (8 * (b & 3))) & 0xFF;
+      const uint32_t h2 = e2m1x2_to_f16x2(byte);
+      const __half2 v2 = __hmul2(*reinterpret_cast<const __half2*>(&h2), sc2);
+      wv[b] = *reinterpret_cast<const uint32_t*>(&v2);
+    }
+    sm100::st_shared_v4(s_vb + swz<VROWB>(r, 2 * gi), wv[0], wv[1], wv[2], wv[3]);
+    sm100::st_shared_v4(s_vb + swz<VROWB>(r, 2 * gi + 1), wv[4], wv[5], wv[6], wv[7]);
+  }
+  __syncthreads();
+  float o[NC][4];
+#pragma unroll
+  for (int n = 0; n < NC; ++n)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[n][i] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {  // 16 tokens per k-step
+    const uint32_t a0 = f16x2_of(pr[2 * j][0], pr[2 * j][1]);
+    const uint32_t a2 = f16x2_of(pr[2 * j + 1][0], pr[2 * j + 1][1]);
+    const int r = tok0 + 16 * j + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+    for (int n = 0; n < NC; n += 2) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(s_vb + swz<VROWB>(r, n + (lane >> 4)), b0, b1, b2, b3);
+      mma_f16_16816(o[n], a0, 0u, a2, 0u, b0, b1);
+      mma_f16_16816(o[n + 1], a0, 0u, a2, 0u, b2, b3);
+    }
+  }
+  __syncthreads();  // every warp is done with the V tile: reuse it
+  float* red = reinterpret_cast<float*>(dsm + 2 * CTILE + 2 * STILE);  // [4 warps][8 heads][RS]
+  if (gq < G) {
+#pragma unroll
+    for (int n = 0; n < NC; ++n)
+      *reinterpret_cast<float2*>(red + (w * 8 + gq) * RS + 8 * n + 2 * t4) =
+          make_float2(o[n][0], o[n][1]);
+    if (t4 == 0) {
+      s_m[w][gq] = mw;
+      s_l[w][gq] = lw;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < G * D; e += 128) {
+    const int h = e / D, c = e % D;
+    float M = s_m[0][h];
+#pragma unroll
+    for (int i = 1; i < 4; ++i) M = fmaxf(M, s_m[i][h]);  // finite: token 0 is in warp 0
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float f = ex2_approx(s_m[i][h] - M);
+      num = fmaf(f, red[(i * 8 + h) * RS + c], num);
+      den = fmaf(f, s_l[i][h], den);
+    }
+    const size_t dst = ((size_t)s * H_q + (size_t)g * G + h) * k + slot;
+    part_o[dst * D + c] = num / den;
+    if (c == 0) part_lse[dst] = (M + __log2f(den)) * 0.69314718055994531f;
+  }
+}
+
 // One warp per (sequence, head). Lane i < k holds slot i: its block id, its
 // LSE and (through the warp reductions) the slot's weight. Every lane owns D/32
 // contiguous output columns, and the k partial rows of those columns are all
@@ -801,6 +1060,44 @@ cudaError_t launch_decode_attn(const void* q, const void* k_pages, const void* v
 #undef MSA_DEC
   int64_t nw = (int64_t)B * H_q;
   unsigned mg = (unsigned)std::min<int64_t>((nw * 32 + 255) / 256, 152 * 32);
+  if (d == 128)
+    decode_merge_kernel<128><<<mg, 256, 0, st>>>(part_o, part_lse, ids, seq_lens, max_pages, B,
+                                                 H_q, H_kv, k, (uint16_t*)out, lse);
+  else
+    decode_merge_kernel<64><<<mg, 256, 0, st>>>(part_o, part_lse, ids, seq_lens, max_pages, B,
+                                                H_q, H_kv, k, (uint16_t*)out, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_attn_fp4(const void* q, const void* k_codes, const void* k_scales,
+                                   const void* v_codes, const void* v_scales,
+                                   const int32_t* page_table, const int32_t* seq_lens,
+                                   const int32_t* ids, int B, int max_pages, int H_q, int H_kv,
+                                   int d, int k, float scale, void* out, float* lse, void* ws,
+                                   const Diag& dg, cudaStream_t st) {
+  float* part_o = (float*)ws;
+  float* part_lse = (float*)((unsigned char*)ws + align256((size_t)B * H_q * k * d * 4));
+  const float sl2 = scale * 1.4426950408889634f;
+  const unsigned tasks = (unsigned)((int64_t)B * H_kv * k);
+  if (tasks == 0) return cudaSuccess;
+  note_launches(2);  // attention, merge
+  cudaError_t e = cudaSuccess;
+#define MSA_DEC_FP4(DD)                                                                       \
+  do {                                                                                        \
+    constexpr int sm = dec_fp4_smem_bytes<DD>();                                              \
+    e = cudaFuncSetAttribute(decode_attn_fp4_kernel<DD>,                                      \
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, sm);                \
+    if (e != cudaSuccess) return e;                                                           \
+    decode_attn_fp4_kernel<DD><<<tasks, 128, sm, st>>>(                                       \
+        (const uint16_t*)q, (const uint8_t*)k_codes, (const uint8_t*)k_scales,                \
+        (const uint8_t*)v_codes, (const uint8_t*)v_scales, page_table, seq_lens, ids,         \
+        max_pages, H_q, H_kv, k, sl2, part_o, part_lse, dg);                                  \
+  } while (0)
+  if (d == 128) MSA_DEC_FP4(128);
+  else MSA_DEC_FP4(64);
+#undef MSA_DEC_FP4
+  const int64_t nw = (int64_t)B * H_q;
+  const unsigned mg = (unsigned)std::min<int64_t>((nw * 32 + 255) / 256, 152 * 32);
   if (d == 128)
     decode_merge_kernel<128><<<mg, 256, 0, st>>>(part_o, part_lse, ids, seq_lens, max_pages, B,
                                                  H_q, H_kv, k, (uint16_t*)out, lse);

@@ -160,5 +160,13 @@ cudaError_t launch_decode_attn(const void* q, const void* k_pages, const void* v
                                const int32_t* ids, int B, int max_pages, int H_q, int H_kv,
                                int d, int k, float scale, void* out, float* lse, void* ws,
                                const Diag& dg, cudaStream_t st);
+// decode attention over NVFP4 K / V pages (E2M1 codes, one E4M3 scale per 16
+// dimensions of a row), split-KV partials in ws and their merge
+cudaError_t launch_decode_attn_fp4(const void* q, const void* k_codes, const void* k_scales,
+                                   const void* v_codes, const void* v_scales,
+                                   const int32_t* page_table, const int32_t* seq_lens,
+                                   const int32_t* ids, int B, int max_pages, int H_q, int H_kv,
+                                   int d, int k, float scale, void* out, float* lse, void* ws,
+                                   const Diag& dg, cudaStream_t st);
 
 }  // namespace msa

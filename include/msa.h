@@ -341,6 +341,32 @@ int msa_decode(const void* q, const void* k_pages, const void* v_pages, int kv_d
                int H_q, int H_kv, int d, int Bk, int k, float scale, void* out, float* lse,
                void* workspace, size_t workspace_bytes, void* stream);
 
+/* Main branch of decode over an NVFP4 KV cache (the kernel release lists NVFP4
+ * and FP4 among its precisions: "MiniMax lança MSA ...", section "Kernel open
+ * source e MiniMax-M3"; about a quarter of the bf16 cache's bytes plus one scale
+ * byte per 16 elements):
+ *   k_codes, v_codes    [P, H_kv, Bk, d / 2] uint8: two OCP E2M1 codes per byte,
+ *                       the even dimension in the low nibble
+ *   k_scales, v_scales  [P, H_kv, Bk, d / 16] uint8: one E4M3 scale per 16
+ *                       consecutive dimensions of a row; value = e2m1 * scale
+ *   q                   [B, H_q, d] bf16, rounded to f16 for q . K^T (exact for
+ *                       |x| >= 2^-14 and below 65504, where every bf16 value
+ *                       fits f16's 11 significant bits)
+ * The attention itself is that of msa_decode on the decoded values (every
+ * E2M1 code times an E4M3 scale is a bf16 value). Workspace:
+ * msa_decode_workspace_bytes. Every device pointer is 16-byte aligned and owned
+ * by the caller. Errors as msa_decode: MSA_ERR_INVALID_ARG for a null or
+ * misaligned pointer or H_q not a multiple of H_kv, MSA_ERR_UNSUPPORTED for
+ * Bk != 128, d not 64 or 128, k above the largest top-k or more than 8 query
+ * heads per kv head, MSA_ERR_WORKSPACE for a missing or short workspace; block
+ * ids and sequence lengths are checked on the device (skipped and reported
+ * through msa_get_error). */
+int msa_decode_nvfp4(const void* q, const void* k_codes, const void* k_scales,
+                     const void* v_codes, const void* v_scales, const int32_t* page_table,
+                     const int32_t* seq_lens, const int32_t* block_ids, int B, int max_pages,
+                     int H_q, int H_kv, int d, int Bk, int k, float scale, void* out, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* Decode index branch without any allocation (no counterpart in the pages):
  * same inputs, output and rules as msa_index_select_decode, but the per-page
  * block scores go to a fixed 4 MiB scratch array compiled into the library

@@ -56,11 +56,14 @@ def bf16_to_np(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def check_close(name, got, want, atol):
+def check_close(name, got, want, atol, rtol=0.0):
+    """|got - want| <= atol + rtol * |want| everywhere; returns the largest |got - want|."""
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     err = np.abs(got - want)
-    worst = np.unravel_index(np.argmax(err), err.shape) if err.size else ()
-    assert err.size == 0 or err.max() <= atol, \
-        f"{name}: max |err| {err.max():.3e} > {atol} at {worst} (got {got[worst]}, want {want[worst]})"
+    excess = err - (atol + rtol * np.abs(want))
+    worst = np.unravel_index(np.argmax(excess), err.shape) if err.size else ()
+    assert err.size == 0 or excess.max() <= 0.0, \
+        f"{name}: |err| {err[worst]:.3e} > {atol} + {rtol} |want| at {worst} " \
+        f"(got {got[worst]}, want {want[worst]})"
     return float(err.max()) if err.size else 0.0

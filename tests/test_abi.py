@@ -132,6 +132,28 @@ def test_decode_index_nvfp4_rejects(msa):
              None) == -3                                             # no workspace
 
 
+def test_decode_nvfp4_rejects(msa):
+    f = msa._decode_fp4
+    # q, k_codes, k_scales, v_codes, v_scales, page_table, seq_lens, ids, B, max_pages, H_q,
+    # H_kv, d, Bk, k, scale, out, lse, ws, ws_bytes, stream
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 10, 32, 8, 128, 128, 16, 0.1,
+            FAKE, None, FAKE, 1 << 30, None]
+    a = list(base); a[4] = None
+    assert f(*a) == -1                             # no V scales
+    a = list(base); a[2] = FAKE + 8
+    assert f(*a) == -1                             # misaligned K scales
+    a = list(base); a[10], a[11] = 32, 2
+    assert f(*a) == -2                             # G = 16 > 8
+    a = list(base); a[12] = 96
+    assert f(*a) == -2                             # d not 64 or 128
+    a = list(base); a[13] = 64
+    assert f(*a) == -2                             # Bk != 128
+    a = list(base); a[18] = None
+    assert f(*a) == -3                             # no workspace
+    a = list(base); a[8] = 0
+    assert f(*a) == 0                              # no sequences: nothing to do
+
+
 def test_wait_limit_roundtrip(msa):
     old = msa.msa_set_wait_limit(123)
     assert msa.msa_set_wait_limit(old) == 123

@@ -674,6 +674,87 @@ def test_decode_index_nvfp4(msa, gaussian, d_idx, H_kv):
         assert ((a - b).abs() <= 1e-5 * b.abs().clamp(min=1.0)).all()
 
 
+def _nvfp4_pages(x_bits, rng, shape):
+    """NVFP4 pages of the given shape [P, H, Bk, d]: E2M1 codes two per byte
+    (even dimension low) and one E4M3 scale per 16 dimensions of a row, with the
+    decoded values as bf16 bits (exact). With x_bits (bf16 bits of that shape)
+    the values are quantised (scale = the E4M3 of amax / 6, at least the
+    smallest E4M3 subnormal; codes the nearest E2M1 value); without, codes are
+    drawn uniformly and scales from a few powers of two and 1.5 times one."""
+    e2m1 = np.array([oracle.e2m1_to_f64(c) for c in range(16)])
+    e4m3 = np.array([oracle.e4m3_to_f64(int(c)) for c in range(256)])
+    d = shape[-1]
+    if x_bits is not None:
+        xb = bits_f64(x_bits).reshape(*shape[:-1], d // 16, 16)
+        amax = np.abs(xb).max(axis=-1)
+        sc_codes = torch.from_numpy((np.maximum(amax, 0.012) / 6.0).astype(np.float32)) \
+            .to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        y = xb / e4m3[sc_codes][..., None]
+        idx = np.abs(np.abs(y)[..., None] - e2m1[:8]).argmin(axis=-1)
+        codes = (idx | np.where(y < 0, 8, 0)).astype(np.uint8).reshape(shape)
+    else:
+        codes = rng.integers(0, 16, size=shape).astype(np.uint8)
+        sc_codes = rng.choice(np.array([0x28, 0x30, 0x38, 0x3C, 0x40], dtype=np.uint8),
+                              size=(*shape[:-1], d // 16))
+    vals = e2m1[codes] * np.repeat(e4m3[sc_codes], 16, axis=-1)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
+    bits = (vals.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(bits_f64(bits), vals)                          # exact in bf16
+    return packed, sc_codes.astype(np.uint8), bits
+
+
+@pytest.mark.parametrize("gaussian,d,H_q,H_kv", [(False, 128, 8, 2), (False, 64, 16, 4),
+                                                 (True, 128, 32, 8)])
+def test_decode_nvfp4_kv(msa, gaussian, d, H_q, H_kv):
+    """NVFP4 K/V cache: the main branch of decode on the GPU's own ids against the
+    oracle on the decoded values, and against the bf16 path over the decoded
+    cache, with ragged lengths (one token, a page boundary, mid-page) and a
+    shuffled page table."""
+    kind = synth.KIND_GAUSS if gaussian else synth.KIND_INT
+    w = synth.make("decode", B=4, L=128 * 9 + 37, H_q=H_q, H_kv=H_kv, d=d, d_idx=d, kind=kind,
+                   k=6)
+    lens = np.array([1, 129, 700, w.L], dtype=np.int32)
+    dev = torch.device("cuda")
+    pt = torch.from_numpy(synth.page_table(w)).to(dev)
+    order = pt.flatten().long()
+    sl = torch.from_numpy(lens).to(dev)
+    qidx = synth.device_rows(w, synth.T_QIDX, [(s, int(lens[s]) - 1) for s in range(w.B)])
+    kidx = synth.device_paged(w, synth.T_KIDX, pt)[:, 0].contiguous()
+    ids = msa.msa_index_select_decode(qidx, kidx, pt, sl, w.Bk, w.k)
+    q = synth.device_rows(w, synth.T_Q, [(s, int(lens[s]) - 1) for s in range(w.B)])
+    rng = np.random.default_rng(23)
+    shape = (w.B * w.nb, w.H_kv, w.Bk, d)
+    dev_pages = {}
+    host_bits = {}
+    for name, t in (("k", synth.T_K), ("v", synth.T_V)):
+        packed, sc, bits = _nvfp4_pages(synth.host_paged(w, t) if gaussian else None, rng, shape)
+        for key, arr, dt in ((name + "c", packed, torch.uint8), (name + "s", sc, torch.uint8),
+                             (name + "b", bits.view(np.int16), torch.int16)):
+            x = torch.empty(arr.shape, dtype=dt, device=dev)
+            x[order] = torch.from_numpy(arr).to(dev)
+            dev_pages[key] = x
+        host_bits[name] = bits
+    o4, l4 = msa.msa_decode_nvfp4(q, dev_pages["kc"], dev_pages["ks"], dev_pages["vc"],
+                                  dev_pages["vs"], pt, sl, ids, w.Bk, w.scale)
+    ob, lb = msa.msa_decode(q, dev_pages["kb"].view(torch.bfloat16),
+                            dev_pages["vb"].view(torch.bfloat16), pt, sl, ids, w.Bk, w.scale)
+    torch.cuda.synchronize()
+    assert msa.msa_get_error() == 0
+    qh = np.stack([synth.host_rows(w, synth.T_Q, s, [int(lens[s]) - 1])[0] for s in range(w.B)])
+    o_ref, l_ref = oracle.decode_attn(qh, host_bits["k"], host_bits["v"],
+                                      synth.page_table(w, permute=False), lens, ids.cpu().numpy(),
+                                      w.Bk, w.scale)
+    # V values reach 12 here, so the bound adds the output's own bf16 rounding
+    # to the absolute one: half a step, at most 2^-8 |o|, against the exact
+    # oracle; a whole step, at most 2^-7 |o|, between two rounded outputs
+    e_o = check_close("o", bf16_to_np(o4), o_ref, TOL_O, rtol=2.0 ** -8)
+    e_l = check_close("lse", l4.cpu().numpy(), l_ref, TOL_LSE)
+    check_close("o vs bf16 path", bf16_to_np(o4), bf16_to_np(ob), TOL_O, rtol=2.0 ** -7)
+    check_close("lse vs bf16 path", l4.cpu().numpy(), lb.cpu().numpy(), TOL_LSE)
+    print(f"[decode nvfp4 kv gaussian={gaussian} d={d} G={H_q // H_kv}] max|err| o {e_o:.3e} "
+          f"lse {e_l:.3e}")
+
+
 def test_decode_matches_prefill_row_on_gpu(msa):
     """Decoding the last token against the cache equals the last prefill row."""
     w = synth.make("decode", B=1, L=128 * 9 + 5, H_q=8, H_kv=2, d=128, d_idx=128,
