@@ -14,14 +14,17 @@
 // next row) is already loading while the current one is ranked. Per chunk:
 //   1. the values are staged in the half's shared buffer, and every lane takes
 //      the max of its even and of its odd blocks (32 group maxima per row);
-//   2. tau = max(15th largest group max, worst key kept so far): at least k-1
-//      keys are >= tau, so no key below tau can be in the answer. Once both
-//      rows of the warp keep k-1 keys, the worst kept key alone is tried first,
-//      and the 32-element network runs only when more than 32 values reach it;
+//   2. tau = max((k-1)-th largest group max, worst key kept so far): at least
+//      k-1 keys are >= tau, so no key below tau can be in the answer. The group
+//      maxima are taken as two lists of 16 (even, odd), each bitonic-sorted
+//      across the half, and tau read off their merge. Once both rows of the
+//      warp keep k-1 keys, the worst kept key alone is tried first, and the
+//      group maxima are needed only when more than 32 values reach it;
 //   3. the keys >= tau (typically 15-30) are compacted into shared memory (each
 //      lane reads its survivors back from its staged values); every survivor
-//      counts the survivors that beat it, and the k-1 with the lowest counts
-//      are kept, one per lane, in descending order. More than 32 survivors in
+//      counts the survivors that beat it (on the fp32 scores when no two are
+//      equal, else on the 64-bit keys), and the k-1 with the lowest counts are
+//      kept, one per lane, in descending order. More than 32 survivors in
 //      either half send both halves through k-1 rounds of arg-max instead.
 // Finally the kept ids plus the local block are sorted ascending and written.
 // Blocks past the candidates read as NaN, which no comparison keeps and which
@@ -64,29 +67,30 @@ __device__ __forceinline__ float key_value(uint64_t key) {
   return __uint_as_float(b);
 }
 
-// Bitonic sort, descending, of the 32 floats a half holds 2 per lane: element
-// e = 2 hl + r is a[r] of half-lane hl, so the exchanges at distance 1 stay in
-// the lane and the others are shuffles at lane distance stride / 2. Both
-// elements of a lane share each stage's direction.
-__device__ __forceinline__ void sort32h_desc(float& a0, float& a1, int hl) {
+// The kfar-th largest (1 <= kfar <= 15) of the 32 floats a half holds 2 per
+// lane. a (one per lane) is bitonic-sorted descending and b ascending across the
+// half; the kfar-th largest of the union of two sorted lists is the largest,
+// over the splits i + j = kfar, of min(i-th largest of a, j-th largest of b),
+// with the 0-th largest read as +inf. Lane hl takes the split i = hl + 1 (and
+// lane kfar the split i = 0), then a max over the half. Returned in every lane.
+__device__ __forceinline__ float kth_largest32h(float a, float b, int kfar, int hl) {
 #pragma unroll
-  for (int size = 2; size <= 32; size <<= 1)
+  for (int size = 2; size <= 16; size <<= 1)
 #pragma unroll
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const bool up = ((2 * hl) & size) == 0;  // this pair descends
-      if (stride == 1) {
-        const float mx = fmaxf(a0, a1), mn = fminf(a0, a1);
-        a0 = up ? mx : mn;
-        a1 = up ? mn : mx;
-      } else {
-        const bool lower = (hl & (stride >> 1)) == 0;
-        const bool take_max = lower == up;
-        const float p0 = __shfl_xor_sync(kAll, a0, stride >> 1);
-        const float p1 = __shfl_xor_sync(kAll, a1, stride >> 1);
-        a0 = take_max ? fmaxf(a0, p0) : fminf(a0, p0);
-        a1 = take_max ? fmaxf(a1, p1) : fminf(a1, p1);
-      }
+      const float pa = __shfl_xor_sync(kAll, a, stride);
+      const float pb = __shfl_xor_sync(kAll, b, stride);
+      const bool low_min = ((hl & stride) == 0) == ((hl & size) == 0);  // ascending: lower lane keeps the min
+      a = low_min ? fmaxf(a, pa) : fminf(a, pa);
+      b = low_min ? fminf(b, pb) : fmaxf(b, pb);
     }
+  // b ascending: its j-th largest (1-based) sits in half-lane 16 - j
+  const int src = hl <= kfar - 2 ? 17 - kfar + hl : 16 - kfar;
+  const float bs = __shfl_sync(kAll, b, src, 16);
+  float t = hl <= kfar - 2 ? fminf(a, bs) : hl == kfar - 1 ? a : hl == kfar ? bs : -INFINITY;
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) t = fmaxf(t, __shfl_xor_sync(kAll, t, off));
+  return t;
 }
 
 // bitonic sort of one int per lane within each 16-lane half, ascending
@@ -201,14 +205,14 @@ __device__ __forceinline__ void survivors(const float4* sv, float tau, int kfar,
   total = __shfl_sync(kAll, incl, 15, 16);
 }
 
-__device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1, uint64_t* buf,
-                                           int c0, int kfar, int hl, uint64_t& best,
+__device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1, float* vb,
+                                           int* ib, int c0, int kfar, int hl, uint64_t& best,
                                            float& best_min) {
   uint32_t mask;
   bool keep_old;
   int cnt, incl, total;
   // once both halves keep kfar entries, their worst kept score is a threshold
-  // of its own (kfar values reach it); the sorting network below is needed only
+  // of its own (kfar values reach it); the group maxima below are needed only
   // when too many of the chunk's values reach it
   bool settled = false;
   if (__all_sync(kAll, best_min > -INFINITY)) {
@@ -218,38 +222,72 @@ __device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1,
   if (!settled) {
     // threshold: the kfar-th largest group max (>= kfar values reach it) or the
     // worst value kept so far, whichever is larger
-    sort32h_desc(m0, m1, hl);
-    float tau = __shfl_sync(kAll, (kfar - 1) & 1 ? m1 : m0, (kfar - 1) >> 1, 16);
-    tau = fmaxf(tau, best_min);
+    const float tau = fmaxf(kth_largest32h(m0, m1, kfar, hl), best_min);
     survivors(sv, tau, kfar, hl, best, mask, keep_old, cnt, incl, total);
   }
   const float* svf = reinterpret_cast<const float*>(sv);
   if (!__any_sync(kAll, total > kCap)) {
+    const float nan = __int_as_float(0x7fffffff);
     int p = incl - cnt;
-    if (keep_old) buf[p++] = best;
+    if (keep_old) {
+      vb[p] = key_value(best);
+      ib[p++] = key_id(best);
+    }
     while (mask) {  // this lane's survivors, read back from its own staged values
       const int j = __ffs(mask) - 1;
       mask &= mask - 1;
       const int e = (j >> 2) * 64 + hl * 4 + (j & 3);
-      buf[p++] = rank_key(svf[e], (uint32_t)(c0 + e));
+      vb[p] = svf[e];
+      ib[p++] = c0 + e;
     }
+    if (hl < 4) vb[total + hl] = nan;  // pads the last vector of the loop below
     __syncwarp();
-    const uint64_t a0 = hl < total ? buf[hl] : 0;
-    const uint64_t a1 = hl + 16 < total ? buf[hl + 16] : 0;
+    const float f0 = hl < total ? vb[hl] : nan;
+    const float f1 = hl + 16 < total ? vb[hl + 16] : nan;
+    const int i0 = ib[hl], i1 = ib[hl + 16];  // read only where hl (+ 16) < total
     // rank of a survivor = how many survivors beat it (keys are distinct, so the
-    // ranks are a permutation); the kfar best land in slots 0..kfar-1, descending
+    // ranks are a permutation); the kfar best land in slots 0..kfar-1, descending.
+    // Counted on the scores first: with no two equal scores among the survivors,
+    // the survivors scoring >= a survivor are exactly those beating it plus
+    // itself, and these counts sum to total (total + 1) / 2; equal scores make
+    // the sum larger, and then the ranks are counted on the 64-bit keys.
     int r0 = 0, r1 = 0;
-#pragma unroll 4
-    for (int j = 0; j < total; ++j) {
-      const uint64_t y = buf[j];
-      r0 += y > a0 ? 1 : 0;
-      r1 += y > a1 ? 1 : 0;
+    const float4* vb4 = reinterpret_cast<const float4*>(vb);
+    for (int j = 0; 4 * j < total; ++j) {
+      const float4 y = vb4[j];
+      r0 += (y.x >= f0) + (y.y >= f0) + (y.z >= f0) + (y.w >= f0);
+      r1 += (y.x >= f1) + (y.y >= f1) + (y.z >= f1) + (y.w >= f1);
+    }
+    int sum = r0 + r1;  // NaN rows (past total) count 0
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(kAll, sum, off);
+    if (__any_sync(kAll, sum != total * (total + 1) / 2)) {
+      const uint64_t a0 = hl < total ? rank_key(f0, (uint32_t)i0) : 0;
+      const uint64_t a1 = hl + 16 < total ? rank_key(f1, (uint32_t)i1) : 0;
+      r0 = 0;
+      r1 = 0;
+      for (int j = 0; j < total; ++j) {
+        const uint64_t y = rank_key(vb[j], (uint32_t)ib[j]);
+        r0 += y > a0 ? 1 : 0;
+        r1 += y > a1 ? 1 : 0;
+      }
+    } else {
+      --r0;
+      --r1;
     }
     __syncwarp();
-    if (hl < total && r0 < kfar) buf[r0] = a0;
-    if (hl + 16 < total && r1 < kfar) buf[r1] = a1;
+    if (hl < total && r0 < kfar) {
+      vb[r0] = f0;
+      ib[r0] = i0;
+    }
+    if (hl + 16 < total && r1 < kfar) {
+      vb[r1] = f1;
+      ib[r1] = i1;
+    }
     __syncwarp();
-    best = hl < kfar ? buf[hl] : 0;
+    // total >= kfar: tau leaves at least kfar survivors
+    best = hl < kfar ? rank_key(vb[hl], (uint32_t)ib[hl]) : 0;
+    best_min = vb[kfar - 1];
     __syncwarp();
   } else {
     // rare (heavy ties): extract the kfar best of each half one by one
@@ -272,8 +310,8 @@ __device__ __forceinline__ void rank_chunk(const float4* sv, float m0, float m1,
       prev = m;
     }
     best = nb_best;
+    best_min = key_value(shfl64_h(best, kfar - 1));
   }
-  best_min = key_value(shfl64_h(best, kfar - 1));
 }
 
 template <bool VEC>
@@ -281,7 +319,8 @@ __global__ void __launch_bounds__(kWarps * 32, 6)
 topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, int64_t ld, int Bk,
             int bk_shift, int k, int64_t q_offset, const int32_t* __restrict__ seq_lens,
             int32_t* __restrict__ ids, Diag dg) {
-  __shared__ uint64_t buf[kWarps][2][kCap + 1];  // +1: the halves on different banks
+  __shared__ float4 vbuf[kWarps][2][kCap / 4 + 1];  // survivor scores, NaN-padded
+  __shared__ int ibuf[kWarps][2][kCap + 1];         // their block ids
   __shared__ float4 sval[kWarps][2][8 * 16];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
@@ -291,7 +330,8 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
   const uint32_t rows = (uint32_t)n_rows;           // at most INT_MAX (host check)
   const int sq = (int)(stride / n_g), sr = (int)(stride % n_g);
   float4* sv = sval[wid][half];
-  uint64_t* bf = buf[wid][half];
+  float* vbf = reinterpret_cast<float*>(vbuf[wid][half]);
+  int* ibf = ibuf[wid][half];
 
   // Moves the cursor to the first row at or after it that needs ranking; rows
   // that need none (position outside the score rows, or no more candidates than
@@ -348,7 +388,7 @@ topk_kernel(const float* __restrict__ S, int64_t n_rows, int n_g, int64_t nb, in
     const bool act2 = nxt.r < rows;
     load_chunk<VEC>(vn, S + (act2 ? (int64_t)nxt.r * ld + c2 : 0),
                     act2 ? min(loc2 - c2, kHalf) : 0, hl);
-    rank_chunk(sv, m0, m1, bf, c0, kfar, hl, best, best_min);
+    rank_chunk(sv, m0, m1, vbf, ibf, c0, kfar, hl, best, best_min);
     const bool done = act && c0 + kHalf >= loc;
     if (__any_sync(kAll, done)) {  // kept ids plus the local block, ascending
       int id = hl < kfar ? (best ? key_id(best) : INT_MAX) : (hl == kfar ? loc : INT_MAX);
