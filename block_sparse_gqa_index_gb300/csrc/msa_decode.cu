@@ -18,8 +18,11 @@
 //   query heads of the group against the block's visible tokens, with the
 //   block's K and V bytes all in flight at once (two TMA copies, or 16-byte
 //   cp.async for rows narrower than 128 bytes, into swizzled shared memory)
-//   and both products on mma.m16n8k16; writes the block's normalised output
-//   and LSE (split-KV partials).
+//   and both products on mma.m16n8k16. Each warp scores 32 of the block's
+//   tokens; the block's softmax max and P pass through shared memory, and each
+//   warp then forms P V for a quarter of the output columns over all 128
+//   tokens, so it writes its columns of the block's normalised output (and the
+//   LSE) straight from its accumulators (split-KV partials).
 // decode_merge_kernel: combines the k partials of every (sequence, head), one
 //   warp each, with all of its partial rows in flight at once.
 #include <cuda.h>
@@ -363,9 +366,8 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
   constexpr int TILE = kBk * ROWB;  // bytes of one K or V block
   constexpr int KS = D / 16;        // k-steps of q K^T
   constexpr int NC = D / 8;         // 8-column tiles of P V
-  constexpr int RS = D + 8;         // row stride (floats) of the combine buffer
   constexpr bool TMA = dec_tma<D, FP8>();
-  static_assert(4 * 8 * RS * 4 <= 2 * TILE, "combine buffer fits the K/V tiles");
+  static_assert(8 * (kBk / 2 + 4) * 4 <= TILE, "P fits the K tile");
   extern __shared__ __align__(1024) unsigned char dsm[];
   // tile addressing: TMA boxes or the cp.async layout
   auto tile_off = [](int r, int c) -> uint32_t {
@@ -487,7 +489,8 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       }
   }
 
-  // warp-local softmax of head gq over the warp's 32 tokens (masked past nvalid)
+  // softmax of head gq over the block: each warp's max over its 32 tokens
+  // (masked past nvalid), then the block max through shared memory
   float pr[4][2];
   float mw = -INFINITY;
 #pragma unroll
@@ -500,59 +503,64 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     }
   mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
   mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 2));
-  const float mref = mw == -INFINITY ? 0.f : mw;  // a warp past nvalid keeps p = 0
+  if (t4 == 0) s_m[w][gq] = mw;
+  __syncthreads();  // every warp's max is in, and every warp is done with K
+  // finite: token 0 is valid and belongs to warp 0
+  const float M = fmaxf(fmaxf(s_m[0][gq], s_m[1][gq]), fmaxf(s_m[2][gq], s_m[3][gq]));
+  // P (bf16 pairs, [8 heads][128 tokens], rows padded to PW words so that a
+  // warp's fragment loads hit 32 banks) over the K tile
+  constexpr int PW = kBk / 2 + 4;
+  uint32_t* pw = reinterpret_cast<uint32_t*>(dsm) + gq * PW + t4;
   float lw = 0.f;
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      pr[nt][i] = ex2_approx(pr[nt][i] - mref);
-      lw += pr[nt][i];
-    }
+  for (int nt = 0; nt < 4; ++nt) {
+    const float p0 = ex2_approx(pr[nt][0] - M), p1 = ex2_approx(pr[nt][1] - M);
+    lw += p0 + p1;
+    pw[(tok0 + 8 * nt) / 2] = pack_bf16x2(p0, p1);
+  }
   lw += __shfl_xor_sync(0xffffffffu, lw, 1);
   lw += __shfl_xor_sync(0xffffffffu, lw, 2);
+  if (t4 == 0) s_l[w][gq] = lw;
 
   if constexpr (TMA) {
     if (!sm100::mbar_wait(&kv_bar[1], 0, &abort_flag, dg)) {  // V has landed
       sm100::mbar_drain(&kv_bar[1], 0);
       return;
     }
-    // the block's rows past its last token hold other data: zero this warp's
-    // V rows there (their P is 0, and 0 times a NaN is not)
-    if (nvalid < tok0 + 32) {
-      for (int e = lane; e < 32 * CPR; e += 32) {
-        const int r = tok0 + e / CPR;
-        if (r >= nvalid) sm100::st_shared_v4(sv + tile_off(r, e % CPR), 0u, 0u, 0u, 0u);
-      }
-      __syncwarp();
-    }
+    // the block's rows past its last token hold other data: zero them (their P
+    // is 0, and 0 times a NaN is not)
+    for (int e = nvalid * CPR + tid; e < kBk * CPR; e += 128)
+      sm100::st_shared_v4(sv + tile_off(e / CPR, e % CPR), 0u, 0u, 0u, 0u);
   } else {
     cp_async_wait<0>();  // V has landed
-    __syncthreads();
   }
-  float o[NC][4];
+  __syncthreads();  // P, the sums and V are complete
+
+  // O[:, warp's quarter of the columns] = P V over the block's 128 tokens
+  constexpr int NW = NC / 4;  // 8-column tiles per warp
+  const int cb = w * NW;      // the warp's first 8-column tile
+  float o[NW][4];
 #pragma unroll
-  for (int n = 0; n < NC; ++n)
+  for (int n = 0; n < NW; ++n)
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[n][i] = 0.f;
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {  // 16 tokens per k-step
-    const uint32_t a0 = pack_bf16x2(pr[2 * j][0], pr[2 * j][1]);
-    const uint32_t a2 = pack_bf16x2(pr[2 * j + 1][0], pr[2 * j + 1][1]);
+  for (int j = 0; j < kBk / 16; ++j) {  // 16 tokens per k-step
+    const uint32_t a0 = pw[8 * j], a2 = pw[8 * j + 4];  // tokens 16 j + 2 t4 (+ 8)
     if constexpr (!FP8) {
-      const int r = tok0 + 16 * j + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int r = 16 * j + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-      for (int n = 0; n < NC; n += 2) {
+      for (int n = 0; n < NW; n += 2) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(sv + tile_off(r, n + (lane >> 4)), b0, b1, b2, b3);
+        ldsm_x4_t(sv + tile_off(r, cb + n + (lane >> 4)), b0, b1, b2, b3);
         mma_bf16_16816(o[n], a0, 0u, a2, 0u, b0, b1);
         mma_bf16_16816(o[n + 1], a0, 0u, a2, 0u, b2, b3);
       }
     } else {
-      const int r = tok0 + 16 * j + 2 * t4;
+      const int r = 16 * j + 2 * t4;
 #pragma unroll
-      for (int n = 0; n < NC; ++n) {
-        const int col = 8 * n + gq;
+      for (int n = 0; n < NW; ++n) {
+        const int col = 8 * (cb + n) + gq;
         const int ch = col >> 4, by = col & 15;
         const uint32_t v00 = lds_u8(sv + tile_off(r, ch) + by);
         const uint32_t v01 = lds_u8(sv + tile_off(r + 1, ch) + by);
@@ -563,34 +571,16 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
       }
     }
   }
-  __syncthreads();  // every warp is done with the K and V tiles: reuse them
-  float* red = reinterpret_cast<float*>(dsm);  // [4 warps][8 heads][RS]
+  // the block's partial for head gq: its columns straight from the accumulators
   if (gq < G) {
+    const float l = (s_l[0][gq] + s_l[1][gq]) + (s_l[2][gq] + s_l[3][gq]);
+    const float f = vs / l;
+    const size_t dst = ((size_t)s * H_q + (size_t)g * G + gq) * k + slot;
+    float* po = part_o + dst * D + 8 * cb + 2 * t4;
 #pragma unroll
-    for (int n = 0; n < NC; ++n)
-      *reinterpret_cast<float2*>(red + (w * 8 + gq) * RS + 8 * n + 2 * t4) =
-          make_float2(o[n][0], o[n][1]);
-    if (t4 == 0) {
-      s_m[w][gq] = mw;
-      s_l[w][gq] = lw;
-    }
-  }
-  __syncthreads();
-  for (int e = tid; e < G * D; e += 128) {
-    const int h = e / D, c = e % D;
-    float M = s_m[0][h];
-#pragma unroll
-    for (int i = 1; i < 4; ++i) M = fmaxf(M, s_m[i][h]);  // finite: token 0 is in warp 0
-    float num = 0.f, den = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float f = ex2_approx(s_m[i][h] - M);
-      num = fmaf(f, red[(i * 8 + h) * RS + c], num);
-      den = fmaf(f, s_l[i][h], den);
-    }
-    const size_t dst = ((size_t)s * H_q + (size_t)g * G + h) * k + slot;
-    part_o[dst * D + c] = num * vs / den;
-    if (c == 0) part_lse[dst] = (M + __log2f(den)) * 0.69314718055994531f;
+    for (int n = 0; n < NW; ++n)
+      *reinterpret_cast<float2*>(po + 8 * n) = make_float2(o[n][0] * f, o[n][1] * f);
+    if (w == 0 && t4 == 0) part_lse[dst] = (M + __log2f(l)) * 0.69314718055994531f;
   }
 }
 
@@ -647,8 +637,6 @@ decode_attn_fp4_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict
   constexpr int VROWB = D * 2;       // bf16 row of the widened V tile
   constexpr int MB = D / 16;         // micro-blocks of a row
   constexpr int NC = D / 8;          // 8-column tiles of P V
-  constexpr int RS = D + 8;          // row stride (floats) of the combine buffer
-  static_assert(4 * 8 * RS * 4 <= kBk * VROWB, "combine buffer fits the V tile");
   extern __shared__ __align__(128) unsigned char dsm[];
   const uint32_t s_kc = smem_addr(dsm), s_vc = s_kc + CTILE;
   const uint32_t s_ks = s_vc + CTILE, s_vs = s_ks + STILE;
@@ -756,7 +744,8 @@ decode_attn_fp4_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict
     }
   }
 
-  // warp-local softmax of head gq over the warp's 32 tokens (masked past nvalid)
+  // softmax of head gq over the block: each warp's max over its 32 tokens
+  // (masked past nvalid), then the block max through shared memory
   float pr[4][2];
   float mw = -INFINITY;
 #pragma unroll
@@ -769,22 +758,29 @@ decode_attn_fp4_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict
     }
   mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 1));
   mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 2));
-  const float mref = mw == -INFINITY ? 0.f : mw;  // a warp past nvalid keeps p = 0
+  if (t4 == 0) s_m[w][gq] = mw;
+  cp_async_wait<0>();  // this thread's V chunks have landed
+  __syncthreads();     // every warp's max and V chunks are in, every warp is done with K
+  // finite: token 0 is valid and belongs to warp 0
+  const float M = fmaxf(fmaxf(s_m[0][gq], s_m[1][gq]), fmaxf(s_m[2][gq], s_m[3][gq]));
+  // P (f16 pairs, [8 heads][128 tokens], rows padded to PW words so that a
+  // warp's fragment loads hit 32 banks) over the K codes
+  constexpr int PW = kBk / 2 + 4;
+  static_assert(8 * PW * 4 <= CTILE, "P fits the K code tile");
+  uint32_t* pw = reinterpret_cast<uint32_t*>(dsm) + gq * PW + t4;
   float lw = 0.f;
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      pr[nt][i] = ex2_approx(pr[nt][i] - mref);
-      lw += pr[nt][i];
-    }
+  for (int nt = 0; nt < 4; ++nt) {
+    const float p0 = ex2_approx(pr[nt][0] - M), p1 = ex2_approx(pr[nt][1] - M);
+    lw += p0 + p1;
+    pw[(tok0 + 8 * nt) / 2] = f16x2_of(p0, p1);
+  }
   lw += __shfl_xor_sync(0xffffffffu, lw, 1);
   lw += __shfl_xor_sync(0xffffffffu, lw, 2);
+  if (t4 == 0) s_l[w][gq] = lw;
 
   // V: widen codes times scales to f16 (exact), 16 dimensions (8 code bytes)
   // per job
-  cp_async_wait<0>();
-  __syncthreads();
 #pragma unroll 2
   for (int e = tid; e < kBk * MB; e += 128) {
     const int r = e / MB, gi = e % MB;
@@ -803,53 +799,38 @@ decode_attn_fp4_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict
     sm100::st_shared_v4(s_vb + swz<VROWB>(r, 2 * gi), wv[0], wv[1], wv[2], wv[3]);
     sm100::st_shared_v4(s_vb + swz<VROWB>(r, 2 * gi + 1), wv[4], wv[5], wv[6], wv[7]);
   }
-  __syncthreads();
-  float o[NC][4];
+  __syncthreads();  // P, the sums and the widened V are complete
+
+  // O[:, warp's quarter of the columns] = P V over the block's 128 tokens
+  constexpr int NW = NC / 4;  // 8-column tiles per warp
+  const int cb = w * NW;      // the warp's first 8-column tile
+  float o[NW][4];
 #pragma unroll
-  for (int n = 0; n < NC; ++n)
+  for (int n = 0; n < NW; ++n)
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[n][i] = 0.f;
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {  // 16 tokens per k-step
-    const uint32_t a0 = f16x2_of(pr[2 * j][0], pr[2 * j][1]);
-    const uint32_t a2 = f16x2_of(pr[2 * j + 1][0], pr[2 * j + 1][1]);
-    const int r = tok0 + 16 * j + (lane & 7) + ((lane >> 3) & 1) * 8;
+  for (int j = 0; j < kBk / 16; ++j) {  // 16 tokens per k-step
+    const uint32_t a0 = pw[8 * j], a2 = pw[8 * j + 4];  // tokens 16 j + 2 t4 (+ 8)
+    const int r = 16 * j + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-    for (int n = 0; n < NC; n += 2) {
+    for (int n = 0; n < NW; n += 2) {
       uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(s_vb + swz<VROWB>(r, n + (lane >> 4)), b0, b1, b2, b3);
+      ldsm_x4_t(s_vb + swz<VROWB>(r, cb + n + (lane >> 4)), b0, b1, b2, b3);
       mma_f16_16816(o[n], a0, 0u, a2, 0u, b0, b1);
       mma_f16_16816(o[n + 1], a0, 0u, a2, 0u, b2, b3);
     }
   }
-  __syncthreads();  // every warp is done with the V tile: reuse it
-  float* red = reinterpret_cast<float*>(dsm + 2 * CTILE + 2 * STILE);  // [4 warps][8 heads][RS]
+  // the block's partial for head gq: its columns straight from the accumulators
   if (gq < G) {
+    const float l = (s_l[0][gq] + s_l[1][gq]) + (s_l[2][gq] + s_l[3][gq]);
+    const float f = 1.f / l;
+    const size_t dst = ((size_t)s * H_q + (size_t)g * G + gq) * k + slot;
+    float* po = part_o + dst * D + 8 * cb + 2 * t4;
 #pragma unroll
-    for (int n = 0; n < NC; ++n)
-      *reinterpret_cast<float2*>(red + (w * 8 + gq) * RS + 8 * n + 2 * t4) =
-          make_float2(o[n][0], o[n][1]);
-    if (t4 == 0) {
-      s_m[w][gq] = mw;
-      s_l[w][gq] = lw;
-    }
-  }
-  __syncthreads();
-  for (int e = tid; e < G * D; e += 128) {
-    const int h = e / D, c = e % D;
-    float M = s_m[0][h];
-#pragma unroll
-    for (int i = 1; i < 4; ++i) M = fmaxf(M, s_m[i][h]);  // finite: token 0 is in warp 0
-    float num = 0.f, den = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float f = ex2_approx(s_m[i][h] - M);
-      num = fmaf(f, red[(i * 8 + h) * RS + c], num);
-      den = fmaf(f, s_l[i][h], den);
-    }
-    const size_t dst = ((size_t)s * H_q + (size_t)g * G + h) * k + slot;
-    part_o[dst * D + c] = num / den;
-    if (c == 0) part_lse[dst] = (M + __log2f(den)) * 0.69314718055994531f;
+    for (int n = 0; n < NW; ++n)
+      *reinterpret_cast<float2*>(po + 8 * n) = make_float2(o[n][0] * f, o[n][1] * f);
+    if (w == 0 && t4 == 0) part_lse[dst] = (M + __log2f(l)) * 0.69314718055994531f;
   }
 }
 
