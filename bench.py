@@ -890,7 +890,7 @@ def main():
             "tflops": round((p_fli + p_fla) / (p_ms * 1e-3) / 1e12, 2)}
         wd = synth.make("decode")
         for fp8, fp8_index, fp4_index, fp4_kv in DECODE_VARIANTS:
-            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, 1, fp8_index, fp4_index, fp4_kv)
+            i_ms, a_ms = time_decode(msa, wd, fp8, args.steps, 3, fp8_index, fp4_index, fp4_kv)
             torch.cuda.empty_cache()
             kv_elem = 0.5 + 1.0 / 16 if fp4_kv else (1.0 if fp8 else 2.0)
             kv_bytes = 2.0 * wd.B * wd.n_g * (wd.k - 1) * wd.Bk * wd.d * kv_elem + \

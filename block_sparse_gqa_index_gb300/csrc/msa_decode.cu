@@ -332,8 +332,9 @@ decode_index_fp4_kernel(const uint16_t* __restrict__ q_idx, const unsigned char*
 }
 
 // K / V rows of 128 bytes or a multiple of it arrive by TMA (one thread, two
-// mbarriers, 128-byte swizzled boxes through a 3-D map over the pages);
-// narrower rows by 16-byte cp.async into the row-swizzled layout
+// mbarriers, 128-byte swizzled boxes through a 3-D map over the pages; a whole
+// block as 128-row boxes, the partial last block as the 16-row boxes that hold
+// its tokens); narrower rows by 16-byte cp.async into the row-swizzled layout
 template <int D, bool FP8>
 __host__ __device__ constexpr bool dec_tma() {
   return (D * (FP8 ? 1 : 2)) % 128 == 0;
@@ -354,6 +355,8 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 template <int D, bool FP8>
 __global__ void __launch_bounds__(128, FP8 ? 6 : 3)
 decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_k16,
+                   const __grid_constant__ CUtensorMap tm_v16,
                    const uint16_t* __restrict__ q, const void* __restrict__ kp,
                    const void* __restrict__ vp, const float* __restrict__ k_scale,
                    const float* __restrict__ v_scale, const int32_t* __restrict__ page_table,
@@ -414,14 +417,30 @@ decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_consta
     __syncthreads();
     if (tid == 0) {
       const int32_t z = (int32_t)(page * H_kv + g);
-      sm100::mbar_arrive_expect_tx(&kv_bar[0], TILE);
+      if (nvalid == kBk) {  // a whole block: one 128-row box per 128-byte column chunk
+        sm100::mbar_arrive_expect_tx(&kv_bar[0], TILE);
 #pragma unroll
-      for (int c = 0; c < ROWB / 128; ++c)
-        sm100::tma_load_3d(dsm + c * kBk * 128, &tm_k, &kv_bar[0], c * (128 / EB), 0, z);
-      sm100::mbar_arrive_expect_tx(&kv_bar[1], TILE);
+        for (int c = 0; c < ROWB / 128; ++c)
+          sm100::tma_load_3d(dsm + c * kBk * 128, &tm_k, &kv_bar[0], c * (128 / EB), 0, z);
+        sm100::mbar_arrive_expect_tx(&kv_bar[1], TILE);
 #pragma unroll
-      for (int c = 0; c < ROWB / 128; ++c)
-        sm100::tma_load_3d(dsm + TILE + c * kBk * 128, &tm_v, &kv_bar[1], c * (128 / EB), 0, z);
+        for (int c = 0; c < ROWB / 128; ++c)
+          sm100::tma_load_3d(dsm + TILE + c * kBk * 128, &tm_v, &kv_bar[1], c * (128 / EB), 0,
+                             z);
+      } else {  // the partial last block: only its 16-row groups that hold tokens
+        const int nbox = (nvalid + 15) >> 4;
+        const uint32_t bytes = (uint32_t)(nbox * 16 * ROWB);
+        sm100::mbar_arrive_expect_tx(&kv_bar[0], bytes);
+        for (int c = 0; c < ROWB / 128; ++c)
+          for (int b = 0; b < nbox; ++b)
+            sm100::tma_load_3d(dsm + c * kBk * 128 + b * 16 * 128, &tm_k16, &kv_bar[0],
+                               c * (128 / EB), 16 * b, z);
+        sm100::mbar_arrive_expect_tx(&kv_bar[1], bytes);
+        for (int c = 0; c < ROWB / 128; ++c)
+          for (int b = 0; b < nbox; ++b)
+            sm100::tma_load_3d(dsm + TILE + c * kBk * 128 + b * 16 * 128, &tm_v16, &kv_bar[1],
+                               c * (128 / EB), 16 * b, z);
+      }
     }
   } else {
 #pragma unroll 4
@@ -922,7 +941,7 @@ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // 128 bytes, 128-byte swizzle. The page count is not passed in; 2^25 blocks
 // bound any pool that fits in device memory (a block is at least 8 KB), and a
 // block past the bound would read as zeros instead of faulting.
-bool make_map_dec_pages(CUtensorMap* m, const void* base, int D, bool fp8) {
+bool make_map_dec_pages(CUtensorMap* m, const void* base, int D, bool fp8, int box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
     void* p = nullptr;
@@ -935,7 +954,7 @@ bool make_map_dec_pages(CUtensorMap* m, const void* base, int D, bool fp8) {
   const int eb = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)kBk, (cuuint64_t)1 << 25};
   cuuint64_t strides[2] = {(cuuint64_t)D * eb, (cuuint64_t)kBk * D * eb};
-  cuuint32_t box[3] = {(cuuint32_t)(128 / eb), (cuuint32_t)kBk, 1};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / eb), (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1022,15 +1041,19 @@ cudaError_t launch_decode_attn(const void* q, const void* k_pages, const void* v
 #define MSA_DEC(DD, F8)                                                                    \
   do {                                                                                     \
     constexpr int sm = dec_smem_bytes<DD, F8>();                                           \
-    CUtensorMap tk{}, tv{};                                                                \
+    CUtensorMap tk{}, tv{}, tk16{}, tv16{};                                                \
     if (dec_tma<DD, F8>() &&                                                               \
-        (!make_map_dec_pages(&tk, k_pages, DD, F8) || !make_map_dec_pages(&tv, v_pages, DD, F8))) \
+        (!make_map_dec_pages(&tk, k_pages, DD, F8, kBk) ||                                 \
+         !make_map_dec_pages(&tv, v_pages, DD, F8, kBk) ||                                 \
+         !make_map_dec_pages(&tk16, k_pages, DD, F8, 16) ||                                \
+         !make_map_dec_pages(&tv16, v_pages, DD, F8, 16)))                                 \
       return cudaErrorInvalidValue;                                                        \
     e = cudaFuncSetAttribute(decode_attn_kernel<DD, F8>,                                   \
                              cudaFuncAttributeMaxDynamicSharedMemorySize, sm);             \
     if (e != cudaSuccess) return e;                                                        \
     decode_attn_kernel<DD, F8><<<tasks, 128, sm, st>>>(                                    \
-        tk, tv, (const uint16_t*)q, k_pages, v_pages, k_scale, v_scale, page_table, seq_lens, \
+        tk, tv, tk16, tv16, (const uint16_t*)q, k_pages, v_pages, k_scale, v_scale, page_table, \
+        seq_lens,                                                                          \
         ids, max_pages, H_q, H_kv, k, sl2, part_o, part_lse, dg);                          \
   } while (0)
   if (d == 128) {
