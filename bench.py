@@ -602,6 +602,35 @@ def time_index_project(msa, w, steps, warmup, d_model=4096):
     return a.elapsed_time(b) / steps, 2.0 * w.N * d_model * (w.n_g + 1) * w.d_idx
 
 
+def time_index_nvfp4(msa, w, steps, warmup):
+    """Index branch of the workload on NVFP4 q_idx / k_idx (quantised by torch
+    before the timing): the exact decode to bf16 and the bf16 index kernel, both
+    inside the timed region."""
+    import torch
+    import synth
+    qidx = synth.device_tensor(w, synth.T_QIDX)
+    kidx = synth.device_tensor(w, synth.T_KIDX)[:, 0].contiguous()
+    qc, qs = nvfp4_quantise(qidx)
+    kc, ks = nvfp4_quantise(kidx)
+    del qidx, kidx
+    torch.cuda.empty_cache()
+    ids = torch.empty((w.N, w.n_g, w.k), dtype=torch.int32, device="cuda")
+    ws = torch.empty(msa.msa_index_select_nvfp4_workspace_bytes(w.N, w.n_g, w.d_idx),
+                     dtype=torch.uint8, device="cuda")
+    for _ in range(warmup):
+        msa.msa_index_select_nvfp4(qc, qs, kc, ks, w.Bk, w.k, block_ids=ids, workspace=ws)
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        msa.msa_index_select_nvfp4(qc, qs, kc, ks, w.Bk, w.k, block_ids=ids, workspace=ws)
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    return statistics.mean(ms)
+
+
 def time_prefill_fp8_index(msa, w, steps, warmup):
     """Prefill step with the index branch on FP8-E4M3 codes of q_idx / k_idx
     (rounded to nearest by torch before the timing) and the bf16 main branch."""
@@ -721,7 +750,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=15.0)
-    ap.add_argument("--only", choices=["decode", "topk", "index", "attn", "proj"], default=None,
+    ap.add_argument("--only", choices=["decode", "topk", "index", "index_nvfp4", "attn", "proj"],
+                    default=None,
                     help="time only this path and print its numbers (for profiling runs)")
     ap.add_argument("--batch", type=int, default=None,
                     help="with --only decode: number of sequences (default: the workload's 64)")
@@ -766,6 +796,12 @@ def main():
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / args.steps
         print(json.dumps({"only": "index", "workload": w.name, "ms": ms,
+                          "tflops": index_flops(w.N, w.n_g, w.d_idx) / (ms * 1e-3) / 1e12}))
+        return
+    if args.only == "index_nvfp4":
+        w = synth.make(args.workload)
+        ms = time_index_nvfp4(msa, w, args.steps, args.warmup)
+        print(json.dumps({"only": "index_nvfp4", "workload": w.name, "ms": ms,
                           "tflops": index_flops(w.N, w.n_g, w.d_idx) / (ms * 1e-3) / 1e12}))
         return
     if args.only == "attn":
@@ -866,6 +902,15 @@ def main():
             "index_tflops": round(fl_idx / (f_idx * 1e-3) / 1e12, 2),
             "index_frac_of_fp8_peak": round(fl_idx / (f_idx * 1e-3) / 1e12 / peak_f8, 4),
             "fp8_peak": peak_f8, "fp8_peak_source": "measured bf16 burst x 2 (nominal ratio)"}
+        n4_ms = time_index_nvfp4(msa, w, args.steps, 3)
+        torch.cuda.empty_cache()
+        peak_f4 = peak_t * 4.0  # measured bf16 burst x the nominal fp4 / bf16 ratio
+        extra["prefill_128k_nvfp4_index"] = {
+            "index_ms": round(n4_ms, 3),
+            "index_tflops": round(fl_idx / (n4_ms * 1e-3) / 1e12, 2),
+            "index_frac_of_fp4_peak": round(fl_idx / (n4_ms * 1e-3) / 1e12 / peak_f4, 4),
+            "fp4_peak": peak_f4, "fp4_peak_source": "measured bf16 burst x 4 (nominal ratio)",
+            "path": "exact decode to bf16, then bf16 MMAs"}
         pj_ms, pj_fl = time_index_project(msa, w, args.steps, 3)
         torch.cuda.empty_cache()
         extra["index_projection_128k"] = {

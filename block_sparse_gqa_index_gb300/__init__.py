@@ -63,6 +63,9 @@ _index_dec_noalloc = _sig("msa_index_select_decode_noalloc", [_P, _P, _P, _P, _I
 _noalloc_max = _sig("msa_index_select_decode_noalloc_max_scores", [], _I64)
 _index_project = _sig("msa_index_project", [_P, _P, _P, _I64, _I, _I, _I, _P, _P, _P])
 _index_fp8 = _sig("msa_index_select_fp8", [_P, _P, _I64, _I, _I, _I, _I, _P, _P, _F, _P])
+_ws_index_fp4 = _sig("msa_index_select_nvfp4_workspace_bytes", [_I64, _I, _I], _SZ)
+_index_fp4 = _sig("msa_index_select_nvfp4", [_P, _P, _P, _P, _I64, _I, _I, _I, _I, _P, _P, _P,
+                                             _SZ, _P])
 _index_varlen = _sig("msa_index_select_varlen", [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P])
 _ws_attn_varlen = _sig("msa_sparse_attn_varlen_workspace_bytes", [_P, _I, _I, _I, _I, _I, _I],
                        _SZ)
@@ -94,7 +97,8 @@ EXPORTS = ["msa_status_string", "msa_version", "msa_index_select_workspace_bytes
            "msa_sparse_attn_paged_workspace_bytes", "msa_sparse_attn_paged",
            "msa_index_select_decode_fp8", "msa_kl_teacher_workspace_bytes",
            "msa_kl_teacher", "msa_index_select_decode_nvfp4", "msa_index_project",
-           "msa_decode_nvfp4"]
+           "msa_decode_nvfp4", "msa_index_select_nvfp4_workspace_bytes",
+           "msa_index_select_nvfp4"]
 
 
 class MSAError(RuntimeError):
@@ -204,6 +208,47 @@ def msa_index_select_fp8(q_idx: torch.Tensor, k_idx: torch.Tensor, Bk: int = 128
     _check(_index_fp8(q_idx.data_ptr(), k_idx.data_ptr(), N, n_g, d_idx, Bk, k,
                       block_ids.data_ptr(), _ptr(block_scores), score_scale, _stream(q_idx)),
            "msa_index_select_fp8")
+    return block_ids
+
+
+def msa_index_select_nvfp4_workspace_bytes(N: int, n_groups: int, d_idx: int) -> int:
+    return _ws_index_fp4(N, n_groups, d_idx)
+
+
+def msa_index_select_nvfp4(q_codes: torch.Tensor, q_scales: torch.Tensor,
+                           k_codes: torch.Tensor, k_scales: torch.Tensor, Bk: int = 128,
+                           k: int = 16, block_ids: Optional[torch.Tensor] = None,
+                           block_scores: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Index branch on NVFP4 operands: q_codes [N, n_groups, d_idx / 2] and
+    k_codes [N, d_idx / 2] uint8 (two E2M1 codes per byte, even dimension low),
+    q_scales [N, n_groups, d_idx / 16] and k_scales [N, d_idx / 16] E4M3 scales
+    (float8_e4m3fn or uint8) -> block_ids [N, n_groups, k]."""
+    N, n_g, half = q_codes.shape
+    d_idx = 2 * half
+    for t, name, shape in ((q_codes, "q_codes", (N, n_g, half)),
+                           (q_scales, "q_scales", (N, n_g, d_idx // 16)),
+                           (k_codes, "k_codes", (N, half)),
+                           (k_scales, "k_scales", (N, d_idx // 16))):
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise TypeError(f"{name} must be uint8 (or float8_e4m3fn for the scales)")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {list(shape)}")
+    if block_ids is None:
+        block_ids = torch.empty((N, n_g, k), dtype=torch.int32, device=q_codes.device)
+    _req(block_ids, "block_ids", torch.int32, (N, n_g, k))
+    if block_scores is not None:
+        _req(block_scores, "block_scores", torch.float32, (N, n_g, (N + Bk - 1) // Bk))
+    need = _ws_index_fp4(N, n_g, d_idx)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_codes.device)
+    _check(_index_fp4(q_codes.data_ptr(), q_scales.data_ptr(), k_codes.data_ptr(),
+                      k_scales.data_ptr(), N, n_g, d_idx, Bk, k, block_ids.data_ptr(),
+                      _ptr(block_scores), workspace.data_ptr(),
+                      workspace.numel() * workspace.element_size(), _stream(q_codes)),
+           "msa_index_select_nvfp4")
     return block_ids
 
 

@@ -133,6 +133,33 @@ int msa_index_select_fp8(const void* q_idx, const void* k_idx, int64_t N, int n_
                                             true, score_scale));
 }
 
+size_t msa_index_select_nvfp4_workspace_bytes(int64_t N, int n_groups, int d_idx) {
+  if (N < 1 || n_groups < 1 || d_idx < 1) return 0;
+  const size_t q = (size_t)N * n_groups * d_idx * 2, kb = (size_t)N * d_idx * 2;
+  return ((q + 255) & ~(size_t)255) + ((kb + 255) & ~(size_t)255);
+}
+
+int msa_index_select_nvfp4(const void* q_codes, const void* q_scales, const void* k_codes,
+                           const void* k_scales, int64_t N, int n_groups, int d_idx, int Bk,
+                           int k, int32_t* block_ids, float* block_scores, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (N < 0 || n_groups < 1 || d_idx < 1 || Bk < 1 || k < 1) return MSA_ERR_INVALID_ARG;
+  if (N == 0) return MSA_OK;
+  if (!q_codes || !q_scales || !k_codes || !k_scales || !block_ids || !workspace)
+    return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q_codes) || !aligned16(k_codes) || !aligned16(block_ids) ||
+      !aligned16(workspace) || (block_scores && !aligned16(block_scores)))
+    return MSA_ERR_INVALID_ARG;
+  if (Bk != 128 || !supported_k(k) || !supported_d(d_idx)) return MSA_ERR_UNSUPPORTED;
+  if (N * n_groups >= (1ll << 31)) return MSA_ERR_UNSUPPORTED;
+  if (workspace_bytes < msa_index_select_nvfp4_workspace_bytes(N, n_groups, d_idx))
+    return MSA_ERR_WORKSPACE;
+  int64_t nb = ceil_div(N, Bk);
+  return status_of(msa::launch_index_select_nvfp4(q_codes, q_scales, k_codes, k_scales, N,
+                                                  n_groups, d_idx, k, block_ids, block_scores,
+                                                  nb, workspace, diag(), (cudaStream_t)stream));
+}
+
 int msa_topk_blocks(const float* block_scores, int64_t N, int n_groups, int64_t nb, int Bk,
                     int k, int64_t q_offset, const int32_t* seq_lens, int32_t* block_ids,
                     void* stream) {

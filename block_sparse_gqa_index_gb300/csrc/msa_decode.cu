@@ -212,13 +212,6 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
 // the scales never touch the operands. Within a micro-block the four lanes of
 // a row take 4 contiguous dimensions each (one 16-bit read), and q_idx is
 // permuted the same way.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t r;
-  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}\n"
-      : "=r"(r)
-      : "r"(byte));
-  return r;
-}
 __device__ __forceinline__ void mma_f16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
                                               uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(

@@ -38,6 +38,8 @@
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "msa_kernels.h"
 #include "msa_sm100.cuh"
@@ -509,6 +511,58 @@ cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int64_t N,
                                  block_scores, nb, 1.f, dg, st);
   return launch_tc<64, false>(q_idx, k_idx, N, N, tb, nullptr, n_g, k, block_ids, block_scores,
                               nb, 1.f, dg, st);
+}
+
+namespace {
+// NVFP4 rows -> bf16 rows, one 16-value micro-block (8 code bytes, one E4M3
+// scale) per thread and iteration. A value is an E2M1 value (at most two
+// significant bits, |x| <= 6) times an E4M3 scale (at most four, 2^-9 .. 448):
+// at most six significant bits within bf16's range, so the product in fp32 and
+// its bf16 rounding are exact.
+__global__ void nvfp4_to_bf16_kernel(const uint2* __restrict__ codes,
+                                     const uint8_t* __restrict__ scales, int64_t n_mb,
+                                     uint4* __restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_mb;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint2 c = codes[i];
+    const __half_raw hs = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)scales[i], __NV_E4M3);
+    const float sc = __half2float(__half(hs));
+    uint32_t w[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const uint32_t h2 = e2m1x2_to_f16x2(((b < 4 ? c.x : c.y) >> (8 * (b & 3))) & 0xFF);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      w[b] = pack_bf16x2(f.x * sc, f.y * sc);
+    }
+    out[2 * i] = make_uint4(w[0], w[1], w[2], w[3]);
+    out[2 * i + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+cudaError_t nvfp4_to_bf16(const void* codes, const void* scales, int64_t rows, int d, void* out,
+                          cudaStream_t st) {
+  const int64_t n_mb = rows * (d / 16);
+  if (n_mb == 0) return cudaSuccess;
+  const int64_t g = std::min<int64_t>((n_mb + 255) / 256, (int64_t)num_sms() * 16);
+  nvfp4_to_bf16_kernel<<<(unsigned)g, 256, 0, st>>>((const uint2*)codes, (const uint8_t*)scales,
+                                                   n_mb, (uint4*)out);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_index_select_nvfp4(const void* q_codes, const void* q_scales,
+                                      const void* k_codes, const void* k_scales, int64_t N,
+                                      int n_g, int d_idx, int k, int32_t* block_ids,
+                                      float* block_scores, int64_t nb, void* ws, const Diag& dg,
+                                      cudaStream_t st) {
+  if (N * n_g == 0) return cudaSuccess;
+  unsigned char* qb = (unsigned char*)ws;
+  unsigned char* kb = qb + (((size_t)N * n_g * d_idx * 2 + 255) & ~(size_t)255);
+  note_launches(2);
+  cudaError_t e = nvfp4_to_bf16(q_codes, q_scales, N * n_g, d_idx, qb, st);
+  if (e == cudaSuccess) e = nvfp4_to_bf16(k_codes, k_scales, N, d_idx, kb, st);
+  if (e != cudaSuccess) return e;
+  return launch_index_select(qb, kb, N, n_g, d_idx, k, block_ids, block_scores, nb, dg, st);
 }
 
 cudaError_t launch_index_select_varlen(const void* q_idx, const void* k_idx,

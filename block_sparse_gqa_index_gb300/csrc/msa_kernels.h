@@ -24,6 +24,17 @@ cudaError_t launch_index_select(const void* q_idx, const void* k_idx, int64_t N,
                                 int64_t nb, const Diag& dg, cudaStream_t st, bool e4m3 = false,
                                 float score_scale = 1.f);
 
+// NVFP4 index operands (msa_index.cu): q_idx [N, n_g, d_idx] and k_idx
+// [N, d_idx] as E2M1 codes (two per byte, the even dimension in the low
+// nibble) with one E4M3 scale per 16 dimensions of a row, decoded exactly into
+// bf16 rows in ws (q_idx first, its bytes rounded up to 256, then k_idx), then
+// ranked by the bf16 kernel.
+cudaError_t launch_index_select_nvfp4(const void* q_codes, const void* q_scales,
+                                      const void* k_codes, const void* k_scales, int64_t N,
+                                      int n_g, int d_idx, int k, int32_t* block_ids,
+                                      float* block_scores, int64_t nb, void* ws, const Diag& dg,
+                                      cudaStream_t st);
+
 // One launch per 128 sequences of a packed batch; cu_seqlens is a host
 // array [B + 1] of token offsets (msa_index.cu).
 cudaError_t launch_index_select_varlen(const void* q_idx, const void* k_idx,

@@ -114,6 +114,27 @@ int msa_index_select_fp8(const void* q_idx, const void* k_idx, int64_t N, int n_
                          int d_idx, int Bk, int k, int32_t* block_ids, float* block_scores,
                          float score_scale, void* stream);
 
+/* Index branch with NVFP4 index operands (the kernel release lists NVFP4
+ * among its precisions: "MiniMax lança MSA ...", section "Kernel open source e
+ * MiniMax-M3"; "MiniMax Sparse Attention (MSA) ...", section "内核协同设计"):
+ *   q_codes  [N, n_groups, d_idx / 2] uint8   E2M1 codes, two per byte, the
+ *                                             even dimension in the low nibble
+ *   q_scales [N, n_groups, d_idx / 16] uint8  E4M3 scale of each 16 dimensions
+ *   k_codes  [N, d_idx / 2] uint8, k_scales [N, d_idx / 16] uint8, the same
+ * A value is its E2M1 code's value times its 16 dimensions' scale. Such a
+ * product has at most six significant bits and lies within bf16's range, so
+ * the operands are decoded exactly into bf16 rows in the workspace (device,
+ * caller-owned, msa_index_select_nvfp4_workspace_bytes() bytes, 16-byte
+ * aligned; MSA_ERR_WORKSPACE when smaller) and ranked by the bf16 index
+ * kernel: the result equals msa_index_select on the decoded values. The
+ * tensor cores run bf16, not block-scaled FP4, MMAs. Selection rules,
+ * block_scores, alignment and other errors as msa_index_select. */
+size_t msa_index_select_nvfp4_workspace_bytes(int64_t N, int n_groups, int d_idx);
+int msa_index_select_nvfp4(const void* q_codes, const void* q_scales, const void* k_codes,
+                           const void* k_scales, int64_t N, int n_groups, int d_idx, int Bk,
+                           int k, int32_t* block_ids, float* block_scores, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
 /* Exp-free top-k over given block scores ("内核协同设计": ranking raw scores
  * selects the same blocks as ranking their softmax).
  *   block_scores [n_rows / n_groups... ] laid out [N, n_groups, nb] fp32; row

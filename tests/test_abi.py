@@ -154,6 +154,33 @@ def test_decode_nvfp4_rejects(msa):
     assert f(*a) == 0                              # no sequences: nothing to do
 
 
+def test_index_nvfp4_rejects(msa):
+    f = msa._index_fp4
+    ws = msa.msa_index_select_nvfp4_workspace_bytes(4096, 8, 128)
+    # the decoded q_idx and k_idx rows (bf16), each area rounded up to 256 bytes
+    assert ws == 4096 * 8 * 128 * 2 + 4096 * 128 * 2
+    assert msa.msa_index_select_nvfp4_workspace_bytes(3, 1, 64) == 512 + 512
+    # q_codes, q_scales, k_codes, k_scales, N, n_g, d_idx, Bk, k, ids, scores, ws, ws_bytes,
+    # stream
+    base = [FAKE, FAKE, FAKE, FAKE, 4096, 8, 128, 128, 16, FAKE, None, FAKE, ws, None]
+    a = list(base); a[3] = None
+    assert f(*a) == -1                             # no k_idx scales
+    a = list(base); a[2] = FAKE + 8
+    assert f(*a) == -1                             # misaligned k_idx codes
+    a = list(base); a[11] = None
+    assert f(*a) == -1                             # no workspace
+    a = list(base); a[6] = 96
+    assert f(*a) == -2                             # d_idx not 64 or 128
+    a = list(base); a[7] = 64
+    assert f(*a) == -2                             # Bk != 128
+    a = list(base); a[8] = 17
+    assert f(*a) == -2                             # k > 16
+    a = list(base); a[12] = ws - 1
+    assert f(*a) == -3                             # workspace one byte short
+    a = list(base); a[4] = 0
+    assert f(*a) == 0                              # no queries: nothing to do
+
+
 def test_wait_limit_roundtrip(msa):
     old = msa.msa_set_wait_limit(123)
     assert msa.msa_set_wait_limit(old) == 123

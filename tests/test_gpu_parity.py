@@ -703,6 +703,49 @@ def _nvfp4_pages(x_bits, rng, shape):
     return packed, sc_codes.astype(np.uint8), bits
 
 
+@pytest.mark.parametrize("N,n_g,d_idx", [(1000, 2, 64), (1537, 8, 128), (129, 1, 128)])
+def test_index_select_nvfp4(msa, N, n_g, d_idx):
+    """NVFP4 index operands (E2M1 codes, one E4M3 scale per 16 dimensions):
+    against the oracle on the decoded values (exactly bf16). The codes are drawn
+    uniformly and the scales from a few powers of two and 1.5 times one, so
+    every score is a multiple of 2^-6 below 2^15, exact in fp32: ids and
+    visible block scores must match bit for bit."""
+    rng = np.random.default_rng(N * 10 + n_g)
+    qc, qs, qbits = _nvfp4_pages(None, rng, (N, n_g, d_idx))
+    kc, ks, kbits = _nvfp4_pages(None, rng, (N, d_idx))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    nb = (N + 127) // 128
+    scores = torch.full((N, n_g, nb), float("nan"), device="cuda")
+    ids = msa.msa_index_select_nvfp4(dev(qc), dev(qs), dev(kc), dev(ks), 128, 16,
+                                     block_scores=scores)
+    torch.cuda.synchronize()
+    assert msa.msa_get_error() == 0
+    rows = np.arange(N)
+    want, want_s = oracle.index_select(qbits, rows, kbits, 128, 16, nb_out=nb, want_scores=True)
+    assert np.array_equal(ids.cpu().numpy(), want)
+    sc = scores.cpu().numpy().astype(np.float64)
+    vis = np.broadcast_to(np.arange(nb)[None, None, :] <= (rows // 128)[:, None, None], sc.shape)
+    assert np.array_equal(sc[vis], want_s[vis])
+
+
+def test_index_select_nvfp4_gaussian_equals_bf16_path(msa):
+    """The 32K workload's Gaussian q_idx / k_idx quantised to NVFP4: the NVFP4
+    entry gives exactly what the bf16 entry gives on the decoded values (the
+    decode is exact, then the same kernel ranks the same numbers)."""
+    w = synth.make("32k", L=4096)
+    qx = synth.host_tensor(w, synth.T_QIDX)[0]
+    kx = synth.host_tensor(w, synth.T_KIDX)[0, :, 0]
+    rng = np.random.default_rng(7)
+    qc, qs, qbits = _nvfp4_pages(qx, rng, qx.shape)
+    kc, ks, kbits = _nvfp4_pages(kx, rng, kx.shape)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    ids = msa.msa_index_select_nvfp4(dev(qc), dev(qs), dev(kc), dev(ks), 128, 16)
+    ref = msa.msa_index_select(dev(qbits).view(torch.bfloat16), dev(kbits).view(torch.bfloat16),
+                               128, 16)
+    assert torch.equal(ids, ref)
+    assert msa.msa_get_error() == 0
+
+
 @pytest.mark.parametrize("gaussian,d,H_q,H_kv", [(False, 128, 8, 2), (False, 64, 16, 4),
                                                  (True, 128, 32, 8)])
 def test_decode_nvfp4_kv(msa, gaussian, d, H_q, H_kv):
