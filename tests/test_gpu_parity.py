@@ -703,16 +703,22 @@ def _nvfp4_pages(x_bits, rng, shape):
     return packed, sc_codes.astype(np.uint8), bits
 
 
-@pytest.mark.parametrize("N,n_g,d_idx", [(1000, 2, 64), (1537, 8, 128), (129, 1, 128)])
-def test_index_select_nvfp4(msa, N, n_g, d_idx):
+@pytest.mark.parametrize("N,n_g,d_idx,zero_k", [(1000, 2, 64, False), (1537, 8, 128, False),
+                                                (129, 1, 128, False), (5, 2, 64, False),
+                                                (700, 2, 128, True)])
+def test_index_select_nvfp4(msa, N, n_g, d_idx, zero_k):
     """NVFP4 index operands (E2M1 codes, one E4M3 scale per 16 dimensions):
     against the oracle on the decoded values (exactly bf16). The codes are drawn
     uniformly and the scales from a few powers of two and 1.5 times one, so
     every score is a multiple of 2^-6 below 2^15, exact in fp32: ids and
-    visible block scores must match bit for bit."""
+    visible block scores must match bit for bit. zero_k: every k_idx scale is
+    the E4M3 zero, so every score is 0 and the lowest ids win the ties."""
     rng = np.random.default_rng(N * 10 + n_g)
     qc, qs, qbits = _nvfp4_pages(None, rng, (N, n_g, d_idx))
     kc, ks, kbits = _nvfp4_pages(None, rng, (N, d_idx))
+    if zero_k:
+        ks[:] = 0
+        kbits = np.zeros_like(kbits)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     nb = (N + 127) // 128
     scores = torch.full((N, n_g, nb), float("nan"), device="cuda")
