@@ -242,23 +242,22 @@ kl_tile_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
       unsigned char* qbuf = smem + L::kQOff + qs * L::kQBytes;
       unsigned char* xbuf = smem + L::kXOff + qs * L::kXBytes;
-      // one gather4 per (4 consecutive rows, 64-column chunk)
-      for (int job = lane; job < (kKlRows / 4) * NCH; job += 32) {
-        const int r0 = (job / NCH) * 4, c = job % NCH;
-        int32_t y[4];
+      // one tiled box per (query, 64-column chunk): a query's G head rows are
+      // consecutive in q and in the tile (query-major rows); every lane runs the
+      // same number of iterations (the shuffles need it)
+      constexpr int kQJobs = QT * NCH;
+      for (int jb = 0; jb < (kQJobs + 31) / 32; ++jb) {
+        const int job = lane + 32 * jb;
+        const int qi = (job / NCH) % QT, c = job % NCH;
+        int32_t tv = -1;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int r = r0 + u, qi = r / G;
-          int32_t tv = -1;
-#pragma unroll
-          for (int jj = 0; jj < NJ; ++jj) {
-            const int32_t x = __shfl_sync(0xffffffffu, tq[jj], qi & 31);
-            if (jj == (qi >> 5)) tv = x;
-          }
-          y[u] = tv >= 0 ? (int32_t)((int64_t)tv * H_q + g * G + r % G) : oob_row;
+        for (int jj = 0; jj < NJ; ++jj) {
+          const int32_t x = __shfl_sync(0xffffffffu, tq[jj], qi & 31);
+          if (jj == (qi >> 5)) tv = x;
         }
-        tma_gather4(qbuf + c * kKlRows * 128 + r0 * 128, &tm_q, &q_full[qs], c * 64, y[0], y[1],
-                    y[2], y[3]);
+        const int32_t y = tv >= 0 ? (int32_t)((int64_t)tv * H_q + g * G) : oob_row;
+        if (job < kQJobs)
+          tma_load_2d(qbuf + c * kKlRows * 128 + qi * G * 128, &tm_q, &q_full[qs], c * 64, y);
       }
       // q_idx rows, G copies each, into the swizzled operand layout
 #pragma unroll
@@ -496,7 +495,7 @@ cudaError_t launch_kl_tiles(const void* q, const void* kk, const void* q_idx, co
   const cuuint32_t ib[2] = {64, (cuuint32_t)kKlKeys};
   const cuuint64_t qd[2] = {(cuuint64_t)D, (cuuint64_t)(N * H_q)};
   const cuuint64_t qs[1] = {(cuuint64_t)D * 2};
-  const cuuint32_t qb[2] = {64, 1};
+  const cuuint32_t qb[2] = {64, (cuuint32_t)G};  // a query's G head rows
   if (!kl_map(&tk, kk, 3, kd, ks, kb) || !kl_map(&ti, k_idx, 2, id, is, ib) ||
       !kl_map(&tq, q, 2, qd, qs, qb))
     return cudaErrorInvalidValue;
