@@ -752,6 +752,43 @@ def test_index_select_nvfp4_gaussian_equals_bf16_path(msa):
     assert msa.msa_get_error() == 0
 
 
+def _nvfp4_torch(x):
+    """NVFP4 quantisation by torch on the device (no library code): per 16
+    values one E4M3 scale (amax / 6, at least 2^-9) and the nearest E2M1 code
+    of each value over it; returns (codes two per byte, even dimension low;
+    scale codes; the decoded values as bf16, exact)."""
+    e2m1 = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], device=x.device)
+    xb = x.float().reshape(*x.shape[:-1], x.shape[-1] // 16, 16)
+    sc = (xb.abs().amax(dim=-1).clamp(min=2.0 ** -9) / 6.0).to(torch.float8_e4m3fn)
+    scf = sc.float().unsqueeze(-1)
+    y = xb / scf
+    mag = (y.abs().unsqueeze(-1) - e2m1).abs().argmin(dim=-1)
+    codes = (mag | ((y < 0).to(torch.int64) << 3)).to(torch.uint8).reshape(x.shape)
+    dec = (e2m1[mag] * torch.where(y < 0, -1.0, 1.0) * scf).reshape(x.shape)
+    dec16 = dec.to(torch.bfloat16)
+    assert torch.equal(dec16.float(), dec)  # exact in bf16
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).contiguous()
+    return packed, sc.view(torch.uint8).contiguous(), dec16
+
+
+def test_index_select_nvfp4_full_128k(msa):
+    """The 128K workload (the benchmarked configuration) with q_idx / k_idx
+    quantised to NVFP4: the NVFP4 entry gives exactly the ids of the bf16 entry
+    on the decoded values."""
+    w = synth.make("128k")
+    qidx = synth.device_tensor(w, synth.T_QIDX)
+    kidx = synth.device_tensor(w, synth.T_KIDX)[:, 0].contiguous()
+    qc, qs, qd = _nvfp4_torch(qidx)
+    del qidx
+    kc, ks, kd = _nvfp4_torch(kidx)
+    del kidx
+    torch.cuda.empty_cache()
+    ids = msa.msa_index_select_nvfp4(qc, qs, kc, ks, 128, 16)
+    ref = msa.msa_index_select(qd, kd, 128, 16)
+    assert torch.equal(ids, ref)
+    assert msa.msa_get_error() == 0
+
+
 @pytest.mark.parametrize("gaussian,d,H_q,H_kv", [(False, 128, 8, 2), (False, 64, 16, 4),
                                                  (True, 128, 32, 8)])
 def test_decode_nvfp4_kv(msa, gaussian, d, H_q, H_kv):
