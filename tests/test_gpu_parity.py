@@ -1028,6 +1028,34 @@ def test_kl_teacher_matches_oracle(msa, N, H_q, H_kv, d):
     assert err.max() < 1e-4, (err.max(), np.unravel_index(err.argmax(), err.shape))
 
 
+def test_kl_teacher_full_128k_sampled(msa):
+    """The KL signal over the whole 128K workload (the benchmarked
+    configuration), on the GPU's own ids and LSE, against the oracle's fp64 KL
+    on sampled rows: the first blocks, two random blocks' rows, the tail and
+    random rows."""
+    w = synth.make("128k")
+    qi = synth.device_tensor(w, synth.T_QIDX)
+    ki = kidx2d(synth.device_tensor(w, synth.T_KIDX))
+    ids = msa.msa_index_select(qi, ki, w.Bk, w.k)
+    q = synth.device_tensor(w, synth.T_Q)
+    kk = synth.device_tensor(w, synth.T_K)
+    v = synth.device_tensor(w, synth.T_V)
+    _, lse = msa.msa_sparse_attn(q, kk, v, ids, w.Bk, w.scale)
+    del v
+    kl = msa.msa_kl_teacher(q, kk, qi, ki, ids, lse, w.Bk, w.scale)
+    torch.cuda.synchronize()
+    assert msa.msa_get_error() == 0
+    rows = _sample_rows(w.N, w.Bk, 150, seed=11, n_tail=64)
+    want, mag = oracle.kl_teacher(synth.host_rows(w, synth.T_Q, 0, rows),
+                                  synth.host_rows(w, synth.T_QIDX, 0, rows), rows,
+                                  synth.host_tensor(w, synth.T_K)[0],
+                                  synth.host_tensor(w, synth.T_KIDX)[0, :, 0],
+                                  ids.cpu().numpy()[rows], w.Bk, w.scale)
+    got = kl.cpu().numpy()[rows].astype(np.float64)
+    err = np.abs(got - want) / (1.0 + mag)
+    assert err.max() < 1e-4, (err.max(), np.unravel_index(err.argmax(), err.shape))
+
+
 def test_kl_teacher_zero_when_student_equals_teacher(msa):
     """One group of one head with q_idx = q / 8 and k_idx = k (scale 1/8): the
     index softmax equals the main branch's distribution, so the KL vanishes up
