@@ -71,6 +71,33 @@ def test_projection_gauss_model_width(msa):
         assert (err <= bound).all(), float((err - bound).max())
 
 
+def test_projection_full_128k_sampled(msa):
+    """The benchmarked configuration (131072 rows, d_model = 4096, eight groups of
+    d_idx = 128), Gaussian as above, in one launch: sampled rows (the first and
+    last, every tile's first row, random rows) against the oracle, within one
+    bf16 rounding plus the fp32 accumulation error."""
+    N, d_model, n_g, d_idx = 131072, 4096, 8, 128
+    g = torch.Generator(device="cuda").manual_seed(6)
+    x = torch.randn((N, d_model), generator=g, device="cuda").to(torch.bfloat16)
+    wq = (torch.randn((n_g * d_idx, d_model), generator=g, device="cuda") /
+          d_model ** 0.5).to(torch.bfloat16)
+    wk = (torch.randn((d_idx, d_model), generator=g, device="cuda") /
+          d_model ** 0.5).to(torch.bfloat16)
+    q, k = msa.msa_index_project(x, wq, wk)
+    torch.cuda.synchronize()
+    assert msa.msa_get_error() == 0
+    rng = np.random.default_rng(6)
+    rows = np.unique(np.concatenate([[0, N - 1], np.arange(0, N, 128),
+                                     rng.integers(0, N, 256)]))
+    rt = torch.from_numpy(rows).cuda()
+    qo, ko = oracle.index_project(_bits(x[rt]), _bits(wq), _bits(wk))
+    for got, want in ((q[rt].float().cpu().numpy().astype(np.float64), qo),
+                      (k[rt].float().cpu().numpy().astype(np.float64), ko)):
+        err = np.abs(got - want)
+        bound = 2.0 ** -8 * np.abs(want) + 1e-4
+        assert (err <= bound).all(), float((err - bound).max())
+
+
 def test_projection_feeds_index_branch(msa):
     """x -> projections -> index branch on the GPU selects the oracle's blocks for
     the oracle's projections of the same x (integer data: exact scores)."""
