@@ -841,6 +841,75 @@ def test_decode_nvfp4_kv(msa, gaussian, d, H_q, H_kv):
           f"lse {e_l:.3e}")
 
 
+def test_decode_nvfp4_kv_full_config(msa):
+    """The decode workload at its full size (64 sequences of 131073 tokens, the
+    benchmarked configuration) over an NVFP4 K/V cache of random codes and
+    scales built on the device (in page chunks), on the GPU's own ids: against
+    the bf16 path over the decoded cache for every sequence, and against the
+    oracle on the decoded values of the selected pages for sampled sequences."""
+    w = synth.make("decode")
+    dev = torch.device("cuda")
+    ptn = synth.page_table(w)
+    pt = torch.from_numpy(ptn).to(dev)
+    sl = torch.full((w.B,), w.L, dtype=torch.int32, device=dev)
+    last = [(s, w.L - 1) for s in range(w.B)]
+    kidx_p = synth.device_paged(w, synth.T_KIDX, pt)[:, 0].contiguous()
+    ids = msa.msa_index_select_decode(synth.device_rows(w, synth.T_QIDX, last), kidx_p, pt, sl,
+                                      w.Bk, w.k)
+    del kidx_p
+    q = synth.device_rows(w, synth.T_Q, last)
+    P = w.B * w.nb
+    e2m1 = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], device=dev)
+    scl = torch.tensor([0x28, 0x30, 0x38, 0x3C, 0x40], dtype=torch.uint8, device=dev)
+    gen = torch.Generator(device="cuda").manual_seed(31)
+    cache = {}
+    for name in ("k", "v"):
+        codes = torch.empty((P, w.H_kv, w.Bk, w.d // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty((P, w.H_kv, w.Bk, w.d // 16), dtype=torch.uint8, device=dev)
+        dec = torch.empty((P, w.H_kv, w.Bk, w.d), dtype=torch.bfloat16, device=dev)
+        for p0 in range(0, P, 2048):
+            p1 = min(P, p0 + 2048)
+            c = torch.randint(0, 16, (p1 - p0, w.H_kv, w.Bk, w.d), generator=gen, device=dev)
+            sc = scl[torch.randint(0, 5, (p1 - p0, w.H_kv, w.Bk, w.d // 16), generator=gen,
+                                   device=dev)]
+            val = e2m1[c & 7] * (1.0 - 2.0 * (c >> 3).float()) * \
+                sc.view(torch.float8_e4m3fn).float().repeat_interleave(16, dim=-1)
+            cu = c.to(torch.uint8)
+            codes[p0:p1] = cu[..., 0::2] | (cu[..., 1::2] << 4)
+            scales[p0:p1] = sc
+            dec[p0:p1] = val.to(torch.bfloat16)
+            assert torch.equal(dec[p0:p1].float(), val)  # exact in bf16
+            del c, sc, val, cu
+        cache[name] = (codes, scales, dec)
+    (kc, ks, kd), (vc, vs, vd) = cache["k"], cache["v"]
+    o4, l4 = msa.msa_decode_nvfp4(q, kc, ks, vc, vs, pt, sl, ids, w.Bk, w.scale)
+    ob, lb = msa.msa_decode(q, kd, vd, pt, sl, ids, w.Bk, w.scale)
+    torch.cuda.synchronize()
+    assert msa.msa_get_error() == 0
+    check_close("o vs bf16 path", bf16_to_np(o4), bf16_to_np(ob), TOL_O, rtol=2.0 ** -7)
+    check_close("lse vs bf16 path", l4.cpu().numpy(), lb.cpu().numpy(), TOL_LSE)
+    # the oracle on sampled sequences: their selected pages, in logical order
+    got = ids.cpu().numpy()
+    seqs = np.array([0, 37, 63])
+    host = {}
+    for name, dec in (("k", kd), ("v", vd)):
+        arr = np.zeros((P, w.H_kv, w.Bk, w.d), dtype=np.uint16)  # untouched pages cost nothing
+        for sq in seqs:
+            for b in sorted(set(int(x) for x in got[sq].ravel() if x >= 0)):
+                arr[sq * w.nb + b] = dec[int(ptn[sq, b])].view(torch.int16).cpu().numpy() \
+                    .view(np.uint16)
+        host[name] = arr
+    qh = np.stack([synth.host_rows(w, synth.T_Q, int(sq), [w.L - 1])[0] for sq in seqs])
+    ident = synth.page_table(w, permute=False)
+    o_ref, l_ref = oracle.decode_attn(qh, host["k"], host["v"], ident[seqs],
+                                      np.full(len(seqs), w.L, dtype=np.int32), got[seqs], w.Bk,
+                                      w.scale)
+    e_o = check_close("o", bf16_to_np(o4[torch.from_numpy(seqs).cuda()]), o_ref, TOL_O,
+                      rtol=2.0 ** -8)
+    e_l = check_close("lse", l4[torch.from_numpy(seqs).cuda()].cpu().numpy(), l_ref, TOL_LSE)
+    print(f"[decode nvfp4 kv full config] max|err| o {e_o:.3e} lse {e_l:.3e}")
+
+
 def test_decode_matches_prefill_row_on_gpu(msa):
     """Decoding the last token against the cache equals the last prefill row."""
     w = synth.make("decode", B=1, L=128 * 9 + 5, H_q=8, H_kv=2, d=128, d_idx=128,
