@@ -589,6 +589,81 @@ def test_decode_index_fp8_gauss(msa, d_idx, H_kv):
     assert rel.max() < 1e-4
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "nvfp4"])
+def test_decode_index_lowp_full_config(msa, fmt):
+    """The decode workload at its full size (64 sequences of 131073 tokens) with a
+    k_idx cache of random E4M3 codes (and E4M3 q_idx) or random NVFP4 codes and
+    scales, built on the device: block scores against the bf16 path over the
+    decoded values (fp32 accumulation), and the selection of sampled sequences
+    against the oracle on the decoded values up to near-tie swaps."""
+    w = synth.make("decode")
+    dev = torch.device("cuda")
+    ptn = synth.page_table(w)
+    pt = torch.from_numpy(ptn).to(dev)
+    lens = np.full(w.B, w.L, dtype=np.int32)
+    sl = torch.from_numpy(lens).to(dev)
+    P, d = w.B * w.nb, w.d_idx
+    gen = torch.Generator(device="cuda").manual_seed(41 if fmt == "e4m3" else 43)
+    dec = torch.empty((P, w.Bk, d), dtype=torch.bfloat16, device=dev)
+    e2m1 = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], device=dev)
+    scl = torch.tensor([0x30, 0x38, 0x3C, 0x40, 0x48], dtype=torch.uint8, device=dev)
+
+    def e4m3_codes(shape):
+        c = torch.randint(0, 256, shape, generator=gen, device=dev).to(torch.uint8)
+        return torch.where((c & 0x7F) == 0x7F, c - 1, c)  # no NaN codes
+
+    if fmt == "e4m3":
+        k8 = torch.empty((P, w.Bk, d), dtype=torch.uint8, device=dev)
+        for p0 in range(0, P, 8192):
+            p1 = min(P, p0 + 8192)
+            k8[p0:p1] = e4m3_codes((p1 - p0, w.Bk, d))
+            dec[p0:p1] = k8[p0:p1].view(torch.float8_e4m3fn).to(torch.bfloat16)
+        q8 = e4m3_codes((w.B, w.n_g, d))
+        qidx = q8.view(torch.float8_e4m3fn).to(torch.bfloat16)
+        s_lp = torch.full((w.B, w.n_g, w.nb), float("nan"), device=dev)
+        ids = msa.msa_index_select_decode_fp8(q8, k8, pt, sl, w.Bk, w.k, block_scores=s_lp)
+    else:
+        codes = torch.empty((P, w.Bk, d // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty((P, w.Bk, d // 16), dtype=torch.uint8, device=dev)
+        for p0 in range(0, P, 8192):
+            p1 = min(P, p0 + 8192)
+            c = torch.randint(0, 16, (p1 - p0, w.Bk, d), generator=gen, device=dev)
+            sc = scl[torch.randint(0, 5, (p1 - p0, w.Bk, d // 16), generator=gen, device=dev)]
+            val = e2m1[c & 7] * (1.0 - 2.0 * (c >> 3).float()) * \
+                sc.view(torch.float8_e4m3fn).float().repeat_interleave(16, dim=-1)
+            cu = c.to(torch.uint8)
+            codes[p0:p1] = cu[..., 0::2] | (cu[..., 1::2] << 4)
+            scales[p0:p1] = sc
+            dec[p0:p1] = val.to(torch.bfloat16)
+            del c, sc, val, cu
+        qidx = synth.device_rows(w, synth.T_QIDX, [(s, w.L - 1) for s in range(w.B)])
+        s_lp = torch.full((w.B, w.n_g, w.nb), float("nan"), device=dev)
+        ids = msa.msa_index_select_decode_nvfp4(qidx, codes, scales, pt, sl, w.Bk, w.k,
+                                                block_scores=s_lp)
+    s16 = torch.full((w.B, w.n_g, w.nb), float("nan"), device=dev)
+    msa.msa_index_select_decode(qidx, dec, pt, sl, w.Bk, w.k, block_scores=s16)
+    torch.cuda.synchronize()
+    assert msa.msa_get_error() == 0
+    # every block is visible (L = 131073); fp32 accumulation in two orders, its
+    # error bounded by the row's largest score (terms of random codes cancel)
+    a, b = s_lp.double(), s16.double()
+    row_max = b.abs().amax(dim=-1, keepdim=True).clamp(min=1.0)
+    assert ((a - b).abs() <= 1e-5 * row_max).all(), float(((a - b).abs() / row_max).max())
+    seqs = np.array([0, 31, 63])
+    host = np.zeros((P, w.Bk, d), dtype=np.uint16)  # untouched pages cost nothing
+    phys = torch.from_numpy(ptn[seqs].reshape(-1).astype(np.int64)).cuda()
+    logical = (seqs[:, None] * w.nb + np.arange(w.nb)[None, :]).reshape(-1)
+    host[logical] = dec[phys].view(torch.int16).cpu().numpy().view(np.uint16)
+    qh = qidx[torch.from_numpy(seqs).cuda()].contiguous().view(torch.int16).cpu().numpy() \
+        .view(np.uint16)
+    ident = synth.page_table(w, permute=False)
+    want, want_s = oracle.decode_index_select(qh, host, ident[seqs], lens[seqs], w.Bk, w.k,
+                                              nb_out=w.nb, want_scores=True)
+    got = ids.cpu().numpy()[seqs]
+    swaps = compare_selection(got, want, want_s, lens[seqs] - 1, w.Bk)
+    _swap_bound(swaps, len(seqs), w.n_g)
+
+
 def _nvfp4_cache(w, rng, gaussian):
     """An NVFP4 k_idx cache for the decode workload w: E2M1 codes (two per
     byte, even dimension low) and one E4M3 scale per 16 dimensions of a key,
