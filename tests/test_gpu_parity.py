@@ -158,11 +158,13 @@ def test_index_fp8_exact_on_integer_inputs(msa, N, n_g):
                           want_s[np.broadcast_to(vis, want_s.shape)])
 
 
-def test_index_fp8_gauss_32k(msa):
-    """Gaussian 32K index inputs rounded to E4M3: the FP8 selection matches the
-    oracle on the decoded codes, up to near-tie swaps, and the block scores
-    (times score_scale) agree to fp32 accumulation."""
-    w = synth.make("32k")
+@pytest.mark.parametrize("wl,n_random,n_tail", [("32k", 256, 256), ("128k", 128, 64)])
+def test_index_fp8_gauss(msa, wl, n_random, n_tail):
+    """Gaussian 32K and 128K (the benchmarked configuration) index inputs
+    rounded to E4M3: on sampled rows the FP8 selection matches the oracle on the
+    decoded codes, up to near-tie swaps, and the block scores (times
+    score_scale) agree to fp32 accumulation."""
+    w = synth.make(wl)
     qh = synth.host_tensor(w, synth.T_QIDX)[0]
     kh = synth.host_tensor(w, synth.T_KIDX)[0, :, 0]
     q8, qb = _to_e4m3(qh)
@@ -171,7 +173,7 @@ def test_index_fp8_gauss_32k(msa):
     ids = msa.msa_index_select_fp8(q8.cuda(), k8.cuda(), w.Bk, w.k, block_scores=sc,
                                    score_scale=0.5)
     torch.cuda.synchronize()
-    rows = _sample_rows(w.N, w.Bk, 256, 11)
+    rows = _sample_rows(w.N, w.Bk, n_random, 11, n_tail=n_tail)
     want, want_s = oracle.index_select(qb[rows], rows, kb, w.Bk, w.k, nb_out=w.nb,
                                        want_scores=True)
     got = ids.cpu().numpy()[rows]
