@@ -649,7 +649,8 @@ decode_attn_fp4_kernel(const uint16_t* __restrict__ q, const uint8_t* __restrict
   constexpr int VROWB = D * 2;       // bf16 row of the widened V tile
   constexpr int MB = D / 16;         // micro-blocks of a row
   constexpr int NC = D / 8;          // 8-column tiles of P V
-  extern __shared__ __align__(128) unsigned char dsm[];
+  // (declared as in decode_attn_kernel, whose TMA boxes need 1024-byte alignment)
+  extern __shared__ __align__(1024) unsigned char dsm[];
   const uint32_t s_kc = smem_addr(dsm), s_vc = s_kc + CTILE;
   const uint32_t s_ks = s_vc + CTILE, s_vs = s_ks + STILE;
   const uint32_t s_vb = s_vs + STILE;  // widened V (f16, row-swizzled)
