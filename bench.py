@@ -36,7 +36,6 @@ this method) on the same workload, metric and unit.
 """
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess

@@ -8,7 +8,6 @@ end-to-end pipelines and decode cases those are the GPU's own ids, which the
 oracle takes as given. bf16 output max |err| <= 1e-2, fp32 LSE max |err| <=
 1e-3 (bf16 and FP8-E4M3 KV), FP8-KV output max |err| <= 5e-2.
 """
-import math
 
 import numpy as np
 import pytest
