@@ -749,7 +749,8 @@ def main():
     ap.add_argument("--no-extra", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=15.0)
-    ap.add_argument("--only", choices=["decode", "topk", "index", "index_nvfp4", "attn", "proj"],
+    ap.add_argument("--only", choices=["decode", "topk", "index", "index_nvfp4", "attn", "proj",
+                                       "kl"],
                     default=None,
                     help="time only this path and print its numbers (for profiling runs)")
     ap.add_argument("--batch", type=int, default=None,
@@ -796,6 +797,12 @@ def main():
         ms = a.elapsed_time(b) / args.steps
         print(json.dumps({"only": "index", "workload": w.name, "ms": ms,
                           "tflops": index_flops(w.N, w.n_g, w.d_idx) / (ms * 1e-3) / 1e12}))
+        return
+    if args.only == "kl":
+        w = synth.make(args.workload)
+        ms, fl = time_kl_teacher(msa, w, args.steps, args.warmup)
+        print(json.dumps({"only": "kl", "workload": w.name, "ms": ms,
+                          "tflops": fl / (ms * 1e-3) / 1e12}))
         return
     if args.only == "index_nvfp4":
         w = synth.make(args.workload)
