@@ -245,14 +245,25 @@ bucket_count_smem_kernel(const int32_t* __restrict__ ids, int64_t q0, int64_t q1
 }
 
 // per bucket: percta[c][b] <- offsets[b] + (entries of b in CTAs before c)
+// one warp per bucket: the CTAs' counts 32 at a time, an exclusive prefix sum
+// over the lanes, so each warp has 32 counts in flight instead of one
 __global__ void bucket_cta_base_kernel(const int32_t* __restrict__ offsets, int n_b, int ctas,
                                        int32_t* __restrict__ percta) {
-  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < n_b; b += gridDim.x * blockDim.x) {
+  const int lane = threadIdx.x & 31;
+  for (int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < n_b;
+       b += (gridDim.x * blockDim.x) >> 5) {
     int run = offsets[b];
-    for (int c = 0; c < ctas; ++c) {
-      const int x = percta[(size_t)c * n_b + b];
-      percta[(size_t)c * n_b + b] = run;
-      run += x;
+    for (int c0 = 0; c0 < ctas; c0 += 32) {
+      const int c = c0 + lane;
+      const int x = c < ctas ? percta[(size_t)c * n_b + b] : 0;
+      int incl = x;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      if (c < ctas) percta[(size_t)c * n_b + b] = run + incl - x;
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
 }
@@ -1693,8 +1704,8 @@ cudaError_t launch_bucketing(const int32_t* ids, int64_t q0, int64_t q1, int H_q
                                               ws.counts, ws.rec_of, dg);
   bucket_scan_kernel<<<1, 1024, 0, st>>>(ws.counts, n_b, qt, ws.offsets, ws.tile_off, ws.cursor);
   if (smem_buckets) {
-    bucket_cta_base_kernel<<<(unsigned)((n_b + 255) / 256), 256, 0, st>>>(ws.offsets, (int)n_b,
-                                                                          kBucketCtas, ws.percta);
+    bucket_cta_base_kernel<<<(unsigned)std::min<int64_t>((n_b * 32 + 255) / 256, 152 * 32),
+                             256, 0, st>>>(ws.offsets, (int)n_b, kBucketCtas, ws.percta);
     bucket_fill_smem_kernel<<<kBucketCtas, 1024, n_b * 4, st>>>(
         ids, q0, q1, H_kv, k, nb, bt.qinfo, ws.rowmask, qt, ws.offsets, ws.tile_off, ws.percta,
         ws.entries, ws.rec_of);
