@@ -121,7 +121,8 @@ int msa_index_select_fp8(const void* q_idx, const void* k_idx, int64_t N, int n_
  *                                             even dimension in the low nibble
  *   q_scales [N, n_groups, d_idx / 16] uint8  E4M3 scale of each 16 dimensions
  *   k_codes  [N, d_idx / 2] uint8, k_scales [N, d_idx / 16] uint8, the same
- * A value is its E2M1 code's value times its 16 dimensions' scale. Such a
+ * A value is its E2M1 code's value times its 16 dimensions' scale (plain FP4,
+ * E2M1 codes without block scaling, is every scale code 0x38 = 1.0). Such a
  * product has at most six significant bits and lies within bf16's range, so
  * the operands are decoded exactly into bf16 rows in the workspace (device,
  * caller-owned, msa_index_select_nvfp4_workspace_bytes() bytes, 16-byte
