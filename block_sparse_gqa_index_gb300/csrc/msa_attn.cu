@@ -1373,10 +1373,12 @@ attn_merge_kernel(const unsigned char* __restrict__ part, const int32_t* __restr
 // Lane l covers the E = G*D/32 elements starting at l*E (head l*E/D). Lane
 // s < k holds slot s's record index and LSEs; per head, max and sum come from
 // shuffles over the slots. Used when G*D <= 1024.
-// five CTAs per SM (48 registers): the merge waits on memory, and a fifth CTA
-// per SM took the 128K main branch from 9.09 to 8.87 ms
+// six CTAs per SM (40 registers, a few spilled): the merge waits on memory, and
+// more warps per SM took the 128K main branch from 9.09 ms (four CTAs, 58
+// registers) to 8.87 (five) and 8.77 (six); eight spill far more and were not
+// tried
 template <int D, int E>
-__global__ void __launch_bounds__(256, 5)
+__global__ void __launch_bounds__(256, 6)
 attn_merge_group_kernel(const unsigned char* __restrict__ part,
                         const int32_t* __restrict__ rec_of, int64_t q0, int64_t q1, int H_q,
                         int H_kv, int k, uint16_t* __restrict__ out, float* __restrict__ lse) {
