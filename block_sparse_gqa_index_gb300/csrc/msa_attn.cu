@@ -1375,8 +1375,8 @@ attn_merge_kernel(const unsigned char* __restrict__ part, const int32_t* __restr
 // shuffles over the slots. Used when G*D <= 1024.
 // six CTAs per SM (40 registers, a few spilled): the merge waits on memory, and
 // more warps per SM took the 128K main branch from 9.09 ms (four CTAs, 58
-// registers) to 8.87 (five) and 8.77 (six); eight spill far more and were not
-// tried
+// registers) to 8.87 (five) and 8.77 (six); at seven or eight CTAs the kernel
+// drops to 32 registers and spills ten times as much, so those were not timed
 template <int D, int E>
 __global__ void __launch_bounds__(256, 6)
 attn_merge_group_kernel(const unsigned char* __restrict__ part,
