@@ -295,3 +295,80 @@ def test_index_fp8_rejects(msa):
     assert f(FAKE, FAKE, 10, 1, 64, 128, 16, FAKE, None, 1.0, None) == -2    # d_idx != 128
     assert f(FAKE, FAKE, 10, 1, 128, 64, 16, FAKE, None, 1.0, None) == -2    # Bk != 128
     assert f(FAKE, FAKE, 0, 1, 128, 128, 16, FAKE, None, 1.0, None) == 0     # empty: no-op
+
+
+def test_kl_teacher_rejects(msa):
+    f = msa._kl
+    # q, k, q_idx, k_idx, block_ids, lse, N, H_q, H_kv, d, d_idx, Bk, topk, scale, kl, ws, bytes
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 10, 32, 8, 128, 128, 128, 16, 0.1, FAKE, FAKE,
+            1 << 40, None]
+    a = list(base); a[0] = None
+    assert f(*a) == -1                             # null q
+    a = list(base); a[5] = FAKE + 4
+    assert f(*a) == -1                             # misaligned lse
+    a = list(base); a[7] = 12
+    assert f(*a) == -1                             # H_q not a multiple of H_kv
+    a = list(base); a[8] = 2
+    assert f(*a) == -2                             # G = 16 > 8
+    a = list(base); a[11] = 64
+    assert f(*a) == -2                             # Bk != 128
+    a = list(base); a[9] = 96
+    assert f(*a) == -2                             # d
+    a = list(base); a[12] = 17
+    assert f(*a) == -2                             # top-k > 16
+    a = list(base); a[6] = 1 << 27
+    assert f(*a) == -2                             # N too large
+    a = list(base); a[16] = 16
+    assert f(*a) == -3                             # workspace holds no chunk of rows
+    a = list(base); a[15] = None
+    assert f(*a) == -1                             # no workspace
+    a = list(base); a[6] = 0
+    assert f(*a) == 0                              # empty: no-op
+    a = list(base); a[6] = -1
+    assert f(*a) == -1                             # N < 0
+
+
+def test_index_project_rejects(msa):
+    f = msa._index_project
+    # x, w_qidx, w_kidx, N, d_model, n_groups, d_idx, q_idx, k_idx, stream
+    base = [FAKE, FAKE, FAKE, 10, 4096, 8, 128, FAKE, FAKE, None]
+    a = list(base); a[1] = None
+    assert f(*a) == -1                             # null w_qidx
+    a = list(base); a[8] = FAKE + 2
+    assert f(*a) == -1                             # misaligned k_idx
+    a = list(base); a[4] = 4100
+    assert f(*a) == -2                             # d_model not a multiple of 8
+    a = list(base); a[6] = 96
+    assert f(*a) == -2                             # d_idx
+    a = list(base); a[3] = 1 << 31
+    assert f(*a) == -2                             # N too large
+    a = list(base); a[3] = -1
+    assert f(*a) == -1                             # N < 0
+    a = list(base); a[3] = 0
+    assert f(*a) == 0                              # empty: no-op
+
+
+def test_decode_index_noalloc_rejects(msa):
+    f = msa._index_dec_noalloc
+    cap = msa._noalloc_max()
+    assert cap == 1 << 20
+    # q_idx, k_idx_pages, page_table, seq_lens, B, max_pages, n_groups, d_idx, Bk, k, ids, stream
+    base = [FAKE, FAKE, FAKE, FAKE, 4, 10, 8, 128, 128, 16, FAKE, None]
+    a = list(base); a[2] = None
+    assert f(*a) == -1                             # null page table
+    a = list(base); a[0] = FAKE + 8
+    assert f(*a) == -1                             # misaligned q_idx
+    a = list(base); a[8] = 64
+    assert f(*a) == -2                             # Bk != 128
+    a = list(base); a[9] = 17
+    assert f(*a) == -2                             # k > 16
+    a = list(base); a[6] = 9
+    assert f(*a) == -2                             # more than 8 groups
+    a = list(base); a[7] = 96
+    assert f(*a) == -2                             # d_idx
+    a = list(base); a[4], a[5] = 128, cap // (128 * 8) + 1
+    assert f(*a) == -3                             # scores beyond the fixed array
+    a = list(base); a[4] = 0
+    assert f(*a) == 0                              # empty: no-op
+    a = list(base); a[4] = -1
+    assert f(*a) == -1                             # B < 0
