@@ -16,6 +16,7 @@ import torch
 import oracle
 import synth
 from tests.msa_check import bf16_to_np, check_close, check_structure, compare_selection
+from tests.nvfp4_inputs import bits_f64, nvfp4_pages, nvfp4_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -699,10 +700,6 @@ def _nvfp4_cache(w, rng, gaussian):
     return packed, sc_codes.astype(np.uint8), bits
 
 
-def bits_f64(b):
-    return (np.ascontiguousarray(b).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-
-
 @pytest.mark.parametrize("gaussian,d_idx,H_kv", [(False, 128, 8), (False, 64, 2), (True, 128, 8)])
 def test_decode_index_nvfp4(msa, gaussian, d_idx, H_kv):
     """NVFP4 k_idx cache: ids against the oracle on the decoded values (bit for
@@ -750,35 +747,6 @@ def test_decode_index_nvfp4(msa, gaussian, d_idx, H_kv):
         assert ((a - b).abs() <= 1e-5 * b.abs().clamp(min=1.0)).all()
 
 
-def _nvfp4_pages(x_bits, rng, shape):
-    """NVFP4 pages of the given shape [P, H, Bk, d]: E2M1 codes two per byte
-    (even dimension low) and one E4M3 scale per 16 dimensions of a row, with the
-    decoded values as bf16 bits (exact). With x_bits (bf16 bits of that shape)
-    the values are quantised (scale = the E4M3 of amax / 6, at least the
-    smallest E4M3 subnormal; codes the nearest E2M1 value); without, codes are
-    drawn uniformly and scales from a few powers of two and 1.5 times one."""
-    e2m1 = np.array([oracle.e2m1_to_f64(c) for c in range(16)])
-    e4m3 = np.array([oracle.e4m3_to_f64(int(c)) for c in range(256)])
-    d = shape[-1]
-    if x_bits is not None:
-        xb = bits_f64(x_bits).reshape(*shape[:-1], d // 16, 16)
-        amax = np.abs(xb).max(axis=-1)
-        sc_codes = torch.from_numpy((np.maximum(amax, 0.012) / 6.0).astype(np.float32)) \
-            .to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-        y = xb / e4m3[sc_codes][..., None]
-        idx = np.abs(np.abs(y)[..., None] - e2m1[:8]).argmin(axis=-1)
-        codes = (idx | np.where(y < 0, 8, 0)).astype(np.uint8).reshape(shape)
-    else:
-        codes = rng.integers(0, 16, size=shape).astype(np.uint8)
-        sc_codes = rng.choice(np.array([0x28, 0x30, 0x38, 0x3C, 0x40], dtype=np.uint8),
-                              size=(*shape[:-1], d // 16))
-    vals = e2m1[codes] * np.repeat(e4m3[sc_codes], 16, axis=-1)
-    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).astype(np.uint8)
-    bits = (vals.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
-    assert np.array_equal(bits_f64(bits), vals)                          # exact in bf16
-    return packed, sc_codes.astype(np.uint8), bits
-
-
 @pytest.mark.parametrize("N,n_g,d_idx,zero_k", [(1000, 2, 64, False), (1537, 8, 128, False),
                                                 (129, 1, 128, False), (5, 2, 64, False),
                                                 (700, 2, 128, True)])
@@ -790,8 +758,8 @@ def test_index_select_nvfp4(msa, N, n_g, d_idx, zero_k):
     visible block scores must match bit for bit. zero_k: every k_idx scale is
     the E4M3 zero, so every score is 0 and the lowest ids win the ties."""
     rng = np.random.default_rng(N * 10 + n_g)
-    qc, qs, qbits = _nvfp4_pages(None, rng, (N, n_g, d_idx))
-    kc, ks, kbits = _nvfp4_pages(None, rng, (N, d_idx))
+    qc, qs, qbits = nvfp4_pages(None, rng, (N, n_g, d_idx))
+    kc, ks, kbits = nvfp4_pages(None, rng, (N, d_idx))
     if zero_k:
         ks[:] = 0
         kbits = np.zeros_like(kbits)
@@ -818,33 +786,14 @@ def test_index_select_nvfp4_gaussian_equals_bf16_path(msa):
     qx = synth.host_tensor(w, synth.T_QIDX)[0]
     kx = synth.host_tensor(w, synth.T_KIDX)[0, :, 0]
     rng = np.random.default_rng(7)
-    qc, qs, qbits = _nvfp4_pages(qx, rng, qx.shape)
-    kc, ks, kbits = _nvfp4_pages(kx, rng, kx.shape)
+    qc, qs, qbits = nvfp4_pages(qx, rng, qx.shape)
+    kc, ks, kbits = nvfp4_pages(kx, rng, kx.shape)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     ids = msa.msa_index_select_nvfp4(dev(qc), dev(qs), dev(kc), dev(ks), 128, 16)
     ref = msa.msa_index_select(dev(qbits).view(torch.bfloat16), dev(kbits).view(torch.bfloat16),
                                128, 16)
     assert torch.equal(ids, ref)
     assert msa.msa_get_error() == 0
-
-
-def _nvfp4_torch(x):
-    """NVFP4 quantisation by torch on the device (no library code): per 16
-    values one E4M3 scale (amax / 6, at least 2^-9) and the nearest E2M1 code
-    of each value over it; returns (codes two per byte, even dimension low;
-    scale codes; the decoded values as bf16, exact)."""
-    e2m1 = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], device=x.device)
-    xb = x.float().reshape(*x.shape[:-1], x.shape[-1] // 16, 16)
-    sc = (xb.abs().amax(dim=-1).clamp(min=2.0 ** -9) / 6.0).to(torch.float8_e4m3fn)
-    scf = sc.float().unsqueeze(-1)
-    y = xb / scf
-    mag = (y.abs().unsqueeze(-1) - e2m1).abs().argmin(dim=-1)
-    codes = (mag | ((y < 0).to(torch.int64) << 3)).to(torch.uint8).reshape(x.shape)
-    dec = (e2m1[mag] * torch.where(y < 0, -1.0, 1.0) * scf).reshape(x.shape)
-    dec16 = dec.to(torch.bfloat16)
-    assert torch.equal(dec16.float(), dec)  # exact in bf16
-    packed = (codes[..., 0::2] | (codes[..., 1::2] << 4)).contiguous()
-    return packed, sc.view(torch.uint8).contiguous(), dec16
 
 
 def test_index_select_nvfp4_full_128k(msa):
@@ -854,9 +803,9 @@ def test_index_select_nvfp4_full_128k(msa):
     w = synth.make("128k")
     qidx = synth.device_tensor(w, synth.T_QIDX)
     kidx = synth.device_tensor(w, synth.T_KIDX)[:, 0].contiguous()
-    qc, qs, qd = _nvfp4_torch(qidx)
+    qc, qs, qd = nvfp4_torch(qidx)
     del qidx
-    kc, ks, kd = _nvfp4_torch(kidx)
+    kc, ks, kd = nvfp4_torch(kidx)
     del kidx
     torch.cuda.empty_cache()
     ids = msa.msa_index_select_nvfp4(qc, qs, kc, ks, 128, 16)
@@ -889,7 +838,7 @@ def test_decode_nvfp4_kv(msa, gaussian, d, H_q, H_kv):
     dev_pages = {}
     host_bits = {}
     for name, t in (("k", synth.T_K), ("v", synth.T_V)):
-        packed, sc, bits = _nvfp4_pages(synth.host_paged(w, t) if gaussian else None, rng, shape)
+        packed, sc, bits = nvfp4_pages(synth.host_paged(w, t) if gaussian else None, rng, shape)
         for key, arr, dt in ((name + "c", packed, torch.uint8), (name + "s", sc, torch.uint8),
                              (name + "b", bits.view(np.int16), torch.int16)):
             x = torch.empty(arr.shape, dtype=dt, device=dev)

@@ -14,7 +14,7 @@ import torch
 
 import bench
 import oracle
-from tests.test_gpu_parity import _nvfp4_pages, _nvfp4_torch
+from tests.nvfp4_inputs import nvfp4_pages, nvfp4_torch
 
 # One row of 48 dimensions = three micro-blocks. Block 0 spans every E2M1
 # magnitude with both signs (amax 6: scale 1.0), block 1 is block 0 times 2
@@ -49,7 +49,7 @@ def test_hand_worked_bytes_decode_to_the_row():
 
 
 def test_numpy_packer_matches_hand_worked_bytes():
-    packed, scales, bits = _nvfp4_pages(_bf16_bits(ROW), None, (1, ROW.size))
+    packed, scales, bits = nvfp4_pages(_bf16_bits(ROW), None, (1, ROW.size))
     assert np.array_equal(packed.reshape(-1), WANT_PACKED)
     assert np.array_equal(scales.reshape(-1), WANT_SCALES)
     assert np.array_equal(bits.reshape(-1), _bf16_bits(ROW))
@@ -57,7 +57,7 @@ def test_numpy_packer_matches_hand_worked_bytes():
 
 def test_torch_packer_matches_hand_worked_bytes():
     x = torch.tensor(ROW, dtype=torch.float32).to(torch.bfloat16).reshape(1, -1)
-    packed, scales, dec = _nvfp4_torch(x)
+    packed, scales, dec = nvfp4_torch(x)
     assert np.array_equal(packed.numpy().reshape(-1), WANT_PACKED)
     assert np.array_equal(scales.numpy().reshape(-1), WANT_SCALES)
     assert torch.equal(dec.float().reshape(-1), torch.tensor(ROW, dtype=torch.float32))
@@ -77,8 +77,8 @@ def test_packers_agree_on_random_rows():
     x = rng.standard_normal((64, 128)).astype(np.float32)
     bits = _bf16_bits(x)
     xb = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
-    p_np, s_np, _ = _nvfp4_pages(bits, None, x.shape)
-    p_t, s_t, _ = _nvfp4_torch(xb)
+    p_np, s_np, _ = nvfp4_pages(bits, None, x.shape)
+    p_t, s_t, _ = nvfp4_torch(xb)
     p_b, s_b = bench.nvfp4_quantise(xb)
     assert np.array_equal(s_np, s_t.numpy()) and np.array_equal(s_np, s_b.numpy())
     # Where no value of a byte's two dimensions sits at an E2M1 midpoint, all
