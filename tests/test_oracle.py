@@ -101,6 +101,33 @@ def test_golden_topk_hand_example():
     assert ids.tolist() == g["expected_ids"]
 
 
+def test_golden_attn_hand_example():
+    """Main-branch attention on hand-worked values: scores that are whole
+    multiples of ln 2 make every softmax weight a power of two, so o and
+    exp(lse) are exact fractions. Pins the causal cut inside the local block
+    (rows 2 and 4), the use of only the selected blocks (row 5 skips the block
+    with the largest scores), the scale, the natural-log LSE and two query heads
+    sharing one group."""
+    from fractions import Fraction
+    g = json.load(open(os.path.join(GOLDEN, "attn_hand_example.json")))
+    sh = g["shape"]
+    tok = g["tokens"]
+    to_bits = lambda a: (np.asarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    K = to_bits(tok["K"]).reshape(sh["N"], sh["H_kv"], sh["d"])
+    V = to_bits(tok["V"]).reshape(sh["N"], sh["H_kv"], sh["d"])
+    q = to_bits(np.broadcast_to(np.asarray(g["q_heads"], dtype=np.float32),
+                                (sh["N"], sh["H_q"], sh["d"])))
+    # K rows follow the stated scores kappa (head 0 scores kappa, head 1 1 - kappa)
+    Kf = np.asarray(tok["K"], dtype=np.float64)
+    assert np.array_equal(Kf @ np.asarray(g["q_heads"][0]), tok["kappa"])
+    ids = np.asarray(g["ids"], dtype=np.int32)
+    o, lse = oracle.sparse_attn(q, np.arange(sh["N"]), K, V, ids, sh["Bk"], math.log(2.0))
+    want_o = np.vectorize(lambda x: float(Fraction(x)))(np.asarray(g["expected_o"]))
+    want_lse = np.vectorize(lambda x: math.log(Fraction(x)))(np.asarray(g["expected_exp_lse"]))
+    assert np.allclose(o, want_o, rtol=1e-12, atol=1e-12), (o, want_o)
+    assert np.allclose(lse, want_lse, rtol=0, atol=1e-12), (lse, want_lse)
+
+
 @pytest.mark.parametrize("Bk,N,q_offset,n_g,k", [
     (8, 40, 0, 2, 3), (8, 57, 96, 3, 4), (16, 64, 300, 2, 16), (4, 33, 21, 4, 5),
     (128, 200, 2000, 2, 16), (2, 30, 7, 1, 2)])
